@@ -1,0 +1,709 @@
+/*
+ * nsa_oracle.c -- plain CPU oracle for the native-sparse-attention hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline / reference arm may load this library.  It shares
+ * no code, header, table or helper with the CUDA library; neither includes the
+ * other.  It is deliberately slow: plain loops, fp64 accumulation, one row at a
+ * time, OpenMP only across independent rows.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [NOSA-Triton]  "NOSA-1B source walk-through #3: how the Triton kernel speeds up
+ *                   attention" (kwkr.cn/news/198629)
+ *   [NOSA-Parts]   "NOSA-1B core components: how KV-cache offload gives 5.04x decode
+ *                   throughput" (kwkr.cn/news/199670)
+ *   [NSA-Triton]   "DeepSeek NSA sparse attention in practice: optimising training
+ *                   with Triton" (mcp.csdn.net)
+ *   [TileLang-NSA] "TileLang operator development: Native Sparse Attention
+ *                   implementation and optimisation" (devpress.csdn.net)
+ *
+ * Notation (per sequence of length L, positions t = 0..L-1 relative to its start):
+ *   H query heads, Hkv kv-heads, group size r = H/Hkv, head h reads kv-head h / r
+ *   ([TileLang-NSA] sec. 2, "head_kv = heads // groups").
+ *   compression kernel l and stride s ([NOSA-Parts] core component 1: 32 and 16);
+ *   n_c(L) = floor((L-l)/s)+1 compressed keys when L >= l, else 0 (full windows only).
+ *   selection block size B ([NOSA-Parts] core component 1; [TileLang-NSA] sec. 2: 64).
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *   - compressed key c is causal for query t iff its window ends at or before t:
+ *     c*s + l - 1 <= t.  Rows with no causal compressed key get probability 0.
+ *   - the pooled block score of block j is the mean of the group probabilities of
+ *     the compressed windows lying inside block j, {c : c*s >= jB, c*s+l <= (j+1)B},
+ *     counting only windows that exist (c < n_c(L)); causally masked windows count
+ *     as zeros; an empty set gives 0.
+ *   - top-k keeps the forced blocks (n_init initial, n_local local ending at the
+ *     query's own block), excludes blocks starting after t, breaks ties toward the
+ *     lower block index, pads with -1 and returns ascending order.
+ *
+ * dtype codes: 0 = fp32, 1 = bf16 (raw 16-bit patterns).  Element values are
+ * widened exactly to double.  All arrays are dense row-major.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+
+static double ld(const void* p, int dtype, size_t i) {
+  if (dtype == OR_BF16) {
+    uint32_t u = ((uint32_t)((const uint16_t*)p)[i]) << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+  }
+  return (double)((const float*)p)[i];
+}
+
+/* Correctly rounded (nearest, ties to even) conversion of a double to bf16 bits,
+ * done in one step so that no intermediate float rounding intervenes. */
+static uint16_t to_bf16_bits(double x) {
+  if (isnan(x)) return 0x7fc0;
+  if (x == 0.0) return signbit(x) ? 0x8000 : 0x0000;
+  int e;
+  frexp(x, &e);             /* |x| = m * 2^e with 0.5 <= m < 1 */
+  int q = e - 8;            /* bf16 carries 8 significant bits */
+  if (q < -133) q = -133;   /* smallest bf16 subnormal is 2^-133 */
+  double y = ldexp(nearbyint(ldexp(x, -q)), q);
+  if (fabs(y) >= 0x1p128) return signbit(x) ? 0xff80 : 0x7f80;
+  float f = (float)y;       /* exact: y has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+static void st_rounded(void* p, int dtype, size_t i, double x) {
+  if (dtype == OR_BF16)
+    ((uint16_t*)p)[i] = to_bf16_bits(x);
+  else
+    ((float*)p)[i] = (float)x; /* C conversion rounds to nearest even */
+}
+
+int nsa_oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Number of full compression windows in a sequence of length L. */
+int nsa_oracle_num_cmp(int L, int kernel, int stride) {
+  if (kernel <= 0 || stride <= 0 || L < kernel) return 0;
+  return (L - kernel) / stride + 1;
+}
+
+/* Number of compressed keys that are causal for position t: c*s + l - 1 <= t. */
+static int num_causal_cmp(int t, int n_c, int kernel, int stride) {
+  if (t < kernel - 1) return 0;
+  int n = (t - (kernel - 1)) / stride + 1;
+  return n < n_c ? n : n_c;
+}
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Map a packed token index to its sequence by scanning cu_seqlens. */
+static int seq_of(const int32_t* cu, int n_seqs, int64_t tok) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) / 2;
+    if (cu[mid] <= tok) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+/* First compressed row of every sequence when compressed keys are packed
+ * sequence after sequence (n_seqs+1 entries). */
+static int64_t* cmp_offsets(const int32_t* cu, int n_seqs, int kernel, int stride) {
+  int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_seqs + 1));
+  off[0] = 0;
+  for (int i = 0; i < n_seqs; ++i)
+    off[i + 1] = off[i] + nsa_oracle_num_cmp(cu[i + 1] - cu[i], kernel, stride);
+  return off;
+}
+
+/* ------------------------------------------------------------------------ */
+/* S1: key compression.  [NOSA-Parts] core component 1 ("Key compressor"): cut the
+ * keys into windows of `kernel` tokens at step `stride` and mean-pool each window;
+ * [NOSA-Triton] "beyond the kernel" (kernel 32, stride 16, 50% overlap).  Windows
+ * stay inside their sequence.  out_exact gets the fp64 mean, out_rounded the mean
+ * rounded to the input dtype (the stored compressed key). */
+int nsa_oracle_compress(const void* k, int dtype, const int32_t* cu, int n_seqs, int hkv, int d,
+                        int kernel, int stride, double* out_exact, void* out_rounded) {
+  if (kernel <= 0 || stride <= 0) return 1;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  for (int sq = 0; sq < n_seqs; ++sq) {
+    int L = cu[sq + 1] - cu[sq];
+    int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < n_c; ++c) {
+      for (int g = 0; g < hkv; ++g) {
+        for (int i = 0; i < d; ++i) {
+          double acc = 0.0;
+          for (int w = 0; w < kernel; ++w) {
+            size_t tok = (size_t)cu[sq] + (size_t)c * stride + w;
+            acc += ld(k, dtype, (tok * hkv + g) * d + i);
+          }
+          double mean = acc / kernel;
+          size_t o = ((size_t)(off[sq] + c) * hkv + g) * d + i;
+          if (out_exact) out_exact[o] = mean;
+          if (out_rounded) st_rounded(out_rounded, dtype, o, mean);
+        }
+      }
+    }
+  }
+  free(off);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* S2 for one query row and one kv-group: per head h of group g, the scores
+ * z[h,c] = scale * q[t,h] . kc[c,g] over the causal compressed keys, a softmax
+ * over them, and the group sum P_g[c] = sum_h p[h,c]  ([NSA-Triton] sec. 1.1:
+ * selection reuses the compressed-attention scores; [NOSA-Parts] core component 3,
+ * stage 1: a light attention of q against the compressed keys gives block scores).
+ * pg receives n_c entries (zeros past the causal ones).  If o_cmp is non-NULL the
+ * same probabilities also give the compressed-attention output of each head of
+ * the group, o_cmp[(h - g*r)*d + i] = sum_c p[h,c] vc[c,g,i], and lse[h - g*r]. */
+static void row_group_probs(const void* q, const void* kc, const void* vc, int dtype, int64_t tok,
+                            int64_t kc_base, int n_c, int t, int h, int hkv, int d, int g,
+                            int kernel, int stride, double scale, double* pg, double* z,
+                            double* o_cmp, double* lse) {
+  int r = h / hkv;
+  int nca = num_causal_cmp(t, n_c, kernel, stride);
+  for (int c = 0; c < n_c; ++c) pg[c] = 0.0;
+  for (int hh = g * r; hh < (g + 1) * r; ++hh) {
+    double* oc = o_cmp ? o_cmp + (size_t)(hh - g * r) * d : NULL;
+    if (oc) for (int i = 0; i < d; ++i) oc[i] = 0.0;
+    if (nca == 0) {
+      if (lse) lse[hh - g * r] = -INFINITY;
+      continue;
+    }
+    double mx = -INFINITY;
+    for (int c = 0; c < nca; ++c) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i)
+        acc += ld(q, dtype, ((size_t)tok * h + hh) * d + i) *
+               ld(kc, dtype, ((size_t)(kc_base + c) * hkv + g) * d + i);
+      z[c] = acc * scale;
+      if (z[c] > mx) mx = z[c];
+    }
+    double sum = 0.0;
+    for (int c = 0; c < nca; ++c) sum += exp(z[c] - mx);
+    for (int c = 0; c < nca; ++c) {
+      double p = exp(z[c] - mx) / sum;
+      pg[c] += p;
+      if (oc)
+        for (int i = 0; i < d; ++i) oc[i] += p * ld(vc, dtype, ((size_t)(kc_base + c) * hkv + g) * d + i);
+    }
+    if (lse) lse[hh - g * r] = mx + log(sum);
+  }
+}
+
+/* S3 for one row: pooled block scores.  [NOSA-Triton] mechanisms 2 and 3: the
+ * pooling kernel sums the scores of a window and divides by the number of valid
+ * entries, the validity mask coming from the sequence length.  Block j pools the
+ * compressed windows that lie inside it: {c : c*s >= jB and c*s + l <= (j+1)B},
+ * restricted to existing windows c < n_c; empty -> 0. */
+int nsa_oracle_pool_row(const double* pg, int n_c, int n_b, int block_size, int kernel, int stride,
+                        double* out) {
+  if (block_size <= 0 || kernel <= 0 || stride <= 0) return 1;
+  for (int j = 0; j < n_b; ++j) {
+    long first_tok = (long)j * block_size;           /* window must start here or later */
+    long last_start = (long)(j + 1) * block_size - kernel; /* ... and start no later than this */
+    double acc = 0.0;
+    int cnt = 0;
+    if (last_start >= first_tok) {
+      long c_lo = (first_tok + stride - 1) / stride;
+      long c_hi = last_start / stride;
+      for (long c = c_lo; c <= c_hi; ++c) {
+        if (c >= n_c) break;
+        acc += pg[c];
+        ++cnt;
+      }
+    }
+    out[j] = cnt ? acc / cnt : 0.0;
+  }
+  return 0;
+}
+
+/* P_g for a set of rows: pg[row, g, c] (c < nc_stride; zero past n_c). */
+int nsa_oracle_cmp_probs(const void* q, const void* kc, int dtype, const int32_t* cu, int n_seqs,
+                         int h, int hkv, int d, int kernel, int stride, double scale,
+                         const int64_t* rows, int64_t n_rows, double* pg, int nc_stride) {
+  if (h % hkv) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  int err = 0;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)(nc_stride + 1));
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(nc_stride + 1));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int L = cu[sq + 1] - cu[sq];
+      int t = (int)(tok - cu[sq]);
+      int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+      if (n_c > nc_stride) { err = 1; continue; }
+      for (int g = 0; g < hkv; ++g) {
+        row_group_probs(q, kc, NULL, dtype, tok, off[sq], n_c, t, h, hkv, d, g, kernel, stride,
+                        scale, buf, z, NULL, NULL);
+        double* dst = pg + ((size_t)rr * hkv + g) * nc_stride;
+        for (int c = 0; c < nc_stride; ++c) dst[c] = c < n_c ? buf[c] : 0.0;
+      }
+    }
+    free(z);
+    free(buf);
+  }
+  free(off);
+  return err;
+}
+
+/* S2+S3: pooled block scores scores[row, g, j] for j < nb_stride (zero past n_b(L)). */
+int nsa_oracle_cmp_scores_pool(const void* q, const void* kc, int dtype, const int32_t* cu, int n_seqs,
+                               int h, int hkv, int d, int kernel, int stride, int block_size,
+                               double scale, const int64_t* rows, int64_t n_rows, double* scores,
+                               int nb_stride) {
+  if (h % hkv) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  int maxL = 0;
+  for (int i = 0; i < n_seqs; ++i) if (cu[i + 1] - cu[i] > maxL) maxL = cu[i + 1] - cu[i];
+  int nc_max = nsa_oracle_num_cmp(maxL, kernel, stride) + 1;
+  int err = 0;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* pg = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* sb = (double*)malloc(sizeof(double) * (size_t)(nb_stride + 1));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int L = cu[sq + 1] - cu[sq];
+      int t = (int)(tok - cu[sq]);
+      int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+      int n_b = (L + block_size - 1) / block_size;
+      if (n_b > nb_stride) { err = 1; continue; }
+      for (int g = 0; g < hkv; ++g) {
+        row_group_probs(q, kc, NULL, dtype, tok, off[sq], n_c, t, h, hkv, d, g, kernel, stride,
+                        scale, pg, z, NULL, NULL);
+        nsa_oracle_pool_row(pg, n_c, n_b, block_size, kernel, stride, sb);
+        double* dst = scores + ((size_t)rr * hkv + g) * nb_stride;
+        for (int j = 0; j < nb_stride; ++j) dst[j] = j < n_b ? sb[j] : 0.0;
+      }
+    }
+    free(z);
+    free(pg);
+    free(sb);
+  }
+  free(off);
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* S4 for one row.  [NOSA-Triton] "beyond the kernel: how the sliding window and
+ * top-k cooperate": keep init_blocks + local_blocks + selected candidates, fill the
+ * rest with -inf, take the top-k, and hand the indices on in sorted order.  Forced
+ * blocks score +inf; only blocks j with j*B <= t are candidates; order is by score,
+ * descending, then by lower block index.  k counts the forced blocks. */
+typedef struct { double key; int j; } cand_t;
+
+static int cand_cmp(const void* a, const void* b) {
+  const cand_t* x = (const cand_t*)a;
+  const cand_t* y = (const cand_t*)b;
+  if (x->key > y->key) return -1;
+  if (x->key < y->key) return 1;
+  return (x->j > y->j) - (x->j < y->j);
+}
+
+static int int_cmp(const void* a, const void* b) {
+  int x = *(const int*)a, y = *(const int*)b;
+  return (x > y) - (x < y);
+}
+
+static void row_topk(const double* sc, int t, int block_size, int n_init, int n_local, int k,
+                     int32_t* out, cand_t* cand, int* pick) {
+  int own = t / block_size;
+  int ncand = own + 1;
+  for (int j = 0; j < ncand; ++j) {
+    int forced = (j < n_init) || (j > own - n_local);
+    cand[j].key = forced ? INFINITY : sc[j];
+    cand[j].j = j;
+  }
+  qsort(cand, (size_t)ncand, sizeof(cand_t), cand_cmp);
+  int take = k < ncand ? k : ncand;
+  for (int i = 0; i < take; ++i) pick[i] = cand[i].j;
+  qsort(pick, (size_t)take, sizeof(int), int_cmp);
+  for (int i = 0; i < k; ++i) out[i] = i < take ? pick[i] : -1;
+}
+
+int nsa_oracle_topk(const double* scores, int nb_stride, const int32_t* cu, int n_seqs, int hkv,
+                    int block_size, int n_init, int n_local, int k, const int64_t* rows,
+                    int64_t n_rows, int32_t* idx) {
+  if (k <= 0 || block_size <= 0) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int err = 0;
+#pragma omp parallel
+  {
+    cand_t* cand = (cand_t*)malloc(sizeof(cand_t) * (size_t)(nb_stride + 1));
+    int* pick = (int*)malloc(sizeof(int) * (size_t)(nb_stride + k + 1));
+#pragma omp for schedule(dynamic, 64)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      if (t / block_size + 1 > nb_stride) { err = 1; continue; }
+      for (int g = 0; g < hkv; ++g)
+        row_topk(scores + ((size_t)rr * hkv + g) * nb_stride, t, block_size, n_init, n_local, k,
+                 idx + ((size_t)rr * hkv + g) * k, cand, pick);
+    }
+    free(cand);
+    free(pick);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Softmax attention of one query head over an explicit key list (two passes:
+ * maximum, then normalised sum).  Empty list -> zero output, lse = -inf. */
+static void attend_list(const void* q, const void* k, const void* v, int dtype, int64_t tok, int hh,
+                        int h, int hkv, int d, int g, int64_t seq_start, const int* keys, int n,
+                        double scale, double* s, double* o, double* lse) {
+  for (int i = 0; i < d; ++i) o[i] = 0.0;
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double mx = -INFINITY;
+  for (int e = 0; e < n; ++e) {
+    double acc = 0.0;
+    size_t kr = ((size_t)(seq_start + keys[e]) * hkv + g) * d;
+    for (int i = 0; i < d; ++i) acc += ld(q, dtype, ((size_t)tok * h + hh) * d + i) * ld(k, dtype, kr + i);
+    s[e] = acc * scale;
+    if (s[e] > mx) mx = s[e];
+  }
+  double sum = 0.0;
+  for (int e = 0; e < n; ++e) sum += exp(s[e] - mx);
+  for (int e = 0; e < n; ++e) {
+    double p = exp(s[e] - mx) / sum;
+    size_t vr = ((size_t)(seq_start + keys[e]) * hkv + g) * d;
+    for (int i = 0; i < d; ++i) o[i] += p * ld(v, dtype, vr + i);
+  }
+  *lse = mx + log(sum);
+}
+
+/* Key list of the selected blocks for query t.  [TileLang-NSA] sec. 2: block start
+ * i_s = index * block_size, used only when 0 <= i_s <= t; inside a used block keys
+ * past t are masked.  Every list entry is walked, so a repeated index counts twice. */
+static int selected_keys(const int32_t* idx_row, int S, int block_size, int t, int* keys) {
+  int n = 0;
+  for (int e = 0; e < S; ++e) {
+    long i = idx_row[e];
+    if (i < 0 || i * (long)block_size > t) continue;
+    for (long tau = i * block_size; tau < (i + 1) * (long)block_size && tau <= t; ++tau) keys[n++] = (int)tau;
+  }
+  return n;
+}
+
+/* S5: selected-block attention.  o[row, h, :], lse[row, h] (lse nullable). */
+int nsa_oracle_sparse_attn(const void* q, const void* k, const void* v, int dtype, const int32_t* cu,
+                           int n_seqs, int h, int hkv, int d, const int32_t* idx, int S,
+                           int block_size, double scale, const int64_t* rows, int64_t n_rows,
+                           double* o, double* lse) {
+  if (h % hkv || block_size <= 0) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int r = h / hkv;
+#pragma omp parallel
+  {
+    int* keys = (int*)malloc(sizeof(int) * (size_t)(S * block_size + 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(S * block_size + 1));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      for (int hh = 0; hh < h; ++hh) {
+        int g = hh / r;
+        int n = selected_keys(idx + ((size_t)tok * hkv + g) * S, S, block_size, t, keys);
+        double l;
+        attend_list(q, k, v, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, s,
+                    o + ((size_t)rr * h + hh) * d, &l);
+        if (lse) lse[(size_t)rr * h + hh] = l;
+      }
+    }
+    free(keys);
+    free(s);
+  }
+  return 0;
+}
+
+/* S8: sliding-window attention over keys max(0, t-window+1) .. t ([NSA-Triton]
+ * sec. 1.1: the sliding branch looks at the most recent tokens). */
+int nsa_oracle_swa(const void* q, const void* k, const void* v, int dtype, const int32_t* cu,
+                   int n_seqs, int h, int hkv, int d, int window, double scale,
+                   const int64_t* rows, int64_t n_rows, double* o, double* lse) {
+  if (h % hkv || window <= 0) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int r = h / hkv;
+#pragma omp parallel
+  {
+    int* keys = (int*)malloc(sizeof(int) * (size_t)(window + 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(window + 1));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      int lo = t - window + 1 > 0 ? t - window + 1 : 0;
+      int n = 0;
+      for (int tau = lo; tau <= t; ++tau) keys[n++] = tau;
+      for (int hh = 0; hh < h; ++hh) {
+        double l;
+        attend_list(q, k, v, dtype, tok, hh, h, hkv, d, hh / r, cu[sq], keys, n, scale, s,
+                    o + ((size_t)rr * h + hh) * d, &l);
+        if (lse) lse[(size_t)rr * h + hh] = l;
+      }
+    }
+    free(keys);
+    free(s);
+  }
+  return 0;
+}
+
+/* S7: compressed-attention branch over stored compressed keys/values
+ * ([NSA-Triton] sec. 1.1 and 2.2 taken as a definition): per head, softmax of
+ * scale * q . kc[c] over the causal compressed keys, weighted sum of vc[c]. */
+int nsa_oracle_cmp_attn(const void* q, const void* kc, const void* vc, int dtype, const int32_t* cu,
+                        int n_seqs, int h, int hkv, int d, int kernel, int stride, double scale,
+                        const int64_t* rows, int64_t n_rows, double* o, double* lse) {
+  if (h % hkv) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int r = h / hkv;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  int maxL = 0;
+  for (int i = 0; i < n_seqs; ++i) if (cu[i + 1] - cu[i] > maxL) maxL = cu[i + 1] - cu[i];
+  int nc_max = nsa_oracle_num_cmp(maxL, kernel, stride) + 1;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* pg = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* oc = (double*)malloc(sizeof(double) * (size_t)r * d);
+    double* lg = (double*)malloc(sizeof(double) * (size_t)r);
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int L = cu[sq + 1] - cu[sq];
+      int t = (int)(tok - cu[sq]);
+      int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+      for (int g = 0; g < hkv; ++g) {
+        row_group_probs(q, kc, vc, dtype, tok, off[sq], n_c, t, h, hkv, d, g, kernel, stride, scale,
+                        pg, z, oc, lg);
+        for (int j = 0; j < r; ++j) {
+          memcpy(o + ((size_t)rr * h + g * r + j) * d, oc + (size_t)j * d, sizeof(double) * (size_t)d);
+          if (lse) lse[(size_t)rr * h + g * r + j] = lg[j];
+        }
+      }
+    }
+    free(z);
+    free(pg);
+    free(oc);
+    free(lg);
+  }
+  free(off);
+  return 0;
+}
+
+/* S9: gate combine ([NSA-Triton] sec. 1.1: gates[0]*compressed + gates[1]*selected
+ * + gates[2]*local), each gate the logistic sigmoid of its logit;
+ * gates is [tokens, h, 3] fp32. */
+int nsa_oracle_gate_combine(const double* o_cmp, const double* o_slc, const double* o_swa,
+                            const float* gates, int64_t n_rows, int h, int d, double* o) {
+#pragma omp parallel for schedule(static)
+  for (int64_t rr = 0; rr < n_rows; ++rr)
+    for (int hh = 0; hh < h; ++hh) {
+      size_t gi = ((size_t)rr * h + hh) * 3;
+      double g0 = sigmoid(gates[gi]), g1 = sigmoid(gates[gi + 1]), g2 = sigmoid(gates[gi + 2]);
+      for (int i = 0; i < d; ++i) {
+        size_t x = ((size_t)rr * h + hh) * d + i;
+        o[x] = g0 * o_cmp[x] + g1 * o_slc[x] + g2 * o_swa[x];
+      }
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* S6: one decode step.  [NOSA-Parts] "how decoding uses only 64 KV blocks": the
+ * newest query (position L-1; the cache already holds its key and value) is scored
+ * against the compressed keys, the pooled block scores choose k blocks, and
+ * attention runs over the chosen blocks only.
+ *   q [B, h, d]; k_cache, v_cache [B, max_len, hkv, d]; kc_cache [B, nc_stride, hkv, d]
+ *   with the first n_c(L_b) rows valid.  idx [B, hkv, k] out.  idx_in (nullable)
+ *   overrides the selection used for attention.  o [B, h, d].  scores (nullable)
+ *   [B, hkv, nb_stride] receives the pooled block scores. */
+int nsa_oracle_decode(const void* q, const void* k_cache, const void* v_cache, const void* kc_cache,
+                      int dtype, int B, const int32_t* seqlens, int max_len, int h, int hkv, int d,
+                      int kernel, int stride, int block_size, int n_init, int n_local, int k,
+                      double scale, const int32_t* idx_in, int32_t* idx, double* o, double* scores,
+                      int nb_stride) {
+  if (h % hkv) return 1;
+  int r = h / hkv;
+  int nc_stride = nsa_oracle_num_cmp(max_len, kernel, stride);
+  int nb_max = (max_len + block_size - 1) / block_size;
+  if (scores && nb_stride < nb_max) return 1;
+  int err = 0;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)(nc_stride + 1));
+    double* pg = (double*)malloc(sizeof(double) * (size_t)(nc_stride + 1));
+    double* sb = (double*)malloc(sizeof(double) * (size_t)(nb_max + 1));
+    cand_t* cand = (cand_t*)malloc(sizeof(cand_t) * (size_t)(nb_max + 1));
+    int* pick = (int*)malloc(sizeof(int) * (size_t)(nb_max + k + 1));
+    int* keys = (int*)malloc(sizeof(int) * (size_t)(k * block_size + 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(k * block_size + 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+      int L = seqlens[b];
+      if (L < 1 || L > max_len) { err = 1; continue; }
+      int t = L - 1;
+      int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+      int n_b = (L + block_size - 1) / block_size;
+      for (int g = 0; g < hkv; ++g) {
+        /* the q row of sequence b is token b of a [B, h, d] array; the caches are
+         * sequences of stride max_len (compressed: nc_stride) */
+        for (int c = 0; c < n_c; ++c) pg[c] = 0.0;
+        int nca = num_causal_cmp(t, n_c, kernel, stride);
+        for (int hh = g * r; hh < (g + 1) * r && nca > 0; ++hh) {
+          double mx = -INFINITY;
+          for (int c = 0; c < nca; ++c) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i)
+              acc += ld(q, dtype, ((size_t)b * h + hh) * d + i) *
+                     ld(kc_cache, dtype, (((size_t)b * nc_stride + c) * hkv + g) * d + i);
+            z[c] = acc * scale;
+            if (z[c] > mx) mx = z[c];
+          }
+          double sum = 0.0;
+          for (int c = 0; c < nca; ++c) sum += exp(z[c] - mx);
+          for (int c = 0; c < nca; ++c) pg[c] += exp(z[c] - mx) / sum;
+        }
+        nsa_oracle_pool_row(pg, n_c, n_b, block_size, kernel, stride, sb);
+        if (scores)
+          for (int j = 0; j < nb_stride; ++j) scores[((size_t)b * hkv + g) * nb_stride + j] = j < n_b ? sb[j] : 0.0;
+        int32_t* ir = idx + ((size_t)b * hkv + g) * k;
+        row_topk(sb, t, block_size, n_init, n_local, k, ir, cand, pick);
+        const int32_t* use = idx_in ? idx_in + ((size_t)b * hkv + g) * k : ir;
+        int n = selected_keys(use, k, block_size, t, keys);
+        for (int hh = g * r; hh < (g + 1) * r; ++hh) {
+          double l;
+          /* k/v caches: token tau of sequence b is row b*max_len + tau */
+          attend_list(q, k_cache, v_cache, dtype, b, hh, h, hkv, d, g, (int64_t)b * max_len, keys, n,
+                      scale, s, o + ((size_t)b * h + hh) * d, &l);
+        }
+      }
+    }
+    free(z); free(pg); free(sb); free(cand); free(pick); free(keys); free(s);
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Full three-branch layer ([NSA-Triton] sec. 1.1): compressed attention over the
+ * mean-pooled keys and values, selected-block attention over the blocks chosen
+ * from the same compressed probabilities, sliding-window attention, and the gated
+ * sum.  Compressed keys/values are rounded to the input dtype as stored values.
+ * idx_in (nullable, [tokens, hkv, S]) overrides the selection for the selected
+ * branch.  Outputs are per requested row: idx [n_rows, hkv, S], o and the three
+ * branch outputs [n_rows, h, d] (branch outputs nullable). */
+int nsa_oracle_layer(const void* q, const void* k, const void* v, const float* gates, int dtype,
+                     const int32_t* cu, int n_seqs, int h, int hkv, int d, int kernel, int stride,
+                     int block_size, int S, int n_init, int n_local, int window, double scale,
+                     const int32_t* idx_in, const int64_t* rows, int64_t n_rows, int32_t* idx,
+                     double* o, double* o_cmp_out, double* o_slc_out, double* o_swa_out) {
+  if (h % hkv) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int r = h / hkv;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  size_t ncr = (size_t)off[n_seqs];
+  size_t esz = dtype == OR_BF16 ? 2 : 4;
+  void* kc = malloc(esz * (ncr * hkv * d + 1));
+  void* vc = malloc(esz * (ncr * hkv * d + 1));
+  nsa_oracle_compress(k, dtype, cu, n_seqs, hkv, d, kernel, stride, NULL, kc);
+  nsa_oracle_compress(v, dtype, cu, n_seqs, hkv, d, kernel, stride, NULL, vc);
+  int maxL = 0;
+  for (int i = 0; i < n_seqs; ++i) if (cu[i + 1] - cu[i] > maxL) maxL = cu[i + 1] - cu[i];
+  int nc_max = nsa_oracle_num_cmp(maxL, kernel, stride) + 1;
+  int nb_max = (maxL + block_size - 1) / block_size + 1;
+  int nkeys = (S * block_size > window ? S * block_size : window) + 1;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* pg = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* sb = (double*)malloc(sizeof(double) * (size_t)nb_max);
+    double* oc = (double*)malloc(sizeof(double) * (size_t)r * d);
+    double* lg = (double*)malloc(sizeof(double) * (size_t)r);
+    double* os = (double*)malloc(sizeof(double) * (size_t)d);
+    double* ow = (double*)malloc(sizeof(double) * (size_t)d);
+    cand_t* cand = (cand_t*)malloc(sizeof(cand_t) * (size_t)nb_max);
+    int* pick = (int*)malloc(sizeof(int) * (size_t)(nb_max + S + 1));
+    int* keys = (int*)malloc(sizeof(int) * (size_t)nkeys);
+    int* wkeys = (int*)malloc(sizeof(int) * (size_t)nkeys);
+    double* s = (double*)malloc(sizeof(double) * (size_t)nkeys);
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int L = cu[sq + 1] - cu[sq];
+      int t = (int)(tok - cu[sq]);
+      int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+      int n_b = (L + block_size - 1) / block_size;
+      int lo = t - window + 1 > 0 ? t - window + 1 : 0;
+      int nw = 0;
+      for (int tau = lo; tau <= t; ++tau) wkeys[nw++] = tau;
+      for (int g = 0; g < hkv; ++g) {
+        row_group_probs(q, kc, vc, dtype, tok, off[sq], n_c, t, h, hkv, d, g, kernel, stride, scale,
+                        pg, z, oc, lg);
+        nsa_oracle_pool_row(pg, n_c, n_b, block_size, kernel, stride, sb);
+        int32_t* ir = idx + ((size_t)rr * hkv + g) * S;
+        row_topk(sb, t, block_size, n_init, n_local, S, ir, cand, pick);
+        const int32_t* use = idx_in ? idx_in + ((size_t)tok * hkv + g) * S : ir;
+        int n = selected_keys(use, S, block_size, t, keys);
+        for (int j = 0; j < r; ++j) {
+          int hh = g * r + j;
+          double l;
+          attend_list(q, k, v, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, s, os, &l);
+          attend_list(q, k, v, dtype, tok, hh, h, hkv, d, g, cu[sq], wkeys, nw, scale, s, ow, &l);
+          size_t gi = ((size_t)tok * h + hh) * 3;
+          double g0 = sigmoid(gates[gi]), g1 = sigmoid(gates[gi + 1]), g2 = sigmoid(gates[gi + 2]);
+          size_t base = ((size_t)rr * h + hh) * d;
+          for (int i = 0; i < d; ++i) {
+            double xc = oc[(size_t)j * d + i];
+            o[base + i] = g0 * xc + g1 * os[i] + g2 * ow[i];
+            if (o_cmp_out) o_cmp_out[base + i] = xc;
+            if (o_slc_out) o_slc_out[base + i] = os[i];
+            if (o_swa_out) o_swa_out[base + i] = ow[i];
+          }
+        }
+      }
+    }
+    free(z); free(pg); free(sb); free(oc); free(lg); free(os); free(ow);
+    free(cand); free(pick); free(keys); free(wkeys); free(s);
+  }
+  free(kc);
+  free(vc);
+  free(off);
+  return 0;
+}

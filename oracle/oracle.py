@@ -1,0 +1,259 @@
+"""ctypes binding of the plain CPU oracle (``nsa_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline / reference arm are the only users.  The CUDA library
+never loads it and it never loads the CUDA library.
+
+Arrays are numpy: bf16 tensors travel as ``uint16`` bit patterns, fp32 as
+``float32``; every floating-point result comes back as ``float64``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nsa_oracle.c")
+_SO = os.path.join(_HERE, "libnsa_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fp contraction)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fopenmp",
+                               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = ctypes.CDLL(_SO)
+        _lib.nsa_oracle_num_cmp.restype = ctypes.c_int
+        _lib.nsa_oracle_threads.restype = ctypes.c_int
+    return _lib
+
+
+def _p(a):
+    return ctypes.c_void_p(0 if a is None else a.ctypes.data)
+
+
+def _dt(a) -> int:
+    if a.dtype == np.uint16:
+        return 1
+    if a.dtype == np.float32:
+        return 0
+    raise TypeError(f"oracle inputs must be bf16 bits (uint16) or float32, got {a.dtype}")
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _rows(rows, total):
+    if rows is None:
+        return None, total
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return r, len(r)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (rc={rc})")
+
+
+def threads() -> int:
+    return _load().nsa_oracle_threads()
+
+
+def num_cmp(L: int, kernel: int = 32, stride: int = 16) -> int:
+    return _load().nsa_oracle_num_cmp(int(L), int(kernel), int(stride))
+
+
+def cmp_offsets(cu, kernel=32, stride=16):
+    cu = np.asarray(cu)
+    n = [num_cmp(int(cu[i + 1] - cu[i]), kernel, stride) for i in range(len(cu) - 1)]
+    return np.concatenate([[0], np.cumsum(n)]).astype(np.int64)
+
+
+def compress(k, cu, kernel=32, stride=16):
+    """S1: returns (exact fp64 means, means rounded to k's dtype), both [n_cmp, hkv, d]."""
+    k = np.ascontiguousarray(k)
+    cu = _i32(cu)
+    _, hkv, d = k.shape
+    n = int(cmp_offsets(cu, kernel, stride)[-1])
+    exact = np.zeros((n, hkv, d), np.float64)
+    rounded = np.zeros((n, hkv, d), k.dtype)
+    _check(_load().nsa_oracle_compress(_p(k), _dt(k), _p(cu), len(cu) - 1, hkv, d, kernel, stride,
+                                       _p(exact), _p(rounded)), "compress")
+    return exact, rounded
+
+
+def cmp_probs(q, kc, cu, kernel=32, stride=16, scale=None, rows=None, nc_stride=None):
+    """S2: group-summed probabilities P_g [rows, hkv, nc_stride]."""
+    q, kc, cu = np.ascontiguousarray(q), np.ascontiguousarray(kc), _i32(cu)
+    tot, h, d = q.shape
+    hkv = kc.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    if nc_stride is None:
+        nc_stride = max(1, max(num_cmp(int(cu[i + 1] - cu[i]), kernel, stride) for i in range(len(cu) - 1)))
+    rows, n = _rows(rows, tot)
+    out = np.zeros((n, hkv, nc_stride), np.float64)
+    _check(_load().nsa_oracle_cmp_probs(_p(q), _p(kc), _dt(q), _p(cu), len(cu) - 1, h, hkv, d, kernel,
+                                        stride, ctypes.c_double(scale), _p(rows), ctypes.c_int64(n),
+                                        _p(out), nc_stride), "cmp_probs")
+    return out
+
+
+def pool_row(pg, n_c, n_b, block_size=64, kernel=32, stride=16):
+    """S3 on one row of group probabilities."""
+    pg = np.ascontiguousarray(np.asarray(pg, np.float64))
+    out = np.zeros(n_b, np.float64)
+    _check(_load().nsa_oracle_pool_row(_p(pg), int(n_c), int(n_b), block_size, kernel, stride, _p(out)),
+           "pool_row")
+    return out
+
+
+def cmp_scores_pool(q, kc, cu, kernel=32, stride=16, block_size=64, scale=None, rows=None,
+                    nb_stride=None):
+    """S2+S3: pooled block scores [rows, hkv, nb_stride]."""
+    q, kc, cu = np.ascontiguousarray(q), np.ascontiguousarray(kc), _i32(cu)
+    tot, h, d = q.shape
+    hkv = kc.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    if nb_stride is None:
+        nb_stride = max(1, -(-int(np.max(np.diff(cu))) // block_size))
+    rows, n = _rows(rows, tot)
+    out = np.zeros((n, hkv, nb_stride), np.float64)
+    _check(_load().nsa_oracle_cmp_scores_pool(_p(q), _p(kc), _dt(q), _p(cu), len(cu) - 1, h, hkv, d,
+                                              kernel, stride, block_size, ctypes.c_double(scale),
+                                              _p(rows), ctypes.c_int64(n), _p(out), nb_stride),
+           "cmp_scores_pool")
+    return out
+
+
+def topk(scores, cu, block_size=64, n_init=1, n_local=2, k=16, rows=None):
+    """S4: block indices [rows, hkv, k] from scores [rows, hkv, nb_stride] (float64 or float32)."""
+    scores = np.ascontiguousarray(np.asarray(scores, np.float64))
+    cu = _i32(cu)
+    n_rows, hkv, nb_stride = scores.shape
+    rows, n = _rows(rows, int(cu[-1]))
+    if n != n_rows:
+        raise ValueError("scores must have one row per requested token")
+    out = np.zeros((n, hkv, k), np.int32)
+    _check(_load().nsa_oracle_topk(_p(scores), nb_stride, _p(cu), len(cu) - 1, hkv, block_size, n_init,
+                                   n_local, k, _p(rows), ctypes.c_int64(n), _p(out)), "topk")
+    return out
+
+
+def sparse_attn(q, k, v, idx, cu, block_size=64, scale=None, rows=None):
+    """S5: selected-block attention; returns (o [rows,h,d], lse [rows,h]) in fp64."""
+    q, k, v, idx, cu = (np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v),
+                        _i32(idx), _i32(cu))
+    tot, h, d = q.shape
+    hkv = k.shape[1]
+    S = idx.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    rows, n = _rows(rows, tot)
+    o = np.zeros((n, h, d), np.float64)
+    lse = np.zeros((n, h), np.float64)
+    _check(_load().nsa_oracle_sparse_attn(_p(q), _p(k), _p(v), _dt(q), _p(cu), len(cu) - 1, h, hkv, d,
+                                          _p(idx), S, block_size, ctypes.c_double(scale), _p(rows),
+                                          ctypes.c_int64(n), _p(o), _p(lse)), "sparse_attn")
+    return o, lse
+
+
+def swa(q, k, v, cu, window=512, scale=None, rows=None):
+    """S8: sliding-window attention; returns (o, lse)."""
+    q, k, v, cu = np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v), _i32(cu)
+    tot, h, d = q.shape
+    hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    rows, n = _rows(rows, tot)
+    o = np.zeros((n, h, d), np.float64)
+    lse = np.zeros((n, h), np.float64)
+    _check(_load().nsa_oracle_swa(_p(q), _p(k), _p(v), _dt(q), _p(cu), len(cu) - 1, h, hkv, d, window,
+                                  ctypes.c_double(scale), _p(rows), ctypes.c_int64(n), _p(o), _p(lse)),
+           "swa")
+    return o, lse
+
+
+def cmp_attn(q, kc, vc, cu, kernel=32, stride=16, scale=None, rows=None):
+    """S7: compressed-attention branch over stored compressed keys/values; (o, lse)."""
+    q, kc, vc, cu = (np.ascontiguousarray(q), np.ascontiguousarray(kc), np.ascontiguousarray(vc),
+                     _i32(cu))
+    tot, h, d = q.shape
+    hkv = kc.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    rows, n = _rows(rows, tot)
+    o = np.zeros((n, h, d), np.float64)
+    lse = np.zeros((n, h), np.float64)
+    _check(_load().nsa_oracle_cmp_attn(_p(q), _p(kc), _p(vc), _dt(q), _p(cu), len(cu) - 1, h, hkv, d,
+                                       kernel, stride, ctypes.c_double(scale), _p(rows),
+                                       ctypes.c_int64(n), _p(o), _p(lse)), "cmp_attn")
+    return o, lse
+
+
+def gate_combine(o_cmp, o_slc, o_swa, gates):
+    """S9: sigmoid-gated sum of the three branch outputs."""
+    o_cmp, o_slc, o_swa = (np.ascontiguousarray(np.asarray(a, np.float64)) for a in (o_cmp, o_slc, o_swa))
+    gates = np.ascontiguousarray(np.asarray(gates, np.float32))
+    n, h, d = o_cmp.shape
+    out = np.zeros_like(o_cmp)
+    _check(_load().nsa_oracle_gate_combine(_p(o_cmp), _p(o_slc), _p(o_swa), _p(gates), ctypes.c_int64(n),
+                                           h, d, _p(out)), "gate_combine")
+    return out
+
+
+def decode(q, k_cache, v_cache, kc_cache, seqlens, kernel=32, stride=16, block_size=64, n_init=1,
+           n_local=2, k=64, scale=None, idx_in=None, want_scores=False):
+    """S6: one decode step; returns (idx [B,hkv,k], o [B,h,d] fp64[, scores [B,hkv,nb]])."""
+    q, k_cache, v_cache, kc_cache = (np.ascontiguousarray(a) for a in (q, k_cache, v_cache, kc_cache))
+    seqlens = _i32(seqlens)
+    B, h, d = q.shape
+    max_len, hkv = k_cache.shape[1], k_cache.shape[2]
+    scale = d ** -0.5 if scale is None else scale
+    nb = -(-max_len // block_size)
+    idx = np.zeros((B, hkv, k), np.int32)
+    o = np.zeros((B, h, d), np.float64)
+    sc = np.zeros((B, hkv, nb), np.float64) if want_scores else None
+    ii = None if idx_in is None else _i32(idx_in)
+    _check(_load().nsa_oracle_decode(_p(q), _p(k_cache), _p(v_cache), _p(kc_cache), _dt(q), B,
+                                     _p(seqlens), max_len, h, hkv, d, kernel, stride, block_size, n_init,
+                                     n_local, k, ctypes.c_double(scale), _p(ii), _p(idx), _p(o), _p(sc),
+                                     nb), "decode")
+    return (idx, o, sc) if want_scores else (idx, o)
+
+
+def layer(q, k, v, gates, cu, kernel=32, stride=16, block_size=64, S=16, n_init=1, n_local=2,
+          window=512, scale=None, idx_in=None, rows=None, branches=False):
+    """Three-branch layer; returns dict with idx, o (and o_cmp/o_slc/o_swa if branches)."""
+    q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
+    gates = np.ascontiguousarray(np.asarray(gates, np.float32))
+    cu = _i32(cu)
+    tot, h, d = q.shape
+    hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    rows, n = _rows(rows, tot)
+    idx = np.zeros((n, hkv, S), np.int32)
+    o = np.zeros((n, h, d), np.float64)
+    oc = np.zeros((n, h, d), np.float64) if branches else None
+    os_ = np.zeros((n, h, d), np.float64) if branches else None
+    ow = np.zeros((n, h, d), np.float64) if branches else None
+    ii = None if idx_in is None else _i32(idx_in)
+    _check(_load().nsa_oracle_layer(_p(q), _p(k), _p(v), _p(gates), _dt(q), _p(cu), len(cu) - 1, h, hkv,
+                                    d, kernel, stride, block_size, S, n_init, n_local, window,
+                                    ctypes.c_double(scale), _p(ii), _p(rows), ctypes.c_int64(n), _p(idx),
+                                    _p(o), _p(oc), _p(os_), _p(ow)), "layer")
+    out = {"idx": idx, "o": o}
+    if branches:
+        out.update(o_cmp=oc, o_slc=os_, o_swa=ow)
+    return out

@@ -1,0 +1,426 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Each test checks the oracle against a library routine that computes the same
+definition (avg_pool1d, scaled_dot_product_attention, topk), a hand-computed
+value, or an invariant that determines the result uniquely.  None of them
+re-types the oracle's own formula.  CPU only.
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import oracle as orc
+from sparse_attention_compress_gb300 import inputs as gen
+
+F64 = torch.float64
+
+
+def _t(a):
+    """numpy (bf16 bits or fp32) -> torch float64."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        a = gen.bf16_bits_to_f32(a)
+    return torch.from_numpy(np.asarray(a, np.float64))
+
+
+def _rand(shape, seed, dtype="bf16"):
+    return gen.normal(np.random.Generator(np.random.PCG64(seed)), shape, dtype)
+
+
+def _sdpa_probs(q, k, mask):
+    """Attention probabilities through the library SDPA, using V = identity.
+    q [T,h,d], k [Tk,h,d] (already expanded per head), mask [T,Tk] bool."""
+    T, h, d = q.shape
+    Tk = k.shape[0]
+    eye = torch.eye(Tk, dtype=F64).expand(h, Tk, Tk)
+    return F.scaled_dot_product_attention(q.permute(1, 0, 2), k.permute(1, 0, 2), eye,
+                                          attn_mask=mask).permute(1, 0, 2)  # [T,h,Tk]
+
+
+def _sdpa(q, k, v, mask):
+    """SDPA float64 with GQA expansion; q [T,h,d], k/v [Tk,hkv,d], mask [T,Tk] bool."""
+    h, hkv = q.shape[1], k.shape[1]
+    r = h // hkv
+    ke = k.repeat_interleave(r, dim=1)
+    ve = v.repeat_interleave(r, dim=1)
+    return F.scaled_dot_product_attention(q.permute(1, 0, 2), ke.permute(1, 0, 2), ve.permute(1, 0, 2),
+                                          attn_mask=mask).permute(1, 0, 2)
+
+
+# --------------------------------------------------------------------------- S1
+def test_num_cmp_hand_values():
+    # full windows of 32 at stride 16 (hand-counted)
+    expect = {0: 0, 1: 0, 31: 0, 32: 1, 33: 1, 47: 1, 48: 2, 63: 2, 64: 3, 4100: 255, 32768: 2047,
+              65536: 4095}
+    for L, n in expect.items():
+        assert orc.num_cmp(L) == n, L
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_compress_equals_avg_pool1d(dtype):
+    lengths = [1, 31, 32, 47, 48, 100, 257]
+    cu = gen.varlen_cu_seqlens(lengths)
+    hkv, d = 2, 8
+    k = _rand((cu[-1], hkv, d), 11, dtype)
+    exact, rounded = orc.compress(k, cu)
+    kt = _t(k)
+    off = orc.cmp_offsets(cu)
+    for i, L in enumerate(lengths):
+        n_c = off[i + 1] - off[i]
+        if L < 32:
+            assert n_c == 0
+            continue
+        x = kt[cu[i]:cu[i + 1]].reshape(L, hkv * d).T.unsqueeze(1)  # [hkv*d, 1, L]
+        ref = F.avg_pool1d(x, 32, 16).squeeze(1).T.reshape(-1, hkv, d)
+        assert ref.shape[0] == n_c
+        got = torch.from_numpy(exact[off[i]:off[i + 1]])
+        assert torch.allclose(got, ref, rtol=0, atol=1e-14)
+    # the stored value is the nearest representable value of the storage dtype
+    if dtype == "f32":
+        assert np.array_equal(rounded, exact.astype(np.float32))
+    else:
+        r = rounded.astype(np.int64)
+        val = gen.bf16_bits_to_f32(rounded).astype(np.float64)
+        up = gen.bf16_bits_to_f32(((r & 0x7FFF) + 1 | (r & 0x8000)).astype(np.uint16)).astype(np.float64)
+        dn = gen.bf16_bits_to_f32(np.where((r & 0x7FFF) > 0, r - 1, r).astype(np.uint16)).astype(np.float64)
+        err = np.abs(val - exact)
+        assert np.all(err <= np.abs(up - exact))
+        assert np.all(err <= np.abs(dn - exact))
+        tie = (err == np.abs(up - exact)) | (err == np.abs(dn - exact))
+        tie &= err > 0
+        assert np.all((r[tie] & 1) == 0)  # ties go to the even pattern
+
+
+def test_compress_constant_and_window_independence():
+    cu = gen.varlen_cu_seqlens([64, 80])
+    k = np.full((144, 1, 4), 3.25, np.float32)
+    k[64:] = -1.5  # the second sequence must not leak into the first one's windows
+    exact, _ = orc.compress(k, cu)
+    assert np.all(exact[:3] == 3.25) and np.all(exact[3:] == -1.5)
+
+
+# --------------------------------------------------------------------------- S2
+def test_cmp_probs_kernel1_is_dense_causal_attention():
+    """With kernel = stride = 1 each compressed key is one token and the window rule
+    reduces to plain causal masking: the group probabilities must be the summed
+    causal attention probabilities of the group's heads."""
+    T, h, hkv, d = 40, 4, 2, 16
+    cu = gen.dense_cu_seqlens(1, T)
+    q = _rand((T, h, d), 1)
+    k = _rand((T, hkv, d), 2)
+    _, kc = orc.compress(k, cu, kernel=1, stride=1)
+    assert np.array_equal(kc, k)
+    pg = orc.cmp_probs(q, kc, cu, kernel=1, stride=1)
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    probs = _sdpa_probs(_t(q), _t(k).repeat_interleave(2, dim=1), mask)  # [T,h,T]
+    ref = probs.reshape(T, hkv, 2, T).sum(2)
+    assert torch.allclose(torch.from_numpy(pg), ref, atol=1e-13, rtol=0)
+
+
+def test_cmp_probs_window_causality_via_sdpa_mask():
+    lengths = [200, 77]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d = 4, 1, 32
+    q = _rand((cu[-1], h, d), 3)
+    k = _rand((cu[-1], hkv, d), 4)
+    _, kc = orc.compress(k, cu)
+    pg = orc.cmp_probs(q, kc, cu)
+    off = orc.cmp_offsets(cu)
+    for i, L in enumerate(lengths):
+        n_c = off[i + 1] - off[i]
+        t = torch.arange(L)[:, None]
+        c = torch.arange(n_c)[None, :]
+        mask = (16 * c + 31) <= t
+        live = mask.any(1)
+        qs = _t(q[cu[i]:cu[i + 1]])[live]
+        ks = _t(kc[off[i]:off[i + 1]]).repeat_interleave(h, dim=1)
+        ref = _sdpa_probs(qs, ks, mask[live]).sum(1)
+        got = torch.from_numpy(pg[cu[i]:cu[i + 1], 0, :n_c])
+        assert torch.allclose(got[live], ref, atol=1e-13, rtol=0)
+        assert torch.all(got[~live] == 0)
+        # every row with a causal compressed key sums to the group size
+        assert torch.allclose(got[live].sum(1), torch.full((int(live.sum()),), float(h), dtype=F64))
+
+
+# --------------------------------------------------------------------------- S3
+@pytest.mark.parametrize("L,expect", [
+    (31, [0.0]), (32, [0.0]), (47, [0.0]), (48, [0.5]), (63, [0.5]), (64, [1.0]),
+    (128, [1.0, 5.0]), (112, [1.0, 4.5]),
+])
+def test_pool_ramp_hand_values(L, expect):
+    # P_g[c] = c: block j averages c = 4j, 4j+1, 4j+2 where those windows exist
+    n_c = orc.num_cmp(L)
+    n_b = -(-L // 64)
+    got = orc.pool_row(np.arange(max(n_c, 1), dtype=np.float64), n_c, n_b)
+    assert got.tolist() == expect
+
+
+def test_pool_ramp_long_tail():
+    L = 4100
+    n_c, n_b = orc.num_cmp(L), -(-L // 64)
+    got = orc.pool_row(np.arange(n_c, dtype=np.float64), n_c, n_b)
+    assert n_c == 255 and n_b == 65
+    assert got[:64].tolist() == [4.0 * j + 1 for j in range(64)]
+    assert got[64] == 0.0
+
+
+@pytest.mark.parametrize("n_c", [3, 4, 5, 6, 7, 64, 255, 2047])
+def test_pool_equals_avg_pool1d_ceil(n_c):
+    rng = np.random.default_rng(n_c)
+    pg = rng.random(n_c)
+    n_b = (16 * (n_c - 1) + 32 + 63) // 64 + 1  # room for trailing empty blocks
+    got = orc.pool_row(pg, n_c, n_b)
+    ref = F.avg_pool1d(torch.from_numpy(pg).view(1, 1, -1), 3, 4, ceil_mode=True).flatten().numpy()
+    m = len(ref)
+    assert np.allclose(got[:m], ref, atol=1e-15, rtol=0)
+    assert np.all(got[m:] == 0)
+
+
+# --------------------------------------------------------------------------- S4
+def _check_topk_row(sc, t, bs, n_init, n_local, k, row):
+    own = t // bs
+    ncand = own + 1
+    take = min(k, ncand)
+    chosen = row[:take]
+    assert np.all(row[take:] == -1)
+    assert np.all(np.diff(chosen) > 0), "ascending and distinct"
+    assert chosen.min() >= 0 and chosen.max() <= own, "causal"
+    forced = {j for j in range(ncand) if j < n_init or j > own - n_local}
+    cs = set(chosen.tolist())
+    if len(forced) <= k:
+        assert forced <= cs
+    # dominance: anything chosen and not forced beats anything not chosen
+    for a in cs - forced:
+        for b in set(range(ncand)) - cs:
+            assert b not in forced
+            assert sc[a] > sc[b] or (sc[a] == sc[b] and a < b)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_invariants(seed):
+    rng = np.random.default_rng(seed)
+    bs = 64
+    L = int(rng.integers(1, 3000))
+    n_init, n_local, k = int(rng.integers(0, 3)), int(rng.integers(0, 3)), int(rng.integers(1, 20))
+    cu = gen.dense_cu_seqlens(1, L)
+    nb = -(-L // bs)
+    # few distinct levels -> many exact ties
+    sc = rng.integers(0, 4, size=(L, 1, nb)).astype(np.float64) / 4
+    idx = orc.topk(sc, cu, bs, n_init, n_local, k)
+    for t in range(0, L, max(1, L // 97)):
+        _check_topk_row(sc[t, 0], t, bs, n_init, n_local, k, idx[t, 0])
+
+
+def test_topk_equals_torch_topk_without_forcing():
+    rng = np.random.default_rng(7)
+    L, bs, k = 2048, 64, 9
+    sc = rng.permutation(L * 32).reshape(L, 1, 32).astype(np.float64)  # all distinct
+    idx = orc.topk(sc, gen.dense_cu_seqlens(1, L), bs, 0, 0, k)
+    for t in (0, 63, 64, 600, 2047):
+        own = t // bs
+        ref = torch.topk(torch.from_numpy(sc[t, 0, :own + 1]), min(k, own + 1)).indices.sort().values
+        assert idx[t, 0, :len(ref)].tolist() == ref.tolist()
+
+
+# --------------------------------------------------------------------------- S5
+def _all_causal_idx(cu, hkv, bs):
+    T = int(np.max(np.diff(cu)))
+    nb = -(-T // bs)
+    rows = []
+    for i in range(len(cu) - 1):
+        for t in range(cu[i + 1] - cu[i]):
+            rows.append([j if j <= t // bs else -1 for j in range(nb)])
+    return np.repeat(np.asarray(rows, np.int32)[:, None, :], hkv, axis=1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sparse_all_blocks_equals_dense_causal(dtype):
+    lengths = [150, 64, 33]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, bs = 4, 2, 16, 32
+    q, k, v = (_rand((cu[-1], hh, d), s, dtype) for s, hh in ((5, h), (6, hkv), (7, hkv)))
+    idx = _all_causal_idx(cu, hkv, bs)
+    o, lse = orc.sparse_attn(q, k, v, idx, cu, bs)
+    for i, L in enumerate(lengths):
+        sl = slice(cu[i], cu[i + 1])
+        mask = torch.ones(L, L, dtype=torch.bool).tril()
+        ref = _sdpa(_t(q[sl]), _t(k[sl]), _t(v[sl]), mask)
+        assert torch.allclose(torch.from_numpy(o[sl]), ref, atol=1e-12, rtol=0)
+        s = torch.einsum("thd,shd->ths", _t(q[sl]), _t(k[sl]).repeat_interleave(2, 1)) * d ** -0.5
+        ref_lse = torch.logsumexp(s.masked_fill(~mask[:, None, :], -torch.inf), -1)
+        assert torch.allclose(torch.from_numpy(lse[sl]), ref_lse, atol=1e-12, rtol=0)
+
+
+def test_sparse_own_block_is_local_attention():
+    T, h, hkv, d, bs = 130, 2, 1, 8, 32
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 8), _rand((T, hkv, d), 9), _rand((T, hkv, d), 10)
+    idx = (np.arange(T) // bs).astype(np.int32).reshape(T, 1, 1)
+    o, _ = orc.sparse_attn(q, k, v, idx, cu, bs)
+    t = torch.arange(T)
+    mask = (t[:, None] >= t[None, :]) & (t[:, None] // bs == t[None, :] // bs)
+    assert torch.allclose(torch.from_numpy(o), _sdpa(_t(q), _t(k), _t(v), mask), atol=1e-12, rtol=0)
+
+
+def test_sparse_order_padding_noncausal_and_duplicates():
+    T, h, hkv, d, bs = 256, 2, 1, 8, 32
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 12), _rand((T, hkv, d), 13), _rand((T, hkv, d), 14)
+    t = np.arange(T)
+    own = t // bs
+    base = np.stack([np.zeros(T), own], 1).astype(np.int32)       # {0, own}
+    shuf = np.stack([own, np.full(T, -1), np.full(T, 7), np.zeros(T)], 1).astype(np.int32)
+    o1, _ = orc.sparse_attn(q, k, v, base[:, None, :], cu, bs)
+    o2, _ = orc.sparse_attn(q, k, v, shuf[:, None, :], cu, bs)
+    # block 7 starts at 224: it is non-causal (skipped) for t < 224 only
+    early = t < 224
+    assert np.allclose(o1[early], o2[early], atol=1e-13, rtol=0)
+    # a block listed twice counts twice: same as attention with its keys duplicated
+    tq = 100
+    dup = np.array([[[0, 0, 3]]], np.int32)  # block 0 twice, own block 3 once
+    o3, _ = orc.sparse_attn(q, k, v, np.repeat(dup, T, 0), cu, bs, rows=[tq])
+    keys = list(range(0, 32)) * 2 + list(range(96, 101))
+    kk, vv = _t(k)[keys], _t(v)[keys]
+    ref = _sdpa(_t(q[tq:tq + 1]), kk, vv, torch.ones(1, len(keys), dtype=torch.bool))
+    assert torch.allclose(torch.from_numpy(o3), ref, atol=1e-12, rtol=0)
+
+
+def test_sparse_empty_list_gives_zero():
+    T, h, d = 40, 2, 8
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 15), _rand((T, 1, d), 16), _rand((T, 1, d), 17)
+    idx = np.full((T, 1, 2), -1, np.int32)
+    o, lse = orc.sparse_attn(q, k, v, idx, cu, 32)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+# --------------------------------------------------------------------------- S7, S8, S9
+def test_cmp_attn_kernel1_equals_dense_causal():
+    T, h, hkv, d = 70, 4, 2, 16
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 18), _rand((T, hkv, d), 19), _rand((T, hkv, d), 20)
+    o, _ = orc.cmp_attn(q, k, v, cu, kernel=1, stride=1)
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    assert torch.allclose(torch.from_numpy(o), _sdpa(_t(q), _t(k), _t(v), mask), atol=1e-12, rtol=0)
+
+
+def test_cmp_attn_window_mask_via_sdpa():
+    T, h, hkv, d = 300, 4, 2, 16
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 21), _rand((T, hkv, d), 22), _rand((T, hkv, d), 23)
+    _, kc = orc.compress(k, cu)
+    _, vc = orc.compress(v, cu)
+    o, _ = orc.cmp_attn(q, kc, vc, cu)
+    n_c = kc.shape[0]
+    mask = (16 * torch.arange(n_c)[None, :] + 31) <= torch.arange(T)[:, None]
+    live = mask.any(1)
+    ref = _sdpa(_t(q)[live], _t(kc), _t(vc), mask[live])
+    assert torch.allclose(torch.from_numpy(o)[live], ref, atol=1e-12, rtol=0)
+    assert np.all(o[~live.numpy()] == 0)
+
+
+@pytest.mark.parametrize("window", [1, 17, 64, 1000])
+def test_swa_equals_banded_sdpa(window):
+    T, h, hkv, d = 150, 4, 2, 16
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 24), _rand((T, hkv, d), 25), _rand((T, hkv, d), 26)
+    o, _ = orc.swa(q, k, v, cu, window=window)
+    t = torch.arange(T)
+    mask = (t[:, None] >= t[None, :]) & (t[:, None] - t[None, :] < window)
+    assert torch.allclose(torch.from_numpy(o), _sdpa(_t(q), _t(k), _t(v), mask), atol=1e-12, rtol=0)
+
+
+def test_gate_combine_saturation_and_half():
+    rng = np.random.default_rng(3)
+    a, b, c = (rng.standard_normal((5, 2, 4)) for _ in range(3))
+    sat = np.zeros((5, 2, 3), np.float32)
+    sat[..., 0], sat[..., 1], sat[..., 2] = 60.0, -60.0, -60.0
+    assert np.allclose(orc.gate_combine(a, b, c, sat), a, atol=1e-20, rtol=1e-15)
+    half = np.zeros((5, 2, 3), np.float32)  # sigmoid(0) = 1/2
+    assert np.allclose(orc.gate_combine(a, b, c, half), (a + b + c) / 2, atol=0, rtol=1e-15)
+
+
+# --------------------------------------------------------------------------- S6 and the layer
+def test_decode_equals_prefill_last_row():
+    B, L, h, hkv, d = 3, 700, 4, 2, 16
+    seqlens = np.array([700, 513, 64], np.int32)
+    q = _rand((B, h, d), 27)
+    kcache, vcache = _rand((B, L, hkv, d), 28), _rand((B, L, hkv, d), 29)
+    ncs = orc.num_cmp(L)
+    kc_cache = np.zeros((B, ncs, hkv, d), np.uint16)
+    for b in range(B):
+        _, kc = orc.compress(kcache[b, :seqlens[b]], [0, seqlens[b]])
+        kc_cache[b, :len(kc)] = kc
+    idx, o = orc.decode(q, kcache, vcache, kc_cache, seqlens, k=5)
+    for b in range(B):
+        Lb = int(seqlens[b])
+        cu = np.array([0, Lb], np.int32)
+        qf = np.zeros((Lb, h, d), np.uint16)
+        qf[-1] = q[b]
+        kb, vb = kcache[b, :Lb], vcache[b, :Lb]
+        _, kc = orc.compress(kb, cu)
+        sc = orc.cmp_scores_pool(qf, kc, cu, rows=[Lb - 1])
+        ib = orc.topk(sc, cu, k=5, rows=[Lb - 1])
+        assert np.array_equal(ib[0], idx[b])
+        ob, _ = orc.sparse_attn(qf, kb, vb, np.repeat(ib, Lb, 0), cu, rows=[Lb - 1])
+        assert np.allclose(ob[0], o[b], atol=1e-13, rtol=0)
+
+
+def test_decode_all_blocks_is_dense_last_row():
+    B, L, h, hkv, d = 2, 300, 4, 2, 16
+    q = _rand((B, h, d), 30)
+    kcache, vcache = _rand((B, L, hkv, d), 31), _rand((B, L, hkv, d), 32)
+    kc_cache = np.zeros((B, orc.num_cmp(L), hkv, d), np.uint16)
+    for b in range(B):
+        kc_cache[b] = orc.compress(kcache[b], [0, L])[1]
+    _, o = orc.decode(q, kcache, vcache, kc_cache, np.full(B, L, np.int32), k=64)
+    for b in range(B):
+        ref = _sdpa(_t(q[b:b + 1]), _t(kcache[b]), _t(vcache[b]), torch.ones(1, L, dtype=torch.bool))
+        assert torch.allclose(torch.from_numpy(o[b:b + 1]), ref, atol=1e-12, rtol=0)
+
+
+def test_layer_is_composition_of_branches():
+    T, h, hkv, d = 400, 4, 2, 16
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v = _rand((T, h, d), 33), _rand((T, hkv, d), 34), _rand((T, hkv, d), 35)
+    gates = np.random.default_rng(1).standard_normal((T, h, 3)).astype(np.float32)
+    rows = [0, 31, 63, 64, 200, 399]
+    out = orc.layer(q, k, v, gates, cu, S=4, window=100, rows=rows, branches=True)
+    _, kc = orc.compress(k, cu)
+    _, vc = orc.compress(v, cu)
+    oc, _ = orc.cmp_attn(q, kc, vc, cu, rows=rows)
+    sc = orc.cmp_scores_pool(q, kc, cu, rows=rows)
+    idx = orc.topk(sc, cu, k=4, rows=rows)
+    assert np.array_equal(idx, out["idx"])
+    full_idx = np.full((T, hkv, 4), -1, np.int32)
+    full_idx[rows] = idx
+    os_, _ = orc.sparse_attn(q, k, v, full_idx, cu, rows=rows)
+    ow, _ = orc.swa(q, k, v, cu, window=100, rows=rows)
+    assert np.allclose(out["o_cmp"], oc, atol=1e-14, rtol=0)
+    assert np.allclose(out["o_slc"], os_, atol=1e-14, rtol=0)
+    assert np.allclose(out["o_swa"], ow, atol=1e-14, rtol=0)
+    ref = orc.gate_combine(oc, os_, ow, gates[rows])
+    assert np.allclose(out["o"], ref, atol=1e-14, rtol=0)
+
+
+# --------------------------------------------------------------------------- input generator
+def test_bf16_rounding_matches_torch():
+    x = np.random.default_rng(0).standard_normal(100000).astype(np.float32)
+    x[:4] = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 0.0]  # exact ties
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(gen.f32_to_bf16_bits(x), ref)
+
+
+def test_random_indices_structure():
+    w = gen.prefill(B=2, T=1000)
+    t = np.tile(np.arange(1000), 2)
+    own = t // 64
+    idx = w.idx[:, 0, :]
+    for r in range(0, 2000, 37):
+        row = idx[r]
+        valid = row[row >= 0]
+        assert np.all(np.diff(valid) > 0)
+        assert valid.max() == own[r] and valid.min() == 0
+        assert len(valid) == min(16, own[r] + 1)
+        assert np.all(row[len(valid):] == -1)
