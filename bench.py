@@ -1,0 +1,420 @@
+#!/usr/bin/env python
+"""Benchmark of the native-sparse-attention hot path on GB300.
+
+Headline: selected-attention prefill forward (B=8, T=16384, H=16, Hkv=1, d=128, bf16,
+block 64, S=16 random causal blocks incl. block 0 and the own block) in TFLOP/s of
+algorithmic work (4*d per attended (query head, key) pair).  One step = one
+nsa_sparse_fwd over the whole batch.  Also measured in the same run (N=1): the decode
+step (B=32, context 32768, top-k 64; KV GB/s), the varlen selection stage
+(compress -> block scores -> top-k; tokens/s) and the full three-branch layer at
+65536 tokens (TFLOP/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica (weak scaling, no collective on the data
+path); rank 0 prints one JSON line.  --impl reference times the CPU oracle instead, on a
+bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_compress_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roofline"
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+def selected_pairs(idx: np.ndarray, cu: np.ndarray, block_size: int) -> np.ndarray:
+    """Attended keys per (token, kv-head) row of a block list (causal masking inside blocks)."""
+    t = np.concatenate([np.arange(cu[i + 1] - cu[i]) for i in range(len(cu) - 1)])
+    i = idx.astype(np.int64)
+    n = np.clip(t[:, None, None] - i * block_size + 1, 0, block_size)
+    n = np.where(i >= 0, n, 0)
+    return n.sum(axis=-1)  # [tokens, hkv]
+
+
+def prefill_flops(w) -> float:
+    r = w.h // w.hkv
+    return float(selected_pairs(w.idx, w.cu_seqlens, w.block_size).sum()) * r * 4 * w.d
+
+
+# ----------------------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc = index, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- timing
+def timed(torch, fn, steps, warmup, flush=None, barrier=None):
+    """Warm up, then time exactly `steps` calls of fn with CUDA events on the current stream.
+    The L2 flush (if any) runs between the event pairs.  Returns per-step ms."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        if flush is not None:
+            flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def dev(torch, a, device):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def pinned(torch, a):
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+    return t.pin_memory()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) runs
+def oracle_prefill_sample(w, n_rows: int, seed: int = 0):
+    """Time the CPU oracle on n_rows sampled query tokens; returns (TFLOP/s, seconds, flops, threads)."""
+    from oracle import oracle as orc
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.tokens, size=n_rows, replace=False))
+    t = rows % w.seqlen
+    i = w.idx[rows].astype(np.int64)
+    n = np.where(i >= 0, np.clip(t[:, None, None] - i * w.block_size + 1, 0, w.block_size), 0)
+    flops = float(n.sum()) * (w.h // w.hkv) * 4 * w.d
+    t0 = time.perf_counter()
+    orc.sparse_attn(w.q, w.k, w.v, w.idx, w.cu_seqlens, w.block_size, rows=rows)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, flops, orc.threads()
+
+
+def run_reference(args):
+    """CPU oracle arm: each step is the oracle on a bounded sample of the prefill workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    orc.build()
+    w = gen.prefill()
+    _, dt, _, _ = oracle_prefill_sample(w, 32, seed=99)
+    n_rows = int(min(4096, max(32, 32 * 2.5 / max(dt, 1e-3))))  # ~2.5 s per step
+    for s in range(args.warmup):
+        oracle_prefill_sample(w, n_rows, seed=1000 + s)
+    vals, times = [], []
+    for s in range(args.steps):
+        v, dt, _, thr = oracle_prefill_sample(w, n_rows, seed=s)
+        vals.append(v)
+        times.append(dt)
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill B=8 T=16384 H=16 Hkv=1 d=128 bf16 block=64 S=16",
+                   "sample_rows_per_step": n_rows, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.threads(), "kind": "oracle",
+                         "sample": f"{n_rows} random query tokens (all 16 heads) of the prefill workload per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- extras (N=1)
+def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
+    w = gen.decode()
+    q, kc_, vc_ = dev(torch, w.q, device), dev(torch, w.k_cache, device), dev(torch, w.v_cache, device)
+    sl = dev(torch, w.seqlens, device)
+    n_c = nsa.num_cmp(w.max_len)
+    kcmp = nsa.nsa_compress_k(kc_).view(w.batch, n_c, w.hkv, w.d)
+    ws = torch.empty(nsa.nsa_sparse_decode_workspace_size(w.batch, w.max_len, w.h, w.hkv, w.d, k=w.topk),
+                     dtype=torch.uint8, device=device)
+    idx = torch.empty((w.batch, w.hkv, w.topk), dtype=torch.int32, device=device)
+    out = torch.empty_like(q)
+
+    def step():
+        nsa.nsa_sparse_decode(q, kc_, vc_, kcmp, sl, k=w.topk, workspace=ws, idx_out=idx, out=out)
+
+    # CUDA graph of the four launches
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        step()
+    torch.cuda.current_stream().wait_stream(st)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    ms = timed(torch, g.replay, steps, warmup, flush)
+    # algorithmic bytes: compressed keys of every (seq, kv-head), the chosen K/V rows, q and o
+    ih = idx.cpu().numpy()
+    t = (w.seqlens.astype(np.int64) - 1)[:, None, None]
+    i = ih.astype(np.int64)
+    keys = np.where(i >= 0, np.clip(t - i * 64 + 1, 0, 64), 0).sum()
+    byts = w.batch * w.hkv * n_c * w.d * 2 + keys * w.d * 2 * 2 + 2 * w.batch * w.h * w.d * 2
+    ms_step = float(np.mean(ms))
+    gbs = byts / (ms_step * 1e-3) / 1e9
+    # compressing the cache (timed separately: one HBM pass over 537 MB)
+    msc = timed(torch, lambda: nsa.nsa_compress_k(kc_, out=kcmp.view(-1, w.hkv, w.d)), steps, warmup, flush)
+    cbytes = kc_.numel() * 2 + kcmp.numel() * 2
+    cgbs = cbytes / (float(np.mean(msc)) * 1e-3) / 1e9
+    return {"workload": "decode B=32 L=32768 H=16 Hkv=2 d=128 bf16 top-k 64 (blocks of 64)",
+            "ms_per_step": ms_step, "kv_gbs": gbs, "tokens_per_s": w.batch / (ms_step * 1e-3),
+            "bytes_per_step": int(byts), "hbm_frac": gbs / peaks["hbm_gbs"], "launches_per_step": 4,
+            "cuda_graph": True,
+            "compress_cache": {"ms": float(np.mean(msc)), "gbs": cgbs, "hbm_frac": cgbs / peaks["hbm_gbs"],
+                               "bytes": int(cbytes)}}
+
+
+def bench_selection(torch, nsa, device, steps, warmup, flush):
+    w = gen.selection()
+    q, k = dev(torch, w.q, device), dev(torch, w.k, device)
+    cu = dev(torch, w.cu_seqlens, device)
+    lens = np.diff(w.cu_seqlens)
+    n_cmp = int(sum(nsa.num_cmp(int(L)) for L in lens))
+    kc = torch.empty((n_cmp, w.hkv, w.d), dtype=torch.bfloat16, device=device)
+    nb = -(-w.max_len // 64)
+    nb = (nb + 3) // 4 * 4
+    sc = torch.empty((w.tokens, w.hkv, nb), dtype=torch.float32, device=device)
+    idx = torch.empty((w.tokens, w.hkv, 16), dtype=torch.int32, device=device)
+
+    def step():
+        nsa.nsa_compress_k(k, cu_seqlens=cu, max_seqlen=w.max_len, out=kc)
+        nsa.nsa_cmp_scores_pool(q, kc, w.hkv, cu_seqlens=cu, max_seqlen=w.max_len, nb_stride=nb, out=sc)
+        nsa.nsa_topk_select(sc, 16, cu_seqlens=cu, max_seqlen=w.max_len, out=idx)
+
+    ms = float(np.mean(timed(torch, step, steps, warmup, flush)))
+    t = np.concatenate([np.arange(L) for L in lens])
+    ncaus = np.where(t >= 31, (t - 31) // 16 + 1, 0)
+    flops = float(ncaus.sum()) * w.h * 2 * w.d
+    return {"workload": f"selection varlen lengths {lens.tolist()} H=16 Hkv=2 d=128 bf16 (compress 32/16, "
+                        "pool to 64-token blocks, top-16 with 1 init + 2 local)",
+            "ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "qk_tflops": flops / (ms * 1e-3) / 1e12,
+            "launches_per_step": 3}
+
+
+def bench_layer(torch, nsa, device, steps, warmup, flush):
+    w = gen.layer()
+    q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
+    gates = dev(torch, w.gates, device)
+    shp = nsa.make_shape(w.tokens, w.h, w.hkv, w.d, 1, batch=1, seqlen=w.tokens)
+    ws = torch.empty(nsa.nsa_layer_fwd_workspace_size(shp), dtype=torch.uint8, device=device)
+    idx = torch.empty((w.tokens, w.hkv, 16), dtype=torch.int32, device=device)
+    out = torch.empty_like(q)
+
+    def step():
+        nsa.nsa_layer_fwd(q, k, v, gates, workspace=ws, idx_out=idx, out=out)
+
+    ms = float(np.mean(timed(torch, step, steps, warmup, flush)))
+    t = np.arange(w.tokens)
+    ncaus = np.where(t >= 31, (t - 31) // 16 + 1, 0).astype(np.float64)
+    ih = idx.cpu().numpy().astype(np.int64)
+    sel = np.where(ih >= 0, np.clip(t[:, None, None] - ih * 64 + 1, 0, 64), 0).sum()
+    r = w.h // w.hkv
+    flops = 4 * w.d * (ncaus.sum() * w.h + float(sel) * r + np.minimum(t + 1, 512).sum() * w.h)
+    return {"workload": "layer B=1 T=65536 H=64 Hkv=4 d=128 bf16 (compressed 32/16 + selected 64x16 + window 512 "
+                        "+ sigmoid gates)",
+            "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": w.tokens / (ms * 1e-3),
+            "flops_per_step": flops, "launches_per_step": 8}
+
+
+# ----------------------------------------------------------------------------- main arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import sparse_attention_compress_gb300 as nsa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        barrier = dist.barrier
+    nsa.load()
+    peaks = load_peaks()
+
+    w = gen.prefill()
+    flops = prefill_flops(w)
+    q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
+    idx = dev(torch, w.idx, device)
+    out = torch.empty_like(q)
+    qv = q.view(w.batch, w.seqlen, w.h, w.d)
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    def step():
+        nsa.nsa_sparse_fwd(qv, k, v, idx, w.block_size, out=out)
+
+    clocks = Clocks(local)
+    clocks.start()
+    ms = timed(torch, step, args.steps, args.warmup, flush, barrier)
+    clk = clocks.stop()
+    ms_step = float(np.mean(ms))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    kernel_tflops = flops / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public call with host buffers: inputs in, output out
+    hq, hk, hv, hi = pinned(torch, w.q), pinned(torch, w.k), pinned(torch, w.v), pinned(torch, w.idx)
+    ho = torch.empty((w.tokens, w.h, w.d), dtype=torch.int16).pin_memory()
+    q16, k16, v16 = q.view(torch.int16), k.view(torch.int16), v.view(torch.int16)
+
+    def e2e_step():
+        q16.copy_(hq, non_blocking=True)
+        k16.copy_(hk, non_blocking=True)
+        v16.copy_(hv, non_blocking=True)
+        idx.copy_(hi, non_blocking=True)
+        nsa.nsa_sparse_fwd(qv, k, v, idx, w.block_size, out=out)
+        ho.copy_(out.view(torch.int16).view(w.tokens, w.h, w.d), non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 2)
+    e2e_ms = float(np.mean(timed(torch, e2e_step, e2e_steps, 1, None, barrier)))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hi))
+    d2h = ho.numel() * ho.element_size()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill B=8 T=16384 H=16 Hkv=1 d=128 bf16, block 64, S=16 random causal blocks "
+                               "(block 0 and own block always listed)", "global_batch": 8 * world,
+                   "seq_len": 16384, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (256 MB write outside the event pair)",
+                   "flops_per_step": flops},
+        "roofline": {"kernel": "sparse_fwd_mma<128,64,3>", "bound": "tensor", "achieved": kernel_tflops,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
+                     "peak_source": peaks["source"] + " bf16 dense (cuBLAS burst)", "traffic": None},
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps + e2e_steps,
+        "clocks": clk,
+    }
+    del hq, hk, hv, hi, ho
+
+    if world == 1 and not args.no_extras:
+        del q, k, v, out, qv
+        torch.cuda.empty_cache()
+        try:
+            line["decode"] = bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks)
+            line["gpu_launches"] += 4 * args.steps + args.steps
+        except Exception as e:  # report, never hide
+            line["decode"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["selection"] = bench_selection(torch, nsa, device, args.steps, args.warmup, flush)
+            line["gpu_launches"] += 3 * args.steps
+        except Exception as e:
+            line["selection"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["layer"] = bench_layer(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush)
+            line["gpu_launches"] += 8 * max(3, args.steps // 2)
+        except Exception as e:
+            line["layer"] = {"error": repr(e)}
+
+    if rank == 0 and world == 1:
+        n_rows = args.cpu_sample_rows
+        if n_rows <= 0:
+            _, dt, _, _ = oracle_prefill_sample(w, 16, seed=7)
+            n_rows = int(min(8192, max(16, 16 * 15.0 / max(dt, 1e-3))))
+        val, dt, _, thr = oracle_prefill_sample(w, n_rows, seed=11)
+        line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{n_rows} random query tokens (all heads) of the prefill workload, "
+                                          f"{dt:.1f} s"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

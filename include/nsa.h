@@ -1,0 +1,199 @@
+/*
+ * nsa.h -- C ABI of libnsa.so, the GB300 (sm_103a) native-sparse-attention hot path.
+ *
+ * Sources, cited by page title and section:
+ *   [NOSA-Triton]  "NOSA-1B source walk-through #3: how the Triton kernel speeds up attention"
+ *   [NOSA-Parts]   "NOSA-1B core components: how KV-cache offload gives 5.04x decode throughput"
+ *   [NSA-Triton]   "DeepSeek NSA sparse attention in practice: optimising training with Triton"
+ *   [TileLang-NSA] "TileLang operator development: Native Sparse Attention implementation"
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is caller-owned DEVICE memory, dense row-major in the
+ *     layout given, 16-byte aligned.  The library allocates nothing.
+ *   - Token-major layouts.  Q and O are [tokens, h, d]; K and V are [tokens, h_kv, d].
+ *     A dense batch [B, T, ...] is the packed layout with B sequences of T tokens.
+ *     With cu_seqlens (device int32 [n_seqs+1], prefix sums starting at 0) the tokens of
+ *     sequence i are rows cu_seqlens[i] .. cu_seqlens[i+1]-1.  Positions t are relative
+ *     to the sequence start.
+ *   - Grouped-query attention: head hh reads kv-head hh / (h / h_kv)  ([TileLang-NSA]
+ *     sec. 2, "head_kv = heads // groups").
+ *   - Compressed keys: window `kernel`, step `stride` ([NOSA-Parts] core component 1:
+ *     32 and 16).  A sequence of length L has n_c(L) = (L-kernel)/stride + 1 full windows
+ *     (0 if L < kernel).  Compressed rows of all sequences are packed one sequence after
+ *     another: [sum_i n_c(L_i), h_kv, d].  Compressed key c is causal for query t when
+ *     its window has ended: c*stride + kernel - 1 <= t.
+ *   - Selection blocks of block_size tokens; a sequence has n_b(L) = ceil(L/block_size).
+ *   - scale <= 0 selects 1/sqrt(d).
+ *   - Execution is asynchronous on `stream`; no call synchronises the host.
+ *   - Errors: argument errors return NSA_ERR_INVALID / NSA_ERR_UNSUPPORTED before any
+ *     launch; a failed launch returns NSA_ERR_CUDA.  nsa_last_error() gives a message
+ *     (per calling thread).  No C++ exception crosses this interface.  There is no CPU
+ *     fallback: a shape the kernels do not cover is rejected.
+ */
+#ifndef NSA_H_
+#define NSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define NSA_API __attribute__((visibility("default")))
+#else
+#define NSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NSA_OK = 0,
+  NSA_ERR_INVALID = 1,     /* null/misaligned pointer, inconsistent sizes            */
+  NSA_ERR_UNSUPPORTED = 2, /* valid arguments outside the shapes the kernels cover   */
+  NSA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                   */
+  NSA_ERR_TIMEOUT = 4      /* reserved for device-side bounded waits                  */
+} nsa_status;
+
+typedef enum { NSA_F32 = 0, NSA_BF16 = 1 } nsa_dtype;
+
+typedef struct nsa_shape {
+  int32_t batch;              /* dense layout: number of sequences (cu_seqlens == NULL)   */
+  int32_t seqlen;             /* dense: tokens per sequence; varlen: the longest length   */
+  const int32_t* cu_seqlens;  /* device [n_seqs+1], or NULL for the dense layout          */
+  int32_t n_seqs;             /* varlen only: number of sequences                        */
+  int64_t total_tokens;       /* varlen only: cu_seqlens[n_seqs] (dense: batch*seqlen)   */
+  int32_t h, h_kv, d;         /* query heads, kv-heads, head dimension                    */
+  nsa_dtype dtype;            /* element type of Q, K, V, O and compressed keys          */
+} nsa_shape;
+
+/* Library version string. */
+NSA_API const char* nsa_version(void);
+
+/* Message of the last failed call made by this thread ("" if none). */
+NSA_API const char* nsa_last_error(void);
+
+/* S1 -- key (or value) compression.  [NOSA-Parts] core component 1: keys are cut into
+ * windows of `kernel` tokens at step `stride` and each window is mean-pooled;
+ * [NOSA-Triton] "beyond the kernel": kernel 32, stride 16, 50% overlap.
+ *   k      [tokens, h_kv, d]            in
+ *   k_cmp  [sum_i n_c(L_i), h_kv, d]    out, fp32 mean rounded to nearest (ties even)
+ * Windows never cross a sequence boundary.  Requires kernel % stride == 0 and
+ * kernel/stride <= 4; h_kv*d a multiple of 8 (bf16) or 4 (fp32). */
+NSA_API nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,
+                          cudaStream_t stream);
+
+/* S2+S3 -- compressed scores pooled to selection blocks.  [NSA-Triton] sec. 1.1 (the
+ * selection reuses the compressed-attention scores) and [NOSA-Parts] core component 3,
+ * stage 1 (a light attention of q against the compressed keys): for query t, head hh of
+ * group g, p[hh,c] = softmax over causal c of scale * q[t,hh].k_cmp[c,g]; the group
+ * probability P_g[c] = sum over the group's heads of p[hh,c].  [NOSA-Triton] mechanisms
+ * 2-3 (window mean divided by the count of valid entries): the block score of block j is
+ * the mean of P_g over the windows inside the block, {c : c*stride >= j*block_size,
+ * c*stride + kernel <= (j+1)*block_size}, counting windows c < n_c(L) only (causally
+ * masked ones count as zeros); no such window gives 0.
+ *   q             [tokens, h, d] bf16
+ *   k_cmp         packed compressed keys (nsa_compress_k) bf16
+ *   lse_in        nullable [tokens, h] fp32: the natural-log softmax normaliser of each
+ *                 (token, head) over its causal compressed keys, as written by
+ *                 nsa_cmp_attn_fwd.  Given, the kernel skips its own normaliser pass.
+ *   block_scores  [tokens, h_kv, nb_stride] fp32 out; entries j >= n_b(L) are 0.
+ * Requires kernel 32, stride 16, block_size 64, d in {64,128}, h/h_kv in {1,2,4,8,16},
+ * nb_stride >= n_b(longest sequence). */
+NSA_API nsa_status nsa_cmp_scores_pool(const nsa_shape* shape, const void* q, const void* k_cmp, int kernel,
+                               int stride, int block_size, float scale, const float* lse_in,
+                               float* block_scores, int nb_stride, cudaStream_t stream);
+
+/* S4 -- top-k block selection.  [NOSA-Triton] "beyond the kernel": keep the
+ * n_init initial blocks and the n_local local blocks (ending at the query's own block
+ * t / block_size) as forced candidates, exclude blocks that start after t, take the k
+ * best by score and return them sorted.  Forced blocks rank above every score; equal
+ * scores rank the lower block index first; k counts the forced blocks; when fewer than k
+ * blocks are causal the list is padded with -1 at the end.
+ *   block_scores   [tokens, h_kv, nb_stride] fp32 (finite) in
+ *   block_indices  [tokens, h_kv, k] int32 out, ascending, -1 padded
+ * Requires 1 <= k <= 64 and nb_stride <= 2048. */
+NSA_API nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, int nb_stride,
+                           int block_size, int n_init, int n_local, int k, int32_t* block_indices,
+                           cudaStream_t stream);
+
+/* S5 -- selected-block attention (prefill).  [TileLang-NSA] sec. 2: for each entry of
+ * the query's list the block starting at i_s = index * block_size is used when
+ * 0 <= i_s <= t; keys past t inside it are masked; every query head of a GQA group reads
+ * the same block list ([NSA-Triton] sec. 1.2, group-centric loading).  Softmax in fp32
+ * with base-2 exponentials of scale*log2(e)-folded scores ([TileLang-NSA] sec. 3.1).
+ *   q, o           [tokens, h, d]; k, v [tokens, h_kv, d]
+ *   block_indices  [tokens, h_kv, S] int32; -1 and non-causal entries are skipped; an
+ *                  index listed twice is attended twice
+ *   lse            nullable [tokens, h] fp32 out: natural-log softmax normaliser (-inf
+ *                  and o = 0 when no key is selected)
+ * bf16: d in {64,128}, block_size in {16,32,64}, S <= 64, h/h_kv <= 16 or a multiple
+ * of 16.  fp32: d <= 256, S*block_size <= 4096. */
+NSA_API nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                          const int32_t* block_indices, int S, int block_size, float scale, void* o,
+                          float* lse, cudaStream_t stream);
+
+/* S7 -- compressed-attention branch.  [NSA-Triton] sec. 1.1 and 2.2 (taken as the
+ * definition): softmax over the causal compressed keys of scale * q.k_cmp, weighted sum
+ * of v_cmp.  A query with no causal compressed key gets o = 0 and lse = -inf.
+ *   k_cmp, v_cmp   packed compressed keys / values (nsa_compress_k on K and on V)
+ *   o [tokens, h, d] out; lse nullable [tokens, h] fp32 out (natural log)
+ * bf16 only; d in {64,128}; h/h_kv divides 16 or is a multiple of 16. */
+NSA_API nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k_cmp,
+                            const void* v_cmp, int kernel, int stride, float scale, void* o, float* lse,
+                            cudaStream_t stream);
+
+/* S8 -- sliding-window branch ([NSA-Triton] sec. 1.1: the most recent tokens): keys
+ * max(0, t-window+1) .. t.  Same layouts and limits as nsa_cmp_attn_fwd. */
+NSA_API nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                       int window, float scale, void* o, float* lse, cudaStream_t stream);
+
+/* S9 -- gate combine ([NSA-Triton] sec. 1.1: gates[0]*compressed + gates[1]*selected +
+ * gates[2]*local), each gate the logistic sigmoid of its logit.
+ *   o_cmp, o_slc, o_swa, o  [tokens, h, d] bf16;  gate_logits [tokens, h, 3] fp32.
+ * o may alias any input.  d a multiple of 8. */
+NSA_API nsa_status nsa_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
+                            const void* o_swa, const float* gate_logits, void* o,
+                            cudaStream_t stream);
+
+/* S6 -- one decode step.  [NOSA-Parts] "how decoding uses only 64 KV blocks": the
+ * newest query of each sequence (position L_b - 1; the cache already holds its key and
+ * value) is scored against the compressed keys (S2, S3), k blocks are chosen (S4) and
+ * attention runs over the chosen blocks only (S5).
+ *   seqlens      device int32 [batch], 1 <= L_b <= max_len
+ *   q, o         [batch, h, d] bf16
+ *   k_cache, v_cache  [batch, max_len, h_kv, d] bf16
+ *   k_cmp_cache  [batch, n_c(max_len), h_kv, d] bf16; rows c < n_c(L_b) valid
+ *   idx_out      nullable [batch, h_kv, k] int32: the chosen blocks
+ *   workspace    device scratch of nsa_sparse_decode_workspace_size() bytes, 256-byte
+ *                aligned, owned by the caller, not read before it is written
+ * Requires kernel 32, stride 16, block_size 64, d 128, h/h_kv in {1,2,4,8,16}, k <= 64,
+ * max_len <= 65536. */
+NSA_API size_t nsa_sparse_decode_workspace_size(int batch, int max_len, int h, int h_kv, int d, int kernel,
+                                        int stride, int block_size, int k);
+NSA_API nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d,
+                             const void* q, const void* k_cache, const void* v_cache,
+                             const void* k_cmp_cache, int kernel, int stride, int block_size,
+                             int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Full three-branch layer forward ([NSA-Triton] sec. 1.1): compress K and V (S1), the
+ * compressed branch (S7, which also yields the normaliser reused by the selection),
+ * block scores from the same compressed probabilities (S2, S3), top-S selection (S4),
+ * the selected branch (S5), the sliding-window branch (S8) and the gated sum (S9).
+ *   q, o [tokens, h, d] bf16; k, v [tokens, h_kv, d] bf16; gate_logits [tokens, h, 3]
+ *   idx_out nullable [tokens, h_kv, S] int32 (the chosen blocks)
+ *   workspace of nsa_layer_fwd_workspace_size() bytes (256-byte aligned)
+ * Limits: those of the calls above. */
+NSA_API size_t nsa_layer_fwd_workspace_size(const nsa_shape* shape, int kernel, int stride, int block_size,
+                                    int S);
+NSA_API nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                         const float* gate_logits, int kernel, int stride, int block_size, int S,
+                         int n_init, int n_local, int window, float scale, void* o, int32_t* idx_out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSA_H_ */

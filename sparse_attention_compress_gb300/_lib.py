@@ -1,0 +1,266 @@
+"""ctypes binding of libnsa.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see include/nsa.h)
+and does nothing but shape bookkeeping, output allocation through PyTorch and the
+call itself; all arithmetic of the path runs in the CUDA kernels.  There is no
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnsa.so")
+
+NSA_F32, NSA_BF16 = 0, 1
+_c_int, _c_i64, _c_p, _c_f, _c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+
+
+class NsaShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p),
+                ("n_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int64), ("h", ctypes.c_int32),
+                ("h_kv", ctypes.c_int32), ("d", ctypes.c_int32), ("dtype", ctypes.c_int)]
+
+
+_SIGS = {
+    "nsa_version": ([], ctypes.c_char_p),
+    "nsa_last_error": ([], ctypes.c_char_p),
+    "nsa_compress_k": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_p], _c_int),
+    "nsa_cmp_scores_pool": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_int, _c_p], _c_int),
+    "nsa_topk_select": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
+    "nsa_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
+    "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
+    "nsa_swa_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
+    "nsa_gate_combine": ([_c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p], _c_int),
+    "nsa_sparse_decode_workspace_size": ([_c_int] * 9, _c_sz),
+    "nsa_sparse_decode": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
+                           _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
+    "nsa_layer_fwd_workspace_size": ([_c_p, _c_int, _c_int, _c_int, _c_int], _c_sz),
+    "nsa_layer_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
+                       _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
+}
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libnsa.so (built by __graft_entry__.build() / build.py); raise if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+class NsaError(RuntimeError):
+    pass
+
+
+def _check(rc: int, fn: str) -> None:
+    if rc != 0:
+        msg = load().nsa_last_error().decode()
+        raise NsaError(f"{fn} failed (status {rc}): {msg}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NSA_BF16
+    if t.dtype == torch.float32:
+        return NSA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def make_shape(tokens: int, h: int, h_kv: int, d: int, dtype: int, *, cu_seqlens=None, max_seqlen=None,
+               batch=None, seqlen=None) -> NsaShape:
+    """Dense layout (batch, seqlen) or packed varlen (cu_seqlens device int32, max_seqlen)."""
+    s = NsaShape()
+    s.h, s.h_kv, s.d, s.dtype = h, h_kv, d, dtype
+    if cu_seqlens is not None:
+        if max_seqlen is None:
+            raise ValueError("varlen needs max_seqlen")
+        s.cu_seqlens = cu_seqlens.data_ptr()
+        s.n_seqs = cu_seqlens.numel() - 1
+        s.total_tokens = tokens
+        s.seqlen = int(max_seqlen)
+    else:
+        if batch is None:
+            batch, seqlen = 1, tokens
+        s.batch, s.seqlen = int(batch), int(seqlen)
+        if batch * seqlen != tokens:
+            raise ValueError("batch * seqlen must equal the token count")
+        s.cu_seqlens = None
+        s.total_tokens = tokens
+    return s
+
+
+def _flat(t: torch.Tensor):
+    """[B, T, H, d] -> ([B*T, H, d], B, T); [N, H, d] -> (t, None, None)."""
+    if t.dim() == 4:
+        B, T = t.shape[0], t.shape[1]
+        return t.reshape(B * T, t.shape[2], t.shape[3]), B, T
+    if t.dim() == 3:
+        return t, None, None
+    raise ValueError("expected [B, T, H, d] or [tokens, H, d]")
+
+
+def _shape_for(q, h_kv, cu_seqlens, max_seqlen):
+    qf, B, T = _flat(q)
+    if cu_seqlens is None and B is None:
+        B, T = 1, qf.shape[0]
+    return qf, make_shape(qf.shape[0], qf.shape[1], h_kv, qf.shape[2], _dtype(qf), cu_seqlens=cu_seqlens,
+                          max_seqlen=max_seqlen, batch=B, seqlen=T)
+
+
+def num_cmp(L: int, kernel: int = 32, stride: int = 16) -> int:
+    return (L - kernel) // stride + 1 if L >= kernel else 0
+
+
+# ----------------------------------------------------------------------------- entry points
+def nsa_compress_k(k, kernel=32, stride=16, *, cu_seqlens=None, max_seqlen=None, n_cmp=None, out=None,
+                   stream=None):
+    """S1.  k [B,T,Hkv,d] or packed [tokens,Hkv,d] -> packed compressed rows [n_cmp, Hkv, d]."""
+    kf, shp = _shape_for(k, k.shape[-2], cu_seqlens, max_seqlen)
+    if out is None:
+        if n_cmp is None:
+            if cu_seqlens is not None:
+                lens = (cu_seqlens[1:] - cu_seqlens[:-1]).tolist()
+                n_cmp = sum(num_cmp(int(L), kernel, stride) for L in lens)
+            else:
+                n_cmp = shp.batch * num_cmp(shp.seqlen, kernel, stride)
+        out = torch.empty((n_cmp, kf.shape[1], kf.shape[2]), dtype=kf.dtype, device=kf.device)
+    _check(load().nsa_compress_k(ctypes.byref(shp), _ptr(kf), _ptr(out), kernel, stride, _stream(stream)),
+           "nsa_compress_k")
+    return out
+
+
+def nsa_cmp_scores_pool(q, k_cmp, h_kv, kernel=32, stride=16, block_size=64, scale=0.0, *, lse_in=None,
+                        cu_seqlens=None, max_seqlen=None, nb_stride=None, out=None, stream=None):
+    """S2+S3.  Returns block scores [tokens, Hkv, nb_stride] fp32."""
+    qf, shp = _shape_for(q, h_kv, cu_seqlens, max_seqlen)
+    if nb_stride is None:
+        nb_stride = -(-shp.seqlen // block_size)
+    if out is None:
+        out = torch.empty((qf.shape[0], h_kv, nb_stride), dtype=torch.float32, device=qf.device)
+    _check(load().nsa_cmp_scores_pool(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), kernel, stride, block_size,
+                                      float(scale), _ptr(lse_in), _ptr(out), nb_stride, _stream(stream)),
+           "nsa_cmp_scores_pool")
+    return out
+
+
+def nsa_topk_select(block_scores, k, block_size=64, n_init=1, n_local=2, *, cu_seqlens=None, max_seqlen=None,
+                    batch=None, seqlen=None, out=None, stream=None):
+    """S4.  block_scores [tokens, Hkv, nb_stride] fp32 -> indices [tokens, Hkv, k] int32."""
+    tokens, h_kv, nb_stride = block_scores.shape
+    if cu_seqlens is None and batch is None:
+        batch, seqlen = 1, tokens
+    shp = make_shape(tokens, h_kv, h_kv, 1, NSA_F32, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, batch=batch,
+                     seqlen=seqlen)
+    if out is None:
+        out = torch.empty((tokens, h_kv, k), dtype=torch.int32, device=block_scores.device)
+    _check(load().nsa_topk_select(ctypes.byref(shp), _ptr(block_scores), nb_stride, block_size, n_init, n_local, k,
+                                  _ptr(out), _stream(stream)), "nsa_topk_select")
+    return out
+
+
+def nsa_sparse_fwd(q, k, v, block_indices, block_size=64, scale=0.0, *, cu_seqlens=None, max_seqlen=None,
+                   out=None, lse=None, stream=None):
+    """S5.  q [B,T,H,d] / [tokens,H,d]; k, v with Hkv heads; block_indices [..., Hkv, S] int32."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    S = block_indices.shape[-1]
+    if out is None:
+        out = torch.empty_like(qf)
+    _check(load().nsa_sparse_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(block_indices), S, block_size,
+                                 float(scale), _ptr(out), _ptr(lse), _stream(stream)), "nsa_sparse_fwd")
+    return out.view(q.shape) if q.dim() == 4 else out
+
+
+def nsa_cmp_attn_fwd(q, k_cmp, v_cmp, h_kv, kernel=32, stride=16, scale=0.0, *, cu_seqlens=None,
+                     max_seqlen=None, out=None, lse=None, stream=None):
+    """S7.  Compressed branch over packed compressed keys / values."""
+    qf, shp = _shape_for(q, h_kv, cu_seqlens, max_seqlen)
+    if out is None:
+        out = torch.empty_like(qf)
+    _check(load().nsa_cmp_attn_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), _ptr(v_cmp), kernel, stride,
+                                   float(scale), _ptr(out), _ptr(lse), _stream(stream)), "nsa_cmp_attn_fwd")
+    return out
+
+
+def nsa_swa_fwd(q, k, v, window=512, scale=0.0, *, cu_seqlens=None, max_seqlen=None, out=None, lse=None,
+                stream=None):
+    """S8.  Sliding-window branch."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    if out is None:
+        out = torch.empty_like(qf)
+    _check(load().nsa_swa_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), window, float(scale), _ptr(out),
+                              _ptr(lse), _stream(stream)), "nsa_swa_fwd")
+    return out
+
+
+def nsa_gate_combine(o_cmp, o_slc, o_swa, gate_logits, *, out=None, stream=None):
+    """S9.  out = sigmoid(g0) o_cmp + sigmoid(g1) o_slc + sigmoid(g2) o_swa."""
+    tokens, h, d = o_cmp.shape
+    if out is None:
+        out = torch.empty_like(o_cmp)
+    _check(load().nsa_gate_combine(tokens, h, d, _ptr(o_cmp), _ptr(o_slc), _ptr(o_swa), _ptr(gate_logits),
+                                   _ptr(out), _stream(stream)), "nsa_gate_combine")
+    return out
+
+
+def nsa_sparse_decode_workspace_size(batch, max_len, h, h_kv, d, kernel=32, stride=16, block_size=64, k=64):
+    return int(load().nsa_sparse_decode_workspace_size(batch, max_len, h, h_kv, d, kernel, stride, block_size, k))
+
+
+def nsa_sparse_decode(q, k_cache, v_cache, k_cmp_cache, seqlens, k=64, kernel=32, stride=16, block_size=64,
+                      n_init=1, n_local=2, scale=0.0, *, workspace=None, idx_out=None, out=None, stream=None):
+    """S6.  q [B,H,d]; caches [B,L,Hkv,d]; k_cmp_cache [B,n_c(L),Hkv,d]; seqlens device int32 [B]."""
+    B, h, d = q.shape
+    max_len, h_kv = k_cache.shape[1], k_cache.shape[2]
+    if workspace is None:
+        ws = nsa_sparse_decode_workspace_size(B, max_len, h, h_kv, d, kernel, stride, block_size, k)
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().nsa_sparse_decode(B, _ptr(seqlens), max_len, h, h_kv, d, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_cmp_cache), kernel, stride, block_size, n_init, n_local, k, float(scale),
+                                    _ptr(idx_out), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "nsa_sparse_decode")
+    return out
+
+
+def nsa_layer_fwd_workspace_size(shape: NsaShape, kernel=32, stride=16, block_size=64, S=16) -> int:
+    return int(load().nsa_layer_fwd_workspace_size(ctypes.byref(shape), kernel, stride, block_size, S))
+
+
+def nsa_layer_fwd(q, k, v, gate_logits, kernel=32, stride=16, block_size=64, S=16, n_init=1, n_local=2,
+                  window=512, scale=0.0, *, cu_seqlens=None, max_seqlen=None, workspace=None, idx_out=None,
+                  out=None, stream=None):
+    """Full three-branch layer forward."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    if workspace is None:
+        ws = nsa_layer_fwd_workspace_size(shp, kernel, stride, block_size, S)
+        workspace = torch.empty(ws, dtype=torch.uint8, device=qf.device)
+    if out is None:
+        out = torch.empty_like(qf)
+    _check(load().nsa_layer_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(gate_logits), kernel, stride,
+                                block_size, S, n_init, n_local, window, float(scale), _ptr(out), _ptr(idx_out),
+                                _ptr(workspace), workspace.numel(), _stream(stream)), "nsa_layer_fwd")
+    return out

@@ -1,0 +1,394 @@
+// C ABI of libnsa.so: argument checks, layout bookkeeping and dispatch to the kernels.
+// Every check runs before any launch; nothing here allocates device memory.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "../../include/nsa.h"
+#include "launch.h"
+
+using namespace nsa;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+nsa_status fail(nsa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+nsa_status cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) {
+    g_err[0] = 0;
+    return NSA_OK;
+  }
+  return fail(NSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define NSA_REQUIRE(cond, st, ...)     \
+  do {                                 \
+    if (!(cond)) return fail(st, __VA_ARGS__); \
+  } while (0)
+
+#define NSA_PTR(p)                                                                     \
+  do {                                                                                 \
+    if ((p) == nullptr) return fail(NSA_ERR_INVALID, "%s: null pointer " #p, __func__); \
+    if (!aligned16(p)) return fail(NSA_ERR_INVALID, "%s: " #p " not 16-byte aligned", __func__); \
+  } while (0)
+
+// Validate the common shape and build the kernel-side sequence description.
+nsa_status make_seqs(const nsa_shape* s, Seqs* out, const char* fn) {
+  if (!s) return fail(NSA_ERR_INVALID, "%s: null shape", fn);
+  if (s->h <= 0 || s->h_kv <= 0 || s->d <= 0) return fail(NSA_ERR_INVALID, "%s: h, h_kv, d must be positive", fn);
+  if (s->h % s->h_kv) return fail(NSA_ERR_INVALID, "%s: h (%d) not a multiple of h_kv (%d)", fn, s->h, s->h_kv);
+  if (s->dtype != NSA_F32 && s->dtype != NSA_BF16) return fail(NSA_ERR_INVALID, "%s: unknown dtype", fn);
+  if (s->seqlen < 0) return fail(NSA_ERR_INVALID, "%s: negative seqlen", fn);
+  Seqs q{};
+  if (s->cu_seqlens) {
+    if (s->n_seqs < 1) return fail(NSA_ERR_INVALID, "%s: varlen needs n_seqs >= 1", fn);
+    if (s->total_tokens < 0) return fail(NSA_ERR_INVALID, "%s: negative total_tokens", fn);
+    q.cu = s->cu_seqlens;
+    q.n_seqs = s->n_seqs;
+    q.T = 0;
+    q.tokens = s->total_tokens;
+    q.max_len = s->seqlen;
+  } else {
+    if (s->batch < 0) return fail(NSA_ERR_INVALID, "%s: negative batch", fn);
+    q.cu = nullptr;
+    q.n_seqs = s->batch;
+    q.T = s->seqlen;
+    q.tokens = (int64_t)s->batch * s->seqlen;
+    q.max_len = s->seqlen;
+  }
+  *out = q;
+  return NSA_OK;
+}
+
+bool pow2_le16(int r) { return r == 1 || r == 2 || r == 4 || r == 8 || r == 16; }
+int num_cmp_host(int L, int kernel, int stride) { return L >= kernel ? (L - kernel) / stride + 1 : 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char* nsa_version(void) { return "nsa-gb300 0.1 (sm_103a)"; }
+
+const char* nsa_last_error(void) { return g_err; }
+
+nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,
+                          cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(kernel > 0 && stride > 0, NSA_ERR_INVALID, "nsa_compress_k: kernel and stride must be positive");
+  NSA_REQUIRE(kernel % stride == 0 && kernel / stride <= 4, NSA_ERR_UNSUPPORTED,
+              "nsa_compress_k: needs kernel %% stride == 0 and kernel/stride <= 4 (got %d/%d)", kernel, stride);
+  const int vec = shape->dtype == NSA_BF16 ? 8 : 4;
+  NSA_REQUIRE((shape->h_kv * shape->d) % vec == 0, NSA_ERR_UNSUPPORTED,
+              "nsa_compress_k: h_kv*d must be a multiple of %d", vec);
+  if (s.tokens == 0 || s.max_len < kernel) return NSA_OK;
+  NSA_PTR(k);
+  NSA_PTR(k_cmp);
+  return cuda_status(launch_compress(s, k, k_cmp, shape->h_kv, shape->d, shape->dtype, kernel, stride, stream),
+                     "nsa_compress_k");
+}
+
+nsa_status nsa_cmp_scores_pool(const nsa_shape* shape, const void* q, const void* k_cmp, int kernel,
+                               int stride, int block_size, float scale, const float* lse_in,
+                               float* block_scores, int nb_stride, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
+              "nsa_cmp_scores_pool: supports kernel 32, stride 16, block_size 64");
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_cmp_scores_pool: bf16 only");
+  NSA_REQUIRE(shape->d == 64 || shape->d == 128, NSA_ERR_UNSUPPORTED, "nsa_cmp_scores_pool: d must be 64 or 128");
+  NSA_REQUIRE(pow2_le16(shape->h / shape->h_kv), NSA_ERR_UNSUPPORTED,
+              "nsa_cmp_scores_pool: h/h_kv must be 1, 2, 4, 8 or 16");
+  NSA_REQUIRE(nb_stride >= (s.max_len + block_size - 1) / block_size, NSA_ERR_INVALID,
+              "nsa_cmp_scores_pool: nb_stride %d < blocks of the longest sequence", nb_stride);
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(block_scores);
+  if (s.max_len >= kernel) NSA_PTR(k_cmp);
+  if (lse_in && (reinterpret_cast<uintptr_t>(lse_in) & 3u))
+    return fail(NSA_ERR_INVALID, "nsa_cmp_scores_pool: lse_in misaligned");
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_scores_pool(s, q, k_cmp, shape->h, shape->h_kv, shape->d, scale, lse_in, block_scores,
+                                        nb_stride, stream),
+                     "nsa_cmp_scores_pool");
+}
+
+nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, int nb_stride,
+                           int block_size, int n_init, int n_local, int k, int32_t* block_indices,
+                           cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(block_size > 0 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID,
+              "nsa_topk_select: block_size > 0, n_init >= 0, n_local >= 0");
+  NSA_REQUIRE(k >= 1 && k <= 64, NSA_ERR_UNSUPPORTED, "nsa_topk_select: k must be in [1, 64]");
+  NSA_REQUIRE(nb_stride >= (s.max_len + block_size - 1) / block_size, NSA_ERR_INVALID,
+              "nsa_topk_select: nb_stride %d < blocks of the longest sequence", nb_stride);
+  NSA_REQUIRE(nb_stride <= 2048, NSA_ERR_UNSUPPORTED, "nsa_topk_select: nb_stride must be <= 2048");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(block_scores);
+  NSA_PTR(block_indices);
+  return cuda_status(launch_topk(s, block_scores, nb_stride, shape->h_kv, block_size, n_init, n_local, k,
+                                 block_indices, stream),
+                     "nsa_topk_select");
+}
+
+nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                          const int32_t* block_indices, int S, int block_size, float scale, void* o,
+                          float* lse, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  const int r = shape->h / shape->h_kv;
+  NSA_REQUIRE(S >= 1 && block_size >= 1, NSA_ERR_INVALID, "nsa_sparse_fwd: S and block_size must be positive");
+  if (shape->dtype == NSA_BF16) {
+    NSA_REQUIRE(shape->d == 64 || shape->d == 128, NSA_ERR_UNSUPPORTED, "nsa_sparse_fwd: bf16 needs d 64 or 128");
+    NSA_REQUIRE(block_size == 16 || block_size == 32 || block_size == 64, NSA_ERR_UNSUPPORTED,
+                "nsa_sparse_fwd: bf16 needs block_size 16, 32 or 64");
+    NSA_REQUIRE(S <= 64, NSA_ERR_UNSUPPORTED, "nsa_sparse_fwd: S must be <= 64");
+    NSA_REQUIRE(r <= 16 || r % 16 == 0, NSA_ERR_UNSUPPORTED,
+                "nsa_sparse_fwd: h/h_kv must be <= 16 or a multiple of 16");
+  } else {
+    NSA_REQUIRE(shape->d <= 256, NSA_ERR_UNSUPPORTED, "nsa_sparse_fwd: fp32 needs d <= 256");
+    NSA_REQUIRE((int64_t)S * block_size <= 4096, NSA_ERR_UNSUPPORTED, "nsa_sparse_fwd: fp32 needs S*block_size <= 4096");
+  }
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(block_indices);
+  NSA_PTR(o);
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(NSA_ERR_INVALID, "nsa_sparse_fwd: lse misaligned");
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_sparse_fwd(s, q, k, v, block_indices, S, block_size, shape->h, shape->h_kv, shape->d,
+                                       shape->dtype, scale, o, lse, stream),
+                     "nsa_sparse_fwd");
+}
+
+static nsa_status dense_common(const nsa_shape* shape, Seqs* s, const char* fn) {
+  if (nsa_status st = make_seqs(shape, s, fn)) return st;
+  const int r = shape->h / shape->h_kv;
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);
+  NSA_REQUIRE(shape->d == 64 || shape->d == 128, NSA_ERR_UNSUPPORTED, "%s: d must be 64 or 128", fn);
+  NSA_REQUIRE((r <= 16 && 16 % r == 0) || (r % 16 == 0 && r <= 128), NSA_ERR_UNSUPPORTED,
+              "%s: h/h_kv must divide 16 or be a multiple of 16 up to 128", fn);
+  return NSA_OK;
+}
+
+nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k_cmp,
+                            const void* v_cmp, int kernel, int stride, float scale, void* o, float* lse,
+                            cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = dense_common(shape, &s, __func__)) return st;
+  NSA_REQUIRE(kernel > 0 && stride > 0, NSA_ERR_INVALID, "nsa_cmp_attn_fwd: kernel and stride must be positive");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(o);
+  if (s.max_len >= kernel) {
+    NSA_PTR(k_cmp);
+    NSA_PTR(v_cmp);
+  }
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(NSA_ERR_INVALID, "nsa_cmp_attn_fwd: lse misaligned");
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_dense_attn(0, s, q, k_cmp, v_cmp, shape->h, shape->h_kv, shape->d, kernel, stride, 0,
+                                       scale, o, lse, stream),
+                     "nsa_cmp_attn_fwd");
+}
+
+nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v, int window,
+                       float scale, void* o, float* lse, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = dense_common(shape, &s, __func__)) return st;
+  NSA_REQUIRE(window >= 1, NSA_ERR_INVALID, "nsa_swa_fwd: window must be >= 1");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(o);
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(NSA_ERR_INVALID, "nsa_swa_fwd: lse misaligned");
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_dense_attn(1, s, q, k, v, shape->h, shape->h_kv, shape->d, 0, 1, window, scale, o, lse,
+                                       stream),
+                     "nsa_swa_fwd");
+}
+
+nsa_status nsa_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
+                            const void* o_swa, const float* gate_logits, void* o, cudaStream_t stream) {
+  NSA_REQUIRE(tokens >= 0 && h > 0 && d > 0, NSA_ERR_INVALID, "nsa_gate_combine: bad sizes");
+  NSA_REQUIRE(d % 8 == 0, NSA_ERR_UNSUPPORTED, "nsa_gate_combine: d must be a multiple of 8");
+  if (tokens == 0) return NSA_OK;
+  NSA_PTR(o_cmp);
+  NSA_PTR(o_slc);
+  NSA_PTR(o_swa);
+  NSA_PTR(gate_logits);
+  NSA_PTR(o);
+  return cuda_status(launch_gate_combine(tokens, h, d, o_cmp, o_slc, o_swa, gate_logits, o, stream),
+                     "nsa_gate_combine");
+}
+
+size_t nsa_sparse_decode_workspace_size(int batch, int max_len, int h, int h_kv, int d, int kernel,
+                                        int stride, int block_size, int k) {
+  if (batch <= 0 || max_len <= 0 || h <= 0 || h_kv <= 0 || h % h_kv || k <= 0 || kernel <= 0 || stride <= 0)
+    return 0;
+  return decode_layout(batch, max_len, h, h_kv, d, kernel, stride, block_size, k).total;
+}
+
+nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d,
+                             const void* q, const void* k_cache, const void* v_cache,
+                             const void* k_cmp_cache, int kernel, int stride, int block_size,
+                             int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_REQUIRE(batch >= 0 && max_len >= 1 && h > 0 && h_kv > 0 && h % h_kv == 0, NSA_ERR_INVALID,
+              "nsa_sparse_decode: bad sizes");
+  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
+              "nsa_sparse_decode: supports kernel 32, stride 16, block_size 64");
+  NSA_REQUIRE(d == 128, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: d must be 128");
+  NSA_REQUIRE(pow2_le16(h / h_kv), NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: h/h_kv must be 1, 2, 4, 8 or 16");
+  NSA_REQUIRE(k >= 1 && k <= 64, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: k must be in [1, 64]");
+  NSA_REQUIRE(n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "nsa_sparse_decode: negative n_init/n_local");
+  NSA_REQUIRE(max_len <= 65536, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: max_len must be <= 65536");
+  if (batch == 0) return NSA_OK;
+  NSA_PTR(seqlens);
+  NSA_PTR(q);
+  NSA_PTR(k_cache);
+  NSA_PTR(v_cache);
+  NSA_PTR(o);
+  if (max_len >= kernel) NSA_PTR(k_cmp_cache);
+  if (idx_out) NSA_PTR(idx_out);
+  const DecodeLayout l = decode_layout(batch, max_len, h, h_kv, d, kernel, stride, block_size, k);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_sparse_decode: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= l.total, NSA_ERR_INVALID, "nsa_sparse_decode: workspace %zu < %zu bytes",
+              workspace_bytes, l.total);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  DecodeArgs a{};
+  a.batch = batch;
+  a.max_len = max_len;
+  a.h = h;
+  a.hkv = h_kv;
+  a.d = d;
+  a.kernel = kernel;
+  a.stride = stride;
+  a.block_size = block_size;
+  a.n_init = n_init;
+  a.n_local = n_local;
+  a.k = k;
+  a.scale = scale > 0.f ? scale : 1.f / sqrtf((float)d);
+  a.seqlens = seqlens;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.kc_cache = k_cmp_cache;
+  a.idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + l.idx);
+  a.o = o;
+  a.z = reinterpret_cast<float*>(w + l.z);
+  a.tile_ml = reinterpret_cast<float*>(w + l.tile_ml);
+  a.part_o = reinterpret_cast<float*>(w + l.part_o);
+  a.part_ml = reinterpret_cast<float*>(w + l.part_ml);
+  a.n_split = l.n_split;
+  return cuda_status(launch_decode(a, stream), "nsa_sparse_decode");
+}
+
+// Layer workspace: compressed K and V, the compressed and sliding branch outputs, the
+// compressed normaliser, the block scores and (when idx_out is NULL) the block lists.
+struct LayerLayout {
+  size_t kc, vc, o_cmp, o_swa, lse, scores, idx, total;
+  int nb_stride;
+};
+
+static LayerLayout layer_layout(const Seqs& s, int h, int hkv, int d, int esz, int kernel, int stride,
+                                int block_size, int S) {
+  LayerLayout l{};
+  // packed compressed rows: sum of n_c(L_i) <= tokens/stride + n_seqs
+  const int64_t ncr = s.cu ? s.tokens / stride + s.n_seqs : (int64_t)s.n_seqs * num_cmp_host(s.T, kernel, stride);
+  l.nb_stride = ((s.max_len + block_size - 1) / block_size + 3) / 4 * 4;
+  if (l.nb_stride == 0) l.nb_stride = 4;
+  size_t off = 0;
+  l.kc = off;
+  off = align256(off + (size_t)ncr * hkv * d * esz);
+  l.vc = off;
+  off = align256(off + (size_t)ncr * hkv * d * esz);
+  l.o_cmp = off;
+  off = align256(off + (size_t)s.tokens * h * d * esz);
+  l.o_swa = off;
+  off = align256(off + (size_t)s.tokens * h * d * esz);
+  l.lse = off;
+  off = align256(off + (size_t)s.tokens * h * 4);
+  l.scores = off;
+  off = align256(off + (size_t)s.tokens * hkv * l.nb_stride * 4);
+  l.idx = off;
+  off = align256(off + (size_t)s.tokens * hkv * S * 4);
+  l.total = off;
+  return l;
+}
+
+size_t nsa_layer_fwd_workspace_size(const nsa_shape* shape, int kernel, int stride, int block_size, int S) {
+  Seqs s;
+  if (make_seqs(shape, &s, __func__) != NSA_OK || kernel <= 0 || stride <= 0 || block_size <= 0 || S <= 0) return 0;
+  return layer_layout(s, shape->h, shape->h_kv, shape->d, shape->dtype == NSA_BF16 ? 2 : 4, kernel, stride,
+                      block_size, S)
+      .total;
+}
+
+nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                         const float* gate_logits, int kernel, int stride, int block_size, int S,
+                         int n_init, int n_local, int window, float scale, void* o, int32_t* idx_out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = dense_common(shape, &s, __func__)) return st;
+  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
+              "nsa_layer_fwd: supports kernel 32, stride 16, block_size 64");
+  NSA_REQUIRE(pow2_le16(shape->h / shape->h_kv), NSA_ERR_UNSUPPORTED,
+              "nsa_layer_fwd: h/h_kv must be 1, 2, 4, 8 or 16");
+  NSA_REQUIRE(S >= 1 && S <= 64, NSA_ERR_UNSUPPORTED, "nsa_layer_fwd: S must be in [1, 64]");
+  NSA_REQUIRE(window >= 1 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "nsa_layer_fwd: bad window/n_init/n_local");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(gate_logits);
+  NSA_PTR(o);
+  if (idx_out) NSA_PTR(idx_out);
+  const LayerLayout l = layer_layout(s, shape->h, shape->h_kv, shape->d, 2, kernel, stride, block_size, S);
+  NSA_REQUIRE(l.nb_stride <= 2048, NSA_ERR_UNSUPPORTED, "nsa_layer_fwd: sequences longer than 131072 tokens");
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_layer_fwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= l.total, NSA_ERR_INVALID, "nsa_layer_fwd: workspace %zu < %zu bytes",
+              workspace_bytes, l.total);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  void* kc = w + l.kc;
+  void* vc = w + l.vc;
+  void* o_cmp = w + l.o_cmp;
+  void* o_swa = w + l.o_swa;
+  float* lse = reinterpret_cast<float*>(w + l.lse);
+  float* scores = reinterpret_cast<float*>(w + l.scores);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + l.idx);
+  const int h = shape->h, hkv = shape->h_kv, d = shape->d;
+  cudaError_t e;
+  if ((e = launch_compress(s, k, kc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "nsa_layer_fwd/compress k");
+  if ((e = launch_compress(s, v, vc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "nsa_layer_fwd/compress v");
+  if ((e = launch_dense_attn(0, s, q, kc, vc, h, hkv, d, kernel, stride, 0, scale, o_cmp, lse, stream)))
+    return cuda_status(e, "nsa_layer_fwd/compressed branch");
+  if ((e = launch_scores_pool(s, q, kc, h, hkv, d, scale, lse, scores, l.nb_stride, stream)))
+    return cuda_status(e, "nsa_layer_fwd/block scores");
+  if ((e = launch_topk(s, scores, l.nb_stride, hkv, block_size, n_init, n_local, S, idx, stream)))
+    return cuda_status(e, "nsa_layer_fwd/top-k");
+  // the selected branch writes straight into o; the gated sum then runs in place
+  if ((e = launch_sparse_fwd(s, q, k, v, idx, S, block_size, h, hkv, d, kBF16, scale, o, nullptr, stream)))
+    return cuda_status(e, "nsa_layer_fwd/selected branch");
+  if ((e = launch_dense_attn(1, s, q, k, v, h, hkv, d, kernel, stride, window, scale, o_swa, nullptr, stream)))
+    return cuda_status(e, "nsa_layer_fwd/sliding branch");
+  return cuda_status(launch_gate_combine(s.tokens, h, d, o_cmp, o, o_swa, gate_logits, o, stream),
+                     "nsa_layer_fwd/gate combine");
+}
+
+}  // extern "C"

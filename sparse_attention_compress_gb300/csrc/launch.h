@@ -1,0 +1,60 @@
+// Internal launchers (host side) of the sm_103a kernels.  Arguments are validated by
+// the C ABI layer before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace nsa {
+
+enum DType { kF32 = 0, kBF16 = 1 };
+
+cudaError_t launch_compress(const Seqs& s, const void* k, void* k_cmp, int hkv, int d, int dtype,
+                            int kernel, int stride, cudaStream_t st);
+
+cudaError_t launch_scores_pool(const Seqs& s, const void* q, const void* k_cmp, int h, int hkv, int d,
+                               float scale, const float* lse_in, float* scores, int nb_stride,
+                               cudaStream_t st);
+
+cudaError_t launch_topk(const Seqs& s, const float* scores, int nb_stride, int hkv, int block_size,
+                        int n_init, int n_local, int k, int32_t* idx, cudaStream_t st);
+
+cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const void* v,
+                              const int32_t* idx, int S, int block_size, int h, int hkv, int d,
+                              int dtype, float scale, void* o, float* lse, cudaStream_t st);
+
+// mode 0: compressed-attention branch (keys/values are packed compressed rows)
+// mode 1: sliding-window branch
+cudaError_t launch_dense_attn(int mode, const Seqs& s, const void* q, const void* k, const void* v,
+                              int h, int hkv, int d, int kernel, int stride, int window, float scale,
+                              void* o, float* lse, cudaStream_t st);
+
+cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
+                                const void* o_swa, const float* gates, void* o, cudaStream_t st);
+
+struct DecodeArgs {
+  int batch, max_len, h, hkv, d, kernel, stride, block_size, n_init, n_local, k;
+  float scale;
+  const int32_t* seqlens;
+  const void *q, *k_cache, *v_cache, *kc_cache;
+  int32_t* idx;  // [batch, hkv, k]
+  void* o;
+  // scratch
+  float* z;        // [batch, hkv, r, nc_pad]
+  float* tile_ml;  // [batch, hkv, n_tiles, r, 2]
+  float* part_o;   // [batch, hkv * rtiles, n_split, 16, d]
+  float* part_ml;  // [batch, hkv * rtiles, n_split, 16, 2]
+  int n_split;
+};
+struct DecodeLayout {
+  size_t z, tile_ml, idx, part_o, part_ml, total;
+  int nc_pad, n_tiles, n_split;
+};
+DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int kernel, int stride,
+                           int block_size, int k);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace nsa

@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+entry point its header declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_compress_gb300 as nsa
+from sparse_attention_compress_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nsa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^NSA_API\s+[\w\s\*]+?\b(nsa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = nsa.load()
+    names = _declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib._SIGS), "binding and header disagree"
+
+
+def test_version_and_empty_error():
+    lib = nsa.load()
+    assert lib.nsa_version().startswith(b"nsa-gb300")
+
+
+def _shape(**kw):
+    s = _lib.NsaShape()
+    s.batch, s.seqlen, s.h, s.h_kv, s.d, s.dtype = 1, 128, 16, 1, 128, _lib.NSA_BF16
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)  # aligned, never dereferenced: every call below fails validation first
+MIS = P(0x10008)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"h": 0}, 1), ({"h": 15, "h_kv": 2}, 1), ({"dtype": 7}, 1), ({"batch": -1}, 1), ({"d": 96}, 2),
+])
+def test_sparse_fwd_rejects_bad_shapes(kw, expect):
+    lib = nsa.load()
+    s = _shape(**kw)
+    rc = lib.nsa_sparse_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, 16, 64, 0.0, FAKE, None, None)
+    assert rc == expect
+    assert lib.nsa_last_error()
+
+
+def test_null_and_misaligned_pointers():
+    lib = nsa.load()
+    s = _shape()
+    assert lib.nsa_sparse_fwd(ctypes.byref(s), None, FAKE, FAKE, FAKE, 16, 64, 0.0, FAKE, None, None) == 1
+    assert b"null" in lib.nsa_last_error()
+    assert lib.nsa_sparse_fwd(ctypes.byref(s), MIS, FAKE, FAKE, FAKE, 16, 64, 0.0, FAKE, None, None) == 1
+    assert b"aligned" in lib.nsa_last_error()
+    assert lib.nsa_sparse_fwd(None, FAKE, FAKE, FAKE, FAKE, 16, 64, 0.0, FAKE, None, None) == 1
+
+
+def test_unsupported_parameters():
+    lib = nsa.load()
+    s = _shape(h=16, h_kv=2)
+    assert lib.nsa_cmp_scores_pool(ctypes.byref(s), FAKE, FAKE, 32, 8, 64, 0.0, None, FAKE, 2, None) == 2
+    assert lib.nsa_cmp_scores_pool(ctypes.byref(s), FAKE, FAKE, 32, 16, 64, 0.0, None, FAKE, 1, None) == 1
+    assert lib.nsa_topk_select(ctypes.byref(s), FAKE, 2, 64, 1, 2, 65, FAKE, None) == 2
+    assert lib.nsa_topk_select(ctypes.byref(s), FAKE, 4096, 64, 1, 2, 16, FAKE, None) == 2
+    assert lib.nsa_compress_k(ctypes.byref(s), FAKE, FAKE, 40, 16, None) == 2
+    assert lib.nsa_sparse_decode(2, FAKE, 1024, 16, 2, 64, FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 1, 2, 64, 0.0,
+                                 None, FAKE, FAKE, 1 << 30, None) == 2
+    assert lib.nsa_swa_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, 0, 0.0, FAKE, None, None) == 1
+
+
+def test_decode_workspace_checks():
+    lib = nsa.load()
+    need = nsa.nsa_sparse_decode_workspace_size(32, 32768, 16, 2, 128, k=64)
+    assert need > 0
+    rc = lib.nsa_sparse_decode(32, FAKE, 32768, 16, 2, 128, FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 1, 2, 64, 0.0,
+                               None, FAKE, FAKE, need - 1, None)
+    assert rc == 1 and b"workspace" in lib.nsa_last_error()
+    rc = lib.nsa_sparse_decode(32, FAKE, 32768, 16, 2, 128, FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 1, 2, 64, 0.0,
+                               None, FAKE, P(0x10010), need, None)
+    assert rc == 1 and b"256-byte" in lib.nsa_last_error()
+
+
+def test_empty_inputs_are_no_ops():
+    lib = nsa.load()
+    s = _shape(batch=0)
+    assert lib.nsa_sparse_fwd(ctypes.byref(s), None, None, None, None, 16, 64, 0.0, None, None, None) == 0
+    assert lib.nsa_gate_combine(0, 16, 128, None, None, None, None, None, None) == 0
+
+
+def test_layer_workspace_size_scales_with_tokens():
+    s1 = _lib.make_shape(65536, 64, 4, 128, _lib.NSA_BF16, batch=1, seqlen=65536)
+    s2 = _lib.make_shape(32768, 64, 4, 128, _lib.NSA_BF16, batch=1, seqlen=32768)
+    a, b = nsa.nsa_layer_fwd_workspace_size(s1), nsa.nsa_layer_fwd_workspace_size(s2)
+    assert a > 1.9 * b > 0

@@ -1,0 +1,308 @@
+"""GPU parity: every kernel through the C ABI against the CPU oracle on the same
+seeded inputs.  Indices bit-exact (top-k on identical scores) or within the tie band
+(fused selection); outputs within |gpu - oracle| <= 1e-2 + 1e-2|oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_compress_gb300 as nsa
+from oracle import oracle as orc
+from sparse_attention_compress_gb300 import inputs as gen
+from tests.parity import as_f64, assert_close, dev, host, selection_mismatches
+
+pytestmark = pytest.mark.gpu
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _t_of_rows(cu):
+    cu = np.asarray(cu)
+    return np.concatenate([np.arange(cu[i + 1] - cu[i]) for i in range(len(cu) - 1)])
+
+
+# --------------------------------------------------------------------------- S1
+@pytest.mark.parametrize("dtype,hkv,d,kernel,stride", [
+    ("bf16", 2, 128, 32, 16), ("bf16", 4, 128, 32, 16), ("bf16", 1, 64, 16, 16), ("bf16", 2, 128, 64, 16),
+    ("f32", 1, 64, 32, 16)])
+def test_compress(dtype, hkv, d, kernel, stride):
+    lengths = [1, 31, 32, 100, 1000, 4097]
+    cu = gen.varlen_cu_seqlens(lengths)
+    k = gen.normal(_rng(1), (cu[-1], hkv, d), dtype)
+    exact, rounded = orc.compress(k, cu, kernel, stride)
+    out = nsa.nsa_compress_k(dev(k), kernel, stride, cu_seqlens=dev(cu), max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    g = host(out)
+    assert g.shape == rounded.shape
+    # the mean of bf16 inputs in fp32 rounds to the same bf16 as the exact mean except
+    # at a rounding tie boundary: allow one unit in the last place there
+    assert_close(out, exact, atol=1e-6, rtol=2 ** -7, what="compress")
+    same = np.mean(g == rounded)
+    assert same > 0.999, same
+
+
+def test_compress_dense_batch_layout():
+    B, T, hkv, d = 3, 1000, 2, 128
+    k = gen.normal(_rng(2), (B * T, hkv, d), "bf16")
+    _, rounded = orc.compress(k, gen.dense_cu_seqlens(B, T))
+    out = nsa.nsa_compress_k(dev(k).view(B, T, hkv, d))
+    torch.cuda.synchronize()
+    assert np.mean(host(out) == rounded) > 0.999
+
+
+# --------------------------------------------------------------------------- S2+S3
+@pytest.mark.parametrize("H,hkv,d", [(16, 2, 128), (16, 1, 128), (8, 2, 64), (4, 4, 128), (8, 4, 128)])
+def test_cmp_scores_pool(H, hkv, d):
+    lengths = [40, 700, 3001, 64]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(3)
+    q = gen.normal(rng, (cu[-1], H, d), "bf16")
+    k = gen.normal(rng, (cu[-1], hkv, d), "bf16")
+    _, kc = orc.compress(k, cu)
+    nb = -(-max(lengths) // 64) + 3
+    ref = orc.cmp_scores_pool(q, kc, cu, nb_stride=nb)
+    out = nsa.nsa_cmp_scores_pool(dev(q), dev(kc), hkv, cu_seqlens=dev(cu), max_seqlen=max(lengths), nb_stride=nb)
+    torch.cuda.synchronize()
+    g = host(out).astype(np.float64)
+    assert np.all(g[ref == 0] == 0)
+    np.testing.assert_allclose(g, ref, rtol=1e-4, atol=1e-9)
+
+
+def test_cmp_scores_pool_with_given_normaliser():
+    lengths = [1200, 333]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(4)
+    H, hkv, d = 16, 1, 128
+    q, k, v = (gen.normal(rng, (cu[-1], hh, d), "bf16") for hh in (H, hkv, hkv))
+    _, kc = orc.compress(k, cu)
+    _, vc = orc.compress(v, cu)
+    dcu = dev(cu)
+    lse = torch.empty((cu[-1], H), dtype=torch.float32, device="cuda")
+    nsa.nsa_cmp_attn_fwd(dev(q), dev(kc), dev(vc), hkv, cu_seqlens=dcu, max_seqlen=1200, lse=lse)
+    a = nsa.nsa_cmp_scores_pool(dev(q), dev(kc), hkv, cu_seqlens=dcu, max_seqlen=1200, lse_in=lse)
+    b = nsa.nsa_cmp_scores_pool(dev(q), dev(kc), hkv, cu_seqlens=dcu, max_seqlen=1200)
+    torch.cuda.synchronize()
+    ref = orc.cmp_scores_pool(q, kc, cu)
+    np.testing.assert_allclose(host(a), ref, rtol=1e-4, atol=1e-9)
+    np.testing.assert_allclose(host(b), ref, rtol=1e-4, atol=1e-9)
+
+
+# --------------------------------------------------------------------------- S4
+@pytest.mark.parametrize("nb_stride,k,n_init,n_local,levels", [
+    (40, 16, 1, 2, 0), (40, 16, 1, 2, 3), (129, 7, 0, 0, 5), (512, 64, 1, 2, 0), (1024, 16, 2, 1, 4),
+    (2048, 64, 1, 2, 0), (3, 1, 1, 2, 0), (64, 64, 0, 0, 2)])
+def test_topk_bit_exact(nb_stride, k, n_init, n_local, levels):
+    bs = 64
+    max_len = nb_stride * bs
+    lengths = [max_len, max(1, max_len // 3), 77]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(5 + k)
+    sc = rng.random((cu[-1], 2, nb_stride), dtype=np.float32)
+    if levels:
+        sc = np.floor(sc * levels).astype(np.float32) / levels  # exact ties
+    ref = orc.topk(sc, cu, bs, n_init, n_local, k)
+    out = nsa.nsa_topk_select(dev(sc), k, bs, n_init, n_local, cu_seqlens=dev(cu), max_seqlen=max_len)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(out), ref)
+
+
+# --------------------------------------------------------------------------- S5
+def test_sparse_fwd_tiny_fp32():
+    w = gen.tiny()
+    ref, lse_ref = orc.sparse_attn(w.q, w.k, w.v, w.idx, w.cu_seqlens, w.block_size)
+    lse = torch.empty((w.tokens, w.h), dtype=torch.float32, device="cuda")
+    out = nsa.nsa_sparse_fwd(dev(w.q).view(1, 256, 4, 64), dev(w.k), dev(w.v), dev(w.idx), w.block_size, lse=lse)
+    torch.cuda.synchronize()
+    err = assert_close(out.reshape(w.tokens, w.h, w.d), ref, what="tiny fp32")
+    assert err < 1e-5
+    assert_close(lse, lse_ref, atol=1e-5, rtol=1e-5, what="tiny lse")
+
+
+@pytest.mark.parametrize("H,hkv,d,bs,S", [(16, 1, 128, 64, 16), (16, 2, 128, 64, 8), (8, 1, 64, 32, 6),
+                                          (32, 1, 128, 64, 5), (4, 2, 128, 16, 9), (12, 1, 128, 64, 16)])
+def test_sparse_fwd_bf16_varlen(H, hkv, d, bs, S):
+    lengths = [1, 63, 64, 65, 900, 2000]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(6)
+    q, k, v = (gen.normal(rng, (cu[-1], hh, d), "bf16") for hh in (H, hkv, hkv))
+    idx = gen.random_block_indices(rng, cu, hkv, S, bs, force_first=True)
+    ref, lse_ref = orc.sparse_attn(q, k, v, idx, cu, bs)
+    lse = torch.empty((cu[-1], H), dtype=torch.float32, device="cuda")
+    out = nsa.nsa_sparse_fwd(dev(q), dev(k), dev(v), dev(idx), bs, cu_seqlens=dev(cu), max_seqlen=max(lengths),
+                             lse=lse)
+    torch.cuda.synchronize()
+    assert_close(out, ref, what="sparse bf16")
+    assert_close(lse, lse_ref, atol=1e-3, rtol=1e-3, what="sparse lse")
+
+
+def test_sparse_fwd_edge_lists():
+    """-1 padding, non-causal entries, duplicates and empty lists."""
+    T, H, hkv, d, bs = 300, 16, 1, 128, 64
+    cu = gen.dense_cu_seqlens(1, T)
+    rng = _rng(7)
+    q, k, v = (gen.normal(rng, (T, hh, d), "bf16") for hh in (H, hkv, hkv))
+    t = np.arange(T)
+    idx = np.stack([t // bs, np.full(T, -1), np.full(T, 3), np.zeros(T), np.zeros(T)], 1).astype(np.int32)
+    idx[:10] = -1  # empty lists -> zero output
+    idx = idx[:, None, :]
+    ref, _ = orc.sparse_attn(q, k, v, idx, cu, bs)
+    out = nsa.nsa_sparse_fwd(dev(q), dev(k), dev(v), dev(idx), bs)
+    torch.cuda.synchronize()
+    assert_close(out, ref, what="edge lists")
+    assert np.all(as_f64(host(out))[:10] == 0)
+
+
+def test_sparse_fwd_prefill_full_size_sampled():
+    """B=8, T=16384, H=16, Hkv=1, d=128, block 64, S=16 (the benchmark launch);
+    oracle on sampled rows, including first/last tokens of every sequence."""
+    w = gen.prefill()
+    out = nsa.nsa_sparse_fwd(dev(w.q).view(8, 16384, 16, 128), dev(w.k), dev(w.v), dev(w.idx), 64)
+    torch.cuda.synchronize()
+    rng = _rng(8)
+    rows = np.unique(np.concatenate([rng.integers(0, w.tokens, 400), np.arange(8) * 16384,
+                                     np.arange(1, 9) * 16384 - 1, [63, 64, 65, 16383 + 64]]))
+    ref, _ = orc.sparse_attn(w.q, w.k, w.v, w.idx, w.cu_seqlens, 64, rows=rows)
+    g = out.reshape(w.tokens, 16, 128)[torch.from_numpy(rows).cuda()]
+    assert_close(g, ref, what="prefill sampled")
+
+
+# --------------------------------------------------------------------------- S7, S8, S9
+@pytest.mark.parametrize("H,hkv,d", [(16, 1, 128), (32, 2, 128), (8, 1, 64), (16, 4, 128), (64, 1, 128)])
+def test_cmp_attn(H, hkv, d):
+    lengths = [10, 31, 32, 47, 500, 1777]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(9)
+    q, k, v = (gen.normal(rng, (cu[-1], hh, d), "bf16") for hh in (H, hkv, hkv))
+    _, kc = orc.compress(k, cu)
+    _, vc = orc.compress(v, cu)
+    ref, lse_ref = orc.cmp_attn(q, kc, vc, cu)
+    lse = torch.empty((cu[-1], H), dtype=torch.float32, device="cuda")
+    out = nsa.nsa_cmp_attn_fwd(dev(q), dev(kc), dev(vc), hkv, cu_seqlens=dev(cu), max_seqlen=max(lengths), lse=lse)
+    torch.cuda.synchronize()
+    assert_close(out, ref, what="cmp attn")
+    l = host(lse)
+    assert np.array_equal(np.isneginf(l), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(l[fin], lse_ref[fin], atol=1e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("window,H,hkv", [(512, 16, 1), (1, 16, 2), (100, 8, 1), (5000, 16, 1), (64, 64, 4)])
+def test_swa(window, H, hkv):
+    lengths = [3, 600, 2100]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(10)
+    d = 128
+    q, k, v = (gen.normal(rng, (cu[-1], hh, d), "bf16") for hh in (H, hkv, hkv))
+    ref, _ = orc.swa(q, k, v, cu, window=window)
+    out = nsa.nsa_swa_fwd(dev(q), dev(k), dev(v), window, cu_seqlens=dev(cu), max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    assert_close(out, ref, what="swa")
+
+
+def test_gate_combine():
+    rng = _rng(11)
+    n, h, d = 1000, 16, 128
+    a, b, c = (gen.normal(rng, (n, h, d), "bf16") for _ in range(3))
+    gates = rng.standard_normal((n, h, 3), dtype=np.float32)
+    gates[:5] = [[40.0, -40.0, -40.0]]
+    ref = orc.gate_combine(as_f64(a), as_f64(b), as_f64(c), gates)
+    out = nsa.nsa_gate_combine(dev(a), dev(b), dev(c), dev(gates))
+    torch.cuda.synchronize()
+    assert_close(out, ref, what="gate")
+
+
+# --------------------------------------------------------------------------- S6
+def _decode_case(B, L, seqlens, k, seed):
+    w = gen.decode(B=B, L=L, seqlens=seqlens, topk=k)
+    ncs = orc.num_cmp(L)
+    kc_cache = np.zeros((B, ncs, w.hkv, w.d), np.uint16)
+    for b in range(B):
+        kc_cache[b] = orc.compress(w.k_cache[b], [0, L])[1]
+    return w, kc_cache
+
+
+@pytest.mark.parametrize("B,L,seqlens,k", [(4, 4096, [4096, 2500, 70, 1], 64), (3, 2048, [2048, 2047, 1000], 16),
+                                           (2, 300, [300, 33], 64)])
+def test_decode(B, L, seqlens, k):
+    w, kc_cache = _decode_case(B, L, seqlens, k, 0)
+    ref_idx, _, ref_sc = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, want_scores=True)
+    idx = torch.empty((B, w.hkv, k), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode(dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(kc_cache), dev(w.seqlens), k=k,
+                                idx_out=idx)
+    torch.cuda.synchronize()
+    gi = host(idx)
+    n_mis, outside = selection_mismatches(gi, ref_idx, ref_sc, np.asarray(w.seqlens) - 1)
+    assert outside == 0, (n_mis, outside)
+    # attention over the GPU's own choice
+    _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, idx_in=gi)
+    assert_close(out, ref_o, what="decode")
+
+
+def test_decode_full_size():
+    """B=32, context 32768, H=16, Hkv=2, d=128, top-k 64: all rows."""
+    w = gen.decode()
+    kc = nsa.nsa_compress_k(dev(w.k_cache))  # [B*n_c, Hkv, d]
+    kc_cache = kc.view(32, orc.num_cmp(32768), 2, 128)
+    idx = torch.empty((32, 2, 64), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode(dev(w.q), dev(w.k_cache), dev(w.v_cache), kc_cache, dev(w.seqlens), k=64,
+                                idx_out=idx)
+    torch.cuda.synchronize()
+    kch = host(kc_cache)
+    ref_idx, _, ref_sc = orc.decode(w.q, w.k_cache, w.v_cache, kch, w.seqlens, k=64, want_scores=True)
+    gi = host(idx)
+    n_mis, outside = selection_mismatches(gi, ref_idx, ref_sc, np.asarray(w.seqlens) - 1)
+    assert outside == 0, (n_mis, outside)
+    _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kch, w.seqlens, k=64, idx_in=gi)
+    assert_close(out, ref_o, what="decode full")
+
+
+# --------------------------------------------------------------------------- fused selection and the layer
+def test_selection_varlen_end_to_end():
+    """compress -> scores -> top-k at reduced size of the varlen selection workload."""
+    w = gen.selection(n_seqs=3, lo=1000, hi=3000)
+    dcu = dev(w.cu_seqlens)
+    kc = nsa.nsa_compress_k(dev(w.k), cu_seqlens=dcu, max_seqlen=w.max_len)
+    sc = nsa.nsa_cmp_scores_pool(dev(w.q), kc, w.hkv, cu_seqlens=dcu, max_seqlen=w.max_len)
+    idx = nsa.nsa_topk_select(sc, 16, cu_seqlens=dcu, max_seqlen=w.max_len)
+    torch.cuda.synchronize()
+    kch = host(kc)
+    ref_sc = orc.cmp_scores_pool(w.q, kch, w.cu_seqlens)
+    ref_idx = orc.topk(ref_sc, w.cu_seqlens, k=16)
+    n_mis, outside = selection_mismatches(host(idx), ref_idx, ref_sc, _t_of_rows(w.cu_seqlens))
+    assert outside == 0
+    assert n_mis <= max(3, ref_idx.shape[0] * ref_idx.shape[1] // 200), n_mis
+    # top-k on the GPU's own scores is bit-exact with the oracle's top-k of those scores
+    assert np.array_equal(host(idx), orc.topk(host(sc), w.cu_seqlens, k=16))
+
+
+@pytest.mark.parametrize("T,H,hkv", [(1500, 32, 2), (700, 16, 1)])
+def test_layer_small(T, H, hkv):
+    w = gen.layer(T=T, H=H, HKV=hkv)
+    idx = torch.empty((T, hkv, 16), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_layer_fwd(dev(w.q), dev(w.k), dev(w.v), dev(w.gates), idx_out=idx)
+    torch.cuda.synchronize()
+    gi = host(idx)
+    ref = orc.layer(w.q, w.k, w.v, w.gates, w.cu_seqlens, idx_in=gi)
+    _, kc = orc.compress(w.k, w.cu_seqlens)
+    ref_sc = orc.cmp_scores_pool(w.q, kc, w.cu_seqlens)
+    n_mis, outside = selection_mismatches(gi, ref["idx"], ref_sc, _t_of_rows(w.cu_seqlens))
+    assert outside == 0, (n_mis, outside)
+    assert_close(out, ref["o"], what="layer")
+
+
+def test_layer_full_size_sampled():
+    """B=1, T=65536, H=64, Hkv=4, d=128: the three-branch layer, oracle on sampled rows."""
+    w = gen.layer()
+    idx = torch.empty((w.tokens, 4, 16), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_layer_fwd(dev(w.q), dev(w.k), dev(w.v), dev(w.gates), idx_out=idx)
+    torch.cuda.synchronize()
+    gi = host(idx)
+    rows = np.unique(np.concatenate([_rng(12).integers(0, w.tokens, 24), [0, 31, 32, 511, 512, 65535]]))
+    ref = orc.layer(w.q, w.k, w.v, w.gates, w.cu_seqlens, idx_in=gi, rows=rows)
+    assert_close(out[torch.from_numpy(rows).cuda()], ref["o"], what="layer full")
+    _, kc = orc.compress(w.k, w.cu_seqlens)
+    ref_sc = orc.cmp_scores_pool(w.q, kc, w.cu_seqlens, rows=rows)
+    n_mis, outside = selection_mismatches(gi[rows], ref["idx"], ref_sc, rows)
+    assert outside == 0, (n_mis, outside)
