@@ -164,8 +164,8 @@ def run_reference(args):
     from oracle import oracle as orc
     orc.build()
     w = gen.prefill()
-    _, dt, _, _ = oracle_prefill_sample(w, 32, seed=99)
-    n_rows = int(min(4096, max(32, 32 * 2.5 / max(dt, 1e-3))))  # ~2.5 s per step
+    _, dt, _, _ = oracle_prefill_sample(w, 512, seed=99)
+    n_rows = int(min(w.tokens, max(512, 512 * 2.5 / max(dt, 1e-3))))  # ~2.5 s per step
     for s in range(args.warmup):
         oracle_prefill_sample(w, n_rows, seed=1000 + s)
     vals, times = [], []
@@ -293,6 +293,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
+    ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
+    ap.add_argument("--only", default="", choices=["", "prefill", "decode", "selection", "layer"],
+                    help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -313,17 +316,24 @@ def main():
         barrier = dist.barrier
     nsa.load()
     peaks = load_peaks()
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
 
-    w = gen.prefill()
+    def flush():
+        flush_buf.zero_()
+
+    if args.only in ("decode", "selection", "layer"):
+        fn = {"decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
+              "layer": lambda: bench_layer(torch, nsa, device, args.steps, args.warmup, flush)}[args.only]
+        print(json.dumps({"only": args.only, **fn()}), flush=True)
+        return
+
+    w = gen.prefill(B=args.batch)
     flops = prefill_flops(w)
     q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
     idx = dev(torch, w.idx, device)
     out = torch.empty_like(q)
     qv = q.view(w.batch, w.seqlen, w.h, w.d)
-    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
-
-    def flush():
-        flush_buf.zero_()
 
     def step():
         nsa.nsa_sparse_fwd(qv, k, v, idx, w.block_size, out=out)
@@ -340,6 +350,10 @@ def main():
         ms_step = float(tt.item())
     value = flops * world / (ms_step * 1e-3) / 1e12
     kernel_tflops = flops / (ms_step * 1e-3) / 1e12
+    if args.only == "prefill":
+        print(json.dumps({"only": "prefill", "batch": w.batch, "ms_per_step": ms_step, "tflops": kernel_tflops}),
+              flush=True)
+        return
 
     # end to end through the public call with host buffers: inputs in, output out
     hq, hk, hv, hi = pinned(torch, w.q), pinned(torch, w.k), pinned(torch, w.v), pinned(torch, w.idx)
@@ -364,7 +378,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "prefill B=8 T=16384 H=16 Hkv=1 d=128 bf16, block 64, S=16 random causal blocks "
-                               "(block 0 and own block always listed)", "global_batch": 8 * world,
+                               "(block 0 and own block always listed)", "global_batch": w.batch * world,
                    "seq_len": 16384, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MB write outside the event pair)",
                    "flops_per_step": flops},
@@ -401,9 +415,9 @@ def main():
 
     if rank == 0 and world == 1:
         n_rows = args.cpu_sample_rows
-        if n_rows <= 0:
-            _, dt, _, _ = oracle_prefill_sample(w, 16, seed=7)
-            n_rows = int(min(8192, max(16, 16 * 15.0 / max(dt, 1e-3))))
+        if n_rows <= 0:  # size the sample to ~15 s of oracle work
+            _, dt, _, _ = oracle_prefill_sample(w, 512, seed=7)
+            n_rows = int(min(w.tokens, max(512, 512 * 15.0 / max(dt, 1e-3))))
         val, dt, _, thr = oracle_prefill_sample(w, n_rows, seed=11)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                                 "sample": f"{n_rows} random query tokens (all heads) of the prefill workload, "

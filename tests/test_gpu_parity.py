@@ -39,8 +39,9 @@ def test_compress(dtype, hkv, d, kernel, stride):
     # the mean of bf16 inputs in fp32 rounds to the same bf16 as the exact mean except
     # at a rounding tie boundary: allow one unit in the last place there
     assert_close(out, exact, atol=1e-6, rtol=2 ** -7, what="compress")
-    same = np.mean(g == rounded)
-    assert same > 0.999, same
+    if dtype == "bf16":
+        same = np.mean(g == rounded)
+        assert same > 0.999, same
 
 
 def test_compress_dense_batch_layout():
