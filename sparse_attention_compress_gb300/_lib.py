@@ -13,7 +13,8 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libnsa.so")
+# NSA_LIBRARY may point at another build of the same library (e.g. with other tuning flags)
+LIB_PATH = os.environ.get("NSA_LIBRARY") or os.path.join(_PKG, "libnsa.so")
 
 NSA_F32, NSA_BF16 = 0, 1
 _c_int, _c_i64, _c_p, _c_f, _c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t

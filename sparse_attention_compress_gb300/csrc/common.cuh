@@ -159,6 +159,25 @@ __device__ __forceinline__ void qk_16keys(float (*s)[4], const uint32_t (*qa)[4]
   }
 }
 
+// Same product with the k-steps split over two accumulators (even / odd k-steps), so
+// four independent mma chains are in flight instead of two; the caller adds them.
+template <int D>
+__device__ __forceinline__ void qk_16keys_2acc(float (*s)[4], float (*s2)[4], const uint32_t (*qa)[4],
+                                               uint32_t kbase, int key0, int lane) {
+  const int key = key0 + (lane & 7) + ((lane >> 4) << 3);
+  const int csel = (lane >> 3) & 1;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; kk += 2) {
+    uint32_t b[4], c[4];
+    ldsm_x4(b, tile_addr<D>(kbase, key, 2 * kk + csel));
+    ldsm_x4(c, tile_addr<D>(kbase, key, 2 * kk + 2 + csel));
+    mma_bf16(s[0], qa[kk], b[0], b[1]);
+    mma_bf16(s[1], qa[kk], b[2], b[3]);
+    mma_bf16(s2[0], qa[kk + 1], c[0], c[1]);
+    mma_bf16(s2[1], qa[kk + 1], c[2], c[3]);
+  }
+}
+
 // O[16 x D] += P[16 x 16 keys] * V_tile[key0 .. key0+15] from a swizzled tile.
 // pa is the A fragment of P (bf16).  o[nt] is the C fragment of d-columns nt*8..nt*8+7.
 template <int D>

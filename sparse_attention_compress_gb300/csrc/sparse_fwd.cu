@@ -35,8 +35,20 @@ struct SparseParams {
   float* part_ml;
 };
 
+#ifndef NSA_PREFILL_NSTAGE
+#define NSA_PREFILL_NSTAGE 2
+#endif
+#ifndef NSA_PREFILL_MINBLOCKS
+#define NSA_PREFILL_MINBLOCKS 3
+#endif
+
+// Softmax state is rescaled lazily: the running max m only moves when a new score
+// exceeds it by more than 2^kLazy in base 2, so exponentials stay below 2^kLazy and
+// almost no iteration pays the O rescale (the final normalisation is unchanged).
+constexpr float kLazy = 8.f;
+
 template <int D, int BS, int NSTAGE, bool DECODE>
-__global__ void __launch_bounds__(128) sparse_fwd_mma(const SparseParams p) {
+__global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(const SparseParams p) {
   constexpr int NW = 4;
   constexpr int NSLICE = BS / 16;
   constexpr int NGROUP = NW / NSLICE;
@@ -96,12 +108,16 @@ __global__ void __launch_bounds__(128) sparse_fwd_mma(const SparseParams p) {
     const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
     const __nv_bfloat16* kb = p.k + ((kv_base + key0) * p.hkv + g) * D;
     const __nv_bfloat16* vb = p.v + ((kv_base + key0) * p.hkv + g) * D;
-    load_tile_async<D, 16, 32>(sb, lane, p.k, [&](int row) -> const __nv_bfloat16* {
-      return key0 + row <= t ? kb + row * row_stride : nullptr;
-    });
-    load_tile_async<D, 16, 32>(sb + SLICE_BYTES, lane, p.v, [&](int row) -> const __nv_bfloat16* {
-      return key0 + row <= t ? vb + row * row_stride : nullptr;
-    });
+    const bool full = key0 + 15 <= t;
+    constexpr int CH = D / 8;
+#pragma unroll
+    for (int c = lane; c < 16 * CH; c += 32) {
+      const int row = c / CH, ch = c % CH;
+      const bool ok = full || key0 + row <= t;
+      const int64_t off = row * row_stride + ch * 8;
+      cp_async16(tile_addr<D>(sb, row, ch), ok ? kb + off : p.k, ok ? 16 : 0);
+      cp_async16(tile_addr<D>(sb + SLICE_BYTES, row, ch), ok ? vb + off : p.v, ok ? 16 : 0);
+    }
   };
 
   float o[D / 8][4];
@@ -121,22 +137,41 @@ __global__ void __launch_bounds__(128) sparse_fwd_mma(const SparseParams p) {
     __syncwarp();
     const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    qk_16keys<D>(s, qa, sb, 0, lane);
+    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    qk_16keys_2acc<D>(s, s2, qa, sb, 0, lane);
     const int64_t key0 = (int64_t)s_list[warp][i] * BS + slice * 16;
+    if (key0 + 15 <= t) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t key = key0 + nt * 8 + (lane & 3) * 2 + (j & 1);
-        s[nt][j] = key <= t ? s[nt][j] * p.scale_log2 : kNegInf;
-      }
+        for (int j = 0; j < 4; ++j) s[nt][j] = (s[nt][j] + s2[nt][j]) * p.scale_log2;
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t key = key0 + nt * 8 + (lane & 3) * 2 + (j & 1);
+          s[nt][j] = key <= t ? (s[nt][j] + s2[nt][j]) * p.scale_log2 : kNegInf;
+        }
+    }
     const float mx0 = quad_max(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
     const float mx1 = quad_max(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
-    const float a0 = ex2(m0 - mu0), a1 = ex2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
+    if (!__all_sync(0xffffffffu, mx0 <= m0 + kLazy && mx1 <= m1 + kLazy)) {
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float a0 = ex2(m0 - (mn0 == kNegInf ? 0.f : mn0)), a1 = ex2(m1 - (mn1 == kNegInf ? 0.f : mn1));
+      m0 = mn0;
+      m1 = mn1;
+      l0 *= a0;
+      l1 *= a1;
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt) {
+        o[nt][0] *= a0;
+        o[nt][1] *= a0;
+        o[nt][2] *= a1;
+        o[nt][3] *= a1;
+      }
+    }
+    const float mu0 = m0 == kNegInf ? 0.f : m0, mu1 = m1 == kNegInf ? 0.f : m1;
     float pr[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -145,15 +180,8 @@ __global__ void __launch_bounds__(128) sparse_fwd_mma(const SparseParams p) {
       pr[nt][2] = ex2(s[nt][2] - mu1);
       pr[nt][3] = ex2(s[nt][3] - mu1);
     }
-    l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      o[nt][0] *= a0;
-      o[nt][1] *= a0;
-      o[nt][2] *= a1;
-      o[nt][3] *= a1;
-    }
+    l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
     const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
                             pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
     pv_16keys<D>(o, pa, sb + SLICE_BYTES, 0, lane);
@@ -378,13 +406,15 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   const int r = h / hkv;
   dim3 grid((unsigned)s.tokens, hkv * ((r + 15) / 16), 1);
   if (d == 128) {
-    if (block_size == 64) return run_mma<128, 64, 3, false>(p, grid, st);
-    if (block_size == 32) return run_mma<128, 32, 3, false>(p, grid, st);
-    return run_mma<128, 16, 3, false>(p, grid, st);
+    constexpr int NS = NSA_PREFILL_NSTAGE;
+    if (block_size == 64) return run_mma<128, 64, NS, false>(p, grid, st);
+    if (block_size == 32) return run_mma<128, 32, NS, false>(p, grid, st);
+    return run_mma<128, 16, NS, false>(p, grid, st);
   }
-  if (block_size == 64) return run_mma<64, 64, 3, false>(p, grid, st);
-  if (block_size == 32) return run_mma<64, 32, 3, false>(p, grid, st);
-  return run_mma<64, 16, 3, false>(p, grid, st);
+  constexpr int NS = NSA_PREFILL_NSTAGE;
+  if (block_size == 64) return run_mma<64, 64, NS, false>(p, grid, st);
+  if (block_size == 32) return run_mma<64, 32, NS, false>(p, grid, st);
+  return run_mma<64, 16, NS, false>(p, grid, st);
 }
 
 // Decode attention over the chosen blocks, split over the list, then merged.
