@@ -177,6 +177,29 @@ NSA_API nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_
                              int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Allocation-free variant of nsa_sparse_decode, for callers that cannot allocate device
+ * memory when they run a decode step (code inside an allocator or memory-pool callback,
+ * runtimes that pre-reserve all device memory, plug-ins handed only their input and
+ * output buffers).  The pages have no counterpart: this is an interface convenience.
+ * Same arguments, kernels and results as nsa_sparse_decode, without the workspace: the
+ * scratch is a fixed array of nsa_sparse_decode_noalloc_max_bytes() bytes (16 MiB) in
+ * device memory that the library owns; every GPU that loads the library holds it until
+ * the process exits.  The caller still passes inputs and outputs.
+ *   - Steps whose nsa_sparse_decode_workspace_size() exceeds the fixed size are rejected
+ *     with NSA_ERR_UNSUPPORTED and a message naming both sizes.
+ *   - The first call on a device looks up the array's device address (a CUDA runtime
+ *     symbol query, no allocation); make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents; every byte a
+ *     call reads is written earlier in the same call, so nothing needs clearing.  Calls
+ *     that overlap on the GPU (other streams, other host threads) race on it: order them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+NSA_API size_t nsa_sparse_decode_noalloc_max_bytes(void);
+NSA_API nsa_status nsa_sparse_decode_noalloc(int batch, const int32_t* seqlens, int max_len, int h, int h_kv,
+                                             int d, const void* q, const void* k_cache, const void* v_cache,
+                                             const void* k_cmp_cache, int kernel, int stride, int block_size,
+                                             int n_init, int n_local, int k, float scale, int32_t* idx_out,
+                                             void* o, cudaStream_t stream);
+
 /* Full three-branch layer forward ([NSA-Triton] sec. 1.1): compress K and V (S1), the
  * compressed branch (S7, which also yields the normaliser reused by the selection),
  * block scores from the same compressed probabilities (S2, S3), top-S selection (S4),

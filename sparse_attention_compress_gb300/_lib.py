@@ -39,6 +39,9 @@ _SIGS = {
     "nsa_sparse_decode_workspace_size": ([_c_int] * 9, _c_sz),
     "nsa_sparse_decode": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
+    "nsa_sparse_decode_noalloc_max_bytes": ([], _c_sz),
+    "nsa_sparse_decode_noalloc": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int,
+                                   _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_layer_fwd_workspace_size": ([_c_p, _c_int, _c_int, _c_int, _c_int], _c_sz),
     "nsa_layer_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
                        _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
@@ -244,6 +247,20 @@ def nsa_sparse_decode(q, k_cache, v_cache, k_cmp_cache, seqlens, k=64, kernel=32
                                     _ptr(k_cmp_cache), kernel, stride, block_size, n_init, n_local, k, float(scale),
                                     _ptr(idx_out), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
            "nsa_sparse_decode")
+    return out
+
+
+def nsa_sparse_decode_noalloc(q, k_cache, v_cache, k_cmp_cache, seqlens, k=64, kernel=32, stride=16,
+                              block_size=64, n_init=1, n_local=2, scale=0.0, *, idx_out=None, out=None, stream=None):
+    """S6 without a workspace: the scratch is the library's fixed device array (see nsa.h)."""
+    B, h, d = q.shape
+    max_len, h_kv = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load().nsa_sparse_decode_noalloc(B, _ptr(seqlens), max_len, h, h_kv, d, _ptr(q), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(k_cmp_cache), kernel, stride, block_size, n_init,
+                                            n_local, k, float(scale), _ptr(idx_out), _ptr(out), _stream(stream)),
+           "nsa_sparse_decode_noalloc")
     return out
 
 

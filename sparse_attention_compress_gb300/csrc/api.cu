@@ -75,6 +75,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
+void nsa::set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
 extern "C" {
 
 const char* nsa_version(void) { return "nsa-gb300 0.1 (sm_103a)"; }

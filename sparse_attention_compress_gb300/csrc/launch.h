@@ -12,6 +12,9 @@ namespace nsa {
 
 enum DType { kF32 = 0, kBF16 = 1 };
 
+// Record the message returned by nsa_last_error() for the calling thread.
+void set_error(const char* fmt, ...);
+
 cudaError_t launch_compress(const Seqs& s, const void* k, void* k_cmp, int hkv, int d, int dtype,
                             int kernel, int stride, cudaStream_t st);
 

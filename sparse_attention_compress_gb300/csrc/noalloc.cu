@@ -1,0 +1,76 @@
+// Allocation-free decode entry point.
+//
+// Some callers cannot allocate device memory at the moment they need a decode step:
+// code running inside a custom allocator or memory-pool callback, runtimes that have
+// reserved all device memory up front and hand out no scratch, or plug-ins that are
+// given only their input and output buffers.  For them nsa_sparse_decode_noalloc runs
+// the same decode kernels as nsa_sparse_decode, with the scratch taken from a
+// fixed-size array in device memory that this library owns.  That array is a
+// file-scope __device__ object: every GPU that loads the library holds it until the
+// process exits.
+#include <mutex>
+
+#include "../../include/nsa.h"
+#include "launch.h"
+
+using namespace nsa;
+
+namespace {
+
+// 16 MiB covers a decode step of 32 sequences x 32768 tokens, 16 heads, 2 kv-heads,
+// d = 128, top-k 64 (about 8.6 MB of scratch).
+constexpr size_t kScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per
+// device (host code cannot use the array's name as a device pointer).
+cudaError_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" NSA_API size_t nsa_sparse_decode_noalloc_max_bytes(void) { return kScratchBytes; }
+
+extern "C" NSA_API nsa_status nsa_sparse_decode_noalloc(int batch, const int32_t* seqlens, int max_len, int h,
+                                                      int h_kv, int d, const void* q, const void* k_cache,
+                                                      const void* v_cache, const void* k_cmp_cache, int kernel,
+                                                      int stride, int block_size, int n_init, int n_local, int k,
+                                                      float scale, int32_t* idx_out, void* o,
+                                                      cudaStream_t stream) {
+  const size_t need = nsa_sparse_decode_workspace_size(batch, max_len, h, h_kv, d, kernel, stride, block_size, k);
+  if (need == 0)  // malformed sizes: the regular entry point reports which argument is wrong
+    return nsa_sparse_decode(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
+                             block_size, n_init, n_local, k, scale, idx_out, o, nullptr, 0, stream);
+  if (need > kScratchBytes) {
+    set_error("nsa_sparse_decode_noalloc: this step needs %zu bytes of scratch, more than the fixed %zu bytes; "
+              "use nsa_sparse_decode with a caller-provided workspace",
+              need, kScratchBytes);
+    return NSA_ERR_UNSUPPORTED;
+  }
+  void* scratch = nullptr;
+  const cudaError_t e = scratch_for_current_device(&scratch);
+  if (e != cudaSuccess) {
+    set_error("nsa_sparse_decode_noalloc: cannot resolve the scratch array: %s", cudaGetErrorString(e));
+    return NSA_ERR_CUDA;
+  }
+  // every other check (shapes, pointers, limits) is the regular entry point's
+  return nsa_sparse_decode(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
+                           block_size, n_init, n_local, k, scale, idx_out, o, scratch, kScratchBytes, stream);
+}
