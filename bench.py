@@ -30,6 +30,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from sparse_attention_compress_gb300 import inputs as gen  # noqa: E402
+from sparse_attention_compress_gb300.dist import max_over_ranks  # noqa: E402
 
 METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roofline"
 L2_BYTES = 129 * 2 ** 20
@@ -328,7 +329,7 @@ def main():
         print(json.dumps({"only": args.only, **fn()}), flush=True)
         return
 
-    w = gen.prefill(B=args.batch)
+    w = gen.prefill(B=args.batch, salt=rank)  # every rank processes its own batch
     flops = prefill_flops(w)
     q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
     idx = dev(torch, w.idx, device)
@@ -343,11 +344,7 @@ def main():
     ms = timed(torch, step, args.steps, args.warmup, flush, barrier)
     clk = clocks.stop()
     ms_step = float(np.mean(ms))
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(ms_step, device)
     value = flops * world / (ms_step * 1e-3) / 1e12
     kernel_tflops = flops / (ms_step * 1e-3) / 1e12
     if args.only == "prefill":

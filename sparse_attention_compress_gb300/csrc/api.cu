@@ -300,6 +300,8 @@ nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int
   a.tile_ml = reinterpret_cast<float*>(w + l.tile_ml);
   a.part_o = reinterpret_cast<float*>(w + l.part_o);
   a.part_ml = reinterpret_cast<float*>(w + l.part_ml);
+  a.select_count = reinterpret_cast<int*>(w + l.counters);
+  a.merge_count = a.select_count + (size_t)batch * h_kv;
   a.n_split = l.n_split;
   return cuda_status(launch_decode(a, stream), "nsa_sparse_decode");
 }

@@ -50,10 +50,12 @@ struct DecodeArgs {
   float* tile_ml;  // [batch, hkv, n_tiles, r, 2]
   float* part_o;   // [batch, hkv * rtiles, n_split, 16, d]
   float* part_ml;  // [batch, hkv * rtiles, n_split, 16, 2]
+  int* select_count;  // [batch, hkv] score CTAs done (zeroed per call)
+  int* merge_count;   // [batch, hkv * rtiles] split CTAs done (zeroed per call)
   int n_split;
 };
 struct DecodeLayout {
-  size_t z, tile_ml, idx, part_o, part_ml, total;
+  size_t z, tile_ml, idx, part_o, part_ml, counters, counter_bytes, total;
   int nc_pad, n_tiles, n_split;
 };
 DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int kernel, int stride,

@@ -33,6 +33,7 @@ struct SparseParams {
   int entries_per_split;
   float* part_o;
   float* part_ml;
+  int* merge_count;  // decode: [batch, gridDim.y] split arrivals, zero at launch
 };
 
 #ifndef NSA_PREFILL_NSTAGE
@@ -40,6 +41,10 @@ struct SparseParams {
 #endif
 #ifndef NSA_PREFILL_MINBLOCKS
 #define NSA_PREFILL_MINBLOCKS 3
+#endif
+
+#ifndef NSA_DECODE_NSTAGE
+#define NSA_DECODE_NSTAGE 2
 #endif
 
 // Softmax state is rescaled lazily: the running max m only moves when a new score
@@ -76,6 +81,17 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   const int e0 = DECODE ? blockIdx.z * p.entries_per_split : 0;
   const int e1 = DECODE ? min(p.S, e0 + p.entries_per_split) : p.S;
 
+  // Q fragments of the group's heads (rows past the group read as zero)
+  const int hbase = g * r + rt * 16;
+  const int rlo = lane >> 2, rhi = rlo + 8;
+  const __nv_bfloat16* qb = p.q + (qrow * p.h + hbase) * D;
+  uint32_t qa[D / 16][4];
+  load_a_frags<D>(qa, rt * 16 + rlo < r ? qb + rlo * D : nullptr, rt * 16 + rhi < r ? qb + rhi * D : nullptr,
+                  lane);
+  // decode runs as a programmatic dependent launch: everything above overlaps the
+  // selection kernel; the block lists it writes are read only after this point
+  if (DECODE) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
   // this warp's work list: listed blocks whose slice starts at or before t
   const int32_t* il = p.idx + (qrow * p.hkv + g) * p.S;
   int cnt = 0;
@@ -92,14 +108,6 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
     cnt += __popc(m);
   }
   __syncwarp();
-
-  // Q fragments of the group's heads (rows past the group read as zero)
-  const int hbase = g * r + rt * 16;
-  const int rlo = lane >> 2, rhi = rlo + 8;
-  const __nv_bfloat16* qb = p.q + (qrow * p.h + hbase) * D;
-  uint32_t qa[D / 16][4];
-  load_a_frags<D>(qa, rt * 16 + rlo < r ? qb + rlo * D : nullptr, rt * 16 + rhi < r ? qb + rhi * D : nullptr,
-                  lane);
 
   const uint32_t wbase = smem_u32(smem) + warp * NSTAGE * STAGE_BYTES;
   const int64_t row_stride = (int64_t)p.hkv * D;
@@ -190,114 +198,133 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   cp_async_wait<0>();
   __syncthreads();  // every warp is done with its ring: reuse shared memory to merge
 
-  float* sm_o = reinterpret_cast<float*>(smem);  // [NW][16][D]
-  float* sm_m = sm_o + NW * 16 * D;               // [NW][16]
-  float* sm_l = sm_m + NW * 16;                   // [NW][16]
+  // Warps 1..3 park their (m, l, O) fragments in shared memory; warp 0 merges them
+  // into its own registers in the same fragment layout (rows padded by 8 floats so the
+  // 8-byte fragment stores and loads are free of bank conflicts).
+  constexpr int OS = D + 8;
+  float* sm_o = reinterpret_cast<float*>(smem);  // [NW][16][OS]
+  float* sm_m = sm_o + NW * 16 * OS;             // [NW][16]
+  float* sm_l = sm_m + NW * 16;                  // [NW][16]
   l0 = quad_sum(l0);
   l1 = quad_sum(l1);
-  if ((lane & 3) == 0) {
-    sm_m[warp * 16 + rlo] = m0;
-    sm_m[warp * 16 + rhi] = m1;
-    sm_l[warp * 16 + rlo] = l0;
-    sm_l[warp * 16 + rhi] = l1;
-  }
+  if (warp > 0) {
+    if ((lane & 3) == 0) {
+      sm_m[warp * 16 + rlo] = m0;
+      sm_m[warp * 16 + rhi] = m1;
+      sm_l[warp * 16 + rlo] = l0;
+      sm_l[warp * 16 + rhi] = l1;
+    }
 #pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt) {
-    const int col = nt * 8 + (lane & 3) * 2;
-    *reinterpret_cast<float2*>(&sm_o[(warp * 16 + rlo) * D + col]) = make_float2(o[nt][0], o[nt][1]);
-    *reinterpret_cast<float2*>(&sm_o[(warp * 16 + rhi) * D + col]) = make_float2(o[nt][2], o[nt][3]);
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<float2*>(&sm_o[(warp * 16 + rlo) * OS + col]) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(&sm_o[(warp * 16 + rhi) * OS + col]) = make_float2(o[nt][2], o[nt][3]);
+    }
   }
   __syncthreads();
-
-  const int row = threadIdx.x >> 3;
-  const int c0 = (threadIdx.x & 7) * (D / 8);
-  float M = kNegInf;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * 16 + row]);
-  const float Mu = M == kNegInf ? 0.f : M;
-  float f[NW], L = 0.f;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    f[w] = ex2(sm_m[w * 16 + row] - Mu);
-    L += f[w] * sm_l[w * 16 + row];
-  }
-  if (!DECODE) {
-    if (rt * 16 + row >= r) return;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* dst = p.o + (qrow * p.h + hbase + row) * D + c0;
-#pragma unroll
-    for (int c = 0; c < D / 8; c += 8) {
-      float acc[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float x = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) x += f[w] * sm_o[(w * 16 + row) * D + c0 + c + u];
-        acc[u] = x * inv;
-      }
-      uint4 pk;
-      pk.x = pack_bf16(acc[0], acc[1]);
-      pk.y = pack_bf16(acc[2], acc[3]);
-      pk.z = pack_bf16(acc[4], acc[5]);
-      pk.w = pack_bf16(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(dst + c) = pk;
-    }
-    if (p.lse && (threadIdx.x & 7) == 0)
-      p.lse[qrow * p.h + hbase + row] = L > 0.f ? (Mu + __log2f(L)) * kLn2 : kNegInf;
+  if (warp > 0) {
+    if (!DECODE) return;
   } else {
-    // unnormalised partial state of this split: O * 2^-Mu, (M, L)
-    const int64_t slot = ((qrow * gridDim.y + blockIdx.y) * gridDim.z + blockIdx.z) * 16 + row;
-    float* dst = p.part_o + slot * D + c0;
+    float M0 = m0, M1 = m1;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      float x = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) x += f[w] * sm_o[(w * 16 + row) * D + c0 + c];
-      dst[c] = x;
+    for (int w = 1; w < NW; ++w) {
+      M0 = fmaxf(M0, sm_m[w * 16 + rlo]);
+      M1 = fmaxf(M1, sm_m[w * 16 + rhi]);
     }
-    if ((threadIdx.x & 7) == 0) {
-      p.part_ml[slot * 2] = M;
-      p.part_ml[slot * 2 + 1] = L;
+    const float u0 = M0 == kNegInf ? 0.f : M0, u1 = M1 == kNegInf ? 0.f : M1;
+    float f0[NW], f1[NW];
+    f0[0] = ex2(m0 - u0);
+    f1[0] = ex2(m1 - u1);
+    float L0 = f0[0] * l0, L1 = f1[0] * l1;
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+      f0[w] = ex2(sm_m[w * 16 + rlo] - u0);
+      f1[w] = ex2(sm_m[w * 16 + rhi] - u1);
+      L0 += f0[w] * sm_l[w * 16 + rlo];
+      L1 += f1[w] * sm_l[w * 16 + rhi];
+    }
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      float a0 = f0[0] * o[nt][0], a1 = f0[0] * o[nt][1], a2 = f1[0] * o[nt][2], a3 = f1[0] * o[nt][3];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) {
+        const float2 x = *reinterpret_cast<const float2*>(&sm_o[(w * 16 + rlo) * OS + col]);
+        const float2 y = *reinterpret_cast<const float2*>(&sm_o[(w * 16 + rhi) * OS + col]);
+        a0 += f0[w] * x.x;
+        a1 += f0[w] * x.y;
+        a2 += f1[w] * y.x;
+        a3 += f1[w] * y.y;
+      }
+      o[nt][0] = a0;
+      o[nt][1] = a1;
+      o[nt][2] = a2;
+      o[nt][3] = a3;
+    }
+    if (!DECODE) {
+      const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
+      const bool w0 = rt * 16 + rlo < r, w1 = rt * 16 + rhi < r;
+      __nv_bfloat16* d0 = p.o + (qrow * p.h + hbase + rlo) * D;
+      __nv_bfloat16* d1 = p.o + (qrow * p.h + hbase + rhi) * D;
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt) {
+        const int col = nt * 8 + (lane & 3) * 2;
+        if (w0) *reinterpret_cast<uint32_t*>(d0 + col) = pack_bf16(o[nt][0] * i0, o[nt][1] * i0);
+        if (w1) *reinterpret_cast<uint32_t*>(d1 + col) = pack_bf16(o[nt][2] * i1, o[nt][3] * i1);
+      }
+      if (p.lse && (lane & 3) == 0) {
+        if (w0) p.lse[qrow * p.h + hbase + rlo] = L0 > 0.f ? (u0 + __log2f(L0)) * kLn2 : kNegInf;
+        if (w1) p.lse[qrow * p.h + hbase + rhi] = L1 > 0.f ? (u1 + __log2f(L1)) * kLn2 : kNegInf;
+      }
+      return;
+    }
+    // decode: unnormalised partial state of this split, O * 2^-u, (M, L)
+    const int64_t slot = ((qrow * gridDim.y + blockIdx.y) * gridDim.z + blockIdx.z) * 16;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<float2*>(p.part_o + (slot + rlo) * D + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(p.part_o + (slot + rhi) * D + col) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if ((lane & 3) == 0) {
+      p.part_ml[(slot + rlo) * 2] = M0;
+      p.part_ml[(slot + rlo) * 2 + 1] = L0;
+      p.part_ml[(slot + rhi) * 2] = M1;
+      p.part_ml[(slot + rhi) * 2 + 1] = L1;
     }
   }
-}
-
-// Merge the split partial states of the decode pass: one CTA per (sequence, kv-head
-// row tile), 16 rows x D columns.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge(const float* part_o, const float* part_ml,
-                                                   __nv_bfloat16* o, int h, int hkv, int n_split) {
-  const int r = h / hkv;
-  const int rtiles = (r + 15) >> 4;
-  const int g = blockIdx.y / rtiles, rt = blockIdx.y % rtiles;
-  const int row = threadIdx.x >> 3;
-  const int c0 = (threadIdx.x & 7) * (D / 8);
-  if (rt * 16 + row >= r) return;
-  const int64_t base = ((int64_t)blockIdx.x * gridDim.y + blockIdx.y) * n_split;
-  float M = kNegInf;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_ml[((base + s) * 16 + row) * 2]);
-  const float Mu = M == kNegInf ? 0.f : M;
-  float L = 0.f;
-  float acc[D / 8];
+  if (DECODE) {
+    // The last split CTA of this (sequence, row tile) merges every split's state.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+      s_last = atomicAdd(&p.merge_count[qrow * gridDim.y + blockIdx.y], 1) == (int)gridDim.z - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int row = threadIdx.x >> 3;
+    if (rt * 16 + row >= r) return;
+    const int64_t base = (qrow * gridDim.y + blockIdx.y) * gridDim.z;
+    float M = kNegInf;
+    for (int sp = 0; sp < (int)gridDim.z; ++sp) M = fmaxf(M, __ldcg(p.part_ml + ((base + sp) * 16 + row) * 2));
+    const float Mu = M == kNegInf ? 0.f : M;
+    float L = 0.f;
+    float acc[D / 8];
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const int64_t slot = (base + s) * 16 + row;
-    const float f = ex2(part_ml[slot * 2] - Mu);
-    L += f * part_ml[slot * 2 + 1];
+    for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
+    const int cl = threadIdx.x & 7;  // columns cl, cl+8, ... : 8 lanes read 32 contiguous bytes
+    for (int sp = 0; sp < (int)gridDim.z; ++sp) {
+      const int64_t sl = (base + sp) * 16 + row;
+      const float f = ex2(__ldcg(p.part_ml + sl * 2) - Mu);
+      L += f * __ldcg(p.part_ml + sl * 2 + 1);
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) acc[c] += f * part_o[slot * D + c0 + c];
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* dst = o + ((int64_t)blockIdx.x * h + g * r + rt * 16 + row) * D + c0;
+      for (int c = 0; c < D / 8; ++c) acc[c] += f * __ldcg(p.part_o + sl * D + cl + 8 * c);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* dst = p.o + (qrow * p.h + hbase + row) * D;
 #pragma unroll
-  for (int c = 0; c < D / 8; c += 8) {
-    uint4 pk;
-    pk.x = pack_bf16(acc[c + 0] * inv, acc[c + 1] * inv);
-    pk.y = pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv);
-    pk.z = pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv);
-    pk.w = pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv);
-    *reinterpret_cast<uint4*>(dst + c) = pk;
+    for (int c = 0; c < D / 8; ++c) dst[cl + 8 * c] = __float2bfloat16_rn(acc[c] * inv);
   }
 }
 
@@ -367,13 +394,27 @@ __global__ void __launch_bounds__(128) sparse_fwd_f32(const float* __restrict__ 
 template <int D, int BS, int NSTAGE, bool DECODE>
 static cudaError_t run_mma(const SparseParams& p, dim3 grid, cudaStream_t st) {
   constexpr int pipe = 4 * NSTAGE * 2 * 16 * D * 2;
-  constexpr int merge = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
+  constexpr int merge = 4 * 16 * (D + 8) * 4 + 2 * 4 * 16 * 4;
   constexpr int bytes = pipe > merge ? pipe : merge;
   auto kern = sparse_fwd_mma<D, BS, NSTAGE, DECODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 128, bytes, st>>>(p);
-  return cudaGetLastError();
+  if (!DECODE) {
+    kern<<<grid, 128, bytes, st>>>(p);
+    return cudaGetLastError();
+  }
+  // decode: launched as a programmatic dependent of the selection kernel
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const void* v,
@@ -433,14 +474,13 @@ cudaError_t launch_decode_attn(const DecodeArgs& a, cudaStream_t st) {
   p.entries_per_split = (a.k + a.n_split - 1) / a.n_split;
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
+  p.merge_count = a.merge_count;
+  p.o = (__nv_bfloat16*)a.o;  // the last split CTA writes the merged row here
+  if (!p.o || !p.part_o || !p.part_ml || !p.merge_count || !p.idx) return cudaErrorInvalidValue;
   const int r = a.h / a.hkv;
   const int rtiles = (r + 15) / 16;
   dim3 grid(a.batch, a.hkv * rtiles, a.n_split);
-  cudaError_t e = run_mma<128, 64, 3, true>(p, grid, st);
-  if (e != cudaSuccess) return e;
-  decode_merge<128><<<dim3(a.batch, a.hkv * rtiles), 128, 0, st>>>(a.part_o, a.part_ml, (__nv_bfloat16*)a.o,
-                                                                   a.h, a.hkv, a.n_split);
-  return cudaGetLastError();
+  return run_mma<128, 64, NSA_DECODE_NSTAGE, true>(p, grid, st);
 }
 
 }  // namespace nsa

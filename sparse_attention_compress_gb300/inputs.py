@@ -121,8 +121,8 @@ class Workload:
 
 
 def attention_workload(name: str, config_number: int, B: int, T: int, H: int, HKV: int, D: int,
-                       dtype: str, block_size: int, S: int, force_first: bool) -> Workload:
-    rng = rng_for(config_number)
+                       dtype: str, block_size: int, S: int, force_first: bool, salt: int = 0) -> Workload:
+    rng = rng_for(config_number, salt)
     q = normal(rng, (B * T, H, D), dtype)
     k = normal(rng, (B * T, HKV, D), dtype)
     v = normal(rng, (B * T, HKV, D), dtype)
@@ -137,9 +137,10 @@ def tiny(T: int = 256) -> Workload:
     return attention_workload("tiny", 0, 1, T, 4, 1, 64, "f32", 32, 4, force_first=False)
 
 
-def prefill(B: int = 8, T: int = 16384) -> Workload:
-    """B=8, T=16384, H=16, Hkv=1, d=128, bf16, block 64, S=16, blocks 0 and own listed."""
-    return attention_workload("prefill", 1, B, T, 16, 1, 128, "bf16", 64, 16, force_first=True)
+def prefill(B: int = 8, T: int = 16384, salt: int = 0) -> Workload:
+    """B=8, T=16384, H=16, Hkv=1, d=128, bf16, block 64, S=16, blocks 0 and own listed.
+    `salt` draws an independent batch (one per rank when the work is sharded)."""
+    return attention_workload("prefill", 1, B, T, 16, 1, 128, "bf16", 64, 16, force_first=True, salt=salt)
 
 
 def selection(n_seqs: int = 4, lo: int = 4096, hi: int = 32768, H: int = 16, HKV: int = 2,

@@ -53,11 +53,11 @@ def test_noalloc_rejects_steps_beyond_the_fixed_scratch():
     lib = nsa.load()
     cap = int(lib.nsa_sparse_decode_noalloc_max_bytes())
     assert cap == 16 << 20
-    # 256 sequences of 32768 tokens need far more scratch than the fixed array holds
-    need = nsa.nsa_sparse_decode_workspace_size(256, 32768, 16, 2, 128, k=64)
+    # 1024 sequences of 32768 tokens need far more scratch than the fixed array holds
+    need = nsa.nsa_sparse_decode_workspace_size(1024, 32768, 16, 2, 128, k=64)
     assert need > cap
     fake = ctypes.c_void_p(0x10000)
-    rc = lib.nsa_sparse_decode_noalloc(256, fake, 32768, 16, 2, 128, fake, fake, fake, fake, 32, 16, 64, 1, 2, 64,
+    rc = lib.nsa_sparse_decode_noalloc(1024, fake, 32768, 16, 2, 128, fake, fake, fake, fake, 32, 16, 64, 1, 2, 64,
                                        0.0, None, fake, None)
     assert rc == 2
     msg = lib.nsa_last_error()
