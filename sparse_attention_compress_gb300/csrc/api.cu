@@ -3,7 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
-#include "../../include/nsa.h"
+#include "nsa.h"
 #include "launch.h"
 
 using namespace nsa;

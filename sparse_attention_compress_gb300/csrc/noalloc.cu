@@ -10,7 +10,7 @@
 // process exits.
 #include <mutex>
 
-#include "../../include/nsa.h"
+#include "nsa.h"
 #include "launch.h"
 
 using namespace nsa;

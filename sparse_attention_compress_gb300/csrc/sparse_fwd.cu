@@ -9,10 +9,10 @@
 // GB300 design.  One CTA serves one (query token, kv-head) and every query head of the
 // group (up to 16 rows: the M of one m16n8k16 tile).  Its four warps split each 64-key
 // block into four 16-key slices; each warp streams its slice of every listed block
-// through a private cp.async ring, runs its own online softmax (base-2 exponentials
-// with scale*log2(e) folded in, [TileLang-NSA] sec. 3.1) and the warps merge their
-// (max, sum, O) states once at the end.  Warps never wait on one another inside the
-// loop, so no CTA-wide barrier sits on the gather path.
+// through a private cp.async ring and keeps its own online softmax (warp_attend), and
+// the warps merge their (max, sum, O) states once at the end (cta_merge).  Warps never
+// wait on one another inside the loop, so no CTA-wide barrier sits on the gather path.
+#include "attend.cuh"
 #include "launch.h"
 
 namespace nsa {
@@ -47,18 +47,12 @@ struct SparseParams {
 #define NSA_DECODE_NSTAGE 2
 #endif
 
-// Softmax state is rescaled lazily: the running max m only moves when a new score
-// exceeds it by more than 2^kLazy in base 2, so exponentials stay below 2^kLazy and
-// almost no iteration pays the O rescale (the final normalisation is unchanged).
-constexpr float kLazy = 8.f;
-
 template <int D, int BS, int NSTAGE, bool DECODE>
 __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(const SparseParams p) {
   constexpr int NW = 4;
   constexpr int NSLICE = BS / 16;
   constexpr int NGROUP = NW / NSLICE;
-  constexpr int SLICE_BYTES = 16 * D * 2;
-  constexpr int STAGE_BYTES = 2 * SLICE_BYTES;
+  constexpr int STAGE_BYTES = 2 * 16 * D * 2;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_list[NW][64];
 
@@ -68,13 +62,14 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   const int rtiles = (r + 15) >> 4;
   const int g = blockIdx.y / rtiles, rt = blockIdx.y % rtiles;
 
-  int64_t qrow = blockIdx.x, kv_base;
+  const int64_t qrow = blockIdx.x;
+  int64_t kv_base;
   int t;
   if (DECODE) {
     t = p.seqlens[qrow] - 1;
     kv_base = qrow * (int64_t)p.max_len;
   } else {
-    int sq = seq_of_token(p.seqs, qrow);
+    const int sq = seq_of_token(p.seqs, qrow);
     kv_base = seq_start(p.seqs, sq);
     t = (int)(qrow - kv_base);
   }
@@ -109,177 +104,39 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   }
   __syncwarp();
 
-  const uint32_t wbase = smem_u32(smem) + warp * NSTAGE * STAGE_BYTES;
-  const int64_t row_stride = (int64_t)p.hkv * D;
-  auto issue = [&](int i) {
-    const int64_t key0 = (int64_t)s_list[warp][i] * BS + slice * 16;
-    const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
-    const __nv_bfloat16* kb = p.k + ((kv_base + key0) * p.hkv + g) * D;
-    const __nv_bfloat16* vb = p.v + ((kv_base + key0) * p.hkv + g) * D;
-    const bool full = key0 + 15 <= t;
-    constexpr int CH = D / 8;
-#pragma unroll
-    for (int c = lane; c < 16 * CH; c += 32) {
-      const int row = c / CH, ch = c % CH;
-      const bool ok = full || key0 + row <= t;
-      const int64_t off = row * row_stride + ch * 8;
-      cp_async16(tile_addr<D>(sb, row, ch), ok ? kb + off : p.k, ok ? 16 : 0);
-      cp_async16(tile_addr<D>(sb + SLICE_BYTES, row, ch), ok ? vb + off : p.v, ok ? 16 : 0);
-    }
-  };
-
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+  WarpState st = warp_attend<D, BS, NSTAGE>(s_list[warp], cnt, slice, p.k + (kv_base * p.hkv + g) * D,
+                                            p.v + (kv_base * p.hkv + g) * D, (int64_t)p.hkv * D, t,
+                                            p.scale_log2, qa, smem_u32(smem) + warp * NSTAGE * STAGE_BYTES, p.k,
+                                            o, lane);
+  __syncthreads();  // every warp is done with its ring: the merge reuses the shared memory
+  cta_merge<D, NW>(reinterpret_cast<float*>(smem), o, st, warp, lane);
 
-#pragma unroll
-  for (int i = 0; i < NSTAGE - 1; ++i) {
-    if (i < cnt) issue(i);
-    cp_async_commit();
-  }
-  for (int i = 0; i < cnt; ++i) {
-    if (i + NSTAGE - 1 < cnt) issue(i + NSTAGE - 1);
-    cp_async_commit();
-    cp_async_wait<NSTAGE - 1>();
-    __syncwarp();
-    const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    qk_16keys_2acc<D>(s, s2, qa, sb, 0, lane);
-    const int64_t key0 = (int64_t)s_list[warp][i] * BS + slice * 16;
-    if (key0 + 15 <= t) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) s[nt][j] = (s[nt][j] + s2[nt][j]) * p.scale_log2;
-    } else {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t key = key0 + nt * 8 + (lane & 3) * 2 + (j & 1);
-          s[nt][j] = key <= t ? (s[nt][j] + s2[nt][j]) * p.scale_log2 : kNegInf;
-        }
-    }
-    const float mx0 = quad_max(fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1])));
-    const float mx1 = quad_max(fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3])));
-    if (!__all_sync(0xffffffffu, mx0 <= m0 + kLazy && mx1 <= m1 + kLazy)) {
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float a0 = ex2(m0 - (mn0 == kNegInf ? 0.f : mn0)), a1 = ex2(m1 - (mn1 == kNegInf ? 0.f : mn1));
-      m0 = mn0;
-      m1 = mn1;
-      l0 *= a0;
-      l1 *= a1;
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        o[nt][0] *= a0;
-        o[nt][1] *= a0;
-        o[nt][2] *= a1;
-        o[nt][3] *= a1;
-      }
-    }
-    const float mu0 = m0 == kNegInf ? 0.f : m0, mu1 = m1 == kNegInf ? 0.f : m1;
-    float pr[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = ex2(s[nt][0] - mu0);
-      pr[nt][1] = ex2(s[nt][1] - mu0);
-      pr[nt][2] = ex2(s[nt][2] - mu1);
-      pr[nt][3] = ex2(s[nt][3] - mu1);
-    }
-    l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-    const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
-                            pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
-    pv_16keys<D>(o, pa, sb + SLICE_BYTES, 0, lane);
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-  __syncthreads();  // every warp is done with its ring: reuse shared memory to merge
-
-  // Warps 1..3 park their (m, l, O) fragments in shared memory; warp 0 merges them
-  // into its own registers in the same fragment layout (rows padded by 8 floats so the
-  // 8-byte fragment stores and loads are free of bank conflicts).
-  constexpr int OS = D + 8;
-  float* sm_o = reinterpret_cast<float*>(smem);  // [NW][16][OS]
-  float* sm_m = sm_o + NW * 16 * OS;             // [NW][16]
-  float* sm_l = sm_m + NW * 16;                  // [NW][16]
-  l0 = quad_sum(l0);
-  l1 = quad_sum(l1);
-  if (warp > 0) {
-    if ((lane & 3) == 0) {
-      sm_m[warp * 16 + rlo] = m0;
-      sm_m[warp * 16 + rhi] = m1;
-      sm_l[warp * 16 + rlo] = l0;
-      sm_l[warp * 16 + rhi] = l1;
-    }
+  if (!DECODE) {
+    if (warp != 0) return;
+    const float u0 = st.m0 == kNegInf ? 0.f : st.m0, u1 = st.m1 == kNegInf ? 0.f : st.m1;
+    const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
+    const bool w0 = rt * 16 + rlo < r, w1 = rt * 16 + rhi < r;
+    __nv_bfloat16* d0 = p.o + (qrow * p.h + hbase + rlo) * D;
+    __nv_bfloat16* d1 = p.o + (qrow * p.h + hbase + rhi) * D;
 #pragma unroll
     for (int nt = 0; nt < D / 8; ++nt) {
       const int col = nt * 8 + (lane & 3) * 2;
-      *reinterpret_cast<float2*>(&sm_o[(warp * 16 + rlo) * OS + col]) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(&sm_o[(warp * 16 + rhi) * OS + col]) = make_float2(o[nt][2], o[nt][3]);
+      if (w0) *reinterpret_cast<uint32_t*>(d0 + col) = pack_bf16(o[nt][0] * i0, o[nt][1] * i0);
+      if (w1) *reinterpret_cast<uint32_t*>(d1 + col) = pack_bf16(o[nt][2] * i1, o[nt][3] * i1);
     }
+    if (p.lse && (lane & 3) == 0) {
+      if (w0) p.lse[qrow * p.h + hbase + rlo] = st.l0 > 0.f ? (u0 + __log2f(st.l0)) * kLn2 : kNegInf;
+      if (w1) p.lse[qrow * p.h + hbase + rhi] = st.l1 > 0.f ? (u1 + __log2f(st.l1)) * kLn2 : kNegInf;
+    }
+    return;
   }
-  __syncthreads();
-  if (warp > 0) {
-    if (!DECODE) return;
-  } else {
-    float M0 = m0, M1 = m1;
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-      M0 = fmaxf(M0, sm_m[w * 16 + rlo]);
-      M1 = fmaxf(M1, sm_m[w * 16 + rhi]);
-    }
-    const float u0 = M0 == kNegInf ? 0.f : M0, u1 = M1 == kNegInf ? 0.f : M1;
-    float f0[NW], f1[NW];
-    f0[0] = ex2(m0 - u0);
-    f1[0] = ex2(m1 - u1);
-    float L0 = f0[0] * l0, L1 = f1[0] * l1;
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-      f0[w] = ex2(sm_m[w * 16 + rlo] - u0);
-      f1[w] = ex2(sm_m[w * 16 + rhi] - u1);
-      L0 += f0[w] * sm_l[w * 16 + rlo];
-      L1 += f1[w] * sm_l[w * 16 + rhi];
-    }
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      const int col = nt * 8 + (lane & 3) * 2;
-      float a0 = f0[0] * o[nt][0], a1 = f0[0] * o[nt][1], a2 = f1[0] * o[nt][2], a3 = f1[0] * o[nt][3];
-#pragma unroll
-      for (int w = 1; w < NW; ++w) {
-        const float2 x = *reinterpret_cast<const float2*>(&sm_o[(w * 16 + rlo) * OS + col]);
-        const float2 y = *reinterpret_cast<const float2*>(&sm_o[(w * 16 + rhi) * OS + col]);
-        a0 += f0[w] * x.x;
-        a1 += f0[w] * x.y;
-        a2 += f1[w] * y.x;
-        a3 += f1[w] * y.y;
-      }
-      o[nt][0] = a0;
-      o[nt][1] = a1;
-      o[nt][2] = a2;
-      o[nt][3] = a3;
-    }
-    if (!DECODE) {
-      const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
-      const bool w0 = rt * 16 + rlo < r, w1 = rt * 16 + rhi < r;
-      __nv_bfloat16* d0 = p.o + (qrow * p.h + hbase + rlo) * D;
-      __nv_bfloat16* d1 = p.o + (qrow * p.h + hbase + rhi) * D;
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        const int col = nt * 8 + (lane & 3) * 2;
-        if (w0) *reinterpret_cast<uint32_t*>(d0 + col) = pack_bf16(o[nt][0] * i0, o[nt][1] * i0);
-        if (w1) *reinterpret_cast<uint32_t*>(d1 + col) = pack_bf16(o[nt][2] * i1, o[nt][3] * i1);
-      }
-      if (p.lse && (lane & 3) == 0) {
-        if (w0) p.lse[qrow * p.h + hbase + rlo] = L0 > 0.f ? (u0 + __log2f(L0)) * kLn2 : kNegInf;
-        if (w1) p.lse[qrow * p.h + hbase + rhi] = L1 > 0.f ? (u1 + __log2f(L1)) * kLn2 : kNegInf;
-      }
-      return;
-    }
-    // decode: unnormalised partial state of this split, O * 2^-u, (M, L)
-    const int64_t slot = ((qrow * gridDim.y + blockIdx.y) * gridDim.z + blockIdx.z) * 16;
+
+  // decode: this split's unnormalised state O * 2^-u, (M, L); the last split merges
+  const int64_t slot = ((qrow * gridDim.y + blockIdx.y) * gridDim.z + blockIdx.z) * 16;
+  if (warp == 0) {
 #pragma unroll
     for (int nt = 0; nt < D / 8; ++nt) {
       const int col = nt * 8 + (lane & 3) * 2;
@@ -287,46 +144,44 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
       *reinterpret_cast<float2*>(p.part_o + (slot + rhi) * D + col) = make_float2(o[nt][2], o[nt][3]);
     }
     if ((lane & 3) == 0) {
-      p.part_ml[(slot + rlo) * 2] = M0;
-      p.part_ml[(slot + rlo) * 2 + 1] = L0;
-      p.part_ml[(slot + rhi) * 2] = M1;
-      p.part_ml[(slot + rhi) * 2 + 1] = L1;
+      p.part_ml[(slot + rlo) * 2] = st.m0;
+      p.part_ml[(slot + rlo) * 2 + 1] = st.l0;
+      p.part_ml[(slot + rhi) * 2] = st.m1;
+      p.part_ml[(slot + rhi) * 2 + 1] = st.l1;
     }
   }
-  if (DECODE) {
-    // The last split CTA of this (sequence, row tile) merges every split's state.
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0)
-      s_last = atomicAdd(&p.merge_count[qrow * gridDim.y + blockIdx.y], 1) == (int)gridDim.z - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const int row = threadIdx.x >> 3;
-    if (rt * 16 + row >= r) return;
-    const int64_t base = (qrow * gridDim.y + blockIdx.y) * gridDim.z;
-    float M = kNegInf;
-    for (int sp = 0; sp < (int)gridDim.z; ++sp) M = fmaxf(M, __ldcg(p.part_ml + ((base + sp) * 16 + row) * 2));
-    const float Mu = M == kNegInf ? 0.f : M;
-    float L = 0.f;
-    float acc[D / 8];
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    s_last = atomicAdd(&p.merge_count[qrow * gridDim.y + blockIdx.y], 1) == (int)gridDim.z - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int row = threadIdx.x >> 3;
+  if (rt * 16 + row >= r) return;
+  const int64_t base = (qrow * gridDim.y + blockIdx.y) * gridDim.z;
+  float M = kNegInf;
+  for (int sp = 0; sp < (int)gridDim.z; ++sp) M = fmaxf(M, __ldcg(p.part_ml + ((base + sp) * 16 + row) * 2));
+  const float Mu = M == kNegInf ? 0.f : M;
+  float L = 0.f;
+  float acc[D / 8];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
-    const int cl = threadIdx.x & 7;  // columns cl, cl+8, ... : 8 lanes read 32 contiguous bytes
-    for (int sp = 0; sp < (int)gridDim.z; ++sp) {
-      const int64_t sl = (base + sp) * 16 + row;
-      const float f = ex2(__ldcg(p.part_ml + sl * 2) - Mu);
-      L += f * __ldcg(p.part_ml + sl * 2 + 1);
+  for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
+  const int cl = threadIdx.x & 7;  // columns cl, cl+8, ... : 8 lanes read 32 contiguous bytes
+  for (int sp = 0; sp < (int)gridDim.z; ++sp) {
+    const int64_t sl = (base + sp) * 16 + row;
+    const float f = ex2(__ldcg(p.part_ml + sl * 2) - Mu);
+    L += f * __ldcg(p.part_ml + sl * 2 + 1);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) acc[c] += f * __ldcg(p.part_o + sl * D + cl + 8 * c);
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16* dst = p.o + (qrow * p.h + hbase + row) * D;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) dst[cl + 8 * c] = __float2bfloat16_rn(acc[c] * inv);
+    for (int c = 0; c < D / 8; ++c) acc[c] += f * __ldcg(p.part_o + sl * D + cl + 8 * c);
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* dst = p.o + (qrow * p.h + hbase + row) * D;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) dst[cl + 8 * c] = __float2bfloat16_rn(acc[c] * inv);
 }
+
 
 // fp32 selected attention on CUDA cores (small problems; exact fp32 arithmetic).
 // One CTA per (token, kv-head); warp w serves heads w, w+4, ... of the group.
@@ -394,7 +249,7 @@ __global__ void __launch_bounds__(128) sparse_fwd_f32(const float* __restrict__ 
 template <int D, int BS, int NSTAGE, bool DECODE>
 static cudaError_t run_mma(const SparseParams& p, dim3 grid, cudaStream_t st) {
   constexpr int pipe = 4 * NSTAGE * 2 * 16 * D * 2;
-  constexpr int merge = 4 * 16 * (D + 8) * 4 + 2 * 4 * 16 * 4;
+  constexpr int merge = merge_bytes<D, 4>();
   constexpr int bytes = pipe > merge ? pipe : merge;
   auto kern = sparse_fwd_mma<D, BS, NSTAGE, DECODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
