@@ -36,8 +36,10 @@ DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int ke
 #ifdef NSA_DECODE_SPLIT
   int ns = NSA_DECODE_SPLIT;
 #else
-  int ns = 1;
-  while (ns < 16 && (int64_t)batch * hkv * rtiles * ns < 2 * 152) ns *= 2;
+  // as many splits as keep the attention grid within one resident wave (2 CTAs per SM)
+  const int64_t units = (int64_t)batch * hkv * rtiles;
+  int ns = (int)(2 * 152 / (units > 0 ? units : 1));
+  ns = ns < 1 ? 1 : (ns > 16 ? 16 : ns);
 #endif
   l.n_split = ns < k ? ns : k;
   size_t off = 0;
@@ -80,7 +82,6 @@ template <int D, int R, int NPL>
 __global__ void __launch_bounds__(128) decode_score_select(const ScoreSelectParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_last;
-  __shared__ float s_lse[16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y, g = blockIdx.z;
   const int tile = blockIdx.x * 4 + warp;
@@ -168,50 +169,85 @@ __global__ void __launch_bounds__(128) decode_score_select(const ScoreSelectPara
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // Every global load of the selection is issued in one batch (data written by other
+  // SMs costs a full L2 round trip each time): the row's tile (max, sum) pairs go to
+  // shared memory, this thread's pooled block partials to registers.
+  constexpr int JPT = NPL * 32 / 128;                     // blocks per thread
+  constexpr int ZB = JPT * R <= 64 ? JPT : (64 / R > 0 ? 64 / R : 1);  // blocks per batch
   float* red_m = reinterpret_cast<float*>(smem);  // [R][kMaxTiles]
   float* red_l = red_m + R * kMaxTiles;           // [R][kMaxTiles]
   float* sc = red_l + R * kMaxTiles;              // [NPL*32]
+  float* fac = sc + NPL * 32;                     // [kMaxTiles][R]
+  const int nb = (L + 63) / 64;
+  const float* zr = p.z + row * p.n_tiles * 16 * R;
+  float zreg[ZB][R];
+  auto load_z = [&](int j0) {  // blocks j0 + 128*i, i < ZB
+#pragma unroll
+    for (int i = 0; i < ZB; ++i) {
+      const int j = j0 + 128 * i;
+      const bool ok = j < nb && j / 16 < n_tb;
+#pragma unroll
+      for (int hh = 0; hh < R; ++hh) zreg[i][hh] = ok ? __ldcg(zr + (int64_t)j * R + hh) : 0.f;
+    }
+  };
   for (int i = threadIdx.x; i < R * n_tb; i += blockDim.x) {
     const int hh = i / n_tb, tl = i % n_tb;
     const float* tm = p.tile_ml + ((row * p.n_tiles + tl) * R + hh) * 2;
     red_m[hh * kMaxTiles + tl] = __ldcg(tm);
     red_l[hh * kMaxTiles + tl] = __ldcg(tm + 1);
   }
+  load_z(threadIdx.x);
   __syncthreads();
-  if (threadIdx.x < R) {
-    const float* mm = red_m + threadIdx.x * kMaxTiles;
-    const float* ll = red_l + threadIdx.x * kMaxTiles;
+  // per-head normaliser: one warp per head folds the tile pairs with shuffles, then
+  // writes the factor 2^(m_tile - lse) that turns a tile's partials into probabilities
+  for (int hh = warp; hh < R; hh += 4) {
+    float mv[kMaxTiles / 32], lv[kMaxTiles / 32];
     float M = kNegInf;
-    for (int i = 0; i < n_tb; ++i) M = fmaxf(M, mm[i]);
+#pragma unroll
+    for (int i = 0; i < kMaxTiles / 32; ++i) {
+      const int tl = lane + 32 * i;
+      mv[i] = tl < n_tb ? red_m[hh * kMaxTiles + tl] : kNegInf;
+      lv[i] = tl < n_tb ? red_l[hh * kMaxTiles + tl] : 0.f;
+      M = fmaxf(M, mv[i]);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float Mu = M == kNegInf ? 0.f : M;
     float S = 0.f;
-    for (int i = 0; i < n_tb; ++i) S += ll[i] * ex2(mm[i] - Mu);
-    s_lse[threadIdx.x] = S > 0.f ? Mu + __log2f(S) : 0.f;
-  }
-  __syncthreads();
-  const int nb = (L + 63) / 64;
-  // per (tile, head) factor 2^(m_tile - lse) turns a tile's partials into probabilities
-  float* fac = sc + NPL * 32;  // [n_tb][R]
-  for (int i = threadIdx.x; i < R * n_tb; i += blockDim.x) {
-    const int hh = i / n_tb, tl = i % n_tb;
-    fac[tl * R + hh] = ex2(red_m[hh * kMaxTiles + tl] - s_lse[hh]);
-  }
-  __syncthreads();
-  const float* zr = p.z + row * p.n_tiles * 16 * R;
-  for (int j = threadIdx.x; j < NPL * 32; j += blockDim.x) {
-    float acc = 0.f;
-    const int c0 = 4 * j;
-    const int cnt = (c0 < n_c) + (c0 + 1 < n_c) + (c0 + 2 < n_c);
-    if (j < nb && j / 16 < n_tb) {
-      const float* zj = zr + (int64_t)j * R;  // tile j/16, block j%16
-      const float* fj = fac + (j / 16) * R;
 #pragma unroll
-      for (int hh = 0; hh < R; ++hh) acc += __ldcg(zj + hh) * fj[hh];
+    for (int i = 0; i < kMaxTiles / 32; ++i) S += lv[i] * ex2(mv[i] - Mu);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+    const float lse = S > 0.f ? Mu + __log2f(S) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxTiles / 32; ++i) {
+      const int tl = lane + 32 * i;
+      if (tl < n_tb) fac[tl * R + hh] = ex2(mv[i] - lse);
     }
-    sc[j] = cnt ? acc / (float)cnt : 0.f;
   }
   __syncthreads();
-  if (warp == 0) warp_topk<NPL, true>(sc, nb, (L - 1) / 64, p.n_init, p.n_local, p.k, p.idx + row * p.k, lane);
+  // pooled block scores: mean over the windows inside each block
+  for (int j0 = threadIdx.x; j0 < NPL * 32; j0 += 128 * ZB) {
+    if (j0 != (int)threadIdx.x) load_z(j0);  // only for the largest shapes
+#pragma unroll
+    for (int i = 0; i < ZB; ++i) {
+      const int j = j0 + 128 * i;
+      if (j >= NPL * 32) break;
+      const int c0 = 4 * j;
+      const int cnt = (c0 < n_c) + (c0 + 1 < n_c) + (c0 + 2 < n_c);
+      float acc = 0.f;
+      if (j < nb && j / 16 < n_tb) {
+        const float* fj = fac + (j / 16) * R;
+#pragma unroll
+        for (int hh = 0; hh < R; ++hh) acc += zreg[i][hh] * fj[hh];
+      }
+      sc[j] = cnt ? acc / (float)cnt : 0.f;
+    }
+  }
+  __syncthreads();
+  // the whole CTA runs the top-k: this tail sits on the critical path of the step
+  __shared__ int s_topk[3 * 4];
+  block_topk<NPL * 32 / 128, 128>(sc, nb, (L - 1) / 64, p.n_init, p.n_local, p.k, p.idx + row * p.k, s_topk);
 }
 
 template <int R, int NPL>

@@ -44,7 +44,7 @@ struct SparseParams {
 #endif
 
 #ifndef NSA_DECODE_NSTAGE
-#define NSA_DECODE_NSTAGE 2
+#define NSA_DECODE_NSTAGE 3  // 96 KB: two split CTAs per SM, two slices in flight per warp
 #endif
 
 template <int D, int BS, int NSTAGE, bool DECODE>

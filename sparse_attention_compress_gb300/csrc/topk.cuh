@@ -111,4 +111,87 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
   for (int p = total + lane; p < k; p += 32) out[p] = -1;
 }
 
+// The same selection spread over a whole CTA of NT threads (each owns E consecutive
+// blocks), for rows whose latency matters more than throughput: one barrier per search
+// step, with per-warp counts double buffered in shared memory.  scratch: 2*(NT/32)+NT/32
+// ints of shared memory.  Every thread of the CTA must call it.
+template <int E, int NT>
+__device__ __forceinline__ void block_topk(const float* row, int nb, int own, int n_init, int n_local, int k,
+                                           int32_t* out, int* scratch) {
+  constexpr int NWARP = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* s_cnt = scratch;              // [2][NWARP]
+  int* s_tot = scratch + 2 * NWARP;  // [NWARP]
+  uint32_t key[E];
+  bool valid[E];
+  const int j0 = tid * E;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int j = j0 + i;
+    valid[i] = j <= own && j < nb;
+    const bool forced = j < n_init || j > own - n_local;
+    key[i] = forced ? 0xffffffffu : order_key(valid[i] ? row[j] : 0.f);
+  }
+  const int ncand = min(own + 1, nb);
+  auto block_sum = [&](int c, int buf) {  // c summed over the CTA (one barrier)
+    c = (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
+    if (lane == 0) s_cnt[buf * NWARP + warp] = c;
+    __syncthreads();
+    int tot = 0;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) tot += s_cnt[buf * NWARP + w];
+    return tot;
+  };
+  uint32_t P = 0u;
+  int need = k;
+  if (ncand > k) {
+#pragma unroll 1
+    for (int b = 31; b >= 0; --b) {
+      const uint32_t trial = P | (1u << b);
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < E; ++i) c += (valid[i] && key[i] >= trial) ? 1 : 0;
+      if (block_sum(c, b & 1) >= k) P = trial;
+    }
+    int gt = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) gt += (valid[i] && key[i] > P) ? 1 : 0;
+    need = k - block_sum(gt, 1);  // buffer 1: its last readers passed the b = 0 barrier
+  }
+  // exclusive prefix over the CTA, in block order (threads own consecutive blocks)
+  auto block_scan = [&](int x) {
+    const int incl = warp_excl_scan(x, lane) + x;
+    __syncthreads();  // s_tot may still be read by a previous scan
+    if (lane == 31) s_tot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_tot[w];
+    return before + incl - x;
+  };
+  int tie = 0;
+#pragma unroll
+  for (int i = 0; i < E; ++i) tie += (ncand > k && valid[i] && key[i] == P) ? 1 : 0;
+  int rank = block_scan(tie);
+  bool sel[E];
+  int nsel = 0;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    if (ncand <= k) {
+      sel[i] = valid[i];
+    } else if (valid[i] && key[i] == P) {
+      sel[i] = rank < need;
+      ++rank;
+    } else {
+      sel[i] = valid[i] && key[i] > P;
+    }
+    nsel += sel[i] ? 1 : 0;
+  }
+  int pos = block_scan(nsel);
+#pragma unroll
+  for (int i = 0; i < E; ++i)
+    if (sel[i]) out[pos++] = j0 + i;
+  const int total = min(k, ncand);
+  for (int q = total + tid; q < k; q += NT) out[q] = -1;
+}
+
 }  // namespace nsa
