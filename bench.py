@@ -33,6 +33,10 @@ from sparse_attention_compress_gb300 import inputs as gen  # noqa: E402
 from sparse_attention_compress_gb300.dist import max_over_ranks  # noqa: E402
 
 METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roofline"
+# DRAM bytes (read + write) of one prefill launch from the ncu capture summarised in
+# profiles/sparse_fwd_mma_prefill_b2.md: 248.7 MB at B=2, x4 for the B=8 launch (the
+# traffic grows with the number of query tokens)
+PREFILL_NCU_TRAFFIC = 4 * (153.18e6 + 95.53e6)
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -227,8 +231,10 @@ def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
     cgbs = cbytes / (float(np.mean(msc)) * 1e-3) / 1e9
     return {"workload": "decode B=32 L=32768 H=16 Hkv=2 d=128 bf16 top-k 64 (blocks of 64)",
             "ms_per_step": ms_step, "kv_gbs": gbs, "tokens_per_s": w.batch / (ms_step * 1e-3),
-            "bytes_per_step": int(byts), "hbm_frac": gbs / peaks["hbm_gbs"], "launches_per_step": 4,
-            "cuda_graph": True,
+            "bytes_per_step": int(byts), "hbm_frac": gbs / peaks["hbm_gbs"],
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy"},
+            "launches_per_step": 2, "memsets_per_step": 1, "cuda_graph": True,
             "compress_cache": {"ms": float(np.mean(msc)), "gbs": cgbs, "hbm_frac": cgbs / peaks["hbm_gbs"],
                                "bytes": int(cbytes)}}
 
@@ -260,8 +266,8 @@ def bench_selection(torch, nsa, device, steps, warmup, flush):
             "launches_per_step": 3}
 
 
-def bench_layer(torch, nsa, device, steps, warmup, flush):
-    w = gen.layer()
+def bench_layer(torch, nsa, device, steps, warmup, flush, T=65536):
+    w = gen.layer(T=T)
     q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
     gates = dev(torch, w.gates, device)
     shp = nsa.make_shape(w.tokens, w.h, w.hkv, w.d, 1, batch=1, seqlen=w.tokens)
@@ -279,7 +285,7 @@ def bench_layer(torch, nsa, device, steps, warmup, flush):
     sel = np.where(ih >= 0, np.clip(t[:, None, None] - ih * 64 + 1, 0, 64), 0).sum()
     r = w.h // w.hkv
     flops = 4 * w.d * (ncaus.sum() * w.h + float(sel) * r + np.minimum(t + 1, 512).sum() * w.h)
-    return {"workload": "layer B=1 T=65536 H=64 Hkv=4 d=128 bf16 (compressed 32/16 + selected 64x16 + window 512 "
+    return {"workload": f"layer B=1 T={w.tokens} H=64 Hkv=4 d=128 bf16 (compressed 32/16 + selected 64x16 + window 512 "
                         "+ sigmoid gates)",
             "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": w.tokens / (ms * 1e-3),
             "flops_per_step": flops, "launches_per_step": 8}
@@ -295,6 +301,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
+    ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
     ap.add_argument("--only", default="", choices=["", "prefill", "decode", "selection", "layer"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
@@ -329,7 +336,8 @@ def main():
     if args.only in ("decode", "selection", "layer"):
         fn = {"decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
-              "layer": lambda: bench_layer(torch, nsa, device, args.steps, args.warmup, flush)}[args.only]
+              "layer": lambda: bench_layer(torch, nsa, device, args.steps, args.warmup, flush,
+                                           args.layer_tokens)}[args.only]
         print(json.dumps({"only": args.only, **fn()}), flush=True)
         return
 
@@ -351,6 +359,8 @@ def main():
     ms_step = max_over_ranks(ms_step, device)
     value = flops * world / (ms_step * 1e-3) / 1e12
     kernel_tflops = flops / (ms_step * 1e-3) / 1e12
+    # K and V rows each attended (token, kv-head) pulls from L2 (2 * d bf16 per key)
+    gathered = flops / (w.h // w.hkv) / (4 * w.d) * (2 * w.d * 2)
     if args.only == "prefill":
         print(json.dumps({"only": "prefill", "batch": w.batch, "ms_per_step": ms_step, "tflops": kernel_tflops}),
               flush=True)
@@ -383,9 +393,11 @@ def main():
                    "seq_len": 16384, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (258 MB written, then 258 MB copied; outside the event pair)",
                    "flops_per_step": flops},
-        "roofline": {"kernel": "sparse_fwd_mma<128,64,3>", "bound": "tensor", "achieved": kernel_tflops,
+        "roofline": {"kernel": "sparse_fwd_mma<128,64,2>", "bound": "tensor", "achieved": kernel_tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
-                     "peak_source": peaks["source"] + " bf16 dense (cuBLAS burst)", "traffic": None},
+                     "peak_source": peaks["source"] + " bf16 dense (cuBLAS burst)",
+                     "traffic": PREFILL_NCU_TRAFFIC if args.batch == 8 else None,
+                     "gathered_bytes": gathered, "gather_gbs": gathered / (ms_step * 1e-3) / 1e9},
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps + e2e_steps,
@@ -398,7 +410,7 @@ def main():
         torch.cuda.empty_cache()
         try:
             line["decode"] = bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks)
-            line["gpu_launches"] += 4 * args.steps + args.steps
+            line["gpu_launches"] += 2 * args.steps + args.steps
         except Exception as e:  # report, never hide
             line["decode"] = {"error": repr(e)}
         torch.cuda.empty_cache()
@@ -414,6 +426,21 @@ def main():
         except Exception as e:
             line["layer"] = {"error": repr(e)}
 
+    if rank == 0 and world == 1 and not args.no_extras:
+        try:  # live ceilings of this GPU for the secondary rooflines
+            from sparse_attention_compress_gb300 import probe
+            pr = probe.run()
+            line["probes"] = pr
+            rf = line["roofline"]
+            rf["l2_read_peak_gbs"] = pr["l2_read_gbs"]
+            rf["gather_frac_of_l2"] = rf["gather_gbs"] / pr["l2_read_gbs"]
+            rf["mma_sync_peak_tflops"] = pr["mma_sync_bf16_tflops"]
+            rf["frac_of_mma_sync"] = kernel_tflops / pr["mma_sync_bf16_tflops"]
+            if "tflops" in line.get("layer", {}):
+                line["layer"]["frac_of_mma_sync"] = line["layer"]["tflops"] / pr["mma_sync_bf16_tflops"]
+                line["layer"]["frac_of_bf16_peak"] = line["layer"]["tflops"] / peaks["bf16_tflops"]
+        except Exception as e:
+            line["probes"] = {"error": repr(e)}
     if rank == 0 and world == 1:
         n_rows = args.cpu_sample_rows
         if n_rows <= 0:  # size the sample to ~15 s of oracle work

@@ -1,0 +1,121 @@
+// Micro-benchmarks of the ceilings that bound the hot path on this GPU, printed as one
+// JSON object: L2-resident read bandwidth (the gather of selected K/V blocks is served
+// from L2), HBM read bandwidth, the legacy mma.sync.m16n8k16 bf16 rate (the MMA the
+// selected-attention kernels use) and the ex2.approx rate (softmax exponentials).
+// Standalone program; no part of the library.
+#include <cstdint>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+__global__ void read_kernel(const uint4* __restrict__ p, size_t n, int iters, unsigned* out) {
+  unsigned acc = 0;
+  const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x, stride = (size_t)gridDim.x * blockDim.x;
+  for (int it = 0; it < iters; ++it)
+    for (size_t i = tid; i < n; i += stride) {
+      const uint4 v = __ldcg(p + i);
+      acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+  out[tid] = acc;
+}
+
+__device__ __forceinline__ void mma(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void mma_kernel(float* out, int iters) {
+  const uint32_t a[4] = {0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u};
+  const uint32_t b = 0x3c003c00u;
+  float c[8][4] = {};
+  for (int i = 0; i < iters; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mma(c[j], a, b, b);
+  float s = 0.f;
+  for (int j = 0; j < 8; ++j)
+    for (int q = 0; q < 4; ++q) s += c[j][q];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+__global__ void ex2_kernel(float* out, int iters) {
+  float x[8];
+  for (int j = 0; j < 8; ++j) x[j] = -0.001f * (threadIdx.x + j);
+  for (int i = 0; i < iters; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float y;
+      asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x[j]));
+      x[j] = y - 1.0f;
+    }
+  float s = 0.f;
+  for (int j = 0; j < 8; ++j) s += x[j];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+static float timed_ms(void (*launch)(void*), void* arg) {
+  cudaEvent_t a, b;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  launch(arg);  // warm-up
+  cudaDeviceSynchronize();
+  cudaEventRecord(a);
+  launch(arg);
+  cudaEventRecord(b);
+  cudaEventSynchronize(b);
+  float ms = 0.f;
+  cudaEventElapsedTime(&ms, a, b);
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  return ms;
+}
+
+struct ReadArg { const uint4* p; size_t n; int iters; unsigned* out; int grid; };
+static void launch_read(void* v) {
+  ReadArg* r = static_cast<ReadArg*>(v);
+  read_kernel<<<r->grid, 256>>>(r->p, r->n, r->iters, r->out);
+}
+struct ComputeArg { float* out; int iters; int grid; bool mma; };
+static void launch_compute(void* v) {
+  ComputeArg* c = static_cast<ComputeArg*>(v);
+  if (c->mma) mma_kernel<<<c->grid, 256>>>(c->out, c->iters);
+  else ex2_kernel<<<c->grid, 256>>>(c->out, c->iters);
+}
+
+int main() {
+  int sms = 0, clk_khz = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+  cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, 0);
+  const int grid = sms * 8;
+  unsigned* out = nullptr;
+  cudaMalloc(&out, (size_t)grid * 256 * 4);
+  double bw[2] = {0, 0};
+  const size_t mbs[2] = {64, 4096};  // L2-resident and HBM-sized buffers
+  for (int t = 0; t < 2; ++t) {
+    const size_t n = mbs[t] * (1u << 20) / 16;
+    uint4* p = nullptr;
+    if (cudaMalloc(&p, n * 16) != cudaSuccess) { printf("{\"error\": \"allocation\"}\n"); return 1; }
+    cudaMemset(p, 1, n * 16);
+    ReadArg r{p, n, t == 0 ? 20 : 2, out, grid};
+    const float ms = timed_ms(launch_read, &r);
+    bw[t] = (double)n * 16 * r.iters / (ms * 1e-3) / 1e9;
+    cudaFree(p);
+  }
+  float* fo = nullptr;
+  cudaMalloc(&fo, (size_t)sms * 4 * 256 * 4);
+  ComputeArg cm{fo, 4096, sms * 4, true};
+  const float ms_mma = timed_ms(launch_compute, &cm);
+  const double mma_tf = (double)cm.grid * 256 / 32 * cm.iters * 8 * 4096 / (ms_mma * 1e-3) / 1e12;
+  ComputeArg ce{fo, 4096, sms * 4, false};
+  const float ms_ex2 = timed_ms(launch_compute, &ce);
+  const double ex2_rate = (double)ce.grid * 256 * ce.iters * 8 / (ms_ex2 * 1e-3);
+  const cudaError_t e = cudaGetLastError();
+  printf("{\"l2_read_gbs\": %.1f, \"hbm_read_gbs\": %.1f, \"mma_sync_bf16_tflops\": %.1f, "
+         "\"ex2_per_sm_per_clk\": %.2f, \"sms\": %d, \"clock_mhz\": %.0f, \"error\": \"%s\"}\n",
+         bw[0], bw[1], mma_tf, ex2_rate / sms / (clk_khz * 1e3), sms, clk_khz / 1e3,
+         e == cudaSuccess ? "" : cudaGetErrorString(e));
+  cudaFree(out);
+  cudaFree(fo);
+  return e == cudaSuccess ? 0 : 1;
+}
