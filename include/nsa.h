@@ -52,7 +52,7 @@ typedef enum {
   NSA_ERR_INVALID = 1,     /* null/misaligned pointer, inconsistent sizes            */
   NSA_ERR_UNSUPPORTED = 2, /* valid arguments outside the shapes the kernels cover   */
   NSA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                   */
-  NSA_ERR_TIMEOUT = 4      /* reserved for device-side bounded waits                  */
+  NSA_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (nsa_device_status)  */
 } nsa_status;
 
 typedef enum { NSA_F32 = 0, NSA_BF16 = 1 } nsa_dtype;
@@ -72,6 +72,17 @@ NSA_API const char* nsa_version(void);
 
 /* Message of the last failed call made by this thread ("" if none). */
 NSA_API const char* nsa_last_error(void);
+
+/* Device status word of the current device.  Kernels that wait on the tensor-core
+ * pipeline (the tcgen05 branches of nsa_layer_fwd) bound every wait to about a second;
+ * when one runs out the kernel sets the word to NSA_ERR_TIMEOUT, skips its output and
+ * releases its tensor memory, so the context stays usable.  Runtime error reporting,
+ * with no counterpart in the pages.
+ *   status  host int32 out: NSA_OK or NSA_ERR_TIMEOUT
+ *   reset   nonzero: clear the word after reading it
+ * Blocks until the device is idle (a synchronous copy).  Returns NSA_ERR_INVALID for a
+ * NULL status, NSA_ERR_CUDA when the copy fails. */
+NSA_API nsa_status nsa_device_status(int32_t* status, int reset);
 
 /* S1 -- key (or value) compression.  [NOSA-Parts] core component 1: keys are cut into
  * windows of `kernel` tokens at step `stride` and each window is mean-pooled;

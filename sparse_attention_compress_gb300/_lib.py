@@ -29,6 +29,7 @@ class NsaShape(ctypes.Structure):
 _SIGS = {
     "nsa_version": ([], ctypes.c_char_p),
     "nsa_last_error": ([], ctypes.c_char_p),
+    "nsa_device_status": ([_c_p, _c_int], _c_int),
     "nsa_compress_k": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_p], _c_int),
     "nsa_cmp_scores_pool": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_int, _c_p], _c_int),
     "nsa_topk_select": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
@@ -262,6 +263,13 @@ def nsa_sparse_decode_noalloc(q, k_cache, v_cache, k_cmp_cache, seqlens, k=64, k
                                             n_local, k, float(scale), _ptr(idx_out), _ptr(out), _stream(stream)),
            "nsa_sparse_decode_noalloc")
     return out
+
+
+def nsa_device_status(reset: bool = False) -> int:
+    """Device status word (0 or NSA_ERR_TIMEOUT = 4); synchronises the device."""
+    st = ctypes.c_int32(0)
+    _check(load().nsa_device_status(ctypes.byref(st), int(bool(reset))), "nsa_device_status")
+    return int(st.value)
 
 
 def nsa_layer_fwd_workspace_size(shape: NsaShape, kernel=32, stride=16, block_size=64, S=16) -> int:

@@ -88,6 +88,11 @@ const char* nsa_version(void) { return "nsa-gb300 0.1 (sm_103a)"; }
 
 const char* nsa_last_error(void) { return g_err; }
 
+nsa_status nsa_device_status(int32_t* status, int reset) {
+  NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
+  return cuda_status(read_device_status(status, reset != 0), "nsa_device_status");
+}
+
 nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,
                           cudaStream_t stream) {
   Seqs s;
@@ -306,10 +311,13 @@ nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int
   return cuda_status(launch_decode(a, stream), "nsa_sparse_decode");
 }
 
-// Layer workspace: compressed K and V, the compressed and sliding branch outputs, the
-// compressed normaliser, the block scores and (when idx_out is NULL) the block lists.
+// Layer workspace: compressed K and V, V^T of the compressed and of the full values
+// (K-major operands of the tensor-core branches), the compressed and sliding branch
+// outputs, the compressed normaliser, the block scores and (when idx_out is NULL) the
+// block lists.
 struct LayerLayout {
-  size_t kc, vc, o_cmp, o_swa, lse, scores, idx, total;
+  size_t kc, vc, vtc, vt, o_cmp, o_swa, lse, scores, idx, total;
+  int64_t ncr;
   int nb_stride;
 };
 
@@ -325,6 +333,11 @@ static LayerLayout layer_layout(const Seqs& s, int h, int hkv, int d, int esz, i
   off = align256(off + (size_t)ncr * hkv * d * esz);
   l.vc = off;
   off = align256(off + (size_t)ncr * hkv * d * esz);
+  l.ncr = ncr;
+  l.vtc = off;
+  off = align256(off + (size_t)tc_vt_pad(ncr) * hkv * d * esz);
+  l.vt = off;
+  off = align256(off + (size_t)tc_vt_pad(s.tokens) * hkv * d * esz);
   l.o_cmp = off;
   off = align256(off + (size_t)s.tokens * h * d * esz);
   l.o_swa = off;
@@ -385,8 +398,19 @@ nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, c
   cudaError_t e;
   if ((e = launch_compress(s, k, kc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "nsa_layer_fwd/compress k");
   if ((e = launch_compress(s, v, vc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "nsa_layer_fwd/compress v");
-  if ((e = launch_dense_attn(0, s, q, kc, vc, h, hkv, d, kernel, stride, 0, scale, o_cmp, lse, stream)))
-    return cuda_status(e, "nsa_layer_fwd/compressed branch");
+  const bool tc = d == 128;
+  void* vtc = w + l.vtc;
+  void* vt = w + l.vt;
+  if (tc) {
+    if ((e = launch_transpose_v(s, vc, vtc, l.ncr, hkv, true, kernel, stride, stream)))
+      return cuda_status(e, "nsa_layer_fwd/transpose compressed v");
+    if ((e = launch_transpose_v(s, v, vt, s.tokens, hkv, false, kernel, stride, stream)))
+      return cuda_status(e, "nsa_layer_fwd/transpose v");
+    e = launch_dense_attn_tc(0, s, q, kc, vtc, l.ncr, h, hkv, kernel, stride, 0, scale, o_cmp, lse, stream);
+  } else {
+    e = launch_dense_attn(0, s, q, kc, vc, h, hkv, d, kernel, stride, 0, scale, o_cmp, lse, stream);
+  }
+  if (e) return cuda_status(e, "nsa_layer_fwd/compressed branch");
   if ((e = launch_scores_pool(s, q, kc, h, hkv, d, scale, lse, scores, l.nb_stride, stream)))
     return cuda_status(e, "nsa_layer_fwd/block scores");
   if ((e = launch_topk(s, scores, l.nb_stride, hkv, block_size, n_init, n_local, S, idx, stream)))
@@ -394,8 +418,10 @@ nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, c
   // the selected branch writes straight into o; the gated sum then runs in place
   if ((e = launch_sparse_fwd(s, q, k, v, idx, S, block_size, h, hkv, d, kBF16, scale, o, nullptr, stream)))
     return cuda_status(e, "nsa_layer_fwd/selected branch");
-  if ((e = launch_dense_attn(1, s, q, k, v, h, hkv, d, kernel, stride, window, scale, o_swa, nullptr, stream)))
-    return cuda_status(e, "nsa_layer_fwd/sliding branch");
+  e = tc ? launch_dense_attn_tc(1, s, q, k, vt, s.tokens, h, hkv, kernel, stride, window, scale, o_swa, nullptr,
+                                 stream)
+         : launch_dense_attn(1, s, q, k, v, h, hkv, d, kernel, stride, window, scale, o_swa, nullptr, stream);
+  if (e) return cuda_status(e, "nsa_layer_fwd/sliding branch");
   return cuda_status(launch_gate_combine(s.tokens, h, d, o_cmp, o, o_swa, gate_logits, o, stream),
                      "nsa_layer_fwd/gate combine");
 }

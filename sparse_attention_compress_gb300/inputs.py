@@ -193,12 +193,17 @@ def decode(B: int = 32, L: int = 32768, H: int = 16, HKV: int = 2, D: int = 128,
     return DecodeWorkload(q, kc, vc, sl, H, HKV, D, topk=topk)
 
 
-def layer(T: int = 65536, H: int = 64, HKV: int = 4, D: int = 128, B: int = 1) -> Workload:
-    """Three-branch layer: bf16 Q/K/V N(0,1) and fp32 N(0,1) gate logits [T, H, 3]."""
-    rng = rng_for(4)
-    q = normal(rng, (B * T, H, D), "bf16")
-    k = normal(rng, (B * T, HKV, D), "bf16")
-    v = normal(rng, (B * T, HKV, D), "bf16")
-    gates = rng.standard_normal(size=(B * T, H, 3), dtype=np.float32)
-    return Workload("layer", "bf16", dense_cu_seqlens(B, T), H, HKV, D, q, k, v, S=16, gates=gates,
-                    batch=B, seqlen=T)
+def layer(T: int = 65536, H: int = 64, HKV: int = 4, D: int = 128, B: int = 1, lengths=None) -> Workload:
+    """Three-branch layer: bf16 Q/K/V N(0,1) and fp32 N(0,1) gate logits [tokens, H, 3].
+
+    lengths: packed varlen sequences (cu_seqlens) instead of B dense sequences of T tokens."""
+    rng = rng_for(4, 0 if lengths is None else 1)
+    cu = dense_cu_seqlens(B, T) if lengths is None else varlen_cu_seqlens(lengths)
+    n = int(cu[-1])
+    q = normal(rng, (n, H, D), "bf16")
+    k = normal(rng, (n, HKV, D), "bf16")
+    v = normal(rng, (n, HKV, D), "bf16")
+    gates = rng.standard_normal(size=(n, H, 3), dtype=np.float32)
+    if lengths is None:
+        return Workload("layer", "bf16", cu, H, HKV, D, q, k, v, S=16, gates=gates, batch=B, seqlen=T)
+    return Workload("layer", "bf16", cu, H, HKV, D, q, k, v, S=16, gates=gates)

@@ -278,7 +278,7 @@ def test_selection_varlen_end_to_end():
     assert np.array_equal(host(idx), orc.topk(host(sc), w.cu_seqlens, k=16))
 
 
-@pytest.mark.parametrize("T,H,hkv", [(1500, 32, 2), (700, 16, 1)])
+@pytest.mark.parametrize("T,H,hkv", [(1500, 32, 2), (700, 16, 1), (1100, 16, 2), (900, 8, 2), (333, 4, 4)])
 def test_layer_small(T, H, hkv):
     w = gen.layer(T=T, H=H, HKV=hkv)
     idx = torch.empty((T, hkv, 16), dtype=torch.int32, device="cuda")
@@ -291,6 +291,27 @@ def test_layer_small(T, H, hkv):
     n_mis, outside = selection_mismatches(gi, ref["idx"], ref_sc, _t_of_rows(w.cu_seqlens))
     assert outside == 0, (n_mis, outside)
     assert_close(out, ref["o"], what="layer")
+
+
+def test_layer_varlen():
+    """Packed sequences of ragged lengths (shorter than one compression window, one
+    selection block, one sliding window, and longer): every tile of the tensor-core
+    branches may mix keys of two sequences, which the masks must exclude."""
+    lengths = [700, 65, 1300, 31, 200, 513]
+    w = gen.layer(H=32, HKV=2, lengths=lengths)
+    dcu = dev(w.cu_seqlens)
+    idx = torch.empty((w.tokens, 2, 16), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_layer_fwd(dev(w.q), dev(w.k), dev(w.v), dev(w.gates), cu_seqlens=dcu, max_seqlen=max(lengths),
+                            idx_out=idx)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    gi = host(idx)
+    ref = orc.layer(w.q, w.k, w.v, w.gates, w.cu_seqlens, idx_in=gi)
+    _, kc = orc.compress(w.k, w.cu_seqlens)
+    ref_sc = orc.cmp_scores_pool(w.q, kc, w.cu_seqlens)
+    n_mis, outside = selection_mismatches(gi, ref["idx"], ref_sc, _t_of_rows(w.cu_seqlens))
+    assert outside == 0, (n_mis, outside)
+    assert_close(out, ref["o"], what="layer varlen")
 
 
 def test_layer_full_size_sampled():
