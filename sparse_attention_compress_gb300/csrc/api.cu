@@ -406,20 +406,23 @@ nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, c
       return cuda_status(e, "nsa_layer_fwd/transpose compressed v");
     if ((e = launch_transpose_v(s, v, vt, s.tokens, hkv, false, kernel, stride, stream)))
       return cuda_status(e, "nsa_layer_fwd/transpose v");
-    e = launch_dense_attn_tc(0, s, q, kc, vtc, l.ncr, h, hkv, kernel, stride, 0, scale, o_cmp, lse, stream);
+    // the compressed branch also writes the block scores (second pass over its keys)
+    e = launch_dense_attn_tc(0, s, q, kc, vtc, l.ncr, h, hkv, kernel, stride, 0, scale, o_cmp, nullptr, scores,
+                             l.nb_stride, stream);
+    if (e) return cuda_status(e, "nsa_layer_fwd/compressed branch and block scores");
   } else {
     e = launch_dense_attn(0, s, q, kc, vc, h, hkv, d, kernel, stride, 0, scale, o_cmp, lse, stream);
+    if (e) return cuda_status(e, "nsa_layer_fwd/compressed branch");
+    if ((e = launch_scores_pool(s, q, kc, h, hkv, d, scale, lse, scores, l.nb_stride, stream)))
+      return cuda_status(e, "nsa_layer_fwd/block scores");
   }
-  if (e) return cuda_status(e, "nsa_layer_fwd/compressed branch");
-  if ((e = launch_scores_pool(s, q, kc, h, hkv, d, scale, lse, scores, l.nb_stride, stream)))
-    return cuda_status(e, "nsa_layer_fwd/block scores");
   if ((e = launch_topk(s, scores, l.nb_stride, hkv, block_size, n_init, n_local, S, idx, stream)))
     return cuda_status(e, "nsa_layer_fwd/top-k");
   // the selected branch writes straight into o; the gated sum then runs in place
   if ((e = launch_sparse_fwd(s, q, k, v, idx, S, block_size, h, hkv, d, kBF16, scale, o, nullptr, stream)))
     return cuda_status(e, "nsa_layer_fwd/selected branch");
   e = tc ? launch_dense_attn_tc(1, s, q, k, vt, s.tokens, h, hkv, kernel, stride, window, scale, o_swa, nullptr,
-                                 stream)
+                                 nullptr, 0, stream)
          : launch_dense_attn(1, s, q, k, v, h, hkv, d, kernel, stride, window, scale, o_swa, nullptr, stream);
   if (e) return cuda_status(e, "nsa_layer_fwd/sliding branch");
   return cuda_status(launch_gate_combine(s.tokens, h, d, o_cmp, o, o_swa, gate_logits, o, stream),

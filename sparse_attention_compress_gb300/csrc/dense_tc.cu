@@ -1,23 +1,34 @@
-// Compressed and sliding-window branches on the 5th-generation tensor cores.
+// Compressed and sliding-window branches on the 5th-generation tensor cores, and the
+// block scores of the selection (fused into the compressed branch).
 //
 // [NSA-Triton] "DeepSeek NSA ... with Triton", sec. 1.1: the compressed branch attends
 // to the mean-pooled keys/values, the sliding branch to the most recent tokens; both
-// are dense attention over a contiguous key range per query.
+// are dense attention over a contiguous key range per query.  [NOSA-Triton] mechanisms
+// 2 and 3: the selection scores are the compressed attention probabilities, summed over
+// the heads of a kv-group and mean-pooled over the compressed windows inside each
+// 64-token block.
 //
 // GB300 design.  A CTA takes 128 (token, head) rows of one kv-group (8 tokens x 16 heads
-// at the layer's group size): they share every K/V tile, so the contraction is a real
-// M=128 GEMM.  Per 64-key tile:
-//   S[128 x 64]  = Q K^T  : tcgen05.mma kind::f16, A = Q tile, B = K tile, both K-major
-//                           in 128B-swizzled shared memory, D in TMEM (columns 0..63);
-//   softmax      : thread i owns row i (TMEM lane i): tcgen05.ld of its 64 scores, mask,
-//                  running max with lazy rescale, base-2 exponentials, P (bf16) written
-//                  in the 128B-swizzled layout over the K tile it no longer needs;
-//   O[128 x 128] += P V   : tcgen05.mma, A = P, B = V^T tile (V transposed once per call
-//                           so that this operand is K-major too), D in TMEM (cols 128..255).
-// cp.async double-buffers the K / V^T tiles; tcgen05.commit signals mbarriers whose
-// waits are bounded (a timeout sets the library's device status and the CTA leaves after
-// draining its copies and freeing its TMEM).  Two CTAs share an SM (96 KB shared memory,
-// 256 TMEM columns each), so one CTA's softmax overlaps the other's MMAs.
+// at group size 16): they share every K/V tile, so the contraction is an M = 128 GEMM.
+// Warp roles (192 threads):
+//   warp 4      TMA producer: Q once (a 3-D box of tokens x heads x d), then 64-key K
+//               tiles and V^T tiles through 2-stage rings (128B-swizzled, K-major);
+//   warp 5      MMA issuer (one lane): S(j) = Q K(j)^T into one of two TMEM S buffers,
+//               issued while the softmax of tile j-1 runs, then O += P(j-1) V(j-1) with
+//               P read from TMEM;
+//   warps 0..3  softmax, one row per thread (TMEM lane = row): mask, running max with
+//               lazy rescale, base-2 exponentials, P (bf16) stored over its S buffer.
+// Pass 2 (compressed branch with block scores): the issuer recomputes S over 64-key
+// tiles aligned to the sequence's compressed index, so each tile holds 16 whole
+// selection blocks; the softmax warps turn the scores into probabilities with the final
+// normaliser, pool the three windows of each block, sum the group's heads with a
+// reduce-scatter over lanes and write one fp32 score per (token, kv-head, block).
+// Every mbarrier wait is bounded (about one second; a timeout sets the device status,
+// makes the other roles leave their loops, drains the copies and MMAs in flight and
+// frees the tensor memory).  Two CTAs share an SM (97 KB shared memory and 256 TMEM
+// columns each).
+#include <cuda.h>
+
 #include "nsa.h"
 #include "launch.h"
 
@@ -29,27 +40,41 @@ namespace tc {
 
 constexpr int D = 128;
 constexpr int ROWS = 128;  // query rows per CTA (= tcgen05 M)
-constexpr int KT = 64;     // keys per tile (= N of S, K of PV)
-constexpr int Q_BYTES = ROWS * D * 2;         // 32 KB: two 64-column halves
-constexpr int K_BYTES = KT * D * 2;           // 16 KB: two halves; reused for P (128 x 64)
-constexpr int V_BYTES = D * KT * 2;           // 16 KB: V^T tile, 128 rows of 64 keys
-constexpr int SMEM_BYTES = Q_BYTES + 2 * K_BYTES + 2 * V_BYTES + 1024;  // + alignment
-constexpr int TMEM_COLS = 256;  // S: 0..63, O: 128..255
-constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s: an mbarrier wait longer than this is stuck
+constexpr int KT = 64;     // keys per tile
+constexpr int NS = 2;      // K / V^T ring stages
+constexpr int NTHREADS = 192;
+constexpr int Q_BYTES = ROWS * D * 2;  // two 64-column halves of 16 KB
+constexpr int K_BYTES = KT * D * 2;    // two halves of 8 KB
+constexpr int V_BYTES = D * KT * 2;    // V^T tile: 128 d-rows of 64 keys
+constexpr int SMEM_BYTES = Q_BYTES + NS * (K_BYTES + V_BYTES) + 1024;  // + 1 KB for alignment
+constexpr int TMEM_COLS = 256;  // S buffers at columns 0 and 64 (P over their first 32), O at 128
+constexpr uint32_t O_COL = 128;
+constexpr unsigned long long kWaitNs = 1000000000ull;  // an mbarrier wait longer than 1 s is stuck
 
-// 128B-swizzled K-major tile of R rows x 64 bf16: row r, 16-byte chunk c at
-// base + r*128 + ((c ^ (r & 7)) << 4); 8-row atoms of 1024 bytes.
-__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int chunk) {
-  return base + row * 128 + ((chunk ^ (row & 7)) << 4);
-}
+// barrier slots
+enum {
+  B_Q = 0,
+  B_KFULL = 1,
+  B_KEMPTY = B_KFULL + NS,
+  B_VFULL = B_KEMPTY + NS,
+  B_VEMPTY = B_VFULL + NS,
+  B_SFULL = B_VEMPTY + NS,  // [2] S(j) computed, indexed by j & 1
+  B_SFREE = B_SFULL + 2,    // [2] pass 2: softmax has read S(j)
+  B_PFULL = B_SFREE + 2,    // [2] softmax wrote P(j)
+  B_ODONE = B_PFULL + 2,    // [2] PV(j) finished
+  B_DRAIN = B_ODONE + 2,
+  NBARS
+};
 
-// Shared-memory matrix descriptor: 128B swizzle, K-major, 1024-byte atom stride.
+// Shared-memory matrix descriptor of a K-major tile of rows x 64 bf16 in the layout TMA
+// writes with 128-byte swizzling (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4),
+// 1024-byte atoms of 8 rows).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
-  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
-  d |= (uint64_t)1 << 46;              // descriptor version
-  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;            // descriptor version
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
   return d;
 }
 
@@ -58,11 +83,20 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t accum) {
+// D[tmem] (+)= A[smem] * B[smem]^T
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t accum) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(accum)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t accum) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accum)
       : "memory");
 }
 __device__ __forceinline__ void commit(uint32_t bar) {
@@ -71,10 +105,15 @@ __device__ __forceinline__ void commit(uint32_t bar) {
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -87,23 +126,45 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
   return t;
 }
-// Wait for phase `parity` of an mbarrier for at most kWaitNs; false (and the device
-// status set to NSA_ERR_TIMEOUT) when the limit ran out.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier.  Gives up (false) when *abort is set by
+// another role, or after kWaitNs, in which case it sets *abort and the device status.
+// abort == nullptr: time limit only (used while draining).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
   const unsigned long long t0 = globaltimer();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 32; ++i)
       if (mbar_try(bar, parity)) return true;
+    if (abort && *abort) return false;
     if (globaltimer() - t0 > kWaitNs) break;
   }
+  if (abort) *abort = 1;
   atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
   return false;
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity);
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort);
+}
+// Warp-uniform wait: every lane waits, the result is the AND over the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+__device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 // 32 consecutive TMEM columns of this thread's lane.
@@ -120,8 +181,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
-  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
@@ -133,29 +193,60 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
+// Reduce-scatter of 16 values over the R lanes of a group (R | 32, the lanes of a group
+// contiguous): afterwards lane hd = lane % R holds in v[0 .. 16/R) the group sums of
+// entries hd*(16/R) .. hd*(16/R) + 16/R - 1.
+template <int R>
+__device__ __forceinline__ void group_reduce_scatter(float (&v)[16], int lane) {
+#pragma unroll
+  for (int s = 0; (1 << s) < R; ++s) {
+    const int off = R >> (s + 1), half = 8 >> s;
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+}
+
 struct Params {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;   // [kv_rows, hkv, D]
-  const __nv_bfloat16* vt;  // [hkv, D, kv_pad]: V transposed, zero past kv_rows
   __nv_bfloat16* o;
-  float* lse;
+  float* lse;     // optional natural-log normaliser per (token, head)
+  float* scores;  // MODE 0 with fused block scores: [tokens, hkv, nb_stride]
   Seqs seqs;
-  int h, hkv, R, kernel, stride, window;
-  int64_t kv_rows, kv_pad;
+  int h, hkv, R, kernel, stride, window, nb_stride;
   float scale_log2;
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(128, 2) attn_kernel(const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2];  // 0: S tile ready, 1: O update done
-  __shared__ uint32_t tmem_holder;
-  const uint32_t base = (smem_u32(smem_raw) + 1023) & ~1023u;  // 128B-swizzle atoms need 1 KB alignment
-  const uint32_t q_s = base, k_s = base + Q_BYTES, v_s = k_s + 2 * K_BYTES;
-  const uint32_t bar_s = smem_u32(&bars[0]), bar_o = smem_u32(&bars[1]);
-  const int tid = threadIdx.x, warp = tid >> 5;
+// Index of the last of items 0..last that went to ring stage st (-1 if none).
+__device__ __forceinline__ int last_in_stage(int last, int st) {
+  if (last < st) return -1;
+  return last - (last - st) % NS;
+}
 
-  const int R = p.R;
+// MODE 0: compressed branch (RS = group size when the block scores are fused, else 0);
+// MODE 1: sliding window (RS = 0).
+template <int MODE, int RS>
+__global__ void __launch_bounds__(NTHREADS, 2)
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_vt, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[NBARS];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int s_abort;
+  const uint32_t base = (smem_u32(smem_raw) + 1023) & ~1023u;  // swizzle atoms need 1 KB alignment
+  const uint32_t q_s = base, k_s = base + Q_BYTES, v_s = k_s + NS * K_BYTES;
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  volatile int* abort = &s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // after a timeout anywhere on the device, later CTAs leave at once (the caller reads
+  // the status word; the outputs of this launch are not valid)
+  if (*reinterpret_cast<volatile int*>(&g_device_status) != 0) return;
+  const int R = RS > 0 ? RS : p.R;
   const int TPC = ROWS / R;  // tokens per CTA
   const int sq = blockIdx.y, g = blockIdx.z;
   const int L = seq_len(p.seqs, sq);
@@ -176,28 +267,28 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const Params p) {
     key_lo = max(0, t0 - p.window + 1);
     key_hi = t_last + 1;
   }
-  // 64-key tiles in absolute key rows, so every V^T tile starts 128-byte aligned
+  // pass 1: 64-key tiles in absolute key rows (64-aligned, so every V^T tile starts on a
+  // 128-byte boundary); pass 2: tiles at kv0 + 64 i (16 whole selection blocks each)
   const int64_t a_lo = (kv0 + key_lo) / KT;
   const int n_kt = key_hi > key_lo ? (int)((kv0 + key_hi + KT - 1) / KT - a_lo) : 0;
-
-  // this thread's row (TMEM lane = tid)
-  const int row = tid;
-  const int tl = row / R, hd = row % R;
-  const int t_row = t0 + tl;
-  const bool valid = tl < TPC && t_row < L;
-  int b_lo = 0, b_hi = 0;  // attended keys [b_lo, b_hi), relative to kv0
-  if (valid) {
-    if (MODE == 0) {
-      b_hi = num_causal_cmp(t_row, n_c, p.kernel, p.stride);
-    } else {
-      b_lo = max(0, t_row - p.window + 1);
-      b_hi = t_row + 1;
-    }
-  }
+  const int n_kt2 = RS > 0 ? (key_hi + KT - 1) / KT : 0;
 
   if (tid == 0) {
-    mbar_init(bar_s);
-    mbar_init(bar_o);
+    mbar_init(bar(B_Q), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar(B_KFULL + i), 1);
+      mbar_init(bar(B_KEMPTY + i), 1);
+      mbar_init(bar(B_VFULL + i), 1);
+      mbar_init(bar(B_VEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SFREE + i), 128);
+      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_ODONE + i), 1);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
@@ -207,163 +298,267 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const Params p) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     fence_before();
   }
-
-  // Q: 128 rows x 128 d as two 64-column swizzled halves; rows past the tile are zero
-  const int64_t q_row_stride = (int64_t)p.h * D;
-  for (int c = tid; c < ROWS * (D / 8); c += 128) {
-    const int r = c / (D / 8), ch = c % (D / 8);
-    const int rt = t0 + r / R;
-    const bool ok = r / R < TPC && rt < L;
-    const __nv_bfloat16* src = p.q + (start + rt) * q_row_stride + (g * R + r % R) * D + ch * 8;
-    cp_async16(sw128(q_s + (ch >> 3) * (ROWS * 128), r, ch & 7), ok ? src : (const void*)p.q, ok ? 16 : 0);
-  }
-  const int64_t k_row_stride = (int64_t)p.hkv * D;
-  auto load_tile = [&](int kt, int stage) {
-    const int64_t a0 = (a_lo + kt) * KT;
-    const uint32_t ks = k_s + stage * K_BYTES, vs = v_s + stage * V_BYTES;
-    for (int c = tid; c < KT * (D / 8); c += 128) {  // K: 64 key rows x 16 chunks, two halves
-      const int r = c / (D / 8), ch = c % (D / 8);
-      const bool ok = a0 + r < p.kv_rows;
-      const __nv_bfloat16* src = p.k + (a0 + r) * k_row_stride + g * D + ch * 8;
-      cp_async16(sw128(ks + (ch >> 3) * (KT * 128), r, ch & 7), ok ? src : (const void*)p.k, ok ? 16 : 0);
-    }
-    for (int c = tid; c < D * (KT / 8); c += 128) {  // V^T: 128 d rows x 8 chunks of 8 keys
-      const int r = c / (KT / 8), ch = c % (KT / 8);
-      cp_async16(sw128(vs, r, ch), p.vt + ((int64_t)g * D + r) * p.kv_pad + a0 + ch * 8, 16);
-    }
-  };
-  if (n_kt > 0) load_tile(0, 0);
-  cp_async_commit();
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_holder;
-  const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 TMEM lanes
 
-  float m = kNegInf, l = 0.f;
-  bool bad = false, s_pending = false, o_pending = false;
-  int kt = 0;
-  for (; kt < n_kt; ++kt) {
-    const int stage = kt & 1;
-    // PV(kt-1) read the other stage: wait for it before refilling that stage
-    if (o_pending) {
-      bad |= !mbar_wait(bar_o, (kt - 1) & 1);
-      o_pending = bad;
+  int last_k = -1, last_v = -1;  // producer: last K / V^T tile loads issued
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(B_Q), Q_BYTES);
+      tma3d(q_s, &tm_q, 0, g * R, (int)(start + t0), bar(B_Q));
+      tma3d(q_s + Q_BYTES / 2, &tm_q, 64, g * R, (int)(start + t0), bar(B_Q));
     }
-    if (kt + 1 < n_kt && !bad) load_tile(kt + 1, stage ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    fence_async_smem();
-    if (__syncthreads_or(bad)) break;
-    if (tid == 0) {
-      fence_after();
-      const uint32_t ks = k_s + stage * K_BYTES;
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s)
-        mma(tmem, sdesc(q_s + (s >> 2) * (ROWS * 128) + (s & 3) * 32), sdesc(ks + (s >> 2) * (KT * 128) + (s & 3) * 32),
-            idesc(ROWS, KT), s > 0);
-      commit(bar_s);
-    }
-    s_pending = true;
-    bad |= !mbar_wait(bar_s, kt & 1);
-    s_pending = bad;
-    fence_after();
-    float sv[KT];
-    tmem_ld32(t_lane + 0, sv);
-    tmem_ld32(t_lane + 32, sv + 32);
-    // key row a0 + j is key a0 + j - kv0 of the sequence: attended when in [b_lo, b_hi)
-    const int64_t rel0 = (a_lo + kt) * KT - kv0;
-    const int64_t jl = b_lo - rel0, jh = b_hi - rel0;
-    const int j_lo = jl < 0 ? 0 : (jl > KT ? KT : (int)jl);
-    const int j_hi = jh < 0 ? 0 : (jh > KT ? KT : (int)jh);
-    float mx = kNegInf;
-#pragma unroll
-    for (int j = 0; j < KT; ++j) {
-      sv[j] = (j >= j_lo && j < j_hi) ? sv[j] * p.scale_log2 : kNegInf;
-      mx = fmaxf(mx, sv[j]);
-    }
-    // lazy rescale: the running max moves only when a score exceeds it by 2^8
-    const bool need = mx > m + 8.f;
-    if (__any_sync(0xffffffffu, need)) {
-      const float m_new = need ? mx : m;  // need implies mx > m
-      const float alpha = need ? ex2(m - m_new) : 1.f;
-      if (kt > 0) {
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          float ov[32];
-          tmem_ld32(t_lane + 128 + cc, ov);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] *= alpha;
-          tmem_st32(t_lane + 128 + cc, ov);
+    for (int i = 0; i < n_kt + n_kt2; ++i) {
+      const int st = i % NS;
+      if (i >= NS && !warp_wait(bar(B_KEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
+      const int row = i < n_kt ? (int)((a_lo + i) * KT) : (int)(kv0 + (int64_t)(i - n_kt) * KT);
+      if (lane == 0) {
+        const uint32_t kb = bar(B_KFULL + st);
+        mbar_expect_tx(kb, K_BYTES);
+        tma2d(k_s + st * K_BYTES, &tm_k, g * D, row, kb);
+        tma2d(k_s + st * K_BYTES + K_BYTES / 2, &tm_k, g * D + 64, row, kb);
+      }
+      last_k = i;
+      if (i < n_kt) {
+        if (i >= NS && !warp_wait(bar(B_VEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
+        if (lane == 0) {
+          const uint32_t vb = bar(B_VFULL + st);
+          mbar_expect_tx(vb, V_BYTES);
+          tma2d(v_s + st * V_BYTES, &tm_vt, row, g * D, vb);
         }
+        last_v = i;
       }
-      l *= alpha;
-      m = m_new;
+      __syncwarp();
     }
-    const float mu = m == kNegInf ? 0.f : m;
-    // P (bf16) goes over this stage's K tile, which S(kt) no longer reads
-    const uint32_t ps = k_s + stage * K_BYTES;
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    bool ok = warp_wait(bar(B_Q), 0, abort);
+    for (int kt = -1; ok && kt < n_kt; ++kt) {
+      const int j = kt + 1;
+      if (j < n_kt) {
+        // S buffer j & 1 was last read by PV(j - 2)
+        if (j >= 2) ok = warp_wait(bar(B_ODONE + (j & 1)), ((j - 2) >> 1) & 1, abort);
+        if (ok) ok = warp_wait(bar(B_KFULL + j % NS), (j / NS) & 1, abort);
+        if (!ok) break;
+        if (lane == 0) {
+          fence_after();
+          const uint32_t ks = k_s + (j % NS) * K_BYTES;
 #pragma unroll
-    for (int ch = 0; ch < KT / 8; ++ch) {
-      float e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        e[j] = ex2(sv[ch * 8 + j] - mu);
-        l += e[j];
+          for (int s = 0; s < D / 16; ++s)
+            mma_ss(tmem + (j & 1) * KT, sdesc(q_s + (s >> 2) * (Q_BYTES / 2) + (s & 3) * 32),
+                   sdesc(ks + (s >> 2) * (K_BYTES / 2) + (s & 3) * 32), idesc(ROWS, KT), s > 0);
+          commit(bar(B_SFULL + (j & 1)));
+          commit(bar(B_KEMPTY + j % NS));
+        }
+        __syncwarp();
       }
-      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(sw128(ps, row, ch)), "r"(pack_bf16(e[0], e[1])),
-                   "r"(pack_bf16(e[2], e[3])), "r"(pack_bf16(e[4], e[5])), "r"(pack_bf16(e[6], e[7]))
-                   : "memory");
-    }
-    fence_async_smem();
-    fence_before();
-    if (__syncthreads_or(bad)) break;
-    if (tid == 0) {
-      fence_after();
-      const uint32_t vs = v_s + stage * V_BYTES;
+      if (kt >= 0) {
+        ok = warp_wait(bar(B_PFULL + (kt & 1)), (kt >> 1) & 1, abort);
+        if (ok) ok = warp_wait(bar(B_VFULL + kt % NS), (kt / NS) & 1, abort);
+        if (!ok) break;
+        if (lane == 0) {
+          fence_after();
+          const uint32_t vs = v_s + (kt % NS) * V_BYTES;
 #pragma unroll
-      for (int s = 0; s < KT / 16; ++s)
-        mma(tmem + 128, sdesc(ps + s * 32), sdesc(vs + s * 32), idesc(ROWS, D), (kt > 0 || s > 0) ? 1u : 0u);
-      commit(bar_o);
+          for (int s = 0; s < KT / 16; ++s)
+            mma_ts(tmem + O_COL, tmem + (kt & 1) * KT + s * 8, sdesc(vs + s * 32), idesc(ROWS, D),
+                   (kt > 0 || s > 0) ? 1u : 0u);
+          commit(bar(B_ODONE + (kt & 1)));
+          commit(bar(B_VEMPTY + kt % NS));
+        }
+        __syncwarp();
+      }
     }
-    o_pending = true;
-  }
-  if (o_pending && !bad) {
-    bad |= !mbar_wait(bar_o, (n_kt - 1) & 1);
-    o_pending = bad;
-  }
-  bad = __syncthreads_or(bad);
-  if (bad) {
-    // drain: tensor-core work still in flight must finish before its TMEM is freed
-    if (s_pending) mbar_wait(bar_s, kt & 1);
-    if (o_pending) mbar_wait(bar_o, (kt - 1) & 1);
-  }
-  cp_async_wait<0>();
-  fence_after();
-  if (!bad) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* dst = p.o + ((start + t_row) * p.h + g * R + hd) * D;
-#pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
-      float ov[32];
-      if (n_kt > 0) {
-        tmem_ld32(t_lane + 128 + cc, ov);
+    for (int i = 0; ok && i < n_kt2; ++i) {
+      const int j = n_kt + i, b = j & 1;
+      if (i >= 2)
+        ok = warp_wait(bar(B_SFREE + b), ((i - 2) >> 1) & 1, abort);
+      else if (j >= 2)
+        ok = warp_wait(bar(B_ODONE + b), ((j - 2) >> 1) & 1, abort);
+      if (ok) ok = warp_wait(bar(B_KFULL + j % NS), (j / NS) & 1, abort);
+      if (!ok) break;
+      if (lane == 0) {
+        fence_after();
+        const uint32_t ks = k_s + (j % NS) * K_BYTES;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)
+          mma_ss(tmem + b * KT, sdesc(q_s + (s >> 2) * (Q_BYTES / 2) + (s & 3) * 32),
+                 sdesc(ks + (s >> 2) * (K_BYTES / 2) + (s & 3) * 32), idesc(ROWS, KT), s > 0);
+        commit(bar(B_SFULL + b));
+        commit(bar(B_KEMPTY + j % NS));
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warps
+    const int row = tid;
+    const int tl = row / R, hd = row % R;
+    const int t_row = t0 + tl;
+    const bool valid = t_row < L;
+    int b_lo = 0, b_hi = 0;  // attended keys [b_lo, b_hi), relative to kv0
+    if (valid) {
+      if (MODE == 0) {
+        b_hi = num_causal_cmp(t_row, n_c, p.kernel, p.stride);
       } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] = 0.f;
-      }
-      if (valid) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 pk;
-          pk.x = pack_bf16(ov[j] * inv, ov[j + 1] * inv);
-          pk.y = pack_bf16(ov[j + 2] * inv, ov[j + 3] * inv);
-          pk.z = pack_bf16(ov[j + 4] * inv, ov[j + 5] * inv);
-          pk.w = pack_bf16(ov[j + 6] * inv, ov[j + 7] * inv);
-          *reinterpret_cast<uint4*>(dst + cc + j) = pk;
-        }
+        b_lo = max(0, t_row - p.window + 1);
+        b_hi = t_row + 1;
       }
     }
-    if (p.lse && valid) p.lse[(start + t_row) * p.h + g * R + hd] = l > 0.f ? (m + __log2f(l)) * kLn2 : kNegInf;
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 TMEM lanes
+    float m = kNegInf, l = 0.f;
+    bool ok = true;
+    for (int kt = 0; kt < n_kt; ++kt) {
+      const int b = kt & 1;
+      if (!(ok = warp_wait(bar(B_SFULL + b), (kt >> 1) & 1, abort))) break;
+      fence_after();
+      float sv[KT];
+      tmem_ld32(t_lane + b * KT, sv);
+      tmem_ld32(t_lane + b * KT + 32, sv + 32);
+      // key row a0 + j is key a0 + j - kv0 of the sequence: attended when in [b_lo, b_hi)
+      const int64_t rel0 = (a_lo + kt) * KT - kv0;
+      const int64_t jl = b_lo - rel0, jh = b_hi - rel0;
+      const int j_lo = jl < 0 ? 0 : (jl > KT ? KT : (int)jl);
+      const int j_hi = jh < 0 ? 0 : (jh > KT ? KT : (int)jh);
+      float mx = kNegInf;
+#pragma unroll
+      for (int j = 0; j < KT; ++j) {
+        sv[j] = (j >= j_lo && j < j_hi) ? sv[j] * p.scale_log2 : kNegInf;
+        mx = fmaxf(mx, sv[j]);
+      }
+      // lazy rescale: the running max moves only when a score exceeds it by 2^8
+      const bool need = mx > m + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(m - mx) : 1.f;  // need implies mx finite
+        if (kt > 0) {
+          // O must hold PV(kt-1) before it is rescaled
+          if (!(ok = warp_wait(bar(B_ODONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1, abort))) break;
+          fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            float ov[32];
+            tmem_ld32(t_lane + O_COL + cc, ov);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] *= alpha;
+            tmem_st32(t_lane + O_COL + cc, reinterpret_cast<const uint32_t*>(ov));
+          }
+        }
+        if (need) {
+          l *= alpha;
+          m = mx;
+        }
+      }
+      const float mu = m == kNegInf ? 0.f : m;
+      uint32_t pk[KT / 2];
+#pragma unroll
+      for (int j = 0; j < KT; j += 2) {
+        const float e0 = ex2(sv[j] - mu), e1 = ex2(sv[j + 1] - mu);
+        l += e0 + e1;
+        pk[j / 2] = pack_bf16(e0, e1);
+      }
+      tmem_st32(t_lane + b * KT, pk);  // P over the first 32 columns of its S buffer
+      fence_before();
+      mbar_arrive(bar(B_PFULL + b));
+    }
+    if (ok && n_kt > 0) {
+      ok = warp_wait(bar(B_ODONE + ((n_kt - 1) & 1)), ((n_kt - 1) >> 1) & 1, abort);
+      fence_after();
+    }
+    if (ok) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = p.o + ((start + t_row) * p.h + g * R + hd) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        float ov[32];
+        if (n_kt > 0) {
+          tmem_ld32(t_lane + O_COL + cc, ov);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = 0.f;
+        }
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 v;
+            v.x = pack_bf16(ov[j] * inv, ov[j + 1] * inv);
+            v.y = pack_bf16(ov[j + 2] * inv, ov[j + 3] * inv);
+            v.z = pack_bf16(ov[j + 4] * inv, ov[j + 5] * inv);
+            v.w = pack_bf16(ov[j + 6] * inv, ov[j + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + cc + j) = v;
+          }
+        }
+      }
+      if (p.lse && valid) p.lse[(start + t_row) * p.h + g * R + hd] = l > 0.f ? (m + __log2f(l)) * kLn2 : kNegInf;
+    }
+    if (RS > 0 && ok) {
+      // ---------------------------------------------------------------- pass 2: block scores
+      const float lse2 = l > 0.f ? m + __log2f(l) : 0.f;  // base-2 normaliser of the scaled scores
+      float* out = p.scores + ((start + t_row) * p.hkv + g) * p.nb_stride;
+      constexpr int PER = RS > 0 ? 16 / RS : 1;  // blocks per lane after the head reduction
+      for (int i = 0; i < n_kt2; ++i) {
+        const int j = n_kt + i, b = j & 1;
+        if (!(ok = warp_wait(bar(B_SFULL + b), (j >> 1) & 1, abort))) break;
+        fence_after();
+        float sv[KT];
+        tmem_ld32(t_lane + b * KT, sv);
+        tmem_ld32(t_lane + b * KT + 32, sv + 32);
+        fence_before();
+        mbar_arrive(bar(B_SFREE + b));
+        const int jh = min(KT, max(0, b_hi - i * KT));  // causal compressed keys of this tile
+        float bs[16];
+#pragma unroll
+        for (int jb = 0; jb < 16; ++jb) {
+          float acc = 0.f;
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            const int jj = 4 * jb + c;
+            acc += jj < jh ? ex2(fmaf(sv[jj], p.scale_log2, -lse2)) : 0.f;
+          }
+          bs[jb] = acc;
+        }
+        group_reduce_scatter<RS>(bs, lane);
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < PER; ++u) {
+            const int blk = i * 16 + hd * PER + u;
+            if (blk < p.nb_stride) {
+              const int c0 = 4 * blk;
+              const int cnt = (c0 < n_c) + (c0 + 1 < n_c) + (c0 + 2 < n_c);
+              out[blk] = bs[u] * (cnt == 3 ? (1.f / 3.f) : cnt == 2 ? 0.5f : cnt == 1 ? 1.f : 0.f);
+            }
+          }
+        }
+      }
+      // blocks past the last tile hold no causal probability
+      if (ok && valid)
+        for (int blk = n_kt2 * 16 + hd; blk < p.nb_stride; blk += R) out[blk] = 0.f;
+    }
+  }
+
+  __syncthreads();
+  if (*abort) {
+    // drain: copies and MMAs still in flight must land before the CTA leaves
+    if (warp == 4) {
+      mbar_wait(bar(B_Q), 0, nullptr);
+      for (int st = 0; st < NS; ++st) {
+        const int ik = last_in_stage(last_k, st), iv = last_in_stage(last_v, st);
+        if (ik >= 0) mbar_wait(bar(B_KFULL + st), (ik / NS) & 1, nullptr);
+        if (iv >= 0) mbar_wait(bar(B_VFULL + st), (iv / NS) & 1, nullptr);
+      }
+    } else if (warp == 5) {
+      if (lane == 0) commit(bar(B_DRAIN));
+      __syncwarp();
+      mbar_wait(bar(B_DRAIN), 0, nullptr);
+    }
+  } else if (warp == 4) {
+    // every MMA completion that arrives on a ring barrier lands before the CTA leaves:
+    // wait for the last release of each stage
+    for (int st = 0; st < NS; ++st) {
+      const int ik = last_in_stage(last_k, st), iv = last_in_stage(last_v, st);
+      if (ik >= 0) mbar_wait(bar(B_KEMPTY + st), (ik / NS) & 1, nullptr);
+      if (iv >= 0) mbar_wait(bar(B_VEMPTY + st), (iv / NS) & 1, nullptr);
+    }
   }
   fence_before();
   __syncthreads();
@@ -374,10 +569,12 @@ __global__ void __launch_bounds__(128, 2) attn_kernel(const Params p) {
 // V [rows, hkv, D] -> V^T [hkv, D, pad] with pad = rows rounded up to 64.  Rows at or
 // past `valid` (the rows the producer wrote; for compressed rows of packed sequences the
 // sum of their counts) are written as zeros, so masked keys never multiply garbage.
+// The staging tile keeps row r's 16-byte chunk c at chunk c ^ (r / 8): the column reads
+// of the transpose then hit eight different bank groups.
 __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* __restrict__ v,
                                                         __nv_bfloat16* __restrict__ vt, int64_t pad, int hkv,
                                                         int64_t valid, Seqs seqs, int kernel, int stride) {
-  __shared__ __nv_bfloat16 tile[64][D + 8];
+  __shared__ __align__(16) __nv_bfloat16 tile[64][D];
   if (valid < 0) valid = cmp_offset(seqs, seqs.n_seqs, kernel, stride);
   const int64_t r0 = (int64_t)blockIdx.x * 64;
   const int g = blockIdx.y;
@@ -385,16 +582,52 @@ __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* __r
     const int r = c / (D / 8), ch = c % (D / 8);
     uint4 x = make_uint4(0, 0, 0, 0);
     if (r0 + r < valid) x = *reinterpret_cast<const uint4*>(v + ((r0 + r) * hkv + g) * D + ch * 8);
-    *reinterpret_cast<uint4*>(&tile[r][ch * 8]) = x;
+    *reinterpret_cast<uint4*>(&tile[r][(ch ^ (r >> 3)) * 8]) = x;
   }
   __syncthreads();
   for (int c = threadIdx.x; c < D * 8; c += 256) {  // 128 d rows x 8 chunks of 8 keys
     const int d = c / 8, ch = c % 8;
     __align__(16) __nv_bfloat16 e[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) e[j] = tile[ch * 8 + j][d];
+    for (int j = 0; j < 8; ++j) e[j] = tile[ch * 8 + j][(((d >> 3) ^ ch) << 3) | (d & 7)];
     *reinterpret_cast<uint4*>(vt + ((int64_t)g * D + d) * pad + r0 + ch * 8) = *reinterpret_cast<const uint4*>(e);
   }
+}
+
+// ---------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzling; dims and strides innermost first (strides in
+// bytes, one fewer than dims); out-of-range elements read as zero.
+static bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                     const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[3] = {1, 1, 1}, gs[2] = {0, 0};
+  cuuint32_t bx[3] = {1, 1, 1}, es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs, bx, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc
@@ -410,33 +643,68 @@ cudaError_t launch_transpose_v(const Seqs& s, const void* v, void* vt, int64_t r
   return cudaGetLastError();
 }
 
+template <int MODE, int RS>
+static cudaError_t run_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const tc::Params& p,
+                          dim3 grid, cudaStream_t st) {
+  auto kern = tc::attn_kernel<MODE, RS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, tc::NTHREADS, tc::SMEM_BYTES, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
-                                 void* o, float* lse, cudaStream_t st) {
+                                 void* o, float* lse, float* scores, int nb_stride, cudaStream_t st) {
   if (s.tokens == 0) return cudaSuccess;
+  const int R = h / hkv;
+  const int tpc = tc::ROWS / R;
+  // a map needs nonzero extents; with no key rows no tile is ever loaded
+  const uint64_t rows = kv_rows > 0 ? (uint64_t)kv_rows : 1;
+  const uint64_t pad = (uint64_t)tc_vt_pad((int64_t)rows);
+  CUtensorMap mq, mk, mv;
+  {
+    const uint64_t dims[3] = {(uint64_t)tc::D, (uint64_t)h, (uint64_t)s.tokens};
+    const uint64_t strides[2] = {(uint64_t)tc::D * 2, (uint64_t)h * tc::D * 2};
+    const uint32_t box[3] = {64, (uint32_t)R, (uint32_t)tpc};
+    if (!tc::make_map(&mq, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)hkv * tc::D, rows};
+    const uint64_t strides[1] = {(uint64_t)hkv * tc::D * 2};
+    const uint32_t box[2] = {64, (uint32_t)tc::KT};
+    if (!tc::make_map(&mk, k, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {pad, (uint64_t)hkv * tc::D};
+    const uint64_t strides[1] = {pad * 2};
+    const uint32_t box[2] = {64, (uint32_t)tc::D};
+    if (!tc::make_map(&mv, vt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   tc::Params p{};
-  p.q = (const __nv_bfloat16*)q;
-  p.k = (const __nv_bfloat16*)k;
-  p.vt = (const __nv_bfloat16*)vt;
   p.o = (__nv_bfloat16*)o;
   p.lse = lse;
+  p.scores = scores;
   p.seqs = s;
   p.h = h;
   p.hkv = hkv;
-  p.R = h / hkv;
+  p.R = R;
   p.kernel = kernel;
   p.stride = stride;
   p.window = window;
-  p.kv_rows = kv_rows;
-  p.kv_pad = tc_vt_pad(kv_rows);
+  p.nb_stride = nb_stride;
   p.scale_log2 = scale * kLog2e;
-  const int tpc = tc::ROWS / p.R;
   const dim3 grid((s.max_len + tpc - 1) / tpc, s.n_seqs, hkv);
-  auto kern = mode == 0 ? tc::attn_kernel<0> : tc::attn_kernel<1>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, 128, tc::SMEM_BYTES, st>>>(p);
-  return cudaGetLastError();
+  if (mode == 1) return run_tc<1, 0>(mq, mk, mv, p, grid, st);
+  if (!scores) return run_tc<0, 0>(mq, mk, mv, p, grid, st);
+  switch (R) {
+    case 1: return run_tc<0, 1>(mq, mk, mv, p, grid, st);
+    case 2: return run_tc<0, 2>(mq, mk, mv, p, grid, st);
+    case 4: return run_tc<0, 4>(mq, mk, mv, p, grid, st);
+    case 8: return run_tc<0, 8>(mq, mk, mv, p, grid, st);
+    case 16: return run_tc<0, 16>(mq, mk, mv, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t read_device_status(int32_t* out, bool reset) {

@@ -38,12 +38,14 @@ cudaError_t launch_dense_attn(int mode, const Seqs& s, const void* q, const void
 // Tensor-core (tcgen05) versions of the two dense branches for d = 128, bf16.  They take
 // V transposed per kv-head, [hkv, 128, tc_vt_pad(kv_rows)], written by launch_transpose_v
 // (compressed = true: valid rows are the packed compressed rows of all sequences).
+// mode 0 with scores != nullptr also writes the pooled block scores [tokens, hkv,
+// nb_stride] (h / hkv must then be 1, 2, 4, 8 or 16).
 int64_t tc_vt_pad(int64_t rows);
 cudaError_t launch_transpose_v(const Seqs& s, const void* v, void* vt, int64_t rows, int hkv, bool compressed,
                                int kernel, int stride, cudaStream_t st);
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
-                                 void* o, float* lse, cudaStream_t st);
+                                 void* o, float* lse, float* scores, int nb_stride, cudaStream_t st);
 // Device status word set by bounded waits (NSA_ERR_TIMEOUT); optionally cleared.
 cudaError_t read_device_status(int32_t* out, bool reset);
 

@@ -284,6 +284,7 @@ def test_layer_small(T, H, hkv):
     idx = torch.empty((T, hkv, 16), dtype=torch.int32, device="cuda")
     out = nsa.nsa_layer_fwd(dev(w.q), dev(w.k), dev(w.v), dev(w.gates), idx_out=idx)
     torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
     gi = host(idx)
     ref = orc.layer(w.q, w.k, w.v, w.gates, w.cu_seqlens, idx_in=gi)
     _, kc = orc.compress(w.k, w.cu_seqlens)
@@ -320,6 +321,7 @@ def test_layer_full_size_sampled():
     idx = torch.empty((w.tokens, 4, 16), dtype=torch.int32, device="cuda")
     out = nsa.nsa_layer_fwd(dev(w.q), dev(w.k), dev(w.v), dev(w.gates), idx_out=idx)
     torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
     gi = host(idx)
     rows = np.unique(np.concatenate([_rng(12).integers(0, w.tokens, 24), [0, 31, 32, 511, 512, 65535]]))
     ref = orc.layer(w.q, w.k, w.v, w.gates, w.cu_seqlens, idx_in=gi, rows=rows)
