@@ -90,7 +90,7 @@ const char* nsa_last_error(void) { return g_err; }
 
 nsa_status nsa_device_status(int32_t* status, int reset) {
   NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
-  return cuda_status(read_device_status(status, reset != 0), "nsa_device_status");
+  return cuda_status(status_word_dense_tc(status, reset != 0), "nsa_device_status");
 }
 
 nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,

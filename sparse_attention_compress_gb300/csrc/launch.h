@@ -46,8 +46,9 @@ cudaError_t launch_transpose_v(const Seqs& s, const void* v, void* vt, int64_t r
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
                                  void* o, float* lse, float* scores, int nb_stride, cudaStream_t st);
-// Device status word set by bounded waits (NSA_ERR_TIMEOUT); optionally cleared.
-cudaError_t read_device_status(int32_t* out, bool reset);
+// Status words of the units with bounded waits (NSA_ERR_TIMEOUT once a wait ran out);
+// optionally cleared.
+cudaError_t status_word_dense_tc(int32_t* out, bool reset);
 
 cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gates, void* o, cudaStream_t st);
