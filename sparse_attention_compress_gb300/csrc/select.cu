@@ -21,7 +21,7 @@
 namespace nsa {
 
 constexpr int kSPWarps = 8;
-constexpr int kCmpKernel = 32, kCmpStride = 16, kSelBlock = 64;
+constexpr int kCmpKernel = 32, kCmpStride = 16;
 
 struct ScoresParams {
   const __nv_bfloat16* q;
@@ -247,18 +247,20 @@ cudaError_t launch_scores_pool(const Seqs& s, const void* q, const void* k_cmp, 
 
 // ---------------------------------------------------------------------------
 // Top-k selection: one warp per (token, kv-head) row.
-template <int NPL, bool VEC>
+template <int NPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ scores, int nb_stride, int32_t* out,
                                                   Seqs s, int hkv, int block_size, int n_init, int n_local,
                                                   int k) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  __shared__ uint32_t s_key[8][64];
+  __shared__ int s_idx[8][64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
   if (row >= s.tokens * hkv) return;
-  const int lane = threadIdx.x & 31;
   const int64_t tok = row / hkv;
   const int sq = seq_of_token(s, tok);
   const int t = (int)(tok - seq_start(s, sq));
-  warp_topk<NPL, VEC>(scores + row * nb_stride, nb_stride, t / block_size, n_init, n_local, k,
-                      out + row * k, lane);
+  warp_topk<NPL>(scores + row * nb_stride, nb_stride, t / block_size, n_init, n_local, k, out + row * k,
+                 s_key[warp], s_idx[warp], lane);
 }
 
 cudaError_t launch_topk(const Seqs& s, const float* scores, int nb_stride, int hkv, int block_size,
@@ -266,17 +268,11 @@ cudaError_t launch_topk(const Seqs& s, const float* scores, int nb_stride, int h
   const int64_t rows = s.tokens * hkv;
   if (rows == 0) return cudaSuccess;
   dim3 grid((unsigned)((rows + 7) / 8));
-  const bool vec = nb_stride % 4 == 0;
   const int npl = (nb_stride + 31) / 32;
-#define NSA_TOPK(N)                                                                                   \
-  if (npl <= N) {                                                                                     \
-    if (vec && N % 4 == 0)                                                                            \
-      topk_kernel<N, (N % 4 == 0)><<<grid, 256, 0, st>>>(scores, nb_stride, idx, s, hkv, block_size,  \
-                                                         n_init, n_local, k);                         \
-    else                                                                                              \
-      topk_kernel<N, false><<<grid, 256, 0, st>>>(scores, nb_stride, idx, s, hkv, block_size, n_init, \
-                                                  n_local, k);                                        \
-    return cudaGetLastError();                                                                        \
+#define NSA_TOPK(N)                                                                                        \
+  if (npl <= N) {                                                                                          \
+    topk_kernel<N><<<grid, 256, 0, st>>>(scores, nb_stride, idx, s, hkv, block_size, n_init, n_local, k); \
+    return cudaGetLastError();                                                                             \
   }
   NSA_TOPK(1)
   NSA_TOPK(2)

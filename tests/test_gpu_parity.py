@@ -93,7 +93,8 @@ def test_cmp_scores_pool_with_given_normaliser():
 # --------------------------------------------------------------------------- S4
 @pytest.mark.parametrize("nb_stride,k,n_init,n_local,levels", [
     (40, 16, 1, 2, 0), (40, 16, 1, 2, 3), (129, 7, 0, 0, 5), (512, 64, 1, 2, 0), (1024, 16, 2, 1, 4),
-    (2048, 64, 1, 2, 0), (3, 1, 1, 2, 0), (64, 64, 0, 0, 2)])
+    (2048, 64, 1, 2, 0), (3, 1, 1, 2, 0), (64, 64, 0, 0, 2), (1024, 16, 1, 2, 0), (2048, 32, 1, 2, 0),
+    (256, 32, 0, 0, 50), (1024, 16, 1, 2, 1000)])
 def test_topk_bit_exact(nb_stride, k, n_init, n_local, levels):
     bs = 64
     max_len = nb_stride * bs
