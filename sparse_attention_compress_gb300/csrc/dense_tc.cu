@@ -43,6 +43,9 @@ constexpr int K_BYTES = KT * D * 2;    // two halves of 8 KB
 constexpr int V_BYTES = D * KT * 2;    // V^T tile: 128 d-rows of 64 keys
 constexpr int SMEM_BYTES = Q_BYTES + NS * (K_BYTES + V_BYTES) + 1024;  // + 1 KB for alignment
 constexpr int TMEM_COLS = 256;  // S buffers at columns 0 and 64 (P over their first 32), O at 128
+// scores-only mode: no V ring and no O accumulator (three CTAs per SM)
+constexpr int SMEM_BYTES_SCORES = Q_BYTES + NS * K_BYTES + 1024;
+constexpr int TMEM_COLS_SCORES = 128;
 constexpr uint32_t O_COL = 128;
 
 // barrier slots
@@ -80,8 +83,11 @@ __device__ __forceinline__ void group_reduce_scatter(float (&v)[16], int lane) {
 
 struct Params {
   __nv_bfloat16* o;
-  float* lse;     // optional natural-log normaliser per (token, head)
-  float* scores;  // MODE 0 with fused block scores: [tokens, hkv, nb_stride]
+  float* lse;            // optional natural-log normaliser per (token, head)
+  float* scores;         // MODE 0 with fused block scores, MODE 2: [tokens, hkv, nb_stride]
+  const float* lse_in;   // MODE 2: normaliser given by the caller (pass 1 skipped), or null
+  const __nv_bfloat16* k;  // MODE 2: key rows, for the copies of a tile that ends past them
+  int64_t kv_total;      // MODE 2: key rows the buffer holds (-1: the packed compressed rows)
   Seqs seqs;
   int h, hkv, R, kernel, stride, window, nb_stride;
   float scale_log2;
@@ -94,9 +100,11 @@ __device__ __forceinline__ int last_in_stage(int last, int st) {
 }
 
 // MODE 0: compressed branch (RS = group size when the block scores are fused, else 0);
-// MODE 1: sliding window (RS = 0).
+// MODE 1: sliding window (RS = 0);
+// MODE 2: block scores only (RS = group size): pass 1 keeps just the softmax statistics
+//         (no V, no PV; skipped when the caller gives the normaliser), then pass 2.
 template <int MODE, int RS>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int64_t start = seq_start(p.seqs, sq);
   int n_c = 0, key_lo, key_hi;
   int64_t kv0;  // key row of the sequence's first key
-  if (MODE == 0) {
+  if (MODE != 1) {
     n_c = num_cmp(L, p.kernel, p.stride);
     kv0 = cmp_offset(p.seqs, sq, p.kernel, p.stride);
     key_lo = 0;
@@ -136,9 +144,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
   // pass 1: 64-key tiles in absolute key rows (64-aligned, so every V^T tile starts on a
   // 128-byte boundary); pass 2: tiles at kv0 + 64 i (16 whole selection blocks each)
+  // (MODE 2 needs no V^T, so both of its passes use the sequence-aligned tiles)
   const int64_t a_lo = (kv0 + key_lo) / KT;
-  const int n_kt = key_hi > key_lo ? (int)((kv0 + key_hi + KT - 1) / KT - a_lo) : 0;
   const int n_kt2 = RS > 0 ? (key_hi + KT - 1) / KT : 0;
+  const int n_kt = MODE == 2 ? (p.lse_in ? 0 : n_kt2)
+                             : (key_hi > key_lo ? (int)((kv0 + key_hi + KT - 1) / KT - a_lo) : 0);
+  constexpr int kTmemCols = MODE == 2 ? TMEM_COLS_SCORES : TMEM_COLS;
 
   if (tid == 0) {
     mbar_init(bar(B_Q), 1);
@@ -160,7 +171,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&tmem_holder)),
-                 "r"(TMEM_COLS)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     fence_before();
@@ -177,18 +188,42 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       tma3d(q_s, &tm_q, 0, g * R, (int)(start + t0), bar(B_Q));
       tma3d(q_s + Q_BYTES / 2, &tm_q, 64, g * R, (int)(start + t0), bar(B_Q));
     }
+    int64_t kv_total = p.kv_total;
+    if (MODE == 2 && kv_total < 0) {  // packed compressed rows of all sequences
+      int64_t acc = 0;
+      for (int i = lane; i < p.seqs.n_seqs; i += 32) acc += num_cmp(seq_len(p.seqs, i), p.kernel, p.stride);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      kv_total = acc;
+    }
     for (int i = 0; i < n_kt + n_kt2; ++i) {
       const int st = i % NS;
       if (i >= NS && !warp_wait(bar(B_KEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
-      const int row = i < n_kt ? (int)((a_lo + i) * KT) : (int)(kv0 + (int64_t)(i - n_kt) * KT);
-      if (lane == 0) {
-        const uint32_t kb = bar(B_KFULL + st);
+      const int row = MODE == 2 ? (int)(kv0 + (int64_t)(i < n_kt ? i : i - n_kt) * KT)
+                                : (i < n_kt ? (int)((a_lo + i) * KT) : (int)(kv0 + (int64_t)(i - n_kt) * KT));
+      const uint32_t kb = bar(B_KFULL + st), ks = k_s + st * K_BYTES;
+      if (MODE == 2 && row + KT > kv_total) {
+        // a tile reaching past the caller's rows: bounds-checked copies (zeros past the
+        // end) instead of TMA, then the async-proxy fence and a plain arrival
+        for (int c = lane; c < KT * (D / 8); c += 32) {
+          const int r = c / (D / 8), ch = c % (D / 8);
+          const bool in = row + r < kv_total;
+          const __nv_bfloat16* src = p.k + ((int64_t)(row + r) * p.hkv + g) * D + ch * 8;
+          cp_async16(ks + (ch >> 3) * (K_BYTES / 2) + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                     in ? (const void*)src : (const void*)p.k, in ? 16 : 0);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kb);
+      } else if (lane == 0) {
         mbar_expect_tx(kb, K_BYTES);
-        tma2d(k_s + st * K_BYTES, &tm_k, g * D, row, kb);
-        tma2d(k_s + st * K_BYTES + K_BYTES / 2, &tm_k, g * D + 64, row, kb);
+        tma2d(ks, &tm_k, g * D, row, kb);
+        tma2d(ks + K_BYTES / 2, &tm_k, g * D + 64, row, kb);
       }
       last_k = i;
-      if (i < n_kt) {
+      if (MODE != 2 && i < n_kt) {
         if (i >= NS && !warp_wait(bar(B_VEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
         if (lane == 0) {
           const uint32_t vb = bar(B_VFULL + st);
@@ -202,7 +237,26 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
     bool ok = warp_wait(bar(B_Q), 0, abort);
-    for (int kt = -1; ok && kt < n_kt; ++kt) {
+    if (MODE == 2) {
+      // S buffer j & 1 is free once the softmax warps have read S(j - 2)
+      for (int j = 0; ok && j < n_kt + n_kt2; ++j) {
+        if (j >= 2) ok = warp_wait(bar(B_SFREE + (j & 1)), ((j - 2) >> 1) & 1, abort);
+        if (ok) ok = warp_wait(bar(B_KFULL + j % NS), (j / NS) & 1, abort);
+        if (!ok) break;
+        if (lane == 0) {
+          fence_after();
+          const uint32_t ks = k_s + (j % NS) * K_BYTES;
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s)
+            mma_ss(tmem + (j & 1) * KT, sdesc(q_s + (s >> 2) * (Q_BYTES / 2) + (s & 3) * 32),
+                   sdesc(ks + (s >> 2) * (K_BYTES / 2) + (s & 3) * 32), idesc(ROWS, KT), s > 0);
+          commit(bar(B_SFULL + (j & 1)));
+          commit(bar(B_KEMPTY + j % NS));
+        }
+        __syncwarp();
+      }
+    }
+    for (int kt = -1; MODE != 2 && ok && kt < n_kt; ++kt) {
       const int j = kt + 1;
       if (j < n_kt) {
         // S buffer j & 1 was last read by PV(j - 2)
@@ -238,7 +292,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         __syncwarp();
       }
     }
-    for (int i = 0; ok && i < n_kt2; ++i) {
+    for (int i = 0; MODE != 2 && ok && i < n_kt2; ++i) {
       const int j = n_kt + i, b = j & 1;
       if (i >= 2)
         ok = warp_wait(bar(B_SFREE + b), ((i - 2) >> 1) & 1, abort);
@@ -266,7 +320,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const bool valid = t_row < L;
     int b_lo = 0, b_hi = 0;  // attended keys [b_lo, b_hi), relative to kv0
     if (valid) {
-      if (MODE == 0) {
+      if (MODE != 1) {
         b_hi = num_causal_cmp(t_row, n_c, p.kernel, p.stride);
       } else {
         b_lo = max(0, t_row - p.window + 1);
@@ -276,7 +330,32 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's 32 TMEM lanes
     float m = kNegInf, l = 0.f;
     bool ok = true;
-    for (int kt = 0; kt < n_kt; ++kt) {
+    for (int kt = 0; MODE == 2 && kt < n_kt; ++kt) {
+      // scores-only pass 1: running max and sum of the row, nothing else
+      const int b = kt & 1;
+      if (!(ok = warp_wait(bar(B_SFULL + b), (kt >> 1) & 1, abort))) break;
+      fence_after();
+      float sv[KT];
+      tmem_ld32(t_lane + b * KT, sv);
+      tmem_ld32(t_lane + b * KT + 32, sv + 32);
+      fence_before();
+      mbar_arrive(bar(B_SFREE + b));
+      const int j_hi = min(KT, max(0, b_hi - kt * KT));
+      float mx = kNegInf;
+#pragma unroll
+      for (int j = 0; j < KT; ++j) {
+        sv[j] = j < j_hi ? sv[j] * p.scale_log2 : kNegInf;
+        mx = fmaxf(mx, sv[j]);
+      }
+      if (mx > m + 8.f) {  // lazy rescale, as in the attention pass
+        l *= ex2(m - mx);
+        m = mx;
+      }
+      const float mu = m == kNegInf ? 0.f : m;
+#pragma unroll
+      for (int j = 0; j < KT; ++j) l += ex2(sv[j] - mu);
+    }
+    for (int kt = 0; MODE != 2 && kt < n_kt; ++kt) {
       const int b = kt & 1;
       if (!(ok = warp_wait(bar(B_SFULL + b), (kt >> 1) & 1, abort))) break;
       fence_after();
@@ -328,11 +407,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       fence_before();
       mbar_arrive(bar(B_PFULL + b));
     }
-    if (ok && n_kt > 0) {
+    if (MODE != 2 && ok && n_kt > 0) {
       ok = warp_wait(bar(B_ODONE + ((n_kt - 1) & 1)), ((n_kt - 1) >> 1) & 1, abort);
       fence_after();
     }
-    if (ok) {
+    if (MODE != 2 && ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* dst = p.o + ((start + t_row) * p.h + g * R + hd) * D;
 #pragma unroll 1
@@ -360,7 +439,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     if (RS > 0 && ok) {
       // ---------------------------------------------------------------- pass 2: block scores
-      const float lse2 = l > 0.f ? m + __log2f(l) : 0.f;  // base-2 normaliser of the scaled scores
+      // base-2 normaliser of the scaled scores (0 for rows without keys)
+      float lse2 = l > 0.f ? m + __log2f(l) : 0.f;
+      if (MODE == 2 && p.lse_in && valid) {
+        const float li = p.lse_in[(start + t_row) * p.h + g * R + hd];
+        lse2 = li > kNegInf ? li * kLog2e : 0.f;
+      }
       float* out = p.scores + ((start + t_row) * p.hkv + g) * p.nb_stride;
       constexpr int PER = RS > 0 ? 16 / RS : 1;  // blocks per lane after the head reduction
       for (int i = 0; i < n_kt2; ++i) {
@@ -430,7 +514,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   fence_before();
   __syncthreads();
   if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 // V [rows, hkv, D] -> V^T [hkv, D, pad] with pad = rows rounded up to 64.  Rows at or
@@ -478,9 +562,10 @@ template <int MODE, int RS>
 static cudaError_t run_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const tc::Params& p,
                           dim3 grid, cudaStream_t st) {
   auto kern = tc::attn_kernel<MODE, RS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+  constexpr int smem = MODE == 2 ? tc::SMEM_BYTES_SCORES : tc::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, tc::NTHREADS, tc::SMEM_BYTES, st>>>(mq, mk, mv, p);
+  kern<<<grid, tc::NTHREADS, smem, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -534,6 +619,56 @@ cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const v
     case 4: return run_tc<0, 4>(mq, mk, mv, p, grid, st);
     case 8: return run_tc<0, 8>(mq, mk, mv, p, grid, st);
     case 16: return run_tc<0, 16>(mq, mk, mv, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool scores_tc_supported(int h, int hkv, int d, int kernel, int stride, int block_size) {
+  const int R = hkv > 0 ? h / hkv : 0;
+  return d == tc::D && kernel == 32 && stride == 16 && block_size == 64 && R * hkv == h &&
+         (R == 1 || R == 2 || R == 4 || R == 8 || R == 16);
+}
+
+cudaError_t launch_scores_tc(const Seqs& s, const void* q, const void* k_cmp, int64_t kv_rows, int64_t kv_total,
+                             int h, int hkv, float scale, const float* lse_in, float* scores, int nb_stride,
+                             cudaStream_t st) {
+  if (s.tokens == 0) return cudaSuccess;
+  const int R = h / hkv;
+  const int tpc = tc::ROWS / R;
+  const uint64_t rows = kv_rows > 0 ? (uint64_t)kv_rows : 1;
+  CUtensorMap mq, mk;
+  {
+    const uint64_t dims[3] = {(uint64_t)tc::D, (uint64_t)h, (uint64_t)s.tokens};
+    const uint64_t strides[2] = {(uint64_t)tc::D * 2, (uint64_t)h * tc::D * 2};
+    const uint32_t box[3] = {64, (uint32_t)R, (uint32_t)tpc};
+    if (!tc::make_map(&mq, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)hkv * tc::D, rows};
+    const uint64_t strides[1] = {(uint64_t)hkv * tc::D * 2};
+    const uint32_t box[2] = {64, (uint32_t)tc::KT};
+    if (!tc::make_map(&mk, k_cmp, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  tc::Params p{};
+  p.scores = scores;
+  p.lse_in = lse_in;
+  p.k = (const __nv_bfloat16*)k_cmp;
+  p.kv_total = kv_total;
+  p.seqs = s;
+  p.h = h;
+  p.hkv = hkv;
+  p.R = R;
+  p.kernel = 32;
+  p.stride = 16;
+  p.nb_stride = nb_stride;
+  p.scale_log2 = scale * kLog2e;
+  const dim3 grid((s.max_len + tpc - 1) / tpc, s.n_seqs, hkv);
+  switch (R) {  // the V map is never read in this mode
+    case 1: return run_tc<2, 1>(mq, mk, mk, p, grid, st);
+    case 2: return run_tc<2, 2>(mq, mk, mk, p, grid, st);
+    case 4: return run_tc<2, 4>(mq, mk, mk, p, grid, st);
+    case 8: return run_tc<2, 8>(mq, mk, mk, p, grid, st);
+    case 16: return run_tc<2, 16>(mq, mk, mk, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -46,6 +46,16 @@ cudaError_t launch_transpose_v(const Seqs& s, const void* v, void* vt, int64_t r
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
                                  void* o, float* lse, float* scores, int nb_stride, cudaStream_t st);
+// Block scores (S2 + S3) on the tensor cores, d = 128, kernel 32 / stride 16 / block 64,
+// group size 1..16 (power of two).  kv_rows: rows the key tensor map spans (an upper
+// bound is fine); kv_total: rows the k_cmp buffer holds, or -1 for the packed compressed
+// rows of all sequences (computed on the device).  Tiles reaching past kv_total are
+// read with bounds-checked copies.
+bool scores_tc_supported(int h, int hkv, int d, int kernel, int stride, int block_size);
+cudaError_t launch_scores_tc(const Seqs& s, const void* q, const void* k_cmp, int64_t kv_rows, int64_t kv_total,
+                             int h, int hkv, float scale, const float* lse_in, float* scores, int nb_stride,
+                             cudaStream_t st);
+
 // Status words of the units with bounded waits (NSA_ERR_TIMEOUT once a wait ran out);
 // optionally cleared.
 cudaError_t status_word_dense_tc(int32_t* out, bool reset);

@@ -215,6 +215,12 @@ cudaError_t launch_scores_pool(const Seqs& s, const void* q, const void* k_cmp, 
                                float scale, const float* lse_in, float* scores, int nb_stride,
                                cudaStream_t st) {
   if (s.tokens == 0) return cudaSuccess;
+  if (k_cmp && scores_tc_supported(h, hkv, d, kCmpKernel, kCmpStride, 64)) {
+    // packed compressed rows: exact for the dense layout, an upper bound otherwise
+    const int64_t exact = s.cu ? -1 : (int64_t)s.n_seqs * (s.T >= kCmpKernel ? (s.T - kCmpKernel) / kCmpStride + 1 : 0);
+    const int64_t bound = s.cu ? s.tokens / kCmpStride + s.n_seqs : exact;
+    return launch_scores_tc(s, q, k_cmp, bound, exact, h, hkv, scale, lse_in, scores, nb_stride, st);
+  }
   ScoresParams p{};
   p.q = (const __nv_bfloat16*)q;
   p.kc = (const __nv_bfloat16*)k_cmp;

@@ -71,6 +71,26 @@ def test_cmp_scores_pool(H, hkv, d):
     np.testing.assert_allclose(g, ref, rtol=1e-4, atol=1e-9)
 
 
+@pytest.mark.parametrize("B,T,H,hkv", [(2, 1000, 16, 1), (3, 4100, 32, 4), (1, 31, 16, 2)])
+def test_cmp_scores_pool_dense(B, T, H, hkv):
+    """Dense layout: the compressed-key buffer holds exactly B * n_c(T) rows, so the last
+    64-key tile of the last sequence reaches past it (read with bounds checks)."""
+    d = 128
+    cu = gen.dense_cu_seqlens(B, T)
+    rng = _rng(31)
+    q = gen.normal(rng, (B * T, H, d), "bf16")
+    k = gen.normal(rng, (B * T, hkv, d), "bf16")
+    _, kc = orc.compress(k, cu)
+    ref = orc.cmp_scores_pool(q, kc, cu)
+    kcd = dev(kc).view(B, -1, hkv, d) if kc.shape[0] else None
+    out = nsa.nsa_cmp_scores_pool(dev(q).view(B, T, H, d), kcd, hkv)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    g = host(out).astype(np.float64).reshape(ref.shape)
+    assert np.all(g[ref == 0] == 0)
+    np.testing.assert_allclose(g, ref, rtol=1e-4, atol=1e-9)
+
+
 def test_cmp_scores_pool_with_given_normaliser():
     lengths = [1200, 333]
     cu = gen.varlen_cu_seqlens(lengths)
