@@ -266,6 +266,11 @@ def bench_selection(torch, nsa, device, steps, warmup, flush):
             "launches_per_step": 3}
 
 
+# kernels of one layer call: compress K, compress V, transpose V_cmp, transpose V,
+# compressed branch + block scores, top-k, selected branch, sliding branch, gated sum
+LAYER_LAUNCHES = 9
+
+
 def bench_layer(torch, nsa, device, steps, warmup, flush, T=65536):
     w = gen.layer(T=T)
     q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
@@ -288,7 +293,7 @@ def bench_layer(torch, nsa, device, steps, warmup, flush, T=65536):
     return {"workload": f"layer B=1 T={w.tokens} H=64 Hkv=4 d=128 bf16 (compressed 32/16 + selected 64x16 + window 512 "
                         "+ sigmoid gates)",
             "ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": w.tokens / (ms * 1e-3),
-            "flops_per_step": flops, "launches_per_step": 8}
+            "flops_per_step": flops, "launches_per_step": LAYER_LAUNCHES}
 
 
 # ----------------------------------------------------------------------------- main arm
@@ -422,7 +427,7 @@ def main():
         torch.cuda.empty_cache()
         try:
             line["layer"] = bench_layer(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush)
-            line["gpu_launches"] += 8 * max(3, args.steps // 2)
+            line["gpu_launches"] += LAYER_LAUNCHES * max(3, args.steps // 2)
         except Exception as e:
             line["layer"] = {"error": repr(e)}
 
@@ -437,7 +442,6 @@ def main():
             rf["mma_sync_peak_tflops"] = pr["mma_sync_bf16_tflops"]
             rf["frac_of_mma_sync"] = kernel_tflops / pr["mma_sync_bf16_tflops"]
             if "tflops" in line.get("layer", {}):
-                line["layer"]["frac_of_mma_sync"] = line["layer"]["tflops"] / pr["mma_sync_bf16_tflops"]
                 line["layer"]["frac_of_bf16_peak"] = line["layer"]["tflops"] / peaks["bf16_tflops"]
         except Exception as e:
             line["probes"] = {"error": repr(e)}
