@@ -90,7 +90,11 @@ const char* nsa_last_error(void) { return g_err; }
 
 nsa_status nsa_device_status(int32_t* status, int reset) {
   NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
-  return cuda_status(status_word_dense_tc(status, reset != 0), "nsa_device_status");
+  int32_t a = 0, b = 0;
+  cudaError_t e = status_word_dense_tc(&a, reset != 0);
+  if (e == cudaSuccess) e = status_word_decode(&b, reset != 0);
+  *status = a ? a : b;
+  return cuda_status(e, "nsa_device_status");
 }
 
 nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,
@@ -305,8 +309,7 @@ nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int
   a.tile_ml = reinterpret_cast<float*>(w + l.tile_ml);
   a.part_o = reinterpret_cast<float*>(w + l.part_o);
   a.part_ml = reinterpret_cast<float*>(w + l.part_ml);
-  a.select_count = reinterpret_cast<int*>(w + l.counters);
-  a.merge_count = a.select_count + (size_t)batch * h_kv;
+  a.counters = reinterpret_cast<int*>(w + l.counters);
   a.n_split = l.n_split;
   return cuda_status(launch_decode(a, stream), "nsa_sparse_decode");
 }

@@ -5,23 +5,28 @@
 // selection picks topk = 64 blocks and the sparse attention runs over those blocks only.
 //
 // GB300 design.  A decode step has only batch * h_kv independent rows, far fewer than
-// the 152 SMs, and the path is HBM bound (compressed keys plus the chosen K/V blocks),
-// so both passes are split to fill the machine:
-//   1. decode_score_select: one warp per 64-key tile of compressed keys, for every
-//      (sequence, kv-head); it writes base-2 scaled scores and each tile's (max, sum) per
-//      head.  The last CTA of a (sequence, kv-head) to finish (arrival counter) folds the
-//      tile partials into the per-head normaliser, pools the group probabilities to
-//      64-token blocks in shared memory and runs the warp top-k.
-//   2. the selected-attention kernel in split mode (several CTAs per row, each over a
-//      slice of the block list); the last split CTA merges the softmax states.
-// A memset of the arrival counters and the two kernels are stream ordered and capture
-// into one CUDA graph.
+// the 152 SMs, and the path is HBM bound (compressed keys plus the chosen K/V blocks).
+// The whole step is one persistent kernel (cooperative launch, every CTA resident) that
+// takes work items from a global queue:
+//   score items (row, group of four 64-key tiles of compressed keys), row by row: each
+//      warp scores one tile for the row's heads and writes the tile's (max, sum) per
+//      head and its pooled block partials; the last item of a row (arrival counter)
+//      folds the partials into block scores, runs a CTA-wide radix-select top-k and
+//      publishes the
+//      row's block list with a release flag;
+//   attention items (row, split of the block list): wait for the row's flag (bounded),
+//      stream the split's blocks (four warps, 16-key slices, cp.async rings), write the
+//      split's softmax state; the last split of a row merges them into O.
+// Queue order puts every score item before every attention item, so a waiting CTA only
+// waits for score work that is already running; rows finish scoring in order, so the
+// gather of early rows overlaps the scoring of later ones.  A memset of the counters
+// and the kernel are stream ordered and capture into one CUDA graph.
+#include "attend.cuh"
 #include "launch.h"
+#include "sm100.cuh"
 #include "topk.cuh"
 
 namespace nsa {
-
-cudaError_t launch_decode_attn(const DecodeArgs& a, cudaStream_t st);
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -33,15 +38,13 @@ DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int ke
   const int nc_max = max_len >= kernel ? (max_len - kernel) / stride + 1 : 0;
   l.n_tiles = (nc_max + 63) / 64;
   l.nc_pad = l.n_tiles * 64;
-#ifdef NSA_DECODE_SPLIT
-  int ns = NSA_DECODE_SPLIT;
-#else
-  // as many splits as keep the attention grid within one resident wave (2 CTAs per SM)
+  // about one attention item per resident CTA slot (2 per SM), at most 16 splits
   const int64_t units = (int64_t)batch * hkv * rtiles;
   int ns = (int)(2 * 152 / (units > 0 ? units : 1));
   ns = ns < 1 ? 1 : (ns > 16 ? 16 : ns);
-#endif
-  l.n_split = ns < k ? ns : k;
+  ns = ns < k ? ns : k;
+  const int eps = (k + ns - 1) / ns;  // entries per split; no split is left empty
+  l.n_split = (k + eps - 1) / eps;
   size_t off = 0;
   l.z = off;  // per-tile pooled partial sums [batch, hkv, n_tiles, 16 blocks, r]
   off = align256(off + (size_t)batch * hkv * l.n_tiles * 16 * r * 4);
@@ -54,7 +57,8 @@ DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int ke
   l.part_ml = off;
   off = align256(off + (size_t)batch * hkv * rtiles * l.n_split * 16 * 2 * 4);
   l.counters = off;
-  l.counter_bytes = (size_t)batch * hkv * (1 + rtiles) * 4;
+  // work queue head, score arrivals per row, split arrivals per row, ready flags per row
+  l.counter_bytes = (size_t)(1 + (size_t)batch * hkv * (2 + rtiles)) * 4;
   off = align256(off + l.counter_bytes);
   l.total = off;
   return l;
@@ -62,29 +66,44 @@ DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int ke
 
 constexpr int kTile = 64;
 
-// grid (ceil(n_tiles/4), batch, hkv), 4 warps; warp w scores compressed tile blockIdx.x*4+w;
-// the last CTA of each (sequence, kv-head) then selects its blocks.
 constexpr int kMaxTiles = 64;  // max_len <= 65536
+constexpr int kNW = 4;         // warps per CTA
 
-struct ScoreSelectParams {
+struct DecodeParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* kc;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
   const int32_t* seqlens;
-  int h, hkv, nc_stride, nc_pad, n_tiles, n_init, n_local, k;
+  int h, hkv, max_len, nc_stride, n_tiles, n_groups, n_init, n_local, k, n_split, eps;
   float scale_log2;
   float* z;
   float* tile_ml;
+  float* part_o;
+  float* part_ml;
   int32_t* idx;
-  int* count;
+  __nv_bfloat16* o;
+  int* queue;        // [1]
+  int* score_count;  // [rows]
+  int* merge_count;  // [rows]
+  int* ready;        // [rows]
 };
 
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+
+// Score item: tiles grp*4 + warp of row (b, g); the last item of the row selects.
 template <int D, int R, int NPL>
-__global__ void __launch_bounds__(128) decode_score_select(const ScoreSelectParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_last;
+__device__ __forceinline__ void score_item(const DecodeParams& p, int b, int g, int grp, uint8_t* smem, int* s_flag,
+                                           int* s_topk) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y, g = blockIdx.z;
-  const int tile = blockIdx.x * 4 + warp;
+  const int tile = grp * kNW + warp;
   const int L = p.seqlens[b];
   const int n_c = num_cmp(L, 32, 16);
   const int nca = num_causal_cmp(L - 1, n_c, 32, 16);
@@ -159,15 +178,12 @@ __global__ void __launch_bounds__(128) decode_score_select(const ScoreSelectPara
       }
     }
   }
-  // allow the dependent attention grid to start its prologue; it waits for this grid's
-  // writes (griddepcontrol.wait) before reading the block lists
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  // arrival: the last CTA of this (sequence, kv-head) runs the selection
+  // arrival: the last item of this (sequence, kv-head) runs the selection
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&p.count[row], 1) == (int)gridDim.x - 1;
+  if (threadIdx.x == 0) *s_flag = atomicAdd(&p.score_count[row], 1) == p.n_groups - 1;
   __syncthreads();
-  if (!s_last) return;
+  if (!*s_flag) return;
   __threadfence();
   // Every global load of the selection is issued in one batch (data written by other
   // SMs costs a full L2 round trip each time): the row's tile (max, sum) pairs go to
@@ -245,57 +261,223 @@ __global__ void __launch_bounds__(128) decode_score_select(const ScoreSelectPara
     }
   }
   __syncthreads();
-  // the whole CTA runs the top-k: this tail sits on the critical path of the step
-  __shared__ int s_topk[3 * 4];
-  block_topk<NPL * 32 / 128, 128>(sc, nb, (L - 1) / 64, p.n_init, p.n_local, p.k, p.idx + row * p.k, s_topk);
+  // the whole CTA runs the top-k (radix select, one barrier per pass), then publishes
+  // the list: every thread's writes, the barrier, and one release store
+  block_topk<NPL * 32 / (kNW * 32), kNW * 32>(sc, nb, (L - 1) / 64, p.n_init, p.n_local, p.k, p.idx + row * p.k,
+                                               s_topk);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) st_release(&p.ready[row], 1);
+}
+
+// Attention item: split `sp` of row (b, g).  Four warps each own a 16-key slice of every
+// block in the split's part of the list (warp_attend); the CTA merges the warps, writes
+// the split's state O * 2^-M, (M, L); the last split of the row merges all of them.
+template <int D, int R, int NSTAGE>
+__device__ __forceinline__ void attn_item(const DecodeParams& p, int b, int g, int sp, uint8_t* smem, int* s_flag,
+                                          int (*s_list)[64]) {
+  constexpr int BS = 64;
+  constexpr int STAGE_BYTES = 2 * 16 * D * 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slice = warp;  // four warps, four 16-key slices of a 64-key block
+  const int row = b * p.hkv + g;
+  const int t = p.seqlens[b] - 1;
+  const int64_t kv_base = (int64_t)b * p.max_len;
+  const int e0 = sp * p.eps, e1 = min(p.k, e0 + p.eps);
+  const int hbase = g * R;
+  const int rlo = lane >> 2, rhi = rlo + 8;
+  const __nv_bfloat16* qb = p.q + ((int64_t)b * p.h + hbase) * D;
+  uint32_t qa[D / 16][4];
+  load_a_frags<D>(qa, rlo < R ? qb + rlo * D : nullptr, rhi < R ? qb + rhi * D : nullptr, lane);
+  // the row's block list is ready once its selecting CTA has released the flag
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    if (ld_acquire(&p.ready[row]) == 0) {
+      const unsigned long long t0 = tc::globaltimer();
+      while (ld_acquire(&p.ready[row]) == 0) {
+        if (tc::device_status_set() || tc::globaltimer() - t0 > tc::kWaitNs) {
+          atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    *s_flag = ok;
+  }
+  __syncthreads();
+  if (!*s_flag) return;
+  // this warp's work list: the split's blocks whose slice starts at or before t
+  const int32_t* il = p.idx + (int64_t)row * p.k;
+  int cnt = 0;
+  for (int base = e0; base < e1; base += 32) {
+    const int e = base + lane;
+    int blk = -1;
+    bool ok = false;
+    if (e < e1) {
+      blk = __ldcg(il + e);
+      ok = blk >= 0 && (int64_t)blk * BS + slice * 16 <= t;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    if (ok) s_list[warp][cnt + __popc(m & ((1u << lane) - 1u))] = blk;
+    cnt += __popc(m);
+  }
+  __syncwarp();
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  WarpState st = warp_attend<D, BS, NSTAGE>(s_list[warp], cnt, slice, p.k_cache + (kv_base * p.hkv + g) * D,
+                                            p.v_cache + (kv_base * p.hkv + g) * D, (int64_t)p.hkv * D, t,
+                                            p.scale_log2, qa, smem_u32(smem) + warp * NSTAGE * STAGE_BYTES,
+                                            p.k_cache, o, lane);
+  __syncthreads();  // every warp is done with its ring: the merge reuses the shared memory
+  cta_merge<D, kNW>(reinterpret_cast<float*>(smem), o, st, warp, lane);
+  const int64_t slot = ((int64_t)row * p.n_split + sp) * 16;
+  if (warp == 0) {
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<float2*>(p.part_o + (slot + rlo) * D + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(p.part_o + (slot + rhi) * D + col) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if ((lane & 3) == 0) {
+      p.part_ml[(slot + rlo) * 2] = st.m0;
+      p.part_ml[(slot + rlo) * 2 + 1] = st.l0;
+      p.part_ml[(slot + rhi) * 2] = st.m1;
+      p.part_ml[(slot + rhi) * 2 + 1] = st.l1;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = atomicAdd(&p.merge_count[row], 1) == p.n_split - 1;
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  const int hr = threadIdx.x >> 3;  // head row of the group, 8 threads per row
+  if (hr >= R) return;
+  const int64_t base = (int64_t)row * p.n_split;
+  float M = kNegInf;
+  for (int s2 = 0; s2 < p.n_split; ++s2) M = fmaxf(M, __ldcg(p.part_ml + ((base + s2) * 16 + hr) * 2));
+  const float Mu = M == kNegInf ? 0.f : M;
+  float L = 0.f;
+  float acc[D / 8];
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
+  const int cl = threadIdx.x & 7;  // columns cl, cl+8, ... : 8 lanes read 32 contiguous bytes
+  for (int s2 = 0; s2 < p.n_split; ++s2) {
+    const int64_t sl = (base + s2) * 16 + hr;
+    const float f = ex2(__ldcg(p.part_ml + sl * 2) - Mu);
+    L += f * __ldcg(p.part_ml + sl * 2 + 1);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) acc[c] += f * __ldcg(p.part_o + sl * D + cl + 8 * c);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __nv_bfloat16* dst = p.o + ((int64_t)b * p.h + hbase + hr) * D;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) dst[cl + 8 * c] = __float2bfloat16_rn(acc[c] * inv);
+}
+
+constexpr int kDecodeStages = 3;  // 96 KB of rings: two CTAs per SM
+constexpr int kDecodeSmem = kNW * kDecodeStages * 2 * 16 * 128 * 2;
+
+template <int R, int NPL>
+__global__ void __launch_bounds__(kNW * 32, 2) decode_step(const DecodeParams p, int rows) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_item, s_flag;
+  __shared__ int s_topk[2 * 16 * kNW + 2 * kNW];  // top-k scratch
+  __shared__ int s_list[kNW][64];
+  const int n_score = rows * p.n_groups;
+  const int n_items = n_score + rows * p.n_split;
+  for (;;) {
+    if (threadIdx.x == 0) s_item = atomicAdd(p.queue, 1);
+    __syncthreads();
+    const int item = s_item;
+    __syncthreads();  // s_item is rewritten only after every thread has read it
+    if (item >= n_items || tc::device_status_set()) break;
+    if (item < n_score) {
+      const int row = item / p.n_groups;
+      score_item<128, R, NPL>(p, row / p.hkv, row % p.hkv, item % p.n_groups, smem, &s_flag, s_topk);
+    } else {
+      const int a = item - n_score, row = a / p.n_split;
+      attn_item<128, R, kDecodeStages>(p, row / p.hkv, row % p.hkv, a % p.n_split, smem, &s_flag, s_list);
+    }
+    __syncthreads();
+  }
 }
 
 template <int R, int NPL>
-static cudaError_t run_score_select(const DecodeArgs& a, const DecodeLayout& l, cudaStream_t st) {
-  constexpr int bytes = 4 * kTile * 128 * 2;
-  static_assert(2 * R * kMaxTiles * 4 + NPL * 32 * 4 + kMaxTiles * R * 4 <= bytes,
-                "select scratch must fit the tile buffers");
-  auto kern = decode_score_select<128, R, NPL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+static cudaError_t run_decode(const DecodeArgs& a, const DecodeLayout& l, cudaStream_t st) {
+  static_assert(2 * R * kMaxTiles * 4 + NPL * 32 * 4 + kMaxTiles * R * 4 <= kNW * kTile * 128 * 2,
+                "select scratch must fit the score tile buffers");
+  static_assert(kNW * kTile * 128 * 2 <= kDecodeSmem, "score tiles must fit the rings");
+  auto kern = decode_step<R, NPL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
   if (e != cudaSuccess) return e;
-  ScoreSelectParams p{};
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNW * 32, kDecodeSmem)) != cudaSuccess)
+    return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  DecodeParams p{};
   p.q = (const __nv_bfloat16*)a.q;
   p.kc = (const __nv_bfloat16*)a.kc_cache;
+  p.k_cache = (const __nv_bfloat16*)a.k_cache;
+  p.v_cache = (const __nv_bfloat16*)a.v_cache;
   p.seqlens = a.seqlens;
   p.h = a.h;
   p.hkv = a.hkv;
+  p.max_len = a.max_len;
   p.nc_stride = a.max_len >= a.kernel ? (a.max_len - a.kernel) / a.stride + 1 : 0;
-  p.nc_pad = l.nc_pad;
   p.n_tiles = l.n_tiles;
+  p.n_groups = l.n_tiles > 0 ? (l.n_tiles + kNW - 1) / kNW : 1;  // one item selects even without keys
   p.n_init = a.n_init;
   p.n_local = a.n_local;
   p.k = a.k;
+  p.n_split = l.n_split;
+  p.eps = (a.k + l.n_split - 1) / l.n_split;
   p.scale_log2 = a.scale * kLog2e;
   p.z = a.z;
   p.tile_ml = a.tile_ml;
+  p.part_o = a.part_o;
+  p.part_ml = a.part_ml;
   p.idx = a.idx;
-  p.count = a.select_count;
-  dim3 grid((l.n_tiles + 3) / 4 > 0 ? (l.n_tiles + 3) / 4 : 1, a.batch, a.hkv);
-  kern<<<grid, 128, bytes, st>>>(p);
-  return cudaGetLastError();
+  p.o = (__nv_bfloat16*)a.o;
+  const int rows = a.batch * a.hkv;
+  p.queue = a.counters;
+  p.score_count = a.counters + 1;
+  p.merge_count = p.score_count + rows;
+  p.ready = p.merge_count + rows;
+  const int n_items = rows * (p.n_groups + p.n_split);
+  // persistent: at most one CTA per resident slot (the cooperative launch checks it)
+  const int grid = n_items < per_sm * sms ? n_items : per_sm * sms;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNW * 32);
+  cfg.dynamicSmemBytes = kDecodeSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, rows);
 }
 
 template <int R>
 static cudaError_t run_decode_r(const DecodeArgs& a, const DecodeLayout& l, cudaStream_t st) {
   const int nb_max = (a.max_len + 63) / 64;
-  cudaError_t e;
-  if (nb_max <= 4 * 32) e = run_score_select<R, 4>(a, l, st);
-  else if (nb_max <= 8 * 32) e = run_score_select<R, 8>(a, l, st);
-  else if (nb_max <= 16 * 32) e = run_score_select<R, 16>(a, l, st);
-  else e = run_score_select<R, 32>(a, l, st);
-  if (e != cudaSuccess) return e;
-  return launch_decode_attn(a, st);
+  if (nb_max <= 4 * 32) return run_decode<R, 4>(a, l, st);
+  if (nb_max <= 8 * 32) return run_decode<R, 8>(a, l, st);
+  if (nb_max <= 16 * 32) return run_decode<R, 16>(a, l, st);
+  return run_decode<R, 32>(a, l, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   const DecodeLayout l = decode_layout(a.batch, a.max_len, a.h, a.hkv, a.d, a.kernel, a.stride, a.block_size, a.k);
-  // arrival counters start at zero on every call (a memset, not an allocation)
-  cudaError_t e = cudaMemsetAsync(a.select_count, 0, l.counter_bytes, st);
+  if (!a.o || !a.part_o || !a.part_ml || !a.counters || !a.idx) return cudaErrorInvalidValue;
+  // queue, arrival counters and ready flags start at zero on every call (a memset)
+  cudaError_t e = cudaMemsetAsync(a.counters, 0, l.counter_bytes, st);
   if (e != cudaSuccess) return e;
   switch (a.h / a.hkv) {
     case 1: return run_decode_r<1>(a, l, st);
@@ -305,5 +487,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     default: return run_decode_r<16>(a, l, st);
   }
 }
+
+NSA_STATUS_ACCESSOR(decode)
 
 }  // namespace nsa

@@ -59,6 +59,7 @@ cudaError_t launch_scores_tc(const Seqs& s, const void* q, const void* k_cmp, in
 // Status words of the units with bounded waits (NSA_ERR_TIMEOUT once a wait ran out);
 // optionally cleared.
 cudaError_t status_word_dense_tc(int32_t* out, bool reset);
+cudaError_t status_word_decode(int32_t* out, bool reset);
 
 cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gates, void* o, cudaStream_t st);
@@ -75,8 +76,7 @@ struct DecodeArgs {
   float* tile_ml;  // [batch, hkv, n_tiles, r, 2]
   float* part_o;   // [batch, hkv * rtiles, n_split, 16, d]
   float* part_ml;  // [batch, hkv * rtiles, n_split, 16, 2]
-  int* select_count;  // [batch, hkv] score CTAs done (zeroed per call)
-  int* merge_count;   // [batch, hkv * rtiles] split CTAs done (zeroed per call)
+  int* counters;  // DecodeLayout::counter_bytes: queue head, arrivals, ready flags (zeroed per call)
   int n_split;
 };
 struct DecodeLayout {

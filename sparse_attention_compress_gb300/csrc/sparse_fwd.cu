@@ -1,4 +1,4 @@
-// Selected-block attention (prefill and the split decode pass).
+// Selected-block attention (prefill).
 //
 // [TileLang-NSA] "TileLang operator development: Native Sparse Attention", sec. 2:
 // for each entry of a query's block list, the block starting at index*block_size is
@@ -27,13 +27,6 @@ struct SparseParams {
   Seqs seqs;
   int h, hkv, S;
   float scale_log2;
-  // decode: query row b sits at t = seqlens[b]-1 over cache rows b*max_len ..
-  const int32_t* seqlens;
-  int max_len;
-  int entries_per_split;
-  float* part_o;
-  float* part_ml;
-  int* merge_count;  // decode: [batch, gridDim.y] split arrivals, zero at launch
 };
 
 #ifndef NSA_PREFILL_NSTAGE
@@ -43,11 +36,8 @@ struct SparseParams {
 #define NSA_PREFILL_MINBLOCKS 3
 #endif
 
-#ifndef NSA_DECODE_NSTAGE
-#define NSA_DECODE_NSTAGE 3  // 96 KB: two split CTAs per SM, two slices in flight per warp
-#endif
 
-template <int D, int BS, int NSTAGE, bool DECODE>
+template <int D, int BS, int NSTAGE>
 __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(const SparseParams p) {
   constexpr int NW = 4;
   constexpr int NSLICE = BS / 16;
@@ -63,18 +53,9 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   const int g = blockIdx.y / rtiles, rt = blockIdx.y % rtiles;
 
   const int64_t qrow = blockIdx.x;
-  int64_t kv_base;
-  int t;
-  if (DECODE) {
-    t = p.seqlens[qrow] - 1;
-    kv_base = qrow * (int64_t)p.max_len;
-  } else {
-    const int sq = seq_of_token(p.seqs, qrow);
-    kv_base = seq_start(p.seqs, sq);
-    t = (int)(qrow - kv_base);
-  }
-  const int e0 = DECODE ? blockIdx.z * p.entries_per_split : 0;
-  const int e1 = DECODE ? min(p.S, e0 + p.entries_per_split) : p.S;
+  const int sq = seq_of_token(p.seqs, qrow);
+  const int64_t kv_base = seq_start(p.seqs, sq);
+  const int t = (int)(qrow - kv_base);
 
   // Q fragments of the group's heads (rows past the group read as zero)
   const int hbase = g * r + rt * 16;
@@ -83,20 +64,16 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   uint32_t qa[D / 16][4];
   load_a_frags<D>(qa, rt * 16 + rlo < r ? qb + rlo * D : nullptr, rt * 16 + rhi < r ? qb + rhi * D : nullptr,
                   lane);
-  // decode runs as a programmatic dependent launch: everything above overlaps the
-  // selection kernel; the block lists it writes are read only after this point
-  if (DECODE) asm volatile("griddepcontrol.wait;\n" ::: "memory");
-
   // this warp's work list: listed blocks whose slice starts at or before t
   const int32_t* il = p.idx + (qrow * p.hkv + g) * p.S;
   int cnt = 0;
-  for (int base = e0; base < e1; base += 32) {
+  for (int base = 0; base < p.S; base += 32) {
     const int e = base + lane;
     int blk = -1;
     bool ok = false;
-    if (e < e1) {
+    if (e < p.S) {
       blk = il[e];
-      ok = ((e - e0) % NGROUP == grp) && blk >= 0 && (int64_t)blk * BS + slice * 16 <= t;
+      ok = (e % NGROUP == grp) && blk >= 0 && (int64_t)blk * BS + slice * 16 <= t;
     }
     const unsigned m = __ballot_sync(0xffffffffu, ok);
     if (ok) s_list[warp][cnt + __popc(m & ((1u << lane) - 1u))] = blk;
@@ -114,8 +91,8 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   __syncthreads();  // every warp is done with its ring: the merge reuses the shared memory
   cta_merge<D, NW>(reinterpret_cast<float*>(smem), o, st, warp, lane);
 
-  if (!DECODE) {
-    if (warp != 0) return;
+  if (warp != 0) return;
+  {
     const float u0 = st.m0 == kNegInf ? 0.f : st.m0, u1 = st.m1 == kNegInf ? 0.f : st.m1;
     const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
     const bool w0 = rt * 16 + rlo < r, w1 = rt * 16 + rhi < r;
@@ -131,55 +108,7 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
       if (w0) p.lse[qrow * p.h + hbase + rlo] = st.l0 > 0.f ? (u0 + __log2f(st.l0)) * kLn2 : kNegInf;
       if (w1) p.lse[qrow * p.h + hbase + rhi] = st.l1 > 0.f ? (u1 + __log2f(st.l1)) * kLn2 : kNegInf;
     }
-    return;
   }
-
-  // decode: this split's unnormalised state O * 2^-u, (M, L); the last split merges
-  const int64_t slot = ((qrow * gridDim.y + blockIdx.y) * gridDim.z + blockIdx.z) * 16;
-  if (warp == 0) {
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      const int col = nt * 8 + (lane & 3) * 2;
-      *reinterpret_cast<float2*>(p.part_o + (slot + rlo) * D + col) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(p.part_o + (slot + rhi) * D + col) = make_float2(o[nt][2], o[nt][3]);
-    }
-    if ((lane & 3) == 0) {
-      p.part_ml[(slot + rlo) * 2] = st.m0;
-      p.part_ml[(slot + rlo) * 2 + 1] = st.l0;
-      p.part_ml[(slot + rhi) * 2] = st.m1;
-      p.part_ml[(slot + rhi) * 2 + 1] = st.l1;
-    }
-  }
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0)
-    s_last = atomicAdd(&p.merge_count[qrow * gridDim.y + blockIdx.y], 1) == (int)gridDim.z - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int row = threadIdx.x >> 3;
-  if (rt * 16 + row >= r) return;
-  const int64_t base = (qrow * gridDim.y + blockIdx.y) * gridDim.z;
-  float M = kNegInf;
-  for (int sp = 0; sp < (int)gridDim.z; ++sp) M = fmaxf(M, __ldcg(p.part_ml + ((base + sp) * 16 + row) * 2));
-  const float Mu = M == kNegInf ? 0.f : M;
-  float L = 0.f;
-  float acc[D / 8];
-#pragma unroll
-  for (int c = 0; c < D / 8; ++c) acc[c] = 0.f;
-  const int cl = threadIdx.x & 7;  // columns cl, cl+8, ... : 8 lanes read 32 contiguous bytes
-  for (int sp = 0; sp < (int)gridDim.z; ++sp) {
-    const int64_t sl = (base + sp) * 16 + row;
-    const float f = ex2(__ldcg(p.part_ml + sl * 2) - Mu);
-    L += f * __ldcg(p.part_ml + sl * 2 + 1);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) acc[c] += f * __ldcg(p.part_o + sl * D + cl + 8 * c);
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* dst = p.o + (qrow * p.h + hbase + row) * D;
-#pragma unroll
-  for (int c = 0; c < D / 8; ++c) dst[cl + 8 * c] = __float2bfloat16_rn(acc[c] * inv);
 }
 
 
@@ -246,30 +175,16 @@ __global__ void __launch_bounds__(128) sparse_fwd_f32(const float* __restrict__ 
   }
 }
 
-template <int D, int BS, int NSTAGE, bool DECODE>
+template <int D, int BS, int NSTAGE>
 static cudaError_t run_mma(const SparseParams& p, dim3 grid, cudaStream_t st) {
   constexpr int pipe = 4 * NSTAGE * 2 * 16 * D * 2;
   constexpr int merge = merge_bytes<D, 4>();
   constexpr int bytes = pipe > merge ? pipe : merge;
-  auto kern = sparse_fwd_mma<D, BS, NSTAGE, DECODE>;
+  auto kern = sparse_fwd_mma<D, BS, NSTAGE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  if (!DECODE) {
-    kern<<<grid, 128, bytes, st>>>(p);
-    return cudaGetLastError();
-  }
-  // decode: launched as a programmatic dependent of the selection kernel
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  kern<<<grid, 128, bytes, st>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const void* v,
@@ -303,39 +218,15 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   dim3 grid((unsigned)s.tokens, hkv * ((r + 15) / 16), 1);
   if (d == 128) {
     constexpr int NS = NSA_PREFILL_NSTAGE;
-    if (block_size == 64) return run_mma<128, 64, NS, false>(p, grid, st);
-    if (block_size == 32) return run_mma<128, 32, NS, false>(p, grid, st);
-    return run_mma<128, 16, NS, false>(p, grid, st);
+    if (block_size == 64) return run_mma<128, 64, NS>(p, grid, st);
+    if (block_size == 32) return run_mma<128, 32, NS>(p, grid, st);
+    return run_mma<128, 16, NS>(p, grid, st);
   }
   constexpr int NS = NSA_PREFILL_NSTAGE;
-  if (block_size == 64) return run_mma<64, 64, NS, false>(p, grid, st);
-  if (block_size == 32) return run_mma<64, 32, NS, false>(p, grid, st);
-  return run_mma<64, 16, NS, false>(p, grid, st);
+  if (block_size == 64) return run_mma<64, 64, NS>(p, grid, st);
+  if (block_size == 32) return run_mma<64, 32, NS>(p, grid, st);
+  return run_mma<64, 16, NS>(p, grid, st);
 }
 
 // Decode attention over the chosen blocks, split over the list, then merged.
-cudaError_t launch_decode_attn(const DecodeArgs& a, cudaStream_t st) {
-  SparseParams p{};
-  p.q = (const __nv_bfloat16*)a.q;
-  p.k = (const __nv_bfloat16*)a.k_cache;
-  p.v = (const __nv_bfloat16*)a.v_cache;
-  p.idx = a.idx;
-  p.h = a.h;
-  p.hkv = a.hkv;
-  p.S = a.k;
-  p.scale_log2 = a.scale * kLog2e;
-  p.seqlens = a.seqlens;
-  p.max_len = a.max_len;
-  p.entries_per_split = (a.k + a.n_split - 1) / a.n_split;
-  p.part_o = a.part_o;
-  p.part_ml = a.part_ml;
-  p.merge_count = a.merge_count;
-  p.o = (__nv_bfloat16*)a.o;  // the last split CTA writes the merged row here
-  if (!p.o || !p.part_o || !p.part_ml || !p.merge_count || !p.idx) return cudaErrorInvalidValue;
-  const int r = a.h / a.hkv;
-  const int rtiles = (r + 15) / 16;
-  dim3 grid(a.batch, a.hkv * rtiles, a.n_split);
-  return run_mma<128, 64, NSA_DECODE_NSTAGE, true>(p, grid, st);
-}
-
 }  // namespace nsa

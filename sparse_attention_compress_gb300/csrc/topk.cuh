@@ -47,6 +47,66 @@ __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int k, int lane
   return __shfl_sync(0xffffffffu, v, k - 1);
 }
 
+// Exact k-th largest of the warp's candidate keys (lane owns keys[i] for block
+// i*32 + lane < ncand) by a radix select on 4-bit digits.  Bits shared by every
+// candidate (found with a warp AND / OR) take no pass; each pass counts the digits of
+// the keys that match the digits fixed so far in sixteen 8-bit counters per lane
+// (registers, no shared-memory atomics) and sums each counter over the warp.
+// Returns the key; *need = how many keys equal to it belong to the top k.
+template <int NPL>
+__device__ __forceinline__ uint32_t warp_radix_kth(const uint32_t (&key)[NPL], int ncand, int k, int* need,
+                                                   int lane) {
+  const int n_it = (ncand + 31) / 32;
+  uint32_t all_and = 0xffffffffu, all_or = 0u;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (i < n_it && i * 32 + lane < ncand) {
+      all_and &= key[i];
+      all_or |= key[i];
+    }
+  all_and = __reduce_and_sync(0xffffffffu, all_and);
+  all_or = __reduce_or_sync(0xffffffffu, all_or);
+  const uint32_t varying = all_and ^ all_or;
+  if (varying == 0u) {  // every candidate key is the same
+    *need = k;
+    return all_and;
+  }
+  int shift = ((31 - __clz(varying)) / 4) * 4;  // lowest bit of the highest varying digit
+  uint32_t pmask = shift + 4 >= 32 ? 0u : (0xffffffffu << (shift + 4));
+  uint32_t prefix = all_and & pmask;
+  int left = k;
+#pragma unroll 1
+  for (; shift >= 0; shift -= 4) {
+    unsigned long long lo = 0ull, hi = 0ull;  // digits 0..7 and 8..15, 8 bits each
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (i < n_it && i * 32 + lane < ncand && (key[i] & pmask) == prefix) {
+        const uint32_t d = (key[i] >> shift) & 15u;
+        const unsigned long long inc = 1ull << ((d & 7u) * 8u);
+        if (d < 8u) lo += inc; else hi += inc;
+      }
+    // from the top digit down: the digit where the count of larger-or-equal keys reaches left
+    int run = 0, dsel = 0, above = 0;
+    bool found = false;
+#pragma unroll
+    for (int q = 15; q >= 0; --q) {
+      const unsigned f = (unsigned)(((q < 8 ? lo : hi) >> ((q & 7) * 8)) & 0xffull);
+      const int c = (int)__reduce_add_sync(0xffffffffu, f);
+      if (!found && run + c >= left) {
+        found = true;
+        dsel = q;
+        above = run;
+      }
+      run += c;
+    }
+    left -= above;
+    prefix |= (uint32_t)dsel << shift;
+    pmask |= 15u << shift;
+  }
+  *need = left;
+  return prefix;
+}
+
 // row: scores of blocks 0..nb-1 (global or shared).  own = t / block_size.  Lane owns
 // blocks lane, lane + 32, ... (coalesced loads).  cand_key / cand_idx: 64 entries of
 // warp-private shared memory.
@@ -55,7 +115,7 @@ __device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int k, int lane
 // maxima (k lanes hold a key at least that large), so the top k lie among the keys at or
 // above it; those candidates (usually a few more than k) are ranked exactly by (key
 // descending, block ascending).  With more than 64 candidates, or k > 32, the k-th
-// largest key is found by a 32-step bitwise search with warp-wide counts instead.
+// largest key is found by a radix select instead.
 template <int NPL>
 __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int n_init, int n_local, int k,
                                           int32_t* out, uint32_t* cand_key, int* cand_idx, int lane) {
@@ -125,21 +185,9 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
       return;
     }
   }
-  // exact k-th largest key P by bitwise search
-  uint32_t P = 0u;
-#pragma unroll 1
-  for (int b = 31; b >= 0; --b) {
-    const uint32_t trial = P | (1u << b);
-    int c = 0;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) c += (i * 32 + lane < ncand && key[i] >= trial) ? 1 : 0;
-    c = (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
-    if (c >= k) P = trial;
-  }
-  int gt = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) gt += (i * 32 + lane < ncand && key[i] > P) ? 1 : 0;
-  const int need = k - (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
+  // exact k-th largest key P by radix select
+  int need;
+  const uint32_t P = warp_radix_kth<NPL>(key, ncand, k, &need, lane);
   // keys above P, and the first `need` keys equal to P in block order
   int taken = 0, pos = 0;
 #pragma unroll
@@ -157,54 +205,101 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
   }
 }
 
-// The same selection spread over a whole CTA of NT threads (each owns E consecutive
-// blocks), for rows whose latency matters more than throughput: one barrier per search
-// step, with per-warp counts double buffered in shared memory.  scratch: 2*(NT/32)+NT/32
-// ints of shared memory.  Every thread of the CTA must call it.
+// The same selection spread over a CTA of NT threads, each owning E consecutive blocks
+// of a row (global or shared memory): the radix passes count digits in registers, sum
+// them per warp and combine the warps through shared memory, one barrier per pass; the
+// chosen blocks are written in block order through a CTA prefix count.  For rows whose
+// latency matters (the decode selection): a single warp's chain of dependent
+// reductions is what this avoids.  scratch: 2 * 16 * (NT / 32) + 2 * (NT / 32) ints.
+// Every thread of the CTA must call it.
 template <int E, int NT>
 __device__ __forceinline__ void block_topk(const float* row, int nb, int own, int n_init, int n_local, int k,
                                            int32_t* out, int* scratch) {
   constexpr int NWARP = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* s_cnt = scratch;              // [2][NWARP]
-  int* s_tot = scratch + 2 * NWARP;  // [NWARP]
+  int* s_cnt = scratch;                   // [2][NWARP][16]
+  int* s_red = scratch + 2 * NWARP * 16;  // [2][NWARP]
+  const int ncand = min(own + 1, nb);
+  if (ncand <= k) {
+    for (int q = tid; q < k; q += NT) out[q] = q < ncand ? q : -1;
+    return;
+  }
   uint32_t key[E];
   bool valid[E];
   const int j0 = tid * E;
+  uint32_t all_and = 0xffffffffu, all_or = 0u;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
     const int j = j0 + i;
-    valid[i] = j <= own && j < nb;
+    valid[i] = j < ncand;
     const bool forced = j < n_init || j > own - n_local;
-    key[i] = forced ? 0xffffffffu : order_key(valid[i] ? row[j] : 0.f);
-  }
-  const int ncand = min(own + 1, nb);
-  auto block_sum = [&](int c, int buf) {  // c summed over the CTA (one barrier)
-    c = (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
-    if (lane == 0) s_cnt[buf * NWARP + warp] = c;
-    __syncthreads();
-    int tot = 0;
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) tot += s_cnt[buf * NWARP + w];
-    return tot;
-  };
-  uint32_t P = 0u;
-  int need = k;
-  if (ncand > k) {
-#pragma unroll 1
-    for (int b = 31; b >= 0; --b) {
-      const uint32_t trial = P | (1u << b);
-      int c = 0;
-#pragma unroll
-      for (int i = 0; i < E; ++i) c += (valid[i] && key[i] >= trial) ? 1 : 0;
-      if (block_sum(c, b & 1) >= k) P = trial;
+    key[i] = valid[i] ? (forced ? 0xffffffffu : order_key(row[j])) : 0u;
+    if (valid[i]) {
+      all_and &= key[i];
+      all_or |= key[i];
     }
-    int gt = 0;
+  }
+  // bits shared by every candidate take no pass
+  all_and = __reduce_and_sync(0xffffffffu, all_and);
+  all_or = __reduce_or_sync(0xffffffffu, all_or);
+  if (lane == 0) {
+    s_red[warp] = (int)all_and;
+    s_red[NWARP + warp] = (int)all_or;
+  }
+  __syncthreads();
 #pragma unroll
-    for (int i = 0; i < E; ++i) gt += (valid[i] && key[i] > P) ? 1 : 0;
-    need = k - block_sum(gt, 1);  // buffer 1: its last readers passed the b = 0 barrier
+  for (int w = 0; w < NWARP; ++w) {
+    all_and &= (uint32_t)s_red[w];
+    all_or |= (uint32_t)s_red[NWARP + w];
+  }
+  const uint32_t varying = all_and ^ all_or;
+  uint32_t P = all_and;
+  int left = k;
+  if (varying != 0u) {
+    int shift = ((31 - __clz(varying)) / 4) * 4;
+    uint32_t pmask = shift + 4 >= 32 ? 0u : (0xffffffffu << (shift + 4));
+    uint32_t prefix = all_and & pmask;
+    int buf = 0;
+#pragma unroll 1
+    for (; shift >= 0; shift -= 4, buf ^= 1) {
+      unsigned long long lo = 0ull, hi = 0ull;  // 16 digit counters of this thread, 8 bits each
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        if (valid[i] && (key[i] & pmask) == prefix) {
+          const uint32_t d = (key[i] >> shift) & 15u;
+          const unsigned long long inc = 1ull << ((d & 7u) * 8u);
+          if (d < 8u) lo += inc; else hi += inc;
+        }
+      int* cnt = s_cnt + buf * NWARP * 16 + warp * 16;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const unsigned f = (unsigned)(((q < 8 ? lo : hi) >> ((q & 7) * 8)) & 0xffull);
+        const int c = (int)__reduce_add_sync(0xffffffffu, f);
+        if (lane == 0) cnt[q] = c;
+      }
+      __syncthreads();  // the other buffer is rewritten only after the next barrier
+      int run = 0, dsel = 0, above = 0;
+      bool found = false;
+#pragma unroll
+      for (int q = 15; q >= 0; --q) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) c += s_cnt[buf * NWARP * 16 + w * 16 + q];
+        if (!found && run + c >= left) {
+          found = true;
+          dsel = q;
+          above = run;
+        }
+        run += c;
+      }
+      left -= above;
+      prefix |= (uint32_t)dsel << shift;
+      pmask |= 15u << shift;
+    }
+    P = prefix;
   }
   // exclusive prefix over the CTA, in block order (threads own consecutive blocks)
+  int* s_tot = s_red;  // reused: its last readers passed at least one barrier since
   auto block_scan = [&](int x) {
     const int incl = warp_excl_scan(x, lane) + x;
     __syncthreads();  // s_tot may still be read by a previous scan
@@ -216,16 +311,14 @@ __device__ __forceinline__ void block_topk(const float* row, int nb, int own, in
   };
   int tie = 0;
 #pragma unroll
-  for (int i = 0; i < E; ++i) tie += (ncand > k && valid[i] && key[i] == P) ? 1 : 0;
+  for (int i = 0; i < E; ++i) tie += (valid[i] && key[i] == P) ? 1 : 0;
   int rank = block_scan(tie);
   bool sel[E];
   int nsel = 0;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    if (ncand <= k) {
-      sel[i] = valid[i];
-    } else if (valid[i] && key[i] == P) {
-      sel[i] = rank < need;
+    if (valid[i] && key[i] == P) {
+      sel[i] = rank < left;
       ++rank;
     } else {
       sel[i] = valid[i] && key[i] > P;
@@ -236,8 +329,6 @@ __device__ __forceinline__ void block_topk(const float* row, int nb, int own, in
 #pragma unroll
   for (int i = 0; i < E; ++i)
     if (sel[i]) out[pos++] = j0 + i;
-  const int total = min(k, ncand);
-  for (int q = total + tid; q < k; q += NT) out[q] = -1;
 }
 
 }  // namespace nsa
