@@ -341,19 +341,26 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       fence_before();
       mbar_arrive(bar(B_SFREE + b));
       const int j_hi = min(KT, max(0, b_hi - kt * KT));
+      // max of the raw scores (scaling is monotonic), masked keys at -inf
       float mx = kNegInf;
+      if (j_hi == KT) {
 #pragma unroll
-      for (int j = 0; j < KT; ++j) {
-        sv[j] = j < j_hi ? sv[j] * p.scale_log2 : kNegInf;
-        mx = fmaxf(mx, sv[j]);
+        for (int j = 0; j < KT; ++j) mx = fmaxf(mx, sv[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < KT; ++j) {
+          sv[j] = j < j_hi ? sv[j] : kNegInf;
+          mx = fmaxf(mx, sv[j]);
+        }
       }
+      mx *= p.scale_log2;
       if (mx > m + 8.f) {  // lazy rescale, as in the attention pass
         l *= ex2(m - mx);
         m = mx;
       }
       const float mu = m == kNegInf ? 0.f : m;
 #pragma unroll
-      for (int j = 0; j < KT; ++j) l += ex2(sv[j] - mu);
+      for (int j = 0; j < KT; ++j) l += ex2(fmaf(sv[j], p.scale_log2, -mu));
     }
     for (int kt = 0; MODE != 2 && kt < n_kt; ++kt) {
       const int b = kt & 1;
@@ -367,12 +374,20 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       const int64_t jl = b_lo - rel0, jh = b_hi - rel0;
       const int j_lo = jl < 0 ? 0 : (jl > KT ? KT : (int)jl);
       const int j_hi = jh < 0 ? 0 : (jh > KT ? KT : (int)jh);
+      // max of the raw scores (scaling is monotonic); the mask only where the tile
+      // reaches outside the row's keys
       float mx = kNegInf;
+      if (j_lo == 0 && j_hi == KT) {
 #pragma unroll
-      for (int j = 0; j < KT; ++j) {
-        sv[j] = (j >= j_lo && j < j_hi) ? sv[j] * p.scale_log2 : kNegInf;
-        mx = fmaxf(mx, sv[j]);
+        for (int j = 0; j < KT; ++j) mx = fmaxf(mx, sv[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < KT; ++j) {
+          sv[j] = (j >= j_lo && j < j_hi) ? sv[j] : kNegInf;
+          mx = fmaxf(mx, sv[j]);
+        }
       }
+      mx *= p.scale_log2;
       // lazy rescale: the running max moves only when a score exceeds it by 2^8
       const bool need = mx > m + 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -399,7 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       uint32_t pk[KT / 2];
 #pragma unroll
       for (int j = 0; j < KT; j += 2) {
-        const float e0 = ex2(sv[j] - mu), e1 = ex2(sv[j + 1] - mu);
+        const float e0 = ex2(fmaf(sv[j], p.scale_log2, -mu)), e1 = ex2(fmaf(sv[j + 1], p.scale_log2, -mu));
         l += e0 + e1;
         pk[j / 2] = pack_bf16(e0, e1);
       }
