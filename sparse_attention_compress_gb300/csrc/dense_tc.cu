@@ -81,6 +81,19 @@ __device__ __forceinline__ void group_reduce_scatter(float (&v)[16], int lane) {
   }
 }
 
+// Maximum of a tile row, four independent chains.
+__device__ __forceinline__ float row_max(const float (&v)[KT]) {
+  float a = v[0], b = v[1], c = v[2], d = v[3];
+#pragma unroll
+  for (int j = 4; j < KT; j += 4) {
+    a = fmaxf(a, v[j]);
+    b = fmaxf(b, v[j + 1]);
+    c = fmaxf(c, v[j + 2]);
+    d = fmaxf(d, v[j + 3]);
+  }
+  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
 struct Params {
   __nv_bfloat16* o;
   float* lse;            // optional natural-log normaliser per (token, head)
@@ -342,25 +355,20 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       mbar_arrive(bar(B_SFREE + b));
       const int j_hi = min(KT, max(0, b_hi - kt * KT));
       // max of the raw scores (scaling is monotonic), masked keys at -inf
-      float mx = kNegInf;
-      if (j_hi == KT) {
+      if (j_hi < KT) {
 #pragma unroll
-        for (int j = 0; j < KT; ++j) mx = fmaxf(mx, sv[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < KT; ++j) {
-          sv[j] = j < j_hi ? sv[j] : kNegInf;
-          mx = fmaxf(mx, sv[j]);
-        }
+        for (int j = 0; j < KT; ++j) sv[j] = j < j_hi ? sv[j] : kNegInf;
       }
-      mx *= p.scale_log2;
+      float mx = row_max(sv) * p.scale_log2;
       if (mx > m + 8.f) {  // lazy rescale, as in the attention pass
         l *= ex2(m - mx);
         m = mx;
       }
       const float mu = m == kNegInf ? 0.f : m;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four chains of the row sum
 #pragma unroll
-      for (int j = 0; j < KT; ++j) l += ex2(fmaf(sv[j], p.scale_log2, -mu));
+      for (int j = 0; j < KT; ++j) l4[j & 3] += ex2(fmaf(sv[j], p.scale_log2, -mu));
+      l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
     }
     for (int kt = 0; MODE != 2 && kt < n_kt; ++kt) {
       const int b = kt & 1;
@@ -376,18 +384,11 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       const int j_hi = jh < 0 ? 0 : (jh > KT ? KT : (int)jh);
       // max of the raw scores (scaling is monotonic); the mask only where the tile
       // reaches outside the row's keys
-      float mx = kNegInf;
-      if (j_lo == 0 && j_hi == KT) {
+      if (j_lo > 0 || j_hi < KT) {
 #pragma unroll
-        for (int j = 0; j < KT; ++j) mx = fmaxf(mx, sv[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < KT; ++j) {
-          sv[j] = (j >= j_lo && j < j_hi) ? sv[j] : kNegInf;
-          mx = fmaxf(mx, sv[j]);
-        }
+        for (int j = 0; j < KT; ++j) sv[j] = (j >= j_lo && j < j_hi) ? sv[j] : kNegInf;
       }
-      mx *= p.scale_log2;
+      const float mx = row_max(sv) * p.scale_log2;
       // lazy rescale: the running max moves only when a score exceeds it by 2^8
       const bool need = mx > m + 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -412,12 +413,14 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       }
       const float mu = m == kNegInf ? 0.f : m;
       uint32_t pk[KT / 2];
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four chains of the row sum
 #pragma unroll
       for (int j = 0; j < KT; j += 2) {
         const float e0 = ex2(fmaf(sv[j], p.scale_log2, -mu)), e1 = ex2(fmaf(sv[j + 1], p.scale_log2, -mu));
-        l += e0 + e1;
+        l4[(j >> 1) & 3] += e0 + e1;
         pk[j / 2] = pack_bf16(e0, e1);
       }
+      l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tmem_st32(t_lane + b * KT, pk);  // P over the first 32 columns of its S buffer
       fence_before();
       mbar_arrive(bar(B_PFULL + b));
