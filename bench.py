@@ -36,7 +36,7 @@ METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roo
 # DRAM bytes (read + write) of one prefill launch from the ncu capture summarised in
 # profiles/sparse_fwd_mma_prefill_b2.md: 248.7 MB at B=2, x4 for the B=8 launch (the
 # traffic grows with the number of query tokens)
-PREFILL_NCU_TRAFFIC = 4 * (153.18e6 + 95.53e6)
+PREFILL_NCU_TRAFFIC = 4 * (153.22e6 + 94.12e6)
 L2_BYTES = 129 * 2 ** 20
 
 
