@@ -438,7 +438,8 @@ def main():
             line["probes"] = pr
             rf = line["roofline"]
             rf["l2_read_peak_gbs"] = pr["l2_read_gbs"]
-            rf["gather_frac_of_l2"] = rf["gather_gbs"] / pr["l2_read_gbs"]
+            rf["l2_gather_peak_gbs"] = pr["l2_gather_gbs"]  # random 4 KB slices into shared memory, no compute
+            rf["gather_frac_of_l2_gather"] = rf["gather_gbs"] / pr["l2_gather_gbs"]
             rf["mma_sync_peak_tflops"] = pr["mma_sync_bf16_tflops"]
             rf["frac_of_mma_sync"] = kernel_tflops / pr["mma_sync_bf16_tflops"]
             if "tflops" in line.get("layer", {}):

@@ -1,7 +1,9 @@
 // Micro-benchmarks of the ceilings that bound the hot path on this GPU, printed as one
 // JSON object: L2-resident read bandwidth (the gather of selected K/V blocks is served
-// from L2), HBM read bandwidth, the legacy mma.sync.m16n8k16 bf16 rate (the MMA the
-// selected-attention kernels use) and the ex2.approx rate (softmax exponentials).
+// from L2), the L2 -> shared-memory gather rate of random 4 KB slices by cp.async (the
+// selected-attention access pattern, with no compute), HBM read bandwidth, the legacy
+// mma.sync.m16n8k16 bf16 rate (the MMA the selected-attention kernels use) and the
+// ex2.approx rate (softmax exponentials).
 // Standalone program; no part of the library.
 #include <cstdint>
 #include <cstdio>
@@ -16,6 +18,45 @@ __global__ void read_kernel(const uint4* __restrict__ p, size_t n, int iters, un
       acc ^= v.x ^ v.y ^ v.z ^ v.w;
     }
   out[tid] = acc;
+}
+
+__device__ __forceinline__ uint32_t mix(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352du;
+  x ^= x >> 15;
+  x *= 0x846ca68bu;
+  x ^= x >> 16;
+  return x;
+}
+
+// Each warp streams `iters` random (K, V) slice pairs of 4 KB each (16 rows x 256 B)
+// through a 2-stage cp.async ring of 8 KB stages, as the prefill kernel's warps do.
+__global__ void __launch_bounds__(128) gather_kernel(const uint8_t* __restrict__ buf, uint32_t n_slices,
+                                                     int iters) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(sm) + warp * 2 * 8192;
+  const uint32_t gw = blockIdx.x * 4 + warp;
+  auto issue = [&](int i) {
+    const uint32_t sk = mix(gw * 7919u + i) % n_slices, sv = mix(gw * 104729u + i) % n_slices;
+    const uint32_t dst = wbase + (i & 1) * 8192;
+#pragma unroll
+    for (int c = lane; c < 256; c += 32) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + c * 16),
+                   "l"(buf + (size_t)sk * 4096 + c * 16));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 4096 + c * 16),
+                   "l"(buf + (size_t)sv * 4096 + c * 16));
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+  issue(0);
+  for (int i = 0; i < iters; ++i) {
+    if (i + 1 < iters) issue(i + 1);
+    else asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+    __syncwarp();
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
 __device__ __forceinline__ void mma(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
@@ -76,6 +117,11 @@ static void launch_read(void* v) {
   ReadArg* r = static_cast<ReadArg*>(v);
   read_kernel<<<r->grid, 256>>>(r->p, r->n, r->iters, r->out);
 }
+struct GatherArg { const uint8_t* buf; uint32_t n_slices; int iters; int grid; };
+static void launch_gather(void* v) {
+  GatherArg* g = static_cast<GatherArg*>(v);
+  gather_kernel<<<g->grid, 128, 2 * 4 * 8192>>>(g->buf, g->n_slices, g->iters);
+}
 struct ComputeArg { float* out; int iters; int grid; bool mma; };
 static void launch_compute(void* v) {
   ComputeArg* c = static_cast<ComputeArg*>(v);
@@ -102,6 +148,18 @@ int main() {
     bw[t] = (double)n * 16 * r.iters / (ms * 1e-3) / 1e9;
     cudaFree(p);
   }
+  double gather = 0;
+  {
+    const size_t bytes = (size_t)32 << 20;  // L2 resident, like the benchmark's K and V
+    uint8_t* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) { printf("{\"error\": \"allocation\"}\n"); return 1; }
+    cudaMemset(p, 1, bytes);
+    cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 4 * 8192);
+    GatherArg g{p, (uint32_t)(bytes / 4096), 512, sms * 3};
+    const float ms = timed_ms(launch_gather, &g);
+    gather = (double)g.grid * 4 * g.iters * 8192.0 / (ms * 1e-3) / 1e9;
+    cudaFree(p);
+  }
   float* fo = nullptr;
   cudaMalloc(&fo, (size_t)sms * 4 * 256 * 4);
   ComputeArg cm{fo, 4096, sms * 4, true};
@@ -111,9 +169,10 @@ int main() {
   const float ms_ex2 = timed_ms(launch_compute, &ce);
   const double ex2_rate = (double)ce.grid * 256 * ce.iters * 8 / (ms_ex2 * 1e-3);
   const cudaError_t e = cudaGetLastError();
-  printf("{\"l2_read_gbs\": %.1f, \"hbm_read_gbs\": %.1f, \"mma_sync_bf16_tflops\": %.1f, "
-         "\"ex2_per_sm_per_clk\": %.2f, \"sms\": %d, \"clock_mhz\": %.0f, \"error\": \"%s\"}\n",
-         bw[0], bw[1], mma_tf, ex2_rate / sms / (clk_khz * 1e3), sms, clk_khz / 1e3,
+  printf("{\"l2_read_gbs\": %.1f, \"l2_gather_gbs\": %.1f, \"hbm_read_gbs\": %.1f, "
+         "\"mma_sync_bf16_tflops\": %.1f, \"ex2_per_sm_per_clk\": %.2f, \"sms\": %d, \"clock_mhz\": %.0f, "
+         "\"error\": \"%s\"}\n",
+         bw[0], gather, bw[1], mma_tf, ex2_rate / sms / (clk_khz * 1e3), sms, clk_khz / 1e3,
          e == cudaSuccess ? "" : cudaGetErrorString(e));
   cudaFree(out);
   cudaFree(fo);

@@ -236,8 +236,8 @@ def test_gate_combine():
 
 
 # --------------------------------------------------------------------------- S6
-def _decode_case(B, L, seqlens, k, seed):
-    w = gen.decode(B=B, L=L, seqlens=seqlens, topk=k)
+def _decode_case(B, L, seqlens, k, seed, H=16, HKV=2):
+    w = gen.decode(B=B, L=L, seqlens=seqlens, topk=k, H=H, HKV=HKV)
     ncs = orc.num_cmp(L)
     kc_cache = np.zeros((B, ncs, w.hkv, w.d), np.uint16)
     for b in range(B):
@@ -260,6 +260,26 @@ def test_decode(B, L, seqlens, k):
     # attention over the GPU's own choice
     _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, idx_in=gi)
     assert_close(out, ref_o, what="decode")
+
+
+@pytest.mark.parametrize("B,L,seqlens,k,H,HKV", [
+    (3, 3000, [3000, 1500, 40], 64, 16, 1),     # group 16
+    (2, 2000, [2000, 999], 7, 4, 4),            # group 1, small k
+    (5, 1500, [1500, 31, 64, 65, 1200], 1, 8, 2),  # group 4, k = 1, rows without compressed keys
+    (40, 1024, None, 32, 16, 2)])               # 80 rows: more work items than resident CTAs
+def test_decode_group_sizes(B, L, seqlens, k, H, HKV):
+    w, kc_cache = _decode_case(B, L, seqlens, k, 0, H=H, HKV=HKV)
+    ref_idx, _, ref_sc = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, want_scores=True)
+    idx = torch.empty((B, HKV, k), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode(dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(kc_cache), dev(w.seqlens), k=k,
+                                idx_out=idx)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    gi = host(idx)
+    n_mis, outside = selection_mismatches(gi, ref_idx, ref_sc, np.asarray(w.seqlens) - 1)
+    assert outside == 0, (n_mis, outside)
+    _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, idx_in=gi)
+    assert_close(out, ref_o, what="decode groups")
 
 
 def test_decode_full_size():
