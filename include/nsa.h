@@ -129,6 +129,22 @@ NSA_API nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_sc
                            int block_size, int n_init, int n_local, int k, int32_t* block_indices,
                            cudaStream_t stream);
 
+/* S2-S4 in one call -- block selection from the compressed keys: the block scores of
+ * nsa_cmp_scores_pool (kept in the workspace, never returned) followed by
+ * nsa_topk_select, with the same definitions, arguments and limits ([NOSA-Parts] core
+ * component 3, first stage; [NOSA-Triton] beyond the kernel).
+ *   q              [tokens, h, d]; k_cmp [sum_i n_c(L_i), h_kv, d]
+ *   block_indices  [tokens, h_kv, k] int32 out, ascending, -1 padded
+ *   workspace      device, >= nsa_select_workspace_size(shape, block_size) bytes,
+ *                  256-byte aligned, caller-owned; its contents are scratch
+ * Requires kernel 32, stride 16, block_size 64, bf16, d in {64, 128}, h/h_kv in
+ * {1, 2, 4, 8, 16}, 1 <= k <= 64, sequences up to 131072 tokens. */
+NSA_API size_t nsa_select_workspace_size(const nsa_shape* shape, int block_size);
+NSA_API nsa_status nsa_select(const nsa_shape* shape, const void* q, const void* k_cmp, int kernel, int stride,
+                              int block_size, float scale, int n_init, int n_local, int k,
+                              int32_t* block_indices, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
 /* S5 -- selected-block attention (prefill).  [TileLang-NSA] sec. 2: for each entry of
  * the query's list the block starting at i_s = index * block_size is used when
  * 0 <= i_s <= t; keys past t inside it are masked; every query head of a GQA group reads

@@ -33,6 +33,9 @@ _SIGS = {
     "nsa_compress_k": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_p], _c_int),
     "nsa_cmp_scores_pool": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_int, _c_p], _c_int),
     "nsa_topk_select": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
+    "nsa_select_workspace_size": ([_c_p, _c_int], _c_sz),
+    "nsa_select": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_int, _c_int, _c_int, _c_p, _c_p, _c_sz,
+                    _c_p], _c_int),
     "nsa_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_swa_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
@@ -168,6 +171,21 @@ def nsa_cmp_scores_pool(q, k_cmp, h_kv, kernel=32, stride=16, block_size=64, sca
     _check(load().nsa_cmp_scores_pool(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), kernel, stride, block_size,
                                       float(scale), _ptr(lse_in), _ptr(out), nb_stride, _stream(stream)),
            "nsa_cmp_scores_pool")
+    return out
+
+
+def nsa_select(q, k_cmp, h_kv, k=16, kernel=32, stride=16, block_size=64, n_init=1, n_local=2, scale=0.0, *,
+               cu_seqlens=None, max_seqlen=None, workspace=None, out=None, stream=None):
+    """S2-S4 in one call: block indices [tokens, Hkv, k] int32 from q and the compressed keys."""
+    qf, shp = _shape_for(q, h_kv, cu_seqlens, max_seqlen)
+    if workspace is None:
+        ws = int(load().nsa_select_workspace_size(ctypes.byref(shp), block_size))
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=qf.device)
+    if out is None:
+        out = torch.empty((qf.shape[0], h_kv, k), dtype=torch.int32, device=qf.device)
+    _check(load().nsa_select(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), kernel, stride, block_size, float(scale),
+                             n_init, n_local, k, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "nsa_select")
     return out
 
 

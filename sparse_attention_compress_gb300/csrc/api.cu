@@ -158,6 +158,46 @@ nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, in
                      "nsa_topk_select");
 }
 
+size_t nsa_select_workspace_size(const nsa_shape* shape, int block_size) {
+  Seqs s;
+  if (make_seqs(shape, &s, __func__) != NSA_OK || block_size <= 0) return 0;
+  const int nb = (s.max_len + block_size - 1) / block_size;
+  return align256((size_t)s.tokens * shape->h_kv * (nb > 0 ? nb : 1) * 4);
+}
+
+nsa_status nsa_select(const nsa_shape* shape, const void* q, const void* k_cmp, int kernel, int stride,
+                      int block_size, float scale, int n_init, int n_local, int k, int32_t* block_indices,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
+              "nsa_select: supports kernel 32, stride 16, block_size 64");
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_select: bf16 only");
+  NSA_REQUIRE(shape->d == 64 || shape->d == 128, NSA_ERR_UNSUPPORTED, "nsa_select: d must be 64 or 128");
+  NSA_REQUIRE(pow2_le16(shape->h / shape->h_kv), NSA_ERR_UNSUPPORTED, "nsa_select: h/h_kv must be 1, 2, 4, 8 or 16");
+  NSA_REQUIRE(n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "nsa_select: negative n_init/n_local");
+  NSA_REQUIRE(k >= 1 && k <= 64, NSA_ERR_UNSUPPORTED, "nsa_select: k must be in [1, 64]");
+  const int nb = (s.max_len + block_size - 1) / block_size;
+  NSA_REQUIRE(nb <= 2048, NSA_ERR_UNSUPPORTED, "nsa_select: sequences longer than 131072 tokens");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(block_indices);
+  if (s.max_len >= kernel) NSA_PTR(k_cmp);
+  const size_t need = nsa_select_workspace_size(shape, block_size);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_select: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_select: workspace %zu < %zu bytes", workspace_bytes,
+              need);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  float* scores = static_cast<float*>(workspace);
+  cudaError_t e = launch_scores_pool(s, q, k_cmp, shape->h, shape->h_kv, shape->d, scale, nullptr, scores,
+                                     nb > 0 ? nb : 1, stream);
+  if (e) return cuda_status(e, "nsa_select/block scores");
+  return cuda_status(launch_topk(s, scores, nb > 0 ? nb : 1, shape->h_kv, block_size, n_init, n_local, k,
+                                 block_indices, stream),
+                     "nsa_select/top-k");
+}
+
 nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
                           const int32_t* block_indices, int S, int block_size, float scale, void* o,
                           float* lse, cudaStream_t stream) {

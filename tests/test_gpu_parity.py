@@ -335,6 +335,23 @@ def test_layer_small(T, H, hkv):
     assert_close(out, ref["o"], what="layer")
 
 
+def test_select_fused_call():
+    """nsa_select (S2-S4 in one call) equals scores + top-k by separate calls, bit for
+    bit, and matches the oracle's selection up to near ties."""
+    w = gen.selection(n_seqs=3, lo=900, hi=2500)
+    dcu = dev(w.cu_seqlens)
+    kc = nsa.nsa_compress_k(dev(w.k), cu_seqlens=dcu, max_seqlen=w.max_len)
+    one = nsa.nsa_select(dev(w.q), kc, w.hkv, k=16, cu_seqlens=dcu, max_seqlen=w.max_len)
+    sc = nsa.nsa_cmp_scores_pool(dev(w.q), kc, w.hkv, cu_seqlens=dcu, max_seqlen=w.max_len)
+    two = nsa.nsa_topk_select(sc, 16, cu_seqlens=dcu, max_seqlen=w.max_len)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(one), host(two))
+    ref_sc = orc.cmp_scores_pool(w.q, host(kc), w.cu_seqlens)
+    ref_idx = orc.topk(ref_sc, w.cu_seqlens, k=16)
+    _, outside = selection_mismatches(host(one), ref_idx, ref_sc, _t_of_rows(w.cu_seqlens))
+    assert outside == 0
+
+
 def test_layer_varlen():
     """Packed sequences of ragged lengths (shorter than one compression window, one
     selection block, one sliding window, and longer): every tile of the tensor-core
