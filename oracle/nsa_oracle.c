@@ -447,6 +447,48 @@ int nsa_oracle_sparse_attn(const void* q, const void* k, const void* v, int dtyp
   return 0;
 }
 
+/* Block-mask sparse attention ([TileLang-NSA] sec. 1, block-sparse attention: the
+ * attention matrix is cut into block x block tiles and a mask marks the active ones;
+ * only active tiles are computed; is_causal keeps the lower triangle).  Dense layout:
+ * B sequences of T tokens.  Query (b, t, head hh) attends the keys of every key block
+ * kb with mask[b, hh, t / block, kb] != 0, restricted to keys <= t when causal.  A row
+ * without any attended key gets o = 0 and lse = -inf (the pages leave it undefined).
+ *   mask  uint8 [B, h, nqb, nkb] with nqb = nkb = ceil(T / block). */
+int nsa_oracle_block_sparse_attn(const void* q, const void* k, const void* v, int dtype, int B, int T,
+                                 int h, int hkv, int d, const uint8_t* mask, int block, int causal,
+                                 double scale, const int64_t* rows, int64_t n_rows, double* o, double* lse) {
+  if (h % hkv || block <= 0 || B < 0 || T < 0) return 1;
+  const int nb = (T + block - 1) / block;
+  if (!rows) n_rows = (int64_t)B * T;
+  const int r = h / hkv;
+#pragma omp parallel
+  {
+    int* keys = (int*)malloc(sizeof(int) * (size_t)(T + 1));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      const int64_t tok = rows ? rows[rr] : rr;
+      const int b = (int)(tok / T), t = (int)(tok % T);
+      for (int hh = 0; hh < h; ++hh) {
+        const uint8_t* mrow = mask + (((size_t)b * h + hh) * nb + t / block) * nb;
+        int n = 0;
+        for (int kb = 0; kb < nb; ++kb) {
+          if (!mrow[kb]) continue;
+          for (int tau = kb * block; tau < (kb + 1) * block && tau < T; ++tau)
+            if (!causal || tau <= t) keys[n++] = tau;
+        }
+        double l;
+        attend_list(q, k, v, dtype, tok, hh, h, hkv, d, hh / r, (int64_t)b * T, keys, n, scale, s,
+                    o + ((size_t)rr * h + hh) * d, &l);
+        if (lse) lse[(size_t)rr * h + hh] = l;
+      }
+    }
+    free(keys);
+    free(s);
+  }
+  return 0;
+}
+
 /* S8: sliding-window attention over keys max(0, t-window+1) .. t ([NSA-Triton]
  * sec. 1.1: the sliding branch looks at the most recent tokens). */
 int nsa_oracle_swa(const void* q, const void* k, const void* v, int dtype, const int32_t* cu,

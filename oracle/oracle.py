@@ -186,6 +186,26 @@ def swa(q, k, v, cu, window=512, scale=None, rows=None):
     return o, lse
 
 
+def block_sparse_attn(q, k, v, mask, causal=True, block=64, scale=None, rows=None):
+    """Block-mask sparse attention; q [B*T, h, d], k/v [B*T, hkv, d], mask uint8
+    [B, h, nb, nb]; returns (o, lse) for the requested token rows."""
+    q, k, v = np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v)
+    mask = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+    B, h, nb, _ = mask.shape
+    tot, _, d = q.shape
+    T = tot // B
+    hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    rows, n = _rows(rows, tot)
+    o = np.zeros((n, h, d), np.float64)
+    lse = np.zeros((n, h), np.float64)
+    _check(_load().nsa_oracle_block_sparse_attn(_p(q), _p(k), _p(v), _dt(q), B, T, h, hkv, d, _p(mask), block,
+                                                int(bool(causal)), ctypes.c_double(scale), _p(rows),
+                                                ctypes.c_int64(n), _p(o), _p(lse)),
+           "block_sparse_attn")
+    return o, lse
+
+
 def cmp_attn(q, kc, vc, cu, kernel=32, stride=16, scale=None, rows=None):
     """S7: compressed-attention branch over stored compressed keys/values; (o, lse)."""
     q, kc, vc, cu = (np.ascontiguousarray(q), np.ascontiguousarray(kc), np.ascontiguousarray(vc),

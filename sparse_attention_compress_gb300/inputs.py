@@ -207,3 +207,30 @@ def layer(T: int = 65536, H: int = 64, HKV: int = 4, D: int = 128, B: int = 1, l
     if lengths is None:
         return Workload("layer", "bf16", cu, H, HKV, D, q, k, v, S=16, gates=gates, batch=B, seqlen=T)
     return Workload("layer", "bf16", cu, H, HKV, D, q, k, v, S=16, gates=gates)
+
+
+def block_mask(rng: np.random.Generator, B: int, H: int, T: int, density: float = 0.5, causal: bool = True,
+               block: int = 64) -> np.ndarray:
+    """uint8 [B, H, nb, nb] block mask: each (query block, key block) tile active with
+    probability `density`; the diagonal tile is always active (every query keeps its own
+    block); with causal, tiles above the diagonal are cleared."""
+    nb = -(-T // block)
+    m = (rng.random((B, H, nb, nb)) < density).astype(np.uint8)
+    i = np.arange(nb)
+    m[:, :, i, i] = 1
+    if causal:
+        m &= np.tril(np.ones((nb, nb), np.uint8))
+    return m
+
+
+def block_sparse(B: int = 8, T: int = 16384, H: int = 16, D: int = 128, density: float = 0.5, causal: bool = True,
+                 salt: int = 0) -> Workload:
+    """Block-mask sparse attention (64 x 64 tiles, multi-head K/V): bf16 Q/K/V N(0,1)
+    [B*T, H, D] and the mask in Workload.idx."""
+    rng = rng_for(6, salt)
+    q = normal(rng, (B * T, H, D), "bf16")
+    k = normal(rng, (B * T, H, D), "bf16")
+    v = normal(rng, (B * T, H, D), "bf16")
+    m = block_mask(rng, B, H, T, density, causal)
+    return Workload("block_sparse", "bf16", dense_cu_seqlens(B, T), H, H, D, q, k, v, block_size=64, idx=m,
+                    batch=B, seqlen=T)

@@ -424,3 +424,47 @@ def test_random_indices_structure():
         assert valid.max() == own[r] and valid.min() == 0
         assert len(valid) == min(16, own[r] + 1)
         assert np.all(row[len(valid):] == -1)
+
+
+# --------------------------------------------------------------------------- block-mask variant
+def _token_mask(block_mask_bh, T, block, causal):
+    """Expand one (batch, head) block mask to the token level by a Kronecker product."""
+    m = np.kron(block_mask_bh, np.ones((block, block), np.uint8))[:T, :T].astype(bool)
+    if causal:
+        m &= np.tril(np.ones((T, T), bool))
+    return torch.from_numpy(m)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_block_sparse_equals_masked_sdpa(causal):
+    """Random 64x64 tile masks on ragged lengths: the oracle's key lists equal SDPA with
+    the token-level mask built by expanding the tiles."""
+    B, T, h, d, block = 2, 150, 3, 16, 64
+    q, k, v = (_rand((B * T, h, d), s) for s in (61, 62, 63))
+    mask = gen.block_mask(np.random.Generator(np.random.PCG64(64)), B, h, T, 0.5, causal, block)
+    o, lse = orc.block_sparse_attn(q, k, v, mask, causal=causal, block=block)
+    for b in range(B):
+        sl = slice(b * T, (b + 1) * T)
+        tm = torch.stack([_token_mask(mask[b, hh], T, block, causal) for hh in range(h)])  # [h, T, T]
+        qt, kt, vt = (_t(a[sl]).permute(1, 0, 2) for a in (q, k, v))
+        ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=tm).permute(1, 0, 2)
+        assert torch.allclose(torch.from_numpy(o[sl]), ref, atol=1e-12, rtol=0)
+        s = torch.einsum("htd,hsd->hts", qt, kt) * d ** -0.5
+        ref_lse = torch.logsumexp(s.masked_fill(~tm, -torch.inf), -1).T
+        assert torch.allclose(torch.from_numpy(lse[sl]), ref_lse, atol=1e-12, rtol=0)
+
+
+def test_block_sparse_full_mask_is_dense_causal_and_empty_row_is_zero():
+    B, T, h, d, block = 1, 130, 2, 8, 64
+    q, k, v = (_rand((T, h, d), s) for s in (65, 66, 67))
+    nb = -(-T // block)
+    full = np.ones((B, h, nb, nb), np.uint8)
+    o, _ = orc.block_sparse_attn(q, k, v, full, causal=True, block=block)
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    assert torch.allclose(torch.from_numpy(o), _sdpa(_t(q), _t(k), _t(v), mask), atol=1e-12, rtol=0)
+    # non-causal: query block 1 of head 0 attends nothing -> zero output, lse -inf
+    m = full.copy()
+    m[0, 0, 1, :] = 0
+    o2, lse2 = orc.block_sparse_attn(q, k, v, m, causal=False, block=block)
+    assert np.all(o2[64:128, 0] == 0) and np.all(np.isneginf(lse2[64:128, 0]))
+    assert np.all(np.isfinite(lse2[:64, 0])) and np.all(np.isfinite(lse2[:, 1]))
