@@ -161,6 +161,26 @@ NSA_API nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const v
                           const int32_t* block_indices, int S, int block_size, float scale, void* o,
                           float* lse, cudaStream_t stream);
 
+/* Block-mask sparse attention (the block-sparse companion of the pages' native sparse
+ * attention).  [TileLang-NSA] sec. 1, block-sparse attention: the attention matrix is
+ * cut into block_size x block_size tiles and a mask marks the active ones; only active
+ * tiles are computed; is_causal keeps the lower triangle.  Query (b, t, head h) attends
+ * every key of every key block kb with block_mask[b, h, t / block_size, kb] != 0
+ * (restricted to keys <= t when causal); a query without any attended key gets o = 0,
+ * lse = -inf.
+ *   q, k, v, o  [batch, seqlen, h, d]: dense layout (cu_seqlens NULL), multi-head K/V
+ *               (h_kv == h)
+ *   block_mask  uint8 [batch, h, n, n], n = seqlen / block_size, device
+ *   lse         nullable [batch * seqlen, h] fp32 out (natural log)
+ *   workspace   >= nsa_block_sparse_workspace_size(shape) bytes, 256-byte aligned:
+ *               V transposed per head for the tensor-core PV operand
+ * Requires bf16, d = 128, block_size = 64, seqlen a multiple of 64 and <= 65536. */
+NSA_API size_t nsa_block_sparse_workspace_size(const nsa_shape* shape);
+NSA_API nsa_status nsa_block_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                        const uint8_t* block_mask, int block_size, int causal, float scale,
+                                        void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
 /* S7 -- compressed-attention branch.  [NSA-Triton] sec. 1.1 and 2.2 (taken as the
  * definition): softmax over the causal compressed keys of scale * q.k_cmp, weighted sum
  * of v_cmp.  A query with no causal compressed key gets o = 0 and lse = -inf.

@@ -34,6 +34,9 @@ _SIGS = {
     "nsa_cmp_scores_pool": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_int, _c_p], _c_int),
     "nsa_topk_select": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
     "nsa_select_workspace_size": ([_c_p, _c_int], _c_sz),
+    "nsa_block_sparse_workspace_size": ([_c_p], _c_sz),
+    "nsa_block_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p],
+                             _c_int),
     "nsa_select": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_int, _c_int, _c_int, _c_p, _c_p, _c_sz,
                     _c_p], _c_int),
     "nsa_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
@@ -171,6 +174,21 @@ def nsa_cmp_scores_pool(q, k_cmp, h_kv, kernel=32, stride=16, block_size=64, sca
     _check(load().nsa_cmp_scores_pool(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), kernel, stride, block_size,
                                       float(scale), _ptr(lse_in), _ptr(out), nb_stride, _stream(stream)),
            "nsa_cmp_scores_pool")
+    return out
+
+
+def nsa_block_sparse_fwd(q, k, v, block_mask, causal=True, block_size=64, scale=0.0, *, workspace=None, out=None,
+                         lse=None, stream=None):
+    """Block-mask sparse attention; q/k/v [B, T, H, d] bf16, block_mask uint8 [B, H, T/64, T/64]."""
+    qf, shp = _shape_for(q, k.shape[-2], None, None)
+    if workspace is None:
+        ws = int(load().nsa_block_sparse_workspace_size(ctypes.byref(shp)))
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=qf.device)
+    if out is None:
+        out = torch.empty_like(qf)
+    _check(load().nsa_block_sparse_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(block_mask), block_size,
+                                       int(bool(causal)), float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)), "nsa_block_sparse_fwd")
     return out
 
 

@@ -158,6 +158,45 @@ nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, in
                      "nsa_topk_select");
 }
 
+size_t nsa_block_sparse_workspace_size(const nsa_shape* shape) {
+  Seqs s;
+  if (make_seqs(shape, &s, __func__) != NSA_OK) return 0;
+  return align256((size_t)shape->h * shape->d * tc_vt_pad(s.tokens > 0 ? s.tokens : 1) * 2);
+}
+
+nsa_status nsa_block_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                const uint8_t* block_mask, int block_size, int causal, float scale, void* o,
+                                float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(shape->cu_seqlens == nullptr, NSA_ERR_UNSUPPORTED, "nsa_block_sparse_fwd: dense layout only");
+  NSA_REQUIRE(shape->dtype == NSA_BF16 && shape->d == 128, NSA_ERR_UNSUPPORTED,
+              "nsa_block_sparse_fwd: bf16 with d = 128 only");
+  NSA_REQUIRE(shape->h == shape->h_kv, NSA_ERR_UNSUPPORTED, "nsa_block_sparse_fwd: needs h_kv == h");
+  NSA_REQUIRE(block_size == 64, NSA_ERR_UNSUPPORTED, "nsa_block_sparse_fwd: block_size must be 64");
+  NSA_REQUIRE(shape->seqlen % 64 == 0 && shape->seqlen <= 65536, NSA_ERR_UNSUPPORTED,
+              "nsa_block_sparse_fwd: seqlen must be a multiple of 64, at most 65536");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(o);
+  NSA_REQUIRE(block_mask != nullptr, NSA_ERR_INVALID, "nsa_block_sparse_fwd: block_mask is NULL");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(NSA_ERR_INVALID, "nsa_block_sparse_fwd: lse misaligned");
+  const size_t need = nsa_block_sparse_workspace_size(shape);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_block_sparse_fwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_block_sparse_fwd: workspace %zu < %zu bytes",
+              workspace_bytes, need);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  cudaError_t e = launch_transpose_v(s, v, workspace, s.tokens, shape->h, false, 32, 16, stream);
+  if (e) return cuda_status(e, "nsa_block_sparse_fwd/transpose v");
+  return cuda_status(launch_block_sparse_tc(s, q, k, workspace, shape->h, block_mask, causal ? 1 : 0, scale, o, lse,
+                                            stream),
+                     "nsa_block_sparse_fwd");
+}
+
 size_t nsa_select_workspace_size(const nsa_shape* shape, int block_size) {
   Seqs s;
   if (make_seqs(shape, &s, __func__) != NSA_OK || block_size <= 0) return 0;

@@ -101,6 +101,8 @@ struct Params {
   const float* lse_in;   // MODE 2: normaliser given by the caller (pass 1 skipped), or null
   const __nv_bfloat16* k;  // MODE 2: key rows, for the copies of a tile that ends past them
   int64_t kv_total;      // MODE 2: key rows the buffer holds (-1: the packed compressed rows)
+  const uint8_t* bmask;  // MODE 3: [batch, h, n_qb, n_qb] tile mask (query block, key block)
+  int n_qb, causal;
   Seqs seqs;
   int h, hkv, R, kernel, stride, window, nb_stride;
   float scale_log2;
@@ -115,7 +117,10 @@ __device__ __forceinline__ int last_in_stage(int last, int st) {
 // MODE 0: compressed branch (RS = group size when the block scores are fused, else 0);
 // MODE 1: sliding window (RS = 0);
 // MODE 2: block scores only (RS = group size): pass 1 keeps just the softmax statistics
-//         (no V, no PV; skipped when the caller gives the normaliser), then pass 2.
+//         (no V, no PV; skipped when the caller gives the normaliser), then pass 2;
+// MODE 3: block-mask sparse attention, one head per CTA (128 tokens = two 64-token
+//         query blocks): the key tiles are the 64-key blocks active for either query
+//         block; each row masks the tiles its own block does not list.
 template <int MODE, int RS>
 __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
   const int64_t start = seq_start(p.seqs, sq);
   int n_c = 0, key_lo, key_hi;
   int64_t kv0;  // key row of the sequence's first key
-  if (MODE != 1) {
+  if (MODE == 0 || MODE == 2) {  // compressed keys
     n_c = num_cmp(L, p.kernel, p.stride);
     kv0 = cmp_offset(p.seqs, sq, p.kernel, p.stride);
     key_lo = 0;
@@ -155,13 +160,28 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
     key_lo = max(0, t0 - p.window + 1);
     key_hi = t_last + 1;
   }
+  // MODE 3: per key block, bit 0 / bit 1 = active for the first / second query block
+  uint8_t* tflag = smem_raw + (v_s - smem_u32(smem_raw)) + NS * V_BYTES;
   // pass 1: 64-key tiles in absolute key rows (64-aligned, so every V^T tile starts on a
   // 128-byte boundary); pass 2: tiles at kv0 + 64 i (16 whole selection blocks each)
   // (MODE 2 needs no V^T, so both of its passes use the sequence-aligned tiles)
   const int64_t a_lo = (kv0 + key_lo) / KT;
   const int n_kt2 = RS > 0 ? (key_hi + KT - 1) / KT : 0;
-  const int n_kt = MODE == 2 ? (p.lse_in ? 0 : n_kt2)
-                             : (key_hi > key_lo ? (int)((kv0 + key_hi + KT - 1) / KT - a_lo) : 0);
+  int n_kt = MODE == 2 ? (p.lse_in ? 0 : n_kt2)
+                       : (key_hi > key_lo ? (int)((kv0 + key_hi + KT - 1) / KT - a_lo) : 0);
+  if (MODE == 3) {
+    const int qb0 = t0 / KT, nbw = (p.n_qb + 3) / 4 * 4;
+    const bool two = t0 + KT < L;
+    const uint8_t* m0 = p.bmask + (((int64_t)sq * p.h + g) * p.n_qb + qb0) * p.n_qb;
+    for (int kb = tid; kb < nbw; kb += NTHREADS) {
+      int f = 0;
+      if (kb < p.n_qb) {
+        if (m0[kb] && (!p.causal || kb <= qb0)) f |= 1;
+        if (two && m0[p.n_qb + kb] && (!p.causal || kb <= qb0 + 1)) f |= 2;
+      }
+      tflag[kb] = (uint8_t)f;
+    }
+  }
   constexpr int kTmemCols = MODE == 2 ? TMEM_COLS_SCORES : TMEM_COLS;
 
   if (tid == 0) {
@@ -192,6 +212,17 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
   __syncthreads();
   fence_after();
   const uint32_t tmem = tmem_holder;
+  int kb_cur = -1;  // MODE 3: this role's position in the active key blocks
+  auto next_kb = [&]() {
+    do ++kb_cur;
+    while (tflag[kb_cur] == 0);
+    return kb_cur;
+  };
+  if (MODE == 3) {  // every thread counts the active key blocks
+    n_kt = 0;
+    for (int w = 0; w < (p.n_qb + 3) / 4; ++w)
+      n_kt += __popc(__vcmpne4(reinterpret_cast<const uint32_t*>(tflag)[w], 0u)) >> 3;
+  }
 
   int last_k = -1, last_v = -1;  // producer: last K / V^T tile loads issued
   if (warp == 4) {
@@ -212,8 +243,9 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
     for (int i = 0; i < n_kt + n_kt2; ++i) {
       const int st = i % NS;
       if (i >= NS && !warp_wait(bar(B_KEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
-      const int row = MODE == 2 ? (int)(kv0 + (int64_t)(i < n_kt ? i : i - n_kt) * KT)
-                                : (i < n_kt ? (int)((a_lo + i) * KT) : (int)(kv0 + (int64_t)(i - n_kt) * KT));
+      const int row = MODE == 3   ? (int)(kv0 + (int64_t)next_kb() * KT)
+                      : MODE == 2 ? (int)(kv0 + (int64_t)(i < n_kt ? i : i - n_kt) * KT)
+                                  : (i < n_kt ? (int)((a_lo + i) * KT) : (int)(kv0 + (int64_t)(i - n_kt) * KT));
       const uint32_t kb = bar(B_KFULL + st), ks = k_s + st * K_BYTES;
       if (MODE == 2 && row + KT > kv_total) {
         // a tile reaching past the caller's rows: bounds-checked copies (zeros past the
@@ -333,7 +365,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
     const bool valid = t_row < L;
     int b_lo = 0, b_hi = 0;  // attended keys [b_lo, b_hi), relative to kv0
     if (valid) {
-      if (MODE != 1) {
+      if (MODE == 0 || MODE == 2) {
         b_hi = num_causal_cmp(t_row, n_c, p.kernel, p.stride);
       } else {
         b_lo = max(0, t_row - p.window + 1);
@@ -378,10 +410,19 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       tmem_ld32(t_lane + b * KT, sv);
       tmem_ld32(t_lane + b * KT + 32, sv + 32);
       // key row a0 + j is key a0 + j - kv0 of the sequence: attended when in [b_lo, b_hi)
-      const int64_t rel0 = (a_lo + kt) * KT - kv0;
-      const int64_t jl = b_lo - rel0, jh = b_hi - rel0;
-      const int j_lo = jl < 0 ? 0 : (jl > KT ? KT : (int)jl);
-      const int j_hi = jh < 0 ? 0 : (jh > KT ? KT : (int)jh);
+      int j_lo, j_hi;
+      if (MODE == 3) {
+        const int kb = next_kb();
+        const bool on = valid && (tflag[kb] & (tl < KT ? 1 : 2));
+        const int jh = on ? min(p.causal ? t_row - kb * KT + 1 : KT, L - kb * KT) : 0;
+        j_lo = 0;
+        j_hi = jh < 0 ? 0 : (jh > KT ? KT : jh);
+      } else {
+        const int64_t rel0 = (a_lo + kt) * KT - kv0;
+        const int64_t jl = b_lo - rel0, jh = b_hi - rel0;
+        j_lo = jl < 0 ? 0 : (jl > KT ? KT : (int)jl);
+        j_hi = jh < 0 ? 0 : (jh > KT ? KT : (int)jh);
+      }
       // max of the raw scores (scaling is monotonic); the mask only where the tile
       // reaches outside the row's keys
       if (j_lo > 0 || j_hi < KT) {
@@ -580,7 +621,7 @@ template <int MODE, int RS>
 static cudaError_t run_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const tc::Params& p,
                           dim3 grid, cudaStream_t st) {
   auto kern = tc::attn_kernel<MODE, RS>;
-  constexpr int smem = MODE == 2 ? tc::SMEM_BYTES_SCORES : tc::SMEM_BYTES;
+  constexpr int smem = MODE == 2 ? tc::SMEM_BYTES_SCORES : tc::SMEM_BYTES + (MODE == 3 ? 1024 : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, tc::NTHREADS, smem, st>>>(mq, mk, mv, p);
@@ -639,6 +680,46 @@ cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const v
     case 16: return run_tc<0, 16>(mq, mk, mv, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_block_sparse_tc(const Seqs& s, const void* q, const void* k, const void* vt, int h,
+                                   const uint8_t* mask, int causal, float scale, void* o, float* lse,
+                                   cudaStream_t st) {
+  if (s.tokens == 0) return cudaSuccess;
+  const uint64_t rows = (uint64_t)s.tokens;
+  const uint64_t pad = (uint64_t)tc_vt_pad((int64_t)rows);
+  CUtensorMap mq, mk, mv;
+  {
+    const uint64_t dims[3] = {(uint64_t)tc::D, (uint64_t)h, rows};
+    const uint64_t strides[2] = {(uint64_t)tc::D * 2, (uint64_t)h * tc::D * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)tc::ROWS};
+    if (!tc::make_map(&mq, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)h * tc::D, rows};
+    const uint64_t strides[1] = {(uint64_t)h * tc::D * 2};
+    const uint32_t box[2] = {64, (uint32_t)tc::KT};
+    if (!tc::make_map(&mk, k, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {pad, (uint64_t)h * tc::D};
+    const uint64_t strides[1] = {pad * 2};
+    const uint32_t box[2] = {64, (uint32_t)tc::D};
+    if (!tc::make_map(&mv, vt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  tc::Params p{};
+  p.o = (__nv_bfloat16*)o;
+  p.lse = lse;
+  p.bmask = mask;
+  p.n_qb = (s.max_len + tc::KT - 1) / tc::KT;
+  p.causal = causal;
+  p.seqs = s;
+  p.h = h;
+  p.hkv = h;
+  p.R = 1;
+  p.scale_log2 = scale * kLog2e;
+  const dim3 grid((s.max_len + tc::ROWS - 1) / tc::ROWS, s.n_seqs, h);
+  return run_tc<3, 0>(mq, mk, mv, p, grid, st);
 }
 
 bool scores_tc_supported(int h, int hkv, int d, int kernel, int stride, int block_size) {

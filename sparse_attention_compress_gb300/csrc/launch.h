@@ -46,6 +46,13 @@ cudaError_t launch_transpose_v(const Seqs& s, const void* v, void* vt, int64_t r
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
                                  void* o, float* lse, float* scores, int nb_stride, cudaStream_t st);
+// Block-mask sparse attention on the tensor cores: dense layout, seqlen % 64 == 0,
+// multi-head K/V (h_kv == h), d = 128, bf16; vt = V transposed as for the dense branches;
+// mask uint8 [batch, h, n_qb, n_qb] over 64 x 64 tiles.
+cudaError_t launch_block_sparse_tc(const Seqs& s, const void* q, const void* k, const void* vt, int h,
+                                   const uint8_t* mask, int causal, float scale, void* o, float* lse,
+                                   cudaStream_t st);
+
 // Block scores (S2 + S3) on the tensor cores, d = 128, kernel 32 / stride 16 / block 64,
 // group size 1..16 (power of two).  kv_rows: rows the key tensor map spans (an upper
 // bound is fine); kv_total: rows the k_cmp buffer holds, or -1 for the packed compressed

@@ -388,3 +388,39 @@ def test_layer_full_size_sampled():
     ref_sc = orc.cmp_scores_pool(w.q, kc, w.cu_seqlens, rows=rows)
     n_mis, outside = selection_mismatches(gi[rows], ref["idx"], ref_sc, rows)
     assert outside == 0, (n_mis, outside)
+
+
+# --------------------------------------------------------------------------- block-mask variant
+@pytest.mark.parametrize("B,T,H,causal,density", [(2, 1024, 4, True, 0.5), (2, 1024, 4, False, 0.5),
+                                                  (1, 960, 2, False, 0.3), (3, 384, 2, True, 1.0)])
+def test_block_sparse(B, T, H, causal, density):
+    w = gen.block_sparse(B=B, T=T, H=H, density=density, causal=causal, salt=T)
+    mask = w.idx
+    if not causal:  # a query block with no active tile: zero output, lse -inf
+        mask = mask.copy()
+        mask[0, 0, 1, :] = 0
+    lse = torch.empty((B * T, H), dtype=torch.float32, device="cuda")
+    out = nsa.nsa_block_sparse_fwd(dev(w.q).view(B, T, H, 128), dev(w.k).view(B, T, H, 128),
+                                   dev(w.v).view(B, T, H, 128), dev(mask), causal=causal, lse=lse)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    ref, ref_lse = orc.block_sparse_attn(w.q, w.k, w.v, mask, causal=causal)
+    assert_close(out.reshape(B * T, H, 128), ref, what="block sparse")
+    l = host(lse)
+    assert np.array_equal(np.isneginf(l), np.isneginf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(l[fin], ref_lse[fin], atol=1e-3, rtol=1e-4)
+
+
+def test_block_sparse_full_size_sampled():
+    """B=8, T=16384, H=16, d=128, 50% of the 64x64 tiles (the pages' block-sparse table
+    shape), causal; oracle on sampled rows."""
+    w = gen.block_sparse()
+    out = nsa.nsa_block_sparse_fwd(dev(w.q).view(8, 16384, 16, 128), dev(w.k).view(8, 16384, 16, 128),
+                                   dev(w.v).view(8, 16384, 16, 128), dev(w.idx), causal=True)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([_rng(32).integers(0, w.tokens, 48), [0, 63, 64, 127, 128, 16383,
+                                                                         7 * 16384 + 16383]]))
+    ref, _ = orc.block_sparse_attn(w.q, w.k, w.v, w.idx, causal=True, rows=rows)
+    g = out.reshape(w.tokens, 16, 128)[torch.from_numpy(rows).cuda()]
+    assert_close(g, ref, what="block sparse full")
