@@ -266,6 +266,32 @@ def bench_selection(torch, nsa, device, steps, warmup, flush):
             "launches_per_step": 3}
 
 
+def bench_block_sparse(torch, nsa, device, steps, warmup, flush, peaks, lengths=(1024, 4096, 16384)):
+    """Block-mask sparse attention at the pages' block-sparse table shape (batch 8, 16
+    heads, d 128, 64x64 tiles, half of the tiles active, not causal)."""
+    res = {"workload": "block-mask attention B=8 H=16 d=128 bf16, 64x64 tiles, 50% active, not causal",
+           "launches_per_step": 2}
+    for T in lengths:
+        w = gen.block_sparse(B=8, T=T, H=16, density=0.5, causal=False)
+        q, k, v = (dev(torch, a, device).view(8, T, 16, 128) for a in (w.q, w.k, w.v))
+        m = dev(torch, w.idx, device)
+        out = torch.empty_like(q)
+        ws = torch.empty(nsa.nsa_block_sparse_workspace_size(nsa.make_shape(8 * T, 16, 16, 128, 1, batch=8,
+                                                                              seqlen=T)),
+                         dtype=torch.uint8, device=device)
+
+        def step():
+            nsa.nsa_block_sparse_fwd(q, k, v, m, causal=False, workspace=ws, out=out)
+
+        ms = float(np.mean(timed(torch, step, steps, warmup, flush)))
+        flops = 4.0 * 128 * float(w.idx.astype(np.int64).sum()) * 64 * 64
+        tf = flops / (ms * 1e-3) / 1e12
+        res[f"T{T}"] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "flops": flops}
+        del q, k, v, m, out, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 # kernels of one layer call: compress K, compress V, transpose V_cmp, transpose V,
 # compressed branch + block scores, top-k, selected branch, sliding branch, gated sum
 LAYER_LAUNCHES = 9
@@ -307,7 +333,7 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "decode", "selection", "layer"],
+    ap.add_argument("--only", default="", choices=["", "prefill", "decode", "selection", "layer", "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -338,9 +364,10 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("decode", "selection", "layer"):
+    if args.only in ("decode", "selection", "layer", "block_sparse"):
         fn = {"decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
+              "block_sparse": lambda: bench_block_sparse(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "layer": lambda: bench_layer(torch, nsa, device, args.steps, args.warmup, flush,
                                            args.layer_tokens)}[args.only]
         print(json.dumps({"only": args.only, **fn()}), flush=True)
@@ -424,6 +451,13 @@ def main():
             line["gpu_launches"] += 3 * args.steps
         except Exception as e:
             line["selection"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["block_sparse"] = bench_block_sparse(torch, nsa, device, max(3, args.steps // 2), args.warmup,
+                                                      flush, peaks)
+            line["gpu_launches"] += 2 * 3 * max(3, args.steps // 2)
+        except Exception as e:
+            line["block_sparse"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             line["layer"] = bench_layer(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush)

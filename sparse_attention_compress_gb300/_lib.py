@@ -177,6 +177,14 @@ def nsa_cmp_scores_pool(q, k_cmp, h_kv, kernel=32, stride=16, block_size=64, sca
     return out
 
 
+def nsa_block_sparse_workspace_size(shape: NsaShape) -> int:
+    return int(load().nsa_block_sparse_workspace_size(ctypes.byref(shape)))
+
+
+def nsa_select_workspace_size(shape: NsaShape, block_size=64) -> int:
+    return int(load().nsa_select_workspace_size(ctypes.byref(shape), block_size))
+
+
 def nsa_block_sparse_fwd(q, k, v, block_mask, causal=True, block_size=64, scale=0.0, *, workspace=None, out=None,
                          lse=None, stream=None):
     """Block-mask sparse attention; q/k/v [B, T, H, d] bf16, block_mask uint8 [B, H, T/64, T/64]."""
