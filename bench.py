@@ -239,6 +239,46 @@ def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
                                "bytes": int(cbytes)}}
 
 
+def bench_decode_offload(torch, nsa, device, steps, warmup, flush):
+    """The decode workload with its K/V cache in page-locked host memory (the offloaded
+    cache of the NOSA inference system); compressed keys, q and o stay in HBM."""
+    w = gen.decode()
+    n_c = nsa.num_cmp(w.max_len)
+    kcmp = nsa.nsa_compress_k(dev(torch, w.k_cache, device)).view(w.batch, n_c, w.hkv, w.d)
+    torch.cuda.empty_cache()
+    hk = pinned(torch, w.k_cache).view(torch.bfloat16)
+    hv = pinned(torch, w.v_cache).view(torch.bfloat16)
+    q, sl = dev(torch, w.q, device), dev(torch, w.seqlens, device)
+    ws = torch.empty(nsa.nsa_sparse_decode_workspace_size(w.batch, w.max_len, w.h, w.hkv, w.d, k=w.topk),
+                     dtype=torch.uint8, device=device)
+    idx = torch.empty((w.batch, w.hkv, w.topk), dtype=torch.int32, device=device)
+    out = torch.empty_like(q)
+
+    def step():
+        nsa.nsa_sparse_decode(q, hk, hv, kcmp, sl, k=w.topk, workspace=ws, idx_out=idx, out=out)
+
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        step()
+    torch.cuda.current_stream().wait_stream(st)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    ms_step = float(np.mean(timed(torch, g.replay, steps, warmup, flush)))
+    ih = idx.cpu().numpy().astype(np.int64)
+    t = (w.seqlens.astype(np.int64) - 1)[:, None, None]
+    keys = np.where(ih >= 0, np.clip(t - ih * 64 + 1, 0, 64), 0).sum()
+    link_bytes = int(keys * w.d * 2 * 2)  # chosen K and V rows, read from host memory
+    full_bytes = int(w.seqlens.astype(np.int64).sum() * w.hkv * w.d * 2 * 2)  # every cached K and V row
+    del hk, hv
+    return {"workload": "decode B=32 L=32768 H=16 Hkv=2 d=128 bf16 top-k 64 (blocks of 64), K/V cache "
+                        "(1.07 GB) in page-locked host memory, compressed keys in HBM",
+            "ms_per_step": ms_step, "tokens_per_s": w.batch / (ms_step * 1e-3),
+            "link_bytes_per_step": link_bytes, "link_gbs": link_bytes / (ms_step * 1e-3) / 1e9,
+            "full_cache_bytes": full_bytes, "launches_per_step": 2, "memsets_per_step": 1, "cuda_graph": True}
+
+
 def bench_selection(torch, nsa, device, steps, warmup, flush):
     w = gen.selection()
     q, k = dev(torch, w.q, device), dev(torch, w.k, device)
@@ -333,7 +373,8 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "decode", "selection", "layer", "block_sparse"],
+    ap.add_argument("--only", default="", choices=["", "prefill", "decode", "decode_offload", "selection", "layer",
+                                                    "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -364,8 +405,9 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("decode", "selection", "layer", "block_sparse"):
+    if args.only in ("decode", "decode_offload", "selection", "layer", "block_sparse"):
         fn = {"decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "decode_offload": lambda: bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush),
               "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
               "block_sparse": lambda: bench_block_sparse(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "layer": lambda: bench_layer(torch, nsa, device, args.steps, args.warmup, flush,
@@ -447,6 +489,12 @@ def main():
             line["decode"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
+            line["decode_offload"] = bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush)
+            line["gpu_launches"] += 2 * args.steps
+        except Exception as e:
+            line["decode_offload"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
             line["selection"] = bench_selection(torch, nsa, device, args.steps, args.warmup, flush)
             line["gpu_launches"] += 3 * args.steps
         except Exception as e:
@@ -476,6 +524,15 @@ def main():
             rf["gather_frac_of_l2_gather"] = rf["gather_gbs"] / pr["l2_gather_gbs"]
             rf["mma_sync_peak_tflops"] = pr["mma_sync_bf16_tflops"]
             rf["frac_of_mma_sync"] = kernel_tflops / pr["mma_sync_bf16_tflops"]
+            off = line.get("decode_offload", {})
+            if "link_gbs" in off and pr.get("c2c_gather_gbs"):
+                # the chosen blocks are random 4 KB slices of host memory: the gather probe bounds them
+                off["roofline"] = {"bound": "cpu-gpu link", "achieved": off["link_gbs"], "peak": pr["c2c_gather_gbs"],
+                                   "unit": "GB/s", "frac": off["link_gbs"] / pr["c2c_gather_gbs"],
+                                   "peak_source": "live probe: random 4 KB host-memory slices into shared memory"}
+                # no kernel can attend over the whole offloaded cache faster than it streams over the link
+                off["full_attention_floor_ms"] = off["full_cache_bytes"] / (pr["c2c_read_gbs"] * 1e9) * 1e3
+                off["speedup_vs_full_attention_floor"] = off["full_attention_floor_ms"] / off["ms_per_step"]
             if "tflops" in line.get("layer", {}):
                 line["layer"]["frac_of_bf16_peak"] = line["layer"]["tflops"] / peaks["bf16_tflops"]
         except Exception as e:

@@ -210,8 +210,14 @@ NSA_API nsa_status nsa_gate_combine(int64_t tokens, int h, int d, const void* o_
  * attention runs over the chosen blocks only (S5).
  *   seqlens      device int32 [batch], 1 <= L_b <= max_len
  *   q, o         [batch, h, d] bf16
- *   k_cache, v_cache  [batch, max_len, h_kv, d] bf16
- *   k_cmp_cache  [batch, n_c(max_len), h_kv, d] bf16; rows c < n_c(L_b) valid
+ *   k_cache, v_cache  [batch, max_len, h_kv, d] bf16, in device memory or in page-locked
+ *                host memory ([NOSA-Parts] "core idea": the KV cache is offloaded to host
+ *                memory and only the chosen blocks come back).  A host cache must come from
+ *                cudaHostAlloc or cudaHostRegister; the chosen blocks are then read over the
+ *                CPU-GPU link straight into shared memory, with no device copy of the cache.
+ *                Pageable host memory is rejected with NSA_ERR_INVALID.
+ *   k_cmp_cache  [batch, n_c(max_len), h_kv, d] bf16; rows c < n_c(L_b) valid; device or
+ *                page-locked host memory (keep it on the device: every step reads all of it)
  *   idx_out      nullable [batch, h_kv, k] int32: the chosen blocks
  *   workspace    device scratch of nsa_sparse_decode_workspace_size() bytes, 256-byte
  *                aligned, owned by the caller, not read before it is written

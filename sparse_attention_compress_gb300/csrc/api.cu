@@ -329,6 +329,31 @@ nsa_status nsa_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, con
                      "nsa_gate_combine");
 }
 
+// The address a kernel uses for a K/V cache that may sit in device memory or in
+// page-locked host memory.  [NOSA-Parts] "core idea": the whole KV cache is offloaded to
+// host memory and only the chosen blocks travel back to the GPU; on a Grace-Blackwell
+// node host memory is reachable from the SMs over the coherent chip-to-chip link, so the
+// decode kernel's gather reads the chosen blocks straight from it into shared memory.
+// Pageable host memory is rejected: only allocations known to the CUDA runtime
+// (cudaHostAlloc, cudaHostRegister) have a device address here.
+static nsa_status gpu_address(const void* p, const void** out, const char* what) {
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(NSA_ERR_INVALID, "nsa_sparse_decode: %s: pointer query failed (%s)", what, cudaGetErrorString(e));
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return NSA_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+    *out = a.devicePointer;
+    return NSA_OK;
+  }
+  return fail(NSA_ERR_INVALID, "nsa_sparse_decode: %s must be device memory or page-locked host memory", what);
+}
+
 size_t nsa_sparse_decode_workspace_size(int batch, int max_len, int h, int h_kv, int d, int kernel,
                                         int stride, int block_size, int k) {
   if (batch <= 0 || max_len <= 0 || h <= 0 || h_kv <= 0 || h % h_kv || k <= 0 || kernel <= 0 || stride <= 0)
@@ -379,9 +404,10 @@ nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int
   a.scale = scale > 0.f ? scale : 1.f / sqrtf((float)d);
   a.seqlens = seqlens;
   a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.kc_cache = k_cmp_cache;
+  nsa_status ps = gpu_address(k_cache, &a.k_cache, "k_cache");
+  if (ps == NSA_OK) ps = gpu_address(v_cache, &a.v_cache, "v_cache");
+  if (ps == NSA_OK && max_len >= kernel) ps = gpu_address(k_cmp_cache, &a.kc_cache, "k_cmp_cache");
+  if (ps != NSA_OK) return ps;
   a.idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + l.idx);
   a.o = o;
   a.z = reinterpret_cast<float*>(w + l.z);

@@ -227,6 +227,4 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   if (block_size == 32) return run_mma<64, 32, NS>(p, grid, st);
   return run_mma<64, 16, NS>(p, grid, st);
 }
-
-// Decode attention over the chosen blocks, split over the list, then merged.
 }  // namespace nsa

@@ -1,4 +1,4 @@
-"""Roofline micro-benchmarks (L2 and HBM read bandwidth, mma.sync bf16 and ex2 rates).
+"""Roofline micro-benchmarks (L2, HBM and host-memory read bandwidth, mma.sync bf16 and ex2 rates).
 
 run() compiles rooflines.cu with nvcc for sm_103a and returns its JSON result; the
 benchmark uses it for the secondary ceilings of its roofline report.

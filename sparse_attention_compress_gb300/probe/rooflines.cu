@@ -2,11 +2,14 @@
 // JSON object: L2-resident read bandwidth (the gather of selected K/V blocks is served
 // from L2), the L2 -> shared-memory gather rate of random 4 KB slices by cp.async (the
 // selected-attention access pattern, with no compute), HBM read bandwidth, the legacy
-// mma.sync.m16n8k16 bf16 rate (the MMA the selected-attention kernels use) and the
-// ex2.approx rate (softmax exponentials).
+// mma.sync.m16n8k16 bf16 rate (the MMA the selected-attention kernels use), the
+// ex2.approx rate (softmax exponentials) and, for a KV cache kept in page-locked host
+// memory, the rates at which the SMs read that memory over the CPU-GPU link: a streaming
+// read, the same random 4 KB-slice gather, and a copy-engine host-to-device copy.
 // Standalone program; no part of the library.
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <cuda_runtime.h>
 
 __global__ void read_kernel(const uint4* __restrict__ p, size_t n, int iters, unsigned* out) {
@@ -160,6 +163,38 @@ int main() {
     gather = (double)g.grid * 4 * g.iters * 8192.0 / (ms * 1e-3) / 1e9;
     cudaFree(p);
   }
+  double c2c_read = 0, c2c_gather = 0, h2d_copy = 0;
+  {
+    const size_t bytes = (size_t)1 << 30;
+    uint8_t* h = nullptr;
+    uint8_t* d = nullptr;
+    if (cudaHostAlloc(&h, bytes, cudaHostAllocMapped) != cudaSuccess || cudaMalloc(&d, bytes) != cudaSuccess) {
+      printf("{\"error\": \"host allocation\"}\n");
+      return 1;
+    }
+    memset(h, 1, bytes);
+    uint8_t* hd = nullptr;
+    cudaHostGetDevicePointer(reinterpret_cast<void**>(&hd), h, 0);
+    ReadArg r{reinterpret_cast<const uint4*>(hd), bytes / 16, 1, out, grid};
+    c2c_read = (double)bytes / (timed_ms(launch_read, &r) * 1e-3) / 1e9;
+    GatherArg g{hd, (uint32_t)(bytes / 4096), 64, sms * 3};
+    c2c_gather = (double)g.grid * 4 * g.iters * 8192.0 / (timed_ms(launch_gather, &g) * 1e-3) / 1e9;
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice);
+    cudaEventRecord(a);
+    cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice);
+    cudaEventRecord(b);
+    cudaEventSynchronize(b);
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, a, b);
+    h2d_copy = (double)bytes / (ms * 1e-3) / 1e9;
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    cudaFree(d);
+    cudaFreeHost(h);
+  }
   float* fo = nullptr;
   cudaMalloc(&fo, (size_t)sms * 4 * 256 * 4);
   ComputeArg cm{fo, 4096, sms * 4, true};
@@ -170,9 +205,11 @@ int main() {
   const double ex2_rate = (double)ce.grid * 256 * ce.iters * 8 / (ms_ex2 * 1e-3);
   const cudaError_t e = cudaGetLastError();
   printf("{\"l2_read_gbs\": %.1f, \"l2_gather_gbs\": %.1f, \"hbm_read_gbs\": %.1f, "
-         "\"mma_sync_bf16_tflops\": %.1f, \"ex2_per_sm_per_clk\": %.2f, \"sms\": %d, \"clock_mhz\": %.0f, "
+         "\"mma_sync_bf16_tflops\": %.1f, \"ex2_per_sm_per_clk\": %.2f, \"c2c_read_gbs\": %.1f, "
+         "\"c2c_gather_gbs\": %.1f, \"h2d_copy_gbs\": %.1f, \"sms\": %d, \"clock_mhz\": %.0f, "
          "\"error\": \"%s\"}\n",
-         bw[0], gather, bw[1], mma_tf, ex2_rate / sms / (clk_khz * 1e3), sms, clk_khz / 1e3,
+         bw[0], gather, bw[1], mma_tf, ex2_rate / sms / (clk_khz * 1e3), c2c_read, c2c_gather, h2d_copy, sms,
+         clk_khz / 1e3,
          e == cudaSuccess ? "" : cudaGetErrorString(e));
   cudaFree(out);
   cudaFree(fo);

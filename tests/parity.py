@@ -21,6 +21,14 @@ def dev(a, device="cuda"):
     return torch.from_numpy(a).to(device)
 
 
+def pinned(a):
+    """numpy array -> page-locked host tensor (bf16 bits as uint16 -> bfloat16)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).pin_memory().view(torch.bfloat16)
+    return torch.from_numpy(a).pin_memory()
+
+
 def host(t):
     """device tensor -> numpy (bf16 -> uint16 bits, others as is)."""
     t = t.detach().cpu()

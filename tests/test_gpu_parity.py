@@ -9,7 +9,7 @@ import torch
 import sparse_attention_compress_gb300 as nsa
 from oracle import oracle as orc
 from sparse_attention_compress_gb300 import inputs as gen
-from tests.parity import as_f64, assert_close, dev, host, selection_mismatches
+from tests.parity import as_f64, assert_close, dev, host, pinned, selection_mismatches
 
 pytestmark = pytest.mark.gpu
 
@@ -298,6 +298,62 @@ def test_decode_full_size():
     assert outside == 0, (n_mis, outside)
     _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kch, w.seqlens, k=64, idx_in=gi)
     assert_close(out, ref_o, what="decode full")
+
+
+@pytest.mark.parametrize("B,L,seqlens,k,H,HKV", [(4, 4096, [4096, 2500, 70, 1], 64, 16, 2),
+                                                  (5, 1500, [1500, 31, 64, 65, 1200], 1, 8, 2),
+                                                  (3, 3000, [3000, 1500, 40], 64, 16, 1)])
+def test_decode_offloaded_cache(B, L, seqlens, k, H, HKV):
+    """K/V cache in page-locked host memory, compressed keys on the device: the chosen
+    blocks are read over the CPU-GPU link.  Same kernels, so the outputs equal those of
+    the device-resident cache bit for bit, and they match the oracle."""
+    w, kc_cache = _decode_case(B, L, seqlens, k, 0, H=H, HKV=HKV)
+    hk, hv = pinned(w.k_cache), pinned(w.v_cache)
+    assert hk.device.type == "cpu" and hk.is_pinned()
+    q, kc, sl = dev(w.q), dev(kc_cache), dev(w.seqlens)
+    idx_h = torch.empty((B, HKV, k), dtype=torch.int32, device="cuda")
+    out_h = nsa.nsa_sparse_decode(q, hk, hv, kc, sl, k=k, idx_out=idx_h)
+    idx_d = torch.empty_like(idx_h)
+    out_d = nsa.nsa_sparse_decode(q, dev(w.k_cache), dev(w.v_cache), kc, sl, k=k, idx_out=idx_d)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    assert torch.equal(idx_h, idx_d)
+    assert torch.equal(out_h.view(torch.int16), out_d.view(torch.int16))
+    gi = host(idx_h)
+    ref_idx, _, ref_sc = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, want_scores=True)
+    n_mis, outside = selection_mismatches(gi, ref_idx, ref_sc, np.asarray(w.seqlens) - 1)
+    assert outside == 0, (n_mis, outside)
+    _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, idx_in=gi)
+    assert_close(out_h, ref_o, what="decode offloaded")
+
+
+def test_decode_offloaded_full_size_sampled():
+    """B=32, context 32768, H=16, Hkv=2, d=128, top-k 64 with the 1 GB K/V cache in
+    page-locked host memory; the oracle checks eight sampled sequences."""
+    w = gen.decode()
+    kc_cache = nsa.nsa_compress_k(dev(w.k_cache)).view(32, orc.num_cmp(32768), 2, 128)
+    hk, hv = pinned(w.k_cache), pinned(w.v_cache)
+    idx = torch.empty((32, 2, 64), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode(dev(w.q), hk, hv, kc_cache, dev(w.seqlens), k=64, idx_out=idx)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    rows = np.random.default_rng(5).choice(32, 8, replace=False)
+    kch, gi, go = host(kc_cache)[rows], host(idx)[rows], host(out)[rows]
+    sl = np.asarray(w.seqlens)[rows]
+    ref_idx, _, ref_sc = orc.decode(w.q[rows], w.k_cache[rows], w.v_cache[rows], kch, sl, k=64, want_scores=True)
+    n_mis, outside = selection_mismatches(gi, ref_idx, ref_sc, sl - 1)
+    assert outside == 0, (n_mis, outside)
+    _, ref_o = orc.decode(w.q[rows], w.k_cache[rows], w.v_cache[rows], kch, sl, k=64, idx_in=gi)
+    assert_close(go, ref_o, what="decode offloaded full")
+
+
+def test_decode_rejects_pageable_cache():
+    """A pageable host cache has no device address: the call fails before any launch."""
+    w, kc_cache = _decode_case(2, 300, [300, 33], 16, 0)
+    kp = torch.from_numpy(np.ascontiguousarray(w.k_cache).view(np.int16)).view(torch.bfloat16)
+    assert not kp.is_pinned()
+    with pytest.raises(RuntimeError, match="page-locked"):
+        nsa.nsa_sparse_decode(dev(w.q), kp, dev(w.v_cache), dev(kc_cache), dev(w.seqlens), k=16)
 
 
 # --------------------------------------------------------------------------- fused selection and the layer
