@@ -447,6 +447,154 @@ int nsa_oracle_sparse_attn(const void* q, const void* k, const void* v, int dtyp
   return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Backward of S5: gradients of the selected-block attention with respect to q, k
+ * and v for an upstream gradient dO.  The pages give the forward only ([TileLang-NSA]
+ * sec. 2; the training claims of [NSA-Triton] sec. 4 need its gradient); this is the
+ * derivative of that forward written out.  For one (token, head) with list keys
+ * tau_1..tau_n (as in selected_keys, duplicates included):
+ *   s_e = scale q . k_e,  p = softmax(s),  o = sum_e p_e v_e,
+ *   dp_e = dO . v_e,  D = sum_e p_e dp_e  (= dO . o),  ds_e = p_e (dp_e - D),
+ *   dq = scale sum_e ds_e k_e,  dk[tau_e] += scale ds_e q,  dv[tau_e] += p_e dO.
+ * A row with no key contributes nothing.
+ * dq [n_q_rows, h, d] for q_rows (every token when NULL; n_q_rows < 0 skips dq);
+ * dk, dv [n_kv_rows, hkv, d] for the key rows kv_rows (every token when NULL;
+ * n_kv_rows < 0 skips them).  Only tokens whose lists reach a requested key row are
+ * visited for dk and dv.  Thread-private accumulators are summed in thread order. */
+static void row_probs_grads(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                            int64_t tok, int hh, int h, int hkv, int d, int g, int64_t seq_start,
+                            const int* keys, int n, double scale, double* p, double* ds) {
+  double mx = -INFINITY;
+  for (int e = 0; e < n; ++e) {
+    double acc = 0.0;
+    size_t kr = ((size_t)(seq_start + keys[e]) * hkv + g) * d;
+    for (int i = 0; i < d; ++i) acc += ld(q, dtype, ((size_t)tok * h + hh) * d + i) * ld(k, dtype, kr + i);
+    p[e] = acc * scale;
+    if (p[e] > mx) mx = p[e];
+  }
+  double sum = 0.0;
+  for (int e = 0; e < n; ++e) sum += exp(p[e] - mx);
+  for (int e = 0; e < n; ++e) p[e] = exp(p[e] - mx) / sum;
+  double D = 0.0;
+  for (int e = 0; e < n; ++e) {
+    double acc = 0.0;
+    size_t vr = ((size_t)(seq_start + keys[e]) * hkv + g) * d;
+    for (int i = 0; i < d; ++i) acc += ld(dout, dtype, ((size_t)tok * h + hh) * d + i) * ld(v, dtype, vr + i);
+    ds[e] = acc;  /* dp_e for now */
+    D += p[e] * acc;
+  }
+  for (int e = 0; e < n; ++e) ds[e] = p[e] * (ds[e] - D);
+}
+
+int nsa_oracle_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                               const int32_t* cu, int n_seqs, int h, int hkv, int d, const int32_t* idx, int S,
+                               int block_size, double scale, const int64_t* q_rows, int64_t n_q_rows, double* dq,
+                               const int64_t* kv_rows, int64_t n_kv_rows, double* dk, double* dv) {
+  if (h % hkv || block_size <= 0) return 1;
+  const int64_t total = cu[n_seqs];
+  const int r = h / hkv;
+  const int max_keys = S * block_size + 1;
+  if (n_q_rows >= 0 && !q_rows) n_q_rows = total;
+  if (n_q_rows > 0) {
+#pragma omp parallel
+    {
+      int* keys = (int*)malloc(sizeof(int) * (size_t)max_keys);
+      double* p = (double*)malloc(sizeof(double) * (size_t)max_keys);
+      double* ds = (double*)malloc(sizeof(double) * (size_t)max_keys);
+#pragma omp for schedule(dynamic, 8)
+      for (int64_t rr = 0; rr < n_q_rows; ++rr) {
+        int64_t tok = q_rows ? q_rows[rr] : rr;
+        int sq = seq_of(cu, n_seqs, tok);
+        int t = (int)(tok - cu[sq]);
+        for (int hh = 0; hh < h; ++hh) {
+          int g = hh / r;
+          double* out = dq + ((size_t)rr * h + hh) * d;
+          for (int i = 0; i < d; ++i) out[i] = 0.0;
+          int n = selected_keys(idx + ((size_t)tok * hkv + g) * S, S, block_size, t, keys);
+          if (n == 0) continue;
+          row_probs_grads(q, k, v, dout, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
+          for (int e = 0; e < n; ++e) {
+            size_t kr = ((size_t)(cu[sq] + keys[e]) * hkv + g) * d;
+            for (int i = 0; i < d; ++i) out[i] += scale * ds[e] * ld(k, dtype, kr + i);
+          }
+        }
+      }
+      free(keys);
+      free(p);
+      free(ds);
+    }
+  }
+  if (n_kv_rows >= 0 && !kv_rows) n_kv_rows = total;
+  if (n_kv_rows <= 0) return 0;
+  /* slot of every token as a requested key row (-1: not requested) */
+  int64_t* slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)(total + 1));
+  if (!slot) return 2;
+  for (int64_t i = 0; i < total; ++i) slot[i] = kv_rows ? -1 : i;
+  if (kv_rows)
+    for (int64_t i = 0; i < n_kv_rows; ++i) slot[kv_rows[i]] = i;
+  const size_t acc_len = (size_t)n_kv_rows * hkv * d;
+  for (size_t i = 0; i < acc_len; ++i) dk[i] = dv[i] = 0.0;
+  int nthr = 1;
+#ifdef _OPENMP
+  nthr = omp_get_max_threads();
+#endif
+  double* acc = (double*)calloc((size_t)nthr * 2 * acc_len, sizeof(double));
+  if (!acc) {
+    free(slot);
+    return 2;
+  }
+#pragma omp parallel num_threads(nthr)
+  {
+    int me = 0;
+#ifdef _OPENMP
+    me = omp_get_thread_num();
+#endif
+    double* mdk = acc + (size_t)me * 2 * acc_len;
+    double* mdv = mdk + acc_len;
+    int* keys = (int*)malloc(sizeof(int) * (size_t)max_keys);
+    double* p = (double*)malloc(sizeof(double) * (size_t)max_keys);
+    double* ds = (double*)malloc(sizeof(double) * (size_t)max_keys);
+#pragma omp for schedule(static)
+    for (int64_t tok = 0; tok < total; ++tok) {
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      for (int g = 0; g < hkv; ++g) {
+        int n = selected_keys(idx + ((size_t)tok * hkv + g) * S, S, block_size, t, keys);
+        int hit = 0;
+        for (int e = 0; e < n && !hit; ++e) hit = slot[cu[sq] + keys[e]] >= 0;
+        if (!hit) continue;
+        for (int hh = g * r; hh < (g + 1) * r; ++hh) {
+          row_probs_grads(q, k, v, dout, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
+          for (int e = 0; e < n; ++e) {
+            int64_t sl = slot[cu[sq] + keys[e]];
+            if (sl < 0) continue;
+            double* ak = mdk + ((size_t)sl * hkv + g) * d;
+            double* av = mdv + ((size_t)sl * hkv + g) * d;
+            for (int i = 0; i < d; ++i) {
+              ak[i] += scale * ds[e] * ld(q, dtype, ((size_t)tok * h + hh) * d + i);
+              av[i] += p[e] * ld(dout, dtype, ((size_t)tok * h + hh) * d + i);
+            }
+          }
+        }
+      }
+    }
+    free(keys);
+    free(p);
+    free(ds);
+  }
+  for (int th = 0; th < nthr; ++th) {
+    const double* mdk = acc + (size_t)th * 2 * acc_len;
+    const double* mdv = mdk + acc_len;
+    for (size_t i = 0; i < acc_len; ++i) {
+      dk[i] += mdk[i];
+      dv[i] += mdv[i];
+    }
+  }
+  free(acc);
+  free(slot);
+  return 0;
+}
+
 /* Block-mask sparse attention ([TileLang-NSA] sec. 1, block-sparse attention: the
  * attention matrix is cut into block x block tiles and a mask marks the active ones;
  * only active tiles are computed; is_causal keeps the lower triangle).  Dense layout:

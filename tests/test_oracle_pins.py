@@ -468,3 +468,117 @@ def test_block_sparse_full_mask_is_dense_causal_and_empty_row_is_zero():
     o2, lse2 = orc.block_sparse_attn(q, k, v, m, causal=False, block=block)
     assert np.all(o2[64:128, 0] == 0) and np.all(np.isneginf(lse2[64:128, 0]))
     assert np.all(np.isfinite(lse2[:64, 0])) and np.all(np.isfinite(lse2[:, 1]))
+
+
+# --------------------------------------------------------------------------- S5 backward
+def _bwd_lists(cu, hkv, bs, S, seed, dup=True):
+    """Per (token, kv-head) lists: own block, random blocks (some non-causal), a -1 and,
+    on every other token, a repeated entry."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for i in range(len(cu) - 1):
+        L = int(cu[i + 1] - cu[i])
+        nb = -(-L // bs)
+        for t in range(L):
+            per_g = []
+            for _ in range(hkv):
+                e = [t // bs] + list(rng.integers(0, nb, S - 2)) + [-1]
+                if dup and t % 2:
+                    e[-1] = e[1]
+                per_g.append(e)
+            rows.append(per_g)
+    return np.asarray(rows, np.int32)
+
+
+def _autograd_selected(q, k, v, do, idx, cu, bs, scale):
+    """Selected attention written densely in float64 torch ops (logit + log multiplicity
+    of each key in the token's expanded list), differentiated by autograd."""
+    Q, K, V = (_t(a).requires_grad_(True) for a in (q, k, v))
+    dO = _t(do)
+    h, hkv = Q.shape[1], K.shape[1]
+    r = h // hkv
+    loss = 0.0
+    for i in range(len(cu) - 1):
+        a, b = int(cu[i]), int(cu[i + 1])
+        L = b - a
+        mult = np.zeros((L, hkv, L))
+        for t in range(L):
+            for g in range(hkv):
+                for j in idx[a + t, g]:
+                    if j < 0 or j * bs > t:
+                        continue
+                    for tau in range(j * bs, min((j + 1) * bs, t + 1, L)):
+                        mult[t, g, tau] += 1
+        logm = torch.from_numpy(np.where(mult > 0, np.log(np.maximum(mult, 1)), -np.inf))
+        logm = logm.repeat_interleave(r, dim=1)                          # [L, h, L]
+        s = torch.einsum("thd,shd->ths", Q[a:b], K[a:b].repeat_interleave(r, 1)) * scale + logm
+        p = torch.softmax(s, dim=-1)
+        o = torch.einsum("ths,shd->thd", p, V[a:b].repeat_interleave(r, 1))
+        loss = loss + (o * dO[a:b]).sum()
+    loss.backward()
+    return Q.grad, K.grad, V.grad
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sparse_bwd_equals_autograd(dtype):
+    lengths = [150, 97]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, bs, S = 4, 2, 16, 32, 5
+    q, do = _rand((cu[-1], h, d), 31, dtype), _rand((cu[-1], h, d), 32, dtype)
+    k, v = _rand((cu[-1], hkv, d), 33, dtype), _rand((cu[-1], hkv, d), 34, dtype)
+    idx = _bwd_lists(cu, hkv, bs, S, 35)
+    dq, dk, dv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs)
+    gq, gk, gv = _autograd_selected(q, k, v, do, idx, cu, bs, d ** -0.5)
+    for ours, ref in ((dq, gq), (dk, gk), (dv, gv)):
+        assert torch.allclose(torch.from_numpy(ours), ref, atol=1e-12, rtol=1e-10)
+
+
+def test_sparse_bwd_finite_differences():
+    """Directional derivatives of sum(dO * o) through the (separately pinned) forward."""
+    T, h, hkv, d, bs, S = 70, 2, 1, 8, 16, 3
+    cu = gen.dense_cu_seqlens(1, T)
+    q, k, v, do = (_rand((T, hh, d), s, "f32") for s, hh in ((41, h), (42, hkv), (43, hkv), (44, h)))
+    idx = _bwd_lists(cu, hkv, bs, S, 45, dup=False)
+    dq, dk, dv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs)
+    rng = np.random.default_rng(46)
+    eps = 1e-2
+
+    def loss(qq, kk, vv):
+        o, _ = orc.sparse_attn(qq, kk, vv, idx, cu, bs)
+        return float((o * do.astype(np.float64)).sum())
+
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        args = [q, k, v]
+        delta = rng.standard_normal(args[which].shape)
+        plus, minus = list(args), list(args)
+        plus[which] = (args[which] + eps * delta).astype(np.float32)
+        minus[which] = (args[which] - eps * delta).astype(np.float32)
+        step = plus[which].astype(np.float64) - minus[which].astype(np.float64)
+        fd = loss(*plus) - loss(*minus)
+        an = float((grad * step).sum())
+        assert abs(fd - an) <= 1e-4 * max(1.0, abs(an)), (which, fd, an)
+
+
+def test_sparse_bwd_invariants_and_sampling():
+    """Per sequence and kv-head: the dK rows sum to zero (each row's ds sums to zero)
+    and the dV rows sum to the dO of every row that has keys.  Requested subsets of
+    rows equal the same rows of the full result."""
+    lengths = [300, 129]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, bs, S = 4, 2, 32, 32, 5
+    q, do = _rand((cu[-1], h, d), 51), _rand((cu[-1], h, d), 52)
+    k, v = _rand((cu[-1], hkv, d), 53), _rand((cu[-1], hkv, d), 54)
+    idx = _bwd_lists(cu, hkv, bs, S, 55)
+    dq, dk, dv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs)
+    dof = gen.bf16_bits_to_f32(do).astype(np.float64)
+    for i in range(len(lengths)):
+        sl = slice(cu[i], cu[i + 1])
+        for g in range(hkv):
+            assert np.abs(dk[sl, g].sum(0)).max() < 1e-10
+            want = dof[sl, 2 * g:2 * g + 2].sum((0, 1))  # every row lists its own block
+            assert np.allclose(dv[sl, g].sum(0), want, atol=1e-10, rtol=0)
+    qr = [0, 5, 149, 150, 428]
+    kr = [1, 31, 32, 200, 299, 300, 301, 428]
+    sq, sk, sv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs, q_rows=qr, kv_rows=kr)
+    assert np.allclose(sq, dq[qr], atol=1e-13, rtol=0)
+    assert np.allclose(sk, dk[kr], atol=1e-13, rtol=0) and np.allclose(sv, dv[kr], atol=1e-13, rtol=0)
