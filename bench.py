@@ -239,6 +239,33 @@ def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
                                "bytes": int(cbytes)}}
 
 
+def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks):
+    """Backward of the selected branch on the prefill workload: dq, dk, dv from the
+    forward's o and lse and a seeded upstream gradient."""
+    from sparse_attention_compress_gb300 import _lib
+    w = gen.prefill()
+    q = dev(torch, w.q, device).view(w.batch, w.seqlen, w.h, w.d)
+    k, v, idx = dev(torch, w.k, device), dev(torch, w.v, device), dev(torch, w.idx, device)
+    do = dev(torch, gen.normal(gen.rng_for(1, 99), (w.tokens, w.h, w.d), "bf16"), device)
+    lse = torch.empty((w.tokens, w.h), dtype=torch.float32, device=device)
+    o = nsa.nsa_sparse_fwd(q, k, v, idx, w.block_size, lse=lse).view(w.tokens, w.h, w.d)
+    shp = _lib.make_shape(w.tokens, w.h, w.hkv, w.d, _lib.NSA_BF16, batch=w.batch, seqlen=w.seqlen)
+    ws = torch.empty(nsa.nsa_sparse_bwd_workspace_size(shp, w.S), dtype=torch.uint8, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step():
+        nsa.nsa_sparse_bwd(q, k, v, idx, o, lse, do, w.block_size, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    ms_step = float(np.mean(timed(torch, step, steps, warmup, flush)))
+    # five products per attended (row, key) pair: S and dP recomputed, dQ, dK, dV
+    flops = prefill_flops(w) * 10 / 4
+    tf = flops / (ms_step * 1e-3) / 1e12
+    return {"workload": "backward of selected attention, prefill B=8 T=16384 H=16 Hkv=1 d=128 bf16, block 64, "
+                        "S=16", "ms_per_step": ms_step, "tflops": tf, "flops_per_step": flops,
+            "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "workspace_bytes": int(ws.numel()),
+            "launches_per_step": 3}
+
+
 def bench_decode_offload(torch, nsa, device, steps, warmup, flush):
     """The decode workload with its K/V cache in page-locked host memory (the offloaded
     cache of the NOSA inference system); compressed keys, q and o stay in HBM."""
@@ -373,8 +400,8 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "decode", "decode_offload", "selection", "layer",
-                                                    "block_sparse"],
+    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "decode", "decode_offload", "selection",
+                                                    "layer", "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -405,8 +432,9 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("decode", "decode_offload", "selection", "layer", "block_sparse"):
-        fn = {"decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+    if args.only in ("prefill_bwd", "decode", "decode_offload", "selection", "layer", "block_sparse"):
+        fn = {"prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode_offload": lambda: bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush),
               "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
               "block_sparse": lambda: bench_block_sparse(torch, nsa, device, args.steps, args.warmup, flush, peaks),
@@ -481,6 +509,13 @@ def main():
 
     if world == 1 and not args.no_extras:
         del q, k, v, out, qv
+        torch.cuda.empty_cache()
+        try:
+            line["prefill_bwd"] = bench_prefill_bwd(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush,
+                                                    peaks)
+            line["gpu_launches"] += 3 * max(3, args.steps // 2)
+        except Exception as e:
+            line["prefill_bwd"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             line["decode"] = bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks)

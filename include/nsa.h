@@ -161,6 +161,28 @@ NSA_API nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const v
                           const int32_t* block_indices, int S, int block_size, float scale, void* o,
                           float* lse, cudaStream_t stream);
 
+/* Backward of S5: gradients of the selected-block attention for an upstream gradient
+ * dO.  The pages train with the selected branch ([NSA-Triton] sec. 4) and print its
+ * forward only ([TileLang-NSA] sec. 2); this is the derivative of that forward.  Per
+ * (token, head) row with list keys e (as in nsa_sparse_fwd, an index listed twice
+ * counts twice): p_e = exp(scale q.k_e - lse), dp_e = dO.v_e, D = dO.o,
+ * ds_e = p_e (dp_e - D); dq = scale sum_e ds_e k_e, dk[e] += scale ds_e q,
+ * dv[e] += p_e dO.
+ *   q, o, d_o, dq  [tokens, h, d] bf16;  k, v, dk, dv  [tokens, h_kv, d] bf16
+ *   block_indices  [tokens, h_kv, S] int32 (the forward's lists)
+ *   o, lse         the forward's outputs for the same inputs (lse [tokens, h] fp32)
+ *   workspace      device scratch of nsa_sparse_bwd_workspace_size() bytes, 256-byte
+ *                  aligned, owned by the caller (fp32 partial sums of dk and dv per
+ *                  (sequence, kv-head, key block, 2048-query chunk), and D)
+ * dk and dv are written for every key row (0 where no query selects it).  Results are
+ * deterministic (fixed summation order; no floating-point atomics).
+ * Requires bf16, d 128, block_size 64, S <= 64, h/h_kv <= 16. */
+NSA_API size_t nsa_sparse_bwd_workspace_size(const nsa_shape* shape, int S, int block_size);
+NSA_API nsa_status nsa_sparse_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                  const int32_t* block_indices, int S, int block_size, float scale, const void* o,
+                                  const float* lse, const void* d_o, void* dq, void* dk, void* dv, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
 /* Block-mask sparse attention (the block-sparse companion of the pages' native sparse
  * attention).  [TileLang-NSA] sec. 1, block-sparse attention: the attention matrix is
  * cut into block_size x block_size tiles and a mask marks the active ones; only active

@@ -456,13 +456,16 @@ int nsa_oracle_sparse_attn(const void* q, const void* k, const void* v, int dtyp
  *   s_e = scale q . k_e,  p = softmax(s),  o = sum_e p_e v_e,
  *   dp_e = dO . v_e,  D = sum_e p_e dp_e  (= dO . o),  ds_e = p_e (dp_e - D),
  *   dq = scale sum_e ds_e k_e,  dk[tau_e] += scale ds_e q,  dv[tau_e] += p_e dO.
- * A row with no key contributes nothing.
+ * A row with no key contributes nothing.  When o_in (the forward output the caller
+ * holds, same dtype as q; nullable) is given, D is taken as dO . o_in instead: the
+ * gradient step then uses the stored output, as a training step does when it keeps
+ * only the rounded forward output (D = dO . o is an identity of the exact forward).
  * dq [n_q_rows, h, d] for q_rows (every token when NULL; n_q_rows < 0 skips dq);
  * dk, dv [n_kv_rows, hkv, d] for the key rows kv_rows (every token when NULL;
  * n_kv_rows < 0 skips them).  Only tokens whose lists reach a requested key row are
  * visited for dk and dv.  Thread-private accumulators are summed in thread order. */
-static void row_probs_grads(const void* q, const void* k, const void* v, const void* dout, int dtype,
-                            int64_t tok, int hh, int h, int hkv, int d, int g, int64_t seq_start,
+static void row_probs_grads(const void* q, const void* k, const void* v, const void* dout, const void* o_in,
+                            int dtype, int64_t tok, int hh, int h, int hkv, int d, int g, int64_t seq_start,
                             const int* keys, int n, double scale, double* p, double* ds) {
   double mx = -INFINITY;
   for (int e = 0; e < n; ++e) {
@@ -483,10 +486,16 @@ static void row_probs_grads(const void* q, const void* k, const void* v, const v
     ds[e] = acc;  /* dp_e for now */
     D += p[e] * acc;
   }
+  if (o_in) {
+    D = 0.0;
+    for (int i = 0; i < d; ++i)
+      D += ld(dout, dtype, ((size_t)tok * h + hh) * d + i) * ld(o_in, dtype, ((size_t)tok * h + hh) * d + i);
+  }
   for (int e = 0; e < n; ++e) ds[e] = p[e] * (ds[e] - D);
 }
 
-int nsa_oracle_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
+int nsa_oracle_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* dout, const void* o_in,
+                               int dtype,
                                const int32_t* cu, int n_seqs, int h, int hkv, int d, const int32_t* idx, int S,
                                int block_size, double scale, const int64_t* q_rows, int64_t n_q_rows, double* dq,
                                const int64_t* kv_rows, int64_t n_kv_rows, double* dk, double* dv) {
@@ -512,7 +521,7 @@ int nsa_oracle_sparse_attn_bwd(const void* q, const void* k, const void* v, cons
           for (int i = 0; i < d; ++i) out[i] = 0.0;
           int n = selected_keys(idx + ((size_t)tok * hkv + g) * S, S, block_size, t, keys);
           if (n == 0) continue;
-          row_probs_grads(q, k, v, dout, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
+          row_probs_grads(q, k, v, dout, o_in, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
           for (int e = 0; e < n; ++e) {
             size_t kr = ((size_t)(cu[sq] + keys[e]) * hkv + g) * d;
             for (int i = 0; i < d; ++i) out[i] += scale * ds[e] * ld(k, dtype, kr + i);
@@ -564,7 +573,7 @@ int nsa_oracle_sparse_attn_bwd(const void* q, const void* k, const void* v, cons
         for (int e = 0; e < n && !hit; ++e) hit = slot[cu[sq] + keys[e]] >= 0;
         if (!hit) continue;
         for (int hh = g * r; hh < (g + 1) * r; ++hh) {
-          row_probs_grads(q, k, v, dout, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
+          row_probs_grads(q, k, v, dout, o_in, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
           for (int e = 0; e < n; ++e) {
             int64_t sl = slot[cu[sq] + keys[e]];
             if (sl < 0) continue;

@@ -172,14 +172,20 @@ def sparse_attn(q, k, v, idx, cu, block_size=64, scale=None, rows=None):
 
 
 def sparse_attn_bwd(q, k, v, idx, do, cu, block_size=64, scale=None, q_rows=None, kv_rows=None, want_dq=True,
-                    want_dkv=True):
+                    want_dkv=True, o=None):
     """Backward of S5 for upstream gradient do [tokens, h, d] (same dtype as q).
     Returns (dq [q_rows, h, d], dk [kv_rows, hkv, d], dv [kv_rows, hkv, d]) in fp64; a
-    part not wanted is None.  q_rows / kv_rows select token rows (all when None)."""
+    part not wanted is None.  q_rows / kv_rows select token rows (all when None).
+    o (optional, like q): the stored forward output; D = dO . o is then taken from it
+    instead of the exact sum over the row's keys."""
     q, k, v, do, idx, cu = (np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v),
                             np.ascontiguousarray(do), _i32(idx), _i32(cu))
     if do.dtype != q.dtype or do.shape != q.shape:
         raise ValueError("do must match q in dtype and shape")
+    if o is not None:
+        o = np.ascontiguousarray(o)
+        if o.dtype != q.dtype or o.shape != q.shape:
+            raise ValueError("o must match q in dtype and shape")
     tot, h, d = q.shape
     hkv = k.shape[1]
     S = idx.shape[-1]
@@ -193,7 +199,7 @@ def sparse_attn_bwd(q, k, v, idx, do, cu, block_size=64, scale=None, q_rows=None
     dq = np.zeros((max(nq, 0), h, d), np.float64)
     dk = np.zeros((max(nkv, 0), hkv, d), np.float64)
     dv = np.zeros((max(nkv, 0), hkv, d), np.float64)
-    _check(_load().nsa_oracle_sparse_attn_bwd(_p(q), _p(k), _p(v), _p(do), _dt(q), _p(cu), len(cu) - 1, h, hkv,
+    _check(_load().nsa_oracle_sparse_attn_bwd(_p(q), _p(k), _p(v), _p(do), _p(o), _dt(q), _p(cu), len(cu) - 1, h, hkv,
                                               d, _p(idx), S, block_size, ctypes.c_double(scale), _p(qr),
                                               ctypes.c_int64(nq), _p(dq), _p(kr), ctypes.c_int64(nkv), _p(dk),
                                               _p(dv)), "sparse_attn_bwd")

@@ -40,6 +40,9 @@ _SIGS = {
     "nsa_select": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_int, _c_int, _c_int, _c_p, _c_p, _c_sz,
                     _c_p], _c_int),
     "nsa_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
+    "nsa_sparse_bwd_workspace_size": ([_c_p, _c_int, _c_int], _c_sz),
+    "nsa_sparse_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                        _c_sz, _c_p], _c_int),
     "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_swa_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_gate_combine": ([_c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p], _c_int),
@@ -240,6 +243,28 @@ def nsa_sparse_fwd(q, k, v, block_indices, block_size=64, scale=0.0, *, cu_seqle
     _check(load().nsa_sparse_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(block_indices), S, block_size,
                                  float(scale), _ptr(out), _ptr(lse), _stream(stream)), "nsa_sparse_fwd")
     return out.view(q.shape) if q.dim() == 4 else out
+
+
+def nsa_sparse_bwd_workspace_size(shape: NsaShape, S: int, block_size: int = 64) -> int:
+    return int(load().nsa_sparse_bwd_workspace_size(ctypes.byref(shape), S, block_size))
+
+
+def nsa_sparse_bwd(q, k, v, block_indices, o, lse, d_o, block_size=64, scale=0.0, *, cu_seqlens=None,
+                   max_seqlen=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Backward of S5: returns (dq, dk, dv) shaped like q, k, v.  o and lse come from
+    nsa_sparse_fwd on the same inputs; d_o is the upstream gradient (like q)."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    S = block_indices.shape[-1]
+    if workspace is None:
+        ws = nsa_sparse_bwd_workspace_size(shp, S, block_size)
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(load().nsa_sparse_bwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(block_indices), S, block_size,
+                                 float(scale), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)), "nsa_sparse_bwd")
+    return dq, dk, dv
 
 
 def nsa_cmp_attn_fwd(q, k_cmp, v_cmp, h_kv, kernel=32, stride=16, scale=0.0, *, cu_seqlens=None,

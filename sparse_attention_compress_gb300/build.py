@@ -17,8 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnsa.so")
-SOURCES = ["api.cu", "compress.cu", "select.cu", "sparse_fwd.cu", "dense_attn.cu", "dense_tc.cu", "decode.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "compress.cu", "select.cu", "sparse_fwd.cu", "sparse_bwd.cu", "dense_attn.cu", "dense_tc.cu",
+           "decode.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -158,6 +158,52 @@ nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, in
                      "nsa_topk_select");
 }
 
+static nsa_status check_sparse_bwd(const nsa_shape* shape, int S, int block_size, Seqs* s, const char* fn) {
+  if (nsa_status st = make_seqs(shape, s, fn)) return st;
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);
+  NSA_REQUIRE(shape->d == 128, NSA_ERR_UNSUPPORTED, "%s: d must be 128", fn);
+  NSA_REQUIRE(block_size == 64, NSA_ERR_UNSUPPORTED, "%s: block_size must be 64", fn);
+  NSA_REQUIRE(S >= 1 && S <= 64, NSA_ERR_UNSUPPORTED, "%s: S must be in [1, 64]", fn);
+  NSA_REQUIRE(shape->h / shape->h_kv <= 16, NSA_ERR_UNSUPPORTED, "%s: h/h_kv must be <= 16", fn);
+  NSA_REQUIRE(s->max_len <= (1 << 24), NSA_ERR_UNSUPPORTED, "%s: sequences must be <= 2^24 tokens", fn);
+  return NSA_OK;
+}
+
+size_t nsa_sparse_bwd_workspace_size(const nsa_shape* shape, int S, int block_size) {
+  Seqs s;
+  if (check_sparse_bwd(shape, S, block_size, &s, "nsa_sparse_bwd_workspace_size") != NSA_OK) return 0;
+  return sparse_bwd_workspace_bytes(s, shape->h, shape->h_kv);
+}
+
+nsa_status nsa_sparse_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                          const int32_t* block_indices, int S, int block_size, float scale, const void* o,
+                          const float* lse, const void* d_o, void* dq, void* dk, void* dv, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = check_sparse_bwd(shape, S, block_size, &s, __func__)) return st;
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(block_indices);
+  NSA_PTR(o);
+  NSA_PTR(d_o);
+  NSA_PTR(dq);
+  NSA_PTR(dk);
+  NSA_PTR(dv);
+  NSA_REQUIRE(lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) == 0, NSA_ERR_INVALID,
+              "nsa_sparse_bwd: lse must be non-null and 4-byte aligned");
+  const size_t need = sparse_bwd_workspace_bytes(s, shape->h, shape->h_kv);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_sparse_bwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_sparse_bwd: workspace %zu < %zu bytes",
+              workspace_bytes, need);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_sparse_bwd(s, q, k, v, block_indices, S, shape->h, shape->h_kv, scale, o, lse, d_o, dq,
+                                       dk, dv, workspace, stream),
+                     "nsa_sparse_bwd");
+}
+
 size_t nsa_block_sparse_workspace_size(const nsa_shape* shape) {
   Seqs s;
   if (make_seqs(shape, &s, __func__) != NSA_OK) return 0;

@@ -29,6 +29,13 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
                               const int32_t* idx, int S, int block_size, int h, int hkv, int d,
                               int dtype, float scale, void* o, float* lse, cudaStream_t st);
 
+// Backward of selected attention (bf16, d 128, block 64, h/hkv <= 16): dq [tokens,h,d],
+// dk/dv [tokens,hkv,d] from q, k, v, the block lists, the forward's o and lse and dO.
+size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv);
+cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const void* v, const int32_t* idx, int S,
+                              int h, int hkv, float scale, const void* o, const float* lse, const void* dout,
+                              void* dq, void* dk, void* dv, void* workspace, cudaStream_t st);
+
 // mode 0: compressed-attention branch (keys/values are packed compressed rows)
 // mode 1: sliding-window branch
 cudaError_t launch_dense_attn(int mode, const Seqs& s, const void* q, const void* k, const void* v,

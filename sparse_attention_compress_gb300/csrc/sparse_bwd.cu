@@ -1,0 +1,540 @@
+// Backward of selected-block attention (prefill): dQ, dK, dV for an upstream dO.
+//
+// The forward is [TileLang-NSA] "TileLang operator development: Native Sparse
+// Attention", sec. 2 (a listed block starting at index*block_size is attended when it
+// starts at or before the query; keys past the query are masked); the pages train with
+// it ([NSA-Triton] "DeepSeek NSA ... with Triton", sec. 4) but print no backward, so
+// this is the derivative of that forward.  Per (token, head) row with list keys e:
+//   p_e = exp(scale q.k_e - lse),  dp_e = dO.v_e,  D = dO.o,  ds_e = p_e (dp_e - D),
+//   dq = scale sum_e ds_e k_e,  dk[e] += scale ds_e q,  dv[e] += p_e dO.
+//
+// GB300 design, three launches:
+//   1. sparse_bwd_dq: one CTA per (token, kv-head), the forward's structure (four warps
+//      own the four 16-key slices of every listed block and stream them through private
+//      cp.async rings), recomputing p from the forward's lse (no online softmax), with a
+//      second product dO.V^T and dq accumulated in registers; it also stores D = dO.o.
+//   2. sparse_bwd_dkv: the transpose problem.  A work item is (sequence, kv-head, key
+//      block j, chunk of 2048 query positions); its CTA finds, in token order, the
+//      tokens of the chunk whose list holds j (with multiplicity), keeps K_j and V_j in
+//      shared memory and streams those tokens' Q and dO rows (all r heads of the group:
+//      the M = 16 of one mma tile) through a CTA-wide cp.async ring.  Warp w owns keys
+//      16w..16w+15 of the block and accumulates their dK and dV rows in registers; the
+//      P^T and dS^T operands come from register transposes (movmatrix).  Each item
+//      writes fp32 partials.
+//   3. sparse_bwd_reduce: per (sequence, kv-head, block) the partials are summed in
+//      chunk order (deterministic: no floating-point atomics anywhere) and stored.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace nsa {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBS = 64;
+constexpr int kChunk = 2048;              // query positions per dK/dV work item
+constexpr int kGroup = kChunk / kBS;      // key blocks that share a first chunk
+constexpr int kTileBytes = kBS * kD * 2;  // one 64 x 128 bf16 block
+constexpr int kRowsBytes = 16 * kD * 2;   // 16 rows x 128 bf16
+
+struct BwdParams {
+  const __nv_bfloat16 *q, *k, *v, *o, *dout;
+  const float* lse;
+  const int32_t* idx;
+  __nv_bfloat16 *dq, *dk, *dv;
+  float* dsum;  // [tokens, h]: D = dO . o
+  float* part;  // [n_seqs * hkv][items_per_bg][2][64][128] fp32 partial dK (unscaled), dV
+  Seqs seqs;
+  int h, hkv, S, r;
+  float scale, scale_log2;
+  int n_chunks, nb, items_per_bg;
+};
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float dot_bf16x2(uint32_t a, uint32_t b) {
+  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+  const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
+  return x.x * y.x + x.y * y.y;
+}
+
+// P and dS enter the dV, dQ and dK products as bf16.  Where a warp's 16 x 16 tile holds
+// a |value| above kSplitAbove (rows with few keys, where p is large and a bf16 rounding
+// of it is not small beside the gradient), the bf16 remainder x - bf16(x) goes through a
+// second product, so the operand is carried to about 16 bits.
+constexpr float kSplitAbove = 0.0625f;
+
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(a, b);
+  const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+  lo = pack_bf16(a - h.x, b - h.y);
+}
+
+// base-2 log-sum-exp of a row from the forward's natural-log lse; rows without keys
+// (lse = -inf) give +inf so that every exponential of that row is 0.
+__device__ __forceinline__ float lse_to_log2(float l) { return l == kNegInf ? __builtin_inff() : l * kLog2e; }
+
+// 4-byte global->shared copy (zero-fill when src_bytes == 0).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Item index (within one sequence / kv-head) -> (key block j, chunk c).  Blocks
+// j = m*kGroup .. m*kGroup+kGroup-1 have their first query chunk at m and one item for
+// each chunk m .. n_chunks-1.
+__device__ __forceinline__ void item_to_block(int item, int n_chunks, int nb, int& j, int& c, int& m) {
+  int rem = item;
+  for (m = 0; m < n_chunks; ++m) {
+    const int blocks = min(kGroup, nb - m * kGroup);
+    const int per = n_chunks - m;
+    if (rem < blocks * per) {
+      j = m * kGroup + rem / per;
+      c = m + rem % per;
+      return;
+    }
+    rem -= blocks * per;
+  }
+  j = nb;  // not reached for item < items_per_bg
+  c = n_chunks;
+}
+
+// ---------------------------------------------------------------------------- dQ
+template <int NSTAGE>
+__global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
+  constexpr int D = kD, BS = kBS;
+  constexpr int SLICE_BYTES = 16 * D * 2;
+  constexpr int STAGE_BYTES = 2 * SLICE_BYTES;
+  constexpr int CH = D / 8;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_list[4][64];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slice = warp;
+  const int g = blockIdx.y;
+  const int r = p.r;
+  const int64_t qrow = blockIdx.x;
+  const int sq = seq_of_token(p.seqs, qrow);
+  const int64_t kv_base = seq_start(p.seqs, sq);
+  const int t = (int)(qrow - kv_base);
+  const int hbase = g * r;
+  const int rlo = lane >> 2, rhi = rlo + 8;
+  const bool w0 = rlo < r, w1 = rhi < r;
+  const int64_t row0 = qrow * p.h + hbase;
+
+  uint32_t qa[D / 16][4], da[D / 16][4];
+  load_a_frags<D>(qa, w0 ? p.q + (row0 + rlo) * D : nullptr, w1 ? p.q + (row0 + rhi) * D : nullptr, lane);
+  load_a_frags<D>(da, w0 ? p.dout + (row0 + rlo) * D : nullptr, w1 ? p.dout + (row0 + rhi) * D : nullptr, lane);
+  float d0 = 0.f, d1 = 0.f;
+  {
+    uint32_t oa[D / 16][4];
+    load_a_frags<D>(oa, w0 ? p.o + (row0 + rlo) * D : nullptr, w1 ? p.o + (row0 + rhi) * D : nullptr, lane);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      d0 += dot_bf16x2(da[kk][0], oa[kk][0]) + dot_bf16x2(da[kk][2], oa[kk][2]);
+      d1 += dot_bf16x2(da[kk][1], oa[kk][1]) + dot_bf16x2(da[kk][3], oa[kk][3]);
+    }
+    d0 = quad_sum(d0);
+    d1 = quad_sum(d1);
+  }
+  const float L0 = w0 ? lse_to_log2(p.lse[row0 + rlo]) : __builtin_inff();
+  const float L1 = w1 ? lse_to_log2(p.lse[row0 + rhi]) : __builtin_inff();
+  if (warp == 0 && (lane & 3) == 0) {
+    if (w0) p.dsum[row0 + rlo] = d0;
+    if (w1) p.dsum[row0 + rhi] = d1;
+  }
+
+  // this warp's list: listed blocks whose slice starts at or before t
+  const int32_t* il = p.idx + (qrow * p.hkv + g) * p.S;
+  int cnt = 0;
+  for (int base = 0; base < p.S; base += 32) {
+    const int e = base + lane;
+    int blk = -1;
+    bool ok = false;
+    if (e < p.S) {
+      blk = il[e];
+      ok = blk >= 0 && (int64_t)blk * BS + slice * 16 <= t;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    if (ok) s_list[warp][cnt + __popc(m & ((1u << lane) - 1u))] = blk;
+    cnt += __popc(m);
+  }
+  __syncwarp();
+
+  const __nv_bfloat16* kb = p.k + (kv_base * p.hkv + g) * D;
+  const __nv_bfloat16* vb = p.v + (kv_base * p.hkv + g) * D;
+  const int64_t rs = (int64_t)p.hkv * D;
+  const uint32_t wbase = smem_u32(smem) + warp * NSTAGE * STAGE_BYTES;
+  const int* list = s_list[warp];
+  auto issue = [&](int i) {
+    const int64_t key0 = (int64_t)list[i] * BS + slice * 16;
+    const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
+    const bool full = key0 + 15 <= t;
+#pragma unroll
+    for (int c = lane; c < 16 * CH; c += 32) {
+      const int row = c / CH, ch = c % CH;
+      const bool ok = full || key0 + row <= t;
+      const int64_t off = (key0 + row) * rs + ch * 8;
+      cp_async16(tile_addr<D>(sb, row, ch), ok ? kb + off : (const void*)p.k, ok ? 16 : 0);
+      cp_async16(tile_addr<D>(sb + SLICE_BYTES, row, ch), ok ? vb + off : (const void*)p.k, ok ? 16 : 0);
+    }
+  };
+
+  float acc[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NSTAGE - 1; ++i) {
+    if (i < cnt) issue(i);
+    cp_async_commit();
+  }
+  for (int i = 0; i < cnt; ++i) {
+    if (i + NSTAGE - 1 < cnt) issue(i + NSTAGE - 1);
+    cp_async_commit();
+    cp_async_wait<NSTAGE - 1>();
+    __syncwarp();
+    const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
+    float s[2][4] = {}, s2[2][4] = {}, dp[2][4] = {}, dp2[2][4] = {};
+    qk_16keys_2acc<D>(s, s2, qa, sb, 0, lane);
+    qk_16keys_2acc<D>(dp, dp2, da, sb + SLICE_BYTES, 0, lane);
+    const int64_t key0 = (int64_t)list[i] * BS + slice * 16;
+    float ds[2][4], big = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t key = key0 + nt * 8 + (lane & 3) * 2 + (j & 1);
+        const float pe = key <= t ? ex2((s[nt][j] + s2[nt][j]) * p.scale_log2 - (j < 2 ? L0 : L1)) : 0.f;
+        ds[nt][j] = pe * ((dp[nt][j] + dp2[nt][j]) - (j < 2 ? d0 : d1));
+        big = fmaxf(big, fabsf(ds[nt][j]));
+      }
+    uint32_t dsa[4], dsl[4];
+    split_bf16x2(ds[0][0], ds[0][1], dsa[0], dsl[0]);
+    split_bf16x2(ds[0][2], ds[0][3], dsa[1], dsl[1]);
+    split_bf16x2(ds[1][0], ds[1][1], dsa[2], dsl[2]);
+    split_bf16x2(ds[1][2], ds[1][3], dsa[3], dsl[3]);
+    pv_16keys<D>(acc, dsa, sb, 0, lane);  // dq += dS . K
+    if (__any_sync(0xffffffffu, big > kSplitAbove)) pv_16keys<D>(acc, dsl, sb, 0, lane);
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // every ring is drained: the fold below reuses the shared memory
+
+  constexpr int OS = D + 8;
+  float* sm = reinterpret_cast<float*>(smem);  // [3][16][OS]
+  if (warp > 0) {
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<float2*>(&sm[((warp - 1) * 16 + rlo) * OS + col]) = make_float2(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<float2*>(&sm[((warp - 1) * 16 + rhi) * OS + col]) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) {
+    const int col = nt * 8 + (lane & 3) * 2;
+    float a0 = acc[nt][0], a1 = acc[nt][1], a2 = acc[nt][2], a3 = acc[nt][3];
+#pragma unroll
+    for (int w = 0; w < 3; ++w) {
+      const float2 x = *reinterpret_cast<const float2*>(&sm[(w * 16 + rlo) * OS + col]);
+      const float2 y = *reinterpret_cast<const float2*>(&sm[(w * 16 + rhi) * OS + col]);
+      a0 += x.x;
+      a1 += x.y;
+      a2 += y.x;
+      a3 += y.y;
+    }
+    if (w0) *reinterpret_cast<uint32_t*>(p.dq + (row0 + rlo) * D + col) = pack_bf16(a0 * p.scale, a1 * p.scale);
+    if (w1) *reinterpret_cast<uint32_t*>(p.dq + (row0 + rhi) * D + col) = pack_bf16(a2 * p.scale, a3 * p.scale);
+  }
+}
+
+// ---------------------------------------------------------------------------- dK, dV
+// Shared memory of sparse_bwd_dkv: K_j and V_j tiles, the token ring (Q rows, dO rows,
+// log2-lse and D of 16 head rows per stage) and the item's token list.
+template <int NSTAGE>
+constexpr int dkv_smem_bytes() {
+  return 2 * kTileBytes + NSTAGE * (2 * kRowsBytes + 2 * 16 * 4) + kChunk * 4;
+}
+
+template <int NSTAGE>
+__global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
+  constexpr int D = kD, BS = kBS, CH = D / 8;
+  constexpr int STAGE = 2 * kRowsBytes + 2 * 16 * 4;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_wcount[4];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_bg = p.seqs.n_seqs * p.hkv;
+  const int bg = blockIdx.x % n_bg;
+  const int item = blockIdx.x / n_bg;
+  const int b = bg / p.hkv, g = bg % p.hkv;
+  int j, c, m;
+  item_to_block(item, p.n_chunks, p.nb, j, c, m);
+  const int L = seq_len(p.seqs, b);
+  if (j * BS >= L || (c > m && c * kChunk >= L)) return;  // no partial is read for this item
+  const int64_t base = seq_start(p.seqs, b);
+  const int t_begin = max(j * BS, c * kChunk), t_end = min((c + 1) * kChunk, L);
+
+  const uint32_t kt = smem_u32(smem), vt = kt + kTileBytes;
+  const uint32_t ring = vt + kTileBytes;
+  int* s_tok = reinterpret_cast<int*>(smem + 2 * kTileBytes + NSTAGE * STAGE);
+
+  // K_j and V_j (rows past the sequence read as zeros; no query reaches them)
+  {
+    const int64_t rs = (int64_t)p.hkv * D;
+    const __nv_bfloat16* kb = p.k + ((base + (int64_t)j * BS) * p.hkv + g) * D;
+    const __nv_bfloat16* vb = p.v + ((base + (int64_t)j * BS) * p.hkv + g) * D;
+    for (int i = threadIdx.x; i < BS * CH; i += 128) {
+      const int row = i / CH, ch = i % CH;
+      const bool ok = j * BS + row < L;
+      cp_async16(tile_addr<D>(kt, row, ch), ok ? kb + row * rs + ch * 8 : (const void*)p.k, ok ? 16 : 0);
+      cp_async16(tile_addr<D>(vt, row, ch), ok ? vb + row * rs + ch * 8 : (const void*)p.k, ok ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+
+  // tokens of the chunk whose list holds j, in token order, with multiplicity
+  int n = 0;
+  for (int t0 = t_begin; t0 < t_end; t0 += 128) {
+    const int t = t0 + threadIdx.x;
+    int mult = 0;
+    if (t < t_end) {
+      const int32_t* il = p.idx + ((base + t) * p.hkv + g) * p.S;
+      for (int e = 0; e < p.S; ++e) mult += il[e] == j;
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, mult > 0);
+    if (lane == 0) s_wcount[warp] = __popc(bal);
+    __syncthreads();
+    int off = n;
+    for (int w = 0; w < warp; ++w) off += s_wcount[w];
+    if (mult > 0) s_tok[off + __popc(bal & ((1u << lane) - 1u))] = (t << 7) | mult;
+    n += s_wcount[0] + s_wcount[1] + s_wcount[2] + s_wcount[3];
+    __syncthreads();
+  }
+
+  const int r = p.r;
+  const int hbase = g * r;
+  auto issue = [&](int i) {
+    const int t = s_tok[i] >> 7;
+    const int64_t row0 = (base + t) * p.h + hbase;
+    const uint32_t sb = ring + (i % NSTAGE) * STAGE;
+#pragma unroll
+    for (int e = threadIdx.x; e < 2 * 16 * CH; e += 128) {
+      const int which = e / (16 * CH), rr = (e / CH) % 16, ch = e % CH;
+      const bool ok = rr < r;
+      const __nv_bfloat16* src = (which ? p.dout : p.q) + (row0 + rr) * D + ch * 8;
+      cp_async16(tile_addr<D>(sb + which * kRowsBytes, rr, ch), ok ? (const void*)src : (const void*)p.q,
+                 ok ? 16 : 0);
+    }
+    if (threadIdx.x < 32) {
+      const int rr = threadIdx.x & 15;
+      const bool ok = rr < r;
+      const float* src = (threadIdx.x < 16 ? p.lse : p.dsum) + row0 + rr;
+      cp_async4(sb + 2 * kRowsBytes + threadIdx.x * 4, ok ? (const void*)src : (const void*)p.lse, ok ? 4 : 0);
+    }
+  };
+
+  float dk[D / 8][4], dv[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) {
+    dk[i][0] = dk[i][1] = dk[i][2] = dk[i][3] = 0.f;
+    dv[i][0] = dv[i][1] = dv[i][2] = dv[i][3] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < NSTAGE - 1; ++i) {
+    if (i < n) issue(i);
+    cp_async_commit();
+  }
+  const int rlo = lane >> 2, rhi = rlo + 8;
+  const int arow = (lane & 7) + (((lane >> 3) & 1) << 3), acol = lane >> 4;
+  const int brow = warp * 16 + (lane & 7) + ((lane >> 4) << 3), bcol = (lane >> 3) & 1;
+  for (int i = 0; i < n; ++i) {
+    if (i + NSTAGE - 1 < n) issue(i + NSTAGE - 1);
+    cp_async_commit();
+    cp_async_wait<NSTAGE - 1>();
+    __syncthreads();
+    const int t = s_tok[i] >> 7;
+    const float mult = (float)(s_tok[i] & 127);
+    const uint32_t qt = ring + (i % NSTAGE) * STAGE, dt = qt + kRowsBytes;
+    const float* lrow = reinterpret_cast<const float*>(smem + 2 * kTileBytes + (i % NSTAGE) * STAGE + 2 * kRowsBytes);
+    const float* drow = lrow + 16;
+    // S = Q_t K_w^T and dP = dO_t V_w^T (16 heads x 16 keys)
+    float s[2][4] = {}, dp[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4], bk[4], a2[4], bv[4];
+      ldsm_x4(a, tile_addr<D>(qt, arow, 2 * kk + acol));
+      ldsm_x4(bk, tile_addr<D>(kt, brow, 2 * kk + bcol));
+      ldsm_x4(a2, tile_addr<D>(dt, arow, 2 * kk + acol));
+      ldsm_x4(bv, tile_addr<D>(vt, brow, 2 * kk + bcol));
+      mma_bf16(s[0], a, bk[0], bk[1]);
+      mma_bf16(s[1], a, bk[2], bk[3]);
+      mma_bf16(dp[0], a2, bv[0], bv[1]);
+      mma_bf16(dp[1], a2, bv[2], bv[3]);
+    }
+    const float l0 = lse_to_log2(lrow[rlo]), l1 = lse_to_log2(lrow[rhi]), e0 = drow[rlo], e1 = drow[rhi];
+    float pr[2][4], ds[2][4], big = 0.f, pbig = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int key = j * BS + warp * 16 + nt * 8 + (lane & 3) * 2 + (q & 1);
+        const float pe = key <= t ? ex2(s[nt][q] * p.scale_log2 - (q < 2 ? l0 : l1)) : 0.f;
+        pr[nt][q] = pe * mult;
+        ds[nt][q] = pe * mult * (dp[nt][q] - (q < 2 ? e0 : e1));
+        big = fmaxf(big, fabsf(ds[nt][q]));
+        pbig = fmaxf(pbig, pr[nt][q]);
+      }
+    // A operands of P^T and dS^T (rows = keys, k = heads): transpose the 8x8 quarters
+    uint32_t ph[4], pl[4], sh[4], sl[4];
+    split_bf16x2(pr[0][0], pr[0][1], ph[0], pl[0]);
+    split_bf16x2(pr[1][0], pr[1][1], ph[1], pl[1]);
+    split_bf16x2(pr[0][2], pr[0][3], ph[2], pl[2]);
+    split_bf16x2(pr[1][2], pr[1][3], ph[3], pl[3]);
+    const uint32_t pt[4] = {movmatrix_t(ph[0]), movmatrix_t(ph[1]), movmatrix_t(ph[2]), movmatrix_t(ph[3])};
+    split_bf16x2(ds[0][0], ds[0][1], sh[0], sl[0]);
+    split_bf16x2(ds[1][0], ds[1][1], sh[1], sl[1]);
+    split_bf16x2(ds[0][2], ds[0][3], sh[2], sl[2]);
+    split_bf16x2(ds[1][2], ds[1][3], sh[3], sl[3]);
+    const uint32_t st[4] = {movmatrix_t(sh[0]), movmatrix_t(sh[1]), movmatrix_t(sh[2]), movmatrix_t(sh[3])};
+    pv_16keys<D>(dv, pt, dt, 0, lane);  // dV_w += P^T . dO_t
+    pv_16keys<D>(dk, st, qt, 0, lane);  // dK_w += dS^T . Q_t
+    if (__any_sync(0xffffffffu, pbig > kSplitAbove)) {
+      const uint32_t ptl[4] = {movmatrix_t(pl[0]), movmatrix_t(pl[1]), movmatrix_t(pl[2]), movmatrix_t(pl[3])};
+      pv_16keys<D>(dv, ptl, dt, 0, lane);
+    }
+    if (__any_sync(0xffffffffu, big > kSplitAbove)) {
+      const uint32_t stl[4] = {movmatrix_t(sl[0]), movmatrix_t(sl[1]), movmatrix_t(sl[2]), movmatrix_t(sl[3])};
+      pv_16keys<D>(dk, stl, qt, 0, lane);
+    }
+    __syncthreads();  // the stage is refilled at the next iteration
+  }
+  cp_async_wait<0>();
+
+  float* out = p.part + ((size_t)bg * p.items_per_bg + item) * 2 * BS * D;
+  const int k0 = warp * 16 + rlo, k1 = k0 + 8;
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) {
+    const int col = nt * 8 + (lane & 3) * 2;
+    *reinterpret_cast<float2*>(out + k0 * D + col) = make_float2(dk[nt][0], dk[nt][1]);
+    *reinterpret_cast<float2*>(out + k1 * D + col) = make_float2(dk[nt][2], dk[nt][3]);
+    *reinterpret_cast<float2*>(out + BS * D + k0 * D + col) = make_float2(dv[nt][0], dv[nt][1]);
+    *reinterpret_cast<float2*>(out + BS * D + k1 * D + col) = make_float2(dv[nt][2], dv[nt][3]);
+  }
+}
+
+// Sum of the partials of one (sequence, kv-head, key block) in chunk order.
+__global__ void __launch_bounds__(256) sparse_bwd_reduce(const BwdParams p) {
+  constexpr int D = kD, BS = kBS;
+  const int bg = blockIdx.x / p.nb, j = blockIdx.x % p.nb;
+  const int b = bg / p.hkv, g = bg % p.hkv;
+  const int L = seq_len(p.seqs, b);
+  if (j * BS >= L) return;
+  const int m = j / kGroup;
+  int first = 0;
+  for (int mm = 0; mm < m; ++mm) first += min(kGroup, p.nb - mm * kGroup) * (p.n_chunks - mm);
+  first += (j - m * kGroup) * (p.n_chunks - m);
+  int n_items = 1;
+  while (m + n_items < p.n_chunks && (m + n_items) * kChunk < L) ++n_items;
+  const float4* src = reinterpret_cast<const float4*>(p.part + ((size_t)bg * p.items_per_bg + first) * 2 * BS * D);
+  constexpr int N4 = 2 * BS * D / 4;
+  const int64_t base = seq_start(p.seqs, b);
+  for (int e = threadIdx.x; e < N4; e += 256) {
+    float4 a = src[e];
+    for (int it = 1; it < n_items; ++it) {
+      const float4 x = src[(size_t)it * N4 + e];
+      a.x += x.x;
+      a.y += x.y;
+      a.z += x.z;
+      a.w += x.w;
+    }
+    const int which = e / (BS * D / 4), key = (e / (D / 4)) % BS, col = (e % (D / 4)) * 4;
+    if (j * BS + key >= L) continue;
+    const float f = which ? 1.f : p.scale;
+    __nv_bfloat16* dst = (which ? p.dv : p.dk) + ((base + (int64_t)j * BS + key) * p.hkv + g) * D + col;
+    uint2 w;
+    w.x = pack_bf16(a.x * f, a.y * f);
+    w.y = pack_bf16(a.z * f, a.w * f);
+    *reinterpret_cast<uint2*>(dst) = w;
+  }
+}
+
+struct BwdLayout {
+  int n_chunks, nb, items_per_bg;
+  size_t dsum, part, total;
+};
+
+BwdLayout bwd_layout(const Seqs& s, int h, int hkv) {
+  BwdLayout l{};
+  const int Lmax = s.max_len;
+  l.n_chunks = (Lmax + kChunk - 1) / kChunk;
+  l.nb = (Lmax + kBS - 1) / kBS;
+  for (int m = 0; m < l.n_chunks; ++m) l.items_per_bg += std::min(kGroup, l.nb - m * kGroup) * (l.n_chunks - m);
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  l.dsum = 0;
+  l.part = a256((size_t)s.tokens * h * 4);
+  l.total = a256(l.part + (size_t)s.n_seqs * hkv * l.items_per_bg * 2 * kBS * kD * 4);
+  return l;
+}
+
+}  // namespace
+
+size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv) {
+  if (s.tokens == 0 || s.max_len == 0) return 0;
+  return bwd_layout(s, h, hkv).total;
+}
+
+cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const void* v, const int32_t* idx, int S,
+                              int h, int hkv, float scale, const void* o, const float* lse, const void* dout,
+                              void* dq, void* dk, void* dv, void* workspace, cudaStream_t st) {
+  if (s.tokens == 0) return cudaSuccess;
+  const BwdLayout l = bwd_layout(s, h, hkv);
+  BwdParams p{};
+  p.q = (const __nv_bfloat16*)q;
+  p.k = (const __nv_bfloat16*)k;
+  p.v = (const __nv_bfloat16*)v;
+  p.o = (const __nv_bfloat16*)o;
+  p.dout = (const __nv_bfloat16*)dout;
+  p.lse = lse;
+  p.idx = idx;
+  p.dq = (__nv_bfloat16*)dq;
+  p.dk = (__nv_bfloat16*)dk;
+  p.dv = (__nv_bfloat16*)dv;
+  p.dsum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.dsum);
+  p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.part);
+  p.seqs = s;
+  p.h = h;
+  p.hkv = hkv;
+  p.S = S;
+  p.r = h / hkv;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.n_chunks = l.n_chunks;
+  p.nb = l.nb;
+  p.items_per_bg = l.items_per_bg;
+
+  constexpr int NS_Q = 2, NS_KV = 3;
+  constexpr int dq_bytes = 4 * NS_Q * 2 * 16 * kD * 2;
+  static_assert(dq_bytes >= 3 * 16 * (kD + 8) * 4, "dq fold needs the ring's shared memory");
+  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_dq<NS_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_bytes);
+  if (e != cudaSuccess) return e;
+  sparse_bwd_dq<NS_Q><<<dim3((unsigned)s.tokens, hkv), 128, dq_bytes, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  constexpr int kv_bytes = dkv_smem_bytes<NS_KV>();
+  e = cudaFuncSetAttribute(sparse_bwd_dkv<NS_KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
+  if (e != cudaSuccess) return e;
+  const int64_t items = (int64_t)s.n_seqs * hkv * l.items_per_bg;
+  sparse_bwd_dkv<NS_KV><<<(unsigned)items, 128, kv_bytes, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  sparse_bwd_reduce<<<(unsigned)((int64_t)s.n_seqs * hkv * l.nb), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace nsa

@@ -103,3 +103,36 @@ def test_layer_workspace_size_scales_with_tokens():
     s2 = _lib.make_shape(32768, 64, 4, 128, _lib.NSA_BF16, batch=1, seqlen=32768)
     a, b = nsa.nsa_layer_fwd_workspace_size(s1), nsa.nsa_layer_fwd_workspace_size(s2)
     assert a > 1.9 * b > 0
+
+
+def _items_per_seq_head(T, chunk=2048, block=64):
+    """Brute-force count of dK/dV work items: one per (key block j, query chunk c) with
+    the chunk reaching at or past the block's first key."""
+    nb, nch = -(-T // block), -(-T // chunk)
+    return sum(1 for j in range(nb) for c in range(nch) if (c + 1) * chunk > j * block)
+
+
+@pytest.mark.parametrize("B,T,h,hkv", [(8, 16384, 16, 1), (2, 4500, 8, 2), (1, 64, 16, 16), (3, 1, 4, 1)])
+def test_sparse_bwd_workspace_size(B, T, h, hkv):
+    s = _shape(batch=B, seqlen=T, h=h, h_kv=hkv)
+    got = nsa.nsa_sparse_bwd_workspace_size(s, 16)
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    dsum = a256(B * T * h * 4)
+    want = a256(dsum + B * hkv * _items_per_seq_head(T) * 2 * 64 * 128 * 4)
+    assert got == want
+
+
+def test_sparse_bwd_rejects_unsupported():
+    lib = nsa.load()
+    args = lambda s, S=16, bs=64, lse=FAKE, ws=FAKE, wsb=1 << 40: (  # noqa: E731
+        ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, S, bs, 0.0, FAKE, lse, FAKE, FAKE, FAKE, FAKE, ws, wsb, None)
+    assert lib.nsa_sparse_bwd(*args(_shape(d=64))) == 2
+    assert lib.nsa_sparse_bwd(*args(_shape(dtype=_lib.NSA_F32))) == 2
+    assert lib.nsa_sparse_bwd(*args(_shape(), bs=32)) == 2
+    assert lib.nsa_sparse_bwd(*args(_shape(), S=65)) == 2
+    assert lib.nsa_sparse_bwd(*args(_shape(h=32, h_kv=1))) == 2
+    assert lib.nsa_sparse_bwd(*args(_shape(), lse=None)) == 1
+    assert lib.nsa_sparse_bwd(*args(_shape(), ws=MIS)) == 1
+    assert lib.nsa_sparse_bwd(*args(_shape(), wsb=16)) == 1
+    assert b"workspace" in lib.nsa_last_error()
+    assert lib.nsa_sparse_bwd(*args(_shape(batch=0))) == 0

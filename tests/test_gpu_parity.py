@@ -190,6 +190,98 @@ def test_sparse_fwd_prefill_full_size_sampled():
     assert_close(g, ref, what="prefill sampled")
 
 
+# --------------------------------------------------------------------------- S5 backward
+# The backward takes the forward's stored output o (bf16) and lse; D = dO . o comes from
+# that o.  Both sides get the oracle's own forward (o rounded to bf16, lse in fp32), so
+# the comparison covers the backward alone.
+def _oracle_fwd_inputs(q, k, v, idx, cu, rows=None, bs=64):
+    o64, lse64 = orc.sparse_attn(q, k, v, idx, cu, bs, rows=rows)
+    return gen.f32_to_bf16_bits(o64.astype(np.float32)), lse64.astype(np.float32)
+
+
+def _sparse_bwd_gpu(q, k, v, idx, o, lse, do, cu, max_len, bs=64):
+    gq, gk, gv = nsa.nsa_sparse_bwd(dev(q), dev(k), dev(v), dev(idx), dev(o), dev(lse), dev(do), bs,
+                                    cu_seqlens=dev(cu), max_seqlen=max_len)
+    torch.cuda.synchronize()
+    return gq, gk, gv
+
+
+@pytest.mark.parametrize("H,hkv,S", [(16, 1, 4), (8, 2, 8), (4, 4, 3), (16, 2, 6)])
+def test_sparse_bwd_varlen(H, hkv, S):
+    """Ragged lengths: single-token sequences, block edges, and sequences spanning two and
+    three 2048-query chunks (several dK/dV partials per block)."""
+    lengths = [1, 63, 64, 65, 700, 2100, 4200]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(21)
+    q, do = gen.normal(rng, (cu[-1], H, 128), "bf16"), gen.normal(rng, (cu[-1], H, 128), "bf16")
+    k, v = gen.normal(rng, (cu[-1], hkv, 128), "bf16"), gen.normal(rng, (cu[-1], hkv, 128), "bf16")
+    idx = gen.random_block_indices(rng, cu, hkv, S, 64, force_first=True)
+    o, lse = _oracle_fwd_inputs(q, k, v, idx, cu)
+    gq, gk, gv = _sparse_bwd_gpu(q, k, v, idx, o, lse, do, cu, max(lengths))
+    assert nsa.nsa_device_status() == 0
+    rq, rk, rv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, 64, o=o)
+    assert_close(gq, rq, what="dq")
+    assert_close(gk, rk, what="dk")
+    assert_close(gv, rv, what="dv")
+
+
+def test_sparse_bwd_edge_lists_and_determinism():
+    """-1 padding, non-causal entries, duplicates (count twice) and empty lists (no
+    gradient); two runs give identical bits."""
+    T, H, hkv, bs = 300, 16, 1, 64
+    cu = gen.dense_cu_seqlens(1, T)
+    rng = _rng(22)
+    q, do = gen.normal(rng, (T, H, 128), "bf16"), gen.normal(rng, (T, H, 128), "bf16")
+    k, v = gen.normal(rng, (T, hkv, 128), "bf16"), gen.normal(rng, (T, hkv, 128), "bf16")
+    t = np.arange(T)
+    idx = np.stack([t // bs, np.full(T, -1), np.full(T, 3), np.zeros(T), np.zeros(T)], 1).astype(np.int32)
+    idx[:10] = -1
+    idx = idx[:, None, :]
+    o, lse = _oracle_fwd_inputs(q, k, v, idx, cu)
+    gq, gk, gv = _sparse_bwd_gpu(q, k, v, idx, o, lse, do, cu, T)
+    rq, rk, rv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs, o=o)
+    assert_close(gq, rq, what="dq edge")
+    assert_close(gk, rk, what="dk edge")
+    assert_close(gv, rv, what="dv edge")
+    assert np.all(as_f64(host(gq))[:10] == 0)
+    g2 = _sparse_bwd_gpu(q, k, v, idx, o, lse, do, cu, T)
+    for a, b in zip((gq, gk, gv), g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_sparse_bwd_full_size_sampled():
+    """B=8, T=16384, H=16, Hkv=1, d=128, block 64, S=16 (the benchmark launch, fed by the
+    GPU forward): dq on sampled query rows, dk and dv on sampled key rows of blocks 1, 100
+    and 255.  The oracle takes D from its own forward output on every token it visits."""
+    w = gen.prefill()
+    do = gen.normal(_rng(23), (w.tokens, 16, 128), "bf16")
+    q, k, v, di = dev(w.q), dev(w.k), dev(w.v), dev(w.idx)
+    lse = torch.empty((w.tokens, 16), dtype=torch.float32, device="cuda")
+    o = nsa.nsa_sparse_fwd(q.view(8, 16384, 16, 128), k, v, di, 64, lse=lse).view(w.tokens, 16, 128)
+    gq, gk, gv = nsa.nsa_sparse_bwd(q.view(8, 16384, 16, 128), k, v, di, o, lse, dev(do), 64)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    rng = _rng(24)
+    qr = np.unique(np.concatenate([rng.integers(0, w.tokens, 48), [0, 16383, 16384, 131071]]))
+    kr = np.array([3 * 16384 + 64, 3 * 16384 + 127, 5 * 16384 + 6400 + 17, 7 * 16384 + 16320, 7 * 16384 + 16383])
+    # tokens whose lists reach the sampled key rows (same sequence, block listed, key causal)
+    tok = np.arange(w.tokens)
+    seq, t = tok // 16384, tok % 16384
+    hit = np.zeros(w.tokens, bool)
+    for r_ in kr:
+        s_, j_ = r_ // 16384, (r_ % 16384) // 64
+        hit |= (seq == s_) & (t >= r_ % 16384) & (w.idx[:, 0, :] == j_).any(1)
+    need = np.unique(np.concatenate([qr, tok[hit]]))
+    o_ref = np.zeros((w.tokens, 16, 128), np.uint16)
+    o_ref[need] = _oracle_fwd_inputs(w.q, w.k, w.v, w.idx, w.cu_seqlens, rows=need)[0]
+    rq, _, _ = orc.sparse_attn_bwd(w.q, w.k, w.v, w.idx, do, w.cu_seqlens, 64, q_rows=qr, want_dkv=False, o=o_ref)
+    _, rk, rv = orc.sparse_attn_bwd(w.q, w.k, w.v, w.idx, do, w.cu_seqlens, 64, kv_rows=kr, want_dq=False,
+                                    o=o_ref)
+    assert_close(gq.reshape(w.tokens, 16, 128)[torch.from_numpy(qr).cuda()], rq, what="dq sampled")
+    assert_close(gk[torch.from_numpy(kr).cuda()], rk, what="dk sampled")
+    assert_close(gv[torch.from_numpy(kr).cuda()], rv, what="dv sampled")
+
+
 # --------------------------------------------------------------------------- S7, S8, S9
 @pytest.mark.parametrize("H,hkv,d", [(16, 1, 128), (32, 2, 128), (8, 1, 64), (16, 4, 128), (64, 1, 128)])
 def test_cmp_attn(H, hkv, d):

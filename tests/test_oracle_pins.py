@@ -582,3 +582,21 @@ def test_sparse_bwd_invariants_and_sampling():
     sq, sk, sv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs, q_rows=qr, kv_rows=kr)
     assert np.allclose(sq, dq[qr], atol=1e-13, rtol=0)
     assert np.allclose(sk, dk[kr], atol=1e-13, rtol=0) and np.allclose(sv, dv[kr], atol=1e-13, rtol=0)
+
+
+def test_sparse_bwd_stored_output_reading():
+    """D taken from a given forward output: with the exact output (fp32 here) it agrees
+    with the exact D = sum_e p_e dp_e; a different output changes the result."""
+    lengths = [130, 77]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, bs, S = 4, 1, 16, 32, 4
+    q, do = _rand((cu[-1], h, d), 61, "f32"), _rand((cu[-1], h, d), 62, "f32")
+    k, v = _rand((cu[-1], hkv, d), 63, "f32"), _rand((cu[-1], hkv, d), 64, "f32")
+    idx = _bwd_lists(cu, hkv, bs, S, 65, dup=False)
+    o, _ = orc.sparse_attn(q, k, v, idx, cu, bs)
+    exact = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs)
+    stored = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs, o=o.astype(np.float32))
+    for a, b in zip(exact, stored):
+        assert np.allclose(a, b, atol=1e-6, rtol=1e-5)
+    off = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs, o=np.zeros_like(q))
+    assert not np.allclose(off[0], exact[0], atol=1e-3)
