@@ -17,10 +17,12 @@
 //      block j, chunk of 2048 query positions); its CTA finds, in token order, the
 //      tokens of the chunk whose list holds j (with multiplicity), keeps K_j and V_j in
 //      shared memory and streams those tokens' Q and dO rows (all r heads of the group:
-//      the M = 16 of one mma tile) through a CTA-wide cp.async ring.  Warp w owns keys
-//      16w..16w+15 of the block and accumulates their dK and dV rows in registers; the
-//      P^T and dS^T operands come from register transposes (movmatrix).  Each item
-//      writes fp32 partials.
+//      the N = 16 of one mma tile) through a CTA-wide cp.async ring.  Warp w owns keys
+//      16w..16w+15 of the block: it holds their K and V rows as mma A fragments for
+//      the whole item, forms S^T = K_w Q_t^T and dP^T = V_w dO_t^T with the keys as the
+//      M dimension (so P^T and dS^T come out as the A operands of dV and dK with no
+//      transpose) and accumulates its dK and dV rows in registers.  Each item writes
+//      fp32 partials.
 //   3. sparse_bwd_reduce: per (sequence, kv-head, block) the partials are summed in
 //      chunk order (deterministic: no floating-point atomics anywhere) and stored.
 #include <algorithm>
@@ -51,12 +53,6 @@ struct BwdParams {
   float scale, scale_log2;
   int n_chunks, nb, items_per_bg;
 };
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
 
 __device__ __forceinline__ float dot_bf16x2(uint32_t a, uint32_t b) {
   const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
@@ -352,9 +348,23 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
     if (i < n) issue(i);
     cp_async_commit();
   }
-  const int rlo = lane >> 2, rhi = rlo + 8;
-  const int arow = (lane & 7) + (((lane >> 3) & 1) << 3), acol = lane >> 4;
-  const int brow = warp * 16 + (lane & 7) + ((lane >> 4) << 3), bcol = (lane >> 3) & 1;
+  cp_async_wait<NSTAGE - 1>();  // K_j and V_j (the oldest group) have landed
+  __syncthreads();
+  // A fragments of this warp's 16 keys of K_j and V_j, held for the whole item: the
+  // products are S^T = K_w Q_t^T and dP^T = V_w dO_t^T (16 keys x 16 heads), whose C
+  // fragments are already the A fragments of P^T and dS^T for dV and dK.
+  uint32_t ka[D / 16][4], va[D / 16][4];
+  {
+    const int arow = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), acol = lane >> 4;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      ldsm_x4(ka[kk], tile_addr<D>(kt, arow, 2 * kk + acol));
+      ldsm_x4(va[kk], tile_addr<D>(vt, arow, 2 * kk + acol));
+    }
+  }
+  const int brow = (lane & 7) + ((lane >> 4) << 3), bcol = (lane >> 3) & 1;
+  const int hc = (lane & 3) * 2;  // head columns hc, hc+1 (and hc+8, hc+9)
+  const int key_lo = j * BS + warp * 16 + (lane >> 2), key_hi = key_lo + 8;
   for (int i = 0; i < n; ++i) {
     if (i + NSTAGE - 1 < n) issue(i + NSTAGE - 1);
     cp_async_commit();
@@ -365,59 +375,48 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
     const uint32_t qt = ring + (i % NSTAGE) * STAGE, dt = qt + kRowsBytes;
     const float* lrow = reinterpret_cast<const float*>(smem + 2 * kTileBytes + (i % NSTAGE) * STAGE + 2 * kRowsBytes);
     const float* drow = lrow + 16;
-    // S = Q_t K_w^T and dP = dO_t V_w^T (16 heads x 16 keys)
-    float s[2][4] = {}, dp[2][4] = {};
+    float st[2][4] = {}, dpt[2][4] = {};
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a[4], bk[4], a2[4], bv[4];
-      ldsm_x4(a, tile_addr<D>(qt, arow, 2 * kk + acol));
-      ldsm_x4(bk, tile_addr<D>(kt, brow, 2 * kk + bcol));
-      ldsm_x4(a2, tile_addr<D>(dt, arow, 2 * kk + acol));
-      ldsm_x4(bv, tile_addr<D>(vt, brow, 2 * kk + bcol));
-      mma_bf16(s[0], a, bk[0], bk[1]);
-      mma_bf16(s[1], a, bk[2], bk[3]);
-      mma_bf16(dp[0], a2, bv[0], bv[1]);
-      mma_bf16(dp[1], a2, bv[2], bv[3]);
+      uint32_t bq[4], bd[4];
+      ldsm_x4(bq, tile_addr<D>(qt, brow, 2 * kk + bcol));
+      ldsm_x4(bd, tile_addr<D>(dt, brow, 2 * kk + bcol));
+      mma_bf16(st[0], ka[kk], bq[0], bq[1]);
+      mma_bf16(st[1], ka[kk], bq[2], bq[3]);
+      mma_bf16(dpt[0], va[kk], bd[0], bd[1]);
+      mma_bf16(dpt[1], va[kk], bd[2], bd[3]);
     }
-    const float l0 = lse_to_log2(lrow[rlo]), l1 = lse_to_log2(lrow[rhi]), e0 = drow[rlo], e1 = drow[rhi];
     float pr[2][4], ds[2][4], big = 0.f, pbig = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int key = j * BS + warp * 16 + nt * 8 + (lane & 3) * 2 + (q & 1);
-        const float pe = key <= t ? ex2(s[nt][q] * p.scale_log2 - (q < 2 ? l0 : l1)) : 0.f;
+        const int head = nt * 8 + hc + (q & 1);
+        const int key = q < 2 ? key_lo : key_hi;
+        const float pe = key <= t ? ex2(st[nt][q] * p.scale_log2 - lse_to_log2(lrow[head])) : 0.f;
         pr[nt][q] = pe * mult;
-        ds[nt][q] = pe * mult * (dp[nt][q] - (q < 2 ? e0 : e1));
+        ds[nt][q] = pe * mult * (dpt[nt][q] - drow[head]);
         big = fmaxf(big, fabsf(ds[nt][q]));
         pbig = fmaxf(pbig, pr[nt][q]);
       }
-    // A operands of P^T and dS^T (rows = keys, k = heads): transpose the 8x8 quarters
     uint32_t ph[4], pl[4], sh[4], sl[4];
     split_bf16x2(pr[0][0], pr[0][1], ph[0], pl[0]);
-    split_bf16x2(pr[1][0], pr[1][1], ph[1], pl[1]);
-    split_bf16x2(pr[0][2], pr[0][3], ph[2], pl[2]);
+    split_bf16x2(pr[0][2], pr[0][3], ph[1], pl[1]);
+    split_bf16x2(pr[1][0], pr[1][1], ph[2], pl[2]);
     split_bf16x2(pr[1][2], pr[1][3], ph[3], pl[3]);
-    const uint32_t pt[4] = {movmatrix_t(ph[0]), movmatrix_t(ph[1]), movmatrix_t(ph[2]), movmatrix_t(ph[3])};
     split_bf16x2(ds[0][0], ds[0][1], sh[0], sl[0]);
-    split_bf16x2(ds[1][0], ds[1][1], sh[1], sl[1]);
-    split_bf16x2(ds[0][2], ds[0][3], sh[2], sl[2]);
+    split_bf16x2(ds[0][2], ds[0][3], sh[1], sl[1]);
+    split_bf16x2(ds[1][0], ds[1][1], sh[2], sl[2]);
     split_bf16x2(ds[1][2], ds[1][3], sh[3], sl[3]);
-    const uint32_t st[4] = {movmatrix_t(sh[0]), movmatrix_t(sh[1]), movmatrix_t(sh[2]), movmatrix_t(sh[3])};
-    pv_16keys<D>(dv, pt, dt, 0, lane);  // dV_w += P^T . dO_t
-    pv_16keys<D>(dk, st, qt, 0, lane);  // dK_w += dS^T . Q_t
-    if (__any_sync(0xffffffffu, pbig > kSplitAbove)) {
-      const uint32_t ptl[4] = {movmatrix_t(pl[0]), movmatrix_t(pl[1]), movmatrix_t(pl[2]), movmatrix_t(pl[3])};
-      pv_16keys<D>(dv, ptl, dt, 0, lane);
-    }
-    if (__any_sync(0xffffffffu, big > kSplitAbove)) {
-      const uint32_t stl[4] = {movmatrix_t(sl[0]), movmatrix_t(sl[1]), movmatrix_t(sl[2]), movmatrix_t(sl[3])};
-      pv_16keys<D>(dk, stl, qt, 0, lane);
-    }
+    pv_16keys<D>(dv, ph, dt, 0, lane);  // dV_w += P^T . dO_t
+    pv_16keys<D>(dk, sh, qt, 0, lane);  // dK_w += dS^T . Q_t
+    if (__any_sync(0xffffffffu, pbig > kSplitAbove)) pv_16keys<D>(dv, pl, dt, 0, lane);
+    if (__any_sync(0xffffffffu, big > kSplitAbove)) pv_16keys<D>(dk, sl, qt, 0, lane);
     __syncthreads();  // the stage is refilled at the next iteration
   }
   cp_async_wait<0>();
 
+  const int rlo = lane >> 2;
   float* out = p.part + ((size_t)bg * p.items_per_bg + item) * 2 * BS * D;
   const int k0 = warp * 16 + rlo, k1 = k0 + 8;
 #pragma unroll
