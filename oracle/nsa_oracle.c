@@ -604,6 +604,156 @@ int nsa_oracle_sparse_attn_bwd(const void* q, const void* k, const void* v, cons
   return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* NOSA stage 2.  [NOSA-Parts] core component 2: a scorer gives every key position an
+ * importance score (CIS; here an input, since the scorer is learned); [NOSA-Triton]
+ * mechanisms 1-3: the scores are mean-pooled over windows of `kernel` positions at step
+ * `stride`, aligned with the key compressor; [NOSA-Parts] core component 3: the pooled
+ * scores are brought to the block granularity.  Window c of a sequence averages cis over
+ * positions c*stride .. c*stride+kernel-1 (full windows only, n_c of them, as for the
+ * compressed keys); block j averages the windows inside it exactly as S3 does.
+ *   cis [tokens, hkv] (fp64 values); out [n_seqs, hkv, nb_stride], zero past n_b(L). */
+int nsa_oracle_cis_block_scores(const double* cis, const int32_t* cu, int n_seqs, int hkv, int kernel, int stride,
+                                int block_size, int nb_stride, double* out) {
+  if (kernel <= 0 || stride <= 0 || block_size <= 0) return 1;
+  int err = 0;
+  for (int sq = 0; sq < n_seqs; ++sq) {
+    const int L = cu[sq + 1] - cu[sq];
+    const int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+    const int n_b = (L + block_size - 1) / block_size;
+    if (n_b > nb_stride) {
+      err = 1;
+      continue;
+    }
+    double* win = (double*)malloc(sizeof(double) * (size_t)(n_c + 1));
+    for (int g = 0; g < hkv; ++g) {
+      for (int c = 0; c < n_c; ++c) {
+        double acc = 0.0;
+        for (int i = 0; i < kernel; ++i) acc += cis[((size_t)cu[sq] + (size_t)c * stride + i) * hkv + g];
+        win[c] = acc / kernel;
+      }
+      double* row = out + ((size_t)sq * hkv + g) * nb_stride;
+      for (int j = 0; j < nb_stride; ++j) row[j] = 0.0;
+      nsa_oracle_pool_row(win, n_c, n_b, block_size, kernel, stride, row);
+    }
+    free(win);
+  }
+  return err;
+}
+
+/* NOSA two-stage selection ([NOSA-Parts] core component 3).  Stage 1 keeps, for each
+ * (token, kv-head), the forced blocks and the best blocks by the attention block score:
+ * S4 with k = qk_select.  Stage 2 ranks the kept blocks by the pooled CIS score of the
+ * token's sequence and keeps the forced blocks and the best others up to k in total;
+ * equal scores go to the lower block index; output ascending, -1 padded.
+ *   cis_scores [n_seqs, hkv, nb_stride];  k <= qk_select. */
+int nsa_oracle_topk_two_stage(const double* scores, int nb_stride, const double* cis_scores, const int32_t* cu,
+                              int n_seqs, int hkv, int block_size, int n_init, int n_local, int qk_select, int k,
+                              const int64_t* rows, int64_t n_rows, int32_t* idx) {
+  if (k <= 0 || qk_select < k || block_size <= 0) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int err = 0;
+#pragma omp parallel
+  {
+    cand_t* cand = (cand_t*)malloc(sizeof(cand_t) * (size_t)(nb_stride + 1));
+    int* pick = (int*)malloc(sizeof(int) * (size_t)(nb_stride + qk_select + 1));
+    int32_t* first = (int32_t*)malloc(sizeof(int32_t) * (size_t)qk_select);
+#pragma omp for schedule(dynamic, 64)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      int own = t / block_size;
+      if (own + 1 > nb_stride) {
+        err = 1;
+        continue;
+      }
+      for (int g = 0; g < hkv; ++g) {
+        row_topk(scores + ((size_t)rr * hkv + g) * nb_stride, t, block_size, n_init, n_local, qk_select, first,
+                 cand, pick);
+        const double* cs = cis_scores + ((size_t)sq * hkv + g) * nb_stride;
+        int n = 0;
+        for (int i = 0; i < qk_select; ++i) {
+          int j = first[i];
+          if (j < 0) continue;
+          int forced = (j < n_init) || (j > own - n_local);
+          cand[n].key = forced ? INFINITY : cs[j];
+          cand[n].j = j;
+          ++n;
+        }
+        qsort(cand, (size_t)n, sizeof(cand_t), cand_cmp);
+        int take = k < n ? k : n;
+        for (int i = 0; i < take; ++i) pick[i] = cand[i].j;
+        qsort(pick, (size_t)take, sizeof(int), int_cmp);
+        int32_t* o = idx + ((size_t)rr * hkv + g) * k;
+        for (int i = 0; i < k; ++i) o[i] = i < take ? pick[i] : -1;
+      }
+    }
+    free(cand);
+    free(pick);
+    free(first);
+  }
+  return err;
+}
+
+/* NOSA sparse_forward ([NOSA-Parts] "decoding over only 64 KV blocks"): the values are
+ * scaled by the CIS of their key (scaled_v = v * cis) and the result is divided by the
+ * same attention applied to all-ones values scaled alike (the "fake" attention whose
+ * output is the denominator).  With p the softmax over the listed keys and c_e the CIS
+ * of key e this is o = sum_e p_e c_e v_e / sum_e p_e c_e.  lse (natural log) is
+ * log sum_e exp(s_e) c_e.  A row whose weights sum to zero gets o = 0 and lse = -inf.
+ *   cis [tokens, hkv] (fp64 values), read at the key's own row. */
+int nsa_oracle_sparse_attn_cis(const void* q, const void* k, const void* v, int dtype, const double* cis,
+                               const int32_t* cu, int n_seqs, int h, int hkv, int d, const int32_t* idx, int S,
+                               int block_size, double scale, const int64_t* rows, int64_t n_rows, double* o,
+                               double* lse) {
+  if (h % hkv || block_size <= 0) return 1;
+  int64_t total = cu[n_seqs];
+  if (!rows) n_rows = total;
+  int r = h / hkv;
+#pragma omp parallel
+  {
+    int* keys = (int*)malloc(sizeof(int) * (size_t)(S * block_size + 1));
+    double* w = (double*)malloc(sizeof(double) * (size_t)(S * block_size + 1));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t rr = 0; rr < n_rows; ++rr) {
+      int64_t tok = rows ? rows[rr] : rr;
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      for (int hh = 0; hh < h; ++hh) {
+        int g = hh / r;
+        int n = selected_keys(idx + ((size_t)tok * hkv + g) * S, S, block_size, t, keys);
+        double* out = o + ((size_t)rr * h + hh) * d;
+        for (int i = 0; i < d; ++i) out[i] = 0.0;
+        double mx = -INFINITY;
+        for (int e = 0; e < n; ++e) {
+          double acc = 0.0;
+          size_t kr = ((size_t)(cu[sq] + keys[e]) * hkv + g) * d;
+          for (int i = 0; i < d; ++i) acc += ld(q, dtype, ((size_t)tok * h + hh) * d + i) * ld(k, dtype, kr + i);
+          w[e] = acc * scale;
+          if (w[e] > mx) mx = w[e];
+        }
+        double sum = 0.0;
+        for (int e = 0; e < n; ++e) {
+          w[e] = exp(w[e] - mx) * cis[(size_t)(cu[sq] + keys[e]) * hkv + g];
+          sum += w[e];
+        }
+        if (sum > 0.0) {
+          for (int e = 0; e < n; ++e) {
+            size_t vr = ((size_t)(cu[sq] + keys[e]) * hkv + g) * d;
+            for (int i = 0; i < d; ++i) out[i] += w[e] / sum * ld(v, dtype, vr + i);
+          }
+        }
+        if (lse) lse[(size_t)rr * h + hh] = sum > 0.0 ? mx + log(sum) : -INFINITY;
+      }
+    }
+    free(keys);
+    free(w);
+  }
+  return 0;
+}
+
 /* Block-mask sparse attention ([TileLang-NSA] sec. 1, block-sparse attention: the
  * attention matrix is cut into block x block tiles and a mask marks the active ones;
  * only active tiles are computed; is_causal keeps the lower triangle).  Dense layout:

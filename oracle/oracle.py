@@ -206,6 +206,60 @@ def sparse_attn_bwd(q, k, v, idx, do, cu, block_size=64, scale=None, q_rows=None
     return (dq if want_dq else None), (dk if want_dkv else None), (dv if want_dkv else None)
 
 
+def cis_block_scores(cis, cu, kernel=32, stride=16, block_size=64, nb_stride=None):
+    """NOSA stage 2: CIS [tokens, hkv] pooled over the compressor's windows, then to
+    blocks as in S3; returns [n_seqs, hkv, nb_stride] fp64."""
+    cis = np.ascontiguousarray(np.asarray(cis, np.float64))
+    cu = _i32(cu)
+    hkv = cis.shape[1]
+    if nb_stride is None:
+        nb_stride = max(1, -(-int(np.max(np.diff(cu))) // block_size))
+    out = np.zeros((len(cu) - 1, hkv, nb_stride), np.float64)
+    _check(_load().nsa_oracle_cis_block_scores(_p(cis), _p(cu), len(cu) - 1, hkv, kernel, stride, block_size,
+                                               nb_stride, _p(out)), "cis_block_scores")
+    return out
+
+
+def topk_two_stage(scores, cis_scores, cu, qk_select, k, block_size=64, n_init=1, n_local=2, rows=None):
+    """NOSA two-stage selection: S4 with k = qk_select on the attention block scores, then
+    the best k of those by pooled CIS score (forced blocks kept).  [rows, hkv, k] int32."""
+    scores = np.ascontiguousarray(np.asarray(scores, np.float64))
+    cis_scores = np.ascontiguousarray(np.asarray(cis_scores, np.float64))
+    cu = _i32(cu)
+    n, hkv, nb_stride = scores.shape
+    if cis_scores.shape != (len(cu) - 1, hkv, nb_stride):
+        raise ValueError("cis_scores must be [n_seqs, hkv, nb_stride]")
+    rows, nr = _rows(rows, int(cu[-1]))
+    if nr != n:
+        raise ValueError("scores must have one row per requested token")
+    out = np.zeros((n, hkv, k), np.int32)
+    _check(_load().nsa_oracle_topk_two_stage(_p(scores), nb_stride, _p(cis_scores), _p(cu), len(cu) - 1, hkv,
+                                             block_size, n_init, n_local, qk_select, k, _p(rows),
+                                             ctypes.c_int64(n), _p(out)), "topk_two_stage")
+    return out
+
+
+def sparse_attn_cis(q, k, v, cis, idx, cu, block_size=64, scale=None, rows=None):
+    """NOSA sparse_forward: selected attention with weights p_e * cis_e (normalised);
+    returns (o [rows,h,d], lse [rows,h]) fp64."""
+    q, k, v, idx, cu = (np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v), _i32(idx),
+                        _i32(cu))
+    cis = np.ascontiguousarray(np.asarray(cis, np.float64))
+    tot, h, d = q.shape
+    hkv = k.shape[1]
+    if cis.shape != (tot, hkv):
+        raise ValueError("cis must be [tokens, hkv]")
+    S = idx.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    rows, n = _rows(rows, tot)
+    o = np.zeros((n, h, d), np.float64)
+    lse = np.zeros((n, h), np.float64)
+    _check(_load().nsa_oracle_sparse_attn_cis(_p(q), _p(k), _p(v), _dt(q), _p(cis), _p(cu), len(cu) - 1, h, hkv, d,
+                                              _p(idx), S, block_size, ctypes.c_double(scale), _p(rows),
+                                              ctypes.c_int64(n), _p(o), _p(lse)), "sparse_attn_cis")
+    return o, lse
+
+
 def swa(q, k, v, cu, window=512, scale=None, rows=None):
     """S8: sliding-window attention; returns (o, lse)."""
     q, k, v, cu = np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v), _i32(cu)

@@ -47,6 +47,13 @@ def normal(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
     return f32_to_bf16_bits(x) if dtype == "bf16" else x
 
 
+def cis_scores(rng: np.random.Generator, tokens: int, hkv: int) -> np.ndarray:
+    """Synthetic per-key importance scores [tokens, hkv] fp32 in (0, 1): the logistic
+    sigmoid of N(0,1) draws (the scorer that produces them is learned)."""
+    x = rng.standard_normal(size=(tokens, hkv), dtype=np.float32)
+    return (1.0 / (1.0 + np.exp(-x.astype(np.float64)))).astype(np.float32)
+
+
 def dense_cu_seqlens(batch: int, seqlen: int) -> np.ndarray:
     return (np.arange(batch + 1, dtype=np.int64) * seqlen).astype(np.int32)
 

@@ -600,3 +600,122 @@ def test_sparse_bwd_stored_output_reading():
         assert np.allclose(a, b, atol=1e-6, rtol=1e-5)
     off = orc.sparse_attn_bwd(q, k, v, idx, do, cu, bs, o=np.zeros_like(q))
     assert not np.allclose(off[0], exact[0], atol=1e-3)
+
+
+# --------------------------------------------------------------------------- NOSA stage 2
+def test_cis_block_scores_equal_two_avg_pools():
+    """Windows: avg_pool1d(32, 16) of each sequence's CIS; blocks: avg_pool1d(3, 4,
+    ceil_mode) of the windows (the S3 rule), zero where a block holds no window."""
+    lengths = [10, 31, 32, 47, 100, 700, 1001]
+    cu = gen.varlen_cu_seqlens(lengths)
+    cis = gen.cis_scores(np.random.default_rng(71), int(cu[-1]), 2)
+    got = orc.cis_block_scores(cis, cu)
+    nb = got.shape[2]
+    for i, L in enumerate(lengths):
+        for g in range(2):
+            x = torch.from_numpy(cis[cu[i]:cu[i + 1], g].astype(np.float64)).view(1, 1, -1)
+            ref = np.zeros(nb)
+            if L >= 32:
+                win = F.avg_pool1d(x, 32, 16)
+                r = F.avg_pool1d(win, 3, 4, ceil_mode=True).flatten().numpy()
+                ref[:len(r)] = r
+            assert np.allclose(got[i, g], ref, atol=1e-14, rtol=0), (L, g)
+
+
+def test_cis_block_scores_ramp_hand_values():
+    """cis[t] = t: window c averages 16c .. 16c+31 = 16c + 15.5; a full block j averages
+    windows 4j, 4j+1, 4j+2, i.e. 64j + 31.5."""
+    L = 256
+    cis = np.arange(L, dtype=np.float64)[:, None]
+    got = orc.cis_block_scores(cis, gen.dense_cu_seqlens(1, L))[0, 0]
+    assert np.allclose(got, [31.5, 95.5, 159.5, 223.5], atol=1e-12)
+
+
+def _brute_two_stage(sc, cs, t, bs, n_init, n_local, qk, k):
+    own = t // bs
+    forced = lambda j: j < n_init or j > own - n_local  # noqa: E731
+    key1 = lambda j: (-(np.inf if forced(j) else sc[j]), j)  # noqa: E731
+    first = sorted(range(own + 1), key=key1)[:qk]
+    key2 = lambda j: (-(np.inf if forced(j) else cs[j]), j)  # noqa: E731
+    pick = sorted(sorted(first, key=key2)[:k])
+    return pick + [-1] * (k - len(pick))
+
+
+@pytest.mark.parametrize("qk,k", [(8, 4), (16, 16), (6, 3), (40, 16)])
+def test_topk_two_stage_brute_force_and_reductions(qk, k):
+    rng = np.random.default_rng(qk * 100 + k)
+    lengths = [700, 2000, 64, 1]
+    cu = gen.varlen_cu_seqlens(lengths)
+    nb = 32
+    sc = np.round(rng.random((int(cu[-1]), 2, nb)) * 8) / 8          # many exact ties
+    cs = np.round(rng.random((len(lengths), 2, nb)) * 8) / 8
+    got = orc.topk_two_stage(sc, cs, cu, qk, k)
+    for i in range(len(lengths)):
+        for t in range(lengths[i]):
+            for g in range(2):
+                want = _brute_two_stage(sc[cu[i] + t, g], cs[i, g], t, 64, 1, 2, qk, k)
+                assert got[cu[i] + t, g].tolist() == want
+    # qk_select = k: stage 2 keeps stage 1's choice
+    assert np.array_equal(orc.topk_two_stage(sc, cs, cu, k, k), orc.topk(sc, cu, 64, 1, 2, k))
+    # stage 1 keeps every causal block: the choice is S4 on the CIS scores of the sequence
+    per_row = np.concatenate([np.repeat(cs[i][None], lengths[i], 0) for i in range(len(lengths))])
+    assert np.array_equal(orc.topk_two_stage(sc, cs, cu, nb, k), orc.topk(per_row, cu, 64, 1, 2, k))
+
+
+def _cis_case(dtype, seed):
+    lengths = [150, 64, 33]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, bs = 4, 2, 16, 32
+    q, k, v = (_rand((cu[-1], hh, d), seed + i, dtype) for i, hh in enumerate((h, hkv, hkv)))
+    idx = _bwd_lists(cu, hkv, bs, 4, seed + 5)
+    cis = gen.cis_scores(np.random.default_rng(seed + 6), int(cu[-1]), hkv)
+    return lengths, cu, q, k, v, idx, cis, bs
+
+
+def test_sparse_cis_unit_weights_and_pages_construction():
+    """cis = 1 gives the plain selected attention; otherwise the output equals the pages'
+    recipe: attention of v * cis divided by attention of ones * cis."""
+    lengths, cu, q, k, v, idx, cis, bs = _cis_case("f32", 80)
+    o1, l1 = orc.sparse_attn_cis(q, k, v, np.ones_like(cis), idx, cu, bs)
+    o0, l0 = orc.sparse_attn(q, k, v, idx, cu, bs)
+    assert np.allclose(o1, o0, atol=1e-13) and np.allclose(l1, l0, atol=1e-13)
+    o, _ = orc.sparse_attn_cis(q, k, v, cis, idx, cu, bs)
+    vs = (v * cis[:, :, None]).astype(np.float32)
+    ones = np.repeat(cis[:, :, None], v.shape[2], 2).astype(np.float32)
+    num, _ = orc.sparse_attn(q, k, vs, idx, cu, bs)
+    den, _ = orc.sparse_attn(q, k, ones, idx, cu, bs)
+    assert np.allclose(o, num / den, atol=1e-6, rtol=1e-6)
+
+
+def test_sparse_cis_equals_sdpa_with_log_weight_bias():
+    """Weights p * cis = softmax(s + log cis): SDPA with a float mask (log cis on the listed
+    keys, times their multiplicity; -inf elsewhere)."""
+    lengths, cu, q, k, v, idx, cis, bs = _cis_case("bf16", 90)
+    o, lse = orc.sparse_attn_cis(q, k, v, cis, idx, cu, bs)
+    h, hkv, d = q.shape[1], k.shape[1], q.shape[2]
+    for i, L in enumerate(lengths):
+        a = int(cu[i])
+        for g in range(hkv):
+            mult = np.zeros((L, L))
+            for t in range(L):
+                for j in idx[a + t, g]:
+                    if j < 0 or j * bs > t:
+                        continue
+                    for tau in range(j * bs, min((j + 1) * bs, t + 1)):
+                        mult[t, tau] += 1
+            bias = np.where(mult > 0, np.log(np.maximum(mult, 1)) + np.log(cis[a:a + L, g].astype(np.float64))[None, :],
+                            -np.inf)
+            heads = slice(g * (h // hkv), (g + 1) * (h // hkv))
+            qq = _t(q[a:a + L, heads]).permute(1, 0, 2)
+            kk = _t(k[a:a + L, g:g + 1]).permute(1, 0, 2).expand(h // hkv, L, d)
+            vv = _t(v[a:a + L, g:g + 1]).permute(1, 0, 2).expand(h // hkv, L, d)
+            ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=torch.from_numpy(bias)).permute(1, 0, 2)
+            assert torch.allclose(torch.from_numpy(o[a:a + L, heads]), ref, atol=1e-12, rtol=0)
+            s = torch.einsum("hld,hmd->hlm", qq, kk) * d ** -0.5 + torch.from_numpy(bias)
+            assert torch.allclose(torch.from_numpy(lse[a:a + L, heads]).T, torch.logsumexp(s, -1), atol=1e-12)
+
+
+def test_sparse_cis_zero_weights_give_zero():
+    lengths, cu, q, k, v, idx, cis, bs = _cis_case("f32", 100)
+    o, lse = orc.sparse_attn_cis(q, k, v, np.zeros_like(cis), idx, cu, bs)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
