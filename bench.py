@@ -266,6 +266,42 @@ def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks):
             "launches_per_step": 3}
 
 
+def bench_nosa(torch, nsa, device, steps, warmup, flush, peaks):
+    """NOSA stage 2: CIS-weighted selected attention on the prefill workload, and the
+    block CIS scores plus two-stage selection on the varlen selection workload."""
+    w = gen.prefill()
+    q = dev(torch, w.q, device).view(w.batch, w.seqlen, w.h, w.d)
+    k, v, idx = dev(torch, w.k, device), dev(torch, w.v, device), dev(torch, w.idx, device)
+    cis = dev(torch, gen.cis_scores(gen.rng_for(1, 77), w.tokens, w.hkv), device)
+    out = torch.empty_like(q)
+    ms_att = float(np.mean(timed(torch, lambda: nsa.nsa_sparse_cis_fwd(q, k, v, cis, idx, 64, out=out), steps,
+                                 warmup, flush)))
+    flops = prefill_flops(w)
+    del q, k, v, idx, out, cis
+    sw = gen.selection()
+    cu = dev(torch, sw.cu_seqlens, device)
+    lens = np.diff(sw.cu_seqlens)
+    nb = ((-(-sw.max_len // 64)) + 3) // 4 * 4
+    sc = torch.rand((sw.tokens, sw.hkv, nb), dtype=torch.float32, device=device)
+    scis = dev(torch, gen.cis_scores(gen.rng_for(2, 77), sw.tokens, sw.hkv), device)
+    cs = torch.empty((len(lens), sw.hkv, nb), dtype=torch.float32, device=device)
+    sel = torch.empty((sw.tokens, sw.hkv, 16), dtype=torch.int32, device=device)
+
+    def select():
+        nsa.nsa_cis_block_scores(scis, cu_seqlens=cu, max_seqlen=sw.max_len, nb_stride=nb, out=cs)
+        nsa.nsa_topk_two_stage(sc, cs, 32, 16, cu_seqlens=cu, max_seqlen=sw.max_len, out=sel)
+
+    ms_sel = float(np.mean(timed(torch, select, steps, warmup, flush)))
+    tf = flops / (ms_att * 1e-3) / 1e12
+    return {"cis_attention": {"workload": "CIS-weighted selected attention, prefill B=8 T=16384 H=16 Hkv=1 d=128 "
+                                          "bf16, block 64, S=16", "ms": ms_att, "tflops": tf,
+                              "frac_of_bf16_peak": tf / peaks["bf16_tflops"]},
+            "cis_selection": {"workload": "block CIS scores + two-stage top-16 of 32, selection workload "
+                                          f"({sw.tokens} tokens, Hkv=2)", "ms": ms_sel,
+                              "tokens_per_s": sw.tokens / (ms_sel * 1e-3)},
+            "launches_per_step": 3}
+
+
 def bench_decode_offload(torch, nsa, device, steps, warmup, flush):
     """The decode workload with its K/V cache in page-locked host memory (the offloaded
     cache of the NOSA inference system); compressed keys, q and o stay in HBM."""
@@ -400,8 +436,8 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "decode", "decode_offload", "selection",
-                                                    "layer", "block_sparse"],
+    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "nosa", "decode", "decode_offload",
+                                                    "selection", "layer", "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -432,8 +468,9 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("prefill_bwd", "decode", "decode_offload", "selection", "layer", "block_sparse"):
-        fn = {"prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+    if args.only in ("prefill_bwd", "nosa", "decode", "decode_offload", "selection", "layer", "block_sparse"):
+        fn = {"nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode_offload": lambda: bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush),
               "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
@@ -516,6 +553,12 @@ def main():
             line["gpu_launches"] += 3 * max(3, args.steps // 2)
         except Exception as e:
             line["prefill_bwd"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["nosa"] = bench_nosa(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush, peaks)
+            line["gpu_launches"] += 3 * max(3, args.steps // 2)
+        except Exception as e:
+            line["nosa"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             line["decode"] = bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks)

@@ -161,6 +161,42 @@ NSA_API nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const v
                           const int32_t* block_indices, int S, int block_size, float scale, void* o,
                           float* lse, cudaStream_t stream);
 
+/* NOSA stage 2 -- pooled importance scores per block.  [NOSA-Parts] core component 2:
+ * a scorer gives every key position an importance score (CIS; produced elsewhere, e.g.
+ * by a learned scorer); [NOSA-Triton] mechanisms 1-3: the scores are mean-pooled over
+ * windows of `kernel` positions at step `stride`, aligned with the key compressor (full
+ * windows, n_c(L) of them); [NOSA-Parts] core component 3: the window means are brought
+ * to blocks with the rule of S3 (block j averages the windows lying inside it; no
+ * window -> 0).
+ *   cis  [tokens, h_kv] fp32;  out [n_seqs, h_kv, nb_stride] fp32, 0 past n_b(L). */
+NSA_API nsa_status nsa_cis_block_scores(const nsa_shape* shape, const float* cis, int kernel, int stride,
+                                        int block_size, int nb_stride, float* out, cudaStream_t stream);
+
+/* NOSA two-stage selection ([NOSA-Parts] core component 3).  Stage 1: the forced blocks
+ * and the best blocks by attention block score, qk_select in all (nsa_topk_select with
+ * k = qk_select).  Stage 2: those blocks ranked by their block CIS score (forced blocks
+ * first, equal scores to the lower block index); the best k are returned ascending,
+ * -1 padded.
+ *   block_scores      [tokens, h_kv, nb_stride] fp32 (nsa_cmp_scores_pool)
+ *   cis_block_scores  [n_seqs, h_kv, nb_stride] fp32 (nsa_cis_block_scores)
+ *   block_indices     [tokens, h_kv, k] int32 out
+ * Requires 1 <= k <= qk_select <= 64, nb_stride <= 2048. */
+NSA_API nsa_status nsa_topk_two_stage(const nsa_shape* shape, const float* block_scores, int nb_stride,
+                                      const float* cis_block_scores, int block_size, int n_init, int n_local,
+                                      int qk_select, int k, int32_t* block_indices, cudaStream_t stream);
+
+/* NOSA sparse_forward -- selected attention with CIS-scaled values and the all-ones
+ * normaliser ([NOSA-Parts] "decoding over only 64 KV blocks": scaled_v = v * cis, and the
+ * output divided by the same attention of all-ones values scaled alike).  With p the
+ * softmax over the listed keys and c_e the CIS of key e (per kv-head):
+ * o = sum_e p_e c_e v_e / sum_e p_e c_e;  lse = log sum_e exp(s_e) c_e.  A row whose
+ * weights sum to 0 gets o = 0, lse = -inf.  Lists as in nsa_sparse_fwd.
+ *   cis [tokens, h_kv] fp32 (>= 0);  other arguments as nsa_sparse_fwd.
+ * Requires bf16, d in {64,128}, block_size 64, S <= 64, h/h_kv <= 16 or a multiple of 16. */
+NSA_API nsa_status nsa_sparse_cis_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                      const float* cis, const int32_t* block_indices, int S, int block_size,
+                                      float scale, void* o, float* lse, cudaStream_t stream);
+
 /* Backward of S5: gradients of the selected-block attention for an upstream gradient
  * dO.  The pages train with the selected branch ([NSA-Triton] sec. 4) and print its
  * forward only ([TileLang-NSA] sec. 2); this is the derivative of that forward.  Per

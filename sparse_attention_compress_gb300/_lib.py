@@ -33,6 +33,9 @@ _SIGS = {
     "nsa_compress_k": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_p], _c_int),
     "nsa_cmp_scores_pool": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_int, _c_p], _c_int),
     "nsa_topk_select": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
+    "nsa_cis_block_scores": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
+    "nsa_topk_two_stage": ([_c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
+    "nsa_sparse_cis_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_select_workspace_size": ([_c_p, _c_int], _c_sz),
     "nsa_block_sparse_workspace_size": ([_c_p], _c_sz),
     "nsa_block_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p],
@@ -231,6 +234,54 @@ def nsa_topk_select(block_scores, k, block_size=64, n_init=1, n_local=2, *, cu_s
     _check(load().nsa_topk_select(ctypes.byref(shp), _ptr(block_scores), nb_stride, block_size, n_init, n_local, k,
                                   _ptr(out), _stream(stream)), "nsa_topk_select")
     return out
+
+
+def nsa_cis_block_scores(cis, kernel=32, stride=16, block_size=64, *, cu_seqlens=None, max_seqlen=None, batch=None,
+                         seqlen=None, nb_stride=None, out=None, stream=None):
+    """NOSA stage 2.  cis [tokens, Hkv] fp32 -> block CIS scores [n_seqs, Hkv, nb_stride] fp32."""
+    tokens, h_kv = cis.shape
+    if cu_seqlens is None and batch is None:
+        batch, seqlen = 1, tokens
+    shp = make_shape(tokens, h_kv, h_kv, 1, NSA_F32, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, batch=batch,
+                     seqlen=seqlen)
+    n_seqs = shp.n_seqs if cu_seqlens is not None else shp.batch
+    if nb_stride is None:
+        nb_stride = max(1, -(-shp.seqlen // block_size))
+    if out is None:
+        out = torch.empty((n_seqs, h_kv, nb_stride), dtype=torch.float32, device=cis.device)
+    _check(load().nsa_cis_block_scores(ctypes.byref(shp), _ptr(cis), kernel, stride, block_size, nb_stride,
+                                       _ptr(out), _stream(stream)), "nsa_cis_block_scores")
+    return out
+
+
+def nsa_topk_two_stage(block_scores, cis_block_scores, qk_select, k, block_size=64, n_init=1, n_local=2, *,
+                       cu_seqlens=None, max_seqlen=None, batch=None, seqlen=None, out=None, stream=None):
+    """NOSA two-stage selection: block_scores [tokens, Hkv, nb_stride], cis_block_scores
+    [n_seqs, Hkv, nb_stride] -> indices [tokens, Hkv, k] int32."""
+    tokens, h_kv, nb_stride = block_scores.shape
+    if cu_seqlens is None and batch is None:
+        batch, seqlen = 1, tokens
+    shp = make_shape(tokens, h_kv, h_kv, 1, NSA_F32, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, batch=batch,
+                     seqlen=seqlen)
+    if out is None:
+        out = torch.empty((tokens, h_kv, k), dtype=torch.int32, device=block_scores.device)
+    _check(load().nsa_topk_two_stage(ctypes.byref(shp), _ptr(block_scores), nb_stride, _ptr(cis_block_scores),
+                                     block_size, n_init, n_local, qk_select, k, _ptr(out), _stream(stream)),
+           "nsa_topk_two_stage")
+    return out
+
+
+def nsa_sparse_cis_fwd(q, k, v, cis, block_indices, block_size=64, scale=0.0, *, cu_seqlens=None, max_seqlen=None,
+                       out=None, lse=None, stream=None):
+    """NOSA sparse_forward: selected attention with weights p * cis (normalised); cis [tokens, Hkv] fp32."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    S = block_indices.shape[-1]
+    if out is None:
+        out = torch.empty_like(qf)
+    _check(load().nsa_sparse_cis_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(cis), _ptr(block_indices),
+                                     S, block_size, float(scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "nsa_sparse_cis_fwd")
+    return out.view(q.shape) if q.dim() == 4 else out
 
 
 def nsa_sparse_fwd(q, k, v, block_indices, block_size=64, scale=0.0, *, cu_seqlens=None, max_seqlen=None,

@@ -158,6 +158,69 @@ nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, in
                      "nsa_topk_select");
 }
 
+nsa_status nsa_cis_block_scores(const nsa_shape* shape, const float* cis, int kernel, int stride, int block_size,
+                                int nb_stride, float* out, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(kernel > 0 && stride > 0 && block_size > 0, NSA_ERR_INVALID,
+              "nsa_cis_block_scores: kernel, stride and block_size must be positive");
+  NSA_REQUIRE(nb_stride >= (s.max_len + block_size - 1) / block_size, NSA_ERR_INVALID,
+              "nsa_cis_block_scores: nb_stride %d < blocks of the longest sequence", nb_stride);
+  if (s.n_seqs == 0 || nb_stride == 0) return NSA_OK;
+  NSA_PTR(out);
+  if (s.tokens > 0) NSA_PTR(cis);
+  return cuda_status(launch_cis_block_scores(s, cis, shape->h_kv, kernel, stride, block_size, nb_stride, out, stream),
+                     "nsa_cis_block_scores");
+}
+
+nsa_status nsa_topk_two_stage(const nsa_shape* shape, const float* block_scores, int nb_stride,
+                              const float* cis_block_scores, int block_size, int n_init, int n_local, int qk_select,
+                              int k, int32_t* block_indices, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(block_size > 0 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID,
+              "nsa_topk_two_stage: block_size > 0, n_init >= 0, n_local >= 0");
+  NSA_REQUIRE(k >= 1 && k <= qk_select && qk_select <= 64, NSA_ERR_UNSUPPORTED,
+              "nsa_topk_two_stage: need 1 <= k <= qk_select <= 64");
+  NSA_REQUIRE(nb_stride >= (s.max_len + block_size - 1) / block_size, NSA_ERR_INVALID,
+              "nsa_topk_two_stage: nb_stride %d < blocks of the longest sequence", nb_stride);
+  NSA_REQUIRE(nb_stride <= 2048, NSA_ERR_UNSUPPORTED, "nsa_topk_two_stage: nb_stride must be <= 2048");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(block_scores);
+  NSA_PTR(cis_block_scores);
+  NSA_PTR(block_indices);
+  return cuda_status(launch_topk_two_stage(s, block_scores, nb_stride, cis_block_scores, shape->h_kv, block_size,
+                                           n_init, n_local, qk_select, k, block_indices, stream),
+                     "nsa_topk_two_stage");
+}
+
+nsa_status nsa_sparse_cis_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v, const float* cis,
+                              const int32_t* block_indices, int S, int block_size, float scale, void* o, float* lse,
+                              cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  const int r = shape->h / shape->h_kv;
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_sparse_cis_fwd: bf16 only");
+  NSA_REQUIRE(shape->d == 64 || shape->d == 128, NSA_ERR_UNSUPPORTED, "nsa_sparse_cis_fwd: d must be 64 or 128");
+  NSA_REQUIRE(block_size == 64, NSA_ERR_UNSUPPORTED, "nsa_sparse_cis_fwd: block_size must be 64");
+  NSA_REQUIRE(S >= 1 && S <= 64, NSA_ERR_UNSUPPORTED, "nsa_sparse_cis_fwd: S must be in [1, 64]");
+  NSA_REQUIRE(r <= 16 || r % 16 == 0, NSA_ERR_UNSUPPORTED,
+              "nsa_sparse_cis_fwd: h/h_kv must be <= 16 or a multiple of 16");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(block_indices);
+  NSA_PTR(o);
+  NSA_REQUIRE(cis != nullptr && (reinterpret_cast<uintptr_t>(cis) & 3u) == 0, NSA_ERR_INVALID,
+              "nsa_sparse_cis_fwd: cis must be non-null and 4-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(NSA_ERR_INVALID, "nsa_sparse_cis_fwd: lse misaligned");
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_sparse_fwd(s, q, k, v, block_indices, S, block_size, shape->h, shape->h_kv, shape->d,
+                                       shape->dtype, scale, o, lse, stream, cis),
+                     "nsa_sparse_cis_fwd");
+}
+
 static nsa_status check_sparse_bwd(const nsa_shape* shape, int S, int block_size, Seqs* s, const char* fn) {
   if (nsa_status st = make_seqs(shape, s, fn)) return st;
   NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);

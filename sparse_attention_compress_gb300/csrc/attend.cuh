@@ -5,6 +5,11 @@
 // the query; keys past the query are masked.  Softmax with base-2 exponentials of
 // scale*log2(e)-folded scores (sec. 3.1).
 //
+// With W, each key's softmax weight is multiplied by a per-key weight wb[key * w_stride]
+// before both the PV product and the normaliser: the CIS weighting of NOSA's
+// sparse_forward ([NOSA-Parts] "decoding over 64 KV blocks": values scaled by the CIS and
+// the output divided by the same attention of all-ones values, i.e. weights p*c / sum p*c).
+//
 // A warp owns one 16-key slice of every block in its list and the 16 (head) rows of
 // one query; it streams K and V slices through a private cp.async ring (swizzled rows,
 // conflict-free ldmatrix), keeps an online softmax in registers and returns its
@@ -25,15 +30,31 @@ struct WarpState {
   float m0, m1, l0, l1;
 };
 
+// Ring bytes of one stage of warp_attend (K and V slices, and the slice's 16 weights
+// padded to 128 bytes when weighted).
+template <int D, bool W = false>
+constexpr int attend_stage_bytes() {
+  return 2 * 16 * D * 2 + (W ? 128 : 0);
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float x;
+  asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(x) : "r"(addr));
+  return x;
+}
+
 // list[0..cnt): block indices (already filtered to slices starting at or before t).
 // kb / vb: K / V row 0 of the sequence for this kv-head; row_stride in elements.
-template <int D, int BS, int NSTAGE>
+// wb (with W): weight of key row 0 of the sequence for this kv-head; w_stride in floats.
+
+template <int D, int BS, int NSTAGE, bool W = false>
 __device__ __forceinline__ WarpState warp_attend(const int* list, int cnt, int slice, const __nv_bfloat16* kb,
                                                  const __nv_bfloat16* vb, int64_t row_stride, int64_t t,
                                                  float scale_log2, const uint32_t (*qa)[4], uint32_t wbase,
-                                                 const void* dummy, float (*o)[4], int lane) {
+                                                 const void* dummy, float (*o)[4], int lane,
+                                                 const float* wb = nullptr, int64_t w_stride = 0) {
   constexpr int SLICE_BYTES = 16 * D * 2;
-  constexpr int STAGE_BYTES = 2 * SLICE_BYTES;
+  constexpr int STAGE_BYTES = attend_stage_bytes<D, W>();
   constexpr int CH = D / 8;
   auto issue = [&](int i) {
     const int64_t key0 = (int64_t)list[i] * BS + slice * 16;
@@ -48,6 +69,12 @@ __device__ __forceinline__ WarpState warp_attend(const int* list, int cnt, int s
       const int64_t off = row * row_stride + ch * 8;
       cp_async16(tile_addr<D>(sb, row, ch), ok ? kp + off : dummy, ok ? 16 : 0);
       cp_async16(tile_addr<D>(sb + SLICE_BYTES, row, ch), ok ? vp + off : dummy, ok ? 16 : 0);
+    }
+    if (W && lane < 16) {
+      const bool ok = key0 + lane <= t;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(sb + 2 * SLICE_BYTES + lane * 4),
+                   "l"(ok ? (const void*)(wb + (key0 + lane) * w_stride) : dummy), "r"(ok ? 4 : 0)
+                   : "memory");
     }
   };
 
@@ -106,6 +133,17 @@ __device__ __forceinline__ WarpState warp_attend(const int* list, int cnt, int s
       pr[nt][1] = ex2(s[nt][1] - mu0);
       pr[nt][2] = ex2(s[nt][2] - mu1);
       pr[nt][3] = ex2(s[nt][3] - mu1);
+    }
+    if (W) {
+      const uint32_t sw = sb + 2 * SLICE_BYTES + (lane & 3) * 8;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float w0 = lds_f32(sw + nt * 32), w1 = lds_f32(sw + nt * 32 + 4);
+        pr[nt][0] *= w0;
+        pr[nt][1] *= w1;
+        pr[nt][2] *= w0;
+        pr[nt][3] *= w1;
+      }
     }
     st.l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
     st.l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);

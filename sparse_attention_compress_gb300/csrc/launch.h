@@ -25,9 +25,19 @@ cudaError_t launch_scores_pool(const Seqs& s, const void* q, const void* k_cmp, 
 cudaError_t launch_topk(const Seqs& s, const float* scores, int nb_stride, int hkv, int block_size,
                         int n_init, int n_local, int k, int32_t* idx, cudaStream_t st);
 
+// cis (nullable, bf16 path, block 64): per-key weights [tokens, hkv] fp32 (NOSA CIS).
 cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const void* v,
                               const int32_t* idx, int S, int block_size, int h, int hkv, int d,
-                              int dtype, float scale, void* o, float* lse, cudaStream_t st);
+                              int dtype, float scale, void* o, float* lse, cudaStream_t st,
+                              const float* cis = nullptr);
+
+// NOSA stage 2 (csrc/nosa.cu): block CIS scores [n_seqs, hkv, nb_stride] from per-key
+// CIS [tokens, hkv]; two-stage selection (top qk by attention score, then top k by CIS).
+cudaError_t launch_cis_block_scores(const Seqs& s, const float* cis, int hkv, int kernel, int stride, int block_size,
+                                    int nb_stride, float* out, cudaStream_t st);
+cudaError_t launch_topk_two_stage(const Seqs& s, const float* scores, int nb_stride, const float* cis_scores, int hkv,
+                                  int block_size, int n_init, int n_local, int qk, int k, int32_t* idx,
+                                  cudaStream_t st);
 
 // Backward of selected attention (bf16, d 128, block 64, h/hkv <= 16): dq [tokens,h,d],
 // dk/dv [tokens,hkv,d] from q, k, v, the block lists, the forward's o and lse and dO.

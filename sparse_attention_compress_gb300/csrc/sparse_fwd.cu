@@ -22,6 +22,7 @@ struct SparseParams {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const int32_t* idx;
+  const float* w;  // per-key weights [tokens, hkv] (NOSA CIS), used when the kernel is weighted
   __nv_bfloat16* o;
   float* lse;
   Seqs seqs;
@@ -37,12 +38,12 @@ struct SparseParams {
 #endif
 
 
-template <int D, int BS, int NSTAGE>
+template <int D, int BS, int NSTAGE, bool W = false>
 __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(const SparseParams p) {
   constexpr int NW = 4;
   constexpr int NSLICE = BS / 16;
   constexpr int NGROUP = NW / NSLICE;
-  constexpr int STAGE_BYTES = 2 * 16 * D * 2;
+  constexpr int STAGE_BYTES = attend_stage_bytes<D, W>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_list[NW][64];
 
@@ -84,10 +85,10 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS) sparse_fwd_mma(con
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  WarpState st = warp_attend<D, BS, NSTAGE>(s_list[warp], cnt, slice, p.k + (kv_base * p.hkv + g) * D,
-                                            p.v + (kv_base * p.hkv + g) * D, (int64_t)p.hkv * D, t,
-                                            p.scale_log2, qa, smem_u32(smem) + warp * NSTAGE * STAGE_BYTES, p.k,
-                                            o, lane);
+  WarpState st = warp_attend<D, BS, NSTAGE, W>(s_list[warp], cnt, slice, p.k + (kv_base * p.hkv + g) * D,
+                                               p.v + (kv_base * p.hkv + g) * D, (int64_t)p.hkv * D, t,
+                                               p.scale_log2, qa, smem_u32(smem) + warp * NSTAGE * STAGE_BYTES, p.k,
+                                               o, lane, W ? p.w + kv_base * p.hkv + g : nullptr, p.hkv);
   __syncthreads();  // every warp is done with its ring: the merge reuses the shared memory
   cta_merge<D, NW>(reinterpret_cast<float*>(smem), o, st, warp, lane);
 
@@ -175,12 +176,12 @@ __global__ void __launch_bounds__(128) sparse_fwd_f32(const float* __restrict__ 
   }
 }
 
-template <int D, int BS, int NSTAGE>
+template <int D, int BS, int NSTAGE, bool W = false>
 static cudaError_t run_mma(const SparseParams& p, dim3 grid, cudaStream_t st) {
-  constexpr int pipe = 4 * NSTAGE * 2 * 16 * D * 2;
+  constexpr int pipe = 4 * NSTAGE * attend_stage_bytes<D, W>();
   constexpr int merge = merge_bytes<D, 4>();
   constexpr int bytes = pipe > merge ? pipe : merge;
-  auto kern = sparse_fwd_mma<D, BS, NSTAGE>;
+  auto kern = sparse_fwd_mma<D, BS, NSTAGE, W>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, bytes, st>>>(p);
@@ -189,7 +190,7 @@ static cudaError_t run_mma(const SparseParams& p, dim3 grid, cudaStream_t st) {
 
 cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const void* v,
                               const int32_t* idx, int S, int block_size, int h, int hkv, int d,
-                              int dtype, float scale, void* o, float* lse, cudaStream_t st) {
+                              int dtype, float scale, void* o, float* lse, cudaStream_t st, const float* cis) {
   if (s.tokens == 0) return cudaSuccess;
   if (dtype == kF32) {
     const int max_keys = S * block_size;
@@ -207,6 +208,7 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   p.k = (const __nv_bfloat16*)k;
   p.v = (const __nv_bfloat16*)v;
   p.idx = idx;
+  p.w = cis;
   p.o = (__nv_bfloat16*)o;
   p.lse = lse;
   p.seqs = s;
@@ -216,6 +218,10 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   p.scale_log2 = scale * kLog2e;
   const int r = h / hkv;
   dim3 grid((unsigned)s.tokens, hkv * ((r + 15) / 16), 1);
+  if (cis) {  // CIS-weighted variant: block 64 only (checked by the caller)
+    constexpr int NS = NSA_PREFILL_NSTAGE;
+    return d == 128 ? run_mma<128, 64, NS, true>(p, grid, st) : run_mma<64, 64, NS, true>(p, grid, st);
+  }
   if (d == 128) {
     constexpr int NS = NSA_PREFILL_NSTAGE;
     if (block_size == 64) return run_mma<128, 64, NS>(p, grid, st);

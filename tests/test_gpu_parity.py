@@ -282,6 +282,74 @@ def test_sparse_bwd_full_size_sampled():
     assert_close(gv[torch.from_numpy(kr).cuda()], rv, what="dv sampled")
 
 
+# --------------------------------------------------------------------------- NOSA stage 2
+def test_cis_block_scores():
+    lengths = [10, 31, 32, 47, 100, 700, 5000]
+    cu = gen.varlen_cu_seqlens(lengths)
+    cis = gen.cis_scores(_rng(31), int(cu[-1]), 2)
+    nb = -(-max(lengths) // 64)
+    got = nsa.nsa_cis_block_scores(dev(cis), cu_seqlens=dev(cu), max_seqlen=max(lengths), nb_stride=nb)
+    torch.cuda.synchronize()
+    ref = orc.cis_block_scores(cis, cu, nb_stride=nb)
+    assert np.allclose(host(got), ref, atol=2e-6, rtol=0)
+
+
+@pytest.mark.parametrize("qk,k,nb", [(32, 16, 64), (64, 64, 260), (16, 16, 40), (48, 13, 1024), (3, 1, 8)])
+def test_topk_two_stage_bit_exact(qk, k, nb):
+    """Same fp32 inputs on both sides: the chosen lists must match exactly (many ties)."""
+    rng = _rng(32 + qk)
+    L = nb * 64
+    lengths = [L, min(L, 700), 65]
+    cu = gen.varlen_cu_seqlens(lengths)
+    sc = (np.round(rng.random((int(cu[-1]), 2, nb)) * 16) / 16).astype(np.float32)
+    cs = (np.round(rng.random((len(lengths), 2, nb)) * 16) / 16).astype(np.float32)
+    got = nsa.nsa_topk_two_stage(dev(sc), dev(cs), qk, k, cu_seqlens=dev(cu), max_seqlen=L)
+    torch.cuda.synchronize()
+    ref = orc.topk_two_stage(sc, cs, cu, qk, k)
+    assert np.array_equal(host(got), ref)
+
+
+@pytest.mark.parametrize("H,hkv,d", [(16, 1, 128), (16, 4, 128), (8, 8, 128), (16, 2, 64), (32, 1, 128)])
+def test_sparse_cis_fwd(H, hkv, d):
+    lengths = [1, 63, 64, 65, 900, 2000]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(33)
+    q, k, v = (gen.normal(rng, (cu[-1], hh, d), "bf16") for hh in (H, hkv, hkv))
+    idx = gen.random_block_indices(rng, cu, hkv, 16, 64, force_first=True)
+    cis = gen.cis_scores(rng, int(cu[-1]), hkv)
+    cis[:40] = 0.0  # the first sequences' early keys carry no weight: some rows sum to zero
+    ref, lse_ref = orc.sparse_attn_cis(q, k, v, cis, idx, cu, 64)
+    lse = torch.empty((cu[-1], H), dtype=torch.float32, device="cuda")
+    out = nsa.nsa_sparse_cis_fwd(dev(q), dev(k), dev(v), dev(cis), dev(idx), 64, cu_seqlens=dev(cu),
+                                 max_seqlen=max(lengths), lse=lse)
+    torch.cuda.synchronize()
+    assert_close(out, ref, what="cis-weighted attention")
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(host(lse)), fin)
+    assert_close(host(lse)[fin], lse_ref[fin], atol=1e-3, rtol=1e-3, what="cis lse")
+
+
+def test_nosa_pipeline():
+    """compress -> block scores -> block CIS -> two-stage selection -> CIS-weighted attention,
+    each stage checked against the oracle on the GPU's own inputs to that stage."""
+    w = gen.selection(n_seqs=3, lo=1500, hi=4000)
+    cu, L = w.cu_seqlens, w.max_len
+    dcu = dev(cu)
+    cis = gen.cis_scores(_rng(34), w.tokens, w.hkv)
+    kc = nsa.nsa_compress_k(dev(w.k), cu_seqlens=dcu, max_seqlen=L)
+    nb = ((-(-L // 64)) + 3) // 4 * 4
+    sc = nsa.nsa_cmp_scores_pool(dev(w.q), kc, w.hkv, cu_seqlens=dcu, max_seqlen=L, nb_stride=nb)
+    cs = nsa.nsa_cis_block_scores(dev(cis), cu_seqlens=dcu, max_seqlen=L, nb_stride=nb)
+    idx = nsa.nsa_topk_two_stage(sc, cs, 32, 16, cu_seqlens=dcu, max_seqlen=L)
+    out = nsa.nsa_sparse_cis_fwd(dev(w.q), dev(w.k), dev(w.v), dev(cis), idx, 64, cu_seqlens=dcu, max_seqlen=L)
+    torch.cuda.synchronize()
+    assert np.allclose(host(cs), orc.cis_block_scores(cis, cu, nb_stride=nb), atol=2e-6, rtol=0)
+    assert np.array_equal(host(idx), orc.topk_two_stage(host(sc), host(cs), cu, 32, 16))
+    rows = np.unique(np.concatenate([_rng(35).integers(0, w.tokens, 300), cu[:-1], cu[1:] - 1]))
+    ref, _ = orc.sparse_attn_cis(w.q, w.k, w.v, cis, host(idx), cu, 64, rows=rows)
+    assert_close(out[torch.from_numpy(rows).cuda()], ref, what="nosa pipeline")
+
+
 # --------------------------------------------------------------------------- S7, S8, S9
 @pytest.mark.parametrize("H,hkv,d", [(16, 1, 128), (32, 2, 128), (8, 1, 64), (16, 4, 128), (64, 1, 128)])
 def test_cmp_attn(H, hkv, d):
