@@ -875,6 +875,178 @@ int nsa_oracle_cmp_attn(const void* q, const void* kc, const void* vc, int dtype
   return 0;
 }
 
+/* Backward of S7 (the compressed branch), written as the derivative of the forward
+ * above.  Per (token, head) row over its causal compressed keys c < n_causal(t):
+ *   p_c = softmax_c(scale q . kc_c),  dp_c = dO . vc_c,  D = dO . o (o_in when given,
+ *   else sum_c p_c dp_c),  ds_c = p_c (dp_c - D);
+ *   dq = scale sum_c ds_c kc_c,  dkc[c] += scale ds_c q,  dvc[c] += p_c dO.
+ * A row without causal compressed keys contributes nothing and gets dq = 0.
+ * dq [n_q_rows, h, d] for q_rows (all when NULL; n_q_rows < 0 skips); dkc, dvc
+ * [n_kv_rows, hkv, d] for the packed compressed rows kv_rows (all when NULL; n_kv_rows
+ * < 0 skips).  Thread-private accumulators, summed in thread order. */
+static int cmp_row_grads(const void* q, const void* kc, const void* vc, const void* dout, const void* o_in, int dtype,
+                         int64_t tok, int hh, int h, int hkv, int d, int g, int64_t c0, int n, double scale,
+                         double* p, double* ds) {
+  if (n == 0) return 0;
+  double mx = -INFINITY;
+  for (int c = 0; c < n; ++c) {
+    double acc = 0.0;
+    size_t kr = ((size_t)(c0 + c) * hkv + g) * d;
+    for (int i = 0; i < d; ++i) acc += ld(q, dtype, ((size_t)tok * h + hh) * d + i) * ld(kc, dtype, kr + i);
+    p[c] = acc * scale;
+    if (p[c] > mx) mx = p[c];
+  }
+  double sum = 0.0;
+  for (int c = 0; c < n; ++c) sum += exp(p[c] - mx);
+  double D = 0.0;
+  for (int c = 0; c < n; ++c) {
+    p[c] = exp(p[c] - mx) / sum;
+    double acc = 0.0;
+    size_t vr = ((size_t)(c0 + c) * hkv + g) * d;
+    for (int i = 0; i < d; ++i) acc += ld(dout, dtype, ((size_t)tok * h + hh) * d + i) * ld(vc, dtype, vr + i);
+    ds[c] = acc;
+    D += p[c] * acc;
+  }
+  if (o_in) {
+    D = 0.0;
+    for (int i = 0; i < d; ++i)
+      D += ld(dout, dtype, ((size_t)tok * h + hh) * d + i) * ld(o_in, dtype, ((size_t)tok * h + hh) * d + i);
+  }
+  for (int c = 0; c < n; ++c) ds[c] = p[c] * (ds[c] - D);
+  return n;
+}
+
+int nsa_oracle_cmp_attn_bwd(const void* q, const void* kc, const void* vc, const void* dout, const void* o_in,
+                            int dtype, const int32_t* cu, int n_seqs, int h, int hkv, int d, int kernel, int stride,
+                            double scale, const int64_t* q_rows, int64_t n_q_rows, double* dq,
+                            const int64_t* kv_rows, int64_t n_kv_rows, double* dkc, double* dvc) {
+  if (h % hkv || kernel <= 0 || stride <= 0) return 1;
+  const int64_t total = cu[n_seqs];
+  const int r = h / hkv;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  const int64_t n_cmp = off[n_seqs];
+  int maxL = 0;
+  for (int i = 0; i < n_seqs; ++i) if (cu[i + 1] - cu[i] > maxL) maxL = cu[i + 1] - cu[i];
+  const int nc_max = nsa_oracle_num_cmp(maxL, kernel, stride) + 1;
+  if (n_q_rows >= 0 && !q_rows) n_q_rows = total;
+  if (n_q_rows > 0) {
+#pragma omp parallel
+    {
+      double* p = (double*)malloc(sizeof(double) * (size_t)nc_max);
+      double* ds = (double*)malloc(sizeof(double) * (size_t)nc_max);
+#pragma omp for schedule(dynamic, 8)
+      for (int64_t rr = 0; rr < n_q_rows; ++rr) {
+        int64_t tok = q_rows ? q_rows[rr] : rr;
+        int sq = seq_of(cu, n_seqs, tok);
+        int L = cu[sq + 1] - cu[sq];
+        int t = (int)(tok - cu[sq]);
+        int n = num_causal_cmp(t, nsa_oracle_num_cmp(L, kernel, stride), kernel, stride);
+        for (int hh = 0; hh < h; ++hh) {
+          int g = hh / r;
+          double* out = dq + ((size_t)rr * h + hh) * d;
+          for (int i = 0; i < d; ++i) out[i] = 0.0;
+          if (!cmp_row_grads(q, kc, vc, dout, o_in, dtype, tok, hh, h, hkv, d, g, off[sq], n, scale, p, ds)) continue;
+          for (int c = 0; c < n; ++c) {
+            size_t kr = ((size_t)(off[sq] + c) * hkv + g) * d;
+            for (int i = 0; i < d; ++i) out[i] += scale * ds[c] * ld(kc, dtype, kr + i);
+          }
+        }
+      }
+      free(p);
+      free(ds);
+    }
+  }
+  if (n_kv_rows >= 0 && !kv_rows) n_kv_rows = n_cmp;
+  if (n_kv_rows <= 0) {
+    free(off);
+    return 0;
+  }
+  int64_t* slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_cmp + 1));
+  for (int64_t i = 0; i < n_cmp; ++i) slot[i] = kv_rows ? -1 : i;
+  if (kv_rows)
+    for (int64_t i = 0; i < n_kv_rows; ++i) slot[kv_rows[i]] = i;
+  const size_t acc_len = (size_t)n_kv_rows * hkv * d;
+  for (size_t i = 0; i < acc_len; ++i) dkc[i] = dvc[i] = 0.0;
+  int nthr = 1;
+#ifdef _OPENMP
+  nthr = omp_get_max_threads();
+#endif
+  double* acc = (double*)calloc((size_t)nthr * 2 * acc_len, sizeof(double));
+#pragma omp parallel num_threads(nthr)
+  {
+    int me = 0;
+#ifdef _OPENMP
+    me = omp_get_thread_num();
+#endif
+    double* mk = acc + (size_t)me * 2 * acc_len;
+    double* mv = mk + acc_len;
+    double* p = (double*)malloc(sizeof(double) * (size_t)nc_max);
+    double* ds = (double*)malloc(sizeof(double) * (size_t)nc_max);
+#pragma omp for schedule(static)
+    for (int64_t tok = 0; tok < total; ++tok) {
+      int sq = seq_of(cu, n_seqs, tok);
+      int L = cu[sq + 1] - cu[sq];
+      int t = (int)(tok - cu[sq]);
+      int n = num_causal_cmp(t, nsa_oracle_num_cmp(L, kernel, stride), kernel, stride);
+      int hit = 0;
+      for (int c = 0; c < n && !hit; ++c) hit = slot[off[sq] + c] >= 0;
+      if (!hit) continue;
+      for (int hh = 0; hh < h; ++hh) {
+        int g = hh / r;
+        cmp_row_grads(q, kc, vc, dout, o_in, dtype, tok, hh, h, hkv, d, g, off[sq], n, scale, p, ds);
+        for (int c = 0; c < n; ++c) {
+          int64_t sl = slot[off[sq] + c];
+          if (sl < 0) continue;
+          double* ak = mk + ((size_t)sl * hkv + g) * d;
+          double* av = mv + ((size_t)sl * hkv + g) * d;
+          for (int i = 0; i < d; ++i) {
+            ak[i] += scale * ds[c] * ld(q, dtype, ((size_t)tok * h + hh) * d + i);
+            av[i] += p[c] * ld(dout, dtype, ((size_t)tok * h + hh) * d + i);
+          }
+        }
+      }
+    }
+    free(p);
+    free(ds);
+  }
+  for (int th = 0; th < nthr; ++th) {
+    const double* mk = acc + (size_t)th * 2 * acc_len;
+    const double* mv = mk + acc_len;
+    for (size_t i = 0; i < acc_len; ++i) {
+      dkc[i] += mk[i];
+      dvc[i] += mv[i];
+    }
+  }
+  free(acc);
+  free(slot);
+  free(off);
+  return 0;
+}
+
+/* Backward of S1 (the mean pooling): the gradient of every token row is the sum, over
+ * the compressed windows that contain it, of the window's gradient divided by the window
+ * length.  dkc [n_cmp_total, hkv, d] fp64 in; dk [tokens, hkv, d] fp64 out. */
+int nsa_oracle_compress_bwd(const double* dkc, const int32_t* cu, int n_seqs, int hkv, int d, int kernel, int stride,
+                            double* dk) {
+  if (kernel <= 0 || stride <= 0) return 1;
+  int64_t* off = cmp_offsets(cu, n_seqs, kernel, stride);
+  const int64_t total = cu[n_seqs];
+  for (size_t i = 0; i < (size_t)total * hkv * d; ++i) dk[i] = 0.0;
+  for (int sq = 0; sq < n_seqs; ++sq) {
+    int L = cu[sq + 1] - cu[sq];
+    int n_c = nsa_oracle_num_cmp(L, kernel, stride);
+    for (int c = 0; c < n_c; ++c)
+      for (int w = 0; w < kernel; ++w) {
+        size_t tok = (size_t)cu[sq] + (size_t)c * stride + w;
+        for (int g = 0; g < hkv; ++g)
+          for (int i = 0; i < d; ++i)
+            dk[(tok * hkv + g) * d + i] += dkc[((size_t)(off[sq] + c) * hkv + g) * d + i] / kernel;
+      }
+  }
+  free(off);
+  return 0;
+}
+
 /* S9: gate combine ([NSA-Triton] sec. 1.1: gates[0]*compressed + gates[1]*selected
  * + gates[2]*local), each gate the logistic sigmoid of its logit;
  * gates is [tokens, h, 3] fp32. */

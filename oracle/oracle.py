@@ -311,6 +311,46 @@ def cmp_attn(q, kc, vc, cu, kernel=32, stride=16, scale=None, rows=None):
     return o, lse
 
 
+def cmp_attn_bwd(q, kc, vc, do, cu, kernel=32, stride=16, scale=None, q_rows=None, kv_rows=None, want_dq=True,
+                 want_dkv=True, o=None):
+    """Backward of S7 for upstream gradient do: (dq [q_rows, h, d], dkc, dvc [kv_rows, hkv, d]) fp64
+    (kv_rows index the packed compressed rows).  o: optional stored forward output for D."""
+    q, kc, vc, do, cu = (np.ascontiguousarray(q), np.ascontiguousarray(kc), np.ascontiguousarray(vc),
+                         np.ascontiguousarray(do), _i32(cu))
+    if do.dtype != q.dtype or do.shape != q.shape:
+        raise ValueError("do must match q in dtype and shape")
+    if o is not None:
+        o = np.ascontiguousarray(o)
+        if o.dtype != q.dtype or o.shape != q.shape:
+            raise ValueError("o must match q in dtype and shape")
+    tot, h, d = q.shape
+    hkv = kc.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    qr, nq = _rows(q_rows, tot)
+    kr, nkv = _rows(kv_rows, kc.shape[0])
+    nq = nq if want_dq else -1
+    nkv = nkv if want_dkv else -1
+    dq = np.zeros((max(nq, 0), h, d), np.float64)
+    dk = np.zeros((max(nkv, 0), hkv, d), np.float64)
+    dv = np.zeros((max(nkv, 0), hkv, d), np.float64)
+    _check(_load().nsa_oracle_cmp_attn_bwd(_p(q), _p(kc), _p(vc), _p(do), _p(o), _dt(q), _p(cu), len(cu) - 1, h,
+                                           hkv, d, kernel, stride, ctypes.c_double(scale), _p(qr),
+                                           ctypes.c_int64(nq), _p(dq), _p(kr), ctypes.c_int64(nkv), _p(dk), _p(dv)),
+           "cmp_attn_bwd")
+    return (dq if want_dq else None), (dk if want_dkv else None), (dv if want_dkv else None)
+
+
+def compress_bwd(dkc, cu, kernel=32, stride=16):
+    """Backward of S1: token-row gradient [tokens, hkv, d] fp64 from the window gradient."""
+    dkc = np.ascontiguousarray(np.asarray(dkc, np.float64))
+    cu = _i32(cu)
+    _, hkv, d = dkc.shape
+    out = np.zeros((int(cu[-1]), hkv, d), np.float64)
+    _check(_load().nsa_oracle_compress_bwd(_p(dkc), _p(cu), len(cu) - 1, hkv, d, kernel, stride, _p(out)),
+           "compress_bwd")
+    return out
+
+
 def gate_combine(o_cmp, o_slc, o_swa, gates):
     """S9: sigmoid-gated sum of the three branch outputs."""
     o_cmp, o_slc, o_swa = (np.ascontiguousarray(np.asarray(a, np.float64)) for a in (o_cmp, o_slc, o_swa))

@@ -719,3 +719,100 @@ def test_sparse_cis_zero_weights_give_zero():
     lengths, cu, q, k, v, idx, cis, bs = _cis_case("f32", 100)
     o, lse = orc.sparse_attn_cis(q, k, v, np.zeros_like(cis), idx, cu, bs)
     assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+# --------------------------------------------------------------------------- S7 and S1 backward
+def _cmp_case(dtype, seed, lengths=(150, 97, 20), h=4, hkv=2, d=16):
+    cu = gen.varlen_cu_seqlens(list(lengths))
+    q, do = _rand((cu[-1], h, d), seed, dtype), _rand((cu[-1], h, d), seed + 1, dtype)
+    n_cmp = int(orc.cmp_offsets(cu)[-1])
+    kc, vc = _rand((n_cmp, hkv, d), seed + 2, dtype), _rand((n_cmp, hkv, d), seed + 3, dtype)
+    return list(lengths), cu, q, do, kc, vc
+
+
+def _autograd_cmp(q, kc, vc, do, cu, scale):
+    Q, K, V = (_t(a).requires_grad_(True) for a in (q, kc, vc))
+    dO = _t(do)
+    h, hkv = Q.shape[1], K.shape[1]
+    r = h // hkv
+    off = orc.cmp_offsets(cu)
+    loss = 0.0
+    for i in range(len(cu) - 1):
+        a, L = int(cu[i]), int(cu[i + 1] - cu[i])
+        n_c = orc.num_cmp(L)
+        if n_c == 0:
+            continue
+        kk = K[off[i]:off[i] + n_c].repeat_interleave(r, 1)
+        vv = V[off[i]:off[i] + n_c].repeat_interleave(r, 1)
+        t = torch.arange(31, L)                      # rows with at least one causal window
+        ok = (torch.arange(n_c)[None, :] * 16 + 31) <= t[:, None]
+        s = torch.einsum("thd,chd->thc", Q[a + 31:a + L], kk) * scale
+        s = s.masked_fill(~ok[:, None, :], -torch.inf)
+        o = torch.einsum("thc,chd->thd", torch.softmax(s, -1), vv)
+        loss = loss + (o * dO[a + 31:a + L]).sum()
+    loss.backward()
+    return Q.grad, K.grad, V.grad
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_cmp_attn_bwd_equals_autograd(dtype):
+    lengths, cu, q, do, kc, vc = _cmp_case(dtype, 121)
+    dq, dkc, dvc = orc.cmp_attn_bwd(q, kc, vc, do, cu)
+    gq, gk, gv = _autograd_cmp(q, kc, vc, do, cu, 16 ** -0.5)
+    for ours, ref in ((dq, gq), (dkc, gk), (dvc, gv)):
+        assert torch.allclose(torch.from_numpy(ours), ref, atol=1e-12, rtol=1e-10)
+
+
+def test_cmp_attn_bwd_finite_differences_invariants_and_rows():
+    lengths, cu, q, do, kc, vc = _cmp_case("f32", 131, lengths=(120, 64))
+    dq, dkc, dvc = orc.cmp_attn_bwd(q, kc, vc, do, cu)
+    rng = np.random.default_rng(132)
+    eps = 1e-2
+
+    def loss(qq, kk, vv):
+        o, _ = orc.cmp_attn(qq, kk, vv, cu)
+        return float((o * do.astype(np.float64)).sum())
+
+    for which, grad in ((0, dq), (1, dkc), (2, dvc)):
+        args = [q, kc, vc]
+        delta = rng.standard_normal(args[which].shape)
+        plus, minus = list(args), list(args)
+        plus[which] = (args[which] + eps * delta).astype(np.float32)
+        minus[which] = (args[which] - eps * delta).astype(np.float32)
+        step = plus[which].astype(np.float64) - minus[which].astype(np.float64)
+        fd = loss(*plus) - loss(*minus)
+        an = float((grad * step).sum())
+        assert abs(fd - an) <= 1e-4 * max(1.0, abs(an)), (which, fd, an)
+    off = orc.cmp_offsets(cu)
+    for i, L in enumerate(lengths):
+        sl = slice(off[i], off[i + 1])
+        for g in range(2):
+            assert np.abs(dkc[sl, g].sum(0)).max() < 1e-10
+            rows = slice(cu[i] + 31, cu[i + 1])          # rows with at least one causal window
+            assert np.allclose(dvc[sl, g].sum(0), do[rows, 2 * g:2 * g + 2].astype(np.float64).sum((0, 1)),
+                               atol=1e-10, rtol=0)
+    qr, kr = [0, 30, 31, 100, 183], [0, 3, 5, 8]
+    sq, sk, sv = orc.cmp_attn_bwd(q, kc, vc, do, cu, q_rows=qr, kv_rows=kr)
+    assert np.allclose(sq, dq[qr], atol=1e-13) and np.allclose(sk, dkc[kr], atol=1e-13)
+    assert np.allclose(sv, dvc[kr], atol=1e-13)
+
+
+def test_compress_bwd_is_the_adjoint_of_compress():
+    """<compress(x), y> = <x, compress_bwd(y)> for every x, y (exact means), and it equals
+    autograd of avg_pool1d(32, 16) per sequence."""
+    lengths = [10, 31, 32, 47, 100, 333]
+    cu = gen.varlen_cu_seqlens(lengths)
+    x = _rand((cu[-1], 2, 8), 141, "f32")
+    xe, _ = orc.compress(x, cu)
+    y = np.random.default_rng(142).standard_normal(xe.shape)
+    gx = orc.compress_bwd(y, cu)
+    assert abs(float((xe * y).sum()) - float((x.astype(np.float64) * gx).sum())) < 1e-9
+    off = orc.cmp_offsets(cu)
+    for i, L in enumerate(lengths):
+        X = torch.from_numpy(x[cu[i]:cu[i + 1]].astype(np.float64)).permute(1, 2, 0).requires_grad_(True)
+        if L < 32:
+            assert np.all(gx[cu[i]:cu[i + 1]] == 0)
+            continue
+        P = F.avg_pool1d(X.reshape(1, -1, L), 32, 16).reshape(2, 8, -1)
+        (P * torch.from_numpy(y[off[i]:off[i + 1]]).permute(1, 2, 0)).sum().backward()
+        assert torch.allclose(X.grad.permute(2, 0, 1), torch.from_numpy(gx[cu[i]:cu[i + 1]]), atol=1e-14)
