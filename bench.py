@@ -266,6 +266,37 @@ def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks):
             "launches_per_step": 3}
 
 
+def bench_cmp_bwd(torch, nsa, device, steps, warmup, flush, peaks):
+    """Backward of the compressed branch at the layer shape: dq, d k_cmp, d v_cmp from the
+    forward's o and lse, then the pooling backward to the token rows of K and V."""
+    from sparse_attention_compress_gb300 import _lib
+    w = gen.layer()
+    q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
+    kc, vc = nsa.nsa_compress_k(k), nsa.nsa_compress_k(v)
+    do = dev(torch, gen.normal(gen.rng_for(4, 99), (w.tokens, w.h, w.d), "bf16"), device)
+    lse = torch.empty((w.tokens, w.h), dtype=torch.float32, device=device)
+    o = nsa.nsa_cmp_attn_fwd(q, kc, vc, w.hkv, lse=lse)
+    shp = _lib.make_shape(w.tokens, w.h, w.hkv, w.d, _lib.NSA_BF16, batch=1, seqlen=w.tokens)
+    ws = torch.empty(nsa.nsa_cmp_attn_bwd_workspace_size(shp), dtype=torch.uint8, device=device)
+    dq, dkc, dvc = torch.empty_like(q), torch.empty_like(kc), torch.empty_like(vc)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+
+    def step():
+        nsa.nsa_cmp_attn_bwd(q, kc, vc, o, lse, do, w.hkv, workspace=ws, dq=dq, dk_cmp=dkc, dv_cmp=dvc)
+        nsa.nsa_compress_bwd(dkc, w.tokens, out=dk)
+        nsa.nsa_compress_bwd(dvc, w.tokens, out=dv)
+
+    ms = float(np.mean(timed(torch, step, steps, warmup, flush)))
+    t = np.arange(w.tokens)
+    ncaus = np.clip((t - 31) // 16 + 1, 0, None)
+    flops = float(ncaus.sum()) * w.h * 2 * w.d * 5  # S and dP recomputed, dQ, dK, dV
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "backward of the compressed branch + pooling, layer T=65536 H=64 Hkv=4 d=128 bf16 "
+                        "(32/16 windows)", "ms_per_step": ms, "tflops": tf, "flops_per_step": flops,
+            "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "workspace_bytes": int(ws.numel()),
+            "launches_per_step": 5}
+
+
 def bench_nosa(torch, nsa, device, steps, warmup, flush, peaks):
     """NOSA stage 2: CIS-weighted selected attention on the prefill workload, and the
     block CIS scores plus two-stage selection on the varlen selection workload."""
@@ -436,7 +467,7 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "nosa", "decode", "decode_offload",
+    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "cmp_bwd", "nosa", "decode", "decode_offload",
                                                     "selection", "layer", "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
@@ -468,8 +499,10 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("prefill_bwd", "nosa", "decode", "decode_offload", "selection", "layer", "block_sparse"):
-        fn = {"nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+    if args.only in ("prefill_bwd", "cmp_bwd", "nosa", "decode", "decode_offload", "selection", "layer",
+                     "block_sparse"):
+        fn = {"cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode_offload": lambda: bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush),
@@ -553,6 +586,12 @@ def main():
             line["gpu_launches"] += 3 * max(3, args.steps // 2)
         except Exception as e:
             line["prefill_bwd"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["cmp_bwd"] = bench_cmp_bwd(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush, peaks)
+            line["gpu_launches"] += 5 * max(3, args.steps // 2)
+        except Exception as e:
+            line["cmp_bwd"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             line["nosa"] = bench_nosa(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush, peaks)

@@ -161,6 +161,30 @@ NSA_API nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const v
                           const int32_t* block_indices, int S, int block_size, float scale, void* o,
                           float* lse, cudaStream_t stream);
 
+/* Backward of S7, the compressed branch: gradients for an upstream dO of the attention
+ * over the stored compressed keys and values (the forward nsa_cmp_attn_fwd).  Per (token,
+ * head) row over its causal compressed keys c < n_causal(t): p_c = exp(scale q.kc_c -
+ * lse), dp_c = dO.vc_c, D = dO.o, ds_c = p_c (dp_c - D); dq = scale sum ds_c kc_c,
+ * dk_cmp[c] += scale ds_c q, dv_cmp[c] += p_c dO.  Rows without causal keys give dq = 0.
+ * The pages print the forward only ([NSA-Triton] sec. 1.1); this is its derivative.
+ *   q, o, d_o, dq    [tokens, h, d] bf16;  lse [tokens, h] fp32 (the forward's)
+ *   k_cmp, v_cmp, dk_cmp, dv_cmp  [n_cmp_total, h_kv, d] bf16, packed per sequence
+ *   workspace        nsa_cmp_attn_bwd_workspace_size() bytes, 256-byte aligned
+ * Deterministic.  Requires bf16, d 128, h/h_kv <= 16, at most 4096 compressed keys per
+ * sequence. */
+NSA_API size_t nsa_cmp_attn_bwd_workspace_size(const nsa_shape* shape, int kernel, int stride);
+NSA_API nsa_status nsa_cmp_attn_bwd(const nsa_shape* shape, const void* q, const void* k_cmp, const void* v_cmp,
+                                    int kernel, int stride, float scale, const void* o, const float* lse,
+                                    const void* d_o, void* dq, void* dk_cmp, void* dv_cmp, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward of S1, the mean pooling: token row t of a sequence receives, from every
+ * compressed window c of that sequence containing it (c*stride <= t < c*stride+kernel),
+ * the window's gradient divided by kernel; tokens in no window get 0.
+ *   dk_cmp [n_cmp_total, h_kv, d] bf16;  dk [tokens, h_kv, d] bf16 out.  d % 8 == 0. */
+NSA_API nsa_status nsa_compress_bwd(const nsa_shape* shape, const void* dk_cmp, int kernel, int stride, void* dk,
+                                    cudaStream_t stream);
+
 /* NOSA stage 2 -- pooled importance scores per block.  [NOSA-Parts] core component 2:
  * a scorer gives every key position an importance score (CIS; produced elsewhere, e.g.
  * by a learned scorer); [NOSA-Triton] mechanisms 1-3: the scores are mean-pooled over

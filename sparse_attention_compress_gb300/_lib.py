@@ -44,6 +44,10 @@ _SIGS = {
                     _c_p], _c_int),
     "nsa_sparse_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_sparse_bwd_workspace_size": ([_c_p, _c_int, _c_int], _c_sz),
+    "nsa_cmp_attn_bwd_workspace_size": ([_c_p, _c_int, _c_int], _c_sz),
+    "nsa_cmp_attn_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                          _c_sz, _c_p], _c_int),
+    "nsa_compress_bwd": ([_c_p, _c_p, _c_int, _c_int, _c_p, _c_p], _c_int),
     "nsa_sparse_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                         _c_sz, _c_p], _c_int),
     "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
@@ -316,6 +320,41 @@ def nsa_sparse_bwd(q, k, v, block_indices, o, lse, d_o, block_size=64, scale=0.0
                                  float(scale), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
                                  _ptr(workspace), workspace.numel(), _stream(stream)), "nsa_sparse_bwd")
     return dq, dk, dv
+
+
+def nsa_cmp_attn_bwd_workspace_size(shape: NsaShape, kernel: int = 32, stride: int = 16) -> int:
+    return int(load().nsa_cmp_attn_bwd_workspace_size(ctypes.byref(shape), kernel, stride))
+
+
+def nsa_cmp_attn_bwd(q, k_cmp, v_cmp, o, lse, d_o, h_kv, kernel=32, stride=16, scale=0.0, *, cu_seqlens=None,
+                     max_seqlen=None, workspace=None, dq=None, dk_cmp=None, dv_cmp=None, stream=None):
+    """Backward of S7: (dq like q, dk_cmp and dv_cmp like k_cmp) from the forward's o, lse."""
+    qf, shp = _shape_for(q, h_kv, cu_seqlens, max_seqlen)
+    if workspace is None:
+        ws = nsa_cmp_attn_bwd_workspace_size(shp, kernel, stride)
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk_cmp = torch.empty_like(k_cmp) if dk_cmp is None else dk_cmp
+    dv_cmp = torch.empty_like(v_cmp) if dv_cmp is None else dv_cmp
+    _check(load().nsa_cmp_attn_bwd(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), _ptr(v_cmp), kernel, stride,
+                                   float(scale), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk_cmp), _ptr(dv_cmp),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "nsa_cmp_attn_bwd")
+    return dq, dk_cmp, dv_cmp
+
+
+def nsa_compress_bwd(dk_cmp, tokens, kernel=32, stride=16, *, cu_seqlens=None, max_seqlen=None, batch=None,
+                     seqlen=None, out=None, stream=None):
+    """Backward of S1: token-row gradient [tokens, Hkv, d] from the window gradient dk_cmp."""
+    _, h_kv, d = dk_cmp.shape
+    if cu_seqlens is None and batch is None:
+        batch, seqlen = 1, tokens
+    shp = make_shape(tokens, h_kv, h_kv, d, NSA_BF16, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, batch=batch,
+                     seqlen=seqlen)
+    if out is None:
+        out = torch.empty((tokens, h_kv, d), dtype=dk_cmp.dtype, device=dk_cmp.device)
+    _check(load().nsa_compress_bwd(ctypes.byref(shp), _ptr(dk_cmp), kernel, stride, _ptr(out), _stream(stream)),
+           "nsa_compress_bwd")
+    return out
 
 
 def nsa_cmp_attn_fwd(q, k_cmp, v_cmp, h_kv, kernel=32, stride=16, scale=0.0, *, cu_seqlens=None,

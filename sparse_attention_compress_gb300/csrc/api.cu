@@ -221,6 +221,69 @@ nsa_status nsa_sparse_cis_fwd(const nsa_shape* shape, const void* q, const void*
                      "nsa_sparse_cis_fwd");
 }
 
+static nsa_status check_cmp_bwd(const nsa_shape* shape, int kernel, int stride, Seqs* s, const char* fn) {
+  if (nsa_status st = make_seqs(shape, s, fn)) return st;
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);
+  NSA_REQUIRE(shape->d == 128, NSA_ERR_UNSUPPORTED, "%s: d must be 128", fn);
+  NSA_REQUIRE(kernel >= 1 && stride >= 1 && kernel <= 1024 && stride <= kernel, NSA_ERR_UNSUPPORTED,
+              "%s: needs 1 <= stride <= kernel <= 1024", fn);
+  NSA_REQUIRE(shape->h / shape->h_kv <= 16, NSA_ERR_UNSUPPORTED, "%s: h/h_kv must be <= 16", fn);
+  NSA_REQUIRE(num_cmp_host(s->max_len, kernel, stride) <= 4096, NSA_ERR_UNSUPPORTED,
+              "%s: at most 4096 compressed keys per sequence", fn);
+  NSA_REQUIRE(s->max_len <= (1 << 24), NSA_ERR_UNSUPPORTED, "%s: sequences must be <= 2^24 tokens", fn);
+  return NSA_OK;
+}
+
+size_t nsa_cmp_attn_bwd_workspace_size(const nsa_shape* shape, int kernel, int stride) {
+  Seqs s;
+  if (check_cmp_bwd(shape, kernel, stride, &s, "nsa_cmp_attn_bwd_workspace_size") != NSA_OK) return 0;
+  return cmp_attn_bwd_workspace_bytes(s, shape->h, shape->h_kv, kernel, stride);
+}
+
+nsa_status nsa_cmp_attn_bwd(const nsa_shape* shape, const void* q, const void* k_cmp, const void* v_cmp, int kernel,
+                            int stride, float scale, const void* o, const float* lse, const void* d_o, void* dq,
+                            void* dk_cmp, void* dv_cmp, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = check_cmp_bwd(shape, kernel, stride, &s, __func__)) return st;
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(o);
+  NSA_PTR(d_o);
+  NSA_PTR(dq);
+  if (num_cmp_host(s.max_len, kernel, stride) > 0) {
+    NSA_PTR(k_cmp);
+    NSA_PTR(v_cmp);
+    NSA_PTR(dk_cmp);
+    NSA_PTR(dv_cmp);
+  }
+  NSA_REQUIRE(lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) == 0, NSA_ERR_INVALID,
+              "nsa_cmp_attn_bwd: lse must be non-null and 4-byte aligned");
+  const size_t need = cmp_attn_bwd_workspace_bytes(s, shape->h, shape->h_kv, kernel, stride);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_cmp_attn_bwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_cmp_attn_bwd: workspace %zu < %zu bytes",
+              workspace_bytes, need);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_cmp_attn_bwd(s, q, k_cmp, v_cmp, shape->h, shape->h_kv, kernel, stride, scale, o, lse,
+                                         d_o, dq, dk_cmp, dv_cmp, workspace, stream),
+                     "nsa_cmp_attn_bwd");
+}
+
+nsa_status nsa_compress_bwd(const nsa_shape* shape, const void* dk_cmp, int kernel, int stride, void* dk,
+                            cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_compress_bwd: bf16 only");
+  NSA_REQUIRE(shape->d % 8 == 0, NSA_ERR_UNSUPPORTED, "nsa_compress_bwd: d must be a multiple of 8");
+  NSA_REQUIRE(kernel >= 1 && stride >= 1, NSA_ERR_INVALID, "nsa_compress_bwd: kernel and stride must be positive");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(dk);
+  if (num_cmp_host(s.max_len, kernel, stride) > 0) NSA_PTR(dk_cmp);
+  return cuda_status(launch_compress_bwd(s, dk_cmp, shape->h_kv, shape->d, kernel, stride, dk, stream),
+                     "nsa_compress_bwd");
+}
+
 static nsa_status check_sparse_bwd(const nsa_shape* shape, int S, int block_size, Seqs* s, const char* fn) {
   if (nsa_status st = make_seqs(shape, s, fn)) return st;
   NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);

@@ -45,6 +45,15 @@ size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv);
 cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const void* v, const int32_t* idx, int S,
                               int h, int hkv, float scale, const void* o, const float* lse, const void* dout,
                               void* dq, void* dk, void* dv, void* workspace, cudaStream_t st);
+// Backward of the compressed branch (same kernels over the packed compressed keys):
+// dq [tokens,h,d], dk_cmp/dv_cmp [n_cmp,hkv,d]; and of the mean pooling (bf16, d % 8 == 0).
+size_t cmp_attn_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int kernel, int stride);
+cudaError_t launch_cmp_attn_bwd(const Seqs& s, const void* q, const void* k_cmp, const void* v_cmp, int h, int hkv,
+                                int kernel, int stride, float scale, const void* o, const float* lse,
+                                const void* dout, void* dq, void* dk_cmp, void* dv_cmp, void* workspace,
+                                cudaStream_t st);
+cudaError_t launch_compress_bwd(const Seqs& s, const void* dk_cmp, int hkv, int d, int kernel, int stride, void* dk,
+                                cudaStream_t st);
 
 // mode 0: compressed-attention branch (keys/values are packed compressed rows)
 // mode 1: sliding-window branch

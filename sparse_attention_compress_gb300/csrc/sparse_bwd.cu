@@ -52,7 +52,27 @@ struct BwdParams {
   int h, hkv, S, r;
   float scale, scale_log2;
   int n_chunks, nb, items_per_bg;
+  // compressed branch (cmp_kernel > 0): the keys are the packed compressed rows, query t
+  // reaches the compressed keys c < n_causal(t) and its list is every such block (idx is
+  // unused); otherwise the keys are the tokens and query t reaches keys <= t of its list.
+  int cmp_kernel, cmp_stride;
 };
+
+// Key rows of sequence b start here; the sequence has key_len(L) of them.
+__device__ __forceinline__ int64_t key_base(const BwdParams& p, int b) {
+  return p.cmp_kernel ? cmp_offset(p.seqs, b, p.cmp_kernel, p.cmp_stride) : (int64_t)seq_start(p.seqs, b);
+}
+__device__ __forceinline__ int key_len(const BwdParams& p, int L) {
+  return p.cmp_kernel ? num_cmp(L, p.cmp_kernel, p.cmp_stride) : L;
+}
+// Last key query t may attend (-1: none).
+__device__ __forceinline__ int key_bound(const BwdParams& p, int t, int Lk) {
+  return p.cmp_kernel ? num_causal_cmp(t, Lk, p.cmp_kernel, p.cmp_stride) - 1 : t;
+}
+// First query position that reaches key block j.
+__device__ __forceinline__ int first_query(const BwdParams& p, int j) {
+  return p.cmp_kernel ? p.cmp_stride * kBS * j + p.cmp_kernel - 1 : kBS * j;
+}
 
 __device__ __forceinline__ float dot_bf16x2(uint32_t a, uint32_t b) {
   const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
@@ -61,10 +81,14 @@ __device__ __forceinline__ float dot_bf16x2(uint32_t a, uint32_t b) {
 }
 
 // P and dS enter the dV, dQ and dK products as bf16.  Where a warp's 16 x 16 tile holds
-// a |value| above kSplitAbove (rows with few keys, where p is large and a bf16 rounding
+// a |value| above the threshold (rows with few keys, where p is large and a bf16 rounding
 // of it is not small beside the gradient), the bf16 remainder x - bf16(x) goes through a
-// second product, so the operand is carried to about 16 bits.
-constexpr float kSplitAbove = 0.0625f;
+// second product, so the operand is carried to about 16 bits.  The threshold for P is
+// low: with a nearly uniform softmax (the compressed branch's logits are small, since
+// compressed keys are means) p ~ 1/n rounds alike on every row of the same length, and
+// those errors add up over the thousands of rows that reach a key.
+constexpr float kSplitAbove = 0.0625f;   // dS
+constexpr float kSplitPAbove = 0.00390625f;  // P (1/256)
 
 __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(a, b);
@@ -84,8 +108,21 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src
 // Item index (within one sequence / kv-head) -> (key block j, chunk c).  Blocks
 // j = m*kGroup .. m*kGroup+kGroup-1 have their first query chunk at m and one item for
 // each chunk m .. n_chunks-1.
-__device__ __forceinline__ void item_to_block(int item, int n_chunks, int nb, int& j, int& c, int& m) {
+__device__ __forceinline__ void item_to_block(const BwdParams& p, int item, int& j, int& c, int& m) {
+  const int n_chunks = p.n_chunks, nb = p.nb;
   int rem = item;
+  if (p.cmp_kernel) {  // block j has chunks first_query(j) / kChunk .. n_chunks-1
+    for (j = 0; j < nb; ++j) {
+      m = first_query(p, j) / kChunk;
+      if (rem < n_chunks - m) {
+        c = m + rem;
+        return;
+      }
+      rem -= n_chunks - m;
+    }
+    c = n_chunks;
+    return;
+  }
   for (m = 0; m < n_chunks; ++m) {
     const int blocks = min(kGroup, nb - m * kGroup);
     const int per = n_chunks - m;
@@ -116,8 +153,9 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
   const int r = p.r;
   const int64_t qrow = blockIdx.x;
   const int sq = seq_of_token(p.seqs, qrow);
-  const int64_t kv_base = seq_start(p.seqs, sq);
-  const int t = (int)(qrow - kv_base);
+  const int t = (int)(qrow - seq_start(p.seqs, sq));
+  const int64_t kv_base = key_base(p, sq);
+  const int tb = key_bound(p, t, key_len(p, seq_len(p.seqs, sq)));  // last reachable key
   const int hbase = g * r;
   const int rlo = lane >> 2, rhi = rlo + 8;
   const bool w0 = rlo < r, w1 = rhi < r;
@@ -145,20 +183,26 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
     if (w1) p.dsum[row0 + rhi] = d1;
   }
 
-  // this warp's list: listed blocks whose slice starts at or before t
-  const int32_t* il = p.idx + (qrow * p.hkv + g) * p.S;
+  // this warp's list: listed blocks whose slice starts at or before the bound (every
+  // such block for the compressed branch)
   int cnt = 0;
-  for (int base = 0; base < p.S; base += 32) {
-    const int e = base + lane;
-    int blk = -1;
-    bool ok = false;
-    if (e < p.S) {
-      blk = il[e];
-      ok = blk >= 0 && (int64_t)blk * BS + slice * 16 <= t;
+  if (p.cmp_kernel) {
+    cnt = tb >= slice * 16 ? (tb - slice * 16) / BS + 1 : 0;
+    for (int e = lane; e < cnt; e += 32) s_list[warp][e] = e;
+  } else {
+    const int32_t* il = p.idx + (qrow * p.hkv + g) * p.S;
+    for (int base = 0; base < p.S; base += 32) {
+      const int e = base + lane;
+      int blk = -1;
+      bool ok = false;
+      if (e < p.S) {
+        blk = il[e];
+        ok = blk >= 0 && (int64_t)blk * BS + slice * 16 <= tb;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (ok) s_list[warp][cnt + __popc(m & ((1u << lane) - 1u))] = blk;
+      cnt += __popc(m);
     }
-    const unsigned m = __ballot_sync(0xffffffffu, ok);
-    if (ok) s_list[warp][cnt + __popc(m & ((1u << lane) - 1u))] = blk;
-    cnt += __popc(m);
   }
   __syncwarp();
 
@@ -170,11 +214,11 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
   auto issue = [&](int i) {
     const int64_t key0 = (int64_t)list[i] * BS + slice * 16;
     const uint32_t sb = wbase + (i % NSTAGE) * STAGE_BYTES;
-    const bool full = key0 + 15 <= t;
+    const bool full = key0 + 15 <= tb;
 #pragma unroll
     for (int c = lane; c < 16 * CH; c += 32) {
       const int row = c / CH, ch = c % CH;
-      const bool ok = full || key0 + row <= t;
+      const bool ok = full || key0 + row <= tb;
       const int64_t off = (key0 + row) * rs + ch * 8;
       cp_async16(tile_addr<D>(sb, row, ch), ok ? kb + off : (const void*)p.k, ok ? 16 : 0);
       cp_async16(tile_addr<D>(sb + SLICE_BYTES, row, ch), ok ? vb + off : (const void*)p.k, ok ? 16 : 0);
@@ -205,7 +249,7 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t key = key0 + nt * 8 + (lane & 3) * 2 + (j & 1);
-        const float pe = key <= t ? ex2((s[nt][j] + s2[nt][j]) * p.scale_log2 - (j < 2 ? L0 : L1)) : 0.f;
+        const float pe = key <= tb ? ex2((s[nt][j] + s2[nt][j]) * p.scale_log2 - (j < 2 ? L0 : L1)) : 0.f;
         ds[nt][j] = pe * ((dp[nt][j] + dp2[nt][j]) - (j < 2 ? d0 : d1));
         big = fmaxf(big, fabsf(ds[nt][j]));
       }
@@ -272,11 +316,13 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
   const int item = blockIdx.x / n_bg;
   const int b = bg / p.hkv, g = bg % p.hkv;
   int j, c, m;
-  item_to_block(item, p.n_chunks, p.nb, j, c, m);
+  item_to_block(p, item, j, c, m);
   const int L = seq_len(p.seqs, b);
-  if (j * BS >= L || (c > m && c * kChunk >= L)) return;  // no partial is read for this item
+  const int Lk = key_len(p, L);
+  if (j * BS >= Lk || (c > m && c * kChunk >= L)) return;  // no partial is read for this item
   const int64_t base = seq_start(p.seqs, b);
-  const int t_begin = max(j * BS, c * kChunk), t_end = min((c + 1) * kChunk, L);
+  const int64_t kbase = key_base(p, b);
+  const int t_begin = max(first_query(p, j), c * kChunk), t_end = min((c + 1) * kChunk, L);
 
   const uint32_t kt = smem_u32(smem), vt = kt + kTileBytes;
   const uint32_t ring = vt + kTileBytes;
@@ -285,11 +331,11 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
   // K_j and V_j (rows past the sequence read as zeros; no query reaches them)
   {
     const int64_t rs = (int64_t)p.hkv * D;
-    const __nv_bfloat16* kb = p.k + ((base + (int64_t)j * BS) * p.hkv + g) * D;
-    const __nv_bfloat16* vb = p.v + ((base + (int64_t)j * BS) * p.hkv + g) * D;
+    const __nv_bfloat16* kb = p.k + ((kbase + (int64_t)j * BS) * p.hkv + g) * D;
+    const __nv_bfloat16* vb = p.v + ((kbase + (int64_t)j * BS) * p.hkv + g) * D;
     for (int i = threadIdx.x; i < BS * CH; i += 128) {
       const int row = i / CH, ch = i % CH;
-      const bool ok = j * BS + row < L;
+      const bool ok = j * BS + row < Lk;
       cp_async16(tile_addr<D>(kt, row, ch), ok ? kb + row * rs + ch * 8 : (const void*)p.k, ok ? 16 : 0);
       cp_async16(tile_addr<D>(vt, row, ch), ok ? vb + row * rs + ch * 8 : (const void*)p.k, ok ? 16 : 0);
     }
@@ -302,8 +348,12 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
     const int t = t0 + threadIdx.x;
     int mult = 0;
     if (t < t_end) {
-      const int32_t* il = p.idx + ((base + t) * p.hkv + g) * p.S;
-      for (int e = 0; e < p.S; ++e) mult += il[e] == j;
+      if (p.cmp_kernel) {
+        mult = key_bound(p, t, Lk) >= j * BS;
+      } else {
+        const int32_t* il = p.idx + ((base + t) * p.hkv + g) * p.S;
+        for (int e = 0; e < p.S; ++e) mult += il[e] == j;
+      }
     }
     const unsigned bal = __ballot_sync(0xffffffffu, mult > 0);
     if (lane == 0) s_wcount[warp] = __popc(bal);
@@ -371,6 +421,7 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
     cp_async_wait<NSTAGE - 1>();
     __syncthreads();
     const int t = s_tok[i] >> 7;
+    const int tb = key_bound(p, t, Lk);
     const float mult = (float)(s_tok[i] & 127);
     const uint32_t qt = ring + (i % NSTAGE) * STAGE, dt = qt + kRowsBytes;
     const float* lrow = reinterpret_cast<const float*>(smem + 2 * kTileBytes + (i % NSTAGE) * STAGE + 2 * kRowsBytes);
@@ -393,7 +444,7 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
       for (int q = 0; q < 4; ++q) {
         const int head = nt * 8 + hc + (q & 1);
         const int key = q < 2 ? key_lo : key_hi;
-        const float pe = key <= t ? ex2(st[nt][q] * p.scale_log2 - lse_to_log2(lrow[head])) : 0.f;
+        const float pe = key <= tb ? ex2(st[nt][q] * p.scale_log2 - lse_to_log2(lrow[head])) : 0.f;
         pr[nt][q] = pe * mult;
         ds[nt][q] = pe * mult * (dpt[nt][q] - drow[head]);
         big = fmaxf(big, fabsf(ds[nt][q]));
@@ -410,7 +461,7 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
     split_bf16x2(ds[1][2], ds[1][3], sh[3], sl[3]);
     pv_16keys<D>(dv, ph, dt, 0, lane);  // dV_w += P^T . dO_t
     pv_16keys<D>(dk, sh, qt, 0, lane);  // dK_w += dS^T . Q_t
-    if (__any_sync(0xffffffffu, pbig > kSplitAbove)) pv_16keys<D>(dv, pl, dt, 0, lane);
+    if (__any_sync(0xffffffffu, pbig > kSplitPAbove)) pv_16keys<D>(dv, pl, dt, 0, lane);
     if (__any_sync(0xffffffffu, big > kSplitAbove)) pv_16keys<D>(dk, sl, qt, 0, lane);
     __syncthreads();  // the stage is refilled at the next iteration
   }
@@ -435,16 +486,22 @@ __global__ void __launch_bounds__(256) sparse_bwd_reduce(const BwdParams p) {
   const int bg = blockIdx.x / p.nb, j = blockIdx.x % p.nb;
   const int b = bg / p.hkv, g = bg % p.hkv;
   const int L = seq_len(p.seqs, b);
-  if (j * BS >= L) return;
-  const int m = j / kGroup;
-  int first = 0;
-  for (int mm = 0; mm < m; ++mm) first += min(kGroup, p.nb - mm * kGroup) * (p.n_chunks - mm);
-  first += (j - m * kGroup) * (p.n_chunks - m);
+  const int Lk = key_len(p, L);
+  if (j * BS >= Lk) return;
+  int m, first = 0;
+  if (p.cmp_kernel) {
+    for (int jj = 0; jj < j; ++jj) first += p.n_chunks - first_query(p, jj) / kChunk;
+    m = first_query(p, j) / kChunk;
+  } else {
+    m = j / kGroup;
+    for (int mm = 0; mm < m; ++mm) first += min(kGroup, p.nb - mm * kGroup) * (p.n_chunks - mm);
+    first += (j - m * kGroup) * (p.n_chunks - m);
+  }
   int n_items = 1;
   while (m + n_items < p.n_chunks && (m + n_items) * kChunk < L) ++n_items;
   const float4* src = reinterpret_cast<const float4*>(p.part + ((size_t)bg * p.items_per_bg + first) * 2 * BS * D);
   constexpr int N4 = 2 * BS * D / 4;
-  const int64_t base = seq_start(p.seqs, b);
+  const int64_t base = key_base(p, b);
   for (int e = threadIdx.x; e < N4; e += 256) {
     float4 a = src[e];
     for (int it = 1; it < n_items; ++it) {
@@ -455,7 +512,7 @@ __global__ void __launch_bounds__(256) sparse_bwd_reduce(const BwdParams p) {
       a.w += x.w;
     }
     const int which = e / (BS * D / 4), key = (e / (D / 4)) % BS, col = (e % (D / 4)) * 4;
-    if (j * BS + key >= L) continue;
+    if (j * BS + key >= Lk) continue;
     const float f = which ? 1.f : p.scale;
     __nv_bfloat16* dst = (which ? p.dv : p.dk) + ((base + (int64_t)j * BS + key) * p.hkv + g) * D + col;
     uint2 w;
@@ -470,17 +527,92 @@ struct BwdLayout {
   size_t dsum, part, total;
 };
 
-BwdLayout bwd_layout(const Seqs& s, int h, int hkv) {
+// cmp_kernel > 0: the compressed branch (keys are the n_c(L) compressed rows).
+BwdLayout bwd_layout(const Seqs& s, int h, int hkv, int cmp_kernel = 0, int cmp_stride = 0) {
   BwdLayout l{};
   const int Lmax = s.max_len;
   l.n_chunks = (Lmax + kChunk - 1) / kChunk;
-  l.nb = (Lmax + kBS - 1) / kBS;
-  for (int m = 0; m < l.n_chunks; ++m) l.items_per_bg += std::min(kGroup, l.nb - m * kGroup) * (l.n_chunks - m);
+  if (cmp_kernel) {
+    const int nk = Lmax >= cmp_kernel ? (Lmax - cmp_kernel) / cmp_stride + 1 : 0;
+    l.nb = (nk + kBS - 1) / kBS;
+    for (int j = 0; j < l.nb; ++j) l.items_per_bg += l.n_chunks - (cmp_stride * kBS * j + cmp_kernel - 1) / kChunk;
+  } else {
+    l.nb = (Lmax + kBS - 1) / kBS;
+    for (int m = 0; m < l.n_chunks; ++m) l.items_per_bg += std::min(kGroup, l.nb - m * kGroup) * (l.n_chunks - m);
+  }
   auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
   l.dsum = 0;
   l.part = a256((size_t)s.tokens * h * 4);
   l.total = a256(l.part + (size_t)s.n_seqs * hkv * l.items_per_bg * 2 * kBS * kD * 4);
   return l;
+}
+
+cudaError_t run_bwd(const BwdParams& p0, const BwdLayout& l, void* workspace, cudaStream_t st) {
+  BwdParams p = p0;
+  p.dsum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.dsum);
+  p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.part);
+  p.r = p.h / p.hkv;
+  p.scale_log2 = p.scale * kLog2e;
+  p.n_chunks = l.n_chunks;
+  p.nb = l.nb;
+  p.items_per_bg = l.items_per_bg;
+  const Seqs& s = p.seqs;
+  constexpr int NS_Q = 2, NS_KV = 3;
+  constexpr int dq_bytes = 4 * NS_Q * 2 * 16 * kD * 2;
+  static_assert(dq_bytes >= 3 * 16 * (kD + 8) * 4, "dq fold needs the ring's shared memory");
+  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_dq<NS_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_bytes);
+  if (e != cudaSuccess) return e;
+  sparse_bwd_dq<NS_Q><<<dim3((unsigned)s.tokens, p.hkv), 128, dq_bytes, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t items = (int64_t)s.n_seqs * p.hkv * l.items_per_bg;
+  if (items > 0) {
+    constexpr int kv_bytes = dkv_smem_bytes<NS_KV>();
+    e = cudaFuncSetAttribute(sparse_bwd_dkv<NS_KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
+    if (e != cudaSuccess) return e;
+    sparse_bwd_dkv<NS_KV><<<(unsigned)items, 128, kv_bytes, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    sparse_bwd_reduce<<<(unsigned)((int64_t)s.n_seqs * p.hkv * l.nb), 256, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+// Backward of the mean pooling: token row t of sequence b receives, from each window c
+// of that sequence with c*stride <= t < c*stride + kernel, the window's gradient / kernel.
+// One thread per (token, kv-head, 8 columns).
+__global__ void __launch_bounds__(256) compress_bwd_kernel(const __nv_bfloat16* __restrict__ dkc,
+                                                           __nv_bfloat16* __restrict__ dk, Seqs s, int hkv, int d,
+                                                           int kernel, int stride) {
+  const int cpr = d / 8;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= s.tokens * hkv * cpr) return;
+  const int ch = (int)(i % cpr);
+  const int64_t rg = i / cpr;
+  const int g = (int)(rg % hkv);
+  const int64_t tok = rg / hkv;
+  const int sq = seq_of_token(s, tok);
+  const int t = (int)(tok - seq_start(s, sq));
+  const int n_c = num_cmp(seq_len(s, sq), kernel, stride);
+  const int64_t c0 = cmp_offset(s, sq, kernel, stride);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int c_hi = min(t / stride, n_c - 1);
+  for (int c = max(0, (t - kernel) / stride); c <= c_hi; ++c) {
+    if (c * stride > t || t >= c * stride + kernel) continue;
+    const uint4 w = *reinterpret_cast<const uint4*>(dkc + ((c0 + c) * hkv + g) * d + ch * 8);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h2[e]);
+      acc[2 * e] += f.x;
+      acc[2 * e + 1] += f.y;
+    }
+  }
+  const float inv = 1.f / (float)kernel;
+  uint4 o;
+  o.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  o.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(dk + (tok * hkv + g) * d + ch * 8) = o;
 }
 
 }  // namespace
@@ -490,11 +622,13 @@ size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv) {
   return bwd_layout(s, h, hkv).total;
 }
 
-cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const void* v, const int32_t* idx, int S,
-                              int h, int hkv, float scale, const void* o, const float* lse, const void* dout,
-                              void* dq, void* dk, void* dv, void* workspace, cudaStream_t st) {
-  if (s.tokens == 0) return cudaSuccess;
-  const BwdLayout l = bwd_layout(s, h, hkv);
+size_t cmp_attn_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int kernel, int stride) {
+  if (s.tokens == 0 || s.max_len == 0) return 0;
+  return bwd_layout(s, h, hkv, kernel, stride).total;
+}
+
+static BwdParams bwd_params(const Seqs& s, const void* q, const void* k, const void* v, int h, int hkv, float scale,
+                            const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv) {
   BwdParams p{};
   p.q = (const __nv_bfloat16*)q;
   p.k = (const __nv_bfloat16*)k;
@@ -502,37 +636,43 @@ cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const
   p.o = (const __nv_bfloat16*)o;
   p.dout = (const __nv_bfloat16*)dout;
   p.lse = lse;
-  p.idx = idx;
   p.dq = (__nv_bfloat16*)dq;
   p.dk = (__nv_bfloat16*)dk;
   p.dv = (__nv_bfloat16*)dv;
-  p.dsum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.dsum);
-  p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.part);
   p.seqs = s;
   p.h = h;
   p.hkv = hkv;
-  p.S = S;
-  p.r = h / hkv;
   p.scale = scale;
-  p.scale_log2 = scale * kLog2e;
-  p.n_chunks = l.n_chunks;
-  p.nb = l.nb;
-  p.items_per_bg = l.items_per_bg;
+  return p;
+}
 
-  constexpr int NS_Q = 2, NS_KV = 3;
-  constexpr int dq_bytes = 4 * NS_Q * 2 * 16 * kD * 2;
-  static_assert(dq_bytes >= 3 * 16 * (kD + 8) * 4, "dq fold needs the ring's shared memory");
-  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_dq<NS_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_bytes);
-  if (e != cudaSuccess) return e;
-  sparse_bwd_dq<NS_Q><<<dim3((unsigned)s.tokens, hkv), 128, dq_bytes, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  constexpr int kv_bytes = dkv_smem_bytes<NS_KV>();
-  e = cudaFuncSetAttribute(sparse_bwd_dkv<NS_KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
-  if (e != cudaSuccess) return e;
-  const int64_t items = (int64_t)s.n_seqs * hkv * l.items_per_bg;
-  sparse_bwd_dkv<NS_KV><<<(unsigned)items, 128, kv_bytes, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  sparse_bwd_reduce<<<(unsigned)((int64_t)s.n_seqs * hkv * l.nb), 256, 0, st>>>(p);
+cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const void* v, const int32_t* idx, int S,
+                              int h, int hkv, float scale, const void* o, const float* lse, const void* dout,
+                              void* dq, void* dk, void* dv, void* workspace, cudaStream_t st) {
+  if (s.tokens == 0) return cudaSuccess;
+  BwdParams p = bwd_params(s, q, k, v, h, hkv, scale, o, lse, dout, dq, dk, dv);
+  p.idx = idx;
+  p.S = S;
+  return run_bwd(p, bwd_layout(s, h, hkv), workspace, st);
+}
+
+cudaError_t launch_cmp_attn_bwd(const Seqs& s, const void* q, const void* k_cmp, const void* v_cmp, int h, int hkv,
+                                int kernel, int stride, float scale, const void* o, const float* lse,
+                                const void* dout, void* dq, void* dk_cmp, void* dv_cmp, void* workspace,
+                                cudaStream_t st) {
+  if (s.tokens == 0) return cudaSuccess;
+  BwdParams p = bwd_params(s, q, k_cmp, v_cmp, h, hkv, scale, o, lse, dout, dq, dk_cmp, dv_cmp);
+  p.cmp_kernel = kernel;
+  p.cmp_stride = stride;
+  return run_bwd(p, bwd_layout(s, h, hkv, kernel, stride), workspace, st);
+}
+
+cudaError_t launch_compress_bwd(const Seqs& s, const void* dk_cmp, int hkv, int d, int kernel, int stride, void* dk,
+                                cudaStream_t st) {
+  const int64_t n = s.tokens * hkv * (d / 8);
+  if (n == 0) return cudaSuccess;
+  compress_bwd_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>((const __nv_bfloat16*)dk_cmp, (__nv_bfloat16*)dk,
+                                                                    s, hkv, d, kernel, stride);
   return cudaGetLastError();
 }
 

@@ -136,3 +136,26 @@ def test_sparse_bwd_rejects_unsupported():
     assert lib.nsa_sparse_bwd(*args(_shape(), wsb=16)) == 1
     assert b"workspace" in lib.nsa_last_error()
     assert lib.nsa_sparse_bwd(*args(_shape(batch=0))) == 0
+
+
+@pytest.mark.parametrize("B,T,h,hkv", [(1, 65536, 64, 4), (2, 4500, 16, 1), (3, 31, 8, 2), (1, 2048 + 31, 16, 16)])
+def test_cmp_attn_bwd_workspace_size(B, T, h, hkv):
+    """Work items: (compressed key block j, 2048-query chunk c) with the chunk reaching the
+    first query that sees block j (query 1024 j + 31 for windows of 32 at step 16)."""
+    s = _shape(batch=B, seqlen=T, h=h, h_kv=hkv)
+    n_c = (T - 32) // 16 + 1 if T >= 32 else 0
+    nb, nch = -(-n_c // 64), -(-T // 2048)
+    items = sum(1 for j in range(nb) for c in range(nch) if (c + 1) * 2048 > 1024 * j + 31)
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    want = a256(a256(B * T * h * 4) + B * hkv * items * 2 * 64 * 128 * 4)
+    assert nsa.nsa_cmp_attn_bwd_workspace_size(s, 32, 16) == want
+
+
+def test_cmp_attn_bwd_rejects_unsupported():
+    lib = nsa.load()
+    args = lambda s, ws=FAKE, wsb=1 << 40: (ctypes.byref(s), FAKE, FAKE, FAKE, 32, 16, 0.0, FAKE, FAKE, FAKE,  # noqa: E731
+                                            FAKE, FAKE, FAKE, ws, wsb, None)
+    assert lib.nsa_cmp_attn_bwd(*args(_shape(d=64))) == 2
+    assert lib.nsa_cmp_attn_bwd(*args(_shape(seqlen=70000))) == 2
+    assert lib.nsa_cmp_attn_bwd(*args(_shape(), wsb=8)) == 1
+    assert lib.nsa_compress_bwd(ctypes.byref(_shape(d=12)), FAKE, 32, 16, FAKE, None) == 2

@@ -282,6 +282,65 @@ def test_sparse_bwd_full_size_sampled():
     assert_close(gv[torch.from_numpy(kr).cuda()], rv, what="dv sampled")
 
 
+# --------------------------------------------------------------------------- S7 and S1 backward
+@pytest.mark.parametrize("H,hkv", [(16, 1), (16, 4), (8, 8), (64, 4)])
+def test_cmp_attn_bwd_varlen(H, hkv):
+    """Ragged lengths (no window, one window, several key blocks and query chunks); both
+    sides take the oracle's forward (o rounded to bf16, lse)."""
+    lengths = [10, 31, 32, 47, 500, 2100, 4500]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(41)
+    q, do = gen.normal(rng, (cu[-1], H, 128), "bf16"), gen.normal(rng, (cu[-1], H, 128), "bf16")
+    k, v = gen.normal(rng, (cu[-1], hkv, 128), "bf16"), gen.normal(rng, (cu[-1], hkv, 128), "bf16")
+    _, kc = orc.compress(k, cu)
+    _, vc = orc.compress(v, cu)
+    o64, lse64 = orc.cmp_attn(q, kc, vc, cu)
+    o = gen.f32_to_bf16_bits(o64.astype(np.float32))
+    lse = lse64.astype(np.float32)
+    gq, gk, gv = nsa.nsa_cmp_attn_bwd(dev(q), dev(kc), dev(vc), dev(o), dev(lse), dev(do), hkv, cu_seqlens=dev(cu),
+                                      max_seqlen=max(lengths))
+    gk_tok = nsa.nsa_compress_bwd(gk, int(cu[-1]), cu_seqlens=dev(cu), max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.cmp_attn_bwd(q, kc, vc, do, cu, o=o)
+    assert_close(gq, rq, what="cmp dq")
+    assert_close(gk, rk, what="cmp dk")
+    assert_close(gv, rv, what="cmp dv")
+    # the pooling backward on the GPU's own window gradient
+    assert_close(gk_tok, orc.compress_bwd(as_f64(host(gk)), cu), atol=1e-3, rtol=1e-2, what="compress bwd")
+
+
+def test_cmp_attn_bwd_layer_size_sampled():
+    """T=65536, H=64, Hkv=4 (4095 compressed keys): GPU forward then backward; dq on sampled
+    rows, d k_cmp / d v_cmp on late compressed rows (the oracle visits every token that
+    reaches them), and determinism."""
+    w = gen.layer()
+    cu, T = w.cu_seqlens, w.tokens
+    do = gen.normal(_rng(42), (T, 64, 128), "bf16")
+    dq_, dk_, dv_ = dev(w.q), dev(w.k), dev(w.v)
+    kc = nsa.nsa_compress_k(dk_)
+    vc = nsa.nsa_compress_k(dv_)
+    lse = torch.empty((T, 64), dtype=torch.float32, device="cuda")
+    o = nsa.nsa_cmp_attn_fwd(dq_, kc, vc, 4, lse=lse)
+    gq, gk, gv = nsa.nsa_cmp_attn_bwd(dq_, kc, vc, o, lse, dev(do), 4)
+    g2 = nsa.nsa_cmp_attn_bwd(dq_, kc, vc, o, lse, dev(do), 4)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    for a, b in zip((gq, gk, gv), g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    kch, vch = host(kc), host(vc)
+    qr = np.array([0, 31, 32, 1000, 33333, 65535])
+    kr = np.array([4088, 4094])
+    need = np.unique(np.concatenate([qr, np.arange(16 * 4088 + 31, T)]))
+    o_ref = np.zeros((T, 64, 128), np.uint16)
+    o64, _ = orc.cmp_attn(w.q, kch, vch, cu, rows=need)
+    o_ref[need] = gen.f32_to_bf16_bits(o64.astype(np.float32))
+    rq, _, _ = orc.cmp_attn_bwd(w.q, kch, vch, do, cu, q_rows=qr, want_dkv=False, o=o_ref)
+    _, rk, rv = orc.cmp_attn_bwd(w.q, kch, vch, do, cu, kv_rows=kr, want_dq=False, o=o_ref)
+    assert_close(gq[torch.from_numpy(qr).cuda()], rq, what="cmp dq sampled")
+    assert_close(gk[torch.from_numpy(kr).cuda()], rk, what="cmp dk sampled")
+    assert_close(gv[torch.from_numpy(kr).cuda()], rv, what="cmp dv sampled")
+
+
 # --------------------------------------------------------------------------- NOSA stage 2
 def test_cis_block_scores():
     lengths = [10, 31, 32, 47, 100, 700, 5000]
