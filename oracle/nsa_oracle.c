@@ -1065,6 +1065,138 @@ int nsa_oracle_gate_combine(const double* o_cmp, const double* o_slc, const doub
   return 0;
 }
 
+/* Backward of S8 (the sliding window): the derivative of the forward above; per (token,
+ * head) row over keys max(0, t-window+1) .. t, with the formulas of the S5 backward
+ * (row_probs_grads; D = dO . o_in when o_in is given).  dq for q_rows (all when NULL;
+ * n_q_rows < 0 skips), dk / dv for the token rows kv_rows (all when NULL; n_kv_rows < 0
+ * skips); thread-private accumulators summed in thread order. */
+int nsa_oracle_swa_bwd(const void* q, const void* k, const void* v, const void* dout, const void* o_in, int dtype,
+                       const int32_t* cu, int n_seqs, int h, int hkv, int d, int window, double scale,
+                       const int64_t* q_rows, int64_t n_q_rows, double* dq, const int64_t* kv_rows,
+                       int64_t n_kv_rows, double* dk, double* dv) {
+  if (h % hkv || window <= 0) return 1;
+  const int64_t total = cu[n_seqs];
+  const int r = h / hkv;
+  if (n_q_rows >= 0 && !q_rows) n_q_rows = total;
+  if (n_q_rows > 0) {
+#pragma omp parallel
+    {
+      int* keys = (int*)malloc(sizeof(int) * (size_t)(window + 1));
+      double* p = (double*)malloc(sizeof(double) * (size_t)(window + 1));
+      double* ds = (double*)malloc(sizeof(double) * (size_t)(window + 1));
+#pragma omp for schedule(dynamic, 8)
+      for (int64_t rr = 0; rr < n_q_rows; ++rr) {
+        int64_t tok = q_rows ? q_rows[rr] : rr;
+        int sq = seq_of(cu, n_seqs, tok);
+        int t = (int)(tok - cu[sq]);
+        int lo = t - window + 1 > 0 ? t - window + 1 : 0, n = 0;
+        for (int tau = lo; tau <= t; ++tau) keys[n++] = tau;
+        for (int hh = 0; hh < h; ++hh) {
+          int g = hh / r;
+          double* out = dq + ((size_t)rr * h + hh) * d;
+          for (int i = 0; i < d; ++i) out[i] = 0.0;
+          row_probs_grads(q, k, v, dout, o_in, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
+          for (int e = 0; e < n; ++e) {
+            size_t kr = ((size_t)(cu[sq] + keys[e]) * hkv + g) * d;
+            for (int i = 0; i < d; ++i) out[i] += scale * ds[e] * ld(k, dtype, kr + i);
+          }
+        }
+      }
+      free(keys);
+      free(p);
+      free(ds);
+    }
+  }
+  if (n_kv_rows >= 0 && !kv_rows) n_kv_rows = total;
+  if (n_kv_rows <= 0) return 0;
+  int64_t* slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)(total + 1));
+  for (int64_t i = 0; i < total; ++i) slot[i] = kv_rows ? -1 : i;
+  if (kv_rows)
+    for (int64_t i = 0; i < n_kv_rows; ++i) slot[kv_rows[i]] = i;
+  const size_t acc_len = (size_t)n_kv_rows * hkv * d;
+  for (size_t i = 0; i < acc_len; ++i) dk[i] = dv[i] = 0.0;
+  int nthr = 1;
+#ifdef _OPENMP
+  nthr = omp_get_max_threads();
+#endif
+  double* acc = (double*)calloc((size_t)nthr * 2 * acc_len, sizeof(double));
+#pragma omp parallel num_threads(nthr)
+  {
+    int me = 0;
+#ifdef _OPENMP
+    me = omp_get_thread_num();
+#endif
+    double* mk = acc + (size_t)me * 2 * acc_len;
+    double* mv = mk + acc_len;
+    int* keys = (int*)malloc(sizeof(int) * (size_t)(window + 1));
+    double* p = (double*)malloc(sizeof(double) * (size_t)(window + 1));
+    double* ds = (double*)malloc(sizeof(double) * (size_t)(window + 1));
+#pragma omp for schedule(static)
+    for (int64_t tok = 0; tok < total; ++tok) {
+      int sq = seq_of(cu, n_seqs, tok);
+      int t = (int)(tok - cu[sq]);
+      int lo = t - window + 1 > 0 ? t - window + 1 : 0, n = 0, hit = 0;
+      for (int tau = lo; tau <= t; ++tau) {
+        keys[n++] = tau;
+        hit |= slot[cu[sq] + tau] >= 0;
+      }
+      if (!hit) continue;
+      for (int hh = 0; hh < h; ++hh) {
+        int g = hh / r;
+        row_probs_grads(q, k, v, dout, o_in, dtype, tok, hh, h, hkv, d, g, cu[sq], keys, n, scale, p, ds);
+        for (int e = 0; e < n; ++e) {
+          int64_t sl = slot[cu[sq] + keys[e]];
+          if (sl < 0) continue;
+          double* ak = mk + ((size_t)sl * hkv + g) * d;
+          double* av = mv + ((size_t)sl * hkv + g) * d;
+          for (int i = 0; i < d; ++i) {
+            ak[i] += scale * ds[e] * ld(q, dtype, ((size_t)tok * h + hh) * d + i);
+            av[i] += p[e] * ld(dout, dtype, ((size_t)tok * h + hh) * d + i);
+          }
+        }
+      }
+    }
+    free(keys);
+    free(p);
+    free(ds);
+  }
+  for (int th = 0; th < nthr; ++th) {
+    const double* mk = acc + (size_t)th * 2 * acc_len;
+    const double* mv = mk + acc_len;
+    for (size_t i = 0; i < acc_len; ++i) {
+      dk[i] += mk[i];
+      dv[i] += mv[i];
+    }
+  }
+  free(acc);
+  free(slot);
+  return 0;
+}
+
+/* Backward of S9: with g_i = sigmoid(a_i) and o = sum_i g_i o_i, the branch gradients
+ * are g_i dO and the logit gradients g_i (1 - g_i) (dO . o_i), per (token, head). */
+int nsa_oracle_gate_bwd(const double* o_cmp, const double* o_slc, const double* o_swa, const float* gates,
+                        const double* dout, int64_t n_rows, int h, int d, double* d_cmp, double* d_slc,
+                        double* d_swa, double* d_gates) {
+#pragma omp parallel for schedule(static)
+  for (int64_t rr = 0; rr < n_rows; ++rr)
+    for (int hh = 0; hh < h; ++hh) {
+      size_t gi = ((size_t)rr * h + hh) * 3;
+      const double* br[3] = {o_cmp, o_slc, o_swa};
+      double* db[3] = {d_cmp, d_slc, d_swa};
+      for (int b = 0; b < 3; ++b) {
+        double g = sigmoid(gates[gi + b]), dot = 0.0;
+        for (int i = 0; i < d; ++i) {
+          size_t x = ((size_t)rr * h + hh) * d + i;
+          db[b][x] = g * dout[x];
+          dot += dout[x] * br[b][x];
+        }
+        d_gates[gi + b] = g * (1.0 - g) * dot;
+      }
+    }
+  return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* S6: one decode step.  [NOSA-Parts] "how decoding uses only 64 KV blocks": the
  * newest query (position L-1; the cache already holds its key and value) is scored

@@ -362,6 +362,45 @@ def gate_combine(o_cmp, o_slc, o_swa, gates):
     return out
 
 
+def swa_bwd(q, k, v, do, cu, window=512, scale=None, q_rows=None, kv_rows=None, want_dq=True, want_dkv=True,
+            o=None):
+    """Backward of S8: (dq [q_rows, h, d], dk, dv [kv_rows, hkv, d]) fp64; o optional (D = dO . o)."""
+    q, k, v, do, cu = (np.ascontiguousarray(q), np.ascontiguousarray(k), np.ascontiguousarray(v),
+                       np.ascontiguousarray(do), _i32(cu))
+    if do.dtype != q.dtype or do.shape != q.shape:
+        raise ValueError("do must match q in dtype and shape")
+    if o is not None:
+        o = np.ascontiguousarray(o)
+        if o.dtype != q.dtype or o.shape != q.shape:
+            raise ValueError("o must match q in dtype and shape")
+    tot, h, d = q.shape
+    hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    qr, nq = _rows(q_rows, tot)
+    kr, nkv = _rows(kv_rows, tot)
+    nq = nq if want_dq else -1
+    nkv = nkv if want_dkv else -1
+    dq = np.zeros((max(nq, 0), h, d), np.float64)
+    dk = np.zeros((max(nkv, 0), hkv, d), np.float64)
+    dv = np.zeros((max(nkv, 0), hkv, d), np.float64)
+    _check(_load().nsa_oracle_swa_bwd(_p(q), _p(k), _p(v), _p(do), _p(o), _dt(q), _p(cu), len(cu) - 1, h, hkv, d,
+                                      window, ctypes.c_double(scale), _p(qr), ctypes.c_int64(nq), _p(dq), _p(kr),
+                                      ctypes.c_int64(nkv), _p(dk), _p(dv)), "swa_bwd")
+    return (dq if want_dq else None), (dk if want_dkv else None), (dv if want_dkv else None)
+
+
+def gate_bwd(o_cmp, o_slc, o_swa, gates, do):
+    """Backward of S9: (d o_cmp, d o_slc, d o_swa [n, h, d], d gate logits [n, h, 3]) fp64."""
+    o_cmp, o_slc, o_swa, do = (np.ascontiguousarray(np.asarray(a, np.float64)) for a in (o_cmp, o_slc, o_swa, do))
+    gates = np.ascontiguousarray(np.asarray(gates, np.float32))
+    n, h, d = o_cmp.shape
+    outs = [np.zeros_like(o_cmp) for _ in range(3)]
+    dg = np.zeros((n, h, 3), np.float64)
+    _check(_load().nsa_oracle_gate_bwd(_p(o_cmp), _p(o_slc), _p(o_swa), _p(gates), _p(do), ctypes.c_int64(n), h, d,
+                                       _p(outs[0]), _p(outs[1]), _p(outs[2]), _p(dg)), "gate_bwd")
+    return outs[0], outs[1], outs[2], dg
+
+
 def decode(q, k_cache, v_cache, kc_cache, seqlens, kernel=32, stride=16, block_size=64, n_init=1,
            n_local=2, k=64, scale=None, idx_in=None, want_scores=False):
     """S6: one decode step; returns (idx [B,hkv,k], o [B,h,d] fp64[, scores [B,hkv,nb]])."""
