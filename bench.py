@@ -297,6 +297,31 @@ def bench_cmp_bwd(torch, nsa, device, steps, warmup, flush, peaks):
             "launches_per_step": 5}
 
 
+def bench_swa_bwd(torch, nsa, device, steps, warmup, flush, peaks):
+    """Backward of the sliding-window branch (window 512) and of the gate, layer shape."""
+    from sparse_attention_compress_gb300 import _lib
+    w = gen.layer()
+    q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
+    do = dev(torch, gen.normal(gen.rng_for(4, 98), (w.tokens, w.h, w.d), "bf16"), device)
+    lse = torch.empty((w.tokens, w.h), dtype=torch.float32, device=device)
+    o = nsa.nsa_swa_fwd(q, k, v, 512, lse=lse)
+    shp = _lib.make_shape(w.tokens, w.h, w.hkv, w.d, _lib.NSA_BF16, batch=1, seqlen=w.tokens)
+    ws = torch.empty(nsa.nsa_swa_bwd_workspace_size(shp, 512), dtype=torch.uint8, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ms = float(np.mean(timed(torch, lambda: nsa.nsa_swa_bwd(q, k, v, o, lse, do, 512, workspace=ws, dq=dq, dk=dk,
+                                                             dv=dv), steps, warmup, flush)))
+    t = np.arange(w.tokens)
+    flops = float(np.minimum(t + 1, 512).sum()) * w.h * 2 * w.d * 5
+    logits = dev(torch, w.gates, device)
+    msg = float(np.mean(timed(torch, lambda: nsa.nsa_gate_combine_bwd(do, o, o, o, logits), steps, warmup, flush)))
+    gbytes = w.tokens * w.h * (w.d * 2 * 7 + 3 * 4 * 2)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "backward of the sliding window (512) and of the gate, layer T=65536 H=64 Hkv=4 d=128 bf16",
+            "swa_ms": ms, "swa_tflops": tf, "swa_frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "gate_ms": msg, "gate_gbs": gbytes / (msg * 1e-3) / 1e9,
+            "gate_hbm_frac": gbytes / (msg * 1e-3) / 1e9 / peaks["hbm_gbs"], "launches_per_step": 4}
+
+
 def bench_nosa(torch, nsa, device, steps, warmup, flush, peaks):
     """NOSA stage 2: CIS-weighted selected attention on the prefill workload, and the
     block CIS scores plus two-stage selection on the varlen selection workload."""
@@ -467,7 +492,7 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "cmp_bwd", "nosa", "decode", "decode_offload",
+    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "cmp_bwd", "swa_bwd", "nosa", "decode", "decode_offload",
                                                     "selection", "layer", "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
@@ -499,9 +524,10 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("prefill_bwd", "cmp_bwd", "nosa", "decode", "decode_offload", "selection", "layer",
+    if args.only in ("prefill_bwd", "cmp_bwd", "swa_bwd", "nosa", "decode", "decode_offload", "selection", "layer",
                      "block_sparse"):
-        fn = {"cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+        fn = {"swa_bwd": lambda: bench_swa_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
@@ -592,6 +618,12 @@ def main():
             line["gpu_launches"] += 5 * max(3, args.steps // 2)
         except Exception as e:
             line["cmp_bwd"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["swa_bwd"] = bench_swa_bwd(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush, peaks)
+            line["gpu_launches"] += 4 * max(3, args.steps // 2)
+        except Exception as e:
+            line["swa_bwd"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             line["nosa"] = bench_nosa(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush, peaks)

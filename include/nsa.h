@@ -178,6 +178,23 @@ NSA_API nsa_status nsa_cmp_attn_bwd(const nsa_shape* shape, const void* q, const
                                     const void* d_o, void* dq, void* dk_cmp, void* dv_cmp, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
 
+/* Backward of S8, the sliding window: the derivative of nsa_swa_fwd for an upstream dO
+ * (keys max(0, t-window+1) .. t; the formulas of nsa_sparse_bwd).  Arguments and layouts
+ * as nsa_sparse_bwd without the lists; workspace nsa_swa_bwd_workspace_size() bytes.
+ * Requires bf16, d 128, h/h_kv <= 16, 1 <= window <= 1984. */
+NSA_API size_t nsa_swa_bwd_workspace_size(const nsa_shape* shape, int window);
+NSA_API nsa_status nsa_swa_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v, int window,
+                               float scale, const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                               void* dv, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward of S9, the gate combine: with g_i = sigmoid(a_i) and o = sum_i g_i o_i, the
+ * branch gradients are g_i dO and the logit gradients g_i (1 - g_i) (dO . o_i).
+ *   d_o, o_cmp, o_slc, o_swa, d_cmp, d_slc, d_swa  [tokens, h, d] bf16
+ *   gate_logits, d_gate_logits  [tokens, h, 3] fp32.  d % 8 == 0, d <= 256. */
+NSA_API nsa_status nsa_gate_combine_bwd(int64_t tokens, int h, int d, const void* d_o, const void* o_cmp,
+                                        const void* o_slc, const void* o_swa, const float* gate_logits, void* d_cmp,
+                                        void* d_slc, void* d_swa, float* d_gate_logits, cudaStream_t stream);
+
 /* Backward of S1, the mean pooling: token row t of a sequence receives, from every
  * compressed window c of that sequence containing it (c*stride <= t < c*stride+kernel),
  * the window's gradient divided by kernel; tokens in no window get 0.

@@ -48,6 +48,11 @@ _SIGS = {
     "nsa_cmp_attn_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                           _c_sz, _c_p], _c_int),
     "nsa_compress_bwd": ([_c_p, _c_p, _c_int, _c_int, _c_p, _c_p], _c_int),
+    "nsa_swa_bwd_workspace_size": ([_c_p, _c_int], _c_sz),
+    "nsa_swa_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p],
+                    _c_int),
+    "nsa_gate_combine_bwd": ([_c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p],
+                             _c_int),
     "nsa_sparse_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                         _c_sz, _c_p], _c_int),
     "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
@@ -355,6 +360,37 @@ def nsa_compress_bwd(dk_cmp, tokens, kernel=32, stride=16, *, cu_seqlens=None, m
     _check(load().nsa_compress_bwd(ctypes.byref(shp), _ptr(dk_cmp), kernel, stride, _ptr(out), _stream(stream)),
            "nsa_compress_bwd")
     return out
+
+
+def nsa_swa_bwd_workspace_size(shape: NsaShape, window: int = 512) -> int:
+    return int(load().nsa_swa_bwd_workspace_size(ctypes.byref(shape), window))
+
+
+def nsa_swa_bwd(q, k, v, o, lse, d_o, window=512, scale=0.0, *, cu_seqlens=None, max_seqlen=None, workspace=None,
+                dq=None, dk=None, dv=None, stream=None):
+    """Backward of S8: (dq, dk, dv) shaped like q, k, v from the forward's o and lse."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    if workspace is None:
+        ws = nsa_swa_bwd_workspace_size(shp, window)
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(load().nsa_swa_bwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), window, float(scale), _ptr(o),
+                              _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                              workspace.numel(), _stream(stream)), "nsa_swa_bwd")
+    return dq, dk, dv
+
+
+def nsa_gate_combine_bwd(d_o, o_cmp, o_slc, o_swa, gate_logits, *, stream=None):
+    """Backward of S9: (d o_cmp, d o_slc, d o_swa, d gate_logits)."""
+    tokens, h, d = d_o.shape
+    outs = [torch.empty_like(d_o) for _ in range(3)]
+    dg = torch.empty_like(gate_logits)
+    _check(load().nsa_gate_combine_bwd(tokens, h, d, _ptr(d_o), _ptr(o_cmp), _ptr(o_slc), _ptr(o_swa),
+                                       _ptr(gate_logits), _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(dg),
+                                       _stream(stream)), "nsa_gate_combine_bwd")
+    return outs[0], outs[1], outs[2], dg
 
 
 def nsa_cmp_attn_fwd(q, k_cmp, v_cmp, h_kv, kernel=32, stride=16, scale=0.0, *, cu_seqlens=None,

@@ -284,6 +284,64 @@ nsa_status nsa_compress_bwd(const nsa_shape* shape, const void* dk_cmp, int kern
                      "nsa_compress_bwd");
 }
 
+size_t nsa_swa_bwd_workspace_size(const nsa_shape* shape, int window) {
+  Seqs s;
+  if (make_seqs(shape, &s, "nsa_swa_bwd_workspace_size") != NSA_OK || window < 1 || window > 1984) return 0;
+  return swa_bwd_workspace_bytes(s, shape->h, shape->h_kv, window);
+}
+
+nsa_status nsa_swa_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v, int window, float scale,
+                       const void* o, const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
+  NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_swa_bwd: bf16 only");
+  NSA_REQUIRE(shape->d == 128, NSA_ERR_UNSUPPORTED, "nsa_swa_bwd: d must be 128");
+  NSA_REQUIRE(shape->h / shape->h_kv <= 16, NSA_ERR_UNSUPPORTED, "nsa_swa_bwd: h/h_kv must be <= 16");
+  NSA_REQUIRE(window >= 1 && window <= 1984, NSA_ERR_UNSUPPORTED, "nsa_swa_bwd: window must be in [1, 1984]");
+  NSA_REQUIRE(s.max_len <= (1 << 24), NSA_ERR_UNSUPPORTED, "nsa_swa_bwd: sequences must be <= 2^24 tokens");
+  if (s.tokens == 0) return NSA_OK;
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(o);
+  NSA_PTR(d_o);
+  NSA_PTR(dq);
+  NSA_PTR(dk);
+  NSA_PTR(dv);
+  NSA_REQUIRE(lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) == 0, NSA_ERR_INVALID,
+              "nsa_swa_bwd: lse must be non-null and 4-byte aligned");
+  const size_t need = swa_bwd_workspace_bytes(s, shape->h, shape->h_kv, window);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_swa_bwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_swa_bwd: workspace %zu < %zu bytes", workspace_bytes,
+              need);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
+  return cuda_status(launch_swa_bwd(s, q, k, v, shape->h, shape->h_kv, window, scale, o, lse, d_o, dq, dk, dv,
+                                    workspace, stream),
+                     "nsa_swa_bwd");
+}
+
+nsa_status nsa_gate_combine_bwd(int64_t tokens, int h, int d, const void* d_o, const void* o_cmp, const void* o_slc,
+                                const void* o_swa, const float* gate_logits, void* d_cmp, void* d_slc, void* d_swa,
+                                float* d_gate_logits, cudaStream_t stream) {
+  NSA_REQUIRE(tokens >= 0 && h > 0 && d > 0, NSA_ERR_INVALID, "nsa_gate_combine_bwd: bad sizes");
+  NSA_REQUIRE(d % 8 == 0 && d <= 256, NSA_ERR_UNSUPPORTED, "nsa_gate_combine_bwd: d must be a multiple of 8, <= 256");
+  if (tokens == 0) return NSA_OK;
+  NSA_PTR(d_o);
+  NSA_PTR(o_cmp);
+  NSA_PTR(o_slc);
+  NSA_PTR(o_swa);
+  NSA_PTR(gate_logits);
+  NSA_PTR(d_cmp);
+  NSA_PTR(d_slc);
+  NSA_PTR(d_swa);
+  NSA_PTR(d_gate_logits);
+  return cuda_status(launch_gate_bwd(tokens * h, d, d_o, o_cmp, o_slc, o_swa, gate_logits, d_cmp, d_slc, d_swa,
+                                     d_gate_logits, stream),
+                     "nsa_gate_combine_bwd");
+}
+
 static nsa_status check_sparse_bwd(const nsa_shape* shape, int S, int block_size, Seqs* s, const char* fn) {
   if (nsa_status st = make_seqs(shape, s, fn)) return st;
   NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);

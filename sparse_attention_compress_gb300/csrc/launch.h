@@ -54,6 +54,15 @@ cudaError_t launch_cmp_attn_bwd(const Seqs& s, const void* q, const void* k_cmp,
                                 cudaStream_t st);
 cudaError_t launch_compress_bwd(const Seqs& s, const void* dk_cmp, int hkv, int d, int kernel, int stride, void* dk,
                                 cudaStream_t st);
+// Backward of the sigmoid gate combine over rows = tokens * h (bf16, d % 8 == 0).
+cudaError_t launch_gate_bwd(int64_t rows, int d, const void* dout, const void* o_cmp, const void* o_slc,
+                            const void* o_swa, const float* logits, void* d_cmp, void* d_slc, void* d_swa,
+                            float* d_logits, cudaStream_t st);
+// Backward of the sliding window (same kernels; keys max(0, t-window+1) .. t).
+size_t swa_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int window);
+cudaError_t launch_swa_bwd(const Seqs& s, const void* q, const void* k, const void* v, int h, int hkv, int window,
+                           float scale, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* workspace, cudaStream_t st);
 
 // mode 0: compressed-attention branch (keys/values are packed compressed rows)
 // mode 1: sliding-window branch

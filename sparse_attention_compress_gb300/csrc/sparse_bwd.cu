@@ -56,7 +56,13 @@ struct BwdParams {
   // reaches the compressed keys c < n_causal(t) and its list is every such block (idx is
   // unused); otherwise the keys are the tokens and query t reaches keys <= t of its list.
   int cmp_kernel, cmp_stride;
+  // sliding window (window > 0): query t reaches keys max(0, t-window+1) .. t (idx unused);
+  // one work item per key block covers every query that reaches it.
+  int window;
 };
+
+// First key query t may attend.
+__device__ __forceinline__ int key_lo(const BwdParams& p, int t) { return p.window ? max(0, t - p.window + 1) : 0; }
 
 // Key rows of sequence b start here; the sequence has key_len(L) of them.
 __device__ __forceinline__ int64_t key_base(const BwdParams& p, int b) {
@@ -111,6 +117,11 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src
 __device__ __forceinline__ void item_to_block(const BwdParams& p, int item, int& j, int& c, int& m) {
   const int n_chunks = p.n_chunks, nb = p.nb;
   int rem = item;
+  if (p.window) {
+    j = item;
+    c = m = 0;
+    return;
+  }
   if (p.cmp_kernel) {  // block j has chunks first_query(j) / kChunk .. n_chunks-1
     for (j = 0; j < nb; ++j) {
       m = first_query(p, j) / kChunk;
@@ -156,6 +167,7 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
   const int t = (int)(qrow - seq_start(p.seqs, sq));
   const int64_t kv_base = key_base(p, sq);
   const int tb = key_bound(p, t, key_len(p, seq_len(p.seqs, sq)));  // last reachable key
+  const int tl = key_lo(p, t);                                       // first reachable key
   const int hbase = g * r;
   const int rlo = lane >> 2, rhi = rlo + 8;
   const bool w0 = rlo < r, w1 = rhi < r;
@@ -186,7 +198,17 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
   // this warp's list: listed blocks whose slice starts at or before the bound (every
   // such block for the compressed branch)
   int cnt = 0;
-  if (p.cmp_kernel) {
+  if (p.window) {  // blocks whose slice overlaps [tl, tb]
+    const int j0 = tl / BS, j1 = tb / BS;
+    for (int jj = j0 + lane; jj <= j1; jj += 32) {
+      const int k0 = jj * BS + slice * 16;
+      const bool ok = k0 <= tb && k0 + 15 >= tl;
+      const unsigned m = __ballot_sync(__activemask(), ok);
+      if (ok) s_list[warp][cnt + __popc(m & ((1u << lane) - 1u))] = jj;
+      cnt += __popc(m);
+    }
+    cnt = __shfl_sync(0xffffffffu, cnt, 0);
+  } else if (p.cmp_kernel) {
     cnt = tb >= slice * 16 ? (tb - slice * 16) / BS + 1 : 0;
     for (int e = lane; e < cnt; e += 32) s_list[warp][e] = e;
   } else {
@@ -249,7 +271,8 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dq(const BwdParams p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t key = key0 + nt * 8 + (lane & 3) * 2 + (j & 1);
-        const float pe = key <= tb ? ex2((s[nt][j] + s2[nt][j]) * p.scale_log2 - (j < 2 ? L0 : L1)) : 0.f;
+        const float pe = key <= tb && key >= tl
+                             ? ex2((s[nt][j] + s2[nt][j]) * p.scale_log2 - (j < 2 ? L0 : L1)) : 0.f;
         ds[nt][j] = pe * ((dp[nt][j] + dp2[nt][j]) - (j < 2 ? d0 : d1));
         big = fmaxf(big, fabsf(ds[nt][j]));
       }
@@ -322,7 +345,8 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
   if (j * BS >= Lk || (c > m && c * kChunk >= L)) return;  // no partial is read for this item
   const int64_t base = seq_start(p.seqs, b);
   const int64_t kbase = key_base(p, b);
-  const int t_begin = max(first_query(p, j), c * kChunk), t_end = min((c + 1) * kChunk, L);
+  const int t_begin = p.window ? j * BS : max(first_query(p, j), c * kChunk);
+  const int t_end = p.window ? min(j * BS + BS - 1 + p.window, L) : min((c + 1) * kChunk, L);
 
   const uint32_t kt = smem_u32(smem), vt = kt + kTileBytes;
   const uint32_t ring = vt + kTileBytes;
@@ -348,7 +372,9 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
     const int t = t0 + threadIdx.x;
     int mult = 0;
     if (t < t_end) {
-      if (p.cmp_kernel) {
+      if (p.window) {
+        mult = key_lo(p, t) <= j * BS + BS - 1;  // t >= j*BS here
+      } else if (p.cmp_kernel) {
         mult = key_bound(p, t, Lk) >= j * BS;
       } else {
         const int32_t* il = p.idx + ((base + t) * p.hkv + g) * p.S;
@@ -414,14 +440,14 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
   }
   const int brow = (lane & 7) + ((lane >> 4) << 3), bcol = (lane >> 3) & 1;
   const int hc = (lane & 3) * 2;  // head columns hc, hc+1 (and hc+8, hc+9)
-  const int key_lo = j * BS + warp * 16 + (lane >> 2), key_hi = key_lo + 8;
+  const int krow_lo = j * BS + warp * 16 + (lane >> 2), krow_hi = krow_lo + 8;
   for (int i = 0; i < n; ++i) {
     if (i + NSTAGE - 1 < n) issue(i + NSTAGE - 1);
     cp_async_commit();
     cp_async_wait<NSTAGE - 1>();
     __syncthreads();
     const int t = s_tok[i] >> 7;
-    const int tb = key_bound(p, t, Lk);
+    const int tb = key_bound(p, t, Lk), tl = key_lo(p, t);
     const float mult = (float)(s_tok[i] & 127);
     const uint32_t qt = ring + (i % NSTAGE) * STAGE, dt = qt + kRowsBytes;
     const float* lrow = reinterpret_cast<const float*>(smem + 2 * kTileBytes + (i % NSTAGE) * STAGE + 2 * kRowsBytes);
@@ -443,8 +469,9 @@ __global__ void __launch_bounds__(128, 2) sparse_bwd_dkv(const BwdParams p) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int head = nt * 8 + hc + (q & 1);
-        const int key = q < 2 ? key_lo : key_hi;
-        const float pe = key <= tb ? ex2(st[nt][q] * p.scale_log2 - lse_to_log2(lrow[head])) : 0.f;
+        const int key = q < 2 ? krow_lo : krow_hi;
+        const float pe =
+            key <= tb && key >= tl ? ex2(st[nt][q] * p.scale_log2 - lse_to_log2(lrow[head])) : 0.f;
         pr[nt][q] = pe * mult;
         ds[nt][q] = pe * mult * (dpt[nt][q] - drow[head]);
         big = fmaxf(big, fabsf(ds[nt][q]));
@@ -489,7 +516,10 @@ __global__ void __launch_bounds__(256) sparse_bwd_reduce(const BwdParams p) {
   const int Lk = key_len(p, L);
   if (j * BS >= Lk) return;
   int m, first = 0;
-  if (p.cmp_kernel) {
+  if (p.window) {
+    m = 0;
+    first = j;
+  } else if (p.cmp_kernel) {
     for (int jj = 0; jj < j; ++jj) first += p.n_chunks - first_query(p, jj) / kChunk;
     m = first_query(p, j) / kChunk;
   } else {
@@ -498,7 +528,7 @@ __global__ void __launch_bounds__(256) sparse_bwd_reduce(const BwdParams p) {
     first += (j - m * kGroup) * (p.n_chunks - m);
   }
   int n_items = 1;
-  while (m + n_items < p.n_chunks && (m + n_items) * kChunk < L) ++n_items;
+  while (!p.window && m + n_items < p.n_chunks && (m + n_items) * kChunk < L) ++n_items;
   const float4* src = reinterpret_cast<const float4*>(p.part + ((size_t)bg * p.items_per_bg + first) * 2 * BS * D);
   constexpr int N4 = 2 * BS * D / 4;
   const int64_t base = key_base(p, b);
@@ -528,11 +558,14 @@ struct BwdLayout {
 };
 
 // cmp_kernel > 0: the compressed branch (keys are the n_c(L) compressed rows).
-BwdLayout bwd_layout(const Seqs& s, int h, int hkv, int cmp_kernel = 0, int cmp_stride = 0) {
+BwdLayout bwd_layout(const Seqs& s, int h, int hkv, int cmp_kernel = 0, int cmp_stride = 0, int window = 0) {
   BwdLayout l{};
   const int Lmax = s.max_len;
   l.n_chunks = (Lmax + kChunk - 1) / kChunk;
-  if (cmp_kernel) {
+  if (window) {  // one item per key block
+    l.nb = (Lmax + kBS - 1) / kBS;
+    l.items_per_bg = l.nb;
+  } else if (cmp_kernel) {
     const int nk = Lmax >= cmp_kernel ? (Lmax - cmp_kernel) / cmp_stride + 1 : 0;
     l.nb = (nk + kBS - 1) / kBS;
     for (int j = 0; j < l.nb; ++j) l.items_per_bg += l.n_chunks - (cmp_stride * kBS * j + cmp_kernel - 1) / kChunk;
@@ -615,7 +648,73 @@ __global__ void __launch_bounds__(256) compress_bwd_kernel(const __nv_bfloat16* 
   *reinterpret_cast<uint4*>(dk + (tok * hkv + g) * d + ch * 8) = o;
 }
 
+// Backward of the gate combine: with g_i = sigmoid(a_i) and o = sum_i g_i o_i, the branch
+// gradients are g_i dO and the logit gradients g_i (1 - g_i) (dO . o_i).  One warp per
+// (token, head) row, 8 columns per lane and step; HBM bound.
+__global__ void __launch_bounds__(256) gate_bwd_kernel(const __nv_bfloat16* __restrict__ dout,
+                                                       const __nv_bfloat16* __restrict__ o_cmp,
+                                                       const __nv_bfloat16* __restrict__ o_slc,
+                                                       const __nv_bfloat16* __restrict__ o_swa,
+                                                       const float* __restrict__ logits, __nv_bfloat16* d_cmp,
+                                                       __nv_bfloat16* d_slc, __nv_bfloat16* d_swa, float* d_logits,
+                                                       int64_t rows, int d) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float g[3], dot[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+  for (int b = 0; b < 3; ++b) g[b] = 1.f / (1.f + expf(-logits[row * 3 + b]));
+  const __nv_bfloat16* src[3] = {o_cmp, o_slc, o_swa};
+  __nv_bfloat16* dst[3] = {d_cmp, d_slc, d_swa};
+  for (int c = lane * 8; c < d; c += 256) {
+    const uint4 w = *reinterpret_cast<const uint4*>(dout + row * d + c);
+    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(w2[e]);
+      x[2 * e] = f.x;
+      x[2 * e + 1] = f.y;
+    }
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src[b] + row * d + c);
+      const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(u2[e]);
+        dot[b] += x[2 * e] * f.x + x[2 * e + 1] * f.y;
+      }
+      uint4 o;
+      o.x = pack_bf16(g[b] * x[0], g[b] * x[1]);
+      o.y = pack_bf16(g[b] * x[2], g[b] * x[3]);
+      o.z = pack_bf16(g[b] * x[4], g[b] * x[5]);
+      o.w = pack_bf16(g[b] * x[6], g[b] * x[7]);
+      *reinterpret_cast<uint4*>(dst[b] + row * d + c) = o;
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < 3; ++b)
+    for (int off = 16; off; off >>= 1) dot[b] += __shfl_xor_sync(0xffffffffu, dot[b], off);
+  if (lane < 3) {
+    const float gb = lane == 0 ? g[0] : lane == 1 ? g[1] : g[2];
+    const float db = lane == 0 ? dot[0] : lane == 1 ? dot[1] : dot[2];
+    d_logits[row * 3 + lane] = gb * (1.f - gb) * db;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gate_bwd(int64_t rows, int d, const void* dout, const void* o_cmp, const void* o_slc,
+                            const void* o_swa, const float* logits, void* d_cmp, void* d_slc, void* d_swa,
+                            float* d_logits, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  gate_bwd_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+      (const __nv_bfloat16*)dout, (const __nv_bfloat16*)o_cmp, (const __nv_bfloat16*)o_slc,
+      (const __nv_bfloat16*)o_swa, logits, (__nv_bfloat16*)d_cmp, (__nv_bfloat16*)d_slc, (__nv_bfloat16*)d_swa,
+      d_logits, rows, d);
+  return cudaGetLastError();
+}
 
 size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv) {
   if (s.tokens == 0 || s.max_len == 0) return 0;
@@ -665,6 +764,20 @@ cudaError_t launch_cmp_attn_bwd(const Seqs& s, const void* q, const void* k_cmp,
   p.cmp_kernel = kernel;
   p.cmp_stride = stride;
   return run_bwd(p, bwd_layout(s, h, hkv, kernel, stride), workspace, st);
+}
+
+size_t swa_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int window) {
+  if (s.tokens == 0 || s.max_len == 0) return 0;
+  return bwd_layout(s, h, hkv, 0, 0, window).total;
+}
+
+cudaError_t launch_swa_bwd(const Seqs& s, const void* q, const void* k, const void* v, int h, int hkv, int window,
+                           float scale, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* workspace, cudaStream_t st) {
+  if (s.tokens == 0) return cudaSuccess;
+  BwdParams p = bwd_params(s, q, k, v, h, hkv, scale, o, lse, dout, dq, dk, dv);
+  p.window = window;
+  return run_bwd(p, bwd_layout(s, h, hkv, 0, 0, window), workspace, st);
 }
 
 cudaError_t launch_compress_bwd(const Seqs& s, const void* dk_cmp, int hkv, int d, int kernel, int stride, void* dk,

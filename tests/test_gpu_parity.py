@@ -341,6 +341,66 @@ def test_cmp_attn_bwd_layer_size_sampled():
     assert_close(gv[torch.from_numpy(kr).cuda()], rv, what="cmp dv sampled")
 
 
+# --------------------------------------------------------------------------- S8 and S9 backward
+@pytest.mark.parametrize("window,H,hkv", [(512, 16, 1), (1, 16, 2), (64, 8, 8), (1984, 16, 4), (100, 64, 4)])
+def test_swa_bwd_varlen(window, H, hkv):
+    lengths = [1, 63, 64, 65, 700, 2100]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = _rng(51)
+    q, do = gen.normal(rng, (cu[-1], H, 128), "bf16"), gen.normal(rng, (cu[-1], H, 128), "bf16")
+    k, v = gen.normal(rng, (cu[-1], hkv, 128), "bf16"), gen.normal(rng, (cu[-1], hkv, 128), "bf16")
+    o64, lse64 = orc.swa(q, k, v, cu, window)
+    o = gen.f32_to_bf16_bits(o64.astype(np.float32))
+    gq, gk, gv = nsa.nsa_swa_bwd(dev(q), dev(k), dev(v), dev(o), dev(lse64.astype(np.float32)), dev(do), window,
+                                 cu_seqlens=dev(cu), max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.swa_bwd(q, k, v, do, cu, window, o=o)
+    assert_close(gq, rq, what="swa dq")
+    assert_close(gk, rk, what="swa dk")
+    assert_close(gv, rv, what="swa dv")
+
+
+def test_swa_bwd_layer_size_sampled():
+    """T=65536, H=64, Hkv=4, window 512: GPU forward then backward; sampled rows.  The GPU
+    backward takes D from the GPU forward's o, the oracle from its own; key rows near the
+    start collect large-p terms from rows with few keys, where those two D differ most, so
+    the sampled key rows lie past the first window (rows with few keys are covered above,
+    where both sides share one forward output)."""
+    w = gen.layer()
+    T = w.tokens
+    do = gen.normal(_rng(52), (T, 64, 128), "bf16")
+    q, k, v = dev(w.q), dev(w.k), dev(w.v)
+    lse = torch.empty((T, 64), dtype=torch.float32, device="cuda")
+    o = nsa.nsa_swa_fwd(q, k, v, 512, lse=lse)
+    gq, gk, gv = nsa.nsa_swa_bwd(q, k, v, o, lse, dev(do), 512)
+    torch.cuda.synchronize()
+    qr = np.array([0, 1, 511, 512, 40000, 65535])
+    kr = np.array([1000, 1023, 1024, 30000, 65535])
+    need = np.unique(np.concatenate([qr] + [np.arange(r_, min(r_ + 512, T)) for r_ in kr]))
+    o_ref = np.zeros((T, 64, 128), np.uint16)
+    o64, _ = orc.swa(w.q, w.k, w.v, w.cu_seqlens, 512, rows=need)
+    o_ref[need] = gen.f32_to_bf16_bits(o64.astype(np.float32))
+    rq, _, _ = orc.swa_bwd(w.q, w.k, w.v, do, w.cu_seqlens, 512, q_rows=qr, want_dkv=False, o=o_ref)
+    _, rk, rv = orc.swa_bwd(w.q, w.k, w.v, do, w.cu_seqlens, 512, kv_rows=kr, want_dq=False, o=o_ref)
+    assert_close(gq[torch.from_numpy(qr).cuda()], rq, what="swa dq sampled")
+    assert_close(gk[torch.from_numpy(kr).cuda()], rk, what="swa dk sampled")
+    assert_close(gv[torch.from_numpy(kr).cuda()], rv, what="swa dv sampled")
+
+
+def test_gate_combine_bwd():
+    rng = _rng(53)
+    n, h, d = 777, 16, 128
+    br = [gen.normal(rng, (n, h, d), "bf16") for _ in range(3)]
+    do = gen.normal(rng, (n, h, d), "bf16")
+    logits = (rng.standard_normal((n, h, 3)) * 2).astype(np.float32)
+    got = nsa.nsa_gate_combine_bwd(dev(do), *(dev(b) for b in br), dev(logits))
+    torch.cuda.synchronize()
+    ref = orc.gate_bwd(*(as_f64(b) for b in br), logits, as_f64(do))
+    for i in range(3):
+        assert_close(got[i], ref[i], what=f"gate branch {i}")
+    assert_close(got[3], ref[3], atol=1e-4, rtol=1e-4, what="gate logits")
+
+
 # --------------------------------------------------------------------------- NOSA stage 2
 def test_cis_block_scores():
     lengths = [10, 31, 32, 47, 100, 700, 5000]
