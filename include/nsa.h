@@ -368,6 +368,49 @@ NSA_API nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const vo
                          int n_init, int n_local, int window, float scale, void* o, int32_t* idx_out,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Training pair for the full layer.  nsa_layer_fwd_train is nsa_layer_fwd (same
+ * arguments, limits, workspace and output) that also keeps, in the caller's buffers, what
+ * the backward needs; nsa_layer_bwd then returns the gradients of the layer output o with
+ * respect to q, k, v and the gate logits for an upstream d_o.  The backward chains the
+ * gate backward, the backward of each branch (nsa_cmp_attn_bwd with nsa_compress_bwd for
+ * the pooling of both K and V, nsa_sparse_bwd on the kept block lists, which the
+ * selection does not differentiate through, and nsa_swa_bwd) and sums dq, dk, dv over the
+ * branches.  The pages train with this layer ([NSA-Triton] sec. 4) and print its forward
+ * only; the backward is the forward's derivative.
+ * Buffers of nsa_layer_saved (all device memory, owned by the caller, written by the
+ * training forward, read by the backward):
+ *   k_cmp, v_cmp  [n_cmp_total, h_kv, d] bf16 (n_cmp_total = sum of n_c(L) per sequence)
+ *   o_cmp, o_slc, o_swa  [tokens, h, d] bf16 (branch outputs before the gate)
+ *   lse_cmp, lse_slc, lse_swa  [tokens, h] fp32;  idx [tokens, h_kv, S] int32
+ * nsa_layer_bwd: d_o, dq [tokens, h, d]; dk, dv [tokens, h_kv, d] (bf16);
+ * d_gate_logits [tokens, h, 3] fp32; workspace of nsa_layer_bwd_workspace_size() bytes,
+ * 256-byte aligned.  Requires d 128, window <= 1984, at most 4096 compressed keys per
+ * sequence, plus the limits of nsa_layer_fwd. */
+typedef struct nsa_layer_saved {
+  void* k_cmp;
+  void* v_cmp;
+  void* o_cmp;
+  void* o_slc;
+  void* o_swa;
+  float* lse_cmp;
+  float* lse_slc;
+  float* lse_swa;
+  int32_t* idx;
+} nsa_layer_saved;
+
+NSA_API nsa_status nsa_layer_fwd_train(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                       const float* gate_logits, int kernel, int stride, int block_size, int S,
+                                       int n_init, int n_local, int window, float scale, void* o,
+                                       const nsa_layer_saved* saved, void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
+NSA_API size_t nsa_layer_bwd_workspace_size(const nsa_shape* shape, int kernel, int stride, int block_size, int S,
+                                            int window);
+NSA_API nsa_status nsa_layer_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                 const float* gate_logits, int kernel, int stride, int block_size, int S, int window,
+                                 float scale, const nsa_layer_saved* saved, const void* d_o, void* dq, void* dk,
+                                 void* dv, float* d_gate_logits, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -401,6 +401,52 @@ def gate_bwd(o_cmp, o_slc, o_swa, gates, do):
     return outs[0], outs[1], outs[2], dg
 
 
+def _to_dtype(x, like):
+    """fp64 values rounded to the dtype of `like` (bf16 bits or fp32)."""
+    x32 = np.asarray(x, np.float64).astype(np.float32)
+    if np.asarray(like).dtype == np.uint16:
+        u = x32.view(np.uint32).astype(np.uint64)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return x32
+
+
+def layer_bwd(q, k, v, gates, idx, do, cu, kernel=32, stride=16, block_size=64, window=512, scale=None,
+              branches=None):
+    """Backward of the three-branch layer for fixed block lists idx (the selection is not
+    differentiated): returns (dq, dk, dv [fp64], d gates [n, h, 3]).  The composition of the
+    branch backwards: the gate backward, then each branch's backward on its gradient, which
+    the layer holds in the input dtype (rounded here alike), the pooling backward of the
+    compressed keys and values, and the sum over branches.  branches: optional stored
+    (o_cmp, o_slc, o_swa) in q's dtype (for D and the gate); else the exact outputs."""
+    cu = _i32(cu)
+    _, kc = compress(k, cu, kernel, stride)
+    _, vc = compress(v, cu, kernel, stride)
+    if branches is None:
+        o_cmp, _ = cmp_attn(q, kc, vc, cu, kernel, stride, scale)
+        o_slc, _ = sparse_attn(q, k, v, idx, cu, block_size, scale)
+        o_swa, _ = swa(q, k, v, cu, window, scale)
+        stored = None
+    else:
+        stored = [np.ascontiguousarray(b) for b in branches]
+        o_cmp, o_slc, o_swa = (_to_f64(b) for b in stored)
+    d_cmp, d_slc, d_swa, dg = gate_bwd(o_cmp, o_slc, o_swa, gates, _to_f64(do))
+    d_cmp, d_slc, d_swa = (_to_dtype(x, q) for x in (d_cmp, d_slc, d_swa))
+    st = stored or [None, None, None]
+    dq_c, dkc, dvc = cmp_attn_bwd(q, kc, vc, d_cmp, cu, kernel, stride, scale, o=st[0])
+    dq_s, dk_s, dv_s = sparse_attn_bwd(q, k, v, idx, d_slc, cu, block_size, scale, o=st[1])
+    dq_w, dk_w, dv_w = swa_bwd(q, k, v, d_swa, cu, window, scale, o=st[2])
+    dk_c = compress_bwd(dkc, cu, kernel, stride)
+    dv_c = compress_bwd(dvc, cu, kernel, stride)
+    return dq_c + dq_s + dq_w, dk_c + dk_s + dk_w, dv_c + dv_s + dv_w, dg
+
+
+def _to_f64(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
 def decode(q, k_cache, v_cache, kc_cache, seqlens, kernel=32, stride=16, block_size=64, n_init=1,
            n_local=2, k=64, scale=None, idx_in=None, want_scores=False):
     """S6: one decode step; returns (idx [B,hkv,k], o [B,h,d] fp64[, scores [B,hkv,nb]])."""

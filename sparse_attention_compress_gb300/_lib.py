@@ -26,6 +26,11 @@ class NsaShape(ctypes.Structure):
                 ("h_kv", ctypes.c_int32), ("d", ctypes.c_int32), ("dtype", ctypes.c_int)]
 
 
+class NsaLayerSaved(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("k_cmp", "v_cmp", "o_cmp", "o_slc", "o_swa", "lse_cmp", "lse_slc",
+                                                "lse_swa", "idx")]
+
+
 _SIGS = {
     "nsa_version": ([], ctypes.c_char_p),
     "nsa_last_error": ([], ctypes.c_char_p),
@@ -65,6 +70,11 @@ _SIGS = {
     "nsa_sparse_decode_noalloc": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int,
                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
     "nsa_layer_fwd_workspace_size": ([_c_p, _c_int, _c_int, _c_int, _c_int], _c_sz),
+    "nsa_layer_fwd_train": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                             _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
+    "nsa_layer_bwd_workspace_size": ([_c_p, _c_int, _c_int, _c_int, _c_int, _c_int], _c_sz),
+    "nsa_layer_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p,
+                       _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
     "nsa_layer_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
                        _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
 }
@@ -485,3 +495,58 @@ def nsa_layer_fwd(q, k, v, gate_logits, kernel=32, stride=16, block_size=64, S=1
                                 block_size, S, n_init, n_local, window, float(scale), _ptr(out), _ptr(idx_out),
                                 _ptr(workspace), workspace.numel(), _stream(stream)), "nsa_layer_fwd")
     return out
+
+
+def nsa_layer_saved_buffers(tokens, n_cmp, h, h_kv, d, S, device):
+    """Allocate the tensors a training forward keeps for the backward (a dict of tensors)."""
+    bf = torch.bfloat16
+    return {"k_cmp": torch.empty((n_cmp, h_kv, d), dtype=bf, device=device),
+            "v_cmp": torch.empty((n_cmp, h_kv, d), dtype=bf, device=device),
+            "o_cmp": torch.empty((tokens, h, d), dtype=bf, device=device),
+            "o_slc": torch.empty((tokens, h, d), dtype=bf, device=device),
+            "o_swa": torch.empty((tokens, h, d), dtype=bf, device=device),
+            "lse_cmp": torch.empty((tokens, h), dtype=torch.float32, device=device),
+            "lse_slc": torch.empty((tokens, h), dtype=torch.float32, device=device),
+            "lse_swa": torch.empty((tokens, h), dtype=torch.float32, device=device),
+            "idx": torch.empty((tokens, h_kv, S), dtype=torch.int32, device=device)}
+
+
+def _saved_struct(saved):
+    st = NsaLayerSaved()
+    for name, _ in NsaLayerSaved._fields_:
+        setattr(st, name, saved[name].data_ptr())
+    return st
+
+
+def nsa_layer_fwd_train(q, k, v, gate_logits, saved, kernel=32, stride=16, block_size=64, S=16, n_init=1,
+                        n_local=2, window=512, scale=0.0, *, cu_seqlens=None, max_seqlen=None, workspace=None,
+                        out=None, stream=None):
+    """Layer forward that also fills `saved` (nsa_layer_saved_buffers) for nsa_layer_bwd."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    if workspace is None:
+        ws = int(load().nsa_layer_fwd_workspace_size(ctypes.byref(shp), kernel, stride, block_size, S))
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(qf) if out is None else out
+    st = _saved_struct(saved)
+    _check(load().nsa_layer_fwd_train(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(gate_logits), kernel,
+                                      stride, block_size, S, n_init, n_local, window, float(scale), _ptr(out),
+                                      ctypes.byref(st), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "nsa_layer_fwd_train")
+    return out
+
+
+def nsa_layer_bwd(q, k, v, gate_logits, saved, d_o, kernel=32, stride=16, block_size=64, S=16, window=512,
+                  scale=0.0, *, cu_seqlens=None, max_seqlen=None, workspace=None, stream=None):
+    """Layer backward: returns (dq, dk, dv, d_gate_logits)."""
+    qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
+    if workspace is None:
+        ws = int(load().nsa_layer_bwd_workspace_size(ctypes.byref(shp), kernel, stride, block_size, S, window))
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty_like(gate_logits)
+    st = _saved_struct(saved)
+    _check(load().nsa_layer_bwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), _ptr(gate_logits), kernel, stride,
+                                block_size, S, window, float(scale), ctypes.byref(st), _ptr(d_o), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(dg), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "nsa_layer_bwd")
+    return dq, dk, dv, dg

@@ -4,6 +4,8 @@
 #include <stdio.h>
 
 #include "nsa.h"
+#include <algorithm>
+
 #include "launch.h"
 
 using namespace nsa;
@@ -698,18 +700,20 @@ size_t nsa_layer_fwd_workspace_size(const nsa_shape* shape, int kernel, int stri
       .total;
 }
 
-nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
-                         const float* gate_logits, int kernel, int stride, int block_size, int S,
-                         int n_init, int n_local, int window, float scale, void* o, int32_t* idx_out,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// Layer forward; with `saved`, the compressed keys and values, each branch's output and
+// normaliser and the block lists go to the caller's buffers for nsa_layer_bwd.
+static nsa_status layer_forward(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                                const float* gate_logits, int kernel, int stride, int block_size, int S, int n_init,
+                                int n_local, int window, float scale, void* o, int32_t* idx_out,
+                                const nsa_layer_saved* saved, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream, const char* fn) {
   Seqs s;
-  if (nsa_status st = dense_common(shape, &s, __func__)) return st;
+  if (nsa_status st = dense_common(shape, &s, fn)) return st;
   NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
-              "nsa_layer_fwd: supports kernel 32, stride 16, block_size 64");
-  NSA_REQUIRE(pow2_le16(shape->h / shape->h_kv), NSA_ERR_UNSUPPORTED,
-              "nsa_layer_fwd: h/h_kv must be 1, 2, 4, 8 or 16");
-  NSA_REQUIRE(S >= 1 && S <= 64, NSA_ERR_UNSUPPORTED, "nsa_layer_fwd: S must be in [1, 64]");
-  NSA_REQUIRE(window >= 1 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "nsa_layer_fwd: bad window/n_init/n_local");
+              "%s: supports kernel 32, stride 16, block_size 64", fn);
+  NSA_REQUIRE(pow2_le16(shape->h / shape->h_kv), NSA_ERR_UNSUPPORTED, "%s: h/h_kv must be 1, 2, 4, 8 or 16", fn);
+  NSA_REQUIRE(S >= 1 && S <= 64, NSA_ERR_UNSUPPORTED, "%s: S must be in [1, 64]", fn);
+  NSA_REQUIRE(window >= 1 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "%s: bad window/n_init/n_local", fn);
   if (s.tokens == 0) return NSA_OK;
   NSA_PTR(q);
   NSA_PTR(k);
@@ -717,54 +721,206 @@ nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, c
   NSA_PTR(gate_logits);
   NSA_PTR(o);
   if (idx_out) NSA_PTR(idx_out);
+  if (saved) {
+    NSA_PTR(saved->k_cmp);
+    NSA_PTR(saved->v_cmp);
+    NSA_PTR(saved->o_cmp);
+    NSA_PTR(saved->o_slc);
+    NSA_PTR(saved->o_swa);
+    NSA_PTR(saved->lse_cmp);
+    NSA_PTR(saved->lse_slc);
+    NSA_PTR(saved->lse_swa);
+    NSA_PTR(saved->idx);
+  }
   const LayerLayout l = layer_layout(s, shape->h, shape->h_kv, shape->d, 2, kernel, stride, block_size, S);
-  NSA_REQUIRE(l.nb_stride <= 2048, NSA_ERR_UNSUPPORTED, "nsa_layer_fwd: sequences longer than 131072 tokens");
+  NSA_REQUIRE(l.nb_stride <= 2048, NSA_ERR_UNSUPPORTED, "%s: sequences longer than 131072 tokens", fn);
   NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
-              "nsa_layer_fwd: workspace must be non-null and 256-byte aligned");
-  NSA_REQUIRE(workspace_bytes >= l.total, NSA_ERR_INVALID, "nsa_layer_fwd: workspace %zu < %zu bytes",
-              workspace_bytes, l.total);
+              "%s: workspace must be non-null and 256-byte aligned", fn);
+  NSA_REQUIRE(workspace_bytes >= l.total, NSA_ERR_INVALID, "%s: workspace %zu < %zu bytes", fn, workspace_bytes,
+              l.total);
   if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
   uint8_t* w = static_cast<uint8_t*>(workspace);
-  void* kc = w + l.kc;
-  void* vc = w + l.vc;
-  void* o_cmp = w + l.o_cmp;
-  void* o_swa = w + l.o_swa;
-  float* lse = reinterpret_cast<float*>(w + l.lse);
+  void* kc = saved ? saved->k_cmp : w + l.kc;
+  void* vc = saved ? saved->v_cmp : w + l.vc;
+  void* o_cmp = saved ? saved->o_cmp : w + l.o_cmp;
+  void* o_swa = saved ? saved->o_swa : w + l.o_swa;
+  void* o_slc = saved ? saved->o_slc : o;  // without saved, the selected branch writes o and the gate runs in place
+  float* lse = saved ? saved->lse_cmp : reinterpret_cast<float*>(w + l.lse);
   float* scores = reinterpret_cast<float*>(w + l.scores);
-  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + l.idx);
+  int32_t* idx = saved ? saved->idx : idx_out ? idx_out : reinterpret_cast<int32_t*>(w + l.idx);
   const int h = shape->h, hkv = shape->h_kv, d = shape->d;
   cudaError_t e;
-  if ((e = launch_compress(s, k, kc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "nsa_layer_fwd/compress k");
-  if ((e = launch_compress(s, v, vc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "nsa_layer_fwd/compress v");
+  if ((e = launch_compress(s, k, kc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "layer/compress k");
+  if ((e = launch_compress(s, v, vc, hkv, d, kBF16, kernel, stride, stream))) return cuda_status(e, "layer/compress v");
   const bool tc = d == 128;
   void* vtc = w + l.vtc;
   void* vt = w + l.vt;
   if (tc) {
     if ((e = launch_transpose_v(s, vc, vtc, l.ncr, hkv, true, kernel, stride, stream)))
-      return cuda_status(e, "nsa_layer_fwd/transpose compressed v");
+      return cuda_status(e, "layer/transpose compressed v");
     if ((e = launch_transpose_v(s, v, vt, s.tokens, hkv, false, kernel, stride, stream)))
-      return cuda_status(e, "nsa_layer_fwd/transpose v");
+      return cuda_status(e, "layer/transpose v");
     // the compressed branch also writes the block scores (second pass over its keys)
-    e = launch_dense_attn_tc(0, s, q, kc, vtc, l.ncr, h, hkv, kernel, stride, 0, scale, o_cmp, nullptr, scores,
-                             l.nb_stride, stream);
-    if (e) return cuda_status(e, "nsa_layer_fwd/compressed branch and block scores");
+    e = launch_dense_attn_tc(0, s, q, kc, vtc, l.ncr, h, hkv, kernel, stride, 0, scale, o_cmp,
+                             saved ? saved->lse_cmp : nullptr, scores, l.nb_stride, stream);
+    if (e) return cuda_status(e, "layer/compressed branch and block scores");
   } else {
     e = launch_dense_attn(0, s, q, kc, vc, h, hkv, d, kernel, stride, 0, scale, o_cmp, lse, stream);
-    if (e) return cuda_status(e, "nsa_layer_fwd/compressed branch");
+    if (e) return cuda_status(e, "layer/compressed branch");
     if ((e = launch_scores_pool(s, q, kc, h, hkv, d, scale, lse, scores, l.nb_stride, stream)))
-      return cuda_status(e, "nsa_layer_fwd/block scores");
+      return cuda_status(e, "layer/block scores");
   }
   if ((e = launch_topk(s, scores, l.nb_stride, hkv, block_size, n_init, n_local, S, idx, stream)))
-    return cuda_status(e, "nsa_layer_fwd/top-k");
-  // the selected branch writes straight into o; the gated sum then runs in place
-  if ((e = launch_sparse_fwd(s, q, k, v, idx, S, block_size, h, hkv, d, kBF16, scale, o, nullptr, stream)))
-    return cuda_status(e, "nsa_layer_fwd/selected branch");
-  e = tc ? launch_dense_attn_tc(1, s, q, k, vt, s.tokens, h, hkv, kernel, stride, window, scale, o_swa, nullptr,
-                                 nullptr, 0, stream)
-         : launch_dense_attn(1, s, q, k, v, h, hkv, d, kernel, stride, window, scale, o_swa, nullptr, stream);
-  if (e) return cuda_status(e, "nsa_layer_fwd/sliding branch");
-  return cuda_status(launch_gate_combine(s.tokens, h, d, o_cmp, o, o_swa, gate_logits, o, stream),
-                     "nsa_layer_fwd/gate combine");
+    return cuda_status(e, "layer/top-k");
+  if (saved && idx_out && (e = cudaMemcpyAsync(idx_out, idx, (size_t)s.tokens * hkv * S * 4, cudaMemcpyDeviceToDevice,
+                                                stream)))
+    return cuda_status(e, "layer/copy block lists");
+  if ((e = launch_sparse_fwd(s, q, k, v, idx, S, block_size, h, hkv, d, kBF16, scale, o_slc,
+                             saved ? saved->lse_slc : nullptr, stream)))
+    return cuda_status(e, "layer/selected branch");
+  e = tc ? launch_dense_attn_tc(1, s, q, k, vt, s.tokens, h, hkv, kernel, stride, window, scale, o_swa,
+                                 saved ? saved->lse_swa : nullptr, nullptr, 0, stream)
+         : launch_dense_attn(1, s, q, k, v, h, hkv, d, kernel, stride, window, scale, o_swa,
+                             saved ? saved->lse_swa : nullptr, stream);
+  if (e) return cuda_status(e, "layer/sliding branch");
+  return cuda_status(launch_gate_combine(s.tokens, h, d, o_cmp, o_slc, o_swa, gate_logits, o, stream),
+                     "layer/gate combine");
+}
+
+nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                         const float* gate_logits, int kernel, int stride, int block_size, int S,
+                         int n_init, int n_local, int window, float scale, void* o, int32_t* idx_out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return layer_forward(shape, q, k, v, gate_logits, kernel, stride, block_size, S, n_init, n_local, window, scale, o,
+                       idx_out, nullptr, workspace, workspace_bytes, stream, __func__);
+}
+
+nsa_status nsa_layer_fwd_train(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                               const float* gate_logits, int kernel, int stride, int block_size, int S, int n_init,
+                               int n_local, int window, float scale, void* o, const nsa_layer_saved* saved,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_REQUIRE(saved != nullptr, NSA_ERR_INVALID, "nsa_layer_fwd_train: saved is NULL");
+  return layer_forward(shape, q, k, v, gate_logits, kernel, stride, block_size, S, n_init, n_local, window, scale, o,
+                       nullptr, saved, workspace, workspace_bytes, stream, __func__);
+}
+
+// Layer backward workspace: the three branch gradients of dO, each branch's dq, dk, dv,
+// the compressed-key gradients, and one branch-backward scratch (used in turn).
+struct LayerBwdLayout {
+  size_t d_br, dq3, dk3, dv3, dkc, dvc, scratch, total;
+};
+
+static LayerBwdLayout layer_bwd_layout(const Seqs& s, int h, int hkv, int d, int kernel, int stride, int window) {
+  LayerBwdLayout l{};
+  const int64_t ncr = s.cu ? s.tokens / stride + s.n_seqs : (int64_t)s.n_seqs * num_cmp_host(s.T, kernel, stride);
+  const size_t qsz = (size_t)s.tokens * h * d * 2, ksz = (size_t)s.tokens * hkv * d * 2;
+  size_t off = 0;
+  l.d_br = off;
+  off = align256(off + 3 * qsz);
+  l.dq3 = off;
+  off = align256(off + 3 * qsz);
+  l.dk3 = off;
+  off = align256(off + 3 * ksz);
+  l.dv3 = off;
+  off = align256(off + 3 * ksz);
+  l.dkc = off;
+  off = align256(off + (size_t)ncr * hkv * d * 2);
+  l.dvc = off;
+  off = align256(off + (size_t)ncr * hkv * d * 2);
+  l.scratch = off;
+  size_t sc = sparse_bwd_workspace_bytes(s, h, hkv);
+  sc = std::max(sc, cmp_attn_bwd_workspace_bytes(s, h, hkv, kernel, stride));
+  sc = std::max(sc, swa_bwd_workspace_bytes(s, h, hkv, window));
+  l.total = align256(off + sc);
+  return l;
+}
+
+static nsa_status check_layer_bwd(const nsa_shape* shape, int kernel, int stride, int block_size, int S, int window,
+                                  Seqs* s, const char* fn) {
+  if (nsa_status st = make_seqs(shape, s, fn)) return st;
+  NSA_REQUIRE(shape->dtype == NSA_BF16 && shape->d == 128, NSA_ERR_UNSUPPORTED, "%s: bf16 and d 128 only", fn);
+  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
+              "%s: supports kernel 32, stride 16, block_size 64", fn);
+  NSA_REQUIRE(pow2_le16(shape->h / shape->h_kv), NSA_ERR_UNSUPPORTED, "%s: h/h_kv must be 1, 2, 4, 8 or 16", fn);
+  NSA_REQUIRE(S >= 1 && S <= 64, NSA_ERR_UNSUPPORTED, "%s: S must be in [1, 64]", fn);
+  NSA_REQUIRE(window >= 1 && window <= 1984, NSA_ERR_UNSUPPORTED, "%s: window must be in [1, 1984]", fn);
+  NSA_REQUIRE(num_cmp_host(s->max_len, kernel, stride) <= 4096, NSA_ERR_UNSUPPORTED,
+              "%s: at most 4096 compressed keys per sequence", fn);
+  return NSA_OK;
+}
+
+size_t nsa_layer_bwd_workspace_size(const nsa_shape* shape, int kernel, int stride, int block_size, int S,
+                                    int window) {
+  Seqs s;
+  if (check_layer_bwd(shape, kernel, stride, block_size, S, window, &s, "nsa_layer_bwd_workspace_size") != NSA_OK)
+    return 0;
+  if (s.tokens == 0) return 0;
+  return layer_bwd_layout(s, shape->h, shape->h_kv, shape->d, kernel, stride, window).total;
+}
+
+nsa_status nsa_layer_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
+                         const float* gate_logits, int kernel, int stride, int block_size, int S, int window,
+                         float scale, const nsa_layer_saved* saved, const void* d_o, void* dq, void* dk, void* dv,
+                         float* d_gate_logits, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Seqs s;
+  if (nsa_status st = check_layer_bwd(shape, kernel, stride, block_size, S, window, &s, __func__)) return st;
+  if (s.tokens == 0) return NSA_OK;
+  NSA_REQUIRE(saved != nullptr, NSA_ERR_INVALID, "nsa_layer_bwd: saved is NULL");
+  NSA_PTR(q);
+  NSA_PTR(k);
+  NSA_PTR(v);
+  NSA_PTR(gate_logits);
+  NSA_PTR(d_o);
+  NSA_PTR(dq);
+  NSA_PTR(dk);
+  NSA_PTR(dv);
+  NSA_PTR(d_gate_logits);
+  NSA_PTR(saved->k_cmp);
+  NSA_PTR(saved->v_cmp);
+  NSA_PTR(saved->o_cmp);
+  NSA_PTR(saved->o_slc);
+  NSA_PTR(saved->o_swa);
+  NSA_PTR(saved->lse_cmp);
+  NSA_PTR(saved->lse_slc);
+  NSA_PTR(saved->lse_swa);
+  NSA_PTR(saved->idx);
+  const int h = shape->h, hkv = shape->h_kv, d = shape->d;
+  const LayerBwdLayout l = layer_bwd_layout(s, h, hkv, d, kernel, stride, window);
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_layer_bwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= l.total, NSA_ERR_INVALID, "nsa_layer_bwd: workspace %zu < %zu bytes",
+              workspace_bytes, l.total);
+  if (scale <= 0.f) scale = 1.f / sqrtf((float)d);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const size_t qsz = (size_t)s.tokens * h * d * 2, ksz = (size_t)s.tokens * hkv * d * 2;
+  uint8_t* d_cmp = w + l.d_br;
+  uint8_t* d_slc = d_cmp + qsz;
+  uint8_t* d_swa = d_slc + qsz;
+  uint8_t* dq3 = w + l.dq3;
+  uint8_t* dk3 = w + l.dk3;
+  uint8_t* dv3 = w + l.dv3;
+  void* scratch = w + l.scratch;
+  cudaError_t e;
+  if ((e = launch_gate_bwd(s.tokens * h, d, d_o, saved->o_cmp, saved->o_slc, saved->o_swa, gate_logits, d_cmp, d_slc,
+                           d_swa, d_gate_logits, stream)))
+    return cuda_status(e, "layer bwd/gate");
+  if ((e = launch_cmp_attn_bwd(s, q, saved->k_cmp, saved->v_cmp, h, hkv, kernel, stride, scale, saved->o_cmp,
+                               saved->lse_cmp, d_cmp, dq3, w + l.dkc, w + l.dvc, scratch, stream)))
+    return cuda_status(e, "layer bwd/compressed branch");
+  if ((e = launch_compress_bwd(s, w + l.dkc, hkv, d, kernel, stride, dk3, stream)) ||
+      (e = launch_compress_bwd(s, w + l.dvc, hkv, d, kernel, stride, dv3, stream)))
+    return cuda_status(e, "layer bwd/pooling");
+  if ((e = launch_sparse_bwd(s, q, k, v, saved->idx, S, h, hkv, scale, saved->o_slc, saved->lse_slc, d_slc,
+                             dq3 + qsz, dk3 + ksz, dv3 + ksz, scratch, stream)))
+    return cuda_status(e, "layer bwd/selected branch");
+  if ((e = launch_swa_bwd(s, q, k, v, h, hkv, window, scale, saved->o_swa, saved->lse_swa, d_swa, dq3 + 2 * qsz,
+                          dk3 + 2 * ksz, dv3 + 2 * ksz, scratch, stream)))
+    return cuda_status(e, "layer bwd/sliding branch");
+  if ((e = launch_add3(dq3, dq3 + qsz, dq3 + 2 * qsz, dq, s.tokens * h * d, stream)) ||
+      (e = launch_add3(dk3, dk3 + ksz, dk3 + 2 * ksz, dk, s.tokens * hkv * d, stream)) ||
+      (e = launch_add3(dv3, dv3 + ksz, dv3 + 2 * ksz, dv, s.tokens * hkv * d, stream)))
+    return cuda_status(e, "layer bwd/sum over branches");
+  return NSA_OK;
 }
 
 }  // extern "C"

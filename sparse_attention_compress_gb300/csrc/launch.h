@@ -54,6 +54,8 @@ cudaError_t launch_cmp_attn_bwd(const Seqs& s, const void* q, const void* k_cmp,
                                 cudaStream_t st);
 cudaError_t launch_compress_bwd(const Seqs& s, const void* dk_cmp, int hkv, int d, int kernel, int stride, void* dk,
                                 cudaStream_t st);
+// out = a + b + c (bf16, n a multiple of 8).
+cudaError_t launch_add3(const void* a, const void* b, const void* c, void* out, int64_t n, cudaStream_t st);
 // Backward of the sigmoid gate combine over rows = tokens * h (bf16, d % 8 == 0).
 cudaError_t launch_gate_bwd(int64_t rows, int d, const void* dout, const void* o_cmp, const void* o_slc,
                             const void* o_swa, const float* logits, void* d_cmp, void* d_slc, void* d_swa,

@@ -705,6 +705,32 @@ __global__ void __launch_bounds__(256) gate_bwd_kernel(const __nv_bfloat16* __re
 
 }  // namespace
 
+// out = a + b + c elementwise (bf16 in and out, fp32 sum); n a multiple of 8.
+__global__ void __launch_bounds__(256) add3_kernel(const uint4* __restrict__ a, const uint4* __restrict__ b,
+                                                   const uint4* __restrict__ c, uint4* __restrict__ out, int64_t n8) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint4 x = a[i], y = b[i], z = c[i];
+  const __nv_bfloat162* xs = reinterpret_cast<const __nv_bfloat162*>(&x);
+  const __nv_bfloat162* ys = reinterpret_cast<const __nv_bfloat162*>(&y);
+  const __nv_bfloat162* zs = reinterpret_cast<const __nv_bfloat162*>(&z);
+  uint32_t r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 u = __bfloat1622float2(xs[e]), v = __bfloat1622float2(ys[e]), w = __bfloat1622float2(zs[e]);
+    r[e] = pack_bf16(u.x + v.x + w.x, u.y + v.y + w.y);
+  }
+  out[i] = make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+cudaError_t launch_add3(const void* a, const void* b, const void* c, void* out, int64_t n, cudaStream_t st) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  add3_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>((const uint4*)a, (const uint4*)b, (const uint4*)c,
+                                                             (uint4*)out, n8);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gate_bwd(int64_t rows, int d, const void* dout, const void* o_cmp, const void* o_slc,
                             const void* o_swa, const float* logits, void* d_cmp, void* d_slc, void* d_swa,
                             float* d_logits, cudaStream_t st) {

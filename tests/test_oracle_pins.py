@@ -858,3 +858,57 @@ def test_gate_bwd_equals_autograd():
     for i in range(3):
         assert torch.allclose(torch.from_numpy(got[i]), B[i].grad, atol=1e-14)
     assert torch.allclose(torch.from_numpy(got[3]), A.grad, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- layer backward
+def test_layer_bwd_equals_autograd_of_the_layer():
+    """The whole layer written in float64 torch ops (avg_pool1d compression, window-masked
+    compressed attention, the selected attention on fixed lists, the banded window, the
+    sigmoid gates), differentiated by autograd, against the oracle's composition of branch
+    backwards (fp32 inputs: the stored compressed keys and branch gradients round to fp32)."""
+    lengths = [130, 97]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, bs, S, win = 4, 2, 16, 64, 3, 40
+    q, do = _rand((cu[-1], h, d), 171, "f32"), _rand((cu[-1], h, d), 172, "f32")
+    k, v = _rand((cu[-1], hkv, d), 173, "f32"), _rand((cu[-1], hkv, d), 174, "f32")
+    gates = np.random.default_rng(175).standard_normal((int(cu[-1]), h, 3)).astype(np.float32)
+    idx = gen.random_block_indices(np.random.default_rng(176), cu, hkv, S, bs, force_first=True)
+    dq, dk, dv, dg = orc.layer_bwd(q, k, v, gates, idx, do, cu, 32, 16, bs, win)
+    Q, K, V, A = (_t(a).requires_grad_(True) for a in (q, k, v, gates))
+    r, scale = h // hkv, d ** -0.5
+    loss = 0.0
+    for i, L in enumerate(lengths):
+        a = int(cu[i])
+        qq, kk, vv, aa = Q[a:a + L], K[a:a + L], V[a:a + L], A[a:a + L]
+        t = torch.arange(L)
+        # compressed branch
+        kc = F.avg_pool1d(kk.permute(1, 2, 0), 32, 16).permute(2, 0, 1)  # [n_c, hkv, d]
+        vc = F.avg_pool1d(vv.permute(1, 2, 0), 32, 16).permute(2, 0, 1)
+        n_c = kc.shape[0]
+        ok = (torch.arange(n_c)[None, :] * 16 + 31) <= t[:, None]
+        s = torch.einsum("thd,chd->thc", qq, kc.repeat_interleave(r, 1)) * scale
+        s = s.masked_fill(~ok[:, None, :], -torch.inf)
+        p = torch.softmax(s[31:], -1)
+        o_cmp = torch.cat([torch.zeros(31, h, d, dtype=F64),
+                           torch.einsum("thc,chd->thd", p, vc.repeat_interleave(r, 1))])
+        # selected branch on the fixed lists
+        mult = np.zeros((L, hkv, L))
+        for tt in range(L):
+            for g in range(hkv):
+                for j in idx[a + tt, g]:
+                    if j < 0 or j * bs > tt:
+                        continue
+                    for tau in range(j * bs, min((j + 1) * bs, tt + 1)):
+                        mult[tt, g, tau] += 1
+        logm = torch.from_numpy(np.where(mult > 0, np.log(np.maximum(mult, 1)), -np.inf)).repeat_interleave(r, 1)
+        s2 = torch.einsum("thd,shd->ths", qq, kk.repeat_interleave(r, 1)) * scale + logm
+        o_slc = torch.einsum("ths,shd->thd", torch.softmax(s2, -1), vv.repeat_interleave(r, 1))
+        # sliding window
+        band = (t[:, None] >= t[None, :]) & (t[:, None] - t[None, :] < win)
+        o_swa = _sdpa(qq, kk, vv, band)
+        g = torch.sigmoid(aa)
+        o = g[..., 0:1] * o_cmp + g[..., 1:2] * o_slc + g[..., 2:3] * o_swa
+        loss = loss + (o * _t(do[a:a + L])).sum()
+    loss.backward()
+    for ours, ref, what in ((dq, Q.grad, "dq"), (dk, K.grad, "dk"), (dv, V.grad, "dv"), (dg, A.grad, "dgate")):
+        assert torch.allclose(torch.from_numpy(ours), ref, atol=2e-6, rtol=1e-5), what
