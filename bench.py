@@ -322,6 +322,42 @@ def bench_swa_bwd(torch, nsa, device, steps, warmup, flush, peaks):
             "gate_hbm_frac": gbytes / (msg * 1e-3) / 1e9 / peaks["hbm_gbs"], "launches_per_step": 4}
 
 
+def bench_layer_train(torch, nsa, device, steps, warmup, flush, peaks):
+    """One training step of the layer at T=65536, H=64, Hkv=4: the training forward (keeps
+    the branch outputs) and the layer backward (gate, three branches, pooling, sums)."""
+    w = gen.layer()
+    q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
+    gl = dev(torch, w.gates, device)
+    do = dev(torch, gen.normal(gen.rng_for(4, 97), (w.tokens, w.h, w.d), "bf16"), device)
+    saved = nsa.nsa_layer_saved_buffers(w.tokens, nsa.num_cmp(w.tokens), w.h, w.hkv, w.d, 16, device)
+    from sparse_attention_compress_gb300 import _lib
+    shp = _lib.make_shape(w.tokens, w.h, w.hkv, w.d, _lib.NSA_BF16, batch=1, seqlen=w.tokens)
+    wsf = torch.empty(nsa.nsa_layer_fwd_workspace_size(shp), dtype=torch.uint8, device=device)
+    wsb = torch.empty(int(nsa.load().nsa_layer_bwd_workspace_size(_lib.ctypes.byref(shp), 32, 16, 64, 16, 512)),
+                      dtype=torch.uint8, device=device)
+    out = torch.empty_like(q)
+
+    def fwd():
+        nsa.nsa_layer_fwd_train(q, k, v, gl, saved, workspace=wsf, out=out)
+
+    def bwd():
+        nsa.nsa_layer_bwd(q, k, v, gl, saved, do, workspace=wsb)
+
+    ms_f = float(np.mean(timed(torch, fwd, steps, warmup, flush)))
+    ms_b = float(np.mean(timed(torch, bwd, steps, warmup, flush)))
+    t = np.arange(w.tokens)
+    ncaus = np.clip((t - 31) // 16 + 1, 0, None)
+    r = w.h // w.hkv
+    idx = saved["idx"].cpu().numpy().astype(np.int64)
+    blk = np.where(idx >= 0, np.clip(t[:, None, None] - idx * 64 + 1, 0, 64), 0).sum()
+    pairs_h = ncaus.sum() * w.h + float(blk) * r + np.minimum(t + 1, 512).sum() * w.h
+    fwd_flops, bwd_flops = 4 * w.d * pairs_h, 10 * w.d * pairs_h
+    return {"workload": "layer training step T=65536 H=64 Hkv=4 d=128 bf16 (training forward + backward)",
+            "fwd_ms": ms_f, "bwd_ms": ms_b, "step_ms": ms_f + ms_b,
+            "step_tflops": (fwd_flops + bwd_flops) / ((ms_f + ms_b) * 1e-3) / 1e12,
+            "bwd_tflops": bwd_flops / (ms_b * 1e-3) / 1e12, "bwd_workspace_bytes": int(wsb.numel())}
+
+
 def bench_nosa(torch, nsa, device, steps, warmup, flush, peaks):
     """NOSA stage 2: CIS-weighted selected attention on the prefill workload, and the
     block CIS scores plus two-stage selection on the varlen selection workload."""
@@ -492,7 +528,8 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
     ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "cmp_bwd", "swa_bwd", "nosa", "decode", "decode_offload",
+    ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "cmp_bwd", "swa_bwd", "layer_train", "nosa", "decode",
+                                                    "decode_offload",
                                                     "selection", "layer", "block_sparse"],
                     help="time one workload only, with no e2e or CPU arm (for profiler captures)")
     args = ap.parse_args()
@@ -524,9 +561,10 @@ def main():
         flush_buf.zero_()
         flush_buf.copy_(flush_src)
 
-    if args.only in ("prefill_bwd", "cmp_bwd", "swa_bwd", "nosa", "decode", "decode_offload", "selection", "layer",
-                     "block_sparse"):
-        fn = {"swa_bwd": lambda: bench_swa_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+    if args.only in ("prefill_bwd", "cmp_bwd", "swa_bwd", "layer_train", "nosa", "decode", "decode_offload",
+                     "selection", "layer", "block_sparse"):
+        fn = {"layer_train": lambda: bench_layer_train(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "swa_bwd": lambda: bench_swa_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
@@ -624,6 +662,12 @@ def main():
             line["gpu_launches"] += 4 * max(3, args.steps // 2)
         except Exception as e:
             line["swa_bwd"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+        try:
+            line["layer_train"] = bench_layer_train(torch, nsa, device, 3, args.warmup, flush, peaks)
+            line["gpu_launches"] += 3 * 30
+        except Exception as e:
+            line["layer_train"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
             line["nosa"] = bench_nosa(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush, peaks)

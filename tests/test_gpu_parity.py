@@ -401,6 +401,73 @@ def test_gate_combine_bwd():
     assert_close(got[3], ref[3], atol=1e-4, rtol=1e-4, what="gate logits")
 
 
+# --------------------------------------------------------------------------- layer training pair
+def _layer_train_case(lengths, H, hkv):
+    w = gen.layer(H=H, HKV=hkv, lengths=lengths)
+    cu = w.cu_seqlens
+    do = gen.normal(_rng(61), (w.tokens, H, 128), "bf16")
+    return w, cu, do
+
+
+def test_layer_fwd_train_matches_layer_fwd_and_oracle():
+    """The training forward gives the same output as nsa_layer_fwd (same kernels) and
+    keeps branch outputs and normalisers that match the oracle's branches."""
+    lengths = [700, 1500, 40]
+    w, cu, _ = _layer_train_case(lengths, 16, 2)
+    dcu, L = dev(cu), max(lengths)
+    n_cmp = int(orc.cmp_offsets(cu)[-1])
+    saved = nsa.nsa_layer_saved_buffers(w.tokens, n_cmp, 16, 2, 128, 16, "cuda")
+    q, k, v, gl = dev(w.q), dev(w.k), dev(w.v), dev(w.gates)
+    o_tr = nsa.nsa_layer_fwd_train(q, k, v, gl, saved, cu_seqlens=dcu, max_seqlen=L)
+    o = torch.empty_like(o_tr)
+    idx = torch.empty((w.tokens, 2, 16), dtype=torch.int32, device="cuda")
+    nsa.nsa_layer_fwd(q, k, v, gl, cu_seqlens=dcu, max_seqlen=L, out=o, idx_out=idx)
+    torch.cuda.synchronize()
+    assert torch.equal(o_tr.view(torch.int16), o.view(torch.int16))
+    assert torch.equal(saved["idx"], idx)
+    _, kc = orc.compress(w.k, cu)
+    assert np.array_equal(host(saved["k_cmp"]), kc)
+    gi = host(saved["idx"])
+    ref_c, lc = orc.cmp_attn(w.q, host(saved["k_cmp"]), host(saved["v_cmp"]), cu)
+    ref_s, ls = orc.sparse_attn(w.q, w.k, w.v, gi, cu, 64)
+    ref_w, lw = orc.swa(w.q, w.k, w.v, cu, 512)
+    for got, ref, what in (("o_cmp", ref_c, "cmp"), ("o_slc", ref_s, "slc"), ("o_swa", ref_w, "swa")):
+        assert_close(saved[got], ref, what=f"saved {what}")
+    for got, ref in (("lse_cmp", lc), ("lse_slc", ls), ("lse_swa", lw)):
+        g = host(saved[got])
+        fin = np.isfinite(ref)
+        assert np.array_equal(np.isfinite(g), fin), got
+        assert np.allclose(g[fin], ref[fin], atol=1e-3, rtol=1e-3), got
+
+
+@pytest.mark.parametrize("lengths,H,hkv", [([700, 1500, 40], 16, 2), ([2100], 16, 1), ([300, 64], 8, 8)])
+def test_layer_bwd(lengths, H, hkv):
+    """nsa_layer_bwd on buffers the oracle's forward filled (branch outputs rounded to bf16,
+    normalisers, block lists) against the oracle's composition of branch backwards."""
+    w, cu, do = _layer_train_case(lengths, H, hkv)
+    dcu, L = dev(cu), max(lengths)
+    ref = orc.layer(w.q, w.k, w.v, w.gates, cu, branches=True)
+    idx = ref["idx"]
+    _, kc = orc.compress(w.k, cu)
+    _, vc = orc.compress(w.v, cu)
+    oc, lc = orc.cmp_attn(w.q, kc, vc, cu)
+    os_, ls = orc.sparse_attn(w.q, w.k, w.v, idx, cu, 64)
+    ow, lw = orc.swa(w.q, w.k, w.v, cu, 512)
+    rb = [gen.f32_to_bf16_bits(x.astype(np.float32)) for x in (oc, os_, ow)]
+    saved = {"k_cmp": dev(kc), "v_cmp": dev(vc), "o_cmp": dev(rb[0]), "o_slc": dev(rb[1]), "o_swa": dev(rb[2]),
+             "lse_cmp": dev(lc.astype(np.float32)), "lse_slc": dev(ls.astype(np.float32)),
+             "lse_swa": dev(lw.astype(np.float32)), "idx": dev(idx)}
+    gq, gk, gv, gg = nsa.nsa_layer_bwd(dev(w.q), dev(w.k), dev(w.v), dev(w.gates), saved, dev(do), cu_seqlens=dcu,
+                                       max_seqlen=L)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    rq, rk, rv, rg = orc.layer_bwd(w.q, w.k, w.v, w.gates, idx, do, cu, branches=rb)
+    assert_close(gq, rq, what="layer dq")
+    assert_close(gk, rk, what="layer dk")
+    assert_close(gv, rv, what="layer dv")
+    assert_close(gg, rg, atol=1e-3, rtol=1e-3, what="layer d gates")
+
+
 # --------------------------------------------------------------------------- NOSA stage 2
 def test_cis_block_scores():
     lengths = [10, 31, 32, 47, 100, 700, 5000]
