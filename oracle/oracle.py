@@ -467,6 +467,40 @@ def decode(q, k_cache, v_cache, kc_cache, seqlens, kernel=32, stride=16, block_s
     return (idx, o, sc) if want_scores else (idx, o)
 
 
+def decode_cis(q, k_cache, v_cache, kc_cache, cis_cache, seqlens, qk_select, k=64, block_size=64, n_init=1,
+               n_local=2, scale=None, idx_in=None):
+    """NOSA decode step: the decode scores (S2, S3) of the newest query, the two-stage
+    selection (top qk_select by attention score, then top k by the CIS block score of the
+    sequence) and the CIS-weighted attention over the chosen blocks.  cis_cache [B, max_len,
+    hkv] (fp32); returns (idx [B, hkv, k], o [B, h, d] fp64, stage-1 scores [B, hkv, nb])."""
+    q = np.ascontiguousarray(q)
+    seqlens = _i32(seqlens)
+    B, h, d = q.shape
+    hkv = k_cache.shape[2]
+    idx1, _, sc = decode(q, k_cache, v_cache, kc_cache, seqlens, block_size=block_size, n_init=n_init,
+                         n_local=n_local, k=k, scale=scale, want_scores=True)
+    nb = sc.shape[2]
+    idx = np.zeros((B, hkv, k), np.int32)
+    o = np.zeros((B, h, d), np.float64)
+    for b in range(B):
+        L = int(seqlens[b])
+        cu = np.array([0, L], np.int32)
+        cs = cis_block_scores(cis_cache[b, :L], cu, block_size=block_size, nb_stride=nb)
+        rows = [L - 1]
+        if idx_in is None:
+            sc_rows = np.zeros((1, hkv, nb))
+            sc_rows[0] = sc[b]
+            idx[b] = topk_two_stage(sc_rows, cs, cu, qk_select, k, block_size, n_init, n_local, rows=rows)[0]
+        else:
+            idx[b] = np.asarray(idx_in)[b]
+        full_idx = np.zeros((L, hkv, k), np.int32)
+        full_idx[L - 1] = idx[b]
+        ob, _ = sparse_attn_cis(q[b][None].repeat(L, 0), k_cache[b, :L], v_cache[b, :L], cis_cache[b, :L],
+                                full_idx, cu, block_size, scale, rows=rows)
+        o[b] = ob[0]
+    return idx, o, sc
+
+
 def layer(q, k, v, gates, cu, kernel=32, stride=16, block_size=64, S=16, n_init=1, n_local=2,
           window=512, scale=None, idx_in=None, rows=None, branches=False):
     """Three-branch layer; returns dict with idx, o (and o_cmp/o_slc/o_swa if branches)."""

@@ -912,3 +912,23 @@ def test_layer_bwd_equals_autograd_of_the_layer():
     loss.backward()
     for ours, ref, what in ((dq, Q.grad, "dq"), (dk, K.grad, "dk"), (dv, V.grad, "dv"), (dg, A.grad, "dgate")):
         assert torch.allclose(torch.from_numpy(ours), ref, atol=2e-6, rtol=1e-5), what
+
+
+def test_decode_cis_reductions():
+    """cis = 1 and qk_select = k reduce the NOSA decode step to the plain decode step; with
+    qk_select covering every causal block the choice is S4 on the CIS block scores."""
+    w = gen.decode(B=3, L=1500, seqlens=[1500, 700, 90], topk=8, H=8, HKV=2)
+    ncs = orc.num_cmp(1500)
+    kc = np.zeros((3, ncs, 2, 128), np.uint16)
+    for b in range(3):
+        kc[b] = orc.compress(w.k_cache[b], [0, 1500])[1]
+    ones = np.ones((3, 1500, 2), np.float32)
+    i0, o0 = orc.decode(w.q, w.k_cache, w.v_cache, kc, w.seqlens, k=8)
+    i1, o1, _ = orc.decode_cis(w.q, w.k_cache, w.v_cache, kc, ones, w.seqlens, 8, k=8)
+    assert np.array_equal(i0, i1) and np.allclose(o0, o1, atol=1e-12)
+    cis = gen.cis_scores(np.random.default_rng(181), 3 * 1500, 2).reshape(3, 1500, 2)
+    i2, _, _ = orc.decode_cis(w.q, w.k_cache, w.v_cache, kc, cis, w.seqlens, 64, k=8)
+    for b, L in enumerate([1500, 700, 90]):
+        cs = orc.cis_block_scores(cis[b, :L], np.array([0, L], np.int32), nb_stride=24)
+        want = orc.topk(cs[0][None], np.array([0, L], np.int32), 64, 1, 2, 8, rows=[L - 1])[0]
+        assert np.array_equal(i2[b], want)
