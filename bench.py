@@ -225,6 +225,15 @@ def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
     byts = w.batch * w.hkv * n_c * w.d * 2 + keys * w.d * 2 * 2 + 2 * w.batch * w.h * w.d * 2
     ms_step = float(np.mean(ms))
     gbs = byts / (ms_step * 1e-3) / 1e9
+    # the NOSA decode step: CIS-weighted attention and two-stage selection (k = 64 of
+    # qk_select = 64, so stage 2 keeps every stage-1 block; the weights change the output)
+    cis = dev(torch, gen.cis_scores(gen.rng_for(3, 77), w.batch * w.max_len, w.hkv), device)
+    nbs = -(-w.max_len // 64)
+    cb = nsa.nsa_cis_block_scores(cis, batch=w.batch, seqlen=w.max_len, nb_stride=nbs)
+    cis3 = cis.view(w.batch, w.max_len, w.hkv)
+    ms_nosa = float(np.mean(timed(torch, lambda: nsa.nsa_sparse_decode_cis(
+        q, kc_, vc_, kcmp, cis3, sl, cb, 64, k=w.topk, workspace=ws, idx_out=idx, out=out), steps, warmup, flush)))
+    del cis, cb, cis3
     # compressing the cache (timed separately: one HBM pass over 537 MB)
     msc = timed(torch, lambda: nsa.nsa_compress_k(kc_, out=kcmp.view(-1, w.hkv, w.d)), steps, warmup, flush)
     cbytes = kc_.numel() * 2 + kcmp.numel() * 2
@@ -235,6 +244,7 @@ def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy"},
             "launches_per_step": 2, "memsets_per_step": 1, "cuda_graph": True,
+            "nosa_step_ms": ms_nosa,
             "compress_cache": {"ms": float(np.mean(msc)), "gbs": cgbs, "hbm_frac": cgbs / peaks["hbm_gbs"],
                                "bytes": int(cbytes)}}
 

@@ -330,6 +330,27 @@ NSA_API nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_
                              int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The NOSA decode step ([NOSA-Parts] "decoding over only 64 KV blocks", core component
+ * 3): nsa_sparse_decode with the CIS-weighted attention of nsa_sparse_cis_fwd over the
+ * chosen blocks, and, when cis_block_scores is given, the two-stage selection of
+ * nsa_topk_two_stage (stage 1 keeps the forced blocks and the best qk_select blocks by
+ * attention score, stage 2 keeps the k best of those by block CIS score).
+ *   cis_cache         [batch, max_len, h_kv] fp32 (>= 0), device or page-locked host memory
+ *   cis_block_scores  nullable [batch, h_kv, nb_stride] fp32: the block CIS scores of each
+ *                     sequence (nsa_cis_block_scores over the sequence's own length; only
+ *                     the blocks that stage 1 can keep are read: with n_local >= 1 the
+ *                     query's own block is forced, and a dense call over the padded cache
+ *                     gives the same selection)
+ * Other arguments, workspace (nsa_sparse_decode_workspace_size) and limits as
+ * nsa_sparse_decode; k <= qk_select <= 64 when cis_block_scores is given. */
+NSA_API nsa_status nsa_sparse_decode_cis(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d,
+                                         const void* q, const void* k_cache, const void* v_cache,
+                                         const void* k_cmp_cache, const float* cis_cache,
+                                         const float* cis_block_scores, int nb_stride, int qk_select, int kernel,
+                                         int stride, int block_size, int n_init, int n_local, int k, float scale,
+                                         int32_t* idx_out, void* o, void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
 /* Allocation-free variant of nsa_sparse_decode, for callers that cannot allocate device
  * memory when they run a decode step (code inside an allocator or memory-pool callback,
  * runtimes that pre-reserve all device memory, plug-ins handed only their input and

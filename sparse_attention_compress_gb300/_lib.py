@@ -66,6 +66,9 @@ _SIGS = {
     "nsa_sparse_decode_workspace_size": ([_c_int] * 9, _c_sz),
     "nsa_sparse_decode": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
+    "nsa_sparse_decode_cis": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                               _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p,
+                               _c_sz, _c_p], _c_int),
     "nsa_sparse_decode_noalloc_max_bytes": ([], _c_sz),
     "nsa_sparse_decode_noalloc": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int,
                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
@@ -453,6 +456,27 @@ def nsa_sparse_decode(q, k_cache, v_cache, k_cmp_cache, seqlens, k=64, kernel=32
                                     _ptr(k_cmp_cache), kernel, stride, block_size, n_init, n_local, k, float(scale),
                                     _ptr(idx_out), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
            "nsa_sparse_decode")
+    return out
+
+
+def nsa_sparse_decode_cis(q, k_cache, v_cache, k_cmp_cache, cis_cache, seqlens, cis_block_scores=None, qk_select=0,
+                          k=64, kernel=32, stride=16, block_size=64, n_init=1, n_local=2, scale=0.0, *,
+                          workspace=None, idx_out=None, out=None, stream=None):
+    """NOSA decode step: CIS-weighted attention, two-stage selection when cis_block_scores
+    [B, Hkv, nb_stride] is given.  cis_cache [B, max_len, Hkv] fp32."""
+    B, h, d = q.shape
+    max_len, h_kv = k_cache.shape[1], k_cache.shape[2]
+    if workspace is None:
+        ws = nsa_sparse_decode_workspace_size(B, max_len, h, h_kv, d, kernel, stride, block_size, k)
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    nb_stride = 0 if cis_block_scores is None else cis_block_scores.shape[-1]
+    _check(load().nsa_sparse_decode_cis(B, _ptr(seqlens), max_len, h, h_kv, d, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(k_cmp_cache), _ptr(cis_cache), _ptr(cis_block_scores), nb_stride,
+                                        qk_select, kernel, stride, block_size, n_init, n_local, k, float(scale),
+                                        _ptr(idx_out), _ptr(out), _ptr(workspace), workspace.numel(),
+                                        _stream(stream)), "nsa_sparse_decode_cis")
     return out
 
 

@@ -92,10 +92,11 @@ const char* nsa_last_error(void) { return g_err; }
 
 nsa_status nsa_device_status(int32_t* status, int reset) {
   NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
-  int32_t a = 0, b = 0;
+  int32_t a = 0, b = 0, c = 0;
   cudaError_t e = status_word_dense_tc(&a, reset != 0);
   if (e == cudaSuccess) e = status_word_decode(&b, reset != 0);
-  *status = a ? a : b;
+  if (e == cudaSuccess) e = status_word_decode_nosa(&c, reset != 0);
+  *status = a ? a : b ? b : c;
   return cuda_status(e, "nsa_device_status");
 }
 
@@ -593,11 +594,11 @@ size_t nsa_sparse_decode_workspace_size(int batch, int max_len, int h, int h_kv,
   return decode_layout(batch, max_len, h, h_kv, d, kernel, stride, block_size, k).total;
 }
 
-nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d,
-                             const void* q, const void* k_cache, const void* v_cache,
-                             const void* k_cmp_cache, int kernel, int stride, int block_size,
-                             int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
-                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+static nsa_status decode_call(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d, const void* q,
+                              const void* k_cache, const void* v_cache, const void* k_cmp_cache, int kernel,
+                              int stride, int block_size, int n_init, int n_local, int k, float scale,
+                              int32_t* idx_out, void* o, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                              const float* cis_cache, const float* cis_block, int cis_nb_stride, int qk_select) {
   NSA_REQUIRE(batch >= 0 && max_len >= 1 && h > 0 && h_kv > 0 && h % h_kv == 0, NSA_ERR_INVALID,
               "nsa_sparse_decode: bad sizes");
   NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
@@ -648,7 +649,46 @@ nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int
   a.part_ml = reinterpret_cast<float*>(w + l.part_ml);
   a.counters = reinterpret_cast<int*>(w + l.counters);
   a.n_split = l.n_split;
+  if (cis_cache) {
+    const void* cp = nullptr;
+    if (nsa_status st = gpu_address(cis_cache, &cp, "cis_cache")) return st;
+    a.cis = static_cast<const float*>(cp);
+    a.cis_block = cis_block;
+    a.cis_nb_stride = cis_nb_stride;
+    a.qk = qk_select;
+  }
   return cuda_status(launch_decode(a, stream), "nsa_sparse_decode");
+}
+
+nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d,
+                             const void* q, const void* k_cache, const void* v_cache,
+                             const void* k_cmp_cache, int kernel, int stride, int block_size,
+                             int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return decode_call(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
+                     block_size, n_init, n_local, k, scale, idx_out, o, workspace, workspace_bytes, stream, nullptr,
+                     nullptr, 0, 0);
+}
+
+nsa_status nsa_sparse_decode_cis(int batch, const int32_t* seqlens, int max_len, int h, int h_kv, int d,
+                                 const void* q, const void* k_cache, const void* v_cache, const void* k_cmp_cache,
+                                 const float* cis_cache, const float* cis_block_scores, int nb_stride,
+                                 int qk_select, int kernel, int stride, int block_size, int n_init, int n_local,
+                                 int k, float scale, int32_t* idx_out, void* o, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  NSA_REQUIRE(cis_cache != nullptr && (reinterpret_cast<uintptr_t>(cis_cache) & 3u) == 0, NSA_ERR_INVALID,
+              "nsa_sparse_decode_cis: cis_cache must be non-null and 4-byte aligned");
+  if (cis_block_scores) {
+    NSA_REQUIRE((reinterpret_cast<uintptr_t>(cis_block_scores) & 3u) == 0, NSA_ERR_INVALID,
+                "nsa_sparse_decode_cis: cis_block_scores misaligned");
+    NSA_REQUIRE(qk_select >= k && qk_select <= 64, NSA_ERR_UNSUPPORTED,
+                "nsa_sparse_decode_cis: needs k <= qk_select <= 64");
+    NSA_REQUIRE(nb_stride >= (max_len + block_size - 1) / (block_size > 0 ? block_size : 1), NSA_ERR_INVALID,
+                "nsa_sparse_decode_cis: nb_stride < blocks of max_len");
+  }
+  return decode_call(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
+                     block_size, n_init, n_local, k, scale, idx_out, o, workspace, workspace_bytes, stream, cis_cache,
+                     cis_block_scores, nb_stride, qk_select);
 }
 
 // Layer workspace: compressed K and V, V^T of the compressed and of the full values

@@ -104,6 +104,7 @@ cudaError_t launch_scores_tc(const Seqs& s, const void* q, const void* k_cmp, in
 // optionally cleared.
 cudaError_t status_word_dense_tc(int32_t* out, bool reset);
 cudaError_t status_word_decode(int32_t* out, bool reset);
+cudaError_t status_word_decode_nosa(int32_t* out, bool reset);
 
 cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gates, void* o, cudaStream_t st);
@@ -122,6 +123,11 @@ struct DecodeArgs {
   float* part_ml;  // [batch, hkv * rtiles, n_split, 16, 2]
   int* counters;  // DecodeLayout::counter_bytes: queue head, arrivals, ready flags (zeroed per call)
   int n_split;
+  // NOSA decode (optional; null = plain decode): per-key CIS [batch, max_len, hkv] fp32 and
+  // block CIS scores [batch, hkv, cis_nb_stride] fp32 with stage-1 size qk (k <= qk <= 64)
+  const float* cis = nullptr;
+  const float* cis_block = nullptr;
+  int cis_nb_stride = 0, qk = 0;
 };
 struct DecodeLayout {
   size_t z, tile_ml, idx, part_o, part_ml, counters, counter_bytes, total;
@@ -130,5 +136,7 @@ struct DecodeLayout {
 DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int kernel, int stride,
                            int block_size, int k);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+// The NOSA variant (a.cis set): decode_nosa.cu; launch_decode calls it after the memset.
+cudaError_t launch_decode_nosa(const DecodeArgs& a, const DecodeLayout& l, cudaStream_t st);
 
 }  // namespace nsa

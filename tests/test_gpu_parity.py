@@ -673,6 +673,62 @@ def test_decode_offloaded_cache(B, L, seqlens, k, H, HKV):
     assert_close(out_h, ref_o, what="decode offloaded")
 
 
+def _stage1_near_tie_rows(sc, seqlens, qk, n_init=1, n_local=2, tau=1e-6):
+    """Rows whose stage-1 cut (the qk-th kept block) has a near tie in the oracle's scores."""
+    B, hkv, nb = sc.shape
+    near = np.zeros((B, hkv), bool)
+    for b in range(B):
+        own = (int(seqlens[b]) - 1) // 64
+        for g in range(hkv):
+            free = [j for j in range(own + 1) if not (j < n_init or j > own - n_local)]
+            nf = own + 1 - len(free)
+            keep = qk - nf
+            if 0 < keep < len(free):
+                s_ = np.sort(sc[b, g, free])[::-1]
+                near[b, g] = s_[keep - 1] - s_[keep] < tau * 16
+    return near
+
+
+@pytest.mark.parametrize("B,L,seqlens,k,qk,H,HKV", [(4, 4096, [4096, 2500, 700, 1], 16, 32, 16, 2),
+                                                    (3, 3000, [3000, 1500, 40], 64, 64, 16, 1),
+                                                    (5, 1500, [1500, 31, 64, 65, 1200], 4, 12, 8, 2)])
+def test_decode_cis(B, L, seqlens, k, qk, H, HKV):
+    """NOSA decode: two-stage selection and CIS-weighted attention."""
+    w, kc_cache = _decode_case(B, L, seqlens, k, 0, H=H, HKV=HKV)
+    cis = gen.cis_scores(_rng(71), B * L, HKV).reshape(B, L, HKV)
+    nb = -(-L // 64)
+    cb = nsa.nsa_cis_block_scores(dev(cis.reshape(B * L, HKV)), batch=B, seqlen=L, nb_stride=nb)
+    idx = torch.empty((B, HKV, k), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode_cis(dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(kc_cache), dev(cis),
+                                    dev(w.seqlens), cb, qk, k=k, idx_out=idx)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    gi = host(idx)
+    ref_idx, _, sc = orc.decode_cis(w.q, w.k_cache, w.v_cache, kc_cache, cis, w.seqlens, qk, k=k)
+    near = _stage1_near_tie_rows(sc, w.seqlens, qk)
+    diff = np.any(gi != ref_idx, axis=2)
+    assert not np.any(diff & ~near), np.argwhere(diff & ~near)
+    _, ref_o, _ = orc.decode_cis(w.q, w.k_cache, w.v_cache, kc_cache, cis, w.seqlens, qk, k=k, idx_in=gi)
+    assert_close(out, ref_o, what="decode cis")
+
+
+def test_decode_cis_weights_only_keeps_the_plain_selection():
+    """Without block CIS scores the choice is the plain decode's, bit for bit; the output is
+    the CIS-weighted attention over it."""
+    w, kc_cache = _decode_case(3, 2048, [2048, 2047, 1000], 16, 0)
+    cis = gen.cis_scores(_rng(72), 3 * 2048, 2).reshape(3, 2048, 2)
+    cis[1, :100] = 0.0
+    i0 = torch.empty((3, 2, 16), dtype=torch.int32, device="cuda")
+    i1 = torch.empty_like(i0)
+    nsa.nsa_sparse_decode(dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(kc_cache), dev(w.seqlens), k=16, idx_out=i0)
+    out = nsa.nsa_sparse_decode_cis(dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(kc_cache), dev(cis),
+                                    dev(w.seqlens), k=16, idx_out=i1)
+    torch.cuda.synchronize()
+    assert torch.equal(i0, i1)
+    _, ref_o, _ = orc.decode_cis(w.q, w.k_cache, w.v_cache, kc_cache, cis, w.seqlens, 16, k=16, idx_in=host(i1))
+    assert_close(out, ref_o, what="decode cis weights only")
+
+
 def test_decode_offloaded_full_size_sampled():
     """B=32, context 32768, H=16, Hkv=2, d=128, top-k 64 with the 1 GB K/V cache in
     page-locked host memory; the oracle checks eight sampled sequences."""
