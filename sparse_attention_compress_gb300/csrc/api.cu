@@ -92,11 +92,12 @@ const char* nsa_last_error(void) { return g_err; }
 
 nsa_status nsa_device_status(int32_t* status, int reset) {
   NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
-  int32_t a = 0, b = 0, c = 0;
+  int32_t a = 0, b = 0, c = 0, f = 0;
   cudaError_t e = status_word_dense_tc(&a, reset != 0);
   if (e == cudaSuccess) e = status_word_decode(&b, reset != 0);
   if (e == cudaSuccess) e = status_word_decode_nosa(&c, reset != 0);
-  *status = a ? a : b ? b : c;
+  if (e == cudaSuccess) e = status_word_sparse_fwd(&f, reset != 0);
+  *status = a ? a : b ? b : c ? c : f;
   return cuda_status(e, "nsa_device_status");
 }
 

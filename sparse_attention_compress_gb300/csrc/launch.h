@@ -105,6 +105,7 @@ cudaError_t launch_scores_tc(const Seqs& s, const void* q, const void* k_cmp, in
 cudaError_t status_word_dense_tc(int32_t* out, bool reset);
 cudaError_t status_word_decode(int32_t* out, bool reset);
 cudaError_t status_word_decode_nosa(int32_t* out, bool reset);
+cudaError_t status_word_sparse_fwd(int32_t* out, bool reset);
 
 cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gates, void* o, cudaStream_t st);
