@@ -36,7 +36,7 @@ METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roo
 # DRAM bytes (read + write) of one prefill launch from the ncu capture summarised in
 # profiles/sparse_fwd_mma_prefill_b2.md: 248.7 MB at B=2, x4 for the B=8 launch (the
 # traffic grows with the number of query tokens)
-PREFILL_NCU_TRAFFIC = 4 * (153.22e6 + 94.12e6)
+PREFILL_NCU_TRAFFIC = 4 * (153.12e6 + 99.52e6)  # ncu, sparse_fwd_tma<2> at B=2, scaled to B=8
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -639,7 +639,7 @@ def main():
                    "seq_len": 16384, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (258 MB written, then 258 MB copied; outside the event pair)",
                    "flops_per_step": flops},
-        "roofline": {"kernel": "sparse_fwd_mma<128,64,2>", "bound": "tensor", "achieved": kernel_tflops,
+        "roofline": {"kernel": "sparse_fwd_tma<2>", "bound": "tensor", "achieved": kernel_tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"],
                      "peak_source": peaks["source"] + " bf16 dense (cuBLAS burst)",
                      "traffic": PREFILL_NCU_TRAFFIC if args.batch == 8 else None,
