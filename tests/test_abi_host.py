@@ -159,3 +159,59 @@ def test_cmp_attn_bwd_rejects_unsupported():
     assert lib.nsa_cmp_attn_bwd(*args(_shape(seqlen=70000))) == 2
     assert lib.nsa_cmp_attn_bwd(*args(_shape(), wsb=8)) == 1
     assert lib.nsa_compress_bwd(ctypes.byref(_shape(d=12)), FAKE, 32, 16, FAKE, None) == 2
+
+
+def test_new_entry_points_reject_bad_arguments():
+    """Validation before any launch for the NOSA, backward and layer-training calls."""
+    lib = nsa.load()
+    s = _shape()
+    # NOSA stage 2
+    assert lib.nsa_cis_block_scores(ctypes.byref(s), FAKE, 32, 16, 64, 1, FAKE, None) == 1  # nb_stride too small
+    assert lib.nsa_topk_two_stage(ctypes.byref(s), FAKE, 2, FAKE, 64, 1, 2, 8, 16, FAKE, None) == 2  # k > qk
+    assert lib.nsa_topk_two_stage(ctypes.byref(s), FAKE, 2, FAKE, 64, 1, 2, 65, 16, FAKE, None) == 2  # qk > 64
+    assert lib.nsa_sparse_cis_fwd(ctypes.byref(_shape(dtype=_lib.NSA_F32)), FAKE, FAKE, FAKE, FAKE, FAKE, 16, 64,
+                                  0.0, FAKE, None, None) == 2
+    assert lib.nsa_sparse_cis_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, 16, 32, 0.0, FAKE, None, None) == 2
+    assert lib.nsa_sparse_cis_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, None, FAKE, 16, 64, 0.0, FAKE, None, None) == 1
+    # NOSA decode: null CIS cache, qk outside [k, 64]
+    dec = lambda cis, cb, qk: lib.nsa_sparse_decode_cis(  # noqa: E731
+        2, FAKE, 4096, 16, 2, 128, FAKE, FAKE, FAKE, FAKE, cis, cb, 64, qk, 32, 16, 64, 1, 2, 16, 0.0, None, FAKE,
+        FAKE, 1 << 30, None)
+    assert dec(None, None, 0) == 1
+    assert dec(FAKE, FAKE, 8) == 2
+    assert dec(FAKE, FAKE, 65) == 2
+    # sliding-window and gate backward
+    sw = lambda window, ws=FAKE, wsb=1 << 40: lib.nsa_swa_bwd(  # noqa: E731
+        ctypes.byref(s), FAKE, FAKE, FAKE, window, 0.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, wsb, None)
+    assert sw(1985) == 2 and sw(0) == 2
+    assert sw(512, wsb=8) == 1
+    assert lib.nsa_gate_combine_bwd(10, 4, 12, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 2
+    assert lib.nsa_gate_combine_bwd(10, 4, 128, FAKE, FAKE, FAKE, FAKE, MIS, FAKE, FAKE, FAKE, FAKE, None) == 1
+    # layer training pair
+    assert lib.nsa_layer_fwd_train(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 16, 1, 2, 512, 0.0, FAKE,
+                                   None, FAKE, 1 << 40, None) == 1
+    assert lib.nsa_layer_bwd(ctypes.byref(_shape(d=64)), FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 16, 512, 0.0, None,
+                             FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 2
+    assert lib.nsa_layer_bwd(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 16, 4000, 0.0, None,
+                             FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 2
+    assert lib.nsa_layer_bwd(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 16, 512, 0.0, None,
+                             FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 1  # saved is NULL
+
+
+@pytest.mark.parametrize("T,h,hkv,window", [(65536, 64, 4, 512), (1000, 16, 2, 1984)])
+def test_layer_bwd_workspace_size(T, h, hkv, window):
+    """Branch gradients, per-branch dq/dk/dv and compressed-key gradients, plus the largest
+    branch-backward scratch (used in turn)."""
+    lib = nsa.load()
+    s = _shape(seqlen=T, h=h, h_kv=hkv)
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    qsz, ksz = T * h * 128 * 2, T * hkv * 128 * 2
+    ncr = (T - 32) // 16 + 1
+    off = 0
+    for sz in (3 * qsz, 3 * qsz, 3 * ksz, 3 * ksz, ncr * hkv * 256, ncr * hkv * 256):
+        off = a256(off + sz)
+    scratch = max(lib.nsa_sparse_bwd_workspace_size(ctypes.byref(s), 16, 64),
+                  lib.nsa_cmp_attn_bwd_workspace_size(ctypes.byref(s), 32, 16),
+                  lib.nsa_swa_bwd_workspace_size(ctypes.byref(s), window))
+    got = lib.nsa_layer_bwd_workspace_size(ctypes.byref(s), 32, 16, 64, 16, window)
+    assert got == a256(off + scratch)
