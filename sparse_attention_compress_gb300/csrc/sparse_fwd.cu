@@ -126,7 +126,10 @@ __device__ __forceinline__ uint32_t tma_addr(uint32_t base, int row, int chunk) 
   return base + ((chunk >> 3) << 11) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-template <int NSTAGE>
+// With W, each key's weight (NOSA CIS, p.w [tokens, hkv]) multiplies its softmax weight
+// before the PV product and the normaliser; a stage's 16 weights arrive by 4-byte cp.async
+// into a small array of their own (the TMA stages keep their 1 KB alignment).
+template <int NSTAGE, bool W = false>
 __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
     sparse_fwd_tma(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const SparseParams p) {
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_list[NW][64];
   __shared__ __align__(8) uint64_t s_bar[NW][NSTAGE];
+  __shared__ float s_w[W ? NW : 1][W ? NSTAGE : 1][16];
   const uint32_t smem = (smem_u32(smem_raw) + 1023) & ~1023u;  // swizzle atoms need 1 KB alignment
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -188,12 +192,27 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
     tc::tma2d(sb + SLICE + 2048, &tm_v, x0 + 64, y, bar);
   };
 
+  // weights of slice i (lanes 0-15, one key each; zero past the query); one commit group
+  // per call so that the groups count like the stages
+  auto issue_w = [&](int i) {
+    if (W && lane < 16 && i < cnt) {
+      const int64_t key = (int64_t)list[i] * BS + slice * 16 + lane;
+      const bool kok = key <= t;
+      const float* src = p.w + (kv_base + (kok ? key : 0)) * p.hkv + g;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(&s_w[W ? warp : 0][W ? i % NSTAGE : 0][lane])),
+                   "l"(src), "r"(kok ? 4 : 0)
+                   : "memory");
+    }
+    if (W) cp_async_commit();
+  };
+
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   WarpState st{kNegInf, kNegInf, 0.f, 0.f};
   if (lane == 0)
     for (int i = 0; i < NSTAGE - 1 && i < cnt; ++i) issue(i);
+  for (int i = 0; i < NSTAGE - 1; ++i) issue_w(i);
   int issued = min(cnt, NSTAGE - 1);
   bool ok = true;
   int i = 0;
@@ -202,10 +221,15 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
       if (lane == 0) issue(i + NSTAGE - 1);
       ++issued;
     }
+    issue_w(i + NSTAGE - 1);
     const uint32_t bar = bar0 + (i % NSTAGE) * 8;
     if (!tc::warp_wait(bar, (i / NSTAGE) & 1, nullptr)) {
       ok = false;
       break;
+    }
+    if (W) {
+      cp_async_wait<NSTAGE - 1>();
+      __syncwarp();
     }
     const uint32_t sb = wbase + (i % NSTAGE) * STAGE;
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -265,6 +289,17 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
       pr[nt][2] = ex2(s[nt][2] - mu1);
       pr[nt][3] = ex2(s[nt][3] - mu1);
     }
+    if (W) {
+      const float* sw = s_w[W ? warp : 0][W ? i % NSTAGE : 0];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float w0 = sw[nt * 8 + (lane & 3) * 2], w1 = sw[nt * 8 + (lane & 3) * 2 + 1];
+        pr[nt][0] *= w0;
+        pr[nt][1] *= w1;
+        pr[nt][2] *= w0;
+        pr[nt][3] *= w1;
+      }
+    }
     st.l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
     st.l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
     const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
@@ -285,6 +320,7 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
   if (!ok) {  // a copy never arrived (the status word is set): drain what is in flight
     for (int k = i; k < issued; ++k) tc::warp_wait(bar0 + (k % NSTAGE) * 8, (k / NSTAGE) & 1, nullptr);
   }
+  if (W) cp_async_wait<0>();
   st.l0 = quad_sum(st.l0);
   st.l1 = quad_sum(st.l1);
   __syncthreads();  // every warp is done with its ring: the merge reuses the shared memory
@@ -308,6 +344,7 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
   }
 }
 
+template <bool W>
 static cudaError_t run_tma(const SparseParams& p, const Seqs& s, int hkv, dim3 grid, cudaStream_t st) {
   constexpr int NS = NSA_PREFILL_NSTAGE;
   constexpr int pipe = 4 * NS * 2 * 16 * 128 * 2 + 1024;
@@ -319,7 +356,7 @@ static cudaError_t run_tma(const SparseParams& p, const Seqs& s, int hkv, dim3 g
   const uint32_t box[2] = {64, 16};
   if (!tc::make_map(&mk, p.k, 2, dims, strides, box) || !tc::make_map(&mv, p.v, 2, dims, strides, box))
     return cudaErrorInvalidValue;
-  auto kern = sparse_fwd_tma<NS>;
+  auto kern = sparse_fwd_tma<NS, W>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, 128, bytes, st>>>(mk, mv, p);
@@ -431,7 +468,7 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   p.scale_log2 = scale * kLog2e;
   const int r = h / hkv;
   dim3 grid((unsigned)s.tokens, hkv * ((r + 15) / 16), 1);
-  if (!cis && d == 128 && block_size == 64) return run_tma(p, s, hkv, grid, st);
+  if (d == 128 && block_size == 64) return cis ? run_tma<true>(p, s, hkv, grid, st) : run_tma<false>(p, s, hkv, grid, st);
   if (cis) {  // CIS-weighted variant: block 64 only (checked by the caller)
     constexpr int NS = NSA_PREFILL_NSTAGE;
     return d == 128 ? run_mma<128, 64, NS, true>(p, grid, st) : run_mma<64, 64, NS, true>(p, grid, st);
