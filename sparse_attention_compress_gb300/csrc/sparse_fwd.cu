@@ -9,9 +9,11 @@
 // GB300 design.  One CTA serves one (query token, kv-head) and every query head of the
 // group (up to 16 rows: the M of one m16n8k16 tile).  Its four warps split each 64-key
 // block into four 16-key slices; each warp streams its slice of every listed block
-// through a private cp.async ring and keeps its own online softmax (warp_attend), and
-// the warps merge their (max, sum, O) states once at the end (cta_merge).  Warps never
-// wait on one another inside the loop, so no CTA-wide barrier sits on the gather path.
+// through a private ring and keeps its own online softmax, and the warps merge their
+// (max, sum, O) states once at the end (cta_merge).  Warps never wait on one another
+// inside the loop, so no CTA-wide barrier sits on the gather path.  The ring is fed by
+// TMA for d 128 with blocks of 64 (sparse_fwd_tma, below) and by cp.async otherwise
+// (sparse_fwd_mma, through warp_attend).
 #include "attend.cuh"
 #include "launch.h"
 #include "sm100.cuh"
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(128) sparse_fwd_f32(const float* __restrict__ 
                                                       const float* __restrict__ v, const int32_t* __restrict__ idx,
                                                       float* __restrict__ o, float* __restrict__ lse, Seqs seqs,
                                                       int h, int hkv, int d, int S, int bs, float scale) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int max_keys = S * bs;
   int* keys = reinterpret_cast<int*>(smem);
   float* sc = reinterpret_cast<float*>(keys + max_keys);  // [4][max_keys]
@@ -468,18 +470,14 @@ cudaError_t launch_sparse_fwd(const Seqs& s, const void* q, const void* k, const
   p.scale_log2 = scale * kLog2e;
   const int r = h / hkv;
   dim3 grid((unsigned)s.tokens, hkv * ((r + 15) / 16), 1);
+  // d 128 with blocks of 64: the TMA-fed kernel (plain or CIS-weighted)
   if (d == 128 && block_size == 64) return cis ? run_tma<true>(p, s, hkv, grid, st) : run_tma<false>(p, s, hkv, grid, st);
-  if (cis) {  // CIS-weighted variant: block 64 only (checked by the caller)
-    constexpr int NS = NSA_PREFILL_NSTAGE;
-    return d == 128 ? run_mma<128, 64, NS, true>(p, grid, st) : run_mma<64, 64, NS, true>(p, grid, st);
-  }
+  constexpr int NS = NSA_PREFILL_NSTAGE;
+  if (cis) return run_mma<64, 64, NS, true>(p, grid, st);  // CIS-weighted, d 64 (block 64: checked by the caller)
   if (d == 128) {
-    constexpr int NS = NSA_PREFILL_NSTAGE;
-    if (block_size == 64) return run_mma<128, 64, NS>(p, grid, st);
     if (block_size == 32) return run_mma<128, 32, NS>(p, grid, st);
     return run_mma<128, 16, NS>(p, grid, st);
   }
-  constexpr int NS = NSA_PREFILL_NSTAGE;
   if (block_size == 64) return run_mma<64, 64, NS>(p, grid, st);
   if (block_size == 32) return run_mma<64, 32, NS>(p, grid, st);
   return run_mma<64, 16, NS>(p, grid, st);
