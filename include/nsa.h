@@ -73,12 +73,14 @@ NSA_API const char* nsa_version(void);
 /* Message of the last failed call made by this thread ("" if none). */
 NSA_API const char* nsa_last_error(void);
 
-/* Device status word of the current device.  Kernels that wait on the tensor-core
- * pipeline (the tcgen05 branches of nsa_layer_fwd) bound every wait to about a second;
- * when one runs out the kernel sets the word to NSA_ERR_TIMEOUT, skips its output and
- * releases its tensor memory, so the context stays usable; while the word is set, those
- * kernels skip their work (outputs of such calls are not valid).  Runtime error
- * reporting, with no counterpart in the pages.
+/* Device status word of the current device.  Kernels that wait on other warps, copies
+ * or CTAs (the tcgen05 branches of nsa_layer_fwd, the TMA-fed selected attention, the
+ * decode step's wait for a row's block list) bound every wait to about a second;
+ * when one runs out the kernel sets the word to NSA_ERR_TIMEOUT, stops waiting, drains
+ * its copies in flight and releases its tensor memory, so the context stays usable; while
+ * the word is set, the tcgen05 branches and the decode step skip their work.  Outputs of a
+ * call that set the word are not valid.  Runtime error reporting, with no counterpart in
+ * the pages.
  *   status  host int32 out: NSA_OK or NSA_ERR_TIMEOUT
  *   reset   nonzero: clear the word after reading it
  * Blocks until the device is idle (a synchronous copy).  Returns NSA_ERR_INVALID for a
