@@ -664,7 +664,7 @@ def main():
                      "gathered_bytes": gathered, "gather_gbs": gathered / (ms_step * 1e-3) / 1e9},
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps + e2e_steps,
+        "gpu_launches": args.steps + w.batch * e2e_steps,  # the e2e step launches one kernel per sequence
         "clocks": clk,
     }
     del hq, hk, hv, hi, ho
