@@ -215,3 +215,86 @@ def test_layer_bwd_workspace_size(T, h, hkv, window):
                   lib.nsa_swa_bwd_workspace_size(ctypes.byref(s), window))
     got = lib.nsa_layer_bwd_workspace_size(ctypes.byref(s), 32, 16, 64, 16, window)
     assert got == a256(off + scratch)
+
+
+def test_select_block_mask_cmp_layer_reject_bad_arguments():
+    """The entry points without a dedicated host check above: each rejects an
+    unsupported or malformed argument with its status and a message, before any launch."""
+    lib = nsa.load()
+    s = _shape()  # B 1, T 128, h 16, h_kv 1, d 128, bf16
+    ref = ctypes.byref
+
+    def select(shape=s, kernel=32, k=16, n_init=1, ws=P(0x10000), ws_bytes=1 << 20):
+        return lib.nsa_select(ref(shape), FAKE, FAKE, kernel, 16, 64, 0.0, n_init, 2, k, FAKE, ws, ws_bytes, None)
+
+    assert select(kernel=16) == 2
+    assert select(k=65) == 2
+    assert select(n_init=-1) == 1
+    assert select(shape=_shape(d=96)) == 2
+    assert select(shape=_shape(dtype=_lib.NSA_F32)) == 2
+    assert select(ws=P(0x10100 + 16)) == 1 and b"aligned" in lib.nsa_last_error()
+    assert select(ws_bytes=512) == 1 and b"workspace" in lib.nsa_last_error()
+    assert select(ws=None) == 1
+
+    def block_mask(shape, block_size=64, mask=FAKE, ws_bytes=1 << 30):
+        return lib.nsa_block_sparse_fwd(ref(shape), FAKE, FAKE, FAKE, mask, block_size, 1, 0.0, FAKE, None, FAKE,
+                                        ws_bytes, None)
+
+    mh = dict(h=2, h_kv=2)
+    assert block_mask(_shape()) == 2  # needs h_kv == h
+    assert block_mask(_shape(d=64, **mh)) == 2
+    assert block_mask(_shape(seqlen=100, **mh)) == 2
+    assert block_mask(_shape(**mh), block_size=32) == 2
+    assert block_mask(_shape(**mh), mask=None) == 1
+    assert block_mask(_shape(**mh), ws_bytes=256) == 1 and b"workspace" in lib.nsa_last_error()
+
+    def cmp_fwd(shape=s, kernel=32, lse=None):
+        return lib.nsa_cmp_attn_fwd(ref(shape), FAKE, FAKE, FAKE, kernel, 16, 0.0, FAKE, lse, None)
+
+    assert cmp_fwd(shape=_shape(dtype=_lib.NSA_F32)) == 2
+    assert cmp_fwd(shape=_shape(h=12, h_kv=4)) == 2  # group of 3 heads
+    assert cmp_fwd(kernel=0) == 1
+    assert cmp_fwd(lse=P(0x10002)) == 1 and b"misaligned" in lib.nsa_last_error()
+
+    def layer(shape=s, kernel=32, S=16, window=512, ws_bytes=1 << 30):
+        return lib.nsa_layer_fwd(ref(shape), FAKE, FAKE, FAKE, FAKE, kernel, 16, 64, S, 1, 2, window, 0.0, FAKE,
+                                 None, FAKE, ws_bytes, None)
+
+    assert layer(kernel=16) == 2
+    assert layer(S=65) == 2
+    assert layer(window=0) == 1
+    assert layer(shape=_shape(h=32, h_kv=1)) == 2  # group of 32 heads: selection limit
+    need = lib.nsa_layer_fwd_workspace_size(ref(s), 32, 16, 64, 16)
+    assert need > 0 and need % 256 == 0
+    assert layer(ws_bytes=need - 1) == 1 and b"workspace" in lib.nsa_last_error()
+
+
+@pytest.mark.parametrize("B,T,hkv", [(1, 128, 1), (2, 1000, 2), (3, 64, 4)])
+def test_select_and_block_mask_workspace_sizes(B, T, hkv):
+    lib = nsa.load()
+    s = _shape(batch=B, seqlen=T, h=16, h_kv=hkv)
+    nb = -(-T // 64)
+    want = B * T * hkv * nb * 4
+    assert lib.nsa_select_workspace_size(ctypes.byref(s), 64) == -(-want // 256) * 256
+    assert lib.nsa_select_workspace_size(ctypes.byref(s), 0) == 0
+    m = _shape(batch=B, seqlen=T, h=hkv, h_kv=hkv)
+    ws = lib.nsa_block_sparse_workspace_size(ctypes.byref(m))
+    assert ws % 256 == 0 and ws >= hkv * 128 * B * T * 2  # V transposed per head, bf16
+    assert lib.nsa_block_sparse_workspace_size(ctypes.byref(_shape(h=0))) == 0
+
+
+def test_decode_noalloc_refuses_steps_beyond_its_scratch():
+    """A step whose scratch exceeds the fixed array is refused with the sizes, before any
+    CUDA call; malformed sizes fall through to the regular entry point's checks."""
+    lib = nsa.load()
+    cap = lib.nsa_sparse_decode_noalloc_max_bytes()
+    assert cap > 0
+    big = (256, 131072, 64, 4, 128, 32, 16, 64, 64)  # batch, max_len, h, h_kv, d, kernel, stride, block, k
+    assert lib.nsa_sparse_decode_workspace_size(*big) > cap
+    B, L, h, hkv, d, kern, st, bs, k = big
+    rc = lib.nsa_sparse_decode_noalloc(B, FAKE, L, h, hkv, d, FAKE, FAKE, FAKE, FAKE, kern, st, bs, 1, 2, k, 0.0,
+                                       None, FAKE, None)
+    assert rc == 2 and b"scratch" in lib.nsa_last_error()
+    rc = lib.nsa_sparse_decode_noalloc(2, FAKE, 1024, 0, 1, 128, FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 1, 2, 16, 0.0,
+                                       None, FAKE, None)
+    assert rc == 1
