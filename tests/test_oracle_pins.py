@@ -177,6 +177,47 @@ def test_pool_equals_avg_pool1d_ceil(n_c):
     assert np.all(got[m:] == 0)
 
 
+def test_cmp_scores_pool_equals_sdpa_then_avg_pool():
+    """S2+S3 in one call on ragged varlen sequences with GQA groups, a non-default scale,
+    a padded block stride and a row subset: the library SDPA's probabilities under the
+    window-end mask, summed over each group's heads, then avg_pool1d(3, 4, ceil_mode)
+    over the window axis; blocks past the pooled ones, rows without a causal window and
+    the stride padding are 0."""
+    lengths = [1, 31, 64, 65, 130, 257, 300]
+    cu = gen.varlen_cu_seqlens(lengths)
+    h, hkv, d, scale = 8, 2, 32, 0.3
+    r = h // hkv
+    q = _rand((cu[-1], h, d), 11)
+    k = _rand((cu[-1], hkv, d), 12)
+    _, kc = orc.compress(k, cu)
+    off = orc.cmp_offsets(cu)
+    nb_stride = -(-max(lengths) // 64) + 3
+    got = orc.cmp_scores_pool(q, kc, cu, scale=scale, nb_stride=nb_stride)
+    assert got.shape == (cu[-1], hkv, nb_stride)
+    for i, L in enumerate(lengths):
+        rows = slice(cu[i], cu[i + 1])
+        n_c = off[i + 1] - off[i]
+        ref = torch.zeros(L, hkv, nb_stride, dtype=F64)
+        if n_c > 0:
+            assert n_c >= 3  # avg_pool1d needs a full first window; the lengths above ensure it
+            t = torch.arange(L)[:, None]
+            mask = (16 * torch.arange(n_c)[None, :] + 31) <= t
+            live = mask.any(1)
+            qs = _t(q[rows])[live].permute(1, 0, 2)
+            ks = _t(kc[off[i]:off[i + 1]]).repeat_interleave(r, dim=1).permute(1, 0, 2)
+            eye = torch.eye(n_c, dtype=F64).expand(h, n_c, n_c)
+            probs = F.scaled_dot_product_attention(qs, ks, eye, attn_mask=mask[live], scale=scale)
+            pg = probs.permute(1, 0, 2).reshape(-1, hkv, r, n_c).sum(2)  # [live rows, hkv, n_c]
+            pooled = F.avg_pool1d(pg.reshape(-1, 1, n_c), 3, 4, ceil_mode=True).reshape(pg.shape[0], hkv, -1)
+            m = pooled.shape[-1]
+            assert m <= -(-L // 64)
+            ref[live, :, :m] = pooled
+        assert torch.allclose(torch.from_numpy(got[rows]), ref, atol=1e-13, rtol=0), L
+    sub = [0, 1, 40, cu[3] - 1, cu[5] + 200, cu[-1] - 1]
+    part = orc.cmp_scores_pool(q, kc, cu, scale=scale, nb_stride=nb_stride, rows=sub)
+    assert np.array_equal(part, got[sub])
+
+
 # --------------------------------------------------------------------------- S4
 def _check_topk_row(sc, t, bs, n_init, n_local, k, row):
     own = t // bs
