@@ -810,6 +810,46 @@ def test_select_fused_call():
     assert outside == 0
 
 
+def test_selection_full_size_sampled():
+    """The varlen selection workload at its stated size (4 packed sequences of 7733,
+    14932, 24577 and 8673 tokens, H 16, H_kv 2, d 128, top-16 with 1 initial and 2 local
+    blocks), through the same calls the benchmark times: compression checked on every
+    compressed key; block scores and block lists against the oracle on sampled rows (the
+    first and last row of every sequence, rows around the first compression window and
+    the first selection blocks, and random rows); the top-k of the GPU's own scores
+    bit-exact with the oracle's top-k of those scores on every row; the one-call
+    selection identical to the separate calls."""
+    w = gen.selection()
+    cu = w.cu_seqlens
+    assert list(np.diff(cu)) == [7733, 14932, 24577, 8673]
+    dcu = dev(cu)
+    kc = nsa.nsa_compress_k(dev(w.k), cu_seqlens=dcu, max_seqlen=w.max_len)
+    sc = nsa.nsa_cmp_scores_pool(dev(w.q), kc, w.hkv, cu_seqlens=dcu, max_seqlen=w.max_len)
+    idx = nsa.nsa_topk_select(sc, 16, cu_seqlens=dcu, max_seqlen=w.max_len)
+    one = nsa.nsa_select(dev(w.q), kc, w.hkv, k=16, cu_seqlens=dcu, max_seqlen=w.max_len)
+    torch.cuda.synchronize()
+    kch = host(kc)
+    exact, rounded = orc.compress(w.k, cu)
+    assert_close(kc, exact, atol=1e-6, rtol=2 ** -7, what="selection compress")
+    assert np.mean(kch == rounded) > 0.999
+    nb = sc.shape[-1]
+    assert nb == -(-w.max_len // 64)
+    starts, ends = cu[:-1], cu[1:] - 1
+    special = np.concatenate([starts, ends] + [starts + t for t in (30, 31, 32, 47, 63, 64, 127, 128, 1023)])
+    rows = np.unique(np.concatenate([_rng(13).integers(0, w.tokens, 400), special]))
+    ref_sc = orc.cmp_scores_pool(w.q, kch, cu, rows=rows, nb_stride=nb)
+    g_sc = host(sc)[rows].astype(np.float64)
+    assert np.all(g_sc[ref_sc == 0] == 0)
+    np.testing.assert_allclose(g_sc, ref_sc, rtol=1e-4, atol=1e-9)
+    gi = host(idx)
+    ref_idx = orc.topk(ref_sc, cu, k=16, rows=rows)
+    n_mis, outside = selection_mismatches(gi[rows], ref_idx, ref_sc, _t_of_rows(cu)[rows])
+    assert outside == 0, (n_mis, outside)
+    assert n_mis <= max(3, len(rows) * w.hkv // 200), n_mis
+    assert np.array_equal(gi, orc.topk(host(sc), cu, k=16))
+    assert np.array_equal(host(one), gi)
+
+
 def test_layer_varlen():
     """Packed sequences of ragged lengths (shorter than one compression window, one
     selection block, one sliding window, and longer): every tile of the tensor-core
