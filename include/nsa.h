@@ -87,6 +87,17 @@ NSA_API const char* nsa_last_error(void);
  * NULL status, NSA_ERR_CUDA when the copy fails. */
 NSA_API nsa_status nsa_device_status(int32_t* status, int reset);
 
+/* Limit of those bounded waits, in nanoseconds, on the current device (0 restores the
+ * default of one second).  It applies to the first-level waits (a role waiting for a copy,
+ * for the tensor cores or for another CTA's result); the waits with which a kernel that
+ * gave up drains its copies and tensor-core work in flight keep the one-second limit.  A
+ * diagnostic hook with no counterpart in the pages: a limit far below a wait's normal
+ * length makes the waits run out on purpose, so the give-up path (status word, drain,
+ * return) can be exercised and the caller's error handling tested.
+ * Synchronous (a copy to each kernel unit's constant); returns NSA_ERR_CUDA when it fails.
+ * Set it only while none of this library's kernels run. */
+NSA_API nsa_status nsa_set_wait_limit_ns(uint64_t ns);
+
 /* S1 -- key (or value) compression.  [NOSA-Parts] core component 1: keys are cut into
  * windows of `kernel` tokens at step `stride` and each window is mean-pooled;
  * [NOSA-Triton] "beyond the kernel": kernel 32, stride 16, 50% overlap.
@@ -361,10 +372,14 @@ NSA_API nsa_status nsa_sparse_decode_cis(int batch, const int32_t* seqlens, int 
  * scratch is a fixed array of nsa_sparse_decode_noalloc_max_bytes() bytes (16 MiB) in
  * device memory that the library owns; every GPU that loads the library holds it until
  * the process exits.  The caller still passes inputs and outputs.
- *   - Steps whose nsa_sparse_decode_workspace_size() exceeds the fixed size are rejected
- *     with NSA_ERR_UNSUPPORTED and a message naming both sizes.
+ *   - Sizes the decode step does not support are rejected first, with the status and
+ *     message of nsa_sparse_decode.  Supported steps whose
+ *     nsa_sparse_decode_workspace_size() exceeds the fixed size are then rejected with
+ *     NSA_ERR_UNSUPPORTED and a message naming both sizes.
  *   - The first call on a device looks up the array's device address (a CUDA runtime
- *     symbol query, no allocation); make that first call before any stream capture.
+ *     symbol query, no allocation); make that first call before any stream capture.  The
+ *     address is kept per device and CUDA context: after a device reset (a new context,
+ *     with a new copy of the array) the next call looks it up again.
  *   - All calls share the one array, which keeps the last call's contents; every byte a
  *     call reads is written earlier in the same call, so nothing needs clearing.  Calls
  *     that overlap on the GPU (other streams, other host threads) race on it: order them.

@@ -84,6 +84,20 @@ void nsa::set_error(const char* fmt, ...) {
   va_end(ap);
 }
 
+nsa_status nsa::decode_check_sizes(int batch, int max_len, int h, int h_kv, int d, int kernel, int stride,
+                                   int block_size, int n_init, int n_local, int k) {
+  NSA_REQUIRE(batch >= 0 && max_len >= 1 && h > 0 && h_kv > 0 && h % h_kv == 0, NSA_ERR_INVALID,
+              "nsa_sparse_decode: bad sizes");
+  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
+              "nsa_sparse_decode: supports kernel 32, stride 16, block_size 64");
+  NSA_REQUIRE(d == 128, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: d must be 128");
+  NSA_REQUIRE(pow2_le16(h / h_kv), NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: h/h_kv must be 1, 2, 4, 8 or 16");
+  NSA_REQUIRE(k >= 1 && k <= 64, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: k must be in [1, 64]");
+  NSA_REQUIRE(n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "nsa_sparse_decode: negative n_init/n_local");
+  NSA_REQUIRE(max_len <= 65536, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: max_len must be <= 65536");
+  return NSA_OK;
+}
+
 extern "C" {
 
 const char* nsa_version(void) { return "nsa-gb300 0.1 (sm_103a)"; }
@@ -99,6 +113,15 @@ nsa_status nsa_device_status(int32_t* status, int reset) {
   if (e == cudaSuccess) e = status_word_sparse_fwd(&f, reset != 0);
   *status = a ? a : b ? b : c ? c : f;
   return cuda_status(e, "nsa_device_status");
+}
+
+nsa_status nsa_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns ? (unsigned long long)ns : 1000000000ull;
+  cudaError_t e = wait_limit_dense_tc(v);
+  if (e == cudaSuccess) e = wait_limit_decode(v);
+  if (e == cudaSuccess) e = wait_limit_decode_nosa(v);
+  if (e == cudaSuccess) e = wait_limit_sparse_fwd(v);
+  return cuda_status(e, "nsa_set_wait_limit_ns");
 }
 
 nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,
@@ -600,15 +623,8 @@ static nsa_status decode_call(int batch, const int32_t* seqlens, int max_len, in
                               int stride, int block_size, int n_init, int n_local, int k, float scale,
                               int32_t* idx_out, void* o, void* workspace, size_t workspace_bytes, cudaStream_t stream,
                               const float* cis_cache, const float* cis_block, int cis_nb_stride, int qk_select) {
-  NSA_REQUIRE(batch >= 0 && max_len >= 1 && h > 0 && h_kv > 0 && h % h_kv == 0, NSA_ERR_INVALID,
-              "nsa_sparse_decode: bad sizes");
-  NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
-              "nsa_sparse_decode: supports kernel 32, stride 16, block_size 64");
-  NSA_REQUIRE(d == 128, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: d must be 128");
-  NSA_REQUIRE(pow2_le16(h / h_kv), NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: h/h_kv must be 1, 2, 4, 8 or 16");
-  NSA_REQUIRE(k >= 1 && k <= 64, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: k must be in [1, 64]");
-  NSA_REQUIRE(n_init >= 0 && n_local >= 0, NSA_ERR_INVALID, "nsa_sparse_decode: negative n_init/n_local");
-  NSA_REQUIRE(max_len <= 65536, NSA_ERR_UNSUPPORTED, "nsa_sparse_decode: max_len must be <= 65536");
+  if (nsa_status st = decode_check_sizes(batch, max_len, h, h_kv, d, kernel, stride, block_size, n_init, n_local, k))
+    return st;
   if (batch == 0) return NSA_OK;
   NSA_PTR(seqlens);
   NSA_PTR(q);

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "nsa.h"
 
 namespace nsa {
 
@@ -14,6 +15,11 @@ enum DType { kF32 = 0, kBF16 = 1 };
 
 // Record the message returned by nsa_last_error() for the calling thread.
 void set_error(const char* fmt, ...);
+
+// Size checks of the decode step (kernel/stride/block, d, group size, k, max_len), the
+// first checks of nsa_sparse_decode; NSA_OK or the status with nsa_last_error() set.
+nsa_status decode_check_sizes(int batch, int max_len, int h, int h_kv, int d, int kernel, int stride,
+                              int block_size, int n_init, int n_local, int k);
 
 cudaError_t launch_compress(const Seqs& s, const void* k, void* k_cmp, int hkv, int d, int dtype,
                             int kernel, int stride, cudaStream_t st);
@@ -106,6 +112,11 @@ cudaError_t status_word_dense_tc(int32_t* out, bool reset);
 cudaError_t status_word_decode(int32_t* out, bool reset);
 cudaError_t status_word_decode_nosa(int32_t* out, bool reset);
 cudaError_t status_word_sparse_fwd(int32_t* out, bool reset);
+// Limit (ns) of the first-level bounded waits of each of those units.
+cudaError_t wait_limit_dense_tc(unsigned long long ns);
+cudaError_t wait_limit_decode(unsigned long long ns);
+cudaError_t wait_limit_decode_nosa(unsigned long long ns);
+cudaError_t wait_limit_sparse_fwd(unsigned long long ns);
 
 cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gates, void* o, cudaStream_t st);

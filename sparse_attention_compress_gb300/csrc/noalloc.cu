@@ -8,6 +8,8 @@
 // fixed-size array in device memory that this library owns.  That array is a
 // file-scope __device__ object: every GPU that loads the library holds it until the
 // process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "nsa.h"
@@ -24,23 +26,63 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // CUDA context the address belongs to (0: unknown)
+  void* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once per
-// device (host code cannot use the array's name as a device pointer).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context, or 0 when there is none or it
+// cannot be read.  A device reset or a context torn down and created again gets a new id
+// (and a new copy of the scratch array), so a cached address is only reused within the
+// context it was looked up in.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+    looked_up = true;
+  }
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device.  Host code cannot use the
+// array's name as a device pointer: the address is asked of the runtime once per device
+// and context (the first call on a device does this set-up; make that first call before
+// any stream capture), and asked again whenever the current context has changed.
 cudaError_t scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& s = g_scratch[dev];
+  const unsigned long long id = current_context_id();
+  if (!s.ptr || id == 0 || id != s.ctx_id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // also makes the device's context current
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    s.ptr = p;
+    s.ctx_id = current_context_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return cudaSuccess;
 }
 
@@ -54,10 +96,11 @@ extern "C" NSA_API nsa_status nsa_sparse_decode_noalloc(int batch, const int32_t
                                                       int stride, int block_size, int n_init, int n_local, int k,
                                                       float scale, int32_t* idx_out, void* o,
                                                       cudaStream_t stream) {
+  // sizes the decode step does not support get the regular entry point's message
+  if (nsa_status st = decode_check_sizes(batch, max_len, h, h_kv, d, kernel, stride, block_size, n_init, n_local, k))
+    return st;
+  if (batch == 0) return NSA_OK;
   const size_t need = nsa_sparse_decode_workspace_size(batch, max_len, h, h_kv, d, kernel, stride, block_size, k);
-  if (need == 0)  // malformed sizes: the regular entry point reports which argument is wrong
-    return nsa_sparse_decode(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
-                             block_size, n_init, n_local, k, scale, idx_out, o, nullptr, 0, stream);
   if (need > kScratchBytes) {
     set_error("nsa_sparse_decode_noalloc: this step needs %zu bytes of scratch, more than the fixed %zu bytes; "
               "use nsa_sparse_decode with a caller-provided workspace",
@@ -70,7 +113,7 @@ extern "C" NSA_API nsa_status nsa_sparse_decode_noalloc(int batch, const int32_t
     set_error("nsa_sparse_decode_noalloc: cannot resolve the scratch array: %s", cudaGetErrorString(e));
     return NSA_ERR_CUDA;
   }
-  // every other check (shapes, pointers, limits) is the regular entry point's
+  // every other check (pointers, alignment, memory kinds) is the regular entry point's
   return nsa_sparse_decode(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
                            block_size, n_init, n_local, k, scale, idx_out, o, scratch, kScratchBytes, stream);
 }

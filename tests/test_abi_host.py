@@ -284,17 +284,30 @@ def test_select_and_block_mask_workspace_sizes(B, T, hkv):
 
 
 def test_decode_noalloc_refuses_steps_beyond_its_scratch():
-    """A step whose scratch exceeds the fixed array is refused with the sizes, before any
-    CUDA call; malformed sizes fall through to the regular entry point's checks."""
+    """A supported step whose scratch exceeds the fixed array is refused with the sizes,
+    before any CUDA call; sizes the decode step does not support get the regular entry
+    point's message, not the scratch one."""
     lib = nsa.load()
     cap = lib.nsa_sparse_decode_noalloc_max_bytes()
     assert cap > 0
-    big = (256, 131072, 64, 4, 128, 32, 16, 64, 64)  # batch, max_len, h, h_kv, d, kernel, stride, block, k
+    big = (1024, 32768, 16, 2, 128, 32, 16, 64, 64)  # batch, max_len, h, h_kv, d, kernel, stride, block, k
     assert lib.nsa_sparse_decode_workspace_size(*big) > cap
     B, L, h, hkv, d, kern, st, bs, k = big
     rc = lib.nsa_sparse_decode_noalloc(B, FAKE, L, h, hkv, d, FAKE, FAKE, FAKE, FAKE, kern, st, bs, 1, 2, k, 0.0,
                                        None, FAKE, None)
-    assert rc == 2 and b"scratch" in lib.nsa_last_error()
+    assert rc == 2
+    msg = lib.nsa_last_error()
+    assert b"scratch" in msg and str(cap).encode() in msg
+    # unsupported sizes whose scratch would also exceed the array: the size check speaks
+    for args, word in [((256, 131072, 64, 4, 128, 32, 16, 64, 64), b"max_len"),
+                       ((1024, 32768, 16, 2, 128, 32, 16, 64, 65), b"k must"),
+                       ((1024, 32768, 16, 2, 64, 32, 16, 64, 64), b"d must"),
+                       ((1024, 32768, 16, 2, 128, 64, 16, 64, 64), b"kernel 32")]:
+        B, L, h, hkv, d, kern, st, bs, k = args
+        rc = lib.nsa_sparse_decode_noalloc(B, FAKE, L, h, hkv, d, FAKE, FAKE, FAKE, FAKE, kern, st, bs, 1, 2, k,
+                                           0.0, None, FAKE, None)
+        msg = lib.nsa_last_error()
+        assert rc == 2 and word in msg and b"scratch" not in msg, (args, msg)
     rc = lib.nsa_sparse_decode_noalloc(2, FAKE, 1024, 0, 1, 128, FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 1, 2, 16, 0.0,
                                        None, FAKE, None)
     assert rc == 1

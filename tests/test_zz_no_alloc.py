@@ -45,6 +45,21 @@ def test_noalloc_decode_matches_regular_decode_twice():
         assert_close(out, _f64(ref), what="noalloc decode")
 
 
+@pytest.mark.gpu
+def test_noalloc_decode_keeps_its_block_lists_in_the_shared_array():
+    """Without idx_out the block lists live in the shared array too.  A larger step first
+    leaves its lists (and everything else) there; a smaller step after it, with other
+    inputs, must still give the regular call's output."""
+    big = _case(8, 8192, [8192, 8000, 5000, 4097, 100, 64, 33, 1], 3)
+    small = _case(4, 4096, [4096, 1, 2500, 700], 4)
+    for q, kc, vc, kcmp, sl, w in (big, small):
+        ref = nsa.nsa_sparse_decode(q, kc, vc, kcmp, sl, k=64)
+        out = torch.full_like(q, float("nan"))
+        nsa.nsa_sparse_decode_noalloc(q, kc, vc, kcmp, sl, k=64, out=out)
+        torch.cuda.synchronize()
+        assert_close(out, _f64(ref), what="noalloc decode without idx_out")
+
+
 def _f64(t):
     return host(t.float()).astype(np.float64)
 
