@@ -35,6 +35,7 @@ _SIGS = {
     "nsa_version": ([], ctypes.c_char_p),
     "nsa_last_error": ([], ctypes.c_char_p),
     "nsa_device_status": ([_c_p, _c_int], _c_int),
+    "nsa_set_wait_limit_ns": ([ctypes.c_uint64], _c_int),
     "nsa_compress_k": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_p], _c_int),
     "nsa_cmp_scores_pool": ([_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_p, _c_p, _c_int, _c_p], _c_int),
     "nsa_topk_select": ([_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p], _c_int),
@@ -499,6 +500,11 @@ def nsa_device_status(reset: bool = False) -> int:
     st = ctypes.c_int32(0)
     _check(load().nsa_device_status(ctypes.byref(st), int(bool(reset))), "nsa_device_status")
     return int(st.value)
+
+
+def nsa_set_wait_limit_ns(ns: int = 0) -> None:
+    """Limit of the kernels' first-level bounded waits in ns (0: the default second)."""
+    _check(load().nsa_set_wait_limit_ns(int(ns)), "nsa_set_wait_limit_ns")
 
 
 def nsa_layer_fwd_workspace_size(shape: NsaShape, kernel=32, stride=16, block_size=64, S=16) -> int:

@@ -550,24 +550,24 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
   if (*abort) {
     // drain: copies and MMAs still in flight must land before the CTA leaves
     if (warp == 4) {
-      mbar_wait(bar(B_Q), 0, nullptr);
+      mbar_drain(bar(B_Q), 0);
       for (int st = 0; st < NS; ++st) {
         const int ik = last_in_stage(last_k, st), iv = last_in_stage(last_v, st);
-        if (ik >= 0) mbar_wait(bar(B_KFULL + st), (ik / NS) & 1, nullptr);
-        if (iv >= 0) mbar_wait(bar(B_VFULL + st), (iv / NS) & 1, nullptr);
+        if (ik >= 0) mbar_drain(bar(B_KFULL + st), (ik / NS) & 1);
+        if (iv >= 0) mbar_drain(bar(B_VFULL + st), (iv / NS) & 1);
       }
     } else if (warp == 5) {
       if (lane == 0) commit(bar(B_DRAIN));
       __syncwarp();
-      mbar_wait(bar(B_DRAIN), 0, nullptr);
+      mbar_drain(bar(B_DRAIN), 0);
     }
   } else if (warp == 4) {
     // every MMA completion that arrives on a ring barrier lands before the CTA leaves:
     // wait for the last release of each stage
     for (int st = 0; st < NS; ++st) {
       const int ik = last_in_stage(last_k, st), iv = last_in_stage(last_v, st);
-      if (ik >= 0) mbar_wait(bar(B_KEMPTY + st), (ik / NS) & 1, nullptr);
-      if (iv >= 0) mbar_wait(bar(B_VEMPTY + st), (iv / NS) & 1, nullptr);
+      if (ik >= 0) mbar_drain(bar(B_KEMPTY + st), (ik / NS) & 1);
+      if (iv >= 0) mbar_drain(bar(B_VEMPTY + st), (iv / NS) & 1);
     }
   }
   fence_before();

@@ -15,17 +15,30 @@ namespace nsa {
 // host with NSA_STATUS_ACCESSOR(name); nsa_device_status reads all of them.
 static __device__ int g_device_status = 0;
 
+// Limit of the unit's first-level waits (a copy or a peer's result that a role waits
+// for), in ns; the waits that only drain copies and tensor-core work already in flight
+// keep the fixed one-second limit.  nsa_set_wait_limit_ns sets it in every unit.
+static __device__ unsigned long long g_wait_ns = 1000000000ull;
+
 #define NSA_STATUS_ACCESSOR(name)                                                  \
   cudaError_t status_word_##name(int32_t* out, bool reset) {                       \
     cudaError_t e = cudaMemcpyFromSymbol(out, g_device_status, sizeof(int));       \
     if (e != cudaSuccess || !reset) return e;                                      \
     const int zero = 0;                                                            \
     return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));                \
+  }                                                                                \
+  cudaError_t wait_limit_##name(unsigned long long ns) {                           \
+    return cudaMemcpyToSymbol(g_wait_ns, &ns, sizeof(ns));                         \
   }
 
 namespace tc {
 
-constexpr unsigned long long kWaitNs = 1000000000ull;  // an mbarrier wait longer than 1 s is stuck
+constexpr unsigned long long kWaitNs = 1000000000ull;  // a drain wait longer than 1 s is stuck
+
+// Current limit of the first-level waits (g_wait_ns, default one second).
+__device__ __forceinline__ unsigned long long wait_limit() {
+  return *reinterpret_cast<volatile unsigned long long*>(&g_wait_ns);
+}
 
 // Shared-memory matrix descriptor of a K-major tile of rows x 64 bf16 in the layout TMA
 // writes with 128-byte swizzling (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4),
@@ -94,26 +107,34 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 // Wait for phase `parity` of an mbarrier.  Gives up (false) when *abort is set by
-// another role, or after kWaitNs, in which case it sets *abort and the device status.
-// abort == nullptr: time limit only (used while draining).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
+// another role, or once the limit has passed, in which case it sets *abort and the
+// device status.  First-level waits (drain == false) take the unit's limit
+// (wait_limit()); drain waits take the fixed kWaitNs.  abort == nullptr: time limit only.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort, bool drain) {
+  const unsigned long long lim = drain ? kWaitNs : wait_limit();
   const unsigned long long t0 = globaltimer();
   for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     if (abort && *abort) return false;
-    if (globaltimer() - t0 > kWaitNs) break;
+    if (globaltimer() - t0 >= lim) break;
   }
   if (abort) *abort = 1;
   atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
   return false;
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort);
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort, false);
 }
-// Warp-uniform wait: every lane waits, the result is the AND over the warp.
+// Wait for copies or tensor-core work already in flight to land (before a CTA leaves).
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, nullptr, true);
+}
+// Warp-uniform waits: every lane waits, the result is the AND over the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+__device__ __forceinline__ bool warp_drain(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_drain(bar, parity));
 }
 
 __device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
     __syncwarp();
   }
   if (!ok) {  // a copy never arrived (the status word is set): drain what is in flight
-    for (int k = i; k < issued; ++k) tc::warp_wait(bar0 + (k % NSTAGE) * 8, (k / NSTAGE) & 1, nullptr);
+    for (int k = i; k < issued; ++k) tc::warp_drain(bar0 + (k % NSTAGE) * 8, (k / NSTAGE) & 1);
   }
   if (W) cp_async_wait<0>();
   st.l0 = quad_sum(st.l0);
