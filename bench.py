@@ -33,10 +33,12 @@ from sparse_attention_compress_gb300 import inputs as gen  # noqa: E402
 from sparse_attention_compress_gb300.dist import max_over_ranks  # noqa: E402
 
 METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roofline"
-# DRAM bytes (read + write) of one prefill launch from the ncu capture summarised in
-# profiles/sparse_fwd_mma_prefill_b2.md: 248.7 MB at B=2, x4 for the B=8 launch (the
-# traffic grows with the number of query tokens)
-PREFILL_NCU_TRAFFIC = 4 * (153.12e6 + 99.52e6)  # ncu, sparse_fwd_tma<2> at B=2, scaled to B=8
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the TMA-fed
+# prefill kernel sparse_fwd_tma<2>, captured by ncu at B=2 (153.12 MB read + 99.52 MB
+# written), times 4 for the B=8 launch: every query token reads its own Q row and writes
+# its own O row, and the K/V read grows with the batch in the same way.  None once the
+# kernel has changed since that capture.
+PREFILL_NCU_TRAFFIC = 4 * (153.12e6 + 99.52e6)
 L2_BYTES = 129 * 2 ** 20
 
 
