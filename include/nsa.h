@@ -93,7 +93,9 @@ NSA_API nsa_status nsa_device_status(int32_t* status, int reset);
  * gave up drains its copies and tensor-core work in flight keep the one-second limit.  A
  * diagnostic hook with no counterpart in the pages: a limit far below a wait's normal
  * length makes the waits run out on purpose, so the give-up path (status word, drain,
- * return) can be exercised and the caller's error handling tested.
+ * return) can be exercised and the caller's error handling tested.  A limit below one
+ * microsecond (finer than the device timer) makes a wait give up at its first
+ * unsuccessful probe.
  * Synchronous (a copy to each kernel unit's constant); returns NSA_ERR_CUDA when it fails.
  * Set it only while none of this library's kernels run. */
 NSA_API nsa_status nsa_set_wait_limit_ns(uint64_t ns);

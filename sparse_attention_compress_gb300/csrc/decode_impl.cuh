@@ -285,7 +285,7 @@ __device__ __forceinline__ void attn_item(const DecodeParams& p, int b, int g, i
     if (ld_acquire(&p.ready[row]) == 0) {
       const unsigned long long t0 = tc::globaltimer(), lim = tc::wait_limit();
       while (ld_acquire(&p.ready[row]) == 0) {
-        if (tc::device_status_set() || tc::globaltimer() - t0 >= lim) {
+        if (tc::device_status_set() || lim < tc::kQuickNs || tc::globaltimer() - t0 >= lim) {
           atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
           ok = 0;
           break;

@@ -17,8 +17,9 @@ static __device__ int g_device_status = 0;
 
 // Limit of the unit's first-level waits (a copy or a peer's result that a role waits
 // for), in ns; the waits that only drain copies and tensor-core work already in flight
-// keep the fixed one-second limit.  nsa_set_wait_limit_ns sets it in every unit.
-static __device__ unsigned long long g_wait_ns = 1000000000ull;
+// keep the fixed one-second limit.  nsa_set_wait_limit_ns sets it in every unit.  In
+// constant memory: every wait reads it, and between launches it does not change.
+static __constant__ unsigned long long g_wait_ns = 1000000000ull;
 
 #define NSA_STATUS_ACCESSOR(name)                                                  \
   cudaError_t status_word_##name(int32_t* out, bool reset) {                       \
@@ -35,10 +36,11 @@ namespace tc {
 
 constexpr unsigned long long kWaitNs = 1000000000ull;  // a drain wait longer than 1 s is stuck
 
-// Current limit of the first-level waits (g_wait_ns, default one second).
-__device__ __forceinline__ unsigned long long wait_limit() {
-  return *reinterpret_cast<volatile unsigned long long*>(&g_wait_ns);
-}
+// Current limit of the first-level waits (g_wait_ns, default one second).  A limit
+// below kQuickNs (finer than the timer's resolution) makes a wait give up at its first
+// unsuccessful probe.
+constexpr unsigned long long kQuickNs = 1000ull;
+__device__ __forceinline__ unsigned long long wait_limit() { return g_wait_ns; }
 
 // Shared-memory matrix descriptor of a K-major tile of rows x 64 bf16 in the layout TMA
 // writes with 128-byte swizzling (row r, 16-byte chunk c at r*128 + ((c ^ (r & 7)) << 4),
@@ -92,10 +94,32 @@ __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, int count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
+// Probe of phase `parity` that may suspend the thread until the phase completes (for a
+// time the hardware chooses).
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// The same probe, suspending for at most about `ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking probe.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
@@ -112,18 +136,22 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 // (wait_limit()); drain waits take the fixed kWaitNs.  abort == nullptr: time limit only.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort, bool drain) {
   const unsigned long long lim = drain ? kWaitNs : wait_limit();
-  const unsigned long long t0 = globaltimer();
-  for (;;) {
-    if (mbar_try(bar, parity)) return true;
-    if (abort && *abort) return false;
-    if (globaltimer() - t0 >= lim) break;
+  if (lim >= kQuickNs) {
+    const uint32_t hint = lim < 10000000ull ? (uint32_t)lim : 10000000u;  // suspend at most 10 ms per probe
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+      if (mbar_try_for(bar, parity, hint)) return true;
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 >= lim) break;
+    }
   }
   if (abort) *abort = 1;
   atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
   return false;
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort, false);
+  const bool quick = wait_limit() < kQuickNs;
+  return (quick ? mbar_test(bar, parity) : mbar_try(bar, parity)) || mbar_wait_slow(bar, parity, abort, false);
 }
 // Wait for copies or tensor-core work already in flight to land (before a CTA leaves).
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
