@@ -446,7 +446,9 @@ def bench_decode_offload(torch, nsa, device, steps, warmup, flush):
             "full_cache_bytes": full_bytes, "kernels_per_step": 1, "memsets_per_step": 1, "cuda_graph": True}
 
 
-def bench_selection(torch, nsa, device, steps, warmup, flush):
+def bench_selection(torch, nsa, device, steps, warmup, flush, peaks):
+    """Varlen selection stage: compress -> block scores -> top-16, each call timed on its own
+    (CUDA events between the calls of one step) against its own bound."""
     w = gen.selection()
     q, k = dev(torch, w.q, device), dev(torch, w.k, device)
     cu = dev(torch, w.cu_seqlens, device)
@@ -457,20 +459,45 @@ def bench_selection(torch, nsa, device, steps, warmup, flush):
     nb = (nb + 3) // 4 * 4
     sc = torch.empty((w.tokens, w.hkv, nb), dtype=torch.float32, device=device)
     idx = torch.empty((w.tokens, w.hkv, 16), dtype=torch.int32, device=device)
-
-    def step():
-        nsa.nsa_compress_k(k, cu_seqlens=cu, max_seqlen=w.max_len, out=kc)
-        nsa.nsa_cmp_scores_pool(q, kc, w.hkv, cu_seqlens=cu, max_seqlen=w.max_len, nb_stride=nb, out=sc)
-        nsa.nsa_topk_select(sc, 16, cu_seqlens=cu, max_seqlen=w.max_len, out=idx)
-
-    ms = float(np.mean(timed(torch, step, steps, warmup, flush)))
+    calls = [lambda: nsa.nsa_compress_k(k, cu_seqlens=cu, max_seqlen=w.max_len, out=kc),
+             lambda: nsa.nsa_cmp_scores_pool(q, kc, w.hkv, cu_seqlens=cu, max_seqlen=w.max_len, nb_stride=nb, out=sc),
+             lambda: nsa.nsa_topk_select(sc, 16, cu_seqlens=cu, max_seqlen=w.max_len, out=idx)]
+    for _ in range(warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in ev:
+        flush()
+        e[0].record()
+        for i, c in enumerate(calls):
+            c()
+            e[i + 1].record()
+    torch.cuda.synchronize()
+    seg = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]).mean(axis=0)
+    ms = float(np.mean([e[0].elapsed_time(e[3]) for e in ev]))
     t = np.concatenate([np.arange(L) for L in lens])
     ncaus = np.where(t >= 31, (t - 31) // 16 + 1, 0)
-    flops = float(ncaus.sum()) * w.h * 2 * w.d
+    pass_flops = float(ncaus.sum()) * w.h * 2 * w.d  # one pass of scores over the causal compressed keys
+    # the block scores take two passes over the keys (the softmax normaliser, then the
+    # probabilities pooled to blocks): twice the contraction, one exponential per (head, key) each
+    score_flops, score_exps = 2 * pass_flops, 2 * float(ncaus.sum()) * w.h
+    comp_bytes = w.tokens * w.hkv * w.d * 2 + n_cmp * w.hkv * w.d * 2  # K in, compressed keys out
+    own = np.concatenate([np.arange(L) // 64 for L in lens])
+    topk_bytes = float(np.minimum(own + 1, nb).sum()) * w.hkv * 4 + w.tokens * w.hkv * 16 * 4  # causal scores in, lists out
+    ms_c, ms_s, ms_k = (float(x) for x in seg)
     return {"workload": f"selection varlen lengths {lens.tolist()} H=16 Hkv=2 d=128 bf16 (compress 32/16, "
                         "pool to 64-token blocks, top-16 with 1 init + 2 local)",
-            "ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "qk_tflops": flops / (ms * 1e-3) / 1e12,
-            "launches_per_step": 3}
+            "ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "qk_tflops": pass_flops / (ms * 1e-3) / 1e12,
+            "launches_per_step": 3,
+            "compress": {"ms": ms_c, "bytes": comp_bytes, "gbs": comp_bytes / (ms_c * 1e-3) / 1e9,
+                         "hbm_frac": comp_bytes / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+            "scores": {"ms": ms_s, "flops": score_flops, "exps": score_exps,
+                       "tflops": score_flops / (ms_s * 1e-3) / 1e12,
+                       "tensor_frac": score_flops / (ms_s * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                       "exps_per_s": score_exps / (ms_s * 1e-3)},
+            "topk": {"ms": ms_k, "bytes": topk_bytes, "gbs": topk_bytes / (ms_k * 1e-3) / 1e9,
+                     "hbm_frac": topk_bytes / (ms_k * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
 
 
 def bench_block_sparse(torch, nsa, device, steps, warmup, flush, peaks, lengths=(1024, 4096, 16384)):
@@ -582,7 +609,7 @@ def main():
               "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode_offload": lambda: bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush),
-              "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush),
+              "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "block_sparse": lambda: bench_block_sparse(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "layer": lambda: bench_layer(torch, nsa, device, args.steps, args.warmup, flush,
                                            args.layer_tokens)}[args.only]
@@ -718,7 +745,7 @@ def main():
             line["decode_offload"] = {"error": repr(e)}
         torch.cuda.empty_cache()
         try:
-            line["selection"] = bench_selection(torch, nsa, device, args.steps, args.warmup, flush)
+            line["selection"] = bench_selection(torch, nsa, device, args.steps, args.warmup, flush, peaks)
             line["gpu_launches"] += 3 * args.steps
         except Exception as e:
             line["selection"] = {"error": repr(e)}
@@ -756,6 +783,25 @@ def main():
                 # no kernel can attend over the whole offloaded cache faster than it streams over the link
                 off["full_attention_floor_ms"] = off["full_cache_bytes"] / (pr["c2c_read_gbs"] * 1e9) * 1e3
                 off["speedup_vs_full_attention_floor"] = off["full_attention_floor_ms"] / off["ms_per_step"]
+            sel = line.get("selection", {})
+            if "scores" in sel and pr.get("ex2_per_sm_per_clk"):
+                # the block-score kernel against both of its units: the tensor cores (two
+                # passes of q.k) and the special-function unit (one ex2 per head and key per
+                # pass) at the probe's ex2 rate x SMs x clock
+                sco = sel["scores"]
+                ex2_peak = pr["ex2_per_sm_per_clk"] * pr["sms"] * pr["clock_mhz"] * 1e6
+                sco["mufu_peak_exps_per_s"] = ex2_peak
+                sco["mufu_frac"] = sco["exps_per_s"] / ex2_peak
+                mufu = sco["mufu_frac"] >= sco["tensor_frac"]
+                sel["roofline"] = {"kernel": "block scores (tc::attn_kernel, scores only)",
+                                   "bound": "alu" if mufu else "tensor",
+                                   "achieved": sco["exps_per_s"] / 1e9 if mufu else sco["tflops"],
+                                   "peak": ex2_peak / 1e9 if mufu else peaks["bf16_tflops"],
+                                   "unit": "Gexp/s" if mufu else "TFLOP/s",
+                                   "frac": sco["mufu_frac"] if mufu else sco["tensor_frac"],
+                                   "peak_source": ("live probe: ex2.approx per SM per clock x SMs x clock" if mufu
+                                                   else peaks["source"] + " bf16 dense (cuBLAS burst)"),
+                                   "traffic": None}
             if "tflops" in line.get("layer", {}):
                 line["layer"]["frac_of_bf16_peak"] = line["layer"]["tflops"] / peaks["bf16_tflops"]
         except Exception as e:

@@ -8,6 +8,10 @@
 
 #include "launch.h"
 
+// NVTX ranges name every entry point in a profiler's timeline (nvtx3 is header-only: with
+// no tool attached a range costs one pointer check).
+#include <nvtx3/nvToolsExt.h>
+
 using namespace nsa;
 
 namespace {
@@ -31,6 +35,12 @@ nsa_status cuda_status(cudaError_t e, const char* where) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+};
+#define NSA_RANGE() const Range nsa_range_(__func__)
 
 #define NSA_REQUIRE(cond, st, ...)     \
   do {                                 \
@@ -105,6 +115,7 @@ const char* nsa_version(void) { return "nsa-gb300 0.1 (sm_103a)"; }
 const char* nsa_last_error(void) { return g_err; }
 
 nsa_status nsa_device_status(int32_t* status, int reset) {
+  NSA_RANGE();
   NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
   int32_t a = 0, b = 0, c = 0, f = 0;
   cudaError_t e = status_word_dense_tc(&a, reset != 0);
@@ -116,6 +127,7 @@ nsa_status nsa_device_status(int32_t* status, int reset) {
 }
 
 nsa_status nsa_set_wait_limit_ns(uint64_t ns) {
+  NSA_RANGE();
   const unsigned long long v = ns ? (unsigned long long)ns : 1000000000ull;
   cudaError_t e = wait_limit_dense_tc(v);
   if (e == cudaSuccess) e = wait_limit_decode(v);
@@ -126,6 +138,7 @@ nsa_status nsa_set_wait_limit_ns(uint64_t ns) {
 
 nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, int kernel, int stride,
                           cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(kernel > 0 && stride > 0, NSA_ERR_INVALID, "nsa_compress_k: kernel and stride must be positive");
@@ -144,6 +157,7 @@ nsa_status nsa_compress_k(const nsa_shape* shape, const void* k, void* k_cmp, in
 nsa_status nsa_cmp_scores_pool(const nsa_shape* shape, const void* q, const void* k_cmp, int kernel,
                                int stride, int block_size, float scale, const float* lse_in,
                                float* block_scores, int nb_stride, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
@@ -169,6 +183,7 @@ nsa_status nsa_cmp_scores_pool(const nsa_shape* shape, const void* q, const void
 nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, int nb_stride,
                            int block_size, int n_init, int n_local, int k, int32_t* block_indices,
                            cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(block_size > 0 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID,
@@ -187,6 +202,7 @@ nsa_status nsa_topk_select(const nsa_shape* shape, const float* block_scores, in
 
 nsa_status nsa_cis_block_scores(const nsa_shape* shape, const float* cis, int kernel, int stride, int block_size,
                                 int nb_stride, float* out, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(kernel > 0 && stride > 0 && block_size > 0, NSA_ERR_INVALID,
@@ -203,6 +219,7 @@ nsa_status nsa_cis_block_scores(const nsa_shape* shape, const float* cis, int ke
 nsa_status nsa_topk_two_stage(const nsa_shape* shape, const float* block_scores, int nb_stride,
                               const float* cis_block_scores, int block_size, int n_init, int n_local, int qk_select,
                               int k, int32_t* block_indices, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(block_size > 0 && n_init >= 0 && n_local >= 0, NSA_ERR_INVALID,
@@ -224,6 +241,7 @@ nsa_status nsa_topk_two_stage(const nsa_shape* shape, const float* block_scores,
 nsa_status nsa_sparse_cis_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v, const float* cis,
                               const int32_t* block_indices, int S, int block_size, float scale, void* o, float* lse,
                               cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   const int r = shape->h / shape->h_kv;
@@ -271,6 +289,7 @@ nsa_status nsa_cmp_attn_bwd(const nsa_shape* shape, const void* q, const void* k
                             int stride, float scale, const void* o, const float* lse, const void* d_o, void* dq,
                             void* dk_cmp, void* dv_cmp, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = check_cmp_bwd(shape, kernel, stride, &s, __func__)) return st;
   if (s.tokens == 0) return NSA_OK;
@@ -299,6 +318,7 @@ nsa_status nsa_cmp_attn_bwd(const nsa_shape* shape, const void* q, const void* k
 
 nsa_status nsa_compress_bwd(const nsa_shape* shape, const void* dk_cmp, int kernel, int stride, void* dk,
                             cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_compress_bwd: bf16 only");
@@ -320,6 +340,7 @@ size_t nsa_swa_bwd_workspace_size(const nsa_shape* shape, int window) {
 nsa_status nsa_swa_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v, int window, float scale,
                        const void* o, const float* lse, const void* d_o, void* dq, void* dk, void* dv,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(shape->dtype == NSA_BF16, NSA_ERR_UNSUPPORTED, "nsa_swa_bwd: bf16 only");
@@ -352,6 +373,7 @@ nsa_status nsa_swa_bwd(const nsa_shape* shape, const void* q, const void* k, con
 nsa_status nsa_gate_combine_bwd(int64_t tokens, int h, int d, const void* d_o, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gate_logits, void* d_cmp, void* d_slc, void* d_swa,
                                 float* d_gate_logits, cudaStream_t stream) {
+  NSA_RANGE();
   NSA_REQUIRE(tokens >= 0 && h > 0 && d > 0, NSA_ERR_INVALID, "nsa_gate_combine_bwd: bad sizes");
   NSA_REQUIRE(d % 8 == 0 && d <= 256, NSA_ERR_UNSUPPORTED, "nsa_gate_combine_bwd: d must be a multiple of 8, <= 256");
   if (tokens == 0) return NSA_OK;
@@ -390,6 +412,7 @@ nsa_status nsa_sparse_bwd(const nsa_shape* shape, const void* q, const void* k, 
                           const int32_t* block_indices, int S, int block_size, float scale, const void* o,
                           const float* lse, const void* d_o, void* dq, void* dk, void* dv, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = check_sparse_bwd(shape, S, block_size, &s, __func__)) return st;
   if (s.tokens == 0) return NSA_OK;
@@ -424,6 +447,7 @@ size_t nsa_block_sparse_workspace_size(const nsa_shape* shape) {
 nsa_status nsa_block_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
                                 const uint8_t* block_mask, int block_size, int causal, float scale, void* o,
                                 float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(shape->cu_seqlens == nullptr, NSA_ERR_UNSUPPORTED, "nsa_block_sparse_fwd: dense layout only");
@@ -464,6 +488,7 @@ size_t nsa_select_workspace_size(const nsa_shape* shape, int block_size) {
 nsa_status nsa_select(const nsa_shape* shape, const void* q, const void* k_cmp, int kernel, int stride,
                       int block_size, float scale, int n_init, int n_local, int k, int32_t* block_indices,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   NSA_REQUIRE(kernel == 32 && stride == 16 && block_size == 64, NSA_ERR_UNSUPPORTED,
@@ -497,6 +522,7 @@ nsa_status nsa_select(const nsa_shape* shape, const void* q, const void* k_cmp, 
 nsa_status nsa_sparse_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
                           const int32_t* block_indices, int S, int block_size, float scale, void* o,
                           float* lse, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = make_seqs(shape, &s, __func__)) return st;
   const int r = shape->h / shape->h_kv;
@@ -538,6 +564,7 @@ static nsa_status dense_common(const nsa_shape* shape, Seqs* s, const char* fn) 
 nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k_cmp,
                             const void* v_cmp, int kernel, int stride, float scale, void* o, float* lse,
                             cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = dense_common(shape, &s, __func__)) return st;
   NSA_REQUIRE(kernel > 0 && stride > 0, NSA_ERR_INVALID, "nsa_cmp_attn_fwd: kernel and stride must be positive");
@@ -557,6 +584,7 @@ nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k
 
 nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v, int window,
                        float scale, void* o, float* lse, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = dense_common(shape, &s, __func__)) return st;
   NSA_REQUIRE(window >= 1, NSA_ERR_INVALID, "nsa_swa_fwd: window must be >= 1");
@@ -574,6 +602,7 @@ nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, con
 
 nsa_status nsa_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                             const void* o_swa, const float* gate_logits, void* o, cudaStream_t stream) {
+  NSA_RANGE();
   NSA_REQUIRE(tokens >= 0 && h > 0 && d > 0, NSA_ERR_INVALID, "nsa_gate_combine: bad sizes");
   NSA_REQUIRE(d % 8 == 0, NSA_ERR_UNSUPPORTED, "nsa_gate_combine: d must be a multiple of 8");
   if (tokens == 0) return NSA_OK;
@@ -682,6 +711,7 @@ nsa_status nsa_sparse_decode(int batch, const int32_t* seqlens, int max_len, int
                              const void* k_cmp_cache, int kernel, int stride, int block_size,
                              int n_init, int n_local, int k, float scale, int32_t* idx_out, void* o,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   return decode_call(batch, seqlens, max_len, h, h_kv, d, q, k_cache, v_cache, k_cmp_cache, kernel, stride,
                      block_size, n_init, n_local, k, scale, idx_out, o, workspace, workspace_bytes, stream, nullptr,
                      nullptr, 0, 0);
@@ -693,6 +723,7 @@ nsa_status nsa_sparse_decode_cis(int batch, const int32_t* seqlens, int max_len,
                                  int qk_select, int kernel, int stride, int block_size, int n_init, int n_local,
                                  int k, float scale, int32_t* idx_out, void* o, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   NSA_REQUIRE(cis_cache != nullptr && (reinterpret_cast<uintptr_t>(cis_cache) & 3u) == 0, NSA_ERR_INVALID,
               "nsa_sparse_decode_cis: cis_cache must be non-null and 4-byte aligned");
   if (cis_block_scores) {
@@ -848,6 +879,7 @@ nsa_status nsa_layer_fwd(const nsa_shape* shape, const void* q, const void* k, c
                          const float* gate_logits, int kernel, int stride, int block_size, int S,
                          int n_init, int n_local, int window, float scale, void* o, int32_t* idx_out,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   return layer_forward(shape, q, k, v, gate_logits, kernel, stride, block_size, S, n_init, n_local, window, scale, o,
                        idx_out, nullptr, workspace, workspace_bytes, stream, __func__);
 }
@@ -856,6 +888,7 @@ nsa_status nsa_layer_fwd_train(const nsa_shape* shape, const void* q, const void
                                const float* gate_logits, int kernel, int stride, int block_size, int S, int n_init,
                                int n_local, int window, float scale, void* o, const nsa_layer_saved* saved,
                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   NSA_REQUIRE(saved != nullptr, NSA_ERR_INVALID, "nsa_layer_fwd_train: saved is NULL");
   return layer_forward(shape, q, k, v, gate_logits, kernel, stride, block_size, S, n_init, n_local, window, scale, o,
                        nullptr, saved, workspace, workspace_bytes, stream, __func__);
@@ -919,6 +952,7 @@ nsa_status nsa_layer_bwd(const nsa_shape* shape, const void* q, const void* k, c
                          const float* gate_logits, int kernel, int stride, int block_size, int S, int window,
                          float scale, const nsa_layer_saved* saved, const void* d_o, void* dq, void* dk, void* dv,
                          float* d_gate_logits, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NSA_RANGE();
   Seqs s;
   if (nsa_status st = check_layer_bwd(shape, kernel, stride, block_size, S, window, &s, __func__)) return st;
   if (s.tokens == 0) return NSA_OK;

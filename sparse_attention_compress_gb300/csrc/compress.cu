@@ -53,23 +53,24 @@ struct Vec<float> {
   }
 };
 
-constexpr int kWindowsPerWarp = 16;
-constexpr int kCompressWarps = 8;
+constexpr int kMaxWindowsPerWarp = 16;
+constexpr int kCompressWarps = 4;
 
-// grid: (ceil(max n_c / (kWindowsPerWarp*kCompressWarps)), n_seqs).  Stride <= 32.
+// grid: (ceil(max n_c / (wpw*kCompressWarps)), n_seqs); each warp takes a run of wpw
+// windows (wpw <= 16, chosen by the launcher so that the grid fills the GPU).  Stride <= 32.
 template <typename T, int R>
-__global__ void __launch_bounds__(kCompressWarps * 32) compress_kernel(const T* __restrict__ k, T* __restrict__ kc,
+__global__ void __launch_bounds__(kCompressWarps * 32, 3) compress_kernel(const T* __restrict__ k, T* __restrict__ kc,
                                                                       Seqs s, int chunks, int stride,
-                                                                      float fkernel) {
+                                                                      float fkernel, int wpw) {
   using V = Vec<T>;
   const int sq = blockIdx.y;
   const int L = seq_len(s, sq);
   const int kernel = R * stride;
   const int n_c = num_cmp(L, kernel, stride);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c_begin = (blockIdx.x * kCompressWarps + warp) * kWindowsPerWarp;
+  const int c_begin = (blockIdx.x * kCompressWarps + warp) * wpw;
   if (c_begin >= n_c) return;
-  const int c_end = min(n_c, c_begin + kWindowsPerWarp);
+  const int c_end = min(n_c, c_begin + wpw);
   const int64_t start = seq_start(s, sq);
   const int64_t out0 = cmp_offset(s, sq, kernel, stride);
   const uint4* src = reinterpret_cast<const uint4*>(k);
@@ -91,13 +92,13 @@ __global__ void __launch_bounds__(kCompressWarps * 32) compress_kernel(const T* 
 #pragma unroll
       for (int e = 0; e < V::N; ++e) acc[e] = 0.f;
       const int64_t row0 = start + (int64_t)u * stride;
-      uint4 buf[8];
-      for (int i0 = 0; i0 < stride; i0 += 8) {
+      uint4 buf[16];  // the rows of one partial sum are in flight together
+      for (int i0 = 0; i0 < stride; i0 += 16) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 16; ++i)
           if (i0 + i < stride) buf[i] = __ldg(src + (row0 + i0 + i) * chunks + ch);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 16; ++i)
           if (i0 + i < stride) V::add(acc, buf[i]);
       }
 #pragma unroll
@@ -123,7 +124,15 @@ cudaError_t launch_compress(const Seqs& s, const void* k, void* k_cmp, int hkv, 
   const int R = kernel / stride;
   const int n_c_max = s.max_len >= kernel ? (s.max_len - kernel) / stride + 1 : 0;
   if (n_c_max == 0 || s.n_seqs == 0) return cudaSuccess;
-  const int per_cta = kWindowsPerWarp * kCompressWarps;
+  // windows per warp: long runs read each key row once (plus one partial sum of overlap
+  // per run), short runs give more warps; take the longest run (<= 16) that still gives
+  // about 32 warps per SM for the total number of windows
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t windows = (int64_t)s.n_seqs * n_c_max;  // an upper bound for packed sequences
+  int wpw = (int)(windows / ((int64_t)sms * 32));
+  wpw = wpw < 1 ? 1 : (wpw > kMaxWindowsPerWarp ? kMaxWindowsPerWarp : wpw);
+  const int per_cta = wpw * kCompressWarps;
   dim3 grid((n_c_max + per_cta - 1) / per_cta, s.n_seqs);
   const float inv = (float)kernel;  // the kernel divides the window sum by this
   const int threads = kCompressWarps * 32;
@@ -131,19 +140,19 @@ cudaError_t launch_compress(const Seqs& s, const void* k, void* k_cmp, int hkv, 
     const int chunks = hkv * d / 8;
     using T = __nv_bfloat16;
     switch (R) {
-      case 1: compress_kernel<T, 1><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
-      case 2: compress_kernel<T, 2><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
-      case 3: compress_kernel<T, 3><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
-      default: compress_kernel<T, 4><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
+      case 1: compress_kernel<T, 1><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
+      case 2: compress_kernel<T, 2><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
+      case 3: compress_kernel<T, 3><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
+      default: compress_kernel<T, 4><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
     }
   } else {
     const int chunks = hkv * d / 4;
     using T = float;
     switch (R) {
-      case 1: compress_kernel<T, 1><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
-      case 2: compress_kernel<T, 2><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
-      case 3: compress_kernel<T, 3><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
-      default: compress_kernel<T, 4><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv); break;
+      case 1: compress_kernel<T, 1><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
+      case 2: compress_kernel<T, 2><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
+      case 3: compress_kernel<T, 3><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
+      default: compress_kernel<T, 4><<<grid, threads, 0, st>>>((const T*)k, (T*)k_cmp, s, chunks, stride, inv, wpw); break;
     }
   }
   return cudaGetLastError();

@@ -128,6 +128,10 @@ __device__ __forceinline__ uint32_t tma_addr(uint32_t base, int row, int chunk) 
   return base + ((chunk >> 3) << 11) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// Distance (in query tokens, i.e. CTAs of one kv-head row) of the L2 prefetch of a later
+// CTA's query rows and block list: about the number of CTAs resident on the GPU at once.
+constexpr int kPrefetchTokens = 512;
+
 // With W, each key's weight (NOSA CIS, p.w [tokens, hkv]) multiplies its softmax weight
 // before the PV product and the normaliser; a stage's 16 weights arrive by 4-byte cp.async
 // into a small array of their own (the TMA stages keep their 1 KB alignment).
@@ -156,6 +160,17 @@ __global__ void __launch_bounds__(128, NSA_PREFILL_MINBLOCKS)
   const int hbase = g * r + rt * 16;
   const int rlo = lane >> 2, rhi = rlo + 8;
   const __nv_bfloat16* qb = p.q + (qrow * p.h + hbase) * D;
+  // the CTA of token qrow + kPrefetchTokens starts about one resident wave later: bring
+  // its query rows and block list into L2 now, so that its start does not wait on DRAM
+  if (warp == NW - 1) {
+    const int64_t fut = qrow + kPrefetchTokens;
+    if (fut < gridDim.x) {
+      const int row = lane >> 1;
+      if (rt * 16 + row < r)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.q + (fut * p.h + hbase + row) * D + (lane & 1) * 64));
+      if (lane == 0) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.idx + (fut * p.hkv + g) * p.S));
+    }
+  }
   uint32_t qa[D / 16][4];
   load_a_frags<D>(qa, rt * 16 + rlo < r ? qb + rlo * D : nullptr, rt * 16 + rhi < r ? qb + rhi * D : nullptr,
                   lane);

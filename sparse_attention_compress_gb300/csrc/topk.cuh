@@ -59,11 +59,13 @@ __device__ __forceinline__ uint32_t warp_radix_kth(const uint32_t (&key)[NPL], i
   const int n_it = (ncand + 31) / 32;
   uint32_t all_and = 0xffffffffu, all_or = 0u;
 #pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (i < n_it && i * 32 + lane < ncand) {
+  for (int i = 0; i < NPL; ++i) {
+    if (i >= n_it) break;  // warp-uniform: rows shorter than NPL * 32 skip the rest
+    if (i * 32 + lane < ncand) {
       all_and &= key[i];
       all_or |= key[i];
     }
+  }
   all_and = __reduce_and_sync(0xffffffffu, all_and);
   all_or = __reduce_or_sync(0xffffffffu, all_or);
   const uint32_t varying = all_and ^ all_or;
@@ -79,12 +81,14 @@ __device__ __forceinline__ uint32_t warp_radix_kth(const uint32_t (&key)[NPL], i
   for (; shift >= 0; shift -= 4) {
     unsigned long long lo = 0ull, hi = 0ull;  // digits 0..7 and 8..15, 8 bits each
 #pragma unroll
-    for (int i = 0; i < NPL; ++i)
-      if (i < n_it && i * 32 + lane < ncand && (key[i] & pmask) == prefix) {
+    for (int i = 0; i < NPL; ++i) {
+      if (i >= n_it) break;
+      if (i * 32 + lane < ncand && (key[i] & pmask) == prefix) {
         const uint32_t d = (key[i] >> shift) & 15u;
         const unsigned long long inc = 1ull << ((d & 7u) * 8u);
         if (d < 8u) lo += inc; else hi += inc;
       }
+    }
     // from the top digit down: the digit where the count of larger-or-equal keys reaches left
     int run = 0, dsel = 0, above = 0;
     bool found = false;
@@ -125,38 +129,51 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
     return;
   }
   const unsigned lt = (1u << lane) - 1u;
+  const int n_it = (ncand + 31) / 32;
   uint32_t key[NPL];
   uint32_t lmax = 0u;
+  // every loop over the lane's blocks stops at the row's own length (a warp-uniform
+  // exit), so a short row costs its length, not NPL * 32; the loads of the row are all
+  // issued before the first of them is used
+  float sv[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
+    if (i >= n_it) break;
+    const int j = i * 32 + lane;
+    sv[i] = j < ncand ? row[j] : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    if (i >= n_it) break;
     const int j = i * 32 + lane;
     key[i] = 0u;
     if (j < ncand) {
       const bool forced = j < n_init || j > own - n_local;
-      key[i] = forced ? 0xffffffffu : order_key(row[j]);
+      key[i] = forced ? 0xffffffffu : order_key(sv[i]);
       lmax = max(lmax, key[i]);
     }
   }
-  const int n_it = (ncand + 31) / 32;
   if (k <= 32) {
     const uint32_t tau = warp_kth_largest(lmax, k, lane);
+    unsigned in_mask[NPL];  // the ballots of the candidate test, kept for the compaction
     int c = 0;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i)
-      if (i < n_it) c += __popc(__ballot_sync(0xffffffffu, i * 32 + lane < ncand && key[i] >= tau));
+    for (int i = 0; i < NPL; ++i) {
+      if (i >= n_it) break;
+      in_mask[i] = __ballot_sync(0xffffffffu, i * 32 + lane < ncand && key[i] >= tau);
+      c += __popc(in_mask[i]);
+    }
     if (c <= 64) {
       int base = 0;
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
-        if (i < n_it) {
-          const bool in = i * 32 + lane < ncand && key[i] >= tau;
-          const unsigned m = __ballot_sync(0xffffffffu, in);
-          if (in) {
-            cand_key[base + __popc(m & lt)] = key[i];
-            cand_idx[base + __popc(m & lt)] = i * 32 + lane;
-          }
-          base += __popc(m);
+        if (i >= n_it) break;
+        const unsigned m = in_mask[i];
+        if ((m >> lane) & 1u) {
+          cand_key[base + __popc(m & lt)] = key[i];
+          cand_idx[base + __popc(m & lt)] = i * 32 + lane;
         }
+        base += __popc(m);
       }
       __syncwarp();
       // candidates are in ascending block order: rank by key, ties by position
@@ -192,16 +209,15 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
   int taken = 0, pos = 0;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
-    if (i < n_it) {
-      const bool v = i * 32 + lane < ncand;
-      const bool eq = v && key[i] == P;
-      const unsigned me = __ballot_sync(0xffffffffu, eq);
-      const bool s = (v && key[i] > P) || (eq && taken + __popc(me & lt) < need);
-      taken += __popc(me);
-      const unsigned ms = __ballot_sync(0xffffffffu, s);
-      if (s) out[pos + __popc(ms & lt)] = i * 32 + lane;
-      pos += __popc(ms);
-    }
+    if (i >= n_it) break;
+    const bool v = i * 32 + lane < ncand;
+    const bool eq = v && key[i] == P;
+    const unsigned me = __ballot_sync(0xffffffffu, eq);
+    const bool s = (v && key[i] > P) || (eq && taken + __popc(me & lt) < need);
+    taken += __popc(me);
+    const unsigned ms = __ballot_sync(0xffffffffu, s);
+    if (s) out[pos + __popc(ms & lt)] = i * 32 + lane;
+    pos += __popc(ms);
   }
 }
 

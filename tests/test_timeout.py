@@ -23,6 +23,15 @@ pytestmark = pytest.mark.gpu
 NSA_ERR_TIMEOUT = 4
 
 
+def _flush_l2():
+    """Write a buffer larger than the L2 (129 MB): the first copies of the next kernel then
+    come from DRAM, slower than a wait's first probe, so a 1 ns limit runs out."""
+    buf = torch.empty(96 * 2 ** 20, dtype=torch.float32, device="cuda")
+    buf.fill_(1.0)
+    torch.cuda.synchronize()
+    del buf
+
+
 @pytest.fixture
 def clean_status():
     assert nsa.nsa_device_status(reset=True) == 0
@@ -42,6 +51,7 @@ def test_decode_wait_runs_out_then_recovers(clean_status):
     w, kc, k = _decode_inputs()
     q, kcache, vcache, sl = dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(w.seqlens)
     torch.cuda.synchronize()
+    _flush_l2()
     nsa.nsa_set_wait_limit_ns(1)
     nsa.nsa_sparse_decode(q, kcache, vcache, kc, sl, k=k)
     torch.cuda.synchronize()  # the kernel returned: no hang, no fault
@@ -63,6 +73,7 @@ def test_selected_attention_wait_runs_out_then_recovers(clean_status):
     idx = gen.random_block_indices(rng, cu, 1, 16, 64, force_first=True)
     dq, dk, dv, di, dcu = dev(q), dev(k), dev(v), dev(idx), dev(cu)
     torch.cuda.synchronize()
+    _flush_l2()
     nsa.nsa_set_wait_limit_ns(1)
     nsa.nsa_sparse_fwd(dq, dk, dv, di, 64, cu_seqlens=dcu, max_seqlen=max(lengths))
     torch.cuda.synchronize()
@@ -80,6 +91,7 @@ def test_layer_wait_runs_out_then_recovers(clean_status):
     w = gen.layer(T=T, H=H, HKV=hkv)
     q, k, v, g = dev(w.q), dev(w.k), dev(w.v), dev(w.gates)
     torch.cuda.synchronize()
+    _flush_l2()
     nsa.nsa_set_wait_limit_ns(1)
     nsa.nsa_layer_fwd(q, k, v, g)
     torch.cuda.synchronize()
