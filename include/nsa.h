@@ -298,17 +298,27 @@ NSA_API nsa_status nsa_block_sparse_fwd(const nsa_shape* shape, const void* q, c
 /* S7 -- compressed-attention branch.  [NSA-Triton] sec. 1.1 and 2.2 (taken as the
  * definition): softmax over the causal compressed keys of scale * q.k_cmp, weighted sum
  * of v_cmp.  A query with no causal compressed key gets o = 0 and lse = -inf.
- *   k_cmp, v_cmp   packed compressed keys / values (nsa_compress_k on K and on V)
+ *   k_cmp, v_cmp   packed compressed keys / values (nsa_compress_k on K and on V), exactly
+ *                  the packed rows of the sequences (tiles reaching past them are read with
+ *                  bounds checks)
  *   o [tokens, h, d] out; lse nullable [tokens, h] fp32 out (natural log)
- * bf16 only; d in {64,128}; h/h_kv divides 16 or is a multiple of 16. */
+ *   workspace      nsa_cmp_attn_fwd_workspace_size() bytes, 256-byte aligned (V transposed
+ *                  for the tensor cores); NULL allowed when that size is 0
+ * bf16 only; d in {64,128}; h/h_kv divides 16 or is a multiple of 16.  d = 128 with h/h_kv a
+ * power of two runs on the tcgen05 tensor cores (the layer's kernel); other shapes on
+ * mma.sync, with no workspace. */
+NSA_API size_t nsa_cmp_attn_fwd_workspace_size(const nsa_shape* shape, int kernel, int stride);
 NSA_API nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k_cmp,
                             const void* v_cmp, int kernel, int stride, float scale, void* o, float* lse,
-                            cudaStream_t stream);
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* S8 -- sliding-window branch ([NSA-Triton] sec. 1.1: the most recent tokens): keys
- * max(0, t-window+1) .. t.  Same layouts and limits as nsa_cmp_attn_fwd. */
+ * max(0, t-window+1) .. t.  Same layouts, limits and kernel choice as nsa_cmp_attn_fwd;
+ * workspace of nsa_swa_fwd_workspace_size() bytes. */
+NSA_API size_t nsa_swa_fwd_workspace_size(const nsa_shape* shape);
 NSA_API nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
-                       int window, float scale, void* o, float* lse, cudaStream_t stream);
+                       int window, float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
 
 /* S9 -- gate combine ([NSA-Triton] sec. 1.1: gates[0]*compressed + gates[1]*selected +
  * gates[2]*local), each gate the logistic sigmoid of its logit.

@@ -61,8 +61,10 @@ _SIGS = {
                              _c_int),
     "nsa_sparse_bwd": ([_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                         _c_sz, _c_p], _c_int),
-    "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
-    "nsa_swa_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_f, _c_p, _c_p, _c_p], _c_int),
+    "nsa_cmp_attn_fwd_workspace_size": ([_c_p, _c_int, _c_int], _c_sz),
+    "nsa_cmp_attn_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
+    "nsa_swa_fwd_workspace_size": ([_c_p], _c_sz),
+    "nsa_swa_fwd": ([_c_p, _c_p, _c_p, _c_p, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz, _c_p], _c_int),
     "nsa_gate_combine": ([_c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p], _c_int),
     "nsa_sparse_decode_workspace_size": ([_c_int] * 9, _c_sz),
     "nsa_sparse_decode": ([_c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
@@ -407,25 +409,36 @@ def nsa_gate_combine_bwd(d_o, o_cmp, o_slc, o_swa, gate_logits, *, stream=None):
     return outs[0], outs[1], outs[2], dg
 
 
+def _workspace(nbytes, device, workspace=None):
+    """Caller's workspace, or a fresh one of nbytes (None when nothing is needed)."""
+    if workspace is not None or nbytes == 0:
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
 def nsa_cmp_attn_fwd(q, k_cmp, v_cmp, h_kv, kernel=32, stride=16, scale=0.0, *, cu_seqlens=None,
-                     max_seqlen=None, out=None, lse=None, stream=None):
+                     max_seqlen=None, out=None, lse=None, workspace=None, stream=None):
     """S7.  Compressed branch over packed compressed keys / values."""
     qf, shp = _shape_for(q, h_kv, cu_seqlens, max_seqlen)
     if out is None:
         out = torch.empty_like(qf)
+    ws = _workspace(int(load().nsa_cmp_attn_fwd_workspace_size(ctypes.byref(shp), kernel, stride)), qf.device,
+                    workspace)
     _check(load().nsa_cmp_attn_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k_cmp), _ptr(v_cmp), kernel, stride,
-                                   float(scale), _ptr(out), _ptr(lse), _stream(stream)), "nsa_cmp_attn_fwd")
+                                   float(scale), _ptr(out), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
+                                   _stream(stream)), "nsa_cmp_attn_fwd")
     return out
 
 
 def nsa_swa_fwd(q, k, v, window=512, scale=0.0, *, cu_seqlens=None, max_seqlen=None, out=None, lse=None,
-                stream=None):
+                workspace=None, stream=None):
     """S8.  Sliding-window branch."""
     qf, shp = _shape_for(q, k.shape[-2], cu_seqlens, max_seqlen)
     if out is None:
         out = torch.empty_like(qf)
+    ws = _workspace(int(load().nsa_swa_fwd_workspace_size(ctypes.byref(shp))), qf.device, workspace)
     _check(load().nsa_swa_fwd(ctypes.byref(shp), _ptr(qf), _ptr(k), _ptr(v), window, float(scale), _ptr(out),
-                              _ptr(lse), _stream(stream)), "nsa_swa_fwd")
+                              _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)), "nsa_swa_fwd")
     return out
 
 

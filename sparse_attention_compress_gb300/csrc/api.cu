@@ -561,9 +561,30 @@ static nsa_status dense_common(const nsa_shape* shape, Seqs* s, const char* fn) 
   return NSA_OK;
 }
 
+// Scratch of the tensor-core dense branches: V transposed per kv-head ([h_kv, d, rows
+// padded to 64]), the K-major B operand of the PV product.  Rows: the caller's value rows
+// (tokens), or for the compressed branch a bound on the packed compressed rows.
+static int64_t cmp_rows_bound(const Seqs& s, int kernel, int stride) {
+  return s.cu ? s.tokens / stride + s.n_seqs : (int64_t)s.n_seqs * num_cmp_host(s.T, kernel, stride);
+}
+
+size_t nsa_cmp_attn_fwd_workspace_size(const nsa_shape* shape, int kernel, int stride) {
+  Seqs s;
+  if (make_seqs(shape, &s, __func__) != NSA_OK || kernel <= 0 || stride <= 0) return 0;
+  if (shape->dtype != NSA_BF16 || !dense_tc_supported(shape->h, shape->h_kv, shape->d)) return 0;
+  return align256((size_t)tc_vt_pad(cmp_rows_bound(s, kernel, stride)) * shape->h_kv * shape->d * 2);
+}
+
+size_t nsa_swa_fwd_workspace_size(const nsa_shape* shape) {
+  Seqs s;
+  if (make_seqs(shape, &s, __func__) != NSA_OK) return 0;
+  if (shape->dtype != NSA_BF16 || !dense_tc_supported(shape->h, shape->h_kv, shape->d)) return 0;
+  return align256((size_t)tc_vt_pad(s.tokens) * shape->h_kv * shape->d * 2);
+}
+
 nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k_cmp,
                             const void* v_cmp, int kernel, int stride, float scale, void* o, float* lse,
-                            cudaStream_t stream) {
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   NSA_RANGE();
   Seqs s;
   if (nsa_status st = dense_common(shape, &s, __func__)) return st;
@@ -577,13 +598,28 @@ nsa_status nsa_cmp_attn_fwd(const nsa_shape* shape, const void* q, const void* k
   }
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(NSA_ERR_INVALID, "nsa_cmp_attn_fwd: lse misaligned");
   if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
-  return cuda_status(launch_dense_attn(0, s, q, k_cmp, v_cmp, shape->h, shape->h_kv, shape->d, kernel, stride, 0,
-                                       scale, o, lse, stream),
-                     "nsa_cmp_attn_fwd");
+  const size_t need = nsa_cmp_attn_fwd_workspace_size(shape, kernel, stride);
+  // d 64, a group size the tensor-core kernel does not take, or no sequence with a
+  // compressed key (k_cmp / v_cmp may then be NULL): the mma.sync kernel
+  if (need == 0 || s.max_len < kernel)
+    return cuda_status(launch_dense_attn(0, s, q, k_cmp, v_cmp, shape->h, shape->h_kv, shape->d, kernel, stride, 0,
+                                         scale, o, lse, stream),
+                       "nsa_cmp_attn_fwd");
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_cmp_attn_fwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_cmp_attn_fwd: workspace %zu < %zu bytes", workspace_bytes,
+              need);
+  const int64_t rows = cmp_rows_bound(s, kernel, stride);
+  cudaError_t e = launch_transpose_v(s, v_cmp, workspace, rows, shape->h_kv, true, kernel, stride, stream);
+  if (e == cudaSuccess)  // the caller's k_cmp holds exactly the packed compressed rows: tiles past them are bounds-checked
+    e = launch_dense_attn_tc(0, s, q, k_cmp, workspace, rows, shape->h, shape->h_kv, kernel, stride, 0, scale, o, lse,
+                             nullptr, 0, stream, -1);
+  return cuda_status(e, "nsa_cmp_attn_fwd");
 }
 
 nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, const void* v, int window,
-                       float scale, void* o, float* lse, cudaStream_t stream) {
+                       float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
   NSA_RANGE();
   Seqs s;
   if (nsa_status st = dense_common(shape, &s, __func__)) return st;
@@ -595,9 +631,20 @@ nsa_status nsa_swa_fwd(const nsa_shape* shape, const void* q, const void* k, con
   NSA_PTR(o);
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(NSA_ERR_INVALID, "nsa_swa_fwd: lse misaligned");
   if (scale <= 0.f) scale = 1.f / sqrtf((float)shape->d);
-  return cuda_status(launch_dense_attn(1, s, q, k, v, shape->h, shape->h_kv, shape->d, 0, 1, window, scale, o, lse,
-                                       stream),
-                     "nsa_swa_fwd");
+  const size_t need = nsa_swa_fwd_workspace_size(shape);
+  if (need == 0)  // d 64 or a group size the tensor-core kernel does not take
+    return cuda_status(launch_dense_attn(1, s, q, k, v, shape->h, shape->h_kv, shape->d, 0, 1, window, scale, o, lse,
+                                         stream),
+                       "nsa_swa_fwd");
+  NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
+              "nsa_swa_fwd: workspace must be non-null and 256-byte aligned");
+  NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_swa_fwd: workspace %zu < %zu bytes", workspace_bytes,
+              need);
+  cudaError_t e = launch_transpose_v(s, v, workspace, s.tokens, shape->h_kv, false, 0, 1, stream);
+  if (e == cudaSuccess)
+    e = launch_dense_attn_tc(1, s, q, k, workspace, s.tokens, shape->h, shape->h_kv, 0, 1, window, scale, o, lse,
+                             nullptr, 0, stream);
+  return cuda_status(e, "nsa_swa_fwd");
 }
 
 nsa_status nsa_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,

@@ -65,7 +65,10 @@ __global__ void __launch_bounds__(kDWarps * 32) dense_attn_kernel(const DensePar
   const int gl = warp * 16 + rlo, gh = warp * 16 + rhi;
   const int t_lo = t0 + gl / R, t_hi = t0 + gh / R;
   const int hd_lo = gl % R, hd_hi = gh % R;
-  const bool v_lo = t_lo < L, v_hi = t_hi < L;
+  // rows past the CTA's TPC tokens (a group size that does not divide 128) belong to the
+  // next CTA: they take no part
+  const int rows = TPC * R;
+  const bool v_lo = gl < rows && t_lo < L, v_hi = gh < rows && t_hi < L;
   // per-row key bounds [a, b)
   int a_lo, b_lo, a_hi, b_hi;
   if (MODE == 0) {
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(kDWarps * 32) dense_attn_kernel(const DensePar
     b_hi = v_hi ? t_hi + 1 : 0;
   }
   // key range touched by this warp's rows
-  const int tw0 = min(t0 + (warp * 16) / R, L - 1), tw1 = min(t0 + (warp * 16 + 15) / R, L - 1);
+  const int tw0 = min(t0 + (warp * 16) / R, L - 1), tw1 = min(t0 + (min(warp * 16 + 15, rows - 1)) / R, L - 1);
   int w_lo, w_hi;
   if (MODE == 0) {
     w_lo = 0;
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kDWarps * 32) dense_attn_kernel(const DensePar
     w_lo = max(0, tw0 - p.window + 1);
     w_hi = tw1 + 1;
   }
-  const bool warp_live = t0 + (warp * 16) / R < L;
+  const bool warp_live = warp * 16 < rows && t0 + (warp * 16) / R < L;
 
   uint32_t qa[D / 16][4];
   load_a_frags<D>(qa, v_lo ? p.q + ((start + t_lo) * p.h + g * R + hd_lo) * D : nullptr,

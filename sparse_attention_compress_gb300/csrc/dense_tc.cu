@@ -99,8 +99,10 @@ struct Params {
   float* lse;            // optional natural-log normaliser per (token, head)
   float* scores;         // MODE 0 with fused block scores, MODE 2: [tokens, hkv, nb_stride]
   const float* lse_in;   // MODE 2: normaliser given by the caller (pass 1 skipped), or null
-  const __nv_bfloat16* k;  // MODE 2: key rows, for the copies of a tile that ends past them
-  int64_t kv_total;      // MODE 2: key rows the buffer holds (-1: the packed compressed rows)
+  const __nv_bfloat16* k;  // MODE 0 / 2: key rows, for the copies of a tile that ends past them
+  // MODE 0 / 2: key rows the buffer holds (-1: the packed compressed rows of all sequences;
+  // 0, MODE 0 only: the buffer extends past every tile, no bounds checks)
+  int64_t kv_total;
   const uint8_t* bmask;  // MODE 3: [batch, h, n_qb, n_qb] tile mask (query block, key block)
   int n_qb, causal;
   Seqs seqs;
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       tma3d(q_s + Q_BYTES / 2, &tm_q, 64, g * R, (int)(start + t0), bar(B_Q));
     }
     int64_t kv_total = p.kv_total;
-    if (MODE == 2 && kv_total < 0) {  // packed compressed rows of all sequences
+    if ((MODE == 0 || MODE == 2) && kv_total < 0) {  // packed compressed rows of all sequences
       int64_t acc = 0;
       for (int i = lane; i < p.seqs.n_seqs; i += 32) acc += num_cmp(seq_len(p.seqs, i), p.kernel, p.stride);
 #pragma unroll
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
                       : MODE == 2 ? (int)(kv0 + (int64_t)(i < n_kt ? i : i - n_kt) * KT)
                                   : (i < n_kt ? (int)((a_lo + i) * KT) : (int)(kv0 + (int64_t)(i - n_kt) * KT));
       const uint32_t kb = bar(B_KFULL + st), ks = k_s + st * K_BYTES;
-      if (MODE == 2 && row + KT > kv_total) {
+      if ((MODE == 2 || (MODE == 0 && kv_total != 0)) && row + KT > kv_total) {
         // a tile reaching past the caller's rows: bounds-checked copies (zeros past the
         // end) instead of TMA, then the async-proxy fence and a plain arrival
         for (int c = lane; c < KT * (D / 8); c += 32) {
@@ -630,7 +632,8 @@ static cudaError_t run_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CU
 
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
-                                 void* o, float* lse, float* scores, int nb_stride, cudaStream_t st) {
+                                 void* o, float* lse, float* scores, int nb_stride, cudaStream_t st,
+                                 int64_t kv_total) {
   if (s.tokens == 0) return cudaSuccess;
   const int R = h / hkv;
   const int tpc = tc::ROWS / R;
@@ -660,6 +663,8 @@ cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const v
   p.o = (__nv_bfloat16*)o;
   p.lse = lse;
   p.scores = scores;
+  p.k = (const __nv_bfloat16*)k;
+  p.kv_total = mode == 0 ? kv_total : 0;
   p.seqs = s;
   p.h = h;
   p.hkv = hkv;
@@ -720,6 +725,11 @@ cudaError_t launch_block_sparse_tc(const Seqs& s, const void* q, const void* k, 
   p.scale_log2 = scale * kLog2e;
   const dim3 grid((s.max_len + tc::ROWS - 1) / tc::ROWS, s.n_seqs, h);
   return run_tc<3, 0>(mq, mk, mv, p, grid, st);
+}
+
+bool dense_tc_supported(int h, int hkv, int d) {
+  const int R = hkv > 0 ? h / hkv : 0;
+  return d == tc::D && R >= 1 && R * hkv == h && R <= tc::ROWS && (R & (R - 1)) == 0;
 }
 
 bool scores_tc_supported(int h, int hkv, int d, int kernel, int stride, int block_size) {

@@ -86,9 +86,16 @@ cudaError_t launch_dense_attn(int mode, const Seqs& s, const void* q, const void
 int64_t tc_vt_pad(int64_t rows);
 cudaError_t launch_transpose_v(const Seqs& s, const void* v, void* vt, int64_t rows, int hkv, bool compressed,
                                int kernel, int stride, cudaStream_t st);
+// kv_total (mode 0): key rows the k buffer holds; tiles reaching past them are read with
+// bounds-checked copies (-1: the packed compressed rows of all sequences, computed on the
+// device; 0: the buffer extends past every tile, as in the layer's workspace).
 cudaError_t launch_dense_attn_tc(int mode, const Seqs& s, const void* q, const void* k, const void* vt,
                                  int64_t kv_rows, int h, int hkv, int kernel, int stride, int window, float scale,
-                                 void* o, float* lse, float* scores, int nb_stride, cudaStream_t st);
+                                 void* o, float* lse, float* scores, int nb_stride, cudaStream_t st,
+                                 int64_t kv_total = 0);
+// Whether the tensor-core dense branches take this shape (d 128 and a group size that is
+// a power of two up to 128).
+bool dense_tc_supported(int h, int hkv, int d);
 // Block-mask sparse attention on the tensor cores: dense layout, seqlen % 64 == 0,
 // multi-head K/V (h_kv == h), d = 128, bf16; vt = V transposed as for the dense branches;
 // mask uint8 [batch, h, n_qb, n_qb] over 64 x 64 tiles.

@@ -76,7 +76,7 @@ def test_unsupported_parameters():
     assert lib.nsa_compress_k(ctypes.byref(s), FAKE, FAKE, 40, 16, None) == 2
     assert lib.nsa_sparse_decode(2, FAKE, 1024, 16, 2, 64, FAKE, FAKE, FAKE, FAKE, 32, 16, 64, 1, 2, 64, 0.0,
                                  None, FAKE, FAKE, 1 << 30, None) == 2
-    assert lib.nsa_swa_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, 0, 0.0, FAKE, None, None) == 1
+    assert lib.nsa_swa_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, 0, 0.0, FAKE, None, None, 0, None) == 1
 
 
 def test_decode_workspace_checks():
@@ -248,13 +248,19 @@ def test_select_block_mask_cmp_layer_reject_bad_arguments():
     assert block_mask(_shape(**mh), mask=None) == 1
     assert block_mask(_shape(**mh), ws_bytes=256) == 1 and b"workspace" in lib.nsa_last_error()
 
-    def cmp_fwd(shape=s, kernel=32, lse=None):
-        return lib.nsa_cmp_attn_fwd(ref(shape), FAKE, FAKE, FAKE, kernel, 16, 0.0, FAKE, lse, None)
+    def cmp_fwd(shape=s, kernel=32, lse=None, ws=FAKE, ws_bytes=1 << 30):
+        return lib.nsa_cmp_attn_fwd(ref(shape), FAKE, FAKE, FAKE, kernel, 16, 0.0, FAKE, lse, ws, ws_bytes, None)
 
     assert cmp_fwd(shape=_shape(dtype=_lib.NSA_F32)) == 2
     assert cmp_fwd(shape=_shape(h=12, h_kv=4)) == 2  # group of 3 heads
     assert cmp_fwd(kernel=0) == 1
     assert cmp_fwd(lse=P(0x10002)) == 1 and b"misaligned" in lib.nsa_last_error()
+    # d 128 with a power-of-two group runs on the tensor cores and needs the V^T workspace
+    assert cmp_fwd(ws=None) == 1 and b"workspace" in lib.nsa_last_error()
+    assert cmp_fwd(ws_bytes=256) == 1 and b"workspace" in lib.nsa_last_error()
+    assert lib.nsa_swa_fwd(ref(s), FAKE, FAKE, FAKE, 512, 0.0, FAKE, None, None, 0, None) == 1
+    assert b"workspace" in lib.nsa_last_error()
+
 
     def layer(shape=s, kernel=32, S=16, window=512, ws_bytes=1 << 30):
         return lib.nsa_layer_fwd(ref(shape), FAKE, FAKE, FAKE, FAKE, kernel, 16, 64, S, 1, 2, window, 0.0, FAKE,
@@ -268,6 +274,22 @@ def test_select_block_mask_cmp_layer_reject_bad_arguments():
     assert need > 0 and need % 256 == 0
     assert layer(ws_bytes=need - 1) == 1 and b"workspace" in lib.nsa_last_error()
 
+
+@pytest.mark.parametrize("B,T,h,hkv,d,tc", [(1, 128, 16, 1, 128, True), (2, 1000, 16, 2, 128, True),
+                                            (3, 100, 64, 1, 128, True), (2, 100, 48, 1, 128, False),
+                                            (2, 100, 16, 1, 64, False)])
+def test_branch_workspace_sizes(B, T, h, hkv, d, tc):
+    """The compressed and sliding branches ask for V transposed (bf16, rows padded to 64 per
+    kv-head) exactly when they run on the tensor cores (d 128, power-of-two group)."""
+    lib = nsa.load()
+    s = _shape(batch=B, seqlen=T, h=h, h_kv=hkv, d=d)
+    pad = lambda rows: -(-rows // 64) * 64
+    up = lambda x: -(-x // 256) * 256
+    n_c = max(0, (T - 32) // 16 + 1)
+    want_cmp = up(pad(B * n_c) * hkv * d * 2) if tc else 0
+    want_swa = up(pad(B * T) * hkv * d * 2) if tc else 0
+    assert lib.nsa_cmp_attn_fwd_workspace_size(ctypes.byref(s), 32, 16) == want_cmp
+    assert lib.nsa_swa_fwd_workspace_size(ctypes.byref(s)) == want_swa
 
 @pytest.mark.parametrize("B,T,hkv", [(1, 128, 1), (2, 1000, 2), (3, 64, 4)])
 def test_select_and_block_mask_workspace_sizes(B, T, hkv):

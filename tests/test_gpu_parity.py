@@ -537,7 +537,10 @@ def test_nosa_pipeline():
 
 
 # --------------------------------------------------------------------------- S7, S8, S9
-@pytest.mark.parametrize("H,hkv,d", [(16, 1, 128), (32, 2, 128), (8, 1, 64), (16, 4, 128), (64, 1, 128)])
+# d 128 with a power-of-two group runs on the tcgen05 kernel (group 128: one token per
+# CTA); group 48 and d 64 run on mma.sync
+@pytest.mark.parametrize("H,hkv,d", [(16, 1, 128), (32, 2, 128), (8, 1, 64), (16, 4, 128), (64, 1, 128),
+                                     (48, 1, 128), (128, 1, 128)])
 def test_cmp_attn(H, hkv, d):
     lengths = [10, 31, 32, 47, 500, 1777]
     cu = gen.varlen_cu_seqlens(lengths)
@@ -556,7 +559,8 @@ def test_cmp_attn(H, hkv, d):
     np.testing.assert_allclose(l[fin], lse_ref[fin], atol=1e-3, rtol=1e-4)
 
 
-@pytest.mark.parametrize("window,H,hkv", [(512, 16, 1), (1, 16, 2), (100, 8, 1), (5000, 16, 1), (64, 64, 4)])
+@pytest.mark.parametrize("window,H,hkv", [(512, 16, 1), (1, 16, 2), (100, 8, 1), (5000, 16, 1), (64, 64, 4),
+                                          (300, 32, 1), (77, 48, 1)])
 def test_swa(window, H, hkv):
     lengths = [3, 600, 2100]
     cu = gen.varlen_cu_seqlens(lengths)
