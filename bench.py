@@ -34,11 +34,11 @@ from sparse_attention_compress_gb300.dist import max_over_ranks  # noqa: E402
 
 METRIC = "NSA selected-attn fwd TFLOP/s (prefill), KV GB/s (decode) vs GB300 roofline"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the TMA-fed
-# prefill kernel sparse_fwd_tma<2>, captured by ncu at B=2 (153.12 MB read + 99.52 MB
-# written), times 4 for the B=8 launch: every query token reads its own Q row and writes
-# its own O row, and the K/V read grows with the batch in the same way.  None once the
-# kernel has changed since that capture.
-PREFILL_NCU_TRAFFIC = 4 * (153.12e6 + 99.52e6)
+# prefill kernel sparse_fwd_tma<2> (with the L2 prefetch of later tokens' query rows),
+# captured by ncu at B=2 (153.22 MB read + 99.70 MB written), times 4 for the B=8 launch:
+# every query token reads its own Q row and writes its own O row, and the K/V read grows
+# with the batch in the same way.  To be set to None once the kernel changes again.
+PREFILL_NCU_TRAFFIC = 4 * (153.22e6 + 99.70e6)
 L2_BYTES = 129 * 2 ** 20
 
 

@@ -176,7 +176,34 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
         base += __popc(m);
       }
       __syncwarp();
-      // candidates are in ascending block order: rank by key, ties by position
+      if (c <= 32) {
+        // one candidate per lane: a bitonic sort of (key descending, list position
+        // ascending) puts the chosen blocks in lanes 0 .. k-1; the positions, being in
+        // ascending block order, then give each chosen block its output slot
+        uint32_t ck = lane < c ? cand_key[lane] : 0u;
+        int cp = lane < c ? lane : 0x7fffffff;
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t ok = __shfl_xor_sync(0xffffffffu, ck, stride);
+            const int op = __shfl_xor_sync(0xffffffffu, cp, stride);
+            const bool mine_first = ck > ok || (ck == ok && cp < op);
+            const bool desc = (lane & size) == 0 || size == 32;  // the final order is descending
+            const bool lower = (lane & stride) == 0;
+            if ((lower == desc) != mine_first) {
+              ck = ok;
+              cp = op;
+            }
+          }
+        }
+        const bool chosen = lane < k && cp < c;
+        const unsigned pos_mask = __reduce_or_sync(0xffffffffu, chosen ? 1u << cp : 0u);
+        if (chosen) out[__popc(pos_mask & ((1u << cp) - 1u))] = cand_idx[cp];
+        __syncwarp();  // cand_* may be reused by the next row of this warp
+        return;
+      }
+      // 33 .. 64 candidates: rank each by key, ties by position
       bool sel[2];
       int idx[2];
 #pragma unroll
