@@ -383,8 +383,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       if (!(ok = warp_wait(bar(B_SFULL + b), (kt >> 1) & 1, abort))) break;
       fence_after();
       float sv[KT];
-      tmem_ld32(t_lane + b * KT, sv);
-      tmem_ld32(t_lane + b * KT + 32, sv + 32);
+      tmem_ld64(t_lane + b * KT, sv);
       fence_before();
       mbar_arrive(bar(B_SFREE + b));
       const int j_hi = min(KT, max(0, b_hi - kt * KT));
@@ -409,8 +408,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       if (!(ok = warp_wait(bar(B_SFULL + b), (kt >> 1) & 1, abort))) break;
       fence_after();
       float sv[KT];
-      tmem_ld32(t_lane + b * KT, sv);
-      tmem_ld32(t_lane + b * KT + 32, sv + 32);
+      tmem_ld64(t_lane + b * KT, sv);
       // key row a0 + j is key a0 + j - kv0 of the sequence: attended when in [b_lo, b_hi)
       int j_lo, j_hi;
       if (MODE == 3) {
@@ -513,8 +511,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
         if (!(ok = warp_wait(bar(B_SFULL + b), (j >> 1) & 1, abort))) break;
         fence_after();
         float sv[KT];
-        tmem_ld32(t_lane + b * KT, sv);
-        tmem_ld32(t_lane + b * KT + 32, sv + 32);
+        tmem_ld64(t_lane + b * KT, sv);
         fence_before();
         mbar_arrive(bar(B_SFREE + b));
         const int jh = min(KT, max(0, b_hi - i * KT));  // causal compressed keys of this tile
