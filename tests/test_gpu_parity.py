@@ -926,3 +926,55 @@ def test_block_sparse_full_size_sampled():
     ref, _ = orc.block_sparse_attn(w.q, w.k, w.v, w.idx, causal=True, rows=rows)
     g = out.reshape(w.tokens, 16, 128)[torch.from_numpy(rows).cuda()]
     assert_close(g, ref, what="block sparse full")
+
+
+# --------------------------------------------------------------------------- sizes at the edges
+def test_zero_token_calls():
+    """A batch without tokens is valid input: every forward entry point returns without
+    launching and leaves its (empty) outputs alone."""
+    q = torch.empty((0, 16, 128), dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty((0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    cu = dev(np.zeros(2, np.int32))
+    assert nsa.nsa_compress_k(kv, cu_seqlens=cu, max_seqlen=0).shape[0] == 0
+    assert nsa.nsa_sparse_fwd(q, kv, kv, torch.empty((0, 1, 16), dtype=torch.int32, device="cuda"), 64,
+                              cu_seqlens=cu, max_seqlen=0).shape == (0, 16, 128)
+    assert nsa.nsa_swa_fwd(q, kv, kv, 512, cu_seqlens=cu, max_seqlen=0).shape == (0, 16, 128)
+    assert nsa.nsa_cmp_attn_fwd(q, kv, kv, 1, cu_seqlens=cu, max_seqlen=0).shape == (0, 16, 128)
+    sc = torch.empty((0, 1, 4), dtype=torch.float32, device="cuda")
+    assert nsa.nsa_topk_select(sc, 16, cu_seqlens=cu, max_seqlen=0).shape == (0, 1, 16)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+
+
+def test_sparse_fwd_longest_list():
+    """S = 64, the longest block list the entry point takes: with every causal block of a
+    4096-token sequence listed, selected attention is dense causal attention."""
+    T, H, d, S = 4096, 16, 128, 64
+    cu = gen.dense_cu_seqlens(1, T)
+    rng = _rng(14)
+    q, k, v = (gen.normal(rng, (T, hh, d), "bf16") for hh in (H, 1, 1))
+    t = np.arange(T)
+    idx = np.where(np.arange(S)[None, :] <= (t // 64)[:, None], np.arange(S)[None, :], -1).astype(np.int32)[:, None, :]
+    out = nsa.nsa_sparse_fwd(dev(q), dev(k), dev(v), dev(idx), 64)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([_rng(15).integers(0, T, 200), [0, 1, 63, 64, 4095]]))
+    ref, _ = orc.sparse_attn(q, k, v, idx, cu, 64, rows=rows)
+    assert_close(out[torch.from_numpy(rows).cuda()], ref, what="S = 64")
+
+
+def test_decode_longest_context():
+    """A decode step at the longest context it takes (65536 tokens, 4095 compressed keys,
+    1024 selection blocks), top-64, with a ragged second sequence."""
+    B, L, k = 2, 65536, 64
+    w, kc_cache = _decode_case(B, L, [65536, 40000], k, 0)
+    ref_idx, _, ref_sc = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, want_scores=True)
+    idx = torch.empty((B, w.hkv, k), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode(dev(w.q), dev(w.k_cache), dev(w.v_cache), dev(kc_cache), dev(w.seqlens), k=k,
+                                idx_out=idx)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    gi = host(idx)
+    n_mis, outside = selection_mismatches(gi, ref_idx, ref_sc, np.asarray(w.seqlens) - 1)
+    assert outside == 0, (n_mis, outside)
+    _, ref_o = orc.decode(w.q, w.k_cache, w.v_cache, kc_cache, w.seqlens, k=k, idx_in=gi)
+    assert_close(out, ref_o, what="decode at 65536")
