@@ -737,7 +737,7 @@ static nsa_status decode_call(int batch, const int32_t* seqlens, int max_len, in
   a.idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + l.idx);
   a.o = o;
   a.z = reinterpret_cast<float*>(w + l.z);
-  a.tile_ml = reinterpret_cast<float*>(w + l.tile_ml);
+  a.unit_ml = reinterpret_cast<float*>(w + l.unit_ml);
   a.part_o = reinterpret_cast<float*>(w + l.part_o);
   a.part_ml = reinterpret_cast<float*>(w + l.part_ml);
   a.counters = reinterpret_cast<int*>(w + l.counters);

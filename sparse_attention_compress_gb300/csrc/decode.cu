@@ -6,21 +6,23 @@
 //
 // GB300 design.  A decode step has only batch * h_kv independent rows, far fewer than
 // the 152 SMs, and the path is HBM bound (compressed keys plus the chosen K/V blocks).
-// The whole step is one persistent kernel (cooperative launch, every CTA resident) that
-// takes work items from a global queue:
-//   score items (row, group of four 64-key tiles of compressed keys), row by row: each
-//      warp scores one tile for the row's heads and writes the tile's (max, sum) per
-//      head and its pooled block partials; the last item of a row (arrival counter)
-//      folds the partials into block scores, runs a CTA-wide radix-select top-k and
-//      publishes the
-//      row's block list with a release flag;
-//   attention items (row, split of the block list): wait for the row's flag (bounded),
-//      stream the split's blocks (four warps, 16-key slices, cp.async rings), write the
-//      split's softmax state; the last split of a row merges them into O.
-// Queue order puts every score item before every attention item, so a waiting CTA only
-// waits for score work that is already running; rows finish scoring in order, so the
-// gather of early rows overlaps the scoring of later ones.  A memset of the counters
-// and the kernel are stream ordered and capture into one CUDA graph.
+// The whole step is one persistent kernel (cooperative launch, every CTA resident) in two
+// phases:
+//   scoring: the (row, 32-key unit) space of the compressed keys is cut into one
+//      contiguous run per CTA; each warp streams its units through a cp.async ring and
+//      writes each unit's (max, sum) per head and its pooled block partials, so the whole
+//      phase is one HBM stream with every load issued up front.  A CTA then adds its unit
+//      count to each row it touched (arrival counter); the CTA that completes a row folds
+//      the partials into block scores, runs a CTA-wide top-k and publishes the row's block
+//      list with a release flag;
+//   attention: the CTAs take items (row, split of the block list) from a global queue,
+//      wait for the row's flag (bounded), stream the split's blocks (four warps, 16-key
+//      slices, cp.async rings) and write the split's softmax state; the last split of a
+//      row merges them into O.
+// A CTA makes its selections before it takes any attention item, so a waiting CTA only
+// waits for a selection that a running CTA is making; the gather of the rows selected
+// first overlaps the selection of the others.  A memset of the counters and the kernel
+// are stream ordered and capture into one CUDA graph.
 #include "decode_impl.cuh"
 
 namespace nsa {
@@ -33,8 +35,7 @@ DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int ke
   const int r = h / hkv;
   const int rtiles = (r + 15) / 16;
   const int nc_max = max_len >= kernel ? (max_len - kernel) / stride + 1 : 0;
-  l.n_tiles = (nc_max + 63) / 64;
-  l.nc_pad = l.n_tiles * 64;
+  l.n_units = nc_max > 0 ? (nc_max + 31) / 32 : 1;  // units of 32 compressed keys
   // about one attention item per resident CTA slot (2 per SM), at most 16 splits
   const int64_t units = (int64_t)batch * hkv * rtiles;
   int ns = (int)(2 * 152 / (units > 0 ? units : 1));
@@ -43,10 +44,10 @@ DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int ke
   const int eps = (k + ns - 1) / ns;  // entries per split; no split is left empty
   l.n_split = (k + eps - 1) / eps;
   size_t off = 0;
-  l.z = off;  // per-tile pooled partial sums [batch, hkv, n_tiles, 16 blocks, r]
-  off = align256(off + (size_t)batch * hkv * l.n_tiles * 16 * r * 4);
-  l.tile_ml = off;
-  off = align256(off + (size_t)batch * hkv * l.n_tiles * r * 2 * 4);
+  l.z = off;  // per-unit pooled partial sums [batch, hkv, n_units, 8 blocks, r]
+  off = align256(off + (size_t)batch * hkv * l.n_units * 8 * r * 4);
+  l.unit_ml = off;  // per unit and head (max, sum) [batch, hkv, n_units, r, 2]
+  off = align256(off + (size_t)batch * hkv * l.n_units * r * 2 * 4);
   l.idx = off;
   off = align256(off + (size_t)batch * hkv * k * 4);
   l.part_o = off;

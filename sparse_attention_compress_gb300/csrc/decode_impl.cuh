@@ -11,10 +11,11 @@
 
 namespace nsa {
 
-constexpr int kTile = 64;
-
-constexpr int kMaxTiles = 64;  // max_len <= 65536
-constexpr int kNW = 4;         // warps per CTA
+constexpr int kUnit = 32;        // compressed keys per score unit
+constexpr int kMaxUnits = 128;   // units per row: max_len <= 65536
+constexpr int kNW = 4;           // warps per CTA
+constexpr int kDecodeStages = 3;  // ring stages per warp (score units and attention slices)
+constexpr int kUnitBytes = kUnit * 128 * 2;
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -22,10 +23,10 @@ struct DecodeParams {
   const __nv_bfloat16* k_cache;
   const __nv_bfloat16* v_cache;
   const int32_t* seqlens;
-  int h, hkv, max_len, nc_stride, n_tiles, n_groups, n_init, n_local, k, n_split, eps;
+  int h, hkv, max_len, nc_stride, n_units, n_init, n_local, k, n_split, eps;
   float scale_log2;
-  float* z;
-  float* tile_ml;
+  float* z;        // pooled block partials [rows, n_units * 8 blocks, r]
+  float* unit_ml;  // per unit and head (max, sum) [rows, n_units, r, 2]
   float* part_o;
   float* part_ml;
   int32_t* idx;
@@ -50,133 +51,222 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int atom_acq_rel_add(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+// Cross-CTA hand-offs follow one pattern: the writers' stores, a CTA barrier, then a
+// release (store, reduction or read-modify-write) by one thread; the reader's acquire by
+// one thread, then a CTA barrier, then the reads.  The barrier orders every thread's
+// accesses with the one thread's release or acquire, and release and acquire carry that
+// order across CTAs.
 
-// Score item: tiles grp*4 + warp of row (b, g); the last item of the row selects.
-template <int D, int R, int NPL, bool W>
-__device__ __forceinline__ void score_item(const DecodeParams& p, int b, int g, int grp, uint8_t* smem, int* s_flag,
-                                           int* s_topk, int (*s_two)[64]) {
+// Thread 0 waits (bounded) until *f >= v (an acquire load), then every thread learns the
+// outcome; on a timeout the device status records it.
+__device__ __forceinline__ bool cta_wait_ge(const int* f, int v, int* s_flag) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    if (ld_acquire(f) < v) {
+      const unsigned long long t0 = tc::globaltimer(), lim = tc::wait_limit();
+      while (ld_acquire(f) < v) {
+        if (tc::device_status_set() || lim < tc::kQuickNs || tc::globaltimer() - t0 >= lim) {
+          atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    *s_flag = ok;
+  }
+  __syncthreads();
+  const bool ok = *s_flag;
+  __syncthreads();  // s_flag is rewritten only after every thread has read it
+  return ok;
+}
+
+// Causal compressed keys of the newest query of sequence b.
+__device__ __forceinline__ int decode_nca(const DecodeParams& p, int b) {
+  const int L = p.seqlens[b];
+  return num_causal_cmp(L - 1, num_cmp(L, 32, 16), 32, 16);
+}
+
+// Score phase of one CTA: units [u0, u1) of the flattened (row, unit) space, unit u of a
+// row being its compressed keys 32u .. 32u+31.  Warp w takes units u0 + w, u0 + w + 4, ...
+// and streams them through its own cp.async ring, so every load of the phase is issued
+// at once and the next unit's keys arrive while the current one is scored.  For each
+// unit and head the warp writes the (max, sum) of its probabilities relative to the
+// unit's own max, and the pooled partials of its 8 blocks (block jl of the unit sums the
+// windows 4jl, 4jl+1, 4jl+2).  Units past a row's causal keys are skipped; the first
+// stages are issued before the row's length is known (bounded only by the cache
+// extent), so the phase's loads start at once, and scoring masks them.
+template <int D, int R>
+__device__ __forceinline__ void score_units(const DecodeParams& p, int u0, int u1, uint8_t* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = grp * kNW + warp;
+  const int U = p.n_units;
+  const int first = u0 + warp;
+  const int n = first < u1 ? (u1 - first + kNW - 1) / kNW : 0;
+  const uint32_t ring = smem_u32(smem) + warp * kDecodeStages * kUnitBytes;
+  const int64_t row_stride = (int64_t)p.hkv * D;
+  int c_row = -1, c_nca = 0;  // row of the last issued unit and its causal key count
+  auto issue = [&](int i, bool early) {
+    if (i < n) {
+      const int u = first + i * kNW;
+      const int row = u / U, uu = u - row * U;
+      const int b = row / p.hkv, g = row % p.hkv;
+      if (early) {
+        c_row = -1;
+        c_nca = p.nc_stride;  // every cached compressed row; scoring masks the row's own length
+      } else if (row != c_row) {
+        c_row = row;
+        c_nca = decode_nca(p, b);
+      }
+      if (uu * kUnit < c_nca) {
+        const __nv_bfloat16* kbase = p.kc + (((int64_t)b * p.nc_stride) * p.hkv + g) * D;
+        const int nca = c_nca;
+        load_tile_async<D, kUnit, 32>(ring + (i % kDecodeStages) * kUnitBytes, lane, p.kc,
+                                      [&](int rr) -> const __nv_bfloat16* {
+                                        const int c = uu * kUnit + rr;
+                                        return c < nca ? kbase + c * row_stride : nullptr;
+                                      });
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kDecodeStages - 1; ++i) issue(i, true);
+  const int rlo = lane >> 2, rhi = rlo + 8, q4 = lane & 3;
+  int q_row = -1, nca = 0;
+  uint32_t qa[D / 16][4];
+  for (int i = 0; i < n; ++i) {
+    issue(i + kDecodeStages - 1, false);
+    const int u = first + i * kNW;
+    const int row = u / U, uu = u - row * U;
+    if (row != q_row) {  // a warp's units cross at most a few row boundaries
+      q_row = row;
+      const int b = row / p.hkv, g = row % p.hkv;
+      nca = decode_nca(p, b);
+      const __nv_bfloat16* qb = p.q + ((int64_t)b * p.h + g * R) * D;
+      load_a_frags<D>(qa, rlo < R ? qb + rlo * D : nullptr, rhi < R ? qb + rhi * D : nullptr, lane);
+    }
+    cp_async_wait<kDecodeStages - 1>();
+    __syncwarp();
+    if (uu * kUnit < nca) {
+      const uint32_t sb = ring + (i % kDecodeStages) * kUnitBytes;
+      float s[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) s[a][0] = s[a][1] = s[a][2] = s[a][3] = 0.f;
+      qk_16keys<D>(&s[0], qa, sb, 0, lane);
+      qk_16keys<D>(&s[2], qa, sb, 16, lane);
+      float x_lo = kNegInf, x_hi = kNegInf;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = uu * kUnit + nt * 8 + q4 * 2 + (j & 1);
+          s[nt][j] = c < nca ? s[nt][j] * p.scale_log2 : kNegInf;
+          if (j < 2) x_lo = fmaxf(x_lo, s[nt][j]); else x_hi = fmaxf(x_hi, s[nt][j]);
+        }
+      const float mx_lo = quad_max(x_lo), mx_hi = quad_max(x_hi);
+      const float m_lo = mx_lo == kNegInf ? 0.f : mx_lo, m_hi = mx_hi == kNegInf ? 0.f : mx_hi;
+      float l_lo = 0.f, l_hi = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        s[nt][0] = ex2(s[nt][0] - m_lo);
+        s[nt][1] = ex2(s[nt][1] - m_lo);
+        s[nt][2] = ex2(s[nt][2] - m_hi);
+        s[nt][3] = ex2(s[nt][3] - m_hi);
+        l_lo += s[nt][0] + s[nt][1];
+        l_hi += s[nt][2] + s[nt][3];
+      }
+      l_lo = quad_sum(l_lo);
+      l_hi = quad_sum(l_hi);
+      float* zt = p.z + ((int64_t)row * U + uu) * 8 * R;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {  // n-tile nt holds blocks 2nt and 2nt+1 of the unit
+        float x = (q4 & 1) ? s[nt][0] : s[nt][0] + s[nt][1];
+        float y = (q4 & 1) ? s[nt][2] : s[nt][2] + s[nt][3];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        y += __shfl_xor_sync(0xffffffffu, y, 1);
+        if ((q4 & 1) == 0) {
+          const int jl = 2 * nt + (q4 >> 1);
+          if (rlo < R) zt[jl * R + rlo] = x;
+          if (rhi < R) zt[jl * R + rhi] = y;
+        }
+      }
+      if (q4 == 0) {
+        float* um = p.unit_ml + (((int64_t)row * U + uu) * R) * 2;
+        if (rlo < R) {
+          um[rlo * 2] = m_lo;
+          um[rlo * 2 + 1] = l_lo;
+        }
+        if (rhi < R) {
+          um[rhi * 2] = m_hi;
+          um[rhi * 2 + 1] = l_hi;
+        }
+      }
+    }
+    __syncwarp();  // the stage is refilled by the next iteration's issue
+  }
+  cp_async_wait<0>();
+}
+
+// Selection of one row (b, g), run by the CTA that completed the row's score units:
+// the normaliser per head from the units' (max, sum), the pooled block scores, the
+// top-k, and the release of the row's block list.  Every thread of the CTA calls it.
+template <int D, int R, int NPL, bool W>
+__device__ __forceinline__ void select_row(const DecodeParams& p, int row, uint8_t* smem, int* s_topk,
+                                           int (*s_two)[64]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = row / p.hkv;
   const int L = p.seqlens[b];
   const int n_c = num_cmp(L, 32, 16);
   const int nca = num_causal_cmp(L - 1, n_c, 32, 16);
-  const int n_tb = (nca + kTile - 1) / kTile;
-  const int64_t row = (int64_t)b * p.hkv + g;
-  if (tile < n_tb) {
-    const uint32_t sb = smem_u32(smem) + warp * kTile * D * 2;
-    const __nv_bfloat16* kbase = p.kc + (((int64_t)b * p.nc_stride) * p.hkv + g) * D;
-    const int64_t row_stride = (int64_t)p.hkv * D;
-    load_tile_async<D, kTile, 32>(sb, lane, p.kc, [&](int rr) -> const __nv_bfloat16* {
-      const int c = tile * kTile + rr;
-      return c < nca ? kbase + c * row_stride : nullptr;
-    });
-    cp_async_commit();
-    const int rlo = lane >> 2, rhi = rlo + 8;
-    const __nv_bfloat16* qb = p.q + ((int64_t)b * p.h + g * R) * D;
-    uint32_t qa[D / 16][4];
-    load_a_frags<D>(qa, rlo < R ? qb + rlo * D : nullptr, rhi < R ? qb + rhi * D : nullptr, lane);
-    cp_async_wait<0>();
-    __syncwarp();
-    float s[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int k16 = 0; k16 < 4; ++k16) qk_16keys<D>(&s[2 * k16], qa, sb, k16 * 16, lane);
-    float x_lo = kNegInf, x_hi = kNegInf;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = tile * kTile + nt * 8 + (lane & 3) * 2 + (j & 1);
-        s[nt][j] = c < nca ? s[nt][j] * p.scale_log2 : kNegInf;
-        if (j < 2) x_lo = fmaxf(x_lo, s[nt][j]); else x_hi = fmaxf(x_hi, s[nt][j]);
-      }
-    const float mx_lo = quad_max(x_lo), mx_hi = quad_max(x_hi);
-    const float m_lo = mx_lo == kNegInf ? 0.f : mx_lo, m_hi = mx_hi == kNegInf ? 0.f : mx_hi;
-    float l_lo = 0.f, l_hi = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      l_lo += ex2(s[nt][0] - m_lo) + ex2(s[nt][1] - m_lo);
-      l_hi += ex2(s[nt][2] - m_hi) + ex2(s[nt][3] - m_hi);
-    }
-    l_lo = quad_sum(l_lo);
-    l_hi = quad_sum(l_hi);
-    // pooled partials of this tile relative to its own row max: block jl (0..15) of the
-    // tile sums the windows 4jl, 4jl+1, 4jl+2 (n-tile nt holds blocks 2nt and 2nt+1)
-    float* zt = p.z + (row * p.n_tiles + tile) * 16 * R;
-    const int q4 = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p0 = ex2(s[nt][0] - m_lo), p1 = ex2(s[nt][1] - m_lo);
-      const float p2 = ex2(s[nt][2] - m_hi), p3 = ex2(s[nt][3] - m_hi);
-      float x = (q4 & 1) ? p0 : p0 + p1;
-      float y = (q4 & 1) ? p2 : p2 + p3;
-      x += __shfl_xor_sync(0xffffffffu, x, 1);
-      y += __shfl_xor_sync(0xffffffffu, y, 1);
-      if ((q4 & 1) == 0) {
-        const int jl = 2 * nt + (q4 >> 1);
-        if (rlo < R) zt[jl * R + rlo] = x;
-        if (rhi < R) zt[jl * R + rhi] = y;
-      }
-    }
-    if ((lane & 3) == 0) {
-      float* tm = p.tile_ml + ((row * p.n_tiles + tile) * R) * 2;
-      if (rlo < R) {
-        tm[rlo * 2] = m_lo;
-        tm[rlo * 2 + 1] = l_lo;
-      }
-      if (rhi < R) {
-        tm[rhi * 2] = m_hi;
-        tm[rhi * 2 + 1] = l_hi;
-      }
-    }
-  }
-  // arrival: the last item of this (sequence, kv-head) runs the selection
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = atomicAdd(&p.score_count[row], 1) == p.n_groups - 1;
-  __syncthreads();
-  if (!*s_flag) return;
-  __threadfence();
+  const int n_u = (nca + kUnit - 1) / kUnit;
+  const int U = p.n_units;
   // Every global load of the selection is issued in one batch (data written by other
-  // SMs costs a full L2 round trip each time): the row's tile (max, sum) pairs go to
+  // SMs costs a full L2 round trip each time): the row's unit (max, sum) pairs go to
   // shared memory, this thread's pooled block partials to registers.
   constexpr int JPT = NPL * 32 / 128;                     // blocks per thread
   constexpr int ZB = JPT * R <= 64 ? JPT : (64 / R > 0 ? 64 / R : 1);  // blocks per batch
-  float* red_m = reinterpret_cast<float*>(smem);  // [R][kMaxTiles]
-  float* red_l = red_m + R * kMaxTiles;           // [R][kMaxTiles]
-  float* sc = red_l + R * kMaxTiles;              // [NPL*32]
-  float* fac = sc + NPL * 32;                     // [kMaxTiles][R]
+  float* red_m = reinterpret_cast<float*>(smem);  // [R][kMaxUnits]
+  float* red_l = red_m + R * kMaxUnits;           // [R][kMaxUnits]
+  float* sc = red_l + R * kMaxUnits;              // [NPL*32]
+  float* fac = sc + NPL * 32;                     // [kMaxUnits][R]
   const int nb = (L + 63) / 64;
-  const float* zr = p.z + row * p.n_tiles * 16 * R;
+  const float* zr = p.z + (int64_t)row * U * 8 * R;
   float zreg[ZB][R];
   auto load_z = [&](int j0) {  // blocks j0 + 128*i, i < ZB
 #pragma unroll
     for (int i = 0; i < ZB; ++i) {
       const int j = j0 + 128 * i;
-      const bool ok = j < nb && j / 16 < n_tb;
+      const bool ok = j < nb && j / 8 < n_u;
 #pragma unroll
       for (int hh = 0; hh < R; ++hh) zreg[i][hh] = ok ? __ldcg(zr + (int64_t)j * R + hh) : 0.f;
     }
   };
-  for (int i = threadIdx.x; i < R * n_tb; i += blockDim.x) {
-    const int hh = i / n_tb, tl = i % n_tb;
-    const float* tm = p.tile_ml + ((row * p.n_tiles + tl) * R + hh) * 2;
-    red_m[hh * kMaxTiles + tl] = __ldcg(tm);
-    red_l[hh * kMaxTiles + tl] = __ldcg(tm + 1);
+  for (int i = threadIdx.x; i < R * n_u; i += blockDim.x) {
+    const int hh = i / n_u, ul = i % n_u;
+    const float* um = p.unit_ml + (((int64_t)row * U + ul) * R + hh) * 2;
+    red_m[hh * kMaxUnits + ul] = __ldcg(um);
+    red_l[hh * kMaxUnits + ul] = __ldcg(um + 1);
   }
   load_z(threadIdx.x);
   __syncthreads();
-  // per-head normaliser: one warp per head folds the tile pairs with shuffles, then
-  // writes the factor 2^(m_tile - lse) that turns a tile's partials into probabilities
-  for (int hh = warp; hh < R; hh += 4) {
-    float mv[kMaxTiles / 32], lv[kMaxTiles / 32];
+  // per-head normaliser: one warp per head folds the unit pairs with shuffles, then
+  // writes the factor 2^(m_unit - lse) that turns a unit's partials into probabilities
+  for (int hh = warp; hh < R; hh += kNW) {
+    float mv[kMaxUnits / 32], lv[kMaxUnits / 32];
     float M = kNegInf;
 #pragma unroll
-    for (int i = 0; i < kMaxTiles / 32; ++i) {
-      const int tl = lane + 32 * i;
-      mv[i] = tl < n_tb ? red_m[hh * kMaxTiles + tl] : kNegInf;
-      lv[i] = tl < n_tb ? red_l[hh * kMaxTiles + tl] : 0.f;
+    for (int i = 0; i < kMaxUnits / 32; ++i) {
+      const int ul = lane + 32 * i;
+      mv[i] = ul < n_u ? red_m[hh * kMaxUnits + ul] : kNegInf;
+      lv[i] = ul < n_u ? red_l[hh * kMaxUnits + ul] : 0.f;
       M = fmaxf(M, mv[i]);
     }
 #pragma unroll
@@ -184,14 +274,14 @@ __device__ __forceinline__ void score_item(const DecodeParams& p, int b, int g, 
     const float Mu = M == kNegInf ? 0.f : M;
     float S = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxTiles / 32; ++i) S += lv[i] * ex2(mv[i] - Mu);
+    for (int i = 0; i < kMaxUnits / 32; ++i) S += lv[i] * ex2(mv[i] - Mu);
 #pragma unroll
     for (int off = 16; off; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
     const float lse = S > 0.f ? Mu + __log2f(S) : 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxTiles / 32; ++i) {
-      const int tl = lane + 32 * i;
-      if (tl < n_tb) fac[tl * R + hh] = ex2(mv[i] - lse);
+    for (int i = 0; i < kMaxUnits / 32; ++i) {
+      const int ul = lane + 32 * i;
+      if (ul < n_u) fac[ul * R + hh] = ex2(mv[i] - lse);
     }
   }
   __syncthreads();
@@ -205,8 +295,8 @@ __device__ __forceinline__ void score_item(const DecodeParams& p, int b, int g, 
       const int c0 = 4 * j;
       const int cnt = (c0 < n_c) + (c0 + 1 < n_c) + (c0 + 2 < n_c);
       float acc = 0.f;
-      if (j < nb && j / 16 < n_tb) {
-        const float* fj = fac + (j / 16) * R;
+      if (j < nb && j / 8 < n_u) {
+        const float* fj = fac + (j / 8) * R;
 #pragma unroll
         for (int hh = 0; hh < R; ++hh) acc += zreg[i][hh] * fj[hh];
       }
@@ -255,7 +345,6 @@ __device__ __forceinline__ void score_item(const DecodeParams& p, int b, int g, 
     }
     for (int q = nsel + e; q < p.k; q += blockDim.x) p.idx[row * p.k + q] = -1;
   }
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) st_release(&p.ready[row], 1);
 }
@@ -280,23 +369,7 @@ __device__ __forceinline__ void attn_item(const DecodeParams& p, int b, int g, i
   uint32_t qa[D / 16][4];
   load_a_frags<D>(qa, rlo < R ? qb + rlo * D : nullptr, rhi < R ? qb + rhi * D : nullptr, lane);
   // the row's block list is ready once its selecting CTA has released the flag
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    if (ld_acquire(&p.ready[row]) == 0) {
-      const unsigned long long t0 = tc::globaltimer(), lim = tc::wait_limit();
-      while (ld_acquire(&p.ready[row]) == 0) {
-        if (tc::device_status_set() || lim < tc::kQuickNs || tc::globaltimer() - t0 >= lim) {
-          atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
-          ok = 0;
-          break;
-        }
-        __nanosleep(128);
-      }
-    }
-    *s_flag = ok;
-  }
-  __syncthreads();
-  if (!*s_flag) return;
+  if (!cta_wait_ge(&p.ready[row], 1, s_flag)) return;
   // this warp's work list: the split's blocks whose slice starts at or before t
   const int32_t* il = p.idx + (int64_t)row * p.k;
   int cnt = 0;
@@ -338,12 +411,10 @@ __device__ __forceinline__ void attn_item(const DecodeParams& p, int b, int g, i
       p.part_ml[(slot + rhi) * 2 + 1] = st.l1;
     }
   }
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *s_flag = atomicAdd(&p.merge_count[row], 1) == p.n_split - 1;
+  if (threadIdx.x == 0) *s_flag = atom_acq_rel_add(&p.merge_count[row], 1) == p.n_split - 1;
   __syncthreads();
   if (!*s_flag) return;
-  __threadfence();
   const int hr = threadIdx.x >> 3;  // head row of the group, 8 threads per row
   if (hr >= R) return;
   const int64_t base = (int64_t)row * p.n_split;
@@ -368,32 +439,54 @@ __device__ __forceinline__ void attn_item(const DecodeParams& p, int b, int g, i
   for (int c = 0; c < D / 8; ++c) dst[cl + 8 * c] = __float2bfloat16_rn(acc[c] * inv);
 }
 
-constexpr int kDecodeStages = 3;  // 96 KB of rings: two CTAs per SM
+// 96 KB of rings: two CTAs per SM
 template <bool W>
 constexpr int decode_smem() {
   return kNW * kDecodeStages * attend_stage_bytes<128, W>();
 }
 
+// The step.  Phase 1: every CTA scores a contiguous run of the (row, unit) space and
+// adds its unit count to each row it touched (it waits on nothing).  Phase 2: the CTAs
+// take items from the queue, first one selection per row, then the attention items
+// (row, split).  A selection waits (bounded) until all of its row's units have arrived,
+// an attention item until its row's list is released.  Every CTA is resident
+// (cooperative launch) and finishes phase 1 before it takes an item, and the queue
+// hands out every selection before any attention item, so every awaited count or list
+// is being made by a running CTA.
 template <int R, int NPL, bool W>
 __global__ void __launch_bounds__(kNW * 32, 2) decode_step(const DecodeParams p, int rows) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_item, s_flag;
-  __shared__ int s_topk[2 * 16 * kNW + 2 * kNW];  // top-k scratch
+  __shared__ __align__(16) int s_topk[block_topk_scratch_ints<kNW * 32>()];  // top-k scratch
   __shared__ int s_list[kNW][64];
   __shared__ int s_two[W ? 4 : 1][64];  // two-stage selection: kept list, keys, blocks, chosen flags
-  const int n_score = rows * p.n_groups;
-  const int n_items = n_score + rows * p.n_split;
+  const int U = p.n_units;
+  const int64_t total = (int64_t)rows * U;  // < 2^31 (checked by the launcher)
+  const int u0 = (int)(total * blockIdx.x / gridDim.x), u1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  score_units<128, R>(p, u0, u1, smem);
+  __syncthreads();
+  if (u0 < u1) {
+    const int r_first = u0 / U, r_last = (u1 - 1) / U;
+    for (int r = r_first + (int)threadIdx.x; r <= r_last; r += kNW * 32) {
+      const int lo = u0 > r * U ? u0 : r * U;
+      const int hi = u1 < (r + 1) * U ? u1 : (r + 1) * U;
+      red_release_add(&p.score_count[r], hi - lo);
+    }
+  }
+  __syncthreads();  // the shared memory of the score rings is reused by the items
+  const int n_items = rows + rows * p.n_split;
   for (;;) {
     if (threadIdx.x == 0) s_item = atomicAdd(p.queue, 1);
     __syncthreads();
     const int item = s_item;
     __syncthreads();  // s_item is rewritten only after every thread has read it
     if (item >= n_items || tc::device_status_set()) break;
-    if (item < n_score) {
-      const int row = item / p.n_groups;
-      score_item<128, R, NPL, W>(p, row / p.hkv, row % p.hkv, item % p.n_groups, smem, &s_flag, s_topk, s_two);
+    if (item < rows) {
+      if (cta_wait_ge(&p.score_count[item], U, &s_flag)) {
+        select_row<128, R, NPL, W>(p, item, smem, s_topk, s_two);
+      }
     } else {
-      const int a = item - n_score, row = a / p.n_split;
+      const int a = item - rows, row = a / p.n_split;
       attn_item<128, R, kDecodeStages, W>(p, row / p.hkv, row % p.hkv, a % p.n_split, smem, &s_flag, s_list);
     }
     __syncthreads();
@@ -403,9 +496,9 @@ __global__ void __launch_bounds__(kNW * 32, 2) decode_step(const DecodeParams p,
 template <int R, int NPL, bool W>
 static cudaError_t run_decode(const DecodeArgs& a, const DecodeLayout& l, cudaStream_t st) {
   constexpr int kDecodeSmem = decode_smem<W>();
-  static_assert(2 * R * kMaxTiles * 4 + NPL * 32 * 4 + kMaxTiles * R * 4 <= kNW * kTile * 128 * 2,
-                "select scratch must fit the score tile buffers");
-  static_assert(kNW * kTile * 128 * 2 <= kDecodeSmem, "score tiles must fit the rings");
+  static_assert(2 * R * kMaxUnits * 4 + NPL * 32 * 4 + kMaxUnits * R * 4 <= kDecodeSmem,
+                "selection scratch must fit the rings");
+  static_assert(kNW * kDecodeStages * kUnitBytes <= kDecodeSmem, "score rings must fit");
   auto kern = decode_step<R, NPL, W>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
   if (e != cudaSuccess) return e;
@@ -425,8 +518,7 @@ static cudaError_t run_decode(const DecodeArgs& a, const DecodeLayout& l, cudaSt
   p.hkv = a.hkv;
   p.max_len = a.max_len;
   p.nc_stride = a.max_len >= a.kernel ? (a.max_len - a.kernel) / a.stride + 1 : 0;
-  p.n_tiles = l.n_tiles;
-  p.n_groups = l.n_tiles > 0 ? (l.n_tiles + kNW - 1) / kNW : 1;  // one item selects even without keys
+  p.n_units = l.n_units;  // >= 1: a row without compressed keys still has a unit to complete
   p.n_init = a.n_init;
   p.n_local = a.n_local;
   p.k = a.k;
@@ -434,7 +526,7 @@ static cudaError_t run_decode(const DecodeArgs& a, const DecodeLayout& l, cudaSt
   p.eps = (a.k + l.n_split - 1) / l.n_split;
   p.scale_log2 = a.scale * kLog2e;
   p.z = a.z;
-  p.tile_ml = a.tile_ml;
+  p.unit_ml = a.unit_ml;
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
   p.idx = a.idx;
@@ -448,9 +540,10 @@ static cudaError_t run_decode(const DecodeArgs& a, const DecodeLayout& l, cudaSt
   p.score_count = a.counters + 1;
   p.merge_count = p.score_count + rows;
   p.ready = p.merge_count + rows;
-  const int n_items = rows * (p.n_groups + p.n_split);
+  if ((int64_t)rows * p.n_units >= (int64_t)1 << 31) return cudaErrorInvalidValue;
+  const int64_t work = (int64_t)rows * (p.n_units > p.n_split ? p.n_units : p.n_split);
   // persistent: at most one CTA per resident slot (the cooperative launch checks it)
-  const int grid = n_items < per_sm * sms ? n_items : per_sm * sms;
+  const int grid = work < (int64_t)per_sm * sms ? (int)work : per_sm * sms;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kNW * 32);

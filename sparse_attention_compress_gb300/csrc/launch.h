@@ -136,8 +136,8 @@ struct DecodeArgs {
   int32_t* idx;  // [batch, hkv, k]
   void* o;
   // scratch
-  float* z;        // [batch, hkv, r, nc_pad]
-  float* tile_ml;  // [batch, hkv, n_tiles, r, 2]
+  float* z;        // [batch, hkv, n_units, 8, r]
+  float* unit_ml;  // [batch, hkv, n_units, r, 2]
   float* part_o;   // [batch, hkv * rtiles, n_split, 16, d]
   float* part_ml;  // [batch, hkv * rtiles, n_split, 16, 2]
   int* counters;  // DecodeLayout::counter_bytes: queue head, arrivals, ready flags (zeroed per call)
@@ -149,8 +149,8 @@ struct DecodeArgs {
   int cis_nb_stride = 0, qk = 0;
 };
 struct DecodeLayout {
-  size_t z, tile_ml, idx, part_o, part_ml, counters, counter_bytes, total;
-  int nc_pad, n_tiles, n_split;
+  size_t z, unit_ml, idx, part_o, part_ml, counters, counter_bytes, total;
+  int n_units, n_split;
 };
 DecodeLayout decode_layout(int batch, int max_len, int h, int hkv, int d, int kernel, int stride,
                            int block_size, int k);

@@ -248,130 +248,202 @@ __device__ __forceinline__ void warp_topk(const float* row, int nb, int own, int
   }
 }
 
-// The same selection spread over a CTA of NT threads, each owning E consecutive blocks
-// of a row (global or shared memory): the radix passes count digits in registers, sum
-// them per warp and combine the warps through shared memory, one barrier per pass; the
-// chosen blocks are written in block order through a CTA prefix count.  For rows whose
-// latency matters (the decode selection): a single warp's chain of dependent
-// reductions is what this avoids.  scratch: 2 * 16 * (NT / 32) + 2 * (NT / 32) ints.
-// Every thread of the CTA must call it.
+// Exclusive prefix of x over the CTA in thread order; tot: NW ints of shared scratch
+// that no thread reads or writes around the call.  Every thread must call it.
+template <int NW>
+__device__ __forceinline__ int block_excl_scan(int x, int* tot, int lane, int warp) {
+  const int incl = warp_excl_scan(x, lane) + x;
+  if (lane == 31) tot[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += tot[w];
+  __syncthreads();  // tot may be rewritten after this
+  return before + incl - x;
+}
+
+// The same selection spread over a CTA of NT = 128 threads, each owning E consecutive
+// blocks of a row (global or shared memory), for rows whose latency matters (the decode
+// selection, k <= NT).  The steps are chosen for few dependent CTA-wide exchanges:
+//  1. the forced blocks are counted apart (always kept; if they alone reach k, the k
+//     lowest are kept), and the bits shared by every other candidate's key are found
+//     with one reduction, so no pass spends itself on them;
+//  2. radix passes over 8 bits at a time: a shared-memory histogram of the candidates
+//     that match the prefix so far, and a suffix count over the bins that finds the bin
+//     holding the remaining k-th best; its bits join the prefix.  One pass usually
+//     leaves a handful of keys in that bin;
+//  3. once the bin holds at most NT candidates, they are ranked exactly against each
+//     other by (key descending, block ascending), one candidate per thread, and the
+//     winners are marked in a per-block table; if a bin is still larger when every bit is
+//     used, its keys are equal and the lowest blocks win.
+// The chosen blocks are written in block order through a CTA prefix count.
+// scratch: block_topk_scratch_ints<NT>() ints, 8-byte aligned.  Every thread of the CTA
+// must call it.
+template <int NT>
+constexpr int block_topk_scratch_ints() {
+  return 2 * 256 + 2 * NT + 32 + 1024 / 4;
+}
+
 template <int E, int NT>
 __device__ __forceinline__ void block_topk(const float* row, int nb, int own, int n_init, int n_local, int k,
                                            int32_t* out, int* scratch) {
+  static_assert(NT == 128, "four warps: two histogram bins per thread");
   constexpr int NWARP = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* s_cnt = scratch;                   // [2][NWARP][16]
-  int* s_red = scratch + 2 * NWARP * 16;  // [2][NWARP]
+  int* hist = scratch;                                              // [2][256]
+  uint64_t* cand = reinterpret_cast<uint64_t*>(scratch + 512);      // [NT]
+  int* misc = scratch + 512 + 2 * NT;                               // [32]
+  uint8_t* won = reinterpret_cast<uint8_t*>(scratch + 512 + 2 * NT + 32);  // [1024] bin winners
   const int ncand = min(own + 1, nb);
   if (ncand <= k) {
     for (int q = tid; q < k; q += NT) out[q] = q < ncand ? q : -1;
     return;
   }
   uint32_t key[E];
-  bool valid[E];
-  const int j0 = tid * E;
+  bool norm[E], forced[E];
+  int nf = 0;
   uint32_t all_and = 0xffffffffu, all_or = 0u;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    const int j = j0 + i;
-    valid[i] = j < ncand;
-    const bool forced = j < n_init || j > own - n_local;
-    key[i] = valid[i] ? (forced ? 0xffffffffu : order_key(row[j])) : 0u;
-    if (valid[i]) {
+    const int j = tid * E + i;
+    const bool valid = j < ncand;
+    forced[i] = valid && (j < n_init || j > own - n_local);
+    norm[i] = valid && !forced[i];
+    key[i] = norm[i] ? order_key(row[j]) : 0u;
+    nf += forced[i];
+    if (norm[i]) {
       all_and &= key[i];
       all_or |= key[i];
     }
   }
-  // bits shared by every candidate take no pass
-  all_and = __reduce_and_sync(0xffffffffu, all_and);
-  all_or = __reduce_or_sync(0xffffffffu, all_or);
-  if (lane == 0) {
-    s_red[warp] = (int)all_and;
-    s_red[NWARP + warp] = (int)all_or;
+  // step 1: forced count and the bits shared by the other candidates
+  {
+    const int f = (int)__reduce_add_sync(0xffffffffu, (unsigned)nf);
+    const uint32_t a = __reduce_and_sync(0xffffffffu, all_and), o = __reduce_or_sync(0xffffffffu, all_or);
+    for (int q = tid; q < 256; q += NT) hist[q] = 0;
+    if (lane == 0) {
+      misc[warp] = f;
+      misc[NWARP + warp] = (int)a;
+      misc[2 * NWARP + warp] = (int)o;
+    }
   }
   __syncthreads();
+  int n_forced = 0;
+  all_and = 0xffffffffu;
+  all_or = 0u;
 #pragma unroll
   for (int w = 0; w < NWARP; ++w) {
-    all_and &= (uint32_t)s_red[w];
-    all_or |= (uint32_t)s_red[NWARP + w];
+    n_forced += misc[w];
+    all_and &= (uint32_t)misc[NWARP + w];
+    all_or |= (uint32_t)misc[2 * NWARP + w];
   }
-  const uint32_t varying = all_and ^ all_or;
-  uint32_t P = all_and;
-  int left = k;
-  if (varying != 0u) {
-    int shift = ((31 - __clz(varying)) / 4) * 4;
-    uint32_t pmask = shift + 4 >= 32 ? 0u : (0xffffffffu << (shift + 4));
-    uint32_t prefix = all_and & pmask;
-    int buf = 0;
-#pragma unroll 1
-    for (; shift >= 0; shift -= 4, buf ^= 1) {
-      unsigned long long lo = 0ull, hi = 0ull;  // 16 digit counters of this thread, 8 bits each
+  bool sel[E];
+  int left = k - n_forced;
+  if (left <= 0) {
+    // the forced blocks alone fill the list: the k lowest of them
+    int rank = block_excl_scan<NWARP>(nf, misc + 16, lane, warp);
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      sel[i] = forced[i] && rank < k;
+      rank += forced[i];
+    }
+  } else {
+    const uint32_t varying = all_and ^ all_or;
+    int shift = varying ? 31 - __clz(varying) + 1 : 0;  // bits [shift, 32) are settled
+    uint32_t mask = shift >= 32 ? 0u : (0xffffffffu << shift);
+    uint32_t prefix = all_and & mask;
+    int buf = 0, in_bin = ncand - n_forced;
+    // step 2: radix passes while the k-th best's bin is larger than NT
+    while (shift > 0 && in_bin > NT) {
+      const int w = shift < 8 ? shift : 8;
+      shift -= w;
+      int* h = hist + buf * 256;
+      int* h_next = hist + (buf ^ 1) * 256;
+      for (int q = tid; q < 256; q += NT) h_next[q] = 0;  // read-free until the next pass
 #pragma unroll
       for (int i = 0; i < E; ++i)
-        if (valid[i] && (key[i] & pmask) == prefix) {
-          const uint32_t d = (key[i] >> shift) & 15u;
-          const unsigned long long inc = 1ull << ((d & 7u) * 8u);
-          if (d < 8u) lo += inc; else hi += inc;
-        }
-      int* cnt = s_cnt + buf * NWARP * 16 + warp * 16;
+        if (norm[i] && (key[i] & mask) == prefix) atomicAdd(&h[(key[i] >> shift) & ((1u << w) - 1u)], 1);
+      __syncthreads();
+      // suffix counts: thread t owns bins 2t and 2t+1; counts above a bin are those of
+      // higher bins
+      const int b0 = h[2 * tid], b1 = h[2 * tid + 1], c = b0 + b1;
+      int sfx = c;  // inclusive suffix sum within the warp (higher lanes hold higher bins)
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const unsigned f = (unsigned)(((q < 8 ? lo : hi) >> ((q & 7) * 8)) & 0xffull);
-        const int c = (int)__reduce_add_sync(0xffffffffu, f);
-        if (lane == 0) cnt[q] = c;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, sfx, off);
+        if (lane + off < 32) sfx += y;
       }
-      __syncthreads();  // the other buffer is rewritten only after the next barrier
-      int run = 0, dsel = 0, above = 0;
-      bool found = false;
-#pragma unroll
-      for (int q = 15; q >= 0; --q) {
-        int c = 0;
-#pragma unroll
-        for (int w = 0; w < NWARP; ++w) c += s_cnt[buf * NWARP * 16 + w * 16 + q];
-        if (!found && run + c >= left) {
-          found = true;
-          dsel = q;
-          above = run;
-        }
-        run += c;
+      if (lane == 0) misc[16 + warp] = sfx;
+      __syncthreads();
+      int higher = sfx - c;  // count in bins above this thread's two
+      for (int w2 = warp + 1; w2 < NWARP; ++w2) higher += misc[16 + w2];
+      if (higher < left && left <= higher + c) {  // the k-th best lies in one of this thread's bins
+        const bool top = left <= higher + b1;
+        misc[20] = top ? 2 * tid + 1 : 2 * tid;
+        misc[21] = top ? higher : higher + b1;
+        misc[22] = top ? b1 : b0;
       }
-      left -= above;
-      prefix |= (uint32_t)dsel << shift;
-      pmask |= 15u << shift;
+      __syncthreads();
+      const uint32_t d = (uint32_t)misc[20];
+      left -= misc[21];
+      in_bin = misc[22];
+      prefix |= d << shift;
+      mask |= ((1u << w) - 1u) << shift;
+      buf ^= 1;
+      __syncthreads();  // misc is rewritten by the next pass
     }
-    P = prefix;
-  }
-  // exclusive prefix over the CTA, in block order (threads own consecutive blocks)
-  int* s_tot = s_red;  // reused: its last readers passed at least one barrier since
-  auto block_scan = [&](int x) {
-    const int incl = warp_excl_scan(x, lane) + x;
-    __syncthreads();  // s_tot may still be read by a previous scan
-    if (lane == 31) s_tot[warp] = incl;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += s_tot[w];
-    return before + incl - x;
-  };
-  int tie = 0;
+    // step 3: the k-th best's bin (keys equal to prefix on the settled bits)
+    int rank_tie = 0;
+    if (in_bin > NT) {  // every bit settled: equal keys, the lowest blocks win
+      int eq = 0;
 #pragma unroll
-  for (int i = 0; i < E; ++i) tie += (valid[i] && key[i] == P) ? 1 : 0;
-  int rank = block_scan(tie);
-  bool sel[E];
+      for (int i = 0; i < E; ++i) eq += norm[i] && key[i] == prefix;
+      rank_tie = block_excl_scan<NWARP>(eq, misc + 16, lane, warp);
+    } else {
+      if (tid == 0) misc[23] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        if (norm[i] && (key[i] & mask) == prefix)
+          cand[atomicAdd(&misc[23], 1)] = ((uint64_t)key[i] << 32) | (uint32_t)~(uint32_t)(tid * E + i);
+      __syncthreads();
+      const int nc = in_bin;
+      if (tid < nc) {  // candidate tid's rank in the bin: the candidates above it
+        const uint64_t me = cand[tid];
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        int q = 0;
+        for (; q + 4 <= nc; q += 4) {
+          r0 += cand[q] > me;
+          r1 += cand[q + 1] > me;
+          r2 += cand[q + 2] > me;
+          r3 += cand[q + 3] > me;
+        }
+        for (; q < nc; ++q) r0 += cand[q] > me;
+        won[~(uint32_t)me] = (r0 + r1) + (r2 + r3) < left;
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const bool inb = norm[i] && (key[i] & mask) == prefix;
+      bool s = forced[i] || (norm[i] && (key[i] & mask) > prefix);
+      if (inb) {
+        if (in_bin > NT) {
+          s = rank_tie < left;
+          ++rank_tie;
+        } else {
+          s = won[tid * E + i] != 0;
+        }
+      }
+      sel[i] = s;
+    }
+  }
   int nsel = 0;
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    if (valid[i] && key[i] == P) {
-      sel[i] = rank < left;
-      ++rank;
-    } else {
-      sel[i] = valid[i] && key[i] > P;
-    }
-    nsel += sel[i] ? 1 : 0;
-  }
-  int pos = block_scan(nsel);
+  for (int i = 0; i < E; ++i) nsel += sel[i];
+  int pos = block_excl_scan<NWARP>(nsel, misc + 24, lane, warp);
 #pragma unroll
   for (int i = 0; i < E; ++i)
-    if (sel[i]) out[pos++] = j0 + i;
+    if (sel[i]) out[pos++] = tid * E + i;
 }
 
 }  // namespace nsa
