@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnsa.so")
-SOURCES = ["api.cu", "compress.cu", "select.cu", "sparse_fwd.cu", "sparse_bwd.cu", "dense_attn.cu", "dense_tc.cu",
+SOURCES = ["api.cu", "compress.cu", "select.cu", "sparse_fwd.cu", "sparse_bwd.cu", "sparse_bwd_tc.cu", "dense_attn.cu", "dense_tc.cu",
            "decode.cu", "decode_nosa.cu", "noalloc.cu", "nosa.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

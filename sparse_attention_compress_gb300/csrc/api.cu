@@ -117,12 +117,13 @@ const char* nsa_last_error(void) { return g_err; }
 nsa_status nsa_device_status(int32_t* status, int reset) {
   NSA_RANGE();
   NSA_REQUIRE(status != nullptr, NSA_ERR_INVALID, "nsa_device_status: status is NULL");
-  int32_t a = 0, b = 0, c = 0, f = 0;
+  int32_t a = 0, b = 0, c = 0, f = 0, k = 0;
   cudaError_t e = status_word_dense_tc(&a, reset != 0);
   if (e == cudaSuccess) e = status_word_decode(&b, reset != 0);
   if (e == cudaSuccess) e = status_word_decode_nosa(&c, reset != 0);
   if (e == cudaSuccess) e = status_word_sparse_fwd(&f, reset != 0);
-  *status = a ? a : b ? b : c ? c : f;
+  if (e == cudaSuccess) e = status_word_sparse_bwd_tc(&k, reset != 0);
+  *status = a ? a : b ? b : c ? c : f ? f : k;
   return cuda_status(e, "nsa_device_status");
 }
 
@@ -133,6 +134,7 @@ nsa_status nsa_set_wait_limit_ns(uint64_t ns) {
   if (e == cudaSuccess) e = wait_limit_decode(v);
   if (e == cudaSuccess) e = wait_limit_decode_nosa(v);
   if (e == cudaSuccess) e = wait_limit_sparse_fwd(v);
+  if (e == cudaSuccess) e = wait_limit_sparse_bwd_tc(v);
   return cuda_status(e, "nsa_set_wait_limit_ns");
 }
 
@@ -405,7 +407,7 @@ static nsa_status check_sparse_bwd(const nsa_shape* shape, int S, int block_size
 size_t nsa_sparse_bwd_workspace_size(const nsa_shape* shape, int S, int block_size) {
   Seqs s;
   if (check_sparse_bwd(shape, S, block_size, &s, "nsa_sparse_bwd_workspace_size") != NSA_OK) return 0;
-  return sparse_bwd_workspace_bytes(s, shape->h, shape->h_kv);
+  return sparse_bwd_workspace_bytes(s, shape->h, shape->h_kv, S);
 }
 
 nsa_status nsa_sparse_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
@@ -427,7 +429,7 @@ nsa_status nsa_sparse_bwd(const nsa_shape* shape, const void* q, const void* k, 
   NSA_PTR(dv);
   NSA_REQUIRE(lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) == 0, NSA_ERR_INVALID,
               "nsa_sparse_bwd: lse must be non-null and 4-byte aligned");
-  const size_t need = sparse_bwd_workspace_bytes(s, shape->h, shape->h_kv);
+  const size_t need = sparse_bwd_workspace_bytes(s, shape->h, shape->h_kv, S);
   NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
               "nsa_sparse_bwd: workspace must be non-null and 256-byte aligned");
   NSA_REQUIRE(workspace_bytes >= need, NSA_ERR_INVALID, "nsa_sparse_bwd: workspace %zu < %zu bytes",
@@ -947,7 +949,8 @@ struct LayerBwdLayout {
   size_t d_br, dq3, dk3, dv3, dkc, dvc, scratch, total;
 };
 
-static LayerBwdLayout layer_bwd_layout(const Seqs& s, int h, int hkv, int d, int kernel, int stride, int window) {
+static LayerBwdLayout layer_bwd_layout(const Seqs& s, int h, int hkv, int d, int kernel, int stride, int window,
+                                       int S) {
   LayerBwdLayout l{};
   const int64_t ncr = s.cu ? s.tokens / stride + s.n_seqs : (int64_t)s.n_seqs * num_cmp_host(s.T, kernel, stride);
   const size_t qsz = (size_t)s.tokens * h * d * 2, ksz = (size_t)s.tokens * hkv * d * 2;
@@ -965,7 +968,7 @@ static LayerBwdLayout layer_bwd_layout(const Seqs& s, int h, int hkv, int d, int
   l.dvc = off;
   off = align256(off + (size_t)ncr * hkv * d * 2);
   l.scratch = off;
-  size_t sc = sparse_bwd_workspace_bytes(s, h, hkv);
+  size_t sc = sparse_bwd_workspace_bytes(s, h, hkv, S);
   sc = std::max(sc, cmp_attn_bwd_workspace_bytes(s, h, hkv, kernel, stride));
   sc = std::max(sc, swa_bwd_workspace_bytes(s, h, hkv, window));
   l.total = align256(off + sc);
@@ -992,7 +995,7 @@ size_t nsa_layer_bwd_workspace_size(const nsa_shape* shape, int kernel, int stri
   if (check_layer_bwd(shape, kernel, stride, block_size, S, window, &s, "nsa_layer_bwd_workspace_size") != NSA_OK)
     return 0;
   if (s.tokens == 0) return 0;
-  return layer_bwd_layout(s, shape->h, shape->h_kv, shape->d, kernel, stride, window).total;
+  return layer_bwd_layout(s, shape->h, shape->h_kv, shape->d, kernel, stride, window, S).total;
 }
 
 nsa_status nsa_layer_bwd(const nsa_shape* shape, const void* q, const void* k, const void* v,
@@ -1023,7 +1026,7 @@ nsa_status nsa_layer_bwd(const nsa_shape* shape, const void* q, const void* k, c
   NSA_PTR(saved->lse_swa);
   NSA_PTR(saved->idx);
   const int h = shape->h, hkv = shape->h_kv, d = shape->d;
-  const LayerBwdLayout l = layer_bwd_layout(s, h, hkv, d, kernel, stride, window);
+  const LayerBwdLayout l = layer_bwd_layout(s, h, hkv, d, kernel, stride, window, S);
   NSA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, NSA_ERR_INVALID,
               "nsa_layer_bwd: workspace must be non-null and 256-byte aligned");
   NSA_REQUIRE(workspace_bytes >= l.total, NSA_ERR_INVALID, "nsa_layer_bwd: workspace %zu < %zu bytes",

@@ -47,7 +47,7 @@ cudaError_t launch_topk_two_stage(const Seqs& s, const float* scores, int nb_str
 
 // Backward of selected attention (bf16, d 128, block 64, h/hkv <= 16): dq [tokens,h,d],
 // dk/dv [tokens,hkv,d] from q, k, v, the block lists, the forward's o and lse and dO.
-size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv);
+size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int S);
 cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const void* v, const int32_t* idx, int S,
                               int h, int hkv, float scale, const void* o, const float* lse, const void* dout,
                               void* dq, void* dk, void* dv, void* workspace, cudaStream_t st);
@@ -119,11 +119,13 @@ cudaError_t status_word_dense_tc(int32_t* out, bool reset);
 cudaError_t status_word_decode(int32_t* out, bool reset);
 cudaError_t status_word_decode_nosa(int32_t* out, bool reset);
 cudaError_t status_word_sparse_fwd(int32_t* out, bool reset);
+cudaError_t status_word_sparse_bwd_tc(int32_t* out, bool reset);
 // Limit (ns) of the first-level bounded waits of each of those units.
 cudaError_t wait_limit_dense_tc(unsigned long long ns);
 cudaError_t wait_limit_decode(unsigned long long ns);
 cudaError_t wait_limit_decode_nosa(unsigned long long ns);
 cudaError_t wait_limit_sparse_fwd(unsigned long long ns);
+cudaError_t wait_limit_sparse_bwd_tc(unsigned long long ns);
 
 cudaError_t launch_gate_combine(int64_t tokens, int h, int d, const void* o_cmp, const void* o_slc,
                                 const void* o_swa, const float* gates, void* o, cudaStream_t st);

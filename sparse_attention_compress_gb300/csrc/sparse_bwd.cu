@@ -27,126 +27,13 @@
 //      chunk order (deterministic: no floating-point atomics anywhere) and stored.
 #include <algorithm>
 
-#include "common.cuh"
-#include "launch.h"
+#include "sparse_bwd.cuh"
 
 namespace nsa {
 
 namespace {
 
-constexpr int kD = 128;
-constexpr int kBS = 64;
-constexpr int kChunk = 2048;              // query positions per dK/dV work item
-constexpr int kGroup = kChunk / kBS;      // key blocks that share a first chunk
-constexpr int kTileBytes = kBS * kD * 2;  // one 64 x 128 bf16 block
-constexpr int kRowsBytes = 16 * kD * 2;   // 16 rows x 128 bf16
-
-struct BwdParams {
-  const __nv_bfloat16 *q, *k, *v, *o, *dout;
-  const float* lse;
-  const int32_t* idx;
-  __nv_bfloat16 *dq, *dk, *dv;
-  float* dsum;  // [tokens, h]: D = dO . o
-  float* part;  // [n_seqs * hkv][items_per_bg][2][64][128] fp32 partial dK (unscaled), dV
-  Seqs seqs;
-  int h, hkv, S, r;
-  float scale, scale_log2;
-  int n_chunks, nb, items_per_bg;
-  // compressed branch (cmp_kernel > 0): the keys are the packed compressed rows, query t
-  // reaches the compressed keys c < n_causal(t) and its list is every such block (idx is
-  // unused); otherwise the keys are the tokens and query t reaches keys <= t of its list.
-  int cmp_kernel, cmp_stride;
-  // sliding window (window > 0): query t reaches keys max(0, t-window+1) .. t (idx unused);
-  // one work item per key block covers every query that reaches it.
-  int window;
-};
-
-// First key query t may attend.
-__device__ __forceinline__ int key_lo(const BwdParams& p, int t) { return p.window ? max(0, t - p.window + 1) : 0; }
-
-// Key rows of sequence b start here; the sequence has key_len(L) of them.
-__device__ __forceinline__ int64_t key_base(const BwdParams& p, int b) {
-  return p.cmp_kernel ? cmp_offset(p.seqs, b, p.cmp_kernel, p.cmp_stride) : (int64_t)seq_start(p.seqs, b);
-}
-__device__ __forceinline__ int key_len(const BwdParams& p, int L) {
-  return p.cmp_kernel ? num_cmp(L, p.cmp_kernel, p.cmp_stride) : L;
-}
-// Last key query t may attend (-1: none).
-__device__ __forceinline__ int key_bound(const BwdParams& p, int t, int Lk) {
-  return p.cmp_kernel ? num_causal_cmp(t, Lk, p.cmp_kernel, p.cmp_stride) - 1 : t;
-}
-// First query position that reaches key block j.
-__device__ __forceinline__ int first_query(const BwdParams& p, int j) {
-  return p.cmp_kernel ? p.cmp_stride * kBS * j + p.cmp_kernel - 1 : kBS * j;
-}
-
-__device__ __forceinline__ float dot_bf16x2(uint32_t a, uint32_t b) {
-  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-  const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
-  return x.x * y.x + x.y * y.y;
-}
-
-// P and dS enter the dV, dQ and dK products as bf16.  Where a warp's 16 x 16 tile holds
-// a |value| above the threshold (rows with few keys, where p is large and a bf16 rounding
-// of it is not small beside the gradient), the bf16 remainder x - bf16(x) goes through a
-// second product, so the operand is carried to about 16 bits.  The threshold for P is
-// low: with a nearly uniform softmax (the compressed branch's logits are small, since
-// compressed keys are means) p ~ 1/n rounds alike on every row of the same length, and
-// those errors add up over the thousands of rows that reach a key.
-constexpr float kSplitAbove = 0.0625f;   // dS
-constexpr float kSplitPAbove = 0.00390625f;  // P (1/256)
-
-__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(a, b);
-  const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
-  lo = pack_bf16(a - h.x, b - h.y);
-}
-
-// base-2 log-sum-exp of a row from the forward's natural-log lse; rows without keys
-// (lse = -inf) give +inf so that every exponential of that row is 0.
-__device__ __forceinline__ float lse_to_log2(float l) { return l == kNegInf ? __builtin_inff() : l * kLog2e; }
-
-// 4-byte global->shared copy (zero-fill when src_bytes == 0).
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
-// Item index (within one sequence / kv-head) -> (key block j, chunk c).  Blocks
-// j = m*kGroup .. m*kGroup+kGroup-1 have their first query chunk at m and one item for
-// each chunk m .. n_chunks-1.
-__device__ __forceinline__ void item_to_block(const BwdParams& p, int item, int& j, int& c, int& m) {
-  const int n_chunks = p.n_chunks, nb = p.nb;
-  int rem = item;
-  if (p.window) {
-    j = item;
-    c = m = 0;
-    return;
-  }
-  if (p.cmp_kernel) {  // block j has chunks first_query(j) / kChunk .. n_chunks-1
-    for (j = 0; j < nb; ++j) {
-      m = first_query(p, j) / kChunk;
-      if (rem < n_chunks - m) {
-        c = m + rem;
-        return;
-      }
-      rem -= n_chunks - m;
-    }
-    c = n_chunks;
-    return;
-  }
-  for (m = 0; m < n_chunks; ++m) {
-    const int blocks = min(kGroup, nb - m * kGroup);
-    const int per = n_chunks - m;
-    if (rem < blocks * per) {
-      j = m * kGroup + rem / per;
-      c = m + rem % per;
-      return;
-    }
-    rem -= blocks * per;
-  }
-  j = nb;  // not reached for item < items_per_bg
-  c = n_chunks;
-}
+using namespace bwd;
 
 // ---------------------------------------------------------------------------- dQ
 template <int NSTAGE>
@@ -554,11 +441,13 @@ __global__ void __launch_bounds__(256) sparse_bwd_reduce(const BwdParams p) {
 
 struct BwdLayout {
   int n_chunks, nb, items_per_bg;
-  size_t dsum, part, total;
+  size_t dsum, part, inv_list, inv_tab, total;
 };
 
-// cmp_kernel > 0: the compressed branch (keys are the n_c(L) compressed rows).
-BwdLayout bwd_layout(const Seqs& s, int h, int hkv, int cmp_kernel = 0, int cmp_stride = 0, int window = 0) {
+// cmp_kernel > 0: the compressed branch (keys are the n_c(L) compressed rows).  S > 0:
+// selected blocks with lists of S entries (room for the inverted lists).
+BwdLayout bwd_layout(const Seqs& s, int h, int hkv, int cmp_kernel = 0, int cmp_stride = 0, int window = 0,
+                     int S = 0) {
   BwdLayout l{};
   const int Lmax = s.max_len;
   l.n_chunks = (Lmax + kChunk - 1) / kChunk;
@@ -576,7 +465,11 @@ BwdLayout bwd_layout(const Seqs& s, int h, int hkv, int cmp_kernel = 0, int cmp_
   auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
   l.dsum = 0;
   l.part = a256((size_t)s.tokens * h * 4);
-  l.total = a256(l.part + (size_t)s.n_seqs * hkv * l.items_per_bg * 2 * kBS * kD * 4);
+  l.inv_list = a256(l.part + (size_t)s.n_seqs * hkv * l.items_per_bg * 2 * kBS * kD * 4);
+  const bool inv = !cmp_kernel && !window && S > 0 && dkv_tc_shape(h / hkv, false, l.nb);
+  const size_t lists = inv ? (size_t)s.n_seqs * hkv * l.n_chunks : 0;
+  l.inv_tab = a256(l.inv_list + lists * kChunk * S * 4);
+  l.total = a256(l.inv_tab + lists * l.nb * 8);
   return l;
 }
 
@@ -584,6 +477,8 @@ cudaError_t run_bwd(const BwdParams& p0, const BwdLayout& l, void* workspace, cu
   BwdParams p = p0;
   p.dsum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.dsum);
   p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + l.part);
+  p.inv_list = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + l.inv_list);
+  p.inv_tab = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + l.inv_tab);
   p.r = p.h / p.hkv;
   p.scale_log2 = p.scale * kLog2e;
   p.n_chunks = l.n_chunks;
@@ -599,11 +494,16 @@ cudaError_t run_bwd(const BwdParams& p0, const BwdLayout& l, void* workspace, cu
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t items = (int64_t)s.n_seqs * p.hkv * l.items_per_bg;
   if (items > 0) {
-    constexpr int kv_bytes = dkv_smem_bytes<NS_KV>();
-    e = cudaFuncSetAttribute(sparse_bwd_dkv<NS_KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
-    if (e != cudaSuccess) return e;
-    sparse_bwd_dkv<NS_KV><<<(unsigned)items, 128, kv_bytes, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (dkv_tc_supported(p)) {  // group sizes 8 and 16: the tensor-core kernel
+      if (!p.cmp_kernel && !p.window && (e = launch_invert(p, st)) != cudaSuccess) return e;
+      if ((e = launch_dkv_tc(p, items, s.tokens * p.h, st)) != cudaSuccess) return e;
+    } else {
+      constexpr int kv_bytes = dkv_smem_bytes<NS_KV>();
+      e = cudaFuncSetAttribute(sparse_bwd_dkv<NS_KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_bytes);
+      if (e != cudaSuccess) return e;
+      sparse_bwd_dkv<NS_KV><<<(unsigned)items, 128, kv_bytes, st>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     sparse_bwd_reduce<<<(unsigned)((int64_t)s.n_seqs * p.hkv * l.nb), 256, 0, st>>>(p);
   }
   return cudaGetLastError();
@@ -742,9 +642,9 @@ cudaError_t launch_gate_bwd(int64_t rows, int d, const void* dout, const void* o
   return cudaGetLastError();
 }
 
-size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv) {
+size_t sparse_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int S) {
   if (s.tokens == 0 || s.max_len == 0) return 0;
-  return bwd_layout(s, h, hkv).total;
+  return bwd_layout(s, h, hkv, 0, 0, 0, S).total;
 }
 
 size_t cmp_attn_bwd_workspace_bytes(const Seqs& s, int h, int hkv, int kernel, int stride) {
@@ -778,7 +678,7 @@ cudaError_t launch_sparse_bwd(const Seqs& s, const void* q, const void* k, const
   BwdParams p = bwd_params(s, q, k, v, h, hkv, scale, o, lse, dout, dq, dk, dv);
   p.idx = idx;
   p.S = S;
-  return run_bwd(p, bwd_layout(s, h, hkv), workspace, st);
+  return run_bwd(p, bwd_layout(s, h, hkv, 0, 0, 0, S), workspace, st);
 }
 
 cudaError_t launch_cmp_attn_bwd(const Seqs& s, const void* q, const void* k_cmp, const void* v_cmp, int h, int hkv,

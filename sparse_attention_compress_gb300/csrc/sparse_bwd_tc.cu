@@ -1,0 +1,651 @@
+// dK and dV of selected-block attention (and of the compressed and sliding-window branches,
+// the same kernel in their key spaces) on the fifth-generation tensor cores.
+//
+// The derivative is the one sparse_bwd.cu states ([TileLang-NSA] "TileLang operator
+// development: Native Sparse Attention", sec. 2 for the forward; [NSA-Triton] "DeepSeek
+// NSA ... with Triton", sec. 4 for training with it): per (token, head) row that reaches
+// key e, p = exp(scale q.k_e - lse), ds = p (dO.v_e - D), dk[e] += scale ds q,
+// dv[e] += p dO.
+//
+// GB300 design.  A work item is (sequence, kv-head, key block j, query chunk), as for
+// sparse_bwd_dkv, and writes the same fp32 partials, so sparse_bwd_reduce sums them.
+// The rows that reach block j are gathered 128 at a time (128 / r tokens of r heads):
+//   S = Q K_j^T and dP = dO V_j^T      M = 128 rows, N = 64 keys, K = d   (TMEM)
+//   P, dS from S, dP, lse, D            softmax warps, one row per thread
+//   dV^T += dO^T P,  dK^T += Q^T dS     M = 128 (d), N = 64 keys, K = 128 rows (TMEM)
+// The same shared-memory tile of Q (or dO) is the K-major A operand of the first
+// product and the MN-major A operand of the second, so no transpose is made.  P and dS
+// enter the second products as bf16 pairs (the rounded value and its remainder, so the
+// operand carries about 16 bits), as in sparse_bwd_dkv.  Roles: warp 8 takes the tokens
+// that reach j and gathers their Q and dO rows by TMA into a two-stage ring; warp 9
+// issues the MMAs (S and dP into one of two TMEM buffers, so the next tile's products run
+// while the softmax warps work on this one); warps 0-7, two per scheduler, form P and dS
+// (each a half of every row's 64 keys) and finally read dK^T and dV^T out of TMEM.  One
+// CTA per SM (224 KB of shared memory).
+#include <algorithm>
+
+#include "sm100.cuh"
+#include "sparse_bwd.cuh"
+#include "topk.cuh"
+
+namespace nsa {
+namespace bwd {
+
+namespace {
+
+constexpr int kSoftWarps = 8;  // two per scheduler: warp w takes rows 32 (w % 4) .. and key half w / 4
+constexpr int kSoft = kSoftWarps * 32;
+constexpr int kProducer = kSoftWarps, kIssuer = kSoftWarps + 1;  // warp roles
+constexpr int kThreads = kSoft + 64;
+constexpr int kTileRows = 128;                   // gathered (token, head) rows per tile
+constexpr int kKVBytes = kBS * kD * 2;           // K_j or V_j: two 64-column halves of 64 rows
+constexpr int kHalfRows = kTileRows * 128;       // one 64-column half of a 128-row tile
+constexpr int kQBytes = 2 * kHalfRows;           // Q (or dO) of one tile
+constexpr int kStageBytes = 2 * kQBytes;         // Q and dO
+constexpr int kPBytes = kTileRows * kBS * 2;     // P or dS (hi or lo) of one tile: 128 rows x 64 keys
+constexpr int kSmemBytes = 2 * kKVBytes + 2 * kStageBytes + 4 * kPBytes + 1024;  // + base alignment
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: S and dP of tile buffer b at 128 b and 128 b + 64; then dV^T and dK^T in
+// two parts each, the products of the bf16-rounded P / dS and of their remainders (four
+// independent accumulation chains; the epilogue adds the parts)
+constexpr uint32_t kColDV = 256, kColDK = 320, kColDVlo = 384, kColDKlo = 448;
+// P or dS values above these make the remainder products count (as in sparse_bwd_dkv)
+constexpr float kLoP = 0.00390625f, kLoS = 0.0625f;
+
+enum : int {
+  B_FULL = 0,    // [2] a stage's Q, dO and token list landed
+  B_EMPTY = 2,   // [2] the MMAs reading a stage are done
+  B_KV = 4,      // K_j and V_j are in shared memory
+  B_SFULL = 5,   // [2] S and dP of a tile buffer computed
+  B_SFREE = 7,   // [2] the softmax warps have read a tile buffer
+  B_PFULL = 9,   // P and dS of a tile are in shared memory
+  B_PFREE = 10,  // the dV / dK products of that tile are done
+  B_ADONE = 11,  // every product of the item is done
+  B_DRAIN = 12,
+  B_COUNT = 13
+};
+
+// Shared-memory descriptor of an MN-major tile with 128-byte swizzling: rows of 64
+// MN-elements (128 B) along K, 1024-byte atoms of 8 K-rows.  lbo: byte distance between
+// groups of 64 MN-elements; sbo: between groups of 8 K-rows.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+// bf16 x bf16 -> fp32 with both operands MN-major
+constexpr uint32_t idesc_mn(int M, int N) { return tc::idesc(M, N) | (1u << 15) | (1u << 16); }
+
+// Item slot in the numbering of item_to_block (the order sparse_bwd_reduce reads).
+__device__ __forceinline__ int slot_of(const BwdParams& p, int j, int c) {
+  if (p.window) return j;
+  if (p.cmp_kernel) {
+    int s = 0;
+    for (int jj = 0; jj < j; ++jj) s += p.n_chunks - first_query(p, jj) / kChunk;
+    return s + c - first_query(p, j) / kChunk;
+  }
+  const int m = j / kGroup;
+  int s = 0;
+  for (int mm = 0; mm < m; ++mm) s += min(kGroup, p.nb - mm * kGroup) * (p.n_chunks - mm);
+  return s + (j - m * kGroup) * (p.n_chunks - m) + (c - m);
+}
+
+// CTA x -> (sequence and kv-head bg, key block j, query chunk c).  Selected blocks: every
+// block-0 item first (each token's list holds block 0, so these items are the longest),
+// then per (sequence, kv-head) the chunks in order and, within a chunk, the blocks it
+// reaches in order, so that the CTAs running together share their chunk's Q and dO in L2.
+// Compressed keys: per (sequence, kv-head), chunk-major the same way.  Window: one item
+// per block.
+__device__ __forceinline__ void dispatch(const BwdParams& p, int x, int& bg, int& j, int& c) {
+  const int n_bg = p.seqs.n_seqs * p.hkv;
+  if (p.window) {
+    bg = x / p.nb;
+    j = x % p.nb;
+    c = 0;
+    return;
+  }
+  if (!p.cmp_kernel) {
+    const int head = n_bg * p.n_chunks;
+    if (x < head) {
+      bg = x / p.n_chunks;
+      j = 0;
+      c = x % p.n_chunks;
+      return;
+    }
+    x -= head;
+    const int per = p.items_per_bg - p.n_chunks;
+    bg = x / per;
+    int rem = x % per;
+    for (c = 0; c < p.n_chunks; ++c) {
+      const int nbc = min(p.nb, (c + 1) * kGroup) - 1;  // blocks 1 .. reached by chunk c
+      if (rem < nbc) {
+        j = rem + 1;
+        return;
+      }
+      rem -= nbc;
+    }
+    j = p.nb;  // not reached
+    return;
+  }
+  bg = x / p.items_per_bg;
+  int rem = x % p.items_per_bg;
+  const int span = p.cmp_stride * kBS;  // tokens per compressed key block
+  for (c = 0; c < p.n_chunks; ++c) {
+    // blocks whose first reaching query lies in chunk c or before
+    const int lim = (c + 1) * kChunk - p.cmp_kernel + 1;
+    const int nbc = min(p.nb, lim > 0 ? (lim + span - 1) / span : 0);
+    if (rem < nbc) {
+      j = rem;
+      return;
+    }
+    rem -= nbc;
+  }
+  j = p.nb;  // not reached
+}
+
+// Whether query t reaches key block j in the compressed-key and window key spaces (the
+// selected blocks' lists are inverted by invert_kernel instead).
+__device__ __forceinline__ int token_mult(const BwdParams& p, int t, int j, int Lk) {
+  if (p.window) return key_lo(p, t) <= j * kBS + kBS - 1;  // t >= j * kBS here
+  return key_bound(p, t, Lk) >= j * kBS;
+}
+
+// Chunk-wise inverted lists of the selected blocks.  Block (chunk c, sequence and kv-head
+// bg): the tokens t of the chunk whose list holds a block j with 64 j <= t (the entries
+// that reach a key), grouped by j.  Eight warps own 256 consecutive tokens each; pass 1
+// counts (warp, block) pairs, a prefix over the blocks and warps places each warp's run
+// inside each block's bucket, and pass 2 writes the tokens in warp, token and list-entry
+// order (ranks within a warp from __match_any_sync), so the lists, and the dK / dV sums
+// over them, are the same on every run.  Shared memory: 8 x min(nb, (c + 1) * kGroup) ints.
+__global__ void __launch_bounds__(256) invert_kernel(const BwdParams p) {
+  extern __shared__ int s_cnt[];  // [8][nbr]
+  __shared__ int s_tot[8];
+  const int c = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.hkv, g = bg % p.hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = seq_len(p.seqs, b);
+  const int nbr = min(p.nb, (c + 1) * kGroup);  // blocks a query of chunk c can reach
+  const size_t seg = (size_t)bg * p.n_chunks + c;
+  int2* tab = p.inv_tab + seg * p.nb;
+  for (int jj = nbr + tid; jj < p.nb; jj += 256) tab[jj] = make_int2(0, 0);
+  const int t0 = c * kChunk, t1 = min(L, t0 + kChunk);
+  for (int i = tid; i < 8 * nbr; i += 256) s_cnt[i] = 0;
+  __syncthreads();
+  const int64_t base = seq_start(p.seqs, b);
+  const int wt0 = t0 + warp * (kChunk / 8), wt1 = min(t1, wt0 + kChunk / 8);
+  auto entry = [&](int t, int e) -> int {  // block of list entry e of token t, or -1
+    const int jj = __ldg(p.idx + ((base + t) * p.hkv + g) * p.S + e);
+    return (jj >= 0 && jj < nbr && jj * kBS <= t) ? jj : -1;
+  };
+  for (int tb = wt0; tb < wt1; tb += 32) {
+    const int t = tb + lane;
+    if (t < wt1)
+      for (int e = 0; e < p.S; ++e) {
+        const int jj = entry(t, e);
+        if (jj >= 0) atomicAdd(&s_cnt[warp * nbr + jj], 1);
+      }
+  }
+  __syncthreads();
+  // bucket offsets: blocks 4 tid .. 4 tid + 3 per thread (nbr <= 1024)
+  int tot[4], sum = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int jj = 4 * tid + u;
+    tot[u] = 0;
+    if (jj < nbr)
+      for (int w = 0; w < 8; ++w) tot[u] += s_cnt[w * nbr + jj];
+    sum += tot[u];
+  }
+  int off = block_excl_scan<8>(sum, s_tot, lane, warp);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int jj = 4 * tid + u;
+    if (jj < nbr) {
+      tab[jj] = make_int2(off, tot[u]);
+      int run = off;
+      for (int w = 0; w < 8; ++w) {
+        const int x = s_cnt[w * nbr + jj];
+        s_cnt[w * nbr + jj] = run;
+        run += x;
+      }
+    }
+    off += tot[u];
+  }
+  __syncthreads();
+  int32_t* list = p.inv_list + seg * kChunk * p.S;
+  for (int tb = wt0; tb < wt1; tb += 32) {
+    const int t = tb + lane;
+    for (int e = 0; e < p.S; ++e) {
+      const int jj = t < wt1 ? entry(t, e) : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, jj);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      if (jj >= 0) list[s_cnt[warp * nbr + jj] + rank] = t;
+      __syncwarp();
+      if (jj >= 0 && rank == 0) s_cnt[warp * nbr + jj] += __popc(same);
+      __syncwarp();
+    }
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[4]) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  constexpr int TPT = kTileRows / R;  // tokens per tile
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t s_bar[B_COUNT];
+  __shared__ int s_meta[2][TPT + 2];  // per stage: (token << 7 | multiplicity) per slot, count, last
+  __shared__ int s_need[kSoftWarps];  // per softmax warp, for the tile in the P buffer: remainder products needed
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int bg, j, c;
+  dispatch(p, blockIdx.x, bg, j, c);
+  const int b = bg / p.hkv, g = bg % p.hkv;
+  const int L = seq_len(p.seqs, b);
+  const int Lk = key_len(p, L);
+  const int m = p.window ? 0 : (p.cmp_kernel ? first_query(p, j) / kChunk : j / kGroup);
+  if (j >= p.nb || j * kBS >= Lk || (c > m && c * kChunk >= L)) return;  // no partial is read for this item
+  const int slot_item = slot_of(p, j, c);
+  const int64_t base = seq_start(p.seqs, b);
+  const int64_t kbase = key_base(p, b);
+  const int t_begin = p.window ? j * kBS : max(first_query(p, j), c * kChunk);
+  const int t_end = p.window ? min(j * kBS + kBS - 1 + p.window, L) : min((c + 1) * kChunk, L);
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023) & ~1023u;
+  const uint32_t kt = sbase, vt = kt + kKVBytes;
+  const uint32_t stage0 = vt + kKVBytes;
+  const uint32_t p_hi = stage0 + 2 * kStageBytes, p_lo = p_hi + kPBytes, s_hi = p_lo + kPBytes, s_lo = s_hi + kPBytes;
+  auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
+  volatile int* abort = &s_abort;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bar(B_FULL + i), 1);
+      tc::mbar_init(bar(B_EMPTY + i), 1);
+      tc::mbar_init(bar(B_SFULL + i), 1);
+      tc::mbar_init(bar(B_SFREE + i), kSoft);
+    }
+    tc::mbar_init(bar(B_KV), kSoft);
+    tc::mbar_init(bar(B_PFULL), kSoft);
+    tc::mbar_init(bar(B_PFREE), 1);
+    tc::mbar_init(bar(B_ADONE), 1);
+    tc::mbar_init(bar(B_DRAIN), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == kIssuer) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    tc::fence_before();
+  }
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = s_tmem;
+
+  int n_tiles = 0;      // producer: tiles handed to the ring
+  int last_full[2] = {-1, -1};  // producer: last tile with rows in each stage
+  if (warp == kProducer) {
+    // ------------------------------------------------------------------ token scan + TMA
+    int slot = 0, last_tok = -1;
+    bool ok = true;
+    auto begin_tile = [&]() -> bool {  // the stage of tile n_tiles is free (warp-uniform)
+      if (n_tiles < 2) return true;
+      return tc::warp_wait(bar(B_EMPTY + (n_tiles & 1)), ((n_tiles - 2) >> 1) & 1, abort);
+    };
+    auto put = [&](int t, int mult) {  // lane 0: one token's Q and dO rows into slot `slot`
+      const int s = n_tiles & 1;
+      const uint32_t qs = stage0 + s * kStageBytes + slot * R * 128, ds = qs + kQBytes;
+      const int y = (int)((base + t) * p.h + g * R);
+      const uint32_t fb = bar(B_FULL + s);
+      tc::tma2d(qs, &tm_q, 0, y, fb);
+      tc::tma2d(qs + kHalfRows, &tm_q, 64, y, fb);
+      tc::tma2d(ds, &tm_do, 0, y, fb);
+      tc::tma2d(ds + kHalfRows, &tm_do, 64, y, fb);
+      s_meta[s][slot] = (t << 7) | mult;
+    };
+    auto end_tile = [&](int cnt, int last) {  // lane 0: the token list, then the arrival
+      const int s = n_tiles & 1;
+      s_meta[s][TPT] = cnt;
+      s_meta[s][TPT + 1] = last;
+      tc::mbar_expect_tx(bar(B_FULL + s), cnt > 0 ? (uint32_t)kStageBytes : 0u);
+    };
+    // hand 32 candidate tokens (t, mult; mult 0: not gathered) to the tiles, in lane order
+    auto take = [&](int t, int mult) {
+      unsigned bal = __ballot_sync(0xffffffffu, mult > 0);
+      while (bal) {
+        const int src = __ffs(bal) - 1;
+        bal &= bal - 1;
+        const int tt = __shfl_sync(0xffffffffu, t, src), mm = __shfl_sync(0xffffffffu, mult, src);
+        if (slot == 0 && !(ok = begin_tile())) return;
+        if (lane == 0) put(tt, mm);
+        last_tok = tt;
+        if (++slot == TPT) {
+          if (lane == 0) end_tile(TPT, 0);
+          last_full[n_tiles & 1] = n_tiles;
+          ++n_tiles;
+          slot = 0;
+        }
+      }
+    };
+    if (!p.cmp_kernel && !p.window) {
+      // selected blocks: the tokens of the chunk that list j, from the inverted lists (a
+      // token listing j twice appears twice)
+      const size_t seg = (size_t)bg * p.n_chunks + c;
+      const int2 bk = p.inv_tab[seg * p.nb + j];
+      const int32_t* lst = p.inv_list + seg * kChunk * p.S + bk.x;
+      for (int k0 = 0; ok && k0 < bk.y; k0 += 32) {
+        const int k = k0 + lane;
+        take(k < bk.y ? __ldg(lst + k) : 0, k < bk.y ? 1 : 0);
+      }
+    } else {
+      // compressed keys and window: every query of the range reaching j, by arithmetic
+      for (int t0 = t_begin; ok && t0 < t_end; t0 += 32) {
+        const int t = t0 + lane;
+        take(t, t < t_end ? token_mult(p, t, j, Lk) : 0);
+      }
+    }
+    if (ok) {
+      if (slot > 0) {  // the last tile: empty slots repeat a gathered token with multiplicity 0
+        for (; slot < TPT; ++slot)
+          if (lane == 0) put(last_tok, 0);
+        if (lane == 0) end_tile(TPT, 1);
+        last_full[n_tiles & 1] = n_tiles;
+        ++n_tiles;
+      } else if (begin_tile()) {  // the list ended on a tile boundary (or is empty): a marker tile
+        if (lane == 0) end_tile(0, 1);
+        ++n_tiles;
+      }
+    }
+    __syncwarp();
+  }
+
+  int pn = 0;  // MMA warp and softmax warps: tiles whose P and dS went through the P buffer
+  bool adone = false;  // MMA warp: the item's last commit was issued
+  if (warp == kIssuer) {
+    // ------------------------------------------------------------------ MMA issuer
+    // A polling loop (lane 0 probes, the warp follows): the dV / dK products of the oldest
+    // tile whose P and dS are written go first, since they release its stage to the
+    // producer; otherwise S and dP of the next loaded tile once its TMEM buffer is free.
+    // Waits are bounded: without progress for the unit's limit the item gives up.
+    bool ok = tc::warp_wait(bar(B_KV), 0, abort);
+    int next_s = 0;        // next tile for S and dP
+    int n_rows_tiles = 0;  // tiles with rows whose S and dP were issued
+    bool s_done = false;   // the last tile was seen
+    bool lo_init = false;  // the remainder accumulators hold a first product
+    unsigned long long t_idle = tc::globaltimer();
+    const unsigned long long lim = tc::wait_limit();
+    while (ok) {
+      int act = 0;  // 1: dV / dK of tile pn; 2: S and dP of tile next_s
+      if (lane == 0) {
+        if (pn < n_rows_tiles && tc::mbar_test(bar(B_PFULL), pn & 1)) {
+          act = 1;
+        } else if (!s_done && tc::mbar_test(bar(B_FULL + (next_s & 1)), (next_s >> 1) & 1) &&
+                   (next_s < 2 || tc::mbar_test(bar(B_SFREE + (next_s & 1)), ((next_s - 2) >> 1) & 1))) {
+          act = 2;
+        }
+      }
+      act = __shfl_sync(0xffffffffu, act, 0);
+      if (act == 1) {
+        const int u = pn;  // P tiles are the row tiles, in order
+        if (lane == 0) {  // lane 0 observed the P buffer's arrival: it reads the warps' flags
+          int lo = 3;
+          if (lo_init) {
+            lo = 0;
+#pragma unroll
+            for (int w = 0; w < kSoftWarps; ++w) lo |= s_need[w];
+          }
+          tc::fence_after();
+          const uint32_t qs = stage0 + (u & 1) * kStageBytes, ds = qs + kQBytes;
+          constexpr uint32_t id = idesc_mn(128, kBS);
+#pragma unroll 1
+          for (int k = 0; k < kTileRows / 16; ++k) {
+            const uint32_t ro = k * 2048;
+            const uint32_t acc_hi = (u > 0 || k > 0) ? 1u : 0u, acc_lo = (lo_init || k > 0) ? 1u : 0u;
+            const uint64_t a_do = sdesc_mn(ds + ro, kHalfRows, 1024), a_q = sdesc_mn(qs + ro, kHalfRows, 1024);
+            tc::mma_ss(tmem + kColDV, a_do, sdesc_mn(p_hi + ro, 1024, 1024), id, acc_hi);
+            tc::mma_ss(tmem + kColDK, a_q, sdesc_mn(s_hi + ro, 1024, 1024), id, acc_hi);
+            if (lo & 1) tc::mma_ss(tmem + kColDVlo, a_do, sdesc_mn(p_lo + ro, 1024, 1024), id, acc_lo);
+            if (lo & 2) tc::mma_ss(tmem + kColDKlo, a_q, sdesc_mn(s_lo + ro, 1024, 1024), id, acc_lo);
+          }
+          tc::commit(bar(B_PFREE));
+          tc::commit(bar(B_EMPTY + (u & 1)));
+        }
+        __syncwarp();
+        lo_init = true;
+        ++pn;
+        t_idle = tc::globaltimer();
+      } else if (act == 2) {
+        const int s = next_s & 1;
+        int cnt = 0, last = 0;  // lane 0 observed the stage's arrival: it reads the list's header
+        if (lane == 0) {
+          cnt = s_meta[s][TPT];
+          last = s_meta[s][TPT + 1];
+        }
+        cnt = __shfl_sync(0xffffffffu, cnt, 0);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (cnt > 0) {
+          if (lane == 0) {
+            tc::fence_after();
+            const uint32_t qs = stage0 + s * kStageBytes, ds = qs + kQBytes;
+            constexpr uint32_t id = tc::idesc(128, kBS);
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+              const uint32_t ao = (k >> 2) * kHalfRows + (k & 3) * 32, bo = (k >> 2) * (kKVBytes / 2) + (k & 3) * 32;
+              tc::mma_ss(tmem + s * 128, tc::sdesc(qs + ao), tc::sdesc(kt + bo), id, k > 0);
+              tc::mma_ss(tmem + s * 128 + 64, tc::sdesc(ds + ao), tc::sdesc(vt + bo), id, k > 0);
+            }
+            tc::commit(bar(B_SFULL + s));
+          }
+          __syncwarp();
+          ++n_rows_tiles;
+        }
+        s_done = last != 0;
+        ++next_s;
+        t_idle = tc::globaltimer();
+      } else {
+        if (s_done && pn == n_rows_tiles) {  // every product is issued
+          if (lane == 0) tc::commit(bar(B_ADONE));
+          __syncwarp();
+          adone = true;
+          break;
+        }
+        if (*abort) {
+          ok = false;
+        } else if (tc::globaltimer() - t_idle >= lim) {
+          *abort = 1;
+          atomicExch(&g_device_status, (int)NSA_ERR_TIMEOUT);
+          ok = false;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        __nanosleep(32);  // leave the issue slots to the softmax warp on this scheduler
+      }
+    }
+  }
+  if (warp < kSoftWarps) {
+    // ------------------------------------------------------------------ softmax warps
+    // K_j and V_j, bounds-checked (rows past the sequence's keys read as zeros; no query
+    // reaches them), in the K-major layout of the S and dP products; the async-proxy fence
+    // makes these generic-proxy writes visible to the MMAs
+    {
+      const int64_t rs = (int64_t)p.hkv * kD;
+      const __nv_bfloat16* kb = p.k + ((kbase + (int64_t)j * kBS) * p.hkv + g) * kD;
+      const __nv_bfloat16* vb = p.v + ((kbase + (int64_t)j * kBS) * p.hkv + g) * kD;
+      for (int e = tid; e < 2 * kBS * (kD / 8); e += kSoft) {
+        const int which = e / (kBS * (kD / 8)), r = (e / (kD / 8)) % kBS, ch = e % (kD / 8);
+        const bool in = j * kBS + r < Lk;
+        const __nv_bfloat16* src = (which ? vb : kb) + r * rs + ch * 8;
+        const uint32_t dst = (which ? vt : kt) + (ch >> 3) * (kKVBytes / 2) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        cp_async16(dst, in ? (const void*)src : (const void*)p.k, in ? 16 : 0);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc::mbar_arrive(bar(B_KV));
+    }
+    // TMEM lanes 32 (warp % 4) .. are this warp's rows; kh: its half of the 64 keys
+    const int row = (warp & 3) * 32 + lane, kh = warp >> 2, slot = row / R, hd = row % R;
+    const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      const int s = i & 1;
+      if (!(ok = tc::warp_wait(bar(B_FULL + s), (i >> 1) & 1, abort))) break;
+      const int cnt = s_meta[s][TPT], last = s_meta[s][TPT + 1];
+      if (cnt == 0) break;  // the marker that ends the list
+      const int info = s_meta[s][slot];
+      const int t = info >> 7, mult = info & 127;
+      float lse2 = __builtin_inff(), dsum = 0.f;
+      if (mult > 0) {
+        const int64_t rg = (base + t) * p.h + (int64_t)g * R + hd;
+        lse2 = lse_to_log2(p.lse[rg]);
+        dsum = p.dsum[rg];
+      }
+      const int tb = key_bound(p, t, Lk), tl = key_lo(p, t);
+      if (!(ok = tc::warp_wait(bar(B_SFULL + s), (i >> 1) & 1, abort))) break;
+      tc::fence_after();
+      float sv[32], dpv[32];
+      tc::tmem_ld32_nowait(t_lane + s * 128 + kh * 32, sv);
+      tc::tmem_ld32_nowait(t_lane + s * 128 + 64 + kh * 32, dpv);
+      tc::tmem_wait_ld();
+      tc::fence_before();
+      tc::mbar_arrive(bar(B_SFREE + s));
+      // the P buffer is free once the previous tile's dV / dK products are done
+      if (pn > 0 && !(ok = tc::warp_wait(bar(B_PFREE), (pn - 1) & 1, abort))) break;
+      const float fm = (float)mult;
+      float pmax = 0.f, smax = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {  // keys 8 c8 .. 8 c8 + 7 (one 16-byte chunk), c8 = 4 kh + cc
+        const int c8 = kh * 4 + cc;
+        uint32_t ph[4], pl[4], sh[4], sl[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int k0 = j * kBS + c8 * 8 + e;
+          const float p0 = k0 <= tb && k0 >= tl ? fm * ex2(sv[cc * 8 + e] * p.scale_log2 - lse2) : 0.f;
+          const float p1 = k0 + 1 <= tb && k0 + 1 >= tl ? fm * ex2(sv[cc * 8 + e + 1] * p.scale_log2 - lse2) : 0.f;
+          const float d0 = p0 * (dpv[cc * 8 + e] - dsum), d1 = p1 * (dpv[cc * 8 + e + 1] - dsum);
+          pmax = fmaxf(pmax, fmaxf(p0, p1));
+          smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
+          split_bf16x2(p0, p1, ph[e / 2], pl[e / 2]);
+          split_bf16x2(d0, d1, sh[e / 2], sl[e / 2]);
+        }
+        const uint32_t off = row * 128 + ((c8 ^ (row & 7)) << 4);
+        st_shared_v4(p_hi + off, ph);
+        st_shared_v4(p_lo + off, pl);
+        st_shared_v4(s_hi + off, sh);
+        st_shared_v4(s_lo + off, sl);
+      }
+      {  // which remainder products this warp's rows need (read by the MMA warp after PFULL)
+        const unsigned bp = __ballot_sync(0xffffffffu, pmax > kLoP), bs = __ballot_sync(0xffffffffu, smax > kLoS);
+        if (lane == 0) s_need[warp] = (bp ? 1 : 0) | (bs ? 2 : 0);
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc::mbar_arrive(bar(B_PFULL));
+      ++pn;
+      if (last) break;
+    }
+    // ------------------------------------------------------------------ epilogue
+    // TMEM lane = d: row d of dK^T and dV^T holds the 64 keys' values of column d; this
+    // thread writes keys 32 kh .. 32 kh + 31
+    float* out = p.part + ((size_t)bg * p.items_per_bg + slot_item) * 2 * kBS * kD;
+    if (ok && pn > 0) ok = tc::warp_wait(bar(B_ADONE), 0, abort);
+    if (ok) {
+      tc::fence_after();
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        {
+          const int cc = kh * 32;
+          float v[32];
+          if (pn > 0) {
+            float w[32];
+            tc::tmem_ld32_nowait(t_lane + (which ? kColDV : kColDK) + cc, v);
+            tc::tmem_ld32_nowait(t_lane + (which ? kColDVlo : kColDKlo) + cc, w);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] += w[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          }
+          float* o = out + (size_t)which * kBS * kD + (size_t)cc * kD + row;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[(size_t)e * kD] = v[e];
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort) {
+    // copies and tensor-core work still in flight land before the CTA leaves
+    if (warp == kProducer) {
+      for (int s = 0; s < 2; ++s) {
+        const int i = n_tiles - 1 - ((n_tiles - 1 - s) & 1);  // last tile handed to stage s
+        if (i >= 0 && (i & 1) == s) tc::warp_drain(bar(B_FULL + s), (i >> 1) & 1);
+      }
+    } else if (warp == kIssuer) {
+      if (lane == 0) tc::commit(bar(B_DRAIN));
+      __syncwarp();
+      tc::warp_drain(bar(B_DRAIN), 0);
+    }
+  } else if (warp == kProducer) {
+    // the MMA warp's last release of each stage lands before the CTA leaves
+    for (int s = 0; s < 2; ++s)
+      if (last_full[s] >= 0) tc::warp_drain(bar(B_EMPTY + s), (last_full[s] >> 1) & 1);
+  } else if (warp == kIssuer) {
+    if (pn > 0) tc::warp_drain(bar(B_PFREE), (pn - 1) & 1);
+    if (adone) tc::warp_drain(bar(B_ADONE), 0);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == kIssuer)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_invert(const BwdParams& p, cudaStream_t st) {
+  const int n_bg = p.seqs.n_seqs * p.hkv;
+  if (n_bg == 0 || p.n_chunks == 0) return cudaSuccess;
+  const int smem = 8 * std::min(p.nb, p.n_chunks * kGroup) * 4;
+  cudaError_t e = cudaFuncSetAttribute(invert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  invert_kernel<<<dim3(p.n_chunks, n_bg), 256, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// The inverted lists take up to 1024 key blocks per chunk (4 per thread of invert_kernel).
+bool dkv_tc_supported(const BwdParams& p) { return dkv_tc_shape(p.h / p.hkv, p.cmp_kernel || p.window, p.nb); }
+
+// q_rows: rows of q and dout ([tokens, h, d]), the extent of their tensor maps.
+cudaError_t launch_dkv_tc(const BwdParams& p, int64_t items, int64_t q_rows, cudaStream_t st) {
+  if (items <= 0) return cudaSuccess;
+  const int r = p.h / p.hkv;
+  CUtensorMap mq, mdo;
+  const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)q_rows};
+  const uint64_t strides[1] = {(uint64_t)kD * 2};
+  const uint32_t box[2] = {64, (uint32_t)r};
+  if (!tc::make_map(&mq, p.q, 2, dims, strides, box) || !tc::make_map(&mdo, p.dout, 2, dims, strides, box))
+    return cudaErrorInvalidValue;
+  auto kern = r == 16 ? dkv_tc_kernel<16> : dkv_tc_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)items, kThreads, kSmemBytes, st>>>(mq, mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+NSA_STATUS_ACCESSOR(sparse_bwd_tc)
+
+}  // namespace nsa

@@ -118,7 +118,12 @@ def test_sparse_bwd_workspace_size(B, T, h, hkv):
     got = nsa.nsa_sparse_bwd_workspace_size(s, 16)
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     dsum = a256(B * T * h * 4)
-    want = a256(dsum + B * hkv * _items_per_seq_head(T) * 2 * 64 * 128 * 4)
+    part = a256(dsum + B * hkv * _items_per_seq_head(T) * 2 * 64 * 128 * 4)
+    # group sizes 8 and 16 (the tensor-core dK/dV kernel): chunk-wise inverted lists, 2048 * S
+    # token slots and an (offset, count) pair per key block for each (sequence, kv-head, chunk)
+    lists = B * hkv * -(-T // 2048) if h // hkv in (8, 16) else 0
+    nb = -(-T // 64)
+    want = a256(a256(part + lists * 2048 * 16 * 4) + lists * nb * 8)
     assert got == want
 
 
