@@ -251,11 +251,12 @@ def bench_decode(torch, nsa, device, steps, warmup, flush, peaks):
                                "bytes": int(cbytes)}}
 
 
-def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks):
+def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks, batch=8):
     """Backward of the selected branch on the prefill workload: dq, dk, dv from the
-    forward's o and lse and a seeded upstream gradient."""
+    forward's o and lse and a seeded upstream gradient (batch 8 is the workload; smaller
+    batches for profiler captures)."""
     from sparse_attention_compress_gb300 import _lib
-    w = gen.prefill()
+    w = gen.prefill(B=batch)
     q = dev(torch, w.q, device).view(w.batch, w.seqlen, w.h, w.d)
     k, v, idx = dev(torch, w.k, device), dev(torch, w.v, device), dev(torch, w.idx, device)
     do = dev(torch, gen.normal(gen.rng_for(1, 99), (w.tokens, w.h, w.d), "bf16"), device)
@@ -272,7 +273,7 @@ def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks):
     # five products per attended (row, key) pair: S and dP recomputed, dQ, dK, dV
     flops = prefill_flops(w) * 10 / 4
     tf = flops / (ms_step * 1e-3) / 1e12
-    return {"workload": "backward of selected attention, prefill B=8 T=16384 H=16 Hkv=1 d=128 bf16, block 64, "
+    return {"workload": f"backward of selected attention, prefill B={batch} T=16384 H=16 Hkv=1 d=128 bf16, block 64, "
                         "S=16", "ms_per_step": ms_step, "tflops": tf, "flops_per_step": flops,
             "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "workspace_bytes": int(ws.numel()),
             "launches_per_step": 3}
@@ -606,7 +607,8 @@ def main():
               "swa_bwd": lambda: bench_swa_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
-              "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks,
+                                                       batch=args.batch),
               "decode": lambda: bench_decode(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "decode_offload": lambda: bench_decode_offload(torch, nsa, device, args.steps, args.warmup, flush),
               "selection": lambda: bench_selection(torch, nsa, device, args.steps, args.warmup, flush, peaks),

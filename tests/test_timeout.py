@@ -1,7 +1,8 @@
 """Bounded waits that run out, on purpose, without breaking any kernel.
 
 The kernels that wait (the tensor-core branches and the TMA-fed selected attention of the
-layer, the decode step's wait for a row's block list) bound every first-level wait.  Here
+layer, the decode step's wait for a row's block list, the tensor-core dK / dV of the
+backward) bound every first-level wait.  Here
 that limit is set to 1 ns through the C ABI (nsa_set_wait_limit_ns), far below any wait's
 normal length; nothing else changes: no copy is withheld, no barrier left unarrived.  The
 waits give up, the kernels set the device status word to NSA_ERR_TIMEOUT, drain the copies
@@ -103,3 +104,32 @@ def test_layer_wait_runs_out_then_recovers(clean_status):
     assert nsa.nsa_device_status() == 0
     ref = orc.layer(w.q, w.k, w.v, w.gates, w.cu_seqlens, idx_in=host(idx))
     assert_close(out, ref["o"], what="layer after a timeout")
+
+
+def test_sparse_bwd_wait_runs_out_then_recovers(clean_status):
+    """The tensor-core dK / dV kernel (group size 16): its producer, MMA and softmax roles
+    give up, drain the gathers and products in flight and free the TMEM."""
+    lengths = [2100, 700, 65]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = np.random.Generator(np.random.PCG64(43))
+    q, do = (gen.normal(rng, (cu[-1], 16, 128), "bf16") for _ in range(2))
+    k, v = (gen.normal(rng, (cu[-1], 1, 128), "bf16") for _ in range(2))
+    idx = gen.random_block_indices(rng, cu, 1, 8, 64, force_first=True)
+    o64, lse64 = orc.sparse_attn(q, k, v, idx, cu, 64)
+    o, lse = gen.f32_to_bf16_bits(o64.astype(np.float32)), lse64.astype(np.float32)
+    args = [dev(x) for x in (q, k, v, idx, o, lse, do)]
+    dcu = dev(cu)
+    torch.cuda.synchronize()
+    _flush_l2()
+    nsa.nsa_set_wait_limit_ns(1)
+    nsa.nsa_sparse_bwd(*args, 64, cu_seqlens=dcu, max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status(reset=True) == NSA_ERR_TIMEOUT
+    nsa.nsa_set_wait_limit_ns(0)
+    gq, gk, gv = nsa.nsa_sparse_bwd(*args, 64, cu_seqlens=dcu, max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    rq, rk, rv = orc.sparse_attn_bwd(q, k, v, idx, do, cu, 64, o=o)
+    assert_close(gq, rq, what="dq after a timeout")
+    assert_close(gk, rk, what="dk after a timeout")
+    assert_close(gv, rv, what="dv after a timeout")
