@@ -46,9 +46,11 @@ constexpr int kPBytes = kTileRows * kBS * 2;     // P or dS (hi or lo) of one ti
 constexpr int kSmemBytes = 2 * kKVBytes + 2 * kStageBytes + 4 * kPBytes + 1024;  // + base alignment
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S and dP of tile buffer b at 128 b and 128 b + 64; then dV^T and dK^T in
-// two parts each, the products of the bf16-rounded P / dS and of their remainders (four
-// independent accumulation chains; the epilogue adds the parts)
-constexpr uint32_t kColDV = 256, kColDK = 320, kColDVlo = 384, kColDKlo = 448;
+// two parts each, the products of the bf16-rounded P / dS and of their remainders (the
+// epilogue adds the parts).  A part pair is contiguous, so one N = 128 product fills both:
+// its B operand is the rounded and the remainder buffer (adjacent, kPBytes apart) as the
+// two 64-column groups of one MN-major operand.
+constexpr uint32_t kColDV = 256, kColDVlo = 320, kColDK = 384, kColDKlo = 448;
 // P or dS values above these make the remainder products count (as in sparse_bwd_dkv)
 constexpr float kLoP = 0.00390625f, kLoS = 0.0625f;
 
@@ -408,16 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after();
           const uint32_t qs = stage0 + (u & 1) * kStageBytes, ds = qs + kQBytes;
-          constexpr uint32_t id = idesc_mn(128, kBS);
+          // the first tile runs both parts (it initialises the remainder columns); later
+          // tiles only the parts their values need
+          const uint32_t id_v = idesc_mn(128, (lo & 1) ? 2 * kBS : kBS), id_k = idesc_mn(128, (lo & 2) ? 2 * kBS : kBS);
 #pragma unroll 1
           for (int k = 0; k < kTileRows / 16; ++k) {
             const uint32_t ro = k * 2048;
-            const uint32_t acc_hi = (u > 0 || k > 0) ? 1u : 0u, acc_lo = (lo_init || k > 0) ? 1u : 0u;
+            const uint32_t acc = (u > 0 || k > 0) ? 1u : 0u;
             const uint64_t a_do = sdesc_mn(ds + ro, kHalfRows, 1024), a_q = sdesc_mn(qs + ro, kHalfRows, 1024);
-            tc::mma_ss(tmem + kColDV, a_do, sdesc_mn(p_hi + ro, 1024, 1024), id, acc_hi);
-            tc::mma_ss(tmem + kColDK, a_q, sdesc_mn(s_hi + ro, 1024, 1024), id, acc_hi);
-            if (lo & 1) tc::mma_ss(tmem + kColDVlo, a_do, sdesc_mn(p_lo + ro, 1024, 1024), id, acc_lo);
-            if (lo & 2) tc::mma_ss(tmem + kColDKlo, a_q, sdesc_mn(s_lo + ro, 1024, 1024), id, acc_lo);
+            tc::mma_ss(tmem + kColDV, a_do, sdesc_mn(p_hi + ro, kPBytes, 1024), id_v, acc);
+            tc::mma_ss(tmem + kColDK, a_q, sdesc_mn(s_hi + ro, kPBytes, 1024), id_k, acc);
           }
           tc::commit(bar(B_PFREE));
           tc::commit(bar(B_EMPTY + (u & 1)));
