@@ -632,6 +632,32 @@ def test_decode_group_sizes(B, L, seqlens, k, H, HKV):
     assert_close(out, ref_o, what="decode groups")
 
 
+@pytest.mark.parametrize("L,k", [(20000, 64), (4000, 16)])
+def test_decode_exact_ties(L, k):
+    """A cache of identical keys: every compressed key scores alike, so every block that is
+    not forced has the same pooled score (three windows each) on both sides, bit for bit.
+    The choice must then be the lowest blocks, exactly: with 310 tied candidates the CTA
+    top-k settles every bit and takes ties by block order; with 60 it ranks the bin."""
+    B, H, HKV = 2, 16, 2
+    rng = _rng(77)
+    q = gen.normal(rng, (B, H, 128), "bf16")
+    kcache = np.full((B, L, HKV, 128), gen.f32_to_bf16_bits(np.float32(0.25)), np.uint16)
+    vcache = gen.normal(rng, (B, L, HKV, 128), "bf16")
+    seqlens = np.array([L, L - 37], np.int32)
+    ncs = orc.num_cmp(L)
+    kc_cache = np.zeros((B, ncs, HKV, 128), np.uint16)
+    for b in range(B):
+        kc_cache[b] = orc.compress(kcache[b], [0, L])[1]
+    ref_idx, _ = orc.decode(q, kcache, vcache, kc_cache, seqlens, k=k)
+    idx = torch.empty((B, HKV, k), dtype=torch.int32, device="cuda")
+    out = nsa.nsa_sparse_decode(dev(q), dev(kcache), dev(vcache), dev(kc_cache), dev(seqlens), k=k, idx_out=idx)
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    assert np.array_equal(host(idx), ref_idx)
+    _, ref_o = orc.decode(q, kcache, vcache, kc_cache, seqlens, k=k, idx_in=host(idx))
+    assert_close(out, ref_o, what="decode ties")
+
+
 def test_decode_full_size():
     """B=32, context 32768, H=16, Hkv=2, d=128, top-k 64: all rows."""
     w = gen.decode()
