@@ -283,7 +283,7 @@ def test_sparse_bwd_full_size_sampled():
 
 
 # --------------------------------------------------------------------------- S7 and S1 backward
-@pytest.mark.parametrize("H,hkv", [(16, 1), (16, 4), (8, 8), (64, 4)])
+@pytest.mark.parametrize("H,hkv", [(16, 1), (16, 2), (16, 4), (8, 8), (64, 4)])
 def test_cmp_attn_bwd_varlen(H, hkv):
     """Ragged lengths (no window, one window, several key blocks and query chunks); both
     sides take the oracle's forward (o rounded to bf16, lse)."""
