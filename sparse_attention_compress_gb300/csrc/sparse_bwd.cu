@@ -488,10 +488,18 @@ cudaError_t run_bwd(const BwdParams& p0, const BwdLayout& l, void* workspace, cu
   constexpr int NS_Q = 2, NS_KV = 3;
   constexpr int dq_bytes = 4 * NS_Q * 2 * 16 * kD * 2;
   static_assert(dq_bytes >= 3 * 16 * (kD + 8) * 4, "dq fold needs the ring's shared memory");
-  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_dq<NS_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_bytes);
-  if (e != cudaSuccess) return e;
-  sparse_bwd_dq<NS_Q><<<dim3((unsigned)s.tokens, p.hkv), 128, dq_bytes, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e;
+  if (dq_tc_supported(p)) {  // compressed keys and window, group sizes 8 and 16: the tensor-core kernel
+    const int64_t kv_rows = !p.cmp_kernel ? s.tokens
+                            : s.cu        ? s.tokens / p.cmp_stride + s.n_seqs
+                                          : (int64_t)s.n_seqs * (s.T >= p.cmp_kernel ? (s.T - p.cmp_kernel) / p.cmp_stride + 1 : 0);
+    if ((e = launch_dq_tc(p, kv_rows, st)) != cudaSuccess) return e;
+  } else {
+    e = cudaFuncSetAttribute(sparse_bwd_dq<NS_Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_bytes);
+    if (e != cudaSuccess) return e;
+    sparse_bwd_dq<NS_Q><<<dim3((unsigned)s.tokens, p.hkv), 128, dq_bytes, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const int64_t items = (int64_t)s.n_seqs * p.hkv * l.items_per_bg;
   if (items > 0) {
     if (dkv_tc_supported(p)) {  // group sizes 8 and 16: the tensor-core kernel

@@ -139,6 +139,11 @@ inline bool dkv_tc_shape(int r, bool cmp_or_window, int nb) {
 cudaError_t launch_dkv_tc(const BwdParams& p, int64_t items, int64_t q_rows, cudaStream_t st);
 // Selected blocks: the inverted lists the tensor-core kernel reads (p.inv_list, p.inv_tab).
 cudaError_t launch_invert(const BwdParams& p, cudaStream_t st);
+// The tensor-core dQ kernel (sparse_bwd_tc.cu) of the compressed and window key spaces,
+// group sizes 8 and 16; like sparse_bwd_dq it also stores D = dO . o (p.dsum).  kv_rows:
+// the rows of p.k and p.v (for the compressed keys, a bound on the packed rows).
+bool dq_tc_supported(const BwdParams& p);
+cudaError_t launch_dq_tc(const BwdParams& p, int64_t kv_rows, cudaStream_t st);
 
 }  // namespace bwd
 }  // namespace nsa

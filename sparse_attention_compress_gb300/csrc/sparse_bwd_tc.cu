@@ -614,6 +614,324 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
+// ---------------------------------------------------------------------------- dQ, dense key spaces
+// dQ of the compressed and sliding-window branches (group sizes 8 and 16).  There a query
+// reaches a contiguous key range, and the 128 / r tokens of a 128-row tile reach nearly
+// the same one, so the tile walks 64-key tiles of that range (masked per row at its
+// edges, as the tensor-core forward does):
+//   S = Q K^T, dP = dO V^T        M = 128 rows, N = 64 keys, K = d (TMEM, two buffers)
+//   dS = P (dP - D), P = exp(scale S - lse) from the forward's lse (no running max)
+//   dQ += dS K                    M = 128 rows, N = 128 (d), K = 64 keys; dS is the TMEM A
+//                                 operand (bf16 value and remainder), the K tile the
+//                                 MN-major B operand (the same tile as S's K-major B)
+// The kernel also stores D = dO . o per row, which the dK / dV kernel reads.  Roles as
+// in dkv_tc_kernel: warp 8 loads Q and dO once and streams K / V tiles through a
+// four-stage ring, warp 9 issues the MMAs, warps 0-7 (two per row, a half of the keys
+// each) form dS and finally store dQ.
+namespace dqk {
+constexpr int KT = 64;                           // keys per tile
+constexpr int NS = 4;                            // K / V ring stages
+constexpr int TILE = KT * kD * 2;                // a K or V tile: two 64-column halves of 8 KB
+constexpr int QB = kTileRows * kD * 2;           // Q or dO of the 128 rows: two halves of 16 KB
+constexpr int SMEM = 2 * QB + NS * 2 * TILE + 1024;
+// TMEM: S and dP of buffer b at 128 b and 128 b + 64; dS of buffer b at 256 + 64 b (the
+// rounded part in its first 32 columns, the remainder in the next 32); dQ at 384
+constexpr uint32_t COL_DS = 256, COL_DQ = 384;
+enum : int {
+  QB_Q = 0,                    // Q and dO landed
+  QB_KVFULL = 1,               // [NS]
+  QB_KVEMPTY = QB_KVFULL + NS,  // [NS] dQ of the tile done (K is read by it, V by dP before)
+  QB_SFULL = QB_KVEMPTY + NS,   // [2]
+  QB_SFREE = QB_SFULL + 2,      // [2] the softmax warps read S / dP of the buffer
+  QB_DSFULL = QB_SFREE + 2,     // [2] dS of the buffer written
+  QB_DQDONE = QB_DSFULL + 2,    // [2] dQ += dS K of the buffer done
+  QB_DRAIN = QB_DQDONE + 2,
+  QB_COUNT
+};
+}  // namespace dqk
+
+// 16 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const BwdParams p) {
+  using namespace dqk;
+  constexpr int TPC = kTileRows / R;  // tokens per CTA
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t s_bar[QB_COUNT];
+  __shared__ int s_need[2][kSoftWarps];  // per dS buffer and softmax warp: remainder products needed
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tc::device_status_set()) return;  // after a timeout elsewhere, later CTAs leave at once
+  const int sq = blockIdx.y, g = blockIdx.z;
+  const int L = seq_len(p.seqs, sq);
+  const int tile = (L + TPC - 1) / TPC - 1 - (int)blockIdx.x;  // longest key ranges first
+  if (tile < 0) return;
+  const int t0 = tile * TPC, t_last = min(t0 + TPC, L) - 1;
+  const int64_t start = seq_start(p.seqs, sq);
+  const int Lk = key_len(p, L);
+  const int64_t kv0 = key_base(p, sq);  // key row of the sequence's first key
+  const int k_lo = key_lo(p, t0), k_hi = key_bound(p, t_last, Lk) + 1;
+  const int64_t a_lo = (kv0 + k_lo) / KT;  // key tiles at absolute 64-row offsets
+  const int n_kt = k_hi > k_lo ? (int)((kv0 + k_hi + KT - 1) / KT - a_lo) : 0;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023) & ~1023u;
+  const uint32_t q_s = sbase, do_s = q_s + QB, ring = do_s + QB;
+  auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
+  volatile int* abort = &s_abort;
+  if (tid == 0) {
+    tc::mbar_init(bar(QB_Q), 1);
+    for (int i = 0; i < NS; ++i) {
+      tc::mbar_init(bar(QB_KVFULL + i), 1);
+      tc::mbar_init(bar(QB_KVEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bar(QB_SFULL + i), 1);
+      tc::mbar_init(bar(QB_SFREE + i), kSoft);
+      tc::mbar_init(bar(QB_DSFULL + i), kSoft);
+      tc::mbar_init(bar(QB_DQDONE + i), 1);
+    }
+    tc::mbar_init(bar(QB_DRAIN), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == kIssuer) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    tc::fence_before();
+  }
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = s_tmem;
+
+  int last_kv = -1;  // producer: last K / V tile handed to the ring
+  if (warp == kProducer) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_kt > 0) {
+      tc::mbar_expect_tx(bar(QB_Q), 2 * QB);
+      tc::tma3d(q_s, &tm_q, 0, g * R, (int)(start + t0), bar(QB_Q));
+      tc::tma3d(q_s + QB / 2, &tm_q, 64, g * R, (int)(start + t0), bar(QB_Q));
+      tc::tma3d(do_s, &tm_do, 0, g * R, (int)(start + t0), bar(QB_Q));
+      tc::tma3d(do_s + QB / 2, &tm_do, 64, g * R, (int)(start + t0), bar(QB_Q));
+    }
+    // key rows the buffers hold: the tokens (window), or the packed compressed rows of all
+    // sequences, counted here; a tile that reaches past them is copied with bounds checks
+    int64_t kv_total = p.seqs.tokens;
+    if (p.cmp_kernel) {
+      int64_t acc = 0;
+      for (int i = lane; i < p.seqs.n_seqs; i += 32) acc += num_cmp(seq_len(p.seqs, i), p.cmp_kernel, p.cmp_stride);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      kv_total = acc;
+    }
+    for (int i = 0; i < n_kt; ++i) {
+      const int st = i % NS;
+      if (i >= NS && !tc::warp_wait(bar(QB_KVEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
+      const int64_t row = (a_lo + i) * KT;
+      const uint32_t ks = ring + st * 2 * TILE, vs = ks + TILE, fb = bar(QB_KVFULL + st);
+      if (p.cmp_kernel && row + KT > kv_total) {
+        for (int c = lane; c < KT * (kD / 8); c += 32) {
+          const int r = c / (kD / 8), ch = c % (kD / 8);
+          const bool in = row + r < kv_total;
+          const int64_t off = ((row + r) * p.hkv + g) * kD + ch * 8;
+          const uint32_t dst = (ch >> 3) * (TILE / 2) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+          cp_async16(ks + dst, in ? (const void*)(p.k + off) : (const void*)p.k, in ? 16 : 0);
+          cp_async16(vs + dst, in ? (const void*)(p.v + off) : (const void*)p.k, in ? 16 : 0);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(fb);
+      } else if (lane == 0) {
+        tc::mbar_expect_tx(fb, 2 * TILE);
+        tc::tma2d(ks, &tm_k, g * kD, (int)row, fb);
+        tc::tma2d(ks + TILE / 2, &tm_k, g * kD + 64, (int)row, fb);
+        tc::tma2d(vs, &tm_v, g * kD, (int)row, fb);
+        tc::tma2d(vs + TILE / 2, &tm_v, g * kD + 64, (int)row, fb);
+      }
+      last_kv = i;
+      __syncwarp();
+    }
+  }
+
+  if (warp == kIssuer && n_kt > 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    // Step j issues S and dP of tile j into TMEM buffer j % 2 (once the softmax warps have
+    // read that buffer's tile j - 2), then dQ += dS K of tile j - 1 (once its dS is in TMEM).
+    bool ok = tc::warp_wait(bar(QB_Q), 0, abort);
+    for (int j = 0; ok && j <= n_kt; ++j) {
+      if (j < n_kt) {
+        const int b = j & 1, st = j % NS;
+        if (j >= 2 && !(ok = tc::warp_wait(bar(QB_SFREE + b), ((j - 2) >> 1) & 1, abort))) break;
+        if (!(ok = tc::warp_wait(bar(QB_KVFULL + st), (j / NS) & 1, abort))) break;
+        if (lane == 0) {
+          tc::fence_after();
+          const uint32_t ks = ring + st * 2 * TILE, vs = ks + TILE;
+          constexpr uint32_t id = tc::idesc(128, KT);
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t ao = (k >> 2) * (QB / 2) + (k & 3) * 32, bo = (k >> 2) * (TILE / 2) + (k & 3) * 32;
+            tc::mma_ss(tmem + b * 128, tc::sdesc(q_s + ao), tc::sdesc(ks + bo), id, k > 0);
+            tc::mma_ss(tmem + b * 128 + 64, tc::sdesc(do_s + ao), tc::sdesc(vs + bo), id, k > 0);
+          }
+          tc::commit(bar(QB_SFULL + b));
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        const int u = j - 1, bu = u & 1, st = u % NS;
+        if (!(ok = tc::warp_wait(bar(QB_DSFULL + bu), (u >> 1) & 1, abort))) break;
+        if (lane == 0) {  // lane 0 observed the dS arrival: it reads the warps' flags
+          int lo = 0;
+#pragma unroll
+          for (int w = 0; w < kSoftWarps; ++w) lo |= s_need[bu][w];
+          tc::fence_after();
+          const uint32_t ks = ring + st * 2 * TILE;
+          constexpr uint32_t id = tc::idesc(128, kD) | (1u << 16);  // B (the K tile) MN-major
+#pragma unroll
+          for (int s = 0; s < KT / 16; ++s) {
+            const uint64_t bk = sdesc_mn(ks + s * 2048, TILE / 2, 1024);
+            tc::mma_ts(tmem + COL_DQ, tmem + COL_DS + bu * 64 + s * 8, bk, id, (u > 0 || s > 0) ? 1u : 0u);
+            if (lo) tc::mma_ts(tmem + COL_DQ, tmem + COL_DS + bu * 64 + 32 + s * 8, bk, id, 1u);
+          }
+          tc::commit(bar(QB_DQDONE + bu));
+          tc::commit(bar(QB_KVEMPTY + st));
+        }
+        __syncwarp();
+      }
+    }
+  }
+  if (warp < kSoftWarps) {
+    // ------------------------------------------------------------------ softmax warps
+    // TMEM lanes 32 (warp % 4) .. are this warp's rows; kh: its half of the 64 keys
+    __shared__ float s_dd[2][kTileRows];  // D = dO . o, the two halves of d
+    const int row = (warp & 3) * 32 + lane, kh = warp >> 2, slot = row / R, hd = row % R;
+    const int t = t0 + slot;
+    const bool valid = t <= t_last;
+    const int64_t rg = (start + t) * p.h + (int64_t)g * R + hd;
+    const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    {
+      float acc = 0.f;
+      if (valid) {
+        const uint4* a = reinterpret_cast<const uint4*>(p.dout + rg * kD + kh * 64);
+        const uint4* b = reinterpret_cast<const uint4*>(p.o + rg * kD + kh * 64);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = __ldg(a + c), y = __ldg(b + c);
+          acc += dot_bf16x2(x.x, y.x) + dot_bf16x2(x.y, y.y) + dot_bf16x2(x.z, y.z) + dot_bf16x2(x.w, y.w);
+        }
+      }
+      s_dd[kh][row] = acc;
+    }
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kSoft) : "memory");
+    const float dsum = s_dd[0][row] + s_dd[1][row];
+    if (valid && kh == 0) p.dsum[rg] = dsum;
+    const float lse2 = valid ? lse_to_log2(p.lse[rg]) : __builtin_inff();
+    const int tl = key_lo(p, t), tb = valid ? key_bound(p, t, Lk) : -1;
+    bool ok = true;
+    for (int u = 0; u < n_kt; ++u) {
+      const int bu = u & 1;
+      if (!(ok = tc::warp_wait(bar(QB_SFULL + bu), (u >> 1) & 1, abort))) break;
+      tc::fence_after();
+      float sv[32], dpv[32];
+      tc::tmem_ld32_nowait(t_lane + bu * 128 + kh * 32, sv);
+      tc::tmem_ld32_nowait(t_lane + bu * 128 + 64 + kh * 32, dpv);
+      tc::tmem_wait_ld();
+      tc::fence_before();
+      tc::mbar_arrive(bar(QB_SFREE + bu));
+      const int k0 = (int)((a_lo + u) * KT - kv0) + kh * 32;  // key of sv[0] within the sequence
+      uint32_t hi[16], lo[16];
+      float smax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const int k = k0 + e;
+        const float p0 = k >= tl && k <= tb ? ex2(sv[e] * p.scale_log2 - lse2) : 0.f;
+        const float p1 = k + 1 >= tl && k + 1 <= tb ? ex2(sv[e + 1] * p.scale_log2 - lse2) : 0.f;
+        const float d0 = p0 * (dpv[e] - dsum), d1 = p1 * (dpv[e + 1] - dsum);
+        smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
+        split_bf16x2(d0, d1, hi[e / 2], lo[e / 2]);
+      }
+      // the dS buffer is free once the dQ product of tile u - 2 is done
+      if (u >= 2 && !(ok = tc::warp_wait(bar(QB_DQDONE + bu), ((u - 2) >> 1) & 1, abort))) break;
+      {
+        const unsigned bs = __ballot_sync(0xffffffffu, smax > kLoS);
+        if (lane == 0) s_need[bu][warp] = bs ? 1 : 0;
+      }
+      tc::fence_after();
+      tmem_st16(t_lane + COL_DS + bu * 64 + kh * 16, hi);
+      tmem_st16(t_lane + COL_DS + bu * 64 + 32 + kh * 16, lo);
+      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+      tc::fence_before();
+      tc::mbar_arrive(bar(QB_DSFULL + bu));
+    }
+    // ------------------------------------------------------------------ epilogue
+    // both buffers' last products are done (the second wait only drains its arrival)
+    if (ok && n_kt > 0) ok = tc::warp_wait(bar(QB_DQDONE + ((n_kt - 1) & 1)), ((n_kt - 1) >> 1) & 1, abort);
+    if (ok && n_kt > 1) ok = tc::warp_wait(bar(QB_DQDONE + ((n_kt - 2) & 1)), ((n_kt - 2) >> 1) & 1, abort);
+    if (ok) {
+      float v[64];
+      if (n_kt > 0) {
+        tc::fence_after();
+        tc::tmem_ld32_nowait(t_lane + COL_DQ + kh * 64, v);
+        tc::tmem_ld32_nowait(t_lane + COL_DQ + kh * 64 + 32, v + 32);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) v[e] = 0.f;
+      }
+      if (valid) {
+        uint4* o = reinterpret_cast<uint4*>(p.dq + rg * kD + kh * 64);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float* x = v + 8 * c;
+          o[c] = make_uint4(pack_bf16(x[0] * p.scale, x[1] * p.scale), pack_bf16(x[2] * p.scale, x[3] * p.scale),
+                            pack_bf16(x[4] * p.scale, x[5] * p.scale), pack_bf16(x[6] * p.scale, x[7] * p.scale));
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort) {
+    // copies and tensor-core work still in flight land before the CTA leaves
+    if (warp == kProducer) {
+      if (n_kt > 0) tc::warp_drain(bar(QB_Q), 0);
+      for (int st = 0; st < NS; ++st) {
+        const int i = last_kv - ((last_kv - st) % NS + NS) % NS;  // last tile handed to stage st
+        if (i >= 0) tc::warp_drain(bar(QB_KVFULL + st), (i / NS) & 1);
+      }
+    } else if (warp == kIssuer) {
+      if (lane == 0) tc::commit(bar(QB_DRAIN));
+      __syncwarp();
+      tc::warp_drain(bar(QB_DRAIN), 0);
+    }
+  } else if (warp == kProducer) {
+    // the MMA warp's last release of each stage lands before the CTA leaves
+    for (int st = 0; st < NS; ++st) {
+      const int i = last_kv - ((last_kv - st) % NS + NS) % NS;
+      if (i >= 0) tc::warp_drain(bar(QB_KVEMPTY + st), (i / NS) & 1);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == kIssuer)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
 }  // namespace
 
 cudaError_t launch_invert(const BwdParams& p, cudaStream_t st) {
@@ -643,6 +961,40 @@ cudaError_t launch_dkv_tc(const BwdParams& p, int64_t items, int64_t q_rows, cud
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)items, kThreads, kSmemBytes, st>>>(mq, mdo, p);
+  return cudaGetLastError();
+}
+
+bool dq_tc_supported(const BwdParams& p) {
+  const int r = p.h / p.hkv;
+  return (r == 8 || r == 16) && (p.cmp_kernel > 0 || p.window > 0);
+}
+
+// kv_rows: rows of k and v ([kv_rows, hkv, d]; for the compressed keys a bound on the
+// packed rows, past which the kernel reads nothing).
+cudaError_t launch_dq_tc(const BwdParams& p, int64_t kv_rows, cudaStream_t st) {
+  const Seqs& s = p.seqs;
+  if (s.tokens == 0) return cudaSuccess;
+  const int r = p.h / p.hkv, tpc = kTileRows / r;
+  CUtensorMap mq, mdo, mk, mv;
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)p.h, (uint64_t)s.tokens};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)p.h * kD * 2};
+    const uint32_t box[3] = {64, (uint32_t)r, (uint32_t)tpc};
+    if (!tc::make_map(&mq, p.q, 3, dims, strides, box) || !tc::make_map(&mdo, p.dout, 3, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)p.hkv * kD, (uint64_t)std::max<int64_t>(kv_rows, 1)};
+    const uint64_t strides[1] = {(uint64_t)p.hkv * kD * 2};
+    const uint32_t box[2] = {64, (uint32_t)dqk::KT};
+    if (!tc::make_map(&mk, p.k, 2, dims, strides, box) || !tc::make_map(&mv, p.v, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = r == 16 ? dq_tc_kernel<16> : dq_tc_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((s.max_len + tpc - 1) / tpc), (unsigned)s.n_seqs, (unsigned)p.hkv);
+  kern<<<grid, kThreads, dqk::SMEM, st>>>(mq, mdo, mk, mv, p);
   return cudaGetLastError();
 }
 
