@@ -279,11 +279,11 @@ def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks, batch=8):
             "launches_per_step": 3}
 
 
-def bench_cmp_bwd(torch, nsa, device, steps, warmup, flush, peaks):
+def bench_cmp_bwd(torch, nsa, device, steps, warmup, flush, peaks, T=65536):
     """Backward of the compressed branch at the layer shape: dq, d k_cmp, d v_cmp from the
     forward's o and lse, then the pooling backward to the token rows of K and V."""
     from sparse_attention_compress_gb300 import _lib
-    w = gen.layer()
+    w = gen.layer(T=T)
     q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
     kc, vc = nsa.nsa_compress_k(k), nsa.nsa_compress_k(v)
     do = dev(torch, gen.normal(gen.rng_for(4, 99), (w.tokens, w.h, w.d), "bf16"), device)
@@ -304,16 +304,16 @@ def bench_cmp_bwd(torch, nsa, device, steps, warmup, flush, peaks):
     ncaus = np.clip((t - 31) // 16 + 1, 0, None)
     flops = float(ncaus.sum()) * w.h * 2 * w.d * 5  # S and dP recomputed, dQ, dK, dV
     tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": "backward of the compressed branch + pooling, layer T=65536 H=64 Hkv=4 d=128 bf16 "
+    return {"workload": f"backward of the compressed branch + pooling, layer T={T} H=64 Hkv=4 d=128 bf16 "
                         "(32/16 windows)", "ms_per_step": ms, "tflops": tf, "flops_per_step": flops,
             "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "workspace_bytes": int(ws.numel()),
             "launches_per_step": 5}
 
 
-def bench_swa_bwd(torch, nsa, device, steps, warmup, flush, peaks):
+def bench_swa_bwd(torch, nsa, device, steps, warmup, flush, peaks, T=65536):
     """Backward of the sliding-window branch (window 512) and of the gate, layer shape."""
     from sparse_attention_compress_gb300 import _lib
-    w = gen.layer()
+    w = gen.layer(T=T)
     q, k, v = dev(torch, w.q, device), dev(torch, w.k, device), dev(torch, w.v, device)
     do = dev(torch, gen.normal(gen.rng_for(4, 98), (w.tokens, w.h, w.d), "bf16"), device)
     lse = torch.empty((w.tokens, w.h), dtype=torch.float32, device=device)
@@ -329,7 +329,7 @@ def bench_swa_bwd(torch, nsa, device, steps, warmup, flush, peaks):
     msg = float(np.mean(timed(torch, lambda: nsa.nsa_gate_combine_bwd(do, o, o, o, logits), steps, warmup, flush)))
     gbytes = w.tokens * w.h * (w.d * 2 * 7 + 3 * 4 * 2)
     tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": "backward of the sliding window (512) and of the gate, layer T=65536 H=64 Hkv=4 d=128 bf16",
+    return {"workload": f"backward of the sliding window (512) and of the gate, layer T={T} H=64 Hkv=4 d=128 bf16",
             "swa_ms": ms, "swa_tflops": tf, "swa_frac_of_bf16_peak": tf / peaks["bf16_tflops"],
             "gate_ms": msg, "gate_gbs": gbytes / (msg * 1e-3) / 1e9,
             "gate_hbm_frac": gbytes / (msg * 1e-3) / 1e9 / peaks["hbm_gbs"], "launches_per_step": 4}
@@ -567,7 +567,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="0: size the oracle sample to ~15 s")
     ap.add_argument("--batch", type=int, default=8, help="prefill batch (8 is the benchmark; smaller for ncu)")
-    ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark)")
+    ap.add_argument("--layer-tokens", type=int, default=65536, help="layer workload length (65536 is the benchmark; also the branch backwards' length)")
     ap.add_argument("--only", default="", choices=["", "prefill", "prefill_bwd", "cmp_bwd", "swa_bwd", "layer_train", "nosa", "decode",
                                                     "decode_offload",
                                                     "selection", "layer", "block_sparse"],
@@ -604,8 +604,10 @@ def main():
     if args.only in ("prefill_bwd", "cmp_bwd", "swa_bwd", "layer_train", "nosa", "decode", "decode_offload",
                      "selection", "layer", "block_sparse"):
         fn = {"layer_train": lambda: bench_layer_train(torch, nsa, device, args.steps, args.warmup, flush, peaks),
-              "swa_bwd": lambda: bench_swa_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
-              "cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks),
+              "swa_bwd": lambda: bench_swa_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks,
+                                               args.layer_tokens),
+              "cmp_bwd": lambda: bench_cmp_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks,
+                                               args.layer_tokens),
               "nosa": lambda: bench_nosa(torch, nsa, device, args.steps, args.warmup, flush, peaks),
               "prefill_bwd": lambda: bench_prefill_bwd(torch, nsa, device, args.steps, args.warmup, flush, peaks,
                                                        batch=args.batch),

@@ -617,48 +617,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------- dQ, dense key spaces
 // dQ of the compressed and sliding-window branches (group sizes 8 and 16).  There a query
 // reaches a contiguous key range, and the 128 / r tokens of a 128-row tile reach nearly
-// the same one, so the tile walks 64-key tiles of that range (masked per row at its
+// the same one, so the tile walks 128-key tiles of that range (masked per row at its
 // edges, as the tensor-core forward does):
-//   S = Q K^T, dP = dO V^T        M = 128 rows, N = 64 keys, K = d (TMEM, two buffers)
+//   S = Q K^T, dP = dO V^T        M = 128 rows, N = 128 keys, K = d
 //   dS = P (dP - D), P = exp(scale S - lse) from the forward's lse (no running max)
-//   dQ += dS K                    M = 128 rows, N = 128 (d), K = 64 keys; dS is the TMEM A
+//   dQ += dS K                    M = 128 rows, N = 128 (d), K = 128 keys; dS is the TMEM A
 //                                 operand (bf16 value and remainder), the K tile the
 //                                 MN-major B operand (the same tile as S's K-major B)
+// 128-key tiles, since a tcgen05 product occupies the tensor pipe for about as long at
+// N = 64 as at N = 128 (measured: 74 against 70 cycles per M = 128, K = 16 product).
+// TMEM holds two S buffers (dS is written over its tile's S, once every thread has its
+// S values in registers), one dP buffer and the dQ accumulator: 4 x 128 columns.
 // The kernel also stores D = dO . o per row, which the dK / dV kernel reads.  Roles as
-// in dkv_tc_kernel: warp 8 loads Q and dO once and streams K / V tiles through a
-// four-stage ring, warp 9 issues the MMAs, warps 0-7 (two per row, a half of the keys
-// each) form dS and finally store dQ.
+// in dkv_tc_kernel: warp 8 loads Q and dO once and streams K tiles through a three-stage
+// and V tiles through a two-stage ring (V is free once dP is done), warp 9 issues the
+// MMAs (S and dP of the next tile while the softmax warps work on this one), warps 0-7
+// (rows 32 (w % 4) .., keys 64 (w / 4) .. of every tile) form dS and finally store dQ.
 namespace dqk {
-constexpr int KT = 64;                           // keys per tile
-constexpr int NS = 4;                            // K / V ring stages
-constexpr int TILE = KT * kD * 2;                // a K or V tile: two 64-column halves of 8 KB
-constexpr int QB = kTileRows * kD * 2;           // Q or dO of the 128 rows: two halves of 16 KB
-constexpr int SMEM = 2 * QB + NS * 2 * TILE + 1024;
-// TMEM: S and dP of buffer b at 128 b and 128 b + 64; dS of buffer b at 256 + 64 b (the
-// rounded part in its first 32 columns, the remainder in the next 32); dQ at 384
-constexpr uint32_t COL_DS = 256, COL_DQ = 384;
+constexpr int KT = 128;                // keys per tile
+constexpr int NK = 3, NV = 2;          // K and V ring stages
+constexpr int TILE = KT * kD * 2;      // a K or V tile: two 64-column halves of 16 KB
+constexpr int QB = kTileRows * kD * 2;  // Q or dO of the 128 rows: two halves of 16 KB
+constexpr int SMEM = 2 * QB + (NK + NV) * TILE + 1024;
+constexpr uint32_t COL_DP = 256, COL_DQ = 384;  // S / dS buffers at 0 and 128
 enum : int {
   QB_Q = 0,                    // Q and dO landed
-  QB_KVFULL = 1,               // [NS]
-  QB_KVEMPTY = QB_KVFULL + NS,  // [NS] dQ of the tile done (K is read by it, V by dP before)
-  QB_SFULL = QB_KVEMPTY + NS,   // [2]
-  QB_SFREE = QB_SFULL + 2,      // [2] the softmax warps read S / dP of the buffer
-  QB_DSFULL = QB_SFREE + 2,     // [2] dS of the buffer written
-  QB_DQDONE = QB_DSFULL + 2,    // [2] dQ += dS K of the buffer done
-  QB_DRAIN = QB_DQDONE + 2,
+  QB_KFULL = 1,                // [NK]
+  QB_KEMPTY = QB_KFULL + NK,   // [NK] dQ of the tile done
+  QB_VFULL = QB_KEMPTY + NK,   // [NV]
+  QB_VEMPTY = QB_VFULL + NV,   // [NV] dP of the tile done
+  QB_SFULL = QB_VEMPTY + NV,   // [2] S and dP of a tile computed (S buffer = tile % 2)
+  QB_DPFREE = QB_SFULL + 2,    // the softmax warps hold dP of the current tile
+  QB_DSFULL = QB_DPFREE + 1,   // [2] dS written over its tile's S
+  QB_DQDONE = QB_DSFULL + 2,   // [2] dQ += dS K of the buffer's tile done
+  QB_ADONE = QB_DQDONE + 2,    // every product of the CTA done
+  QB_DRAIN,
   QB_COUNT
 };
 }  // namespace dqk
-
-// 16 consecutive TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
 
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -669,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int TPC = kTileRows / R;  // tokens per CTA
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t s_bar[QB_COUNT];
-  __shared__ int s_need[2][kSoftWarps];  // per dS buffer and softmax warp: remainder products needed
+  __shared__ int s_need[2][kSoftWarps];  // per S buffer and softmax warp: remainder products needed
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -683,25 +679,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Lk = key_len(p, L);
   const int64_t kv0 = key_base(p, sq);  // key row of the sequence's first key
   const int k_lo = key_lo(p, t0), k_hi = key_bound(p, t_last, Lk) + 1;
-  const int64_t a_lo = (kv0 + k_lo) / KT;  // key tiles at absolute 64-row offsets
+  const int64_t a_lo = (kv0 + k_lo) / KT;  // key tiles at absolute 128-row offsets
   const int n_kt = k_hi > k_lo ? (int)((kv0 + k_hi + KT - 1) / KT - a_lo) : 0;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023) & ~1023u;
-  const uint32_t q_s = sbase, do_s = q_s + QB, ring = do_s + QB;
+  const uint32_t q_s = sbase, do_s = q_s + QB, k_ring = do_s + QB, v_ring = k_ring + NK * TILE;
   auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
   volatile int* abort = &s_abort;
   if (tid == 0) {
     tc::mbar_init(bar(QB_Q), 1);
-    for (int i = 0; i < NS; ++i) {
-      tc::mbar_init(bar(QB_KVFULL + i), 1);
-      tc::mbar_init(bar(QB_KVEMPTY + i), 1);
+    for (int i = 0; i < NK; ++i) {
+      tc::mbar_init(bar(QB_KFULL + i), 1);
+      tc::mbar_init(bar(QB_KEMPTY + i), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      tc::mbar_init(bar(QB_VFULL + i), 1);
+      tc::mbar_init(bar(QB_VEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(QB_SFULL + i), 1);
-      tc::mbar_init(bar(QB_SFREE + i), kSoft);
       tc::mbar_init(bar(QB_DSFULL + i), kSoft);
       tc::mbar_init(bar(QB_DQDONE + i), 1);
     }
+    tc::mbar_init(bar(QB_DPFREE), kSoft);
+    tc::mbar_init(bar(QB_ADONE), 1);
     tc::mbar_init(bar(QB_DRAIN), 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -717,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = s_tmem;
 
-  int last_kv = -1;  // producer: last K / V tile handed to the ring
+  int last_k = -1, last_v = -1;  // producer: last K / V tile handed to its ring
   if (warp == kProducer) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && n_kt > 0) {
@@ -737,19 +738,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       kv_total = acc;
     }
-    for (int i = 0; i < n_kt; ++i) {
-      const int st = i % NS;
-      if (i >= NS && !tc::warp_wait(bar(QB_KVEMPTY + st), ((i / NS) - 1) & 1, abort)) break;
-      const int64_t row = (a_lo + i) * KT;
-      const uint32_t ks = ring + st * 2 * TILE, vs = ks + TILE, fb = bar(QB_KVFULL + st);
+    // one K or V tile into the stage at dst (warp-uniform)
+    auto load = [&](const CUtensorMap* map, const __nv_bfloat16* src, uint32_t dst, uint32_t fb, int64_t row) {
       if (p.cmp_kernel && row + KT > kv_total) {
         for (int c = lane; c < KT * (kD / 8); c += 32) {
           const int r = c / (kD / 8), ch = c % (kD / 8);
           const bool in = row + r < kv_total;
           const int64_t off = ((row + r) * p.hkv + g) * kD + ch * 8;
-          const uint32_t dst = (ch >> 3) * (TILE / 2) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          cp_async16(ks + dst, in ? (const void*)(p.k + off) : (const void*)p.k, in ? 16 : 0);
-          cp_async16(vs + dst, in ? (const void*)(p.v + off) : (const void*)p.k, in ? 16 : 0);
+          cp_async16(dst + (ch >> 3) * (TILE / 2) + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                     in ? (const void*)(src + off) : (const void*)p.k, in ? 16 : 0);
         }
         cp_async_commit();
         cp_async_wait<0>();
@@ -757,67 +754,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(fb);
       } else if (lane == 0) {
-        tc::mbar_expect_tx(fb, 2 * TILE);
-        tc::tma2d(ks, &tm_k, g * kD, (int)row, fb);
-        tc::tma2d(ks + TILE / 2, &tm_k, g * kD + 64, (int)row, fb);
-        tc::tma2d(vs, &tm_v, g * kD, (int)row, fb);
-        tc::tma2d(vs + TILE / 2, &tm_v, g * kD + 64, (int)row, fb);
+        tc::mbar_expect_tx(fb, TILE);
+        tc::tma2d(dst, map, g * kD, (int)row, fb);
+        tc::tma2d(dst + TILE / 2, map, g * kD + 64, (int)row, fb);
       }
-      last_kv = i;
       __syncwarp();
+    };
+    for (int i = 0; i < n_kt; ++i) {
+      const int64_t row = (a_lo + i) * KT;
+      const int sk = i % NK, sv = i % NV;
+      if (i >= NK && !tc::warp_wait(bar(QB_KEMPTY + sk), ((i / NK) - 1) & 1, abort)) break;
+      load(&tm_k, p.k, k_ring + sk * TILE, bar(QB_KFULL + sk), row);
+      last_k = i;
+      if (i >= NV && !tc::warp_wait(bar(QB_VEMPTY + sv), ((i / NV) - 1) & 1, abort)) break;
+      load(&tm_v, p.v, v_ring + sv * TILE, bar(QB_VFULL + sv), row);
+      last_v = i;
     }
   }
 
   if (warp == kIssuer && n_kt > 0) {
     // ------------------------------------------------------------------ MMA issuer
-    // Step j issues S and dP of tile j into TMEM buffer j % 2 (once the softmax warps have
-    // read that buffer's tile j - 2), then dQ += dS K of tile j - 1 (once its dS is in TMEM).
+    // Per tile u: S and dP of tile u + 1 (S into buffer (u + 1) % 2 once dQ of tile u - 1,
+    // which read the dS over that buffer, is done; dP once the softmax warps hold dP(u)),
+    // then dQ += dS K of tile u once its dS is written.
+    constexpr uint32_t id_s = tc::idesc(128, KT);
+    auto issue_s = [&](int j) -> bool {  // warp-uniform
+      const int sk = j % NK;
+      if (!tc::warp_wait(bar(QB_KFULL + sk), (j / NK) & 1, abort)) return false;
+      if (lane == 0) {
+        tc::fence_after();
+        const uint32_t ks = k_ring + sk * TILE;
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint32_t ao = (k >> 2) * (QB / 2) + (k & 3) * 32, bo = (k >> 2) * (TILE / 2) + (k & 3) * 32;
+          tc::mma_ss(tmem + (j & 1) * 128, tc::sdesc(q_s + ao), tc::sdesc(ks + bo), id_s, k > 0);
+        }
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int j) -> bool {
+      const int sv = j % NV;
+      if (j >= 1 && !tc::warp_wait(bar(QB_DPFREE), (j - 1) & 1, abort)) return false;
+      if (!tc::warp_wait(bar(QB_VFULL + sv), (j / NV) & 1, abort)) return false;
+      if (lane == 0) {
+        tc::fence_after();
+        const uint32_t vs = v_ring + sv * TILE;
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint32_t ao = (k >> 2) * (QB / 2) + (k & 3) * 32, bo = (k >> 2) * (TILE / 2) + (k & 3) * 32;
+          tc::mma_ss(tmem + COL_DP, tc::sdesc(do_s + ao), tc::sdesc(vs + bo), id_s, k > 0);
+        }
+        tc::commit(bar(QB_SFULL + (j & 1)));
+        tc::commit(bar(QB_VEMPTY + sv));
+      }
+      __syncwarp();
+      return true;
+    };
     bool ok = tc::warp_wait(bar(QB_Q), 0, abort);
-    for (int j = 0; ok && j <= n_kt; ++j) {
-      if (j < n_kt) {
-        const int b = j & 1, st = j % NS;
-        if (j >= 2 && !(ok = tc::warp_wait(bar(QB_SFREE + b), ((j - 2) >> 1) & 1, abort))) break;
-        if (!(ok = tc::warp_wait(bar(QB_KVFULL + st), (j / NS) & 1, abort))) break;
-        if (lane == 0) {
-          tc::fence_after();
-          const uint32_t ks = ring + st * 2 * TILE, vs = ks + TILE;
-          constexpr uint32_t id = tc::idesc(128, KT);
-#pragma unroll
-          for (int k = 0; k < kD / 16; ++k) {
-            const uint32_t ao = (k >> 2) * (QB / 2) + (k & 3) * 32, bo = (k >> 2) * (TILE / 2) + (k & 3) * 32;
-            tc::mma_ss(tmem + b * 128, tc::sdesc(q_s + ao), tc::sdesc(ks + bo), id, k > 0);
-            tc::mma_ss(tmem + b * 128 + 64, tc::sdesc(do_s + ao), tc::sdesc(vs + bo), id, k > 0);
-          }
-          tc::commit(bar(QB_SFULL + b));
-        }
-        __syncwarp();
+    if (ok) ok = issue_s(0) && issue_dp(0);
+    for (int u = 0; ok && u < n_kt; ++u) {
+      if (u + 1 < n_kt) {
+        if (u >= 1 && !(ok = tc::warp_wait(bar(QB_DQDONE + ((u - 1) & 1)), ((u - 1) >> 1) & 1, abort))) break;
+        if (!(ok = issue_s(u + 1) && issue_dp(u + 1))) break;
       }
-      if (j >= 1) {
-        const int u = j - 1, bu = u & 1, st = u % NS;
-        if (!(ok = tc::warp_wait(bar(QB_DSFULL + bu), (u >> 1) & 1, abort))) break;
-        if (lane == 0) {  // lane 0 observed the dS arrival: it reads the warps' flags
-          int lo = 0;
+      const int b = u & 1, sk = u % NK;
+      if (!(ok = tc::warp_wait(bar(QB_DSFULL + b), (u >> 1) & 1, abort))) break;
+      if (lane == 0) {  // lane 0 observed the dS arrival: it reads the warps' flags
+        int lo = 0;
 #pragma unroll
-          for (int w = 0; w < kSoftWarps; ++w) lo |= s_need[bu][w];
-          tc::fence_after();
-          const uint32_t ks = ring + st * 2 * TILE;
-          constexpr uint32_t id = tc::idesc(128, kD) | (1u << 16);  // B (the K tile) MN-major
+        for (int w = 0; w < kSoftWarps; ++w) lo |= s_need[b][w];
+        tc::fence_after();
+        const uint32_t ks = k_ring + sk * TILE;
+        constexpr uint32_t id = tc::idesc(128, kD) | (1u << 16);  // B (the K tile) MN-major
 #pragma unroll
-          for (int s = 0; s < KT / 16; ++s) {
-            const uint64_t bk = sdesc_mn(ks + s * 2048, TILE / 2, 1024);
-            tc::mma_ts(tmem + COL_DQ, tmem + COL_DS + bu * 64 + s * 8, bk, id, (u > 0 || s > 0) ? 1u : 0u);
-            if (lo) tc::mma_ts(tmem + COL_DQ, tmem + COL_DS + bu * 64 + 32 + s * 8, bk, id, 1u);
-          }
-          tc::commit(bar(QB_DQDONE + bu));
-          tc::commit(bar(QB_KVEMPTY + st));
+        for (int s = 0; s < KT / 16; ++s) {
+          // dS of keys 16 s .. 16 s + 15: the bf16 values of key half s / 4 over its 64 S
+          // columns, the rounded parts first and the remainders 32 columns on
+          const uint32_t a = tmem + b * 128 + (s >> 2) * 64 + (s & 3) * 8;
+          const uint64_t bk = sdesc_mn(ks + s * 2048, TILE / 2, 1024);
+          tc::mma_ts(tmem + COL_DQ, a, bk, id, (u > 0 || s > 0) ? 1u : 0u);
+          if (lo) tc::mma_ts(tmem + COL_DQ, a + 32, bk, id, 1u);
         }
-        __syncwarp();
+        tc::commit(bar(QB_DQDONE + b));
+        tc::commit(bar(QB_KEMPTY + sk));
+        if (u == n_kt - 1) tc::commit(bar(QB_ADONE));
       }
+      __syncwarp();
     }
   }
   if (warp < kSoftWarps) {
     // ------------------------------------------------------------------ softmax warps
-    // TMEM lanes 32 (warp % 4) .. are this warp's rows; kh: its half of the 64 keys
+    // TMEM lanes 32 (warp % 4) .. are this warp's rows; kh: its half of every tile's keys
     __shared__ float s_dd[2][kTileRows];  // D = dO . o, the two halves of d
     const int row = (warp & 3) * 32 + lane, kh = warp >> 2, slot = row / R, hd = row % R;
     const int t = t0 + slot;
@@ -844,20 +872,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tl = key_lo(p, t), tb = valid ? key_bound(p, t, Lk) : -1;
     bool ok = true;
     for (int u = 0; u < n_kt; ++u) {
-      const int bu = u & 1;
-      if (!(ok = tc::warp_wait(bar(QB_SFULL + bu), (u >> 1) & 1, abort))) break;
+      const int b = u & 1;
+      if (!(ok = tc::warp_wait(bar(QB_SFULL + b), (u >> 1) & 1, abort))) break;
       tc::fence_after();
-      float sv[32], dpv[32];
-      tc::tmem_ld32_nowait(t_lane + bu * 128 + kh * 32, sv);
-      tc::tmem_ld32_nowait(t_lane + bu * 128 + 64 + kh * 32, dpv);
+      float sv[64], dpv[64];
+      const uint32_t sc = t_lane + b * 128 + kh * 64;  // this thread's S (then dS) columns
+      tc::tmem_ld32_nowait(sc, sv);
+      tc::tmem_ld32_nowait(sc + 32, sv + 32);
+      tc::tmem_ld32_nowait(t_lane + COL_DP + kh * 64, dpv);
+      tc::tmem_ld32_nowait(t_lane + COL_DP + kh * 64 + 32, dpv + 32);
       tc::tmem_wait_ld();
       tc::fence_before();
-      tc::mbar_arrive(bar(QB_SFREE + bu));
-      const int k0 = (int)((a_lo + u) * KT - kv0) + kh * 32;  // key of sv[0] within the sequence
-      uint32_t hi[16], lo[16];
+      tc::mbar_arrive(bar(QB_DPFREE));
+      const int k0 = (int)((a_lo + u) * KT - kv0) + kh * 64;  // key of sv[0] within the sequence
+      uint32_t hi[32], lo[32];
       float smax = 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
+      for (int e = 0; e < 64; e += 2) {
         const int k = k0 + e;
         const float p0 = k >= tl && k <= tb ? ex2(sv[e] * p.scale_log2 - lse2) : 0.f;
         const float p1 = k + 1 >= tl && k + 1 <= tb ? ex2(sv[e + 1] * p.scale_log2 - lse2) : 0.f;
@@ -865,21 +896,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
         split_bf16x2(d0, d1, hi[e / 2], lo[e / 2]);
       }
-      // the dS buffer is free once the dQ product of tile u - 2 is done
-      if (u >= 2 && !(ok = tc::warp_wait(bar(QB_DQDONE + bu), ((u - 2) >> 1) & 1, abort))) break;
       {
         const unsigned bs = __ballot_sync(0xffffffffu, smax > kLoS);
-        if (lane == 0) s_need[bu][warp] = bs ? 1 : 0;
+        if (lane == 0) s_need[b][warp] = bs ? 1 : 0;
       }
-      tc::fence_after();
-      tmem_st16(t_lane + COL_DS + bu * 64 + kh * 16, hi);
-      tmem_st16(t_lane + COL_DS + bu * 64 + 32 + kh * 16, lo);
-      asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+      // dS over this thread's own S columns (already read): the MMA warp reuses the
+      // buffer only after the dQ product of this tile
+      tc::tmem_st32(sc, hi);  // (waits for its stores)
+      tc::tmem_st32(sc + 32, lo);
       tc::fence_before();
-      tc::mbar_arrive(bar(QB_DSFULL + bu));
+      tc::mbar_arrive(bar(QB_DSFULL + b));
     }
     // ------------------------------------------------------------------ epilogue
-    // both buffers' last products are done (the second wait only drains its arrival)
+    // every product is done; then the last arrivals on both dQ barriers land (their
+    // earlier phases were observed by the MMA warp)
+    if (ok && n_kt > 0) ok = tc::warp_wait(bar(QB_ADONE), 0, abort);
     if (ok && n_kt > 0) ok = tc::warp_wait(bar(QB_DQDONE + ((n_kt - 1) & 1)), ((n_kt - 1) >> 1) & 1, abort);
     if (ok && n_kt > 1) ok = tc::warp_wait(bar(QB_DQDONE + ((n_kt - 2) & 1)), ((n_kt - 2) >> 1) & 1, abort);
     if (ok) {
@@ -910,9 +941,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // copies and tensor-core work still in flight land before the CTA leaves
     if (warp == kProducer) {
       if (n_kt > 0) tc::warp_drain(bar(QB_Q), 0);
-      for (int st = 0; st < NS; ++st) {
-        const int i = last_kv - ((last_kv - st) % NS + NS) % NS;  // last tile handed to stage st
-        if (i >= 0) tc::warp_drain(bar(QB_KVFULL + st), (i / NS) & 1);
+      for (int st = 0; st < NK; ++st) {
+        const int i = last_k - ((last_k - st) % NK + NK) % NK;  // last K tile handed to stage st
+        if (i >= 0) tc::warp_drain(bar(QB_KFULL + st), (i / NK) & 1);
+      }
+      for (int st = 0; st < NV; ++st) {
+        const int i = last_v - ((last_v - st) % NV + NV) % NV;
+        if (i >= 0) tc::warp_drain(bar(QB_VFULL + st), (i / NV) & 1);
       }
     } else if (warp == kIssuer) {
       if (lane == 0) tc::commit(bar(QB_DRAIN));
@@ -921,9 +956,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kProducer) {
     // the MMA warp's last release of each stage lands before the CTA leaves
-    for (int st = 0; st < NS; ++st) {
-      const int i = last_kv - ((last_kv - st) % NS + NS) % NS;
-      if (i >= 0) tc::warp_drain(bar(QB_KVEMPTY + st), (i / NS) & 1);
+    for (int st = 0; st < NK; ++st) {
+      const int i = last_k - ((last_k - st) % NK + NK) % NK;
+      if (i >= 0) tc::warp_drain(bar(QB_KEMPTY + st), (i / NK) & 1);
+    }
+    for (int st = 0; st < NV; ++st) {
+      const int i = last_v - ((last_v - st) % NV + NV) % NV;
+      if (i >= 0) tc::warp_drain(bar(QB_VEMPTY + st), (i / NV) & 1);
     }
   }
   tc::fence_before();
