@@ -656,6 +656,28 @@ enum : int {
 };
 }  // namespace dqk
 
+// dS of 64 keys of a row from S and dP (P from the forward's base-2 normaliser lse2),
+// as bf16 values and remainders; MASK: keys outside [tl, tb] give 0.  Returns max |dS|.
+template <bool MASK>
+__device__ __forceinline__ float form_ds(const float (&sv)[64], const float (&dpv)[64], int k0, int tl, int tb,
+                                         float scale_log2, float lse2, float dsum, uint32_t (&hi)[32],
+                                         uint32_t (&lo)[32]) {
+  float smax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    float p0 = ex2(fmaf(sv[e], scale_log2, -lse2)), p1 = ex2(fmaf(sv[e + 1], scale_log2, -lse2));
+    if (MASK) {
+      const int k = k0 + e;
+      p0 = k >= tl && k <= tb ? p0 : 0.f;
+      p1 = k + 1 >= tl && k + 1 <= tb ? p1 : 0.f;
+    }
+    const float d0 = p0 * (dpv[e] - dsum), d1 = p1 * (dpv[e + 1] - dsum);
+    smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
+    split_bf16x2(d0, d1, hi[e / 2], lo[e / 2]);
+  }
+  return smax;
+}
+
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -886,16 +908,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(bar(QB_DPFREE));
       const int k0 = (int)((a_lo + u) * KT - kv0) + kh * 64;  // key of sv[0] within the sequence
       uint32_t hi[32], lo[32];
-      float smax = 0.f;
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const int k = k0 + e;
-        const float p0 = k >= tl && k <= tb ? ex2(sv[e] * p.scale_log2 - lse2) : 0.f;
-        const float p1 = k + 1 >= tl && k + 1 <= tb ? ex2(sv[e + 1] * p.scale_log2 - lse2) : 0.f;
-        const float d0 = p0 * (dpv[e] - dsum), d1 = p1 * (dpv[e + 1] - dsum);
-        smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
-        split_bf16x2(d0, d1, hi[e / 2], lo[e / 2]);
-      }
+      // every key of the warp's 64 inside every row's range: no per-key mask (fewer
+      // instructions on the schedulers the MMA warp shares)
+      const float smax = __all_sync(0xffffffffu, k0 >= tl && k0 + 63 <= tb)
+                             ? form_ds<false>(sv, dpv, k0, tl, tb, p.scale_log2, lse2, dsum, hi, lo)
+                             : form_ds<true>(sv, dpv, k0, tl, tb, p.scale_log2, lse2, dsum, hi, lo);
       {
         const unsigned bs = __ballot_sync(0xffffffffu, smax > kLoS);
         if (lane == 0) s_need[b][warp] = bs ? 1 : 0;
