@@ -237,6 +237,44 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint32_t (&v)[
                : "memory");
 }
 
+// P and dS of 32 keys of a gathered row (keys 64 j + 32 kh ..), as bf16 values and
+// remainders into the four shared-memory tiles (the row's 16-byte chunks c8 = 4 kh + cc,
+// 128-byte swizzled); MASK: keys outside [tl, tb] give 0.  Keeps the row's max P, |dS|.
+struct PdsArgs {
+  float fm, scale_log2, lse2, dsum;
+  int tl, tb, kb0, row, kh;
+  uint32_t p_hi, p_lo, s_hi, s_lo;
+};
+template <bool MASK>
+__device__ __forceinline__ void form_pds(const float (&sv)[32], const float (&dpv)[32], const PdsArgs& a, float& pmax,
+                                         float& smax) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {  // keys 8 c8 .. 8 c8 + 7 (one 16-byte chunk), c8 = 4 kh + cc
+    const int c8 = a.kh * 4 + cc;
+    uint32_t ph[4], pl[4], sh[4], sl[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float p0 = a.fm * ex2(fmaf(sv[cc * 8 + e], a.scale_log2, -a.lse2));
+      float p1 = a.fm * ex2(fmaf(sv[cc * 8 + e + 1], a.scale_log2, -a.lse2));
+      if (MASK) {
+        const int k0 = a.kb0 + c8 * 8 + e;
+        p0 = k0 <= a.tb && k0 >= a.tl ? p0 : 0.f;
+        p1 = k0 + 1 <= a.tb && k0 + 1 >= a.tl ? p1 : 0.f;
+      }
+      const float d0 = p0 * (dpv[cc * 8 + e] - a.dsum), d1 = p1 * (dpv[cc * 8 + e + 1] - a.dsum);
+      pmax = fmaxf(pmax, fmaxf(p0, p1));
+      smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
+      split_bf16x2(p0, p1, ph[e / 2], pl[e / 2]);
+      split_bf16x2(d0, d1, sh[e / 2], sl[e / 2]);
+    }
+    const uint32_t off = a.row * 128 + ((c8 ^ (a.row & 7)) << 4);
+    st_shared_v4(a.p_hi + off, ph);
+    st_shared_v4(a.p_lo + off, pl);
+    st_shared_v4(a.s_hi + off, sh);
+    st_shared_v4(a.s_lo + off, sl);
+  }
+}
+
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -524,29 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(bar(B_SFREE + s));
       // the P buffer is free once the previous tile's dV / dK products are done
       if (pn > 0 && !(ok = tc::warp_wait(bar(B_PFREE), (pn - 1) & 1, abort))) break;
-      const float fm = (float)mult;
       float pmax = 0.f, smax = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {  // keys 8 c8 .. 8 c8 + 7 (one 16-byte chunk), c8 = 4 kh + cc
-        const int c8 = kh * 4 + cc;
-        uint32_t ph[4], pl[4], sh[4], sl[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int k0 = j * kBS + c8 * 8 + e;
-          const float p0 = k0 <= tb && k0 >= tl ? fm * ex2(sv[cc * 8 + e] * p.scale_log2 - lse2) : 0.f;
-          const float p1 = k0 + 1 <= tb && k0 + 1 >= tl ? fm * ex2(sv[cc * 8 + e + 1] * p.scale_log2 - lse2) : 0.f;
-          const float d0 = p0 * (dpv[cc * 8 + e] - dsum), d1 = p1 * (dpv[cc * 8 + e + 1] - dsum);
-          pmax = fmaxf(pmax, fmaxf(p0, p1));
-          smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
-          split_bf16x2(p0, p1, ph[e / 2], pl[e / 2]);
-          split_bf16x2(d0, d1, sh[e / 2], sl[e / 2]);
-        }
-        const uint32_t off = row * 128 + ((c8 ^ (row & 7)) << 4);
-        st_shared_v4(p_hi + off, ph);
-        st_shared_v4(p_lo + off, pl);
-        st_shared_v4(s_hi + off, sh);
-        st_shared_v4(s_lo + off, sl);
-      }
+      // every key of the warp's 32 inside every row's range (the usual case: blocks before
+      // the row's own): no per-key mask
+      const int kw = j * kBS + kh * 32;
+      const PdsArgs pa{(float)mult, p.scale_log2, lse2, dsum, tl, tb, j * kBS, row, kh, p_hi, p_lo, s_hi, s_lo};
+      if (__all_sync(0xffffffffu, kw >= tl && kw + 31 <= tb))
+        form_pds<false>(sv, dpv, pa, pmax, smax);
+      else
+        form_pds<true>(sv, dpv, pa, pmax, smax);
       {  // which remainder products this warp's rows need (read by the MMA warp after PFULL)
         const unsigned bp = __ballot_sync(0xffffffffu, pmax > kLoP), bs = __ballot_sync(0xffffffffu, smax > kLoS);
         if (lane == 0) s_need[warp] = (bp ? 1 : 0) | (bs ? 2 : 0);
