@@ -654,9 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S values in registers), one dP buffer and the dQ accumulator: 4 x 128 columns.
 // The kernel also stores D = dO . o per row, which the dK / dV kernel reads.  Roles as
 // in dkv_tc_kernel: warp 8 loads Q and dO once and streams K tiles through a three-stage
-// and V tiles through a two-stage ring (V is free once dP is done), warp 9 issues the
-// MMAs (S and dP of the next tile while the softmax warps work on this one), warps 0-7
-// (rows 32 (w % 4) .., keys 64 (w / 4) .. of every tile) form dS and finally store dQ.
+// and V tiles through a two-stage ring (V is free once dP is done), warp 9 issues S and
+// dP (of the next tile while the softmax warps work on this one), warp 10 the dQ
+// products, warps 0-7 (rows 32 (w % 4) .., keys 64 (w / 4) .. of every tile) form dS and
+// finally store dQ.
 namespace dqk {
 constexpr int KT = 128;                // keys per tile
 constexpr int NK = 3, NV = 2;          // K and V ring stages
@@ -702,8 +703,10 @@ __device__ __forceinline__ float form_ds(const float (&sv)[64], const float (&dp
   return smax;
 }
 
+constexpr int kQIssuer = kSoftWarps + 2, kQThreads = kThreads + 32;  // dq_tc: a second issuing warp
+
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kQThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const BwdParams p) {
@@ -749,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(bar(QB_DPFREE), kSoft);
     tc::mbar_init(bar(QB_ADONE), 1);
-    tc::mbar_init(bar(QB_DRAIN), 1);
+    tc::mbar_init(bar(QB_DRAIN), 2);  // both issuing warps
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -819,10 +822,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == kIssuer && n_kt > 0) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S / dP issuer
     // Per tile u: S and dP of tile u + 1 (S into buffer (u + 1) % 2 once dQ of tile u - 1,
-    // which read the dS over that buffer, is done; dP once the softmax warps hold dP(u)),
-    // then dQ += dS K of tile u once its dS is written.
+    // which read the dS over that buffer, is done; dP once the softmax warps hold dP(u)).
     constexpr uint32_t id_s = tc::idesc(128, KT);
     auto issue_s = [&](int j) -> bool {  // warp-uniform
       const int sk = j % NK;
@@ -859,11 +861,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = tc::warp_wait(bar(QB_Q), 0, abort);
     if (ok) ok = issue_s(0) && issue_dp(0);
+    for (int u = 0; ok && u + 1 < n_kt; ++u) {
+      if (u >= 1 && !(ok = tc::warp_wait(bar(QB_DQDONE + ((u - 1) & 1)), ((u - 1) >> 1) & 1, abort))) break;
+      ok = issue_s(u + 1) && issue_dp(u + 1);
+    }
+  }
+  if (warp == kQIssuer && n_kt > 0) {
+    // ------------------------------------------------------------------ dQ issuer
+    // dQ += dS K of tile u once its dS is written.  A second issuing warp, on another
+    // scheduler: an issuing lane that shares its scheduler with two computing softmax
+    // warps gets few issue slots (measured with eight FMA-bound warps beside it: 158 - 178
+    // cycles per product against 68 - 71 alone), so S / dP and dQ issue in parallel.
+    bool ok = true;
     for (int u = 0; ok && u < n_kt; ++u) {
-      if (u + 1 < n_kt) {
-        if (u >= 1 && !(ok = tc::warp_wait(bar(QB_DQDONE + ((u - 1) & 1)), ((u - 1) >> 1) & 1, abort))) break;
-        if (!(ok = issue_s(u + 1) && issue_dp(u + 1))) break;
-      }
       const int b = u & 1, sk = u % NK;
       if (!(ok = tc::warp_wait(bar(QB_DSFULL + b), (u >> 1) & 1, abort))) break;
       if (lane == 0) {  // lane 0 observed the dS arrival: it reads the warps' flags
@@ -990,13 +1000,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = last_v - ((last_v - st) % NV + NV) % NV;
         if (i >= 0) tc::warp_drain(bar(QB_VFULL + st), (i / NV) & 1);
       }
-    } else if (warp == kIssuer) {
+    } else if (warp == kIssuer || warp == kQIssuer) {
       if (lane == 0) tc::commit(bar(QB_DRAIN));
       __syncwarp();
       tc::warp_drain(bar(QB_DRAIN), 0);
     }
   } else if (warp == kProducer) {
-    // the MMA warp's last release of each stage lands before the CTA leaves
+    // the MMA warps' last release of each stage lands before the CTA leaves
     for (int st = 0; st < NK; ++st) {
       const int i = last_k - ((last_k - st) % NK + NK) % NK;
       if (i >= 0) tc::warp_drain(bar(QB_KEMPTY + st), (i / NK) & 1);
@@ -1074,7 +1084,7 @@ cudaError_t launch_dq_tc(const BwdParams& p, int64_t kv_rows, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dqk::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((s.max_len + tpc - 1) / tpc), (unsigned)s.n_seqs, (unsigned)p.hkv);
-  kern<<<grid, kThreads, dqk::SMEM, st>>>(mq, mdo, mk, mv, p);
+  kern<<<grid, kQThreads, dqk::SMEM, st>>>(mq, mdo, mk, mv, p);
   return cudaGetLastError();
 }
 
