@@ -654,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S values in registers), one dP buffer and the dQ accumulator: 4 x 128 columns.
 // The kernel also stores D = dO . o per row, which the dK / dV kernel reads.  Roles as
 // in dkv_tc_kernel: warp 8 loads Q and dO once and streams K tiles through a three-stage
-// and V tiles through a two-stage ring (V is free once dP is done), warp 9 issues S and
-// dP (of the next tile while the softmax warps work on this one), warp 10 the dQ
+// and V tiles through a two-stage ring (V is free once dP is done), warps 9 and 11 issue
+// S and dP (of the next tile while the softmax warps work on this one), warp 10 the dQ
 // products, warps 0-7 (rows 32 (w % 4) .., keys 64 (w / 4) .. of every tile) form dS and
 // finally store dQ.
 namespace dqk {
@@ -703,7 +703,8 @@ __device__ __forceinline__ float form_ds(const float (&sv)[64], const float (&dp
   return smax;
 }
 
-constexpr int kQIssuer = kSoftWarps + 2, kQThreads = kThreads + 32;  // dq_tc: a second issuing warp
+// dq_tc: issuing warps of the dQ and the dP products beside the S issuer (kIssuer)
+constexpr int kQIssuer = kSoftWarps + 2, kPIssuer = kSoftWarps + 3, kQThreads = kThreads + 64;
 
 template <int R>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -746,13 +747,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       tc::mbar_init(bar(QB_VEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(bar(QB_SFULL + i), 1);
+      tc::mbar_init(bar(QB_SFULL + i), 2);  // the S and the dP issuer
       tc::mbar_init(bar(QB_DSFULL + i), kSoft);
       tc::mbar_init(bar(QB_DQDONE + i), 1);
     }
     tc::mbar_init(bar(QB_DPFREE), kSoft);
     tc::mbar_init(bar(QB_ADONE), 1);
-    tc::mbar_init(bar(QB_DRAIN), 2);  // both issuing warps
+    tc::mbar_init(bar(QB_DRAIN), 3);  // the three issuing warps
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -821,10 +822,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
   }
 
-  if (warp == kIssuer && n_kt > 0) {
-    // ------------------------------------------------------------------ S / dP issuer
-    // Per tile u: S and dP of tile u + 1 (S into buffer (u + 1) % 2 once dQ of tile u - 1,
-    // which read the dS over that buffer, is done; dP once the softmax warps hold dP(u)).
+  if ((warp == kIssuer || warp == kPIssuer) && n_kt > 0) {
+    // ------------------------------------------------------------------ S and dP issuers
+    // Warp 9 issues S of tile u + 1 into buffer (u + 1) % 2 once dQ of tile u - 1, which
+    // read the dS over that buffer, is done; warp 11 issues dP(u + 1) once the softmax
+    // warps hold dP(u).  Each commits the tile's SFULL (two arrivals).
     constexpr uint32_t id_s = tc::idesc(128, KT);
     auto issue_s = [&](int j) -> bool {  // warp-uniform
       const int sk = j % NK;
@@ -837,6 +839,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           const uint32_t ao = (k >> 2) * (QB / 2) + (k & 3) * 32, bo = (k >> 2) * (TILE / 2) + (k & 3) * 32;
           tc::mma_ss(tmem + (j & 1) * 128, tc::sdesc(q_s + ao), tc::sdesc(ks + bo), id_s, k > 0);
         }
+        tc::commit(bar(QB_SFULL + (j & 1)));
       }
       __syncwarp();
       return true;
@@ -860,10 +863,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
       return true;
     };
     bool ok = tc::warp_wait(bar(QB_Q), 0, abort);
-    if (ok) ok = issue_s(0) && issue_dp(0);
-    for (int u = 0; ok && u + 1 < n_kt; ++u) {
-      if (u >= 1 && !(ok = tc::warp_wait(bar(QB_DQDONE + ((u - 1) & 1)), ((u - 1) >> 1) & 1, abort))) break;
-      ok = issue_s(u + 1) && issue_dp(u + 1);
+    if (warp == kIssuer) {  // S
+      if (ok) ok = issue_s(0);
+      for (int u = 0; ok && u + 1 < n_kt; ++u) {
+        if (u >= 1 && !(ok = tc::warp_wait(bar(QB_DQDONE + ((u - 1) & 1)), ((u - 1) >> 1) & 1, abort))) break;
+        ok = issue_s(u + 1);
+      }
+    } else {  // dP
+      for (int u = 0; ok && u < n_kt; ++u) ok = issue_dp(u);
     }
   }
   if (warp == kQIssuer && n_kt > 0) {
@@ -1000,7 +1007,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const int i = last_v - ((last_v - st) % NV + NV) % NV;
         if (i >= 0) tc::warp_drain(bar(QB_VFULL + st), (i / NV) & 1);
       }
-    } else if (warp == kIssuer || warp == kQIssuer) {
+    } else if (warp == kIssuer || warp == kQIssuer || warp == kPIssuer) {
       if (lane == 0) tc::commit(bar(QB_DRAIN));
       __syncwarp();
       tc::warp_drain(bar(QB_DRAIN), 0);
