@@ -10,12 +10,14 @@
 //
 // GB300 design.  A CTA takes 128 (token, head) rows of one kv-group (8 tokens x 16 heads
 // at group size 16): they share every K/V tile, so the contraction is an M = 128 GEMM.
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warp 4      TMA producer: Q once (a 3-D box of tokens x heads x d), then 64-key K
 //               tiles and V^T tiles through 2-stage rings (128B-swizzled, K-major);
-//   warp 5      MMA issuer (one lane): S(j) = Q K(j)^T into one of two TMEM S buffers,
-//               issued while the softmax of tile j-1 runs, then O += P(j-1) V(j-1) with
-//               P read from TMEM;
+//   warp 5      S issuer (one lane): S(j) = Q K(j)^T into one of two TMEM S buffers,
+//               issued while the softmax of tile j-1 runs;
+//   warp 6      PV issuer: O += P(j) V(j) with P read from TMEM (a second issuing warp, on
+//               another scheduler, since an issuing lane beside computing softmax warps
+//               gets few issue slots);
 //   warps 0..3  softmax, one row per thread (TMEM lane = row): mask, running max with
 //               lazy rescale, base-2 exponentials, P (bf16) stored over its S buffer.
 // Pass 2 (compressed branch with block scores): the issuer recomputes S over 64-key
@@ -37,7 +39,9 @@ constexpr int D = 128;
 constexpr int ROWS = 128;  // query rows per CTA (= tcgen05 M)
 constexpr int KT = 64;     // keys per tile
 constexpr int NS = 2;      // K / V^T ring stages
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;
+// scores-only mode: no PV, so no PV issuer (warp 6)
+constexpr int nthreads(int mode) { return mode == 2 ? NTHREADS - 32 : NTHREADS; }
 constexpr int Q_BYTES = ROWS * D * 2;  // two 64-column halves of 16 KB
 constexpr int K_BYTES = KT * D * 2;    // two halves of 8 KB
 constexpr int V_BYTES = D * KT * 2;    // V^T tile: 128 d-rows of 64 keys
@@ -124,7 +128,7 @@ __device__ __forceinline__ int last_in_stage(int last, int st) {
 //         query blocks): the key tiles are the 64-key blocks active for either query
 //         block; each row masks the tiles its own block does not list.
 template <int MODE, int RS>
-__global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
+__global__ void __launch_bounds__(nthreads(MODE), MODE == 2 ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
     const int qb0 = t0 / KT, nbw = (p.n_qb + 3) / 4 * 4;
     const bool two = t0 + KT < L;
     const uint8_t* m0 = p.bmask + (((int64_t)sq * p.h + g) * p.n_qb + qb0) * p.n_qb;
-    for (int kb = tid; kb < nbw; kb += NTHREADS) {
+    for (int kb = tid; kb < nbw; kb += nthreads(MODE)) {
       int f = 0;
       if (kb < p.n_qb) {
         if (m0[kb] && (!p.causal || kb <= qb0)) f |= 1;
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
       mbar_init(bar(B_PFULL + i), 128);
       mbar_init(bar(B_ODONE + i), 1);
     }
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN), MODE == 2 ? 1 : 2);  // the S and the PV issuer
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -303,41 +307,23 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
         __syncwarp();
       }
     }
-    for (int kt = -1; MODE != 2 && ok && kt < n_kt; ++kt) {
-      const int j = kt + 1;
-      if (j < n_kt) {
-        // S buffer j & 1 was last read by PV(j - 2)
-        if (j >= 2) ok = warp_wait(bar(B_ODONE + (j & 1)), ((j - 2) >> 1) & 1, abort);
-        if (ok) ok = warp_wait(bar(B_KFULL + j % NS), (j / NS) & 1, abort);
-        if (!ok) break;
-        if (lane == 0) {
-          fence_after();
-          const uint32_t ks = k_s + (j % NS) * K_BYTES;
+    // S(j) of the attention pass; PV is issued by warp 6
+    for (int j = 0; MODE != 2 && ok && j < n_kt; ++j) {
+      // S buffer j & 1 was last read by PV(j - 2)
+      if (j >= 2) ok = warp_wait(bar(B_ODONE + (j & 1)), ((j - 2) >> 1) & 1, abort);
+      if (ok) ok = warp_wait(bar(B_KFULL + j % NS), (j / NS) & 1, abort);
+      if (!ok) break;
+      if (lane == 0) {
+        fence_after();
+        const uint32_t ks = k_s + (j % NS) * K_BYTES;
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s)
-            mma_ss(tmem + (j & 1) * KT, sdesc(q_s + (s >> 2) * (Q_BYTES / 2) + (s & 3) * 32),
-                   sdesc(ks + (s >> 2) * (K_BYTES / 2) + (s & 3) * 32), idesc(ROWS, KT), s > 0);
-          commit(bar(B_SFULL + (j & 1)));
-          commit(bar(B_KEMPTY + j % NS));
-        }
-        __syncwarp();
+        for (int s = 0; s < D / 16; ++s)
+          mma_ss(tmem + (j & 1) * KT, sdesc(q_s + (s >> 2) * (Q_BYTES / 2) + (s & 3) * 32),
+                 sdesc(ks + (s >> 2) * (K_BYTES / 2) + (s & 3) * 32), idesc(ROWS, KT), s > 0);
+        commit(bar(B_SFULL + (j & 1)));
+        commit(bar(B_KEMPTY + j % NS));
       }
-      if (kt >= 0) {
-        ok = warp_wait(bar(B_PFULL + (kt & 1)), (kt >> 1) & 1, abort);
-        if (ok) ok = warp_wait(bar(B_VFULL + kt % NS), (kt / NS) & 1, abort);
-        if (!ok) break;
-        if (lane == 0) {
-          fence_after();
-          const uint32_t vs = v_s + (kt % NS) * V_BYTES;
-#pragma unroll
-          for (int s = 0; s < KT / 16; ++s)
-            mma_ts(tmem + O_COL, tmem + (kt & 1) * KT + s * 8, sdesc(vs + s * 32), idesc(ROWS, D),
-                   (kt > 0 || s > 0) ? 1u : 0u);
-          commit(bar(B_ODONE + (kt & 1)));
-          commit(bar(B_VEMPTY + kt % NS));
-        }
-        __syncwarp();
-      }
+      __syncwarp();
     }
     for (int i = 0; MODE != 2 && ok && i < n_kt2; ++i) {
       const int j = n_kt + i, b = j & 1;
@@ -356,6 +342,28 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
                  sdesc(ks + (s >> 2) * (K_BYTES / 2) + (s & 3) * 32), idesc(ROWS, KT), s > 0);
         commit(bar(B_SFULL + b));
         commit(bar(B_KEMPTY + j % NS));
+      }
+      __syncwarp();
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------------ PV issuer
+    // O += P(kt) V(kt) once the softmax warps wrote P(kt).  A second issuing warp, on
+    // another scheduler than the S issuer: an issuing lane that shares its scheduler with
+    // computing softmax warps gets few issue slots.
+    bool ok = true;
+    for (int kt = 0; MODE != 2 && ok && kt < n_kt; ++kt) {
+      ok = warp_wait(bar(B_PFULL + (kt & 1)), (kt >> 1) & 1, abort);
+      if (ok) ok = warp_wait(bar(B_VFULL + kt % NS), (kt / NS) & 1, abort);
+      if (!ok) break;
+      if (lane == 0) {
+        fence_after();
+        const uint32_t vs = v_s + (kt % NS) * V_BYTES;
+#pragma unroll
+        for (int s = 0; s < KT / 16; ++s)
+          mma_ts(tmem + O_COL, tmem + (kt & 1) * KT + s * 8, sdesc(vs + s * 32), idesc(ROWS, D),
+                 (kt > 0 || s > 0) ? 1u : 0u);
+        commit(bar(B_ODONE + (kt & 1)));
+        commit(bar(B_VEMPTY + kt % NS));
       }
       __syncwarp();
     }
@@ -555,7 +563,7 @@ __global__ void __launch_bounds__(NTHREADS, MODE == 2 ? 3 : 2)
         if (ik >= 0) mbar_drain(bar(B_KFULL + st), (ik / NS) & 1);
         if (iv >= 0) mbar_drain(bar(B_VFULL + st), (iv / NS) & 1);
       }
-    } else if (warp == 5) {
+    } else if (warp == 5 || warp == 6) {
       if (lane == 0) commit(bar(B_DRAIN));
       __syncwarp();
       mbar_drain(bar(B_DRAIN), 0);
@@ -623,7 +631,7 @@ static cudaError_t run_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   constexpr int smem = MODE == 2 ? tc::SMEM_BYTES_SCORES : tc::SMEM_BYTES + (MODE == 3 ? 1024 : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, tc::NTHREADS, smem, st>>>(mq, mk, mv, p);
+  kern<<<grid, tc::nthreads(MODE), smem, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
