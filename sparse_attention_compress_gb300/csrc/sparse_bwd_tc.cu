@@ -18,10 +18,12 @@
 // enter the second products as bf16 pairs (the rounded value and its remainder, so the
 // operand carries about 16 bits), as in sparse_bwd_dkv.  Roles: warp 8 takes the tokens
 // that reach j and gathers their Q and dO rows by TMA into a two-stage ring; warp 9
-// issues the MMAs (S and dP into one of two TMEM buffers, so the next tile's products run
-// while the softmax warps work on this one); warps 0-7, two per scheduler, form P and dS
-// (each a half of every row's 64 keys) and finally read dK^T and dV^T out of TMEM.  One
-// CTA per SM (224 KB of shared memory).
+// issues S and dP (into one of two TMEM buffers, so the next tile's products run while
+// the softmax warps work on this one) and warp 10 the dV / dK products (two issuing warps
+// on different schedulers: an issuing lane beside computing softmax warps gets few issue
+// slots); warps 0-7, two per scheduler, form P and dS (each a half of every row's 64
+// keys) and finally read dK^T and dV^T out of TMEM.  One CTA per SM (224 KB of shared
+// memory).
 #include <algorithm>
 
 #include "sm100.cuh"
@@ -64,8 +66,10 @@ enum : int {
   B_PFREE = 10,  // the dV / dK products of that tile are done
   B_ADONE = 11,  // every product of the item is done
   B_DRAIN = 12,
-  B_COUNT = 13
+  B_SDONE = 13,  // the S / dP issuer saw the list's last tile (the row-tile count is in s_nrows)
+  B_COUNT = 14
 };
+constexpr int kDvIssuer = kSoftWarps + 2, kKVThreads = kThreads + 32;  // dkv_tc: the dV / dK issuer
 
 // Shared-memory descriptor of an MN-major tile with 128-byte swizzling: rows of 64
 // MN-elements (128 B) along K, 1024-byte atoms of 8 K-rows.  lbo: byte distance between
@@ -276,7 +280,7 @@ __device__ __forceinline__ void form_pds(const float (&sv)[32], const float (&dp
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKVThreads, 1)
     dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
   constexpr int TPT = kTileRows / R;  // tokens per tile
@@ -284,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t s_bar[B_COUNT];
   __shared__ int s_meta[2][TPT + 2];  // per stage: (token << 7 | multiplicity) per slot, count, last
   __shared__ int s_need[kSoftWarps];  // per softmax warp, for the tile in the P buffer: remainder products needed
+  __shared__ int s_nrows;             // tiles with rows (written by the S / dP issuer before SDONE)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -319,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(bar(B_PFULL), kSoft);
     tc::mbar_init(bar(B_PFREE), 1);
     tc::mbar_init(bar(B_ADONE), 1);
-    tc::mbar_init(bar(B_DRAIN), 1);
+    tc::mbar_init(bar(B_DRAIN), 2);  // both issuing warps
+    tc::mbar_init(bar(B_SDONE), 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -411,30 +417,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
-  int pn = 0;  // MMA warp and softmax warps: tiles whose P and dS went through the P buffer
-  bool adone = false;  // MMA warp: the item's last commit was issued
+  int pn = 0;  // dV / dK issuer and softmax warps: tiles whose P and dS went through the P buffer
+  bool adone = false;  // dV / dK issuer: the item's last commit was issued
   if (warp == kIssuer) {
-    // ------------------------------------------------------------------ MMA issuer
-    // A polling loop (lane 0 probes, the warp follows): the dV / dK products of the oldest
-    // tile whose P and dS are written go first, since they release its stage to the
-    // producer; otherwise S and dP of the next loaded tile once its TMEM buffer is free.
-    // Waits are bounded: without progress for the unit's limit the item gives up.
+    // ------------------------------------------------------------------ S / dP issuer
+    // S and dP of each loaded tile with rows, once its TMEM buffer is free (the softmax
+    // warps read the tile two before); at the list's last tile it publishes the number of
+    // tiles with rows.  The dV / dK products come from a second issuing warp on another
+    // scheduler: an issuing lane that shares its scheduler with computing softmax warps
+    // gets few issue slots.
     bool ok = tc::warp_wait(bar(B_KV), 0, abort);
-    int next_s = 0;        // next tile for S and dP
-    int n_rows_tiles = 0;  // tiles with rows whose S and dP were issued
-    bool s_done = false;   // the last tile was seen
-    bool lo_init = false;  // the remainder accumulators hold a first product
+    int n_rows_tiles = 0;
+    for (int next_s = 0; ok; ++next_s) {
+      const int s = next_s & 1;
+      if (!(ok = tc::warp_wait(bar(B_FULL + s), (next_s >> 1) & 1, abort))) break;
+      int cnt = 0, last = 0;  // every lane observed the stage's arrival
+      cnt = s_meta[s][TPT];
+      last = s_meta[s][TPT + 1];
+      if (cnt > 0) {
+        if (next_s >= 2 && !(ok = tc::warp_wait(bar(B_SFREE + s), ((next_s - 2) >> 1) & 1, abort))) break;
+        if (lane == 0) {
+          tc::fence_after();
+          const uint32_t qs = stage0 + s * kStageBytes, ds = qs + kQBytes;
+          constexpr uint32_t id = tc::idesc(128, kBS);
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t ao = (k >> 2) * kHalfRows + (k & 3) * 32, bo = (k >> 2) * (kKVBytes / 2) + (k & 3) * 32;
+            tc::mma_ss(tmem + s * 128, tc::sdesc(qs + ao), tc::sdesc(kt + bo), id, k > 0);
+            tc::mma_ss(tmem + s * 128 + 64, tc::sdesc(ds + ao), tc::sdesc(vt + bo), id, k > 0);
+          }
+          tc::commit(bar(B_SFULL + s));
+        }
+        __syncwarp();
+        ++n_rows_tiles;
+      }
+      if (last) {
+        if (lane == 0) {
+          s_nrows = n_rows_tiles;
+          tc::mbar_arrive(bar(B_SDONE));  // (release: s_nrows is visible to its observers)
+        }
+        __syncwarp();
+        break;
+      }
+    }
+  }
+  if (warp == kDvIssuer) {
+    // ------------------------------------------------------------------ dV / dK issuer
+    // A polling loop (lane 0 probes, the warp follows): dV / dK of the oldest tile whose P
+    // and dS are written, until the S / dP issuer's count of tiles with rows is reached.
+    // Waits are bounded: without progress for the unit's limit the item gives up.
+    bool ok = true;
+    int n_rows_tiles = -1;  // unknown until SDONE
+    bool lo_init = false;   // the remainder accumulators hold a first product
     unsigned long long t_idle = tc::globaltimer();
     const unsigned long long lim = tc::wait_limit();
     while (ok) {
-      int act = 0;  // 1: dV / dK of tile pn; 2: S and dP of tile next_s
+      int act = 0;  // 1: dV / dK of tile pn; 2: the row-tile count arrived
       if (lane == 0) {
-        if (pn < n_rows_tiles && tc::mbar_test(bar(B_PFULL), pn & 1)) {
+        if ((n_rows_tiles < 0 || pn < n_rows_tiles) && tc::mbar_test(bar(B_PFULL), pn & 1))
           act = 1;
-        } else if (!s_done && tc::mbar_test(bar(B_FULL + (next_s & 1)), (next_s >> 1) & 1) &&
-                   (next_s < 2 || tc::mbar_test(bar(B_SFREE + (next_s & 1)), ((next_s - 2) >> 1) & 1))) {
+        else if (n_rows_tiles < 0 && tc::mbar_test(bar(B_SDONE), 0))
           act = 2;
-        }
       }
       act = __shfl_sync(0xffffffffu, act, 0);
       if (act == 1) {
@@ -467,35 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pn;
         t_idle = tc::globaltimer();
       } else if (act == 2) {
-        const int s = next_s & 1;
-        int cnt = 0, last = 0;  // lane 0 observed the stage's arrival: it reads the list's header
-        if (lane == 0) {
-          cnt = s_meta[s][TPT];
-          last = s_meta[s][TPT + 1];
-        }
-        cnt = __shfl_sync(0xffffffffu, cnt, 0);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (cnt > 0) {
-          if (lane == 0) {
-            tc::fence_after();
-            const uint32_t qs = stage0 + s * kStageBytes, ds = qs + kQBytes;
-            constexpr uint32_t id = tc::idesc(128, kBS);
-#pragma unroll
-            for (int k = 0; k < kD / 16; ++k) {
-              const uint32_t ao = (k >> 2) * kHalfRows + (k & 3) * 32, bo = (k >> 2) * (kKVBytes / 2) + (k & 3) * 32;
-              tc::mma_ss(tmem + s * 128, tc::sdesc(qs + ao), tc::sdesc(kt + bo), id, k > 0);
-              tc::mma_ss(tmem + s * 128 + 64, tc::sdesc(ds + ao), tc::sdesc(vt + bo), id, k > 0);
-            }
-            tc::commit(bar(B_SFULL + s));
-          }
-          __syncwarp();
-          ++n_rows_tiles;
-        }
-        s_done = last != 0;
-        ++next_s;
+        int n = 0;
+        if (lane == 0) n = s_nrows;  // lane 0 observed SDONE
+        n_rows_tiles = __shfl_sync(0xffffffffu, n, 0);
         t_idle = tc::globaltimer();
       } else {
-        if (s_done && pn == n_rows_tiles) {  // every product is issued
+        if (n_rows_tiles >= 0 && pn == n_rows_tiles) {  // every product is issued
           if (lane == 0) tc::commit(bar(B_ADONE));
           __syncwarp();
           adone = true;
@@ -509,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         }
         ok = __all_sync(0xffffffffu, ok);
-        __nanosleep(32);  // leave the issue slots to the softmax warp on this scheduler
+        __nanosleep(32);  // leave the issue slots to the softmax warps on this scheduler
       }
     }
   }
@@ -619,16 +639,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = n_tiles - 1 - ((n_tiles - 1 - s) & 1);  // last tile handed to stage s
         if (i >= 0 && (i & 1) == s) tc::warp_drain(bar(B_FULL + s), (i >> 1) & 1);
       }
-    } else if (warp == kIssuer) {
+    } else if (warp == kIssuer || warp == kDvIssuer) {
       if (lane == 0) tc::commit(bar(B_DRAIN));
       __syncwarp();
       tc::warp_drain(bar(B_DRAIN), 0);
     }
   } else if (warp == kProducer) {
-    // the MMA warp's last release of each stage lands before the CTA leaves
+    // the dV / dK issuer's last release of each stage lands before the CTA leaves
     for (int s = 0; s < 2; ++s)
       if (last_full[s] >= 0) tc::warp_drain(bar(B_EMPTY + s), (last_full[s] >> 1) & 1);
-  } else if (warp == kIssuer) {
+  } else if (warp == kDvIssuer) {
     if (pn > 0) tc::warp_drain(bar(B_PFREE), (pn - 1) & 1);
     if (adone) tc::warp_drain(bar(B_ADONE), 0);
   }
@@ -1057,7 +1077,7 @@ cudaError_t launch_dkv_tc(const BwdParams& p, int64_t items, int64_t q_rows, cud
   auto kern = r == 16 ? dkv_tc_kernel<16> : dkv_tc_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)items, kThreads, kSmemBytes, st>>>(mq, mdo, p);
+  kern<<<(unsigned)items, kKVThreads, kSmemBytes, st>>>(mq, mdo, p);
   return cudaGetLastError();
 }
 
