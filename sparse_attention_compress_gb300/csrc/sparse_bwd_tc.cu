@@ -19,9 +19,9 @@
 // operand carries about 16 bits), as in sparse_bwd_dkv.  Roles: warp 8 takes the tokens
 // that reach j and gathers their Q and dO rows by TMA into a two-stage ring; warp 9
 // issues S and dP (into one of two TMEM buffers, so the next tile's products run while
-// the softmax warps work on this one) and warp 10 the dV / dK products (two issuing warps
-// on different schedulers: an issuing lane beside computing softmax warps gets few issue
-// slots); warps 0-7, two per scheduler, form P and dS (each a half of every row's 64
+// the softmax warps work on this one), warps 10 and 11 the dV and the dK products (issuing
+// warps on different schedulers: an issuing lane beside computing softmax warps gets few
+// issue slots); warps 0-7, two per scheduler, form P and dS (each a half of every row's 64
 // keys) and finally read dK^T and dV^T out of TMEM.  One CTA per SM (224 KB of shared
 // memory).
 #include <algorithm>
@@ -69,7 +69,8 @@ enum : int {
   B_SDONE = 13,  // the S / dP issuer saw the list's last tile (the row-tile count is in s_nrows)
   B_COUNT = 14
 };
-constexpr int kDvIssuer = kSoftWarps + 2, kKVThreads = kThreads + 32;  // dkv_tc: the dV / dK issuer
+// dkv_tc: the dV and the dK issuer (beside the S / dP issuer, kIssuer)
+constexpr int kDvIssuer = kSoftWarps + 2, kDkIssuer = kSoftWarps + 3, kKVThreads = kThreads + 64;
 
 // Shared-memory descriptor of an MN-major tile with 128-byte swizzling: rows of 64
 // MN-elements (128 B) along K, 1024-byte atoms of 8 K-rows.  lbo: byte distance between
@@ -316,15 +317,15 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(B_FULL + i), 1);
-      tc::mbar_init(bar(B_EMPTY + i), 1);
+      tc::mbar_init(bar(B_EMPTY + i), 2);  // the dV and the dK issuer
       tc::mbar_init(bar(B_SFULL + i), 1);
       tc::mbar_init(bar(B_SFREE + i), kSoft);
     }
     tc::mbar_init(bar(B_KV), kSoft);
     tc::mbar_init(bar(B_PFULL), kSoft);
-    tc::mbar_init(bar(B_PFREE), 1);
-    tc::mbar_init(bar(B_ADONE), 1);
-    tc::mbar_init(bar(B_DRAIN), 2);  // both issuing warps
+    tc::mbar_init(bar(B_PFREE), 2);  // the dV and the dK issuer
+    tc::mbar_init(bar(B_ADONE), 2);
+    tc::mbar_init(bar(B_DRAIN), 3);  // the three issuing warps
     tc::mbar_init(bar(B_SDONE), 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -461,11 +462,13 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       }
     }
   }
-  if (warp == kDvIssuer) {
-    // ------------------------------------------------------------------ dV / dK issuer
-    // A polling loop (lane 0 probes, the warp follows): dV / dK of the oldest tile whose P
-    // and dS are written, until the S / dP issuer's count of tiles with rows is reached.
+  if (warp == kDvIssuer || warp == kDkIssuer) {
+    // ------------------------------------------------------------------ dV and dK issuers
+    // A polling loop (lane 0 probes, the warp follows): dV (warp 10) or dK (warp 11) of the
+    // oldest tile whose P and dS are written, until the S / dP issuer's count of tiles with
+    // rows is reached; each commits the P buffer's and the stage's release (two arrivals).
     // Waits are bounded: without progress for the unit's limit the item gives up.
+    const bool is_dk = warp == kDkIssuer;
     bool ok = true;
     int n_rows_tiles = -1;  // unknown until SDONE
     bool lo_init = false;   // the remainder accumulators hold a first product
@@ -490,17 +493,17 @@ __global__ void __launch_bounds__(kKVThreads, 1)
             for (int w = 0; w < kSoftWarps; ++w) lo |= s_need[w];
           }
           tc::fence_after();
-          const uint32_t qs = stage0 + (u & 1) * kStageBytes, ds = qs + kQBytes;
-          // the first tile runs both parts (it initialises the remainder columns); later
-          // tiles only the parts their values need
-          const uint32_t id_v = idesc_mn(128, (lo & 1) ? 2 * kBS : kBS), id_k = idesc_mn(128, (lo & 2) ? 2 * kBS : kBS);
+          // dV^T += dO^T P from the P buffer, or dK^T += Q^T dS from the dS buffer; the first
+          // tile runs both parts (it initialises the remainder columns), later tiles only
+          // the parts their values need
+          const uint32_t qs = stage0 + (u & 1) * kStageBytes, a_s = is_dk ? qs : qs + kQBytes;
+          const uint32_t b_s = is_dk ? s_hi : p_hi, d_col = is_dk ? kColDK : kColDV;
+          const uint32_t id = idesc_mn(128, (lo & (is_dk ? 2 : 1)) ? 2 * kBS : kBS);
 #pragma unroll 1
           for (int k = 0; k < kTileRows / 16; ++k) {
             const uint32_t ro = k * 2048;
             const uint32_t acc = (u > 0 || k > 0) ? 1u : 0u;
-            const uint64_t a_do = sdesc_mn(ds + ro, kHalfRows, 1024), a_q = sdesc_mn(qs + ro, kHalfRows, 1024);
-            tc::mma_ss(tmem + kColDV, a_do, sdesc_mn(p_hi + ro, kPBytes, 1024), id_v, acc);
-            tc::mma_ss(tmem + kColDK, a_q, sdesc_mn(s_hi + ro, kPBytes, 1024), id_k, acc);
+            tc::mma_ss(tmem + d_col, sdesc_mn(a_s + ro, kHalfRows, 1024), sdesc_mn(b_s + ro, kPBytes, 1024), id, acc);
           }
           tc::commit(bar(B_PFREE));
           tc::commit(bar(B_EMPTY + (u & 1)));
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const int i = n_tiles - 1 - ((n_tiles - 1 - s) & 1);  // last tile handed to stage s
         if (i >= 0 && (i & 1) == s) tc::warp_drain(bar(B_FULL + s), (i >> 1) & 1);
       }
-    } else if (warp == kIssuer || warp == kDvIssuer) {
+    } else if (warp == kIssuer || warp == kDvIssuer || warp == kDkIssuer) {
       if (lane == 0) tc::commit(bar(B_DRAIN));
       __syncwarp();
       tc::warp_drain(bar(B_DRAIN), 0);
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     // the dV / dK issuer's last release of each stage lands before the CTA leaves
     for (int s = 0; s < 2; ++s)
       if (last_full[s] >= 0) tc::warp_drain(bar(B_EMPTY + s), (last_full[s] >> 1) & 1);
-  } else if (warp == kDvIssuer) {
+  } else if (warp == kDvIssuer || warp == kDkIssuer) {
     if (pn > 0) tc::warp_drain(bar(B_PFREE), (pn - 1) & 1);
     if (adone) tc::warp_drain(bar(B_ADONE), 0);
   }
