@@ -1,8 +1,8 @@
 """Bounded waits that run out, on purpose, without breaking any kernel.
 
 The kernels that wait (the tensor-core branches and the TMA-fed selected attention of the
-layer, the decode step's wait for a row's block list, the tensor-core dK / dV of the
-backward) bound every first-level wait.  Here
+layer, the decode step's wait for a row's block list, the tensor-core dK / dV and dQ of
+the backward) bound every first-level wait.  Here
 that limit is set to 1 ns through the C ABI (nsa_set_wait_limit_ns), far below any wait's
 normal length; nothing else changes: no copy is withheld, no barrier left unarrived.  The
 waits give up, the kernels set the device status word to NSA_ERR_TIMEOUT, drain the copies
@@ -133,3 +133,34 @@ def test_sparse_bwd_wait_runs_out_then_recovers(clean_status):
     assert_close(gq, rq, what="dq after a timeout")
     assert_close(gk, rk, what="dk after a timeout")
     assert_close(gv, rv, what="dv after a timeout")
+
+
+def test_cmp_bwd_wait_runs_out_then_recovers(clean_status):
+    """The compressed branch's tensor-core dQ (its S, dP and dQ issuing warps) and dK / dV
+    kernels (group size 16): every role gives up, drains the copies and products in flight
+    and frees the TMEM; the next call with the default limit is correct."""
+    lengths = [2100, 700, 65]
+    cu = gen.varlen_cu_seqlens(lengths)
+    rng = np.random.Generator(np.random.PCG64(44))
+    q, do = (gen.normal(rng, (cu[-1], 16, 128), "bf16") for _ in range(2))
+    k, v = (gen.normal(rng, (cu[-1], 1, 128), "bf16") for _ in range(2))
+    _, kc = orc.compress(k, cu)
+    _, vc = orc.compress(v, cu)
+    o64, lse64 = orc.cmp_attn(q, kc, vc, cu)
+    o, lse = gen.f32_to_bf16_bits(o64.astype(np.float32)), lse64.astype(np.float32)
+    args = [dev(x) for x in (q, kc, vc, o, lse, do)]
+    dcu = dev(cu)
+    torch.cuda.synchronize()
+    _flush_l2()
+    nsa.nsa_set_wait_limit_ns(1)
+    nsa.nsa_cmp_attn_bwd(*args, 1, cu_seqlens=dcu, max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status(reset=True) == NSA_ERR_TIMEOUT
+    nsa.nsa_set_wait_limit_ns(0)
+    gq, gk, gv = nsa.nsa_cmp_attn_bwd(*args, 1, cu_seqlens=dcu, max_seqlen=max(lengths))
+    torch.cuda.synchronize()
+    assert nsa.nsa_device_status() == 0
+    rq, rk, rv = orc.cmp_attn_bwd(q, kc, vc, do, cu, o=o)
+    assert_close(gq, rq, what="cmp dq after a timeout")
+    assert_close(gk, rk, what="cmp dk after a timeout")
+    assert_close(gv, rv, what="cmp dv after a timeout")
