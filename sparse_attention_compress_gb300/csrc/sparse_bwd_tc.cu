@@ -251,12 +251,13 @@ struct PdsArgs {
   uint32_t p_hi, p_lo, s_hi, s_lo;
 };
 template <bool MASK>
-__device__ __forceinline__ void form_pds(const float (&sv)[32], const float (&dpv)[32], const PdsArgs& a, float& pmax,
+__device__ __forceinline__ void form_pds(float (&sv)[32], float (&dpv)[32], const PdsArgs& a, float& pmax,
                                          float& smax) {
+  // sv holds S on entry and P on return, dpv dP and then dS; the rounded parts are stored
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {  // keys 8 c8 .. 8 c8 + 7 (one 16-byte chunk), c8 = 4 kh + cc
     const int c8 = a.kh * 4 + cc;
-    uint32_t ph[4], pl[4], sh[4], sl[4];
+    uint32_t ph[4], sh[4];
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       float p0 = a.fm * ex2(fmaf(sv[cc * 8 + e], a.scale_log2, -a.lse2));
@@ -267,16 +268,40 @@ __device__ __forceinline__ void form_pds(const float (&sv)[32], const float (&dp
         p1 = k0 + 1 <= a.tb && k0 + 1 >= a.tl ? p1 : 0.f;
       }
       const float d0 = p0 * (dpv[cc * 8 + e] - a.dsum), d1 = p1 * (dpv[cc * 8 + e + 1] - a.dsum);
+      sv[cc * 8 + e] = p0;
+      sv[cc * 8 + e + 1] = p1;
+      dpv[cc * 8 + e] = d0;
+      dpv[cc * 8 + e + 1] = d1;
       pmax = fmaxf(pmax, fmaxf(p0, p1));
       smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
-      split_bf16x2(p0, p1, ph[e / 2], pl[e / 2]);
-      split_bf16x2(d0, d1, sh[e / 2], sl[e / 2]);
+      ph[e / 2] = pack_bf16(p0, p1);
+      sh[e / 2] = pack_bf16(d0, d1);
     }
     const uint32_t off = a.row * 128 + ((c8 ^ (a.row & 7)) << 4);
     st_shared_v4(a.p_hi + off, ph);
-    st_shared_v4(a.p_lo + off, pl);
     st_shared_v4(a.s_hi + off, sh);
-    st_shared_v4(a.s_lo + off, sl);
+  }
+}
+
+// The bf16 remainders of the 32 values x into the remainder tile at base (the row's
+// chunks c8 = 4 kh + cc), or zeros: a warp whose values all lie below the threshold
+// drops its remainders (the remainder products then add nothing for its rows).
+__device__ __forceinline__ void store_remainders(const float (&x)[32], uint32_t base, int row, int kh, bool need) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c8 = kh * 4 + cc;
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      if (need) {
+        const uint32_t h = pack_bf16(x[cc * 8 + e], x[cc * 8 + e + 1]);
+        const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h));
+        r[e / 2] = pack_bf16(x[cc * 8 + e] - hf.x, x[cc * 8 + e + 1] - hf.y);
+      } else {
+        r[e / 2] = 0u;
+      }
+    }
+    st_shared_v4(base + row * 128 + ((c8 ^ (row & 7)) << 4), r);
   }
 }
 
@@ -594,9 +619,11 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         form_pds<false>(sv, dpv, pa, pmax, smax);
       else
         form_pds<true>(sv, dpv, pa, pmax, smax);
-      {  // which remainder products this warp's rows need (read by the MMA warp after PFULL)
+      {  // which remainder products this warp's rows need (read by the issuers after PFULL)
         const unsigned bp = __ballot_sync(0xffffffffu, pmax > kLoP), bs = __ballot_sync(0xffffffffu, smax > kLoS);
         if (lane == 0) s_need[warp] = (bp ? 1 : 0) | (bs ? 2 : 0);
+        store_remainders(sv, p_lo, row, kh, bp != 0);
+        store_remainders(dpv, s_lo, row, kh, bs != 0);
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc::mbar_arrive(bar(B_PFULL));
@@ -704,12 +731,12 @@ enum : int {
 };
 }  // namespace dqk
 
-// dS of 64 keys of a row from S and dP (P from the forward's base-2 normaliser lse2),
-// as bf16 values and remainders; MASK: keys outside [tl, tb] give 0.  Returns max |dS|.
+// dS of 64 keys of a row from S and dP (P from the forward's base-2 normaliser lse2):
+// dv holds dP on entry and dS on return, hi the bf16-rounded pairs; MASK: keys outside
+// [tl, tb] give 0.  Returns max |dS|.
 template <bool MASK>
-__device__ __forceinline__ float form_ds(const float (&sv)[64], const float (&dpv)[64], int k0, int tl, int tb,
-                                         float scale_log2, float lse2, float dsum, uint32_t (&hi)[32],
-                                         uint32_t (&lo)[32]) {
+__device__ __forceinline__ float form_ds(const float (&sv)[64], float (&dv)[64], int k0, int tl, int tb,
+                                         float scale_log2, float lse2, float dsum, uint32_t (&hi)[32]) {
   float smax = 0.f;
 #pragma unroll
   for (int e = 0; e < 64; e += 2) {
@@ -719,11 +746,30 @@ __device__ __forceinline__ float form_ds(const float (&sv)[64], const float (&dp
       p0 = k >= tl && k <= tb ? p0 : 0.f;
       p1 = k + 1 >= tl && k + 1 <= tb ? p1 : 0.f;
     }
-    const float d0 = p0 * (dpv[e] - dsum), d1 = p1 * (dpv[e + 1] - dsum);
+    const float d0 = p0 * (dv[e] - dsum), d1 = p1 * (dv[e + 1] - dsum);
+    dv[e] = d0;
+    dv[e + 1] = d1;
     smax = fmaxf(smax, fmaxf(fabsf(d0), fabsf(d1)));
-    split_bf16x2(d0, d1, hi[e / 2], lo[e / 2]);
+    hi[e / 2] = pack_bf16(d0, d1);
   }
   return smax;
+}
+
+// The bf16 remainders x - bf16(x) of value pairs whose rounded parts are hi, or zeros:
+// a warp whose values all lie below the split threshold drops its remainders (the
+// remainder products then add nothing for its rows, as when no warp needs them).
+template <int N>
+__device__ __forceinline__ void remainders(const float (&x)[2 * N], const uint32_t (&hi)[N], bool need,
+                                           uint32_t (&lo)[N]) {
+#pragma unroll
+  for (int w = 0; w < N; ++w) {
+    if (need) {
+      const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[w]));
+      lo[w] = pack_bf16(x[2 * w] - h.x, x[2 * w + 1] - h.y);
+    } else {
+      lo[w] = 0u;
+    }
+  }
 }
 
 // dq_tc: issuing warps of the dQ and the dP products beside the S issuer (kIssuer)
@@ -975,11 +1021,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // every key of the warp's 64 inside every row's range: no per-key mask (fewer
       // instructions on the schedulers the MMA warp shares)
       const float smax = __all_sync(0xffffffffu, k0 >= tl && k0 + 63 <= tb)
-                             ? form_ds<false>(sv, dpv, k0, tl, tb, p.scale_log2, lse2, dsum, hi, lo)
-                             : form_ds<true>(sv, dpv, k0, tl, tb, p.scale_log2, lse2, dsum, hi, lo);
+                             ? form_ds<false>(sv, dpv, k0, tl, tb, p.scale_log2, lse2, dsum, hi)
+                             : form_ds<true>(sv, dpv, k0, tl, tb, p.scale_log2, lse2, dsum, hi);
       {
         const unsigned bs = __ballot_sync(0xffffffffu, smax > kLoS);
         if (lane == 0) s_need[b][warp] = bs ? 1 : 0;
+        remainders<32>(dpv, hi, bs != 0, lo);
       }
       // dS over this thread's own S columns (already read): the MMA warp reuses the
       // buffer only after the dQ product of this tile
