@@ -153,13 +153,6 @@ __device__ __forceinline__ void dispatch(const BwdParams& p, int x, int& bg, int
   j = p.nb;  // not reached
 }
 
-// Whether query t reaches key block j in the compressed-key and window key spaces (the
-// selected blocks' lists are inverted by invert_kernel instead).
-__device__ __forceinline__ int token_mult(const BwdParams& p, int t, int j, int Lk) {
-  if (p.window) return key_lo(p, t) <= j * kBS + kBS - 1;  // t >= j * kBS here
-  return key_bound(p, t, Lk) >= j * kBS;
-}
-
 // Chunk-wise inverted lists of the selected blocks.  Block (chunk c, sequence and kv-head
 // bg): the tokens t of the chunk whose list holds a block j with 64 j <= t (the entries
 // that reach a key), grouped by j.  Eight warps own 256 consecutive tokens each; pass 1
@@ -308,6 +301,7 @@ __device__ __forceinline__ void store_remainders(const float (&x)[32], uint32_t 
 template <int R>
 __global__ void __launch_bounds__(kKVThreads, 1)
     dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_q3, const __grid_constant__ CUtensorMap tm_do3,
                   const BwdParams p) {
   constexpr int TPT = kTileRows / R;  // tokens per tile
   extern __shared__ uint8_t smem_raw[];
@@ -422,13 +416,38 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         take(k < bk.y ? __ldg(lst + k) : 0, k < bk.y ? 1 : 0);
       }
     } else {
-      // compressed keys and window: every query of the range reaching j, by arithmetic
-      for (int t0 = t_begin; ok && t0 < t_end; t0 += 32) {
-        const int t = t0 + lane;
-        take(t, t < t_end ? token_mult(p, t, j, Lk) : 0);
+      // compressed keys and window: the queries reaching j are the consecutive tokens
+      // t_begin .. t_end - 1, each once (token_mult is 1 on exactly that range), so a tile
+      // is one 3-D box of TPT tokens x r heads per tensor half (four copies instead of four
+      // per token, few instructions on the scheduler this warp shares with softmax warps);
+      // slots past t_end read rows of no query of the item and get multiplicity 0
+      for (int tt = t_begin; ok && tt < t_end; tt += TPT) {
+        if (!(ok = begin_tile())) break;
+        const int s = n_tiles & 1, n_tok = min(TPT, t_end - tt);
+        if (lane == 0) {
+          for (int q = 0; q < TPT; ++q) s_meta[s][q] = ((q < n_tok ? tt + q : tt) << 7) | (q < n_tok ? 1 : 0);
+          s_meta[s][TPT] = TPT;
+          s_meta[s][TPT + 1] = tt + TPT >= t_end ? 1 : 0;
+          const uint32_t qs = stage0 + s * kStageBytes, ds = qs + kQBytes, fb = bar(B_FULL + s);
+          const int z = (int)(base + tt);
+          tc::mbar_expect_tx(fb, (uint32_t)kStageBytes);
+          tc::tma3d(qs, &tm_q3, 0, g * R, z, fb);
+          tc::tma3d(qs + kHalfRows, &tm_q3, 64, g * R, z, fb);
+          tc::tma3d(ds, &tm_do3, 0, g * R, z, fb);
+          tc::tma3d(ds + kHalfRows, &tm_do3, 64, g * R, z, fb);
+        }
+        __syncwarp();
+        last_full[s] = n_tiles;
+        ++n_tiles;
       }
     }
-    if (ok) {
+    const bool boxed = p.cmp_kernel || p.window;
+    if (ok && boxed) {
+      if (n_tiles == 0 && begin_tile()) {  // no query reaches j in this chunk: a marker tile
+        if (lane == 0) end_tile(0, 1);
+        ++n_tiles;
+      }
+    } else if (ok) {
       if (slot > 0) {  // the last tile: empty slots repeat a gathered token with multiplicity 0
         for (; slot < TPT; ++slot)
           if (lane == 0) put(last_tok, 0);
@@ -1118,16 +1137,22 @@ bool dkv_tc_supported(const BwdParams& p) { return dkv_tc_shape(p.h / p.hkv, p.c
 cudaError_t launch_dkv_tc(const BwdParams& p, int64_t items, int64_t q_rows, cudaStream_t st) {
   if (items <= 0) return cudaSuccess;
   const int r = p.h / p.hkv;
-  CUtensorMap mq, mdo;
+  CUtensorMap mq, mdo, mq3, mdo3;
   const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)q_rows};
   const uint64_t strides[1] = {(uint64_t)kD * 2};
   const uint32_t box[2] = {64, (uint32_t)r};
   if (!tc::make_map(&mq, p.q, 2, dims, strides, box) || !tc::make_map(&mdo, p.dout, 2, dims, strides, box))
     return cudaErrorInvalidValue;
+  // the same tensors as (d, h, tokens) with boxes of 128 / r consecutive tokens x r heads
+  const uint64_t dims3[3] = {(uint64_t)kD, (uint64_t)p.h, (uint64_t)(q_rows / p.h)};
+  const uint64_t strides3[2] = {(uint64_t)kD * 2, (uint64_t)p.h * kD * 2};
+  const uint32_t box3[3] = {64, (uint32_t)r, (uint32_t)(kTileRows / r)};
+  if (!tc::make_map(&mq3, p.q, 3, dims3, strides3, box3) || !tc::make_map(&mdo3, p.dout, 3, dims3, strides3, box3))
+    return cudaErrorInvalidValue;
   auto kern = r == 16 ? dkv_tc_kernel<16> : dkv_tc_kernel<8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)items, kKVThreads, kSmemBytes, st>>>(mq, mdo, p);
+  kern<<<(unsigned)items, kKVThreads, kSmemBytes, st>>>(mq, mdo, mq3, mdo3, p);
   return cudaGetLastError();
 }
 
