@@ -363,101 +363,76 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   int n_tiles = 0;      // producer: tiles handed to the ring
   int last_full[2] = {-1, -1};  // producer: last tile with rows in each stage
   if (warp == kProducer) {
-    // ------------------------------------------------------------------ token scan + TMA
-    int slot = 0, last_tok = -1;
+    // ------------------------------------------------------------------ token tiles + TMA
+    // Every tile but an empty item's marker holds TPT slots; the item's last tile is
+    // flagged.  Slots past the item's tokens repeat one of them with multiplicity 0.
     bool ok = true;
     auto begin_tile = [&]() -> bool {  // the stage of tile n_tiles is free (warp-uniform)
       if (n_tiles < 2) return true;
       return tc::warp_wait(bar(B_EMPTY + (n_tiles & 1)), ((n_tiles - 2) >> 1) & 1, abort);
     };
-    auto put = [&](int t, int mult) {  // lane 0: one token's Q and dO rows into slot `slot`
-      const int s = n_tiles & 1;
-      const uint32_t qs = stage0 + s * kStageBytes + slot * R * 128, ds = qs + kQBytes;
-      const int y = (int)((base + t) * p.h + g * R);
-      const uint32_t fb = bar(B_FULL + s);
-      tc::tma2d(qs, &tm_q, 0, y, fb);
-      tc::tma2d(qs + kHalfRows, &tm_q, 64, y, fb);
-      tc::tma2d(ds, &tm_do, 0, y, fb);
-      tc::tma2d(ds + kHalfRows, &tm_do, 64, y, fb);
-      s_meta[s][slot] = (t << 7) | mult;
-    };
-    auto end_tile = [&](int cnt, int last) {  // lane 0: the token list, then the arrival
+    auto end_tile = [&](int cnt, int last) {  // lane 0: the list's header, then the arrival
       const int s = n_tiles & 1;
       s_meta[s][TPT] = cnt;
       s_meta[s][TPT + 1] = last;
       tc::mbar_expect_tx(bar(B_FULL + s), cnt > 0 ? (uint32_t)kStageBytes : 0u);
     };
-    // hand 32 candidate tokens (t, mult; mult 0: not gathered) to the tiles, in lane order
-    auto take = [&](int t, int mult) {
-      unsigned bal = __ballot_sync(0xffffffffu, mult > 0);
-      while (bal) {
-        const int src = __ffs(bal) - 1;
-        bal &= bal - 1;
-        const int tt = __shfl_sync(0xffffffffu, t, src), mm = __shfl_sync(0xffffffffu, mult, src);
-        if (slot == 0 && !(ok = begin_tile())) return;
-        if (lane == 0) put(tt, mm);
-        last_tok = tt;
-        if (++slot == TPT) {
-          if (lane == 0) end_tile(TPT, 0);
-          last_full[n_tiles & 1] = n_tiles;
-          ++n_tiles;
-          slot = 0;
-        }
-      }
-    };
     if (!p.cmp_kernel && !p.window) {
       // selected blocks: the tokens of the chunk that list j, from the inverted lists (a
-      // token listing j twice appears twice)
+      // token listing j twice appears twice).  A tile's TPT tokens are gathered by TPT
+      // lanes at once, each issuing its token's four copies (r rows per tensor half) and
+      // writing its slot; lane 0 then adds the header and arrives.
       const size_t seg = (size_t)bg * p.n_chunks + c;
       const int2 bk = p.inv_tab[seg * p.nb + j];
       const int32_t* lst = p.inv_list + seg * kChunk * p.S + bk.x;
-      for (int k0 = 0; ok && k0 < bk.y; k0 += 32) {
-        const int k = k0 + lane;
-        take(k < bk.y ? __ldg(lst + k) : 0, k < bk.y ? 1 : 0);
+      for (int k0 = 0; ok && k0 < bk.y; k0 += TPT) {
+        if (!(ok = begin_tile())) break;
+        const int s = n_tiles & 1, n_tok = min(TPT, bk.y - k0);
+        if (lane < TPT) {
+          const bool in = lane < n_tok;
+          const int t = __ldg(lst + k0 + (in ? lane : n_tok - 1));
+          const uint32_t qs = stage0 + s * kStageBytes + lane * R * 128, ds = qs + kQBytes;
+          const int y = (int)((base + t) * p.h + g * R);
+          const uint32_t fb = bar(B_FULL + s);
+          tc::tma2d(qs, &tm_q, 0, y, fb);
+          tc::tma2d(qs + kHalfRows, &tm_q, 64, y, fb);
+          tc::tma2d(ds, &tm_do, 0, y, fb);
+          tc::tma2d(ds + kHalfRows, &tm_do, 64, y, fb);
+          s_meta[s][lane] = (t << 7) | (in ? 1 : 0);
+        }
+        __syncwarp();  // (orders the lanes' slot writes before lane 0's arrival)
+        if (lane == 0) end_tile(TPT, k0 + TPT >= bk.y ? 1 : 0);
+        __syncwarp();
+        last_full[s] = n_tiles;
+        ++n_tiles;
       }
     } else {
       // compressed keys and window: the queries reaching j are the consecutive tokens
-      // t_begin .. t_end - 1, each once (token_mult is 1 on exactly that range), so a tile
-      // is one 3-D box of TPT tokens x r heads per tensor half (four copies instead of four
-      // per token, few instructions on the scheduler this warp shares with softmax warps);
-      // slots past t_end read rows of no query of the item and get multiplicity 0
+      // t_begin .. t_end - 1, each once (a query t reaches the block exactly when t lies in
+      // that range), so a tile is one 3-D box of TPT tokens x r heads per tensor half
+      // (four copies, few instructions on the scheduler this warp shares with softmax
+      // warps); slots past t_end read rows of no query of the item and get multiplicity 0
       for (int tt = t_begin; ok && tt < t_end; tt += TPT) {
         if (!(ok = begin_tile())) break;
         const int s = n_tiles & 1, n_tok = min(TPT, t_end - tt);
         if (lane == 0) {
           for (int q = 0; q < TPT; ++q) s_meta[s][q] = ((q < n_tok ? tt + q : tt) << 7) | (q < n_tok ? 1 : 0);
-          s_meta[s][TPT] = TPT;
-          s_meta[s][TPT + 1] = tt + TPT >= t_end ? 1 : 0;
           const uint32_t qs = stage0 + s * kStageBytes, ds = qs + kQBytes, fb = bar(B_FULL + s);
           const int z = (int)(base + tt);
-          tc::mbar_expect_tx(fb, (uint32_t)kStageBytes);
           tc::tma3d(qs, &tm_q3, 0, g * R, z, fb);
           tc::tma3d(qs + kHalfRows, &tm_q3, 64, g * R, z, fb);
           tc::tma3d(ds, &tm_do3, 0, g * R, z, fb);
           tc::tma3d(ds + kHalfRows, &tm_do3, 64, g * R, z, fb);
+          end_tile(TPT, tt + TPT >= t_end ? 1 : 0);
         }
         __syncwarp();
         last_full[s] = n_tiles;
         ++n_tiles;
       }
     }
-    const bool boxed = p.cmp_kernel || p.window;
-    if (ok && boxed) {
-      if (n_tiles == 0 && begin_tile()) {  // no query reaches j in this chunk: a marker tile
-        if (lane == 0) end_tile(0, 1);
-        ++n_tiles;
-      }
-    } else if (ok) {
-      if (slot > 0) {  // the last tile: empty slots repeat a gathered token with multiplicity 0
-        for (; slot < TPT; ++slot)
-          if (lane == 0) put(last_tok, 0);
-        if (lane == 0) end_tile(TPT, 1);
-        last_full[n_tiles & 1] = n_tiles;
-        ++n_tiles;
-      } else if (begin_tile()) {  // the list ended on a tile boundary (or is empty): a marker tile
-        if (lane == 0) end_tile(0, 1);
-        ++n_tiles;
-      }
+    if (ok && n_tiles == 0 && begin_tile()) {  // no token of the chunk reaches j: a marker tile
+      if (lane == 0) end_tile(0, 1);
+      ++n_tiles;
     }
     __syncwarp();
   }
