@@ -276,7 +276,7 @@ def bench_prefill_bwd(torch, nsa, device, steps, warmup, flush, peaks, batch=8):
     return {"workload": f"backward of selected attention, prefill B={batch} T=16384 H=16 Hkv=1 d=128 bf16, block 64, "
                         "S=16", "ms_per_step": ms_step, "tflops": tf, "flops_per_step": flops,
             "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "workspace_bytes": int(ws.numel()),
-            "launches_per_step": 3}
+            "launches_per_step": 4}  # dq, list inversion, dK / dV, reduce
 
 
 def bench_cmp_bwd(torch, nsa, device, steps, warmup, flush, peaks, T=65536):
@@ -708,7 +708,7 @@ def main():
         try:
             line["prefill_bwd"] = bench_prefill_bwd(torch, nsa, device, max(3, args.steps // 2), args.warmup, flush,
                                                     peaks)
-            line["gpu_launches"] += 3 * max(3, args.steps // 2)
+            line["gpu_launches"] += 4 * max(3, args.steps // 2)
         except Exception as e:
             line["prefill_bwd"] = {"error": repr(e)}
         torch.cuda.empty_cache()
@@ -726,7 +726,7 @@ def main():
         torch.cuda.empty_cache()
         try:
             line["layer_train"] = bench_layer_train(torch, nsa, device, 3, args.warmup, flush, peaks)
-            line["gpu_launches"] += 3 * 9 + 3 * 15  # training forward 9 kernels, backward 15
+            line["gpu_launches"] += 3 * 9 + 3 * 16  # training forward 9 kernels, backward 16
         except Exception as e:
             line["layer_train"] = {"error": repr(e)}
         torch.cuda.empty_cache()
