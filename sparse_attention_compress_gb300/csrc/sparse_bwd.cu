@@ -25,6 +25,11 @@
 //      fp32 partials.
 //   3. sparse_bwd_reduce: per (sequence, kv-head, block) the partials are summed in
 //      chunk order (deterministic: no floating-point atomics anywhere) and stored.
+// For group sizes 8 and 16 (run_bwd below) the tensor-core kernels of sparse_bwd_tc.cu
+// take over: dK / dV always (dkv_tc_kernel, with invert_kernel first building the
+// selected blocks' token lists), and dQ with D in the compressed and window key spaces
+// (dq_tc_kernel); sparse_bwd_dq keeps the selected blocks' dQ, and the mma.sync dK / dV
+// the other group sizes.
 #include <algorithm>
 
 #include "sparse_bwd.cuh"
